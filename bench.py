@@ -1,0 +1,448 @@
+#!/usr/bin/env python3
+"""Throughput of the TRA join + aggregate hot path on one GB300 (one JSON line).
+
+Default workload: the extended-semiring pair of "EinDecomp ... tensor relational
+algebra" section 2.1 -- squared distance D[i,k] = sum_j (X[i,j]-Y[j,k])^2 and
+max-plus Z[i,k] = max_j (X[i,j]+Y[j,k]) -- with X 8192x256 and Y 256x8192 fp32
+N(0,1), partition vector d = [8,1,1,8] (64 join tuples).  One step = partition
+the dense Y into its relation (X under [8,1] is already laid out as its
+relation), then both join + aggregate EinSums.
+
+Other workloads (``--workload``): c1 (64^3 fp32 matmul under three d), c3 (4-D
+BF16 contraction + repartition of its output), c4 (multi-head-attention
+EinGraph), c5 (16384^3 BF16 matmul, ``--d``), c5b (8192^3 logsumexp).
+
+``--impl reference`` times the CPU oracle on a bounded sample of the same
+workload (the reference arm).  Under torchrun (N > 1) every rank runs an
+independent replica of the workload (weak scaling, no collective on the data
+path); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "EinSum TRA join+aggregate TFLOP/s & % of roofline (1×GB300), vs CPU oracle"
+FP32_LANES_PER_SM = 128  # FP32 FMA lanes per SM (4 sub-partitions x 32)
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except OSError:
+        return {}
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = str(gpu_index)
+        try:
+            import torch
+
+            u = str(torch.cuda.get_device_properties(gpu_index).uuid)
+            self.gpu = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            pass
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workloads
+class Step:
+    """One named launch group inside a step, with its algorithmic work per launch."""
+
+    def __init__(self, name, fn, work, unit, bound, launches):
+        self.name, self.fn, self.work, self.unit, self.bound, self.launches = name, fn, work, unit, bound, launches
+
+
+def kernel_launches(plan) -> int:
+    return {"semiring_f32": 1, "tc_bf16": 1, "row_reduce": 1, "elementwise": 1, "lse_factored": 3,
+            "literal": 2}[plan.kernel] + (2 if ":sqdiff=expand" in plan.spec else 0)
+
+
+def device_relation(tra, torch, dense_dev, shape, d):
+    if all(v == 1 for v in d):
+        return dense_dev
+    out = torch.empty_like(dense_dev)
+    tra.repartition(dense_dev, out, shape, [1] * len(shape), d)
+    return out
+
+
+class PairWorkload:
+    """Squared distance and max-plus, X 8192x256, Y 256x8192 fp32, d = [8,1,1,8]."""
+
+    name = "semiring pair: sqdist (x-y)^2/sum + max-plus (x+y)/max, X 8192x256, Y 256x8192 fp32, d=[8,1,1,8]"
+    M, K, N = 8192, 256, 8192
+    d = [8, 1, 1, 8]
+
+    def __init__(self, seed_offset=0):
+        self.seed_offset = seed_offset
+
+    def host_inputs(self):
+        import datagen
+
+        X = datagen.normal_f32((self.M, self.K), 0 + self.seed_offset, 0)
+        Y = datagen.normal_f32((self.K, self.N), 1 + self.seed_offset, 0)
+        return [X, Y]
+
+    def setup(self, tra, torch, inputs):
+        X, Y = inputs
+        dev = torch.device("cuda")
+        self.tra, self.torch = tra, torch
+        self.Xd = torch.from_numpy(X).to(dev).reshape(-1)  # [8,1] relation of X == dense X
+        self.Yd = torch.from_numpy(Y).to(dev).reshape(-1)
+        self.Yr = torch.empty_like(self.Yd)
+        self.p_sq = tra.Plan("ij,jk->ik:sqdiff:sum", [self.M, self.K, self.N], self.d)
+        self.p_mx = tra.Plan("ij,jk->ik:add:max", [self.M, self.K, self.N], self.d)
+        self.Zs = torch.empty(self.M * self.N, dtype=torch.float32, device=dev)
+        self.Zm = torch.empty_like(self.Zs)
+        ops = 2 * self.M * self.K * self.N
+        self.steps = [
+            Step("repartition Y [1,1]->[1,8]", lambda: tra.repartition(self.Yd, self.Yr, [self.K, self.N], [1, 1], [1, 8]),
+                 2 * self.K * self.N * 4, "bytes", "hbm", 1),
+            Step("join+agg (x-y)^2/sum", lambda: self.p_sq.execute(self.Xd, self.Yr, self.Zs), ops, "flop", "alu",
+                 kernel_launches(self.p_sq)),
+            Step("join+agg (x+y)/max", lambda: self.p_mx.execute(self.Xd, self.Yr, self.Zm), ops, "flop", "alu",
+                 kernel_launches(self.p_mx)),
+        ]
+        self.inputs_dev = [self.Xd, self.Yd]
+        self.outputs_dev = [self.Zs, self.Zm]
+
+    def ops_per_step(self):
+        return 2 * (2 * self.M * self.K * self.N)
+
+    # reference arm: oracle on output rows [r0, r0+rows) of both EinSums
+    def oracle_sample(self, inputs, r0, rows):
+        import oracle
+
+        X, Y = inputs
+        Xd, Yd = X.astype(np.float64), Y.astype(np.float64)
+        pts = (np.arange(rows, dtype=np.int64)[:, None] % self.M + r0) % self.M * self.N + np.arange(self.N)[None, :]
+        pts = pts.reshape(-1)
+        oracle.einsum_points("ij,jk->ik", Xd, Yd, pts, op="sqdiff", agg="sum")
+        oracle.einsum_points("ij,jk->ik", Xd, Yd, pts, op="add", agg="max")
+        return 2 * 2 * pts.size * self.K  # two EinSums, two ops per tuple
+
+    def sample_text(self, rows):
+        return f"{rows} of 8192 output rows (all 8192 columns) of both EinSums"
+
+    def traffic_key(self, j):
+        return ("k_semiring.cu", ["repartition", "semiring sqdiff/sum", "semiring add/max"][j])
+
+
+WORKLOADS = {"pair": PairWorkload}
+
+
+# ----------------------------------------------------------------------------- measurement
+def time_steps(torch, wl, steps, warmup, flush, sampler=None, e2e_io=None):
+    """Run warmup + timed steps; per-launch-group CUDA events on the launching stream."""
+    stream = torch.cuda.current_stream()
+    n = len(wl.steps)
+
+    def one_step(record):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1 + (2 if e2e_io else 0))] if record else None
+        i = 0
+        if record:
+            evs[0].record(stream)
+        if e2e_io:
+            e2e_io["h2d"]()
+            if record:
+                evs[1].record(stream)
+            i = 1
+        for j, st in enumerate(wl.steps):
+            st.fn()
+            if record:
+                evs[i + j + 1].record(stream)
+        if e2e_io:
+            e2e_io["d2h"]()
+            if record:
+                evs[-1].record(stream)
+        return evs
+
+    for _ in range(warmup):
+        one_step(False)
+        flush()
+    torch.cuda.synchronize()
+    recs = []
+    if sampler:
+        sampler.start()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        recs.append(one_step(True))
+        flush()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop() if sampler else None
+    step_ms = [r[0].elapsed_time(r[-1]) for r in recs]
+    off = 1 if e2e_io else 0
+    per = [[r[off + j].elapsed_time(r[off + j + 1]) for r in recs] for j in range(n)]
+    return step_ms, per, wall, clocks
+
+
+def traffic_for(kernel_file: str, kernel_name: str, units_scale: float = 1.0):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        rec = json.load(open(path))[kernel_name]
+    except (OSError, KeyError, ValueError):
+        return None
+    src = os.path.join(ROOT, "tensor_relational_algebra_gb300", "csrc", kernel_file)
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    if rec.get("source_sha256_16") != h:
+        return None
+    return rec["dram_bytes_per_launch"] * units_scale
+
+
+def run_ours(args):
+    import torch
+
+    import tensor_relational_algebra_gb300 as tra
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    tra.load()
+    wl = WORKLOADS[args.workload](seed_offset=rank)
+    host = wl.host_inputs()
+    wl.setup(tra, torch, host)
+    flush_buf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+
+    def flush():
+        flush_buf.zero_()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # device-resident timing
+    barrier()
+    sampler = ClockSampler(local) if rank == 0 else None
+    step_ms, per, wall, clocks = time_steps(torch, wl, args.steps, args.warmup, flush, sampler)
+    barrier()
+    total_ms = sum(step_ms)
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ops = wl.ops_per_step()
+    value = world * ops * args.steps / (total_ms * 1e-3) / 1e12
+
+    # end to end: pinned host inputs -> device, the step, results -> pinned host
+    pinned_in = [torch.from_numpy(h).reshape(-1).pin_memory() for h in host]
+    pinned_out = [torch.empty(o.numel(), dtype=o.dtype).pin_memory() for o in wl.outputs_dev]
+
+    def h2d():
+        for src, dst in zip(pinned_in, wl.inputs_dev):
+            dst.copy_(src, non_blocking=True)
+
+    def d2h():
+        for src, dst in zip(wl.outputs_dev, pinned_out):
+            dst.copy_(src, non_blocking=True)
+
+    barrier()
+    e2e_ms, _, _, _ = time_steps(torch, wl, max(3, args.steps // 4), args.warmup, flush, None,
+                                 {"h2d": h2d, "d2h": d2h})
+    barrier()
+    e2e_total = sum(e2e_ms)
+    n_e2e = max(3, args.steps // 4)
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([e2e_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e_value = world * ops * n_e2e / (e2e_total * 1e-3) / 1e12
+    h2d_bytes = sum(t.numel() * t.element_size() for t in pinned_in)
+    d2h_bytes = sum(t.numel() * t.element_size() for t in pinned_out)
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+        return
+
+    # roofline of the dominant kernel
+    peaks = measured_peaks()
+    props = torch.cuda.get_device_properties(0)
+    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
+    means = [statistics.mean(p) for p in per]
+    dom = max(range(len(wl.steps)), key=lambda j: means[j])
+    st = wl.steps[dom]
+    dur_s = means[dom] * 1e-3 / st.launches if st.launches else means[dom] * 1e-3
+    if st.bound == "alu":
+        peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+        achieved = st.work / (means[dom] * 1e-3) / 1e12
+        unit = "TFLOP/s"
+    elif st.bound == "tensor":
+        peak = float(peaks.get("bf16_tflops", 1900.0))
+        achieved = st.work / (means[dom] * 1e-3) / 1e12
+        unit = "TFLOP/s"
+    else:
+        peak = float(peaks.get("hbm_gbs", 6800.0))
+        achieved = st.work / (means[dom] * 1e-3) / 1e9
+        unit = "GB/s"
+    traffic = traffic_for(*wl.traffic_key(dom)) if hasattr(wl, "traffic_key") else None
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        rows = args.cpu_rows
+        t0 = time.perf_counter()
+        work = wl.oracle_sample(host, 0, rows)
+        dt = time.perf_counter() - t0
+        cpu = {"value": work / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": wl.sample_text(rows), "seconds": round(dt, 2)}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (Philox-4x32-10 N(0,1), seeded)",
+        "config": {"workload": wl.name, "d": wl.d, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed between steps (512 MiB write outside the step's events)",
+                   "per_launch_group_ms": {s.name: round(m, 4) for s, m in zip(wl.steps, means)}},
+        "roofline": {"bound": st.bound, "kernel": st.name, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": ("derived: SMs x 128 FP32 lanes x 2 x max SM clock (MEASURED_PEAKS sm_max_mhz)"
+                                     if st.bound == "alu" else "MEASURED_PEAKS.json (of measured)")},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d_bytes,
+                "d2h_bytes_per_step": d2h_bytes},
+        "gpu_launches": args.steps * sum(s.launches for s in wl.steps),
+        "clocks": clocks,
+        "wall_s": round(wall, 3),
+    }
+    print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+
+    wl = WORKLOADS[args.workload]()
+    host = wl.host_inputs()
+    rows = args.ref_rows
+    for s in range(args.warmup):
+        wl.oracle_sample(host, s * rows, rows)
+    t0 = time.perf_counter()
+    work = 0
+    for s in range(args.steps):
+        work += wl.oracle_sample(host, (args.warmup + s) * rows, rows)
+    dt = time.perf_counter() - t0
+    value = work / dt / 1e12
+    cores = oracle.num_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (Philox-4x32-10 N(0,1), seeded)",
+        "config": {"workload": wl.name, "d": wl.d},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "per step: " + wl.sample_text(rows)},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="pair")
+    ap.add_argument("--cpu-rows", type=int, default=1024, help="output rows the CPU-baseline oracle computes")
+    ap.add_argument("--ref-rows", type=int, default=32, help="output rows per reference-arm step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

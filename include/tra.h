@@ -1,0 +1,163 @@
+/*
+ * tra.h -- C ABI of libtra.so: tensor-relational-algebra (TRA) execution of one
+ * extended EinSum on one NVIDIA GB300 (sm_103a).
+ *
+ * Source of the operations: "EinDecomp: automatic tensor-parallel
+ * decomposition via Einstein summation + tensor relational algebra".
+ *   section 2.1  extended EinSum: Z[out] = AGG_{contracted} OP(X[..], Y[..]);
+ *                OP any binary scalar function, AGG commutative and associative
+ *   section 2.2  tensor relation (key -> sub-tensor), key -> index range,
+ *                join, aggregation, repartition, EinSum -> TRA lowering,
+ *                partition vector d (matmul: [d_i, d_jX, d_jY, d_k])
+ *   section 3.1  task triple (bound, EinSum, inputs); cost model
+ *   section 3.2  task count = number of tuples produced by the join
+ *
+ * Conventions for every entry point
+ *   - Return value: 0 on success, a negative TRA_ERR_* code on failure; the
+ *     message of the last failure on the calling thread is ein_last_error().
+ *   - Device pointers are plain CUDA device addresses owned by the caller; the
+ *     library never allocates or frees device memory.  Host pointers (plans,
+ *     info structs, arrays of ints) are read or written only during the call.
+ *   - Launches are asynchronous on the given stream (0 = legacy default
+ *     stream); nothing synchronises except ein_status().
+ *   - Plans are immutable after ein_plan and may be executed concurrently on
+ *     different streams.
+ *
+ * Relation layout ("blocked"): a tensor of shape [B1..Br] under d = [D1..Dr]
+ * is one contiguous buffer holding its D1*..*Dr sub-tensors in row-major key
+ * order; each sub-tensor (shape [B1/D1..Br/Dr]) is row-major over the
+ * tensor's own index order.  Key k holds the index range
+ * [k_i*B_i/D_i, (k_i+1)*B_i/D_i) in dimension i (section 2.2).  With d all
+ * ones this is the plain dense row-major tensor.
+ */
+#ifndef TRA_H
+#define TRA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* tra_stream_t; /* a cudaStream_t */
+typedef struct tra_plan* tra_plan_t;      /* opaque, host-owned */
+
+enum {
+    TRA_OK = 0,
+    TRA_ERR_PARSE = -1,          /* malformed spec or option */
+    TRA_ERR_DIVISIBILITY = -2,   /* some D does not divide its extent B (section 2.2) */
+    TRA_ERR_SHARED_LABEL_D = -3, /* a label shared by X and Y got two partition counts */
+    TRA_ERR_RANK = -4,           /* wrong number of bounds / d entries, rank too large */
+    TRA_ERR_UNSUPPORTED = -5,    /* dtype x operator combination or shape not handled */
+    TRA_ERR_WORKSPACE = -6,      /* workspace missing or smaller than ein_plan_info's */
+    TRA_ERR_CUDA = -7,           /* a CUDA runtime / driver call failed */
+    TRA_ERR_TIMEOUT = -8,        /* a bounded device wait gave up (see ein_status) */
+    TRA_ERR_ARG = -9             /* NULL pointer or invalid argument */
+};
+
+#define TRA_MAX_RANK 8
+#define TRA_MAX_LABELS 12
+
+/* Plan summary.  All counts are exact integers (section 3.1 / 3.2 with P read
+ * as the number of join tuples; costs are counted in elements). */
+typedef struct {
+    int32_t n_labels;                  /* distinct labels, first-appearance order X then Y */
+    char labels[TRA_MAX_LABELS];       /* label characters */
+    int64_t bound[TRA_MAX_LABELS];     /* B_l */
+    int32_t part[TRA_MAX_LABELS];      /* D_l */
+    int64_t sub_extent[TRA_MAX_LABELS];/* b_l = B_l / D_l */
+    int32_t role[TRA_MAX_LABELS];      /* 0 batch (X,Y,Z), 1 M (X,Z), 2 N (Y,Z), 3 contracted */
+    int32_t rank_x, rank_y, rank_z;    /* rank_y = 0 for a unary EinSum */
+    int32_t key_grid_x[TRA_MAX_RANK];  /* D per index position of X */
+    int32_t key_grid_y[TRA_MAX_RANK];
+    int32_t key_grid_z[TRA_MAX_RANK];
+    uint64_t n_tasks;                  /* join tuples = prod over labels of X u Y of D_l */
+    uint64_t n_groups;                 /* output keys = prod over Z's labels of D_l */
+    uint64_t n_agg;                    /* join tuples per group = prod over contracted D_l */
+    uint64_t x_sub, y_sub, z_sub;      /* elements per sub-tensor */
+    uint64_t cost_join;                /* n_tasks * (x_sub + y_sub)            (section 3.1) */
+    uint64_t cost_agg;                 /* (n_tasks/n_agg) * (n_agg-1) * z_sub  (section 3.1) */
+    uint64_t workspace_bytes;          /* device scratch ein_execute needs (0 = none) */
+    int32_t in_dtype, out_dtype;       /* 0 = fp32, 1 = bf16 */
+    int32_t kernel;                    /* TRA_KERNEL_* chosen for ein_execute */
+} tra_plan_info;
+
+enum {
+    TRA_KERNEL_SEMIRING_F32 = 1,  /* CUDA-core join+aggregate (register-tiled) */
+    TRA_KERNEL_TC_BF16 = 2,       /* tcgen05 / TMEM / TMA BF16 sum-of-products */
+    TRA_KERNEL_ROW_REDUCE = 3,    /* unary aggregation over the contracted labels */
+    TRA_KERNEL_ELEMENTWISE = 4,   /* join with AGG = none (broadcast operands allowed) */
+    TRA_KERNEL_LSE_FACTORED = 5,  /* logsumexp of a sum: max-shifted exp, then sum-of-products */
+    TRA_KERNEL_LITERAL = 6        /* one partial per join tuple, then ordered combine */
+};
+
+/* ein_plan -- build the TRA plan of one EinSum under partition vector d
+ * (sections 2.2 "EinSum -> TRA" and 3.1 "task triple").  Host only; touches no device.
+ *
+ * spec:   "<X labels>,<Y labels>-><Z labels>:<op>:<agg>[:option]..."  or the unary
+ *         "<X labels>-><Z labels>::<agg>".  Labels are single letters; a label may
+ *         not repeat inside one operand.  op in {mul, add, sqdiff, sub, expsub};
+ *         agg in {sum, max, min, lse, none}; none requires that no label is
+ *         contracted.  Options: in=f32|bf16 (both inputs, default f32),
+ *         out=f32|bf16 (default f32), alpha=<float> (scales the aggregated value),
+ *         mode=fused|literal (literal materialises one partial per join tuple and
+ *         combines them in canonical order), sqdiff=direct|expand.
+ * bounds: B_l for every distinct label in first-appearance order (X then Y);
+ *         n_bounds must equal the number of distinct labels.
+ * d:      partition counts per operand index position, X's then Y's (n_d =
+ *         rank_x + rank_y).  A label shared by X and Y must get equal counts.
+ * out:    receives the plan; release it with ein_plan_destroy.
+ * Errors: TRA_ERR_PARSE, TRA_ERR_RANK, TRA_ERR_DIVISIBILITY, TRA_ERR_SHARED_LABEL_D,
+ *         TRA_ERR_UNSUPPORTED, TRA_ERR_ARG. */
+int ein_plan(const char* spec, const int64_t* bounds, int n_bounds, const int32_t* d, int n_d, tra_plan_t* out);
+
+/* ein_plan_info -- copy the plan summary (key space, task counts, cost terms). */
+int ein_plan_info(tra_plan_t plan, tra_plan_info* info);
+
+/* ein_plan_keys -- the join tuples in canonical order: output key row-major, then the
+ * contracted labels' key components (first-appearance order) row-major.  Writes
+ * n_tasks rows of (rank_x + rank_y + rank_z) int32: X key, Y key, Z key.
+ * capacity: number of int32 the buffer holds; TRA_ERR_ARG if too small. */
+int ein_plan_keys(tra_plan_t plan, int32_t* xyz_keys, int64_t capacity);
+
+/* ein_execute -- run the plan: join key-matched sub-tensors through op and aggregate
+ * with agg (section 2.2).  in0/in1/out are device buffers in the relation layout of
+ * the plan's d (in1 = NULL for a unary EinSum); element types per the in=/out=
+ * options.  workspace: device scratch of at least info.workspace_bytes (may be NULL
+ * when that is 0); it is overwritten.  Asynchronous on stream.
+ * Errors: TRA_ERR_ARG, TRA_ERR_WORKSPACE, TRA_ERR_CUDA (launch failure). */
+int ein_execute(tra_plan_t plan, const void* in0, const void* in1, void* out, void* workspace,
+                size_t workspace_bytes, tra_stream_t stream);
+
+/* ein_repartition -- section 2.2 repartition: copy a tensor of the given shape from the
+ * relation layout under src_d to the relation layout under dst_d (either may be all
+ * ones = dense row-major).  elem_bytes in {1,2,4,8}.  src and dst must not overlap.
+ * Asynchronous on stream.  Errors: TRA_ERR_RANK, TRA_ERR_DIVISIBILITY, TRA_ERR_ARG,
+ * TRA_ERR_CUDA. */
+int ein_repartition(int rank, const int64_t* shape, const int32_t* src_d, const int32_t* dst_d, int elem_bytes,
+                    const void* src, void* dst, tra_stream_t stream);
+
+/* ein_repartition_cost -- section 3.1 repartition term.  The pages give no formula;
+ * this library counts the elements whose owning block changes when blocks are
+ * owned by their row-major linear key id: |T| - sum_L |block_L(src) n block_L(dst)|.
+ * Host only. */
+int ein_repartition_cost(int rank, const int64_t* shape, const int32_t* src_d, const int32_t* dst_d,
+                         uint64_t* cost);
+
+/* ein_status -- synchronise the stream, then read and clear the device status word
+ * that bounded waits inside the kernels set when they give up.  Returns TRA_OK,
+ * TRA_ERR_TIMEOUT or TRA_ERR_CUDA. */
+int ein_status(tra_stream_t stream);
+
+/* ein_plan_destroy -- release a plan (NULL is ignored). */
+void ein_plan_destroy(tra_plan_t plan);
+
+/* ein_last_error -- message of the last failure on this thread ("" if none). */
+const char* ein_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TRA_H */

@@ -1,0 +1,267 @@
+"""GB300-native tensor-relational-algebra (TRA) execution of one extended EinSum.
+
+Python binding of ``libtra.so`` (C ABI in ``include/tra.h``): argument
+marshalling only.  Every step of the path -- join, aggregation, repartition --
+runs in the library's CUDA kernels; PyTorch supplies device memory and streams.
+There is no CPU fallback: if the library cannot be loaded, every call raises.
+
+Source of the operations: "EinDecomp: automatic tensor-parallel decomposition
+via Einstein summation + tensor relational algebra" (sections 2.1, 2.2, 3.1, 3.2).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB as _LIB_PATH, build as _build_lib
+
+__all__ = [
+    "TraError", "build_library", "load", "Plan", "ein_plan", "ein_plan_info", "ein_plan_keys", "ein_execute",
+    "ein_repartition", "ein_repartition_cost", "ein_status", "ein_plan_destroy", "ein_last_error",
+    "repartition", "repartition_cost", "KERNELS", "ROLES",
+]
+
+TRA_MAX_RANK = 8
+TRA_MAX_LABELS = 12
+ERRORS = {
+    -1: "TRA_ERR_PARSE", -2: "TRA_ERR_DIVISIBILITY", -3: "TRA_ERR_SHARED_LABEL_D", -4: "TRA_ERR_RANK",
+    -5: "TRA_ERR_UNSUPPORTED", -6: "TRA_ERR_WORKSPACE", -7: "TRA_ERR_CUDA", -8: "TRA_ERR_TIMEOUT", -9: "TRA_ERR_ARG",
+}
+KERNELS = {1: "semiring_f32", 2: "tc_bf16", 3: "row_reduce", 4: "elementwise", 5: "lse_factored", 6: "literal"}
+ROLES = {0: "batch", 1: "M", 2: "N", 3: "contracted"}
+
+
+class TraError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{ERRORS.get(code, code)}: {msg}")
+        self.code = code
+
+
+class tra_plan_info(ctypes.Structure):
+    _fields_ = [
+        ("n_labels", ctypes.c_int32),
+        ("labels", ctypes.c_char * TRA_MAX_LABELS),
+        ("bound", ctypes.c_int64 * TRA_MAX_LABELS),
+        ("part", ctypes.c_int32 * TRA_MAX_LABELS),
+        ("sub_extent", ctypes.c_int64 * TRA_MAX_LABELS),
+        ("role", ctypes.c_int32 * TRA_MAX_LABELS),
+        ("rank_x", ctypes.c_int32), ("rank_y", ctypes.c_int32), ("rank_z", ctypes.c_int32),
+        ("key_grid_x", ctypes.c_int32 * TRA_MAX_RANK),
+        ("key_grid_y", ctypes.c_int32 * TRA_MAX_RANK),
+        ("key_grid_z", ctypes.c_int32 * TRA_MAX_RANK),
+        ("n_tasks", ctypes.c_uint64), ("n_groups", ctypes.c_uint64), ("n_agg", ctypes.c_uint64),
+        ("x_sub", ctypes.c_uint64), ("y_sub", ctypes.c_uint64), ("z_sub", ctypes.c_uint64),
+        ("cost_join", ctypes.c_uint64), ("cost_agg", ctypes.c_uint64),
+        ("workspace_bytes", ctypes.c_uint64),
+        ("in_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
+        ("kernel", ctypes.c_int32),
+    ]
+
+
+_lib = None
+
+
+def build_library(force: bool = False) -> str:
+    """Compile libtra.so in-tree for sm_103a (no-op when up to date)."""
+    return _build_lib(force=force)
+
+
+def load():
+    """Load libtra.so (building it first if needed) and declare the C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        build_library()
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, i32, i64, u64p = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.POINTER(ctypes.c_uint64)
+    lib.ein_plan.argtypes = [ctypes.c_char_p, vp, i32, vp, i32, ctypes.POINTER(vp)]
+    lib.ein_plan_info.argtypes = [vp, ctypes.POINTER(tra_plan_info)]
+    lib.ein_plan_keys.argtypes = [vp, vp, i64]
+    lib.ein_execute.argtypes = [vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.ein_repartition.argtypes = [i32, vp, vp, vp, i32, vp, vp, vp]
+    lib.ein_repartition_cost.argtypes = [i32, vp, vp, vp, u64p]
+    lib.ein_status.argtypes = [vp]
+    lib.ein_plan_destroy.argtypes = [vp]
+    lib.ein_plan_destroy.restype = None
+    lib.ein_last_error.restype = ctypes.c_char_p
+    for f in ("ein_plan", "ein_plan_info", "ein_plan_keys", "ein_execute", "ein_repartition",
+              "ein_repartition_cost", "ein_status"):
+        getattr(lib, f).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise TraError(rc, load().ein_last_error().decode())
+
+
+def _i64(vals):
+    return (ctypes.c_int64 * max(1, len(vals)))(*vals)
+
+
+def _i32(vals):
+    return (ctypes.c_int32 * max(1, len(vals)))(*vals)
+
+
+def _ptr(t):
+    """Device (or host) address of a torch tensor / int / None."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ----------------------------------------------------------------- raw C names
+def ein_plan(spec: str, bounds, d) -> int:
+    h = ctypes.c_void_p()
+    _check(load().ein_plan(spec.encode(), _i64(bounds), len(bounds), _i32(d), len(d), ctypes.byref(h)))
+    return h.value
+
+
+def ein_plan_info(plan: int) -> tra_plan_info:
+    info = tra_plan_info()
+    _check(load().ein_plan_info(plan, ctypes.byref(info)))
+    return info
+
+
+def ein_plan_keys(plan: int, n_tasks: int, width: int):
+    buf = (ctypes.c_int32 * max(1, n_tasks * width))()
+    _check(load().ein_plan_keys(plan, buf, n_tasks * width))
+    return [tuple(buf[i * width:(i + 1) * width]) for i in range(n_tasks)]
+
+
+def ein_execute(plan: int, in0, in1, out, workspace=None, workspace_bytes: int = 0, stream=None):
+    _check(load().ein_execute(plan, _ptr(in0), _ptr(in1), _ptr(out), _ptr(workspace), workspace_bytes,
+                              _stream(stream)))
+
+
+def ein_repartition(shape, src_d, dst_d, elem_bytes: int, src, dst, stream=None):
+    _check(load().ein_repartition(len(shape), _i64(shape), _i32(src_d), _i32(dst_d), elem_bytes, _ptr(src),
+                                  _ptr(dst), _stream(stream)))
+
+
+def ein_repartition_cost(shape, src_d, dst_d) -> int:
+    c = ctypes.c_uint64()
+    _check(load().ein_repartition_cost(len(shape), _i64(shape), _i32(src_d), _i32(dst_d), ctypes.byref(c)))
+    return c.value
+
+
+def ein_status(stream=None):
+    _check(load().ein_status(_stream(stream)))
+
+
+def ein_plan_destroy(plan: int):
+    load().ein_plan_destroy(plan)
+
+
+def ein_last_error() -> str:
+    return load().ein_last_error().decode()
+
+
+# ----------------------------------------------------------------- convenience layer
+class Plan:
+    """A TRA plan of one EinSum under a partition vector (host object).
+
+    ``bounds``: {label: extent} or a list in first-appearance order.
+    ``d``: partition counts per operand index position, X's then Y's."""
+
+    def __init__(self, spec: str, bounds, d):
+        eq = spec.split(":")[0]
+        lhs = eq.split("->")[0]
+        order = []
+        for c in lhs.replace(",", ""):
+            if c not in order:
+                order.append(c)
+        if isinstance(bounds, dict):
+            bounds = [bounds[c] for c in order]
+        self.handle = None
+        self.handle = ein_plan(spec, list(bounds), list(d))  # the library validates the spec
+        self.info = ein_plan_info(self.handle)
+        self.spec = spec
+        self.labels = order
+        self.operands = lhs.split(",")
+        self.output = eq.split("->")[1]
+        self.bounds = list(bounds)
+        self.d = list(d)
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h and _lib is not None:
+            _lib.ein_plan_destroy(h)
+            self.handle = None
+
+    # plan facts (bit-exact integers)
+    @property
+    def n_tasks(self):
+        return self.info.n_tasks
+
+    @property
+    def n_groups(self):
+        return self.info.n_groups
+
+    @property
+    def n_agg(self):
+        return self.info.n_agg
+
+    @property
+    def cost_join(self):
+        return self.info.cost_join
+
+    @property
+    def cost_agg(self):
+        return self.info.cost_agg
+
+    @property
+    def workspace_bytes(self):
+        return self.info.workspace_bytes
+
+    @property
+    def kernel(self):
+        return KERNELS.get(self.info.kernel, self.info.kernel)
+
+    def part(self, label):
+        return self.info.part[self.labels.index(label)]
+
+    def shape(self, which: str):
+        labs = {"x": self.operands[0], "y": self.operands[1] if len(self.operands) > 1 else "",
+                "z": self.output}[which]
+        return [self.bounds[self.labels.index(c)] for c in labs]
+
+    def dvec(self, which: str):
+        labs = {"x": self.operands[0], "y": self.operands[1] if len(self.operands) > 1 else "",
+                "z": self.output}[which]
+        return [self.info.part[self.labels.index(c)] for c in labs]
+
+    def keys(self):
+        w = self.info.rank_x + self.info.rank_y + self.info.rank_z
+        rows = ein_plan_keys(self.handle, self.info.n_tasks, w)
+        rx, ry = self.info.rank_x, self.info.rank_y
+        return [(r[:rx], r[rx:rx + ry], r[rx + ry:]) for r in rows]
+
+    def execute(self, x, y, z, workspace=None, stream=None):
+        ws_bytes = 0
+        if workspace is not None:
+            ws_bytes = workspace.numel() * workspace.element_size()
+        ein_execute(self.handle, x, y, z, workspace, ws_bytes, stream)
+
+
+def repartition(src, dst, shape, src_d, dst_d, stream=None):
+    """Device permute-copy of a relation from src_d to dst_d (torch tensors)."""
+    ein_repartition(shape, src_d, dst_d, src.element_size(), src, dst, stream)
+
+
+def repartition_cost(shape, src_d, dst_d) -> int:
+    return ein_repartition_cost(shape, src_d, dst_d)

@@ -1,0 +1,433 @@
+// extern "C" entry points of libtra.so (declared and documented in include/tra.h).
+#include <cstring>
+#include <numeric>
+
+#include "plan.h"
+
+using namespace tra;
+
+namespace {
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(TRA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+SemiringParams semiring_params(const Plan& p, const void* x, const void* y, void* z) {
+    SemiringParams sp;
+    memset(&sp, 0, sizeof(sp));
+    sp.x = x;
+    sp.y = y;
+    sp.z = z;
+    sp.xb = role_map(p, p.X, kBatch);
+    sp.xm = role_map(p, p.X, kM);
+    sp.xk = role_map(p, p.X, kK);
+    sp.yb = role_map(p, p.Y, kBatch);
+    sp.yn = role_map(p, p.Y, kN);
+    sp.yk = role_map(p, p.Y, kK);
+    sp.zb = role_map(p, p.Z, kBatch);
+    sp.zm = role_map(p, p.Z, kM);
+    sp.zn = role_map(p, p.Z, kN);
+    sp.nb = (uint32_t)p.ext[kBatch];
+    sp.M = (uint32_t)p.ext[kM];
+    sp.N = (uint32_t)p.ext[kN];
+    sp.K = (uint32_t)p.ext[kK];
+    sp.op = p.op;
+    sp.agg = p.agg;
+    sp.alpha = (float)p.alpha;
+    sp.in_bf16 = p.in_bf16;
+    sp.out_bf16 = p.out_bf16;
+    sp.x_kcontig = affine_stride(sp.xk) == 1;
+    sp.x_mcontig = affine_stride(sp.xm) == 1;
+    sp.y_ncontig = affine_stride(sp.yn) == 1;
+    sp.y_kcontig = affine_stride(sp.yk) == 1;
+    return sp;
+}
+
+// Literal TRA execution (section 2.2 read literally): every join tuple produces its
+// own partial sub-tensor (the contracted labels run over one block only), then the
+// partials of each output key are combined in canonical order.
+int execute_literal(const Plan& p, const void* x, const void* y, void* z, void* ws, cudaStream_t s) {
+    SemiringParams sp = semiring_params(p, x, y, ws);
+    const uint32_t nb0 = sp.nb;
+    // contracted composite restricted to one block: extents b_l, key part zero
+    RoleMap* kmaps[2] = {&sp.xk, &sp.yk};
+    const Operand* ops[2] = {&p.X, &p.Y};
+    for (int a = 0; a < 2; ++a) {
+        RoleMap& m = *kmaps[a];
+        memset(&m, 0, sizeof(m));
+        uint64_t div = 1;
+        for (int l : p.comp[kK]) {
+            const int i = ops[a]->pos_of(l);
+            const uint32_t b = (uint32_t)(p.B[l] / p.D[l]);
+            if (i >= 0) {
+                Term& t = m.t[m.n++];
+                t.div = (uint32_t)div;
+                t.ext = b;
+                t.sub = b;
+                t.key_stride = 0;
+                t.loc_stride = ops[a]->loc_stride[i];
+            }
+            div *= b;
+        }
+    }
+    sp.K = 1;
+    for (int l : p.comp[kK]) sp.K *= (uint32_t)(p.B[l] / p.D[l]);
+    // batch composite extended by the contracted key components
+    uint64_t div = nb0;
+    const uint64_t zsub = (uint64_t)p.Z.sub;
+    for (RoleMap* zm : {&sp.zb, &sp.zm, &sp.zn})
+        for (int i = 0; i < zm->n; ++i) zm->t[i].key_stride *= (int64_t)p.n_agg;
+    for (int l : p.comp[kK]) {
+        const uint32_t D = (uint32_t)p.D[l];
+        for (int a = 0; a < 2; ++a) {
+            const int i = ops[a]->pos_of(l);
+            if (i < 0) continue;
+            RoleMap& bm = a == 0 ? sp.xb : sp.yb;
+            Term& t = bm.t[bm.n++];
+            t.div = (uint32_t)div;
+            t.ext = D;
+            t.sub = 1;
+            t.key_stride = ops[a]->key_stride[i];
+            t.loc_stride = 0;
+        }
+        // the partial's slot: contracted key linearised row-major in first-appearance order
+        int64_t cstride = 1;
+        bool after = false;
+        for (int c : p.contracted) {
+            if (after) cstride *= p.D[c];
+            if (c == l) after = true;
+        }
+        Term& t = sp.zb.t[sp.zb.n++];
+        t.div = (uint32_t)div;
+        t.ext = D;
+        t.sub = 1;
+        t.key_stride = cstride * (int64_t)zsub;
+        t.loc_stride = 0;
+        div *= D;
+    }
+    sp.nb = (uint32_t)div;
+    sp.alpha = 1.f;
+    sp.out_bf16 = 0;
+    sp.x_kcontig = affine_stride(sp.xk) == 1;
+    sp.y_kcontig = affine_stride(sp.yk) == 1;
+    cudaError_t e = launch_semiring(sp, s);
+    if (e != cudaSuccess) return cuda_fail(e, "literal join");
+    CombineParams cp;
+    cp.partials = reinterpret_cast<const float*>(ws);
+    cp.z = z;
+    cp.n_groups = p.n_groups;
+    cp.n_agg = p.n_agg;
+    cp.z_sub = zsub;
+    cp.agg = p.agg;
+    cp.alpha = (float)p.alpha;
+    cp.out_bf16 = p.out_bf16;
+    e = launch_combine(cp, s);
+    if (e != cudaSuccess) return cuda_fail(e, "literal combine");
+    return TRA_OK;
+}
+
+int execute_plan(const Plan& p, const void* x, const void* y, void* z, void* ws, cudaStream_t s) {
+    cudaError_t e = cudaSuccess;
+    switch (p.kernel) {
+        case TRA_KERNEL_SEMIRING_F32: {
+            SemiringParams sp = semiring_params(p, x, y, z);
+            if (p.op == kSqdiff && p.sqdiff_expand) {
+                float* xn = reinterpret_cast<float*>(ws);
+                float* yn = reinterpret_cast<float*>((char*)ws + align256((uint64_t)sp.nb * sp.M * 4));
+                LsePrepParams lp;
+                memset(&lp, 0, sizeof(lp));
+                lp.mode = 1;
+                lp.in_bf16 = 0;
+                lp.nb = sp.nb;
+                lp.K = sp.K;
+                lp.src = x, lp.rmax = xn, lp.b = sp.xb, lp.r = sp.xm, lp.k = sp.xk, lp.R = sp.M;
+                if ((e = launch_lse_prep(lp, s)) != cudaSuccess) return cuda_fail(e, "norms of X");
+                lp.src = y, lp.rmax = yn, lp.b = sp.yb, lp.r = sp.yn, lp.k = sp.yk, lp.R = sp.N;
+                if ((e = launch_lse_prep(lp, s)) != cudaSuccess) return cuda_fail(e, "norms of Y");
+                sp.op = kMul;
+                sp.xnorm = xn;
+                sp.ynorm = yn;
+            }
+            e = launch_semiring(sp, s);
+            break;
+        }
+        case TRA_KERNEL_LSE_FACTORED: {
+            SemiringParams sp = semiring_params(p, x, y, z);
+            char* w = reinterpret_cast<char*>(ws);
+            float* ex = reinterpret_cast<float*>(w);
+            w += align256((uint64_t)p.X.total * 4);
+            float* ey = reinterpret_cast<float*>(w);
+            w += align256((uint64_t)p.Y.total * 4);
+            float* rmax = reinterpret_cast<float*>(w);
+            w += align256((uint64_t)sp.nb * sp.M * 4);
+            float* cmax = reinterpret_cast<float*>(w);
+            LsePrepParams lp;
+            memset(&lp, 0, sizeof(lp));
+            lp.mode = 0;
+            lp.in_bf16 = p.in_bf16;
+            lp.nb = sp.nb;
+            lp.K = sp.K;
+            lp.src = x, lp.dst = ex, lp.rmax = rmax, lp.b = sp.xb, lp.r = sp.xm, lp.k = sp.xk, lp.R = sp.M;
+            if ((e = launch_lse_prep(lp, s)) != cudaSuccess) return cuda_fail(e, "max-shift of X");
+            lp.src = y, lp.dst = ey, lp.rmax = cmax, lp.b = sp.yb, lp.r = sp.yn, lp.k = sp.yk, lp.R = sp.N;
+            if ((e = launch_lse_prep(lp, s)) != cudaSuccess) return cuda_fail(e, "max-shift of Y");
+            sp.x_raw = x;
+            sp.y_raw = y;
+            sp.x = ex;
+            sp.y = ey;
+            sp.rowmax = rmax;
+            sp.colmax = cmax;
+            sp.op = kMul;
+            sp.agg = kSum;
+            e = launch_semiring(sp, s);
+            break;
+        }
+        case TRA_KERNEL_ROW_REDUCE: {
+            RowReduceParams rp;
+            memset(&rp, 0, sizeof(rp));
+            rp.x = x;
+            rp.z = z;
+            rp.xr = role_map(p, p.X, kM);
+            rp.xk = role_map(p, p.X, kK);
+            rp.zr = role_map(p, p.Z, kM);
+            rp.R = (uint32_t)p.ext[kM];
+            rp.K = (uint32_t)p.ext[kK];
+            rp.agg = p.agg;
+            rp.alpha = (float)p.alpha;
+            rp.in_bf16 = p.in_bf16;
+            rp.out_bf16 = p.out_bf16;
+            rp.k_affine = rp.xk.n == 1 && rp.xk.t[0].loc_stride == 1 && rp.xk.t[0].sub == rp.xk.t[0].ext;
+            e = launch_row_reduce(rp, s);
+            break;
+        }
+        case TRA_KERNEL_ELEMENTWISE: {
+            ElementwiseParams ep;
+            memset(&ep, 0, sizeof(ep));
+            ep.x = x;
+            ep.y = p.unary ? nullptr : y;
+            ep.z = z;
+            ep.rank = p.Z.rank;
+            ep.op = p.unary ? kId : p.op;
+            ep.alpha = (float)p.alpha;
+            ep.in_bf16 = p.in_bf16;
+            ep.out_bf16 = p.out_bf16;
+            ep.sub_total = FastDiv((uint32_t)p.Z.sub);
+            for (int i = 0; i < p.Z.rank; ++i) {
+                const int l = p.Z.label[i];
+                ep.grid[i] = FastDiv((uint32_t)p.Z.d[i]);
+                ep.sub[i] = FastDiv((uint32_t)(p.Z.shape[i] / p.Z.d[i]));
+                const int xi = p.X.pos_of(l);
+                if (xi >= 0) ep.x_ks[i] = p.X.key_stride[xi], ep.x_ls[i] = p.X.loc_stride[xi];
+                const int yi = p.unary ? -1 : p.Y.pos_of(l);
+                if (yi >= 0) ep.y_ks[i] = p.Y.key_stride[yi], ep.y_ls[i] = p.Y.loc_stride[yi];
+            }
+            ep.I = (uint32_t)(p.Z.shape[p.Z.rank - 1] / p.Z.d[p.Z.rank - 1]);
+            ep.n_runs = (uint64_t)p.Z.total / ep.I;
+            e = launch_elementwise(ep, s);
+            break;
+        }
+        case TRA_KERNEL_TC_BF16:
+            return tc_execute(p, x, y, z, s);
+        case TRA_KERNEL_LITERAL:
+            return execute_literal(p, x, y, z, ws, s);
+        default:
+            return fail(TRA_ERR_UNSUPPORTED, "no kernel for this plan");
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return TRA_OK;
+}
+
+int check_partition(int rank, const int64_t* shape, const int32_t* d, const char* what) {
+    for (int i = 0; i < rank; ++i) {
+        if (shape[i] < 1 || shape[i] > 0x7fffffffLL)
+            return fail(TRA_ERR_ARG, "%s: extent %lld out of range", what, (long long)shape[i]);
+        if (d[i] < 1 || shape[i] % d[i])
+            return fail(TRA_ERR_DIVISIBILITY, "%s: D=%d does not divide B=%lld in dimension %d", what, d[i],
+                        (long long)shape[i], i);
+    }
+    return TRA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ein_plan(const char* spec, const int64_t* bounds, int n_bounds, const int32_t* d, int n_d, tra_plan_t* out) {
+    clear_error();
+    if (!out) return fail(TRA_ERR_ARG, "out is NULL");
+    *out = nullptr;
+    Plan* p = new Plan();
+    const int rc = build_plan(spec, bounds, n_bounds, d, n_d, p);
+    if (rc != TRA_OK) {
+        delete p;
+        return rc;
+    }
+    *out = reinterpret_cast<tra_plan_t>(p);
+    return TRA_OK;
+}
+
+int ein_plan_info(tra_plan_t plan, tra_plan_info* o) {
+    clear_error();
+    if (!plan || !o) return fail(TRA_ERR_ARG, "NULL argument");
+    const Plan& p = *reinterpret_cast<const Plan*>(plan);
+    memset(o, 0, sizeof(*o));
+    o->n_labels = p.n_labels;
+    for (int l = 0; l < p.n_labels; ++l) {
+        o->labels[l] = p.name[l];
+        o->bound[l] = p.B[l];
+        o->part[l] = p.D[l];
+        o->sub_extent[l] = p.B[l] / p.D[l];
+        o->role[l] = p.role[l];
+    }
+    o->rank_x = p.X.rank;
+    o->rank_y = p.unary ? 0 : p.Y.rank;
+    o->rank_z = p.Z.rank;
+    for (int i = 0; i < p.X.rank; ++i) o->key_grid_x[i] = p.X.d[i];
+    if (!p.unary)
+        for (int i = 0; i < p.Y.rank; ++i) o->key_grid_y[i] = p.Y.d[i];
+    for (int i = 0; i < p.Z.rank; ++i) o->key_grid_z[i] = p.Z.d[i];
+    o->n_tasks = p.n_tasks;
+    o->n_groups = p.n_groups;
+    o->n_agg = p.n_agg;
+    o->x_sub = (uint64_t)p.X.sub;
+    o->y_sub = p.unary ? 0 : (uint64_t)p.Y.sub;
+    o->z_sub = (uint64_t)p.Z.sub;
+    o->cost_join = p.cost_join;
+    o->cost_agg = p.cost_agg;
+    o->workspace_bytes = p.ws_bytes;
+    o->in_dtype = p.in_bf16;
+    o->out_dtype = p.out_bf16;
+    o->kernel = p.kernel;
+    return TRA_OK;
+}
+
+int ein_plan_keys(tra_plan_t plan, int32_t* xyz_keys, int64_t capacity) {
+    clear_error();
+    if (!plan || !xyz_keys) return fail(TRA_ERR_ARG, "NULL argument");
+    const Plan& p = *reinterpret_cast<const Plan*>(plan);
+    const uint64_t need = p.n_tasks * (uint64_t)(p.X.rank + (p.unary ? 0 : p.Y.rank) + p.Z.rank);
+    if (capacity < 0 || (uint64_t)capacity < need)
+        return fail(TRA_ERR_ARG, "key buffer holds %lld int32, %llu needed", (long long)capacity,
+                    (unsigned long long)need);
+    fill_keys(p, xyz_keys);
+    return TRA_OK;
+}
+
+int ein_execute(tra_plan_t plan, const void* in0, const void* in1, void* out, void* workspace, size_t ws_bytes,
+                tra_stream_t stream) {
+    clear_error();
+    if (!plan || !in0 || !out) return fail(TRA_ERR_ARG, "NULL plan, input or output");
+    const Plan& p = *reinterpret_cast<const Plan*>(plan);
+    if (!p.unary && !in1) return fail(TRA_ERR_ARG, "binary EinSum needs in1");
+    if (p.ws_bytes && (!workspace || ws_bytes < p.ws_bytes))
+        return fail(TRA_ERR_WORKSPACE, "workspace of %llu bytes needed, %llu given",
+                    (unsigned long long)p.ws_bytes, (unsigned long long)(workspace ? ws_bytes : 0));
+    return execute_plan(p, in0, in1, out, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ein_repartition(int rank, const int64_t* shape, const int32_t* src_d, const int32_t* dst_d, int elem_bytes,
+                    const void* src, void* dst, tra_stream_t stream) {
+    clear_error();
+    if (rank < 1 || rank > TRA_MAX_RANK) return fail(TRA_ERR_RANK, "rank %d outside 1..%d", rank, TRA_MAX_RANK);
+    if (!shape || !src_d || !dst_d || !src || !dst) return fail(TRA_ERR_ARG, "NULL argument");
+    if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8)
+        return fail(TRA_ERR_ARG, "element size %d not in {1,2,4,8}", elem_bytes);
+    int rc = check_partition(rank, shape, src_d, "source");
+    if (rc == TRA_OK) rc = check_partition(rank, shape, dst_d, "destination");
+    if (rc != TRA_OK) return rc;
+    int64_t total = 1;
+    for (int i = 0; i < rank; ++i) total *= shape[i];
+    if (total >= 0x7fffffffLL) return fail(TRA_ERR_UNSUPPORTED, "tensors above 2^31-1 elements are not supported");
+    if (((uintptr_t)src | (uintptr_t)dst) % elem_bytes) return fail(TRA_ERR_ARG, "misaligned buffer");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (total == 0) return TRA_OK;
+    if (memcmp(src_d, dst_d, sizeof(int32_t) * rank) == 0) {
+        cudaError_t e = cudaMemcpyAsync(dst, src, (size_t)total * elem_bytes, cudaMemcpyDeviceToDevice, s);
+        return e == cudaSuccess ? TRA_OK : cuda_fail(e, "copy");
+    }
+    RepartParams rp;
+    memset(&rp, 0, sizeof(rp));
+    rp.src = src;
+    rp.dst = dst;
+    rp.rank = rank;
+    rp.elem_bytes = elem_bytes;
+    int64_t ssub[TRA_MAX_RANK], dsub[TRA_MAX_RANK];
+    int64_t ssub_total = 1, dsub_total = 1;
+    for (int i = 0; i < rank; ++i) {
+        ssub[i] = shape[i] / src_d[i];
+        dsub[i] = shape[i] / dst_d[i];
+        ssub_total *= ssub[i];
+        dsub_total *= dsub[i];
+    }
+    int64_t ls = 1, ks = ssub_total;
+    for (int i = rank - 1; i >= 0; --i) {
+        rp.src_loc_stride[i] = ls;
+        rp.src_key_stride[i] = ks;
+        ls *= ssub[i];
+        ks *= src_d[i];
+        rp.dst_grid[i] = FastDiv((uint32_t)dst_d[i]);
+        rp.dst_sub[i] = FastDiv((uint32_t)dsub[i]);
+        rp.src_sub[i] = FastDiv((uint32_t)ssub[i]);
+    }
+    rp.dst_sub_total = FastDiv((uint32_t)dsub_total);
+    const int64_t run = std::gcd(ssub[rank - 1], dsub[rank - 1]);
+    int vb = 16;
+    while (vb > elem_bytes && (((run * elem_bytes) % vb) || (((uintptr_t)src | (uintptr_t)dst) % vb))) vb >>= 1;
+    rp.vec_bytes = vb;
+    rp.vec_elems = vb / elem_bytes;
+    rp.n_vec = (uint64_t)total / rp.vec_elems;
+    cudaError_t e = launch_repartition(rp, s);
+    return e == cudaSuccess ? TRA_OK : cuda_fail(e, "repartition launch");
+}
+
+int ein_repartition_cost(int rank, const int64_t* shape, const int32_t* src_d, const int32_t* dst_d,
+                         uint64_t* cost) {
+    clear_error();
+    if (rank < 1 || rank > TRA_MAX_RANK) return fail(TRA_ERR_RANK, "rank %d outside 1..%d", rank, TRA_MAX_RANK);
+    if (!shape || !src_d || !dst_d || !cost) return fail(TRA_ERR_ARG, "NULL argument");
+    for (int i = 0; i < rank; ++i) {
+        if (shape[i] < 1) return fail(TRA_ERR_ARG, "extent < 1");
+        if (src_d[i] < 1 || dst_d[i] < 1 || shape[i] % src_d[i] || shape[i] % dst_d[i])
+            return fail(TRA_ERR_DIVISIBILITY, "partition count does not divide extent %lld", (long long)shape[i]);
+    }
+    uint64_t total = 1, ns = 1, nd = 1;
+    for (int i = 0; i < rank; ++i) {
+        total *= (uint64_t)shape[i];
+        ns *= (uint64_t)src_d[i];
+        nd *= (uint64_t)dst_d[i];
+    }
+    // blocks are owned by their row-major linear key id L; elements in
+    // block_L(src) n block_L(dst) stay, all others move
+    uint64_t stay = 0;
+    const uint64_t n = ns < nd ? ns : nd;
+    for (uint64_t L = 0; L < n; ++L) {
+        uint64_t ls = L, ld = L, inter = 1;
+        for (int i = rank - 1; i >= 0 && inter; --i) {
+            const uint64_t ks = ls % (uint64_t)src_d[i], kd = ld % (uint64_t)dst_d[i];
+            ls /= (uint64_t)src_d[i];
+            ld /= (uint64_t)dst_d[i];
+            const uint64_t bs = (uint64_t)shape[i] / src_d[i], bd = (uint64_t)shape[i] / dst_d[i];
+            const uint64_t lo = ks * bs > kd * bd ? ks * bs : kd * bd;
+            const uint64_t hi = (ks + 1) * bs < (kd + 1) * bd ? (ks + 1) * bs : (kd + 1) * bd;
+            inter *= hi > lo ? hi - lo : 0;
+        }
+        stay += inter;
+    }
+    *cost = total - stay;
+    return TRA_OK;
+}
+
+int ein_status(tra_stream_t stream) {
+    clear_error();
+    int v = 0;
+    cudaError_t e = read_and_clear_status(&v, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (v) return fail(v, "a bounded device wait gave up (status %d)", v);
+    return TRA_OK;
+}
+
+void ein_plan_destroy(tra_plan_t plan) { delete reinterpret_cast<Plan*>(plan); }
+
+const char* ein_last_error(void) { return last_error(); }
+
+}  // extern "C"

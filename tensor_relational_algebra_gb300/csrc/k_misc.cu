@@ -1,0 +1,257 @@
+// HBM-bound kernels of the TRA path ("EinDecomp ... tensor relational algebra"):
+//   * repartition (section 2.2: change the partitioning of a relation),
+//   * unary aggregation over contracted labels (section 2.2 aggregation with no
+//     join partner; the logsumexp / max rows of the attention softmax in the
+//     multi-head-attention example of section 2.1),
+//   * join with aggregation "none" (the element-wise example of section 2.1, with
+//     broadcast operands, e.g. exp(Scores - L)),
+//   * ordered combine of per-join-tuple partials (section 2.2 aggregation, GROUP BY
+//     the output key).
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "tra_internal.h"
+
+namespace tra {
+
+__device__ int g_status;  // TRA_ERR_* set by a bounded wait that gave up; 0 otherwise
+
+namespace {
+
+__device__ __forceinline__ float ld_f(const void* p, int64_t off, int bf16) {
+    return bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[off])
+                : reinterpret_cast<const float*>(p)[off];
+}
+__device__ __forceinline__ void st_f(void* p, int64_t off, float v, int bf16) {
+    if (bf16)
+        reinterpret_cast<__nv_bfloat16*>(p)[off] = __float2bfloat16_rn(v);
+    else
+        reinterpret_cast<float*>(p)[off] = v;
+}
+
+// ---------------------------------------------------------------- repartition
+template <typename V>
+__global__ void repartition_kernel(const __grid_constant__ RepartParams p) {
+    const V* __restrict__ src = reinterpret_cast<const V*>(p.src);
+    V* __restrict__ dst = reinterpret_cast<V*>(p.dst);
+    for (uint64_t v = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; v < p.n_vec;
+         v += (uint64_t)gridDim.x * blockDim.x) {
+        const uint32_t e = (uint32_t)(v * p.vec_elems);  // first element, destination physical order
+        uint32_t key = fdiv(e, p.dst_sub_total);
+        uint32_t loc = e - key * p.dst_sub_total.d;
+        int64_t so = 0;
+        for (int i = p.rank - 1; i >= 0; --i) {
+            const uint32_t kq = fdiv(key, p.dst_grid[i]);
+            const uint32_t ki = key - kq * p.dst_grid[i].d;
+            key = kq;
+            const uint32_t lq = fdiv(loc, p.dst_sub[i]);
+            const uint32_t li = loc - lq * p.dst_sub[i].d;
+            loc = lq;
+            const uint32_t g = ki * p.dst_sub[i].d + li;
+            const uint32_t sq = fdiv(g, p.src_sub[i]);
+            so += (int64_t)sq * p.src_key_stride[i] + (int64_t)(g - sq * p.src_sub[i].d) * p.src_loc_stride[i];
+        }
+        dst[v] = src[so / p.vec_elems];
+    }
+}
+
+// ---------------------------------------------------------------- unary aggregation
+template <int AGG>
+__device__ __forceinline__ void agg_step(float& m, float& s, float v) {
+    if (AGG == kLse) {
+        if (v > m) {
+            s = s * __expf(m - v) + 1.f;
+            m = v;
+        } else {
+            s += __expf(v - m);
+        }
+    } else if (AGG == kMax) {
+        m = fmaxf(m, v);
+    } else if (AGG == kMin) {
+        m = fminf(m, v);
+    } else {
+        s += v;
+    }
+}
+
+template <int AGG>
+__device__ __forceinline__ void agg_merge(float& m, float& s, float m2, float s2) {
+    if (AGG == kLse) {
+        const float mm = fmaxf(m, m2);
+        if (mm == -INFINITY) return;
+        s = s * __expf(m - mm) + s2 * __expf(m2 - mm);
+        m = mm;
+    } else if (AGG == kMax) {
+        m = fmaxf(m, m2);
+    } else if (AGG == kMin) {
+        m = fminf(m, m2);
+    } else {
+        s += s2;
+    }
+}
+
+// One warp per output row.
+template <int AGG>
+__global__ void row_reduce_kernel(const __grid_constant__ RowReduceParams p) {
+    const uint64_t warp = (blockIdx.x * (uint64_t)blockDim.x + threadIdx.x) / 32;
+    const int lane = threadIdx.x % 32;
+    if (warp >= p.R) return;
+    const uint32_t r = (uint32_t)warp;
+    const int64_t xo = role_offset(p.xr, r);
+    float m = AGG == kMin ? INFINITY : -INFINITY, s = 0.f;
+    if (p.k_affine && !p.in_bf16 && (xo % 4) == 0 && (p.K % 4) == 0 && ((uintptr_t)p.x % 16) == 0) {
+        const float4* row = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.x) + xo);
+        for (uint32_t k = lane; k < p.K / 4; k += 32) {
+            float4 v = __ldcs(row + k);
+            agg_step<AGG>(m, s, v.x);
+            agg_step<AGG>(m, s, v.y);
+            agg_step<AGG>(m, s, v.z);
+            agg_step<AGG>(m, s, v.w);
+        }
+    } else if (p.k_affine) {
+        for (uint32_t k = lane; k < p.K; k += 32) agg_step<AGG>(m, s, ld_f(p.x, xo + k, p.in_bf16));
+    } else {
+        for (uint32_t k = lane; k < p.K; k += 32) agg_step<AGG>(m, s, ld_f(p.x, xo + role_offset(p.xk, k), p.in_bf16));
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        agg_merge<AGG>(m, s, m2, s2);
+    }
+    if (lane == 0) {
+        float v;
+        if (AGG == kLse) v = m == -INFINITY ? m : m + logf(s);
+        else if (AGG == kSum) v = s;
+        else v = m;
+        st_f(p.z, role_offset(p.zr, r), p.alpha * v, p.out_bf16);
+    }
+}
+
+// ---------------------------------------------------------------- join with aggregation "none"
+__device__ __forceinline__ float ew_op(int op, float x, float y) {
+    switch (op) {
+        case kMul: return x * y;
+        case kAdd: return x + y;
+        case kSqdiff: { float t = x - y; return t * t; }
+        case kSub: return x - y;
+        case kExpsub: return __expf(x - y);
+        default: return x;
+    }
+}
+
+// One warp per run of I contiguous output elements.
+__global__ void elementwise_kernel(const __grid_constant__ ElementwiseParams p) {
+    const uint64_t run = (blockIdx.x * (uint64_t)blockDim.x + threadIdx.x) / 32;
+    const int lane = threadIdx.x % 32;
+    if (run >= p.n_runs) return;
+    const uint32_t e = (uint32_t)(run * p.I);
+    uint32_t key = fdiv(e, p.sub_total);
+    uint32_t loc = e - key * p.sub_total.d;
+    int64_t xo = 0, yo = 0;
+    for (int i = p.rank - 1; i >= 0; --i) {
+        const uint32_t kq = fdiv(key, p.grid[i]);
+        const uint32_t ki = key - kq * p.grid[i].d;
+        key = kq;
+        const uint32_t lq = fdiv(loc, p.sub[i]);
+        const uint32_t li = loc - lq * p.sub[i].d;
+        loc = lq;
+        xo += (int64_t)ki * p.x_ks[i] + (int64_t)li * p.x_ls[i];
+        yo += (int64_t)ki * p.y_ks[i] + (int64_t)li * p.y_ls[i];
+    }
+    const int last = p.rank - 1;
+    const int64_t xs = p.x_ls[last], ys = p.y_ls[last];
+    for (uint32_t j = lane; j < p.I; j += 32) {
+        const float x = ld_f(p.x, xo + (int64_t)j * xs, p.in_bf16);
+        const float y = p.y ? ld_f(p.y, yo + (int64_t)j * ys, p.in_bf16) : 0.f;
+        st_f(p.z, (int64_t)e + j, p.alpha * ew_op(p.op, x, y), p.out_bf16);
+    }
+}
+
+// ---------------------------------------------------------------- ordered combine of partials
+__global__ void combine_kernel(const __grid_constant__ CombineParams p) {
+    const uint64_t total = p.n_groups * p.z_sub;
+    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < total;
+         i += (uint64_t)gridDim.x * blockDim.x) {
+        const uint64_t g = i / p.z_sub, l = i % p.z_sub;
+        const float* part = p.partials + g * p.n_agg * p.z_sub + l;
+        float acc = part[0];
+        for (uint64_t c = 1; c < p.n_agg; ++c) {
+            const float v = part[c * p.z_sub];
+            switch (p.agg) {
+                case kMax: acc = fmaxf(acc, v); break;
+                case kMin: acc = fminf(acc, v); break;
+                case kLse: {
+                    const float m = fmaxf(acc, v);
+                    if (m != -INFINITY) acc = m + logf(expf(acc - m) + expf(v - m));
+                    break;
+                }
+                default: acc += v;
+            }
+        }
+        st_f(p.z, (int64_t)i, p.alpha * acc, p.out_bf16);
+    }
+}
+
+unsigned grid_for(uint64_t work, unsigned per_block) {
+    uint64_t b = (work + per_block - 1) / per_block;
+    if (b > 152ull * 64) b = 152ull * 64;
+    return (unsigned)(b ? b : 1);
+}
+
+}  // namespace
+
+cudaError_t launch_repartition(const RepartParams& p, cudaStream_t s) {
+    if (p.n_vec == 0) return cudaSuccess;
+    const unsigned g = grid_for(p.n_vec, 256);
+    switch (p.vec_bytes) {
+        case 16: repartition_kernel<uint4><<<g, 256, 0, s>>>(p); break;
+        case 8: repartition_kernel<uint2><<<g, 256, 0, s>>>(p); break;
+        case 4: repartition_kernel<uint32_t><<<g, 256, 0, s>>>(p); break;
+        case 2: repartition_kernel<uint16_t><<<g, 256, 0, s>>>(p); break;
+        case 1: repartition_kernel<uint8_t><<<g, 256, 0, s>>>(p); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_row_reduce(const RowReduceParams& p, cudaStream_t s) {
+    if (p.R == 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)(((uint64_t)p.R * 32 + 255) / 256);
+    switch (p.agg) {
+        case kLse: row_reduce_kernel<kLse><<<blocks, 256, 0, s>>>(p); break;
+        case kMax: row_reduce_kernel<kMax><<<blocks, 256, 0, s>>>(p); break;
+        case kMin: row_reduce_kernel<kMin><<<blocks, 256, 0, s>>>(p); break;
+        case kSum: row_reduce_kernel<kSum><<<blocks, 256, 0, s>>>(p); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_elementwise(const ElementwiseParams& p, cudaStream_t s) {
+    if (p.n_runs == 0) return cudaSuccess;
+    const uint64_t threads = p.n_runs * 32;
+    elementwise_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
+    const uint64_t total = p.n_groups * p.z_sub;
+    if (total == 0) return cudaSuccess;
+    combine_kernel<<<grid_for(total, 256), 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_status(int* value, cudaStream_t s) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(value, g_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    const int zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return e;
+    return cudaStreamSynchronize(s);
+}
+
+}  // namespace tra

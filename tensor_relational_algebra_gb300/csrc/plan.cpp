@@ -1,0 +1,337 @@
+// Host planner: spec parsing, validation, key space, join enumeration, cost
+// terms and kernel choice.  Touches no device.
+//
+// "EinDecomp ... tensor relational algebra":
+//  * section 2.1 -- extended EinSum: labels on the right-hand side that are not in
+//    the output are contracted; aggregation sum/max/min/logsumexp; any binary op.
+//  * section 2.2 -- tensor [B1..] under d=[D1..] (D_i | B_i) is a relation of
+//    prod D_i sub-tensors of shape [B_i/D_i]; matmul's d is [d_i, d_jX, d_jY, d_k]
+//    with d_jX = d_jY; join pairs key-matched sub-tensors; aggregation groups
+//    by the output key.
+//  * section 3.1 -- cost model: join P*(|X_sub|+|Y_sub|), aggregation
+//    (P/n_agg)*(n_agg-1)*|Z_sub|, P read here as the number of join tuples.
+//  * section 3.2 -- the number of tasks is the number of tuples the join produces.
+#include "plan.h"
+
+#include <cctype>
+#include <cerrno>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+namespace tra {
+
+namespace {
+thread_local std::string g_err;
+}
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+void clear_error() { g_err.clear(); }
+const char* last_error() { return g_err.c_str(); }
+
+uint64_t align256(uint64_t v) { return (v + 255) & ~uint64_t(255); }
+
+Plan::~Plan() {
+    if (tc) tc_free(tc);
+}
+
+namespace {
+
+std::vector<std::string> split(const std::string& s, char c) {
+    std::vector<std::string> out;
+    size_t start = 0;
+    for (;;) {
+        size_t pos = s.find(c, start);
+        out.push_back(s.substr(start, pos == std::string::npos ? std::string::npos : pos - start));
+        if (pos == std::string::npos) break;
+        start = pos + 1;
+    }
+    return out;
+}
+
+int parse_op(const std::string& s) {
+    if (s == "mul") return kMul;
+    if (s == "add") return kAdd;
+    if (s == "sqdiff") return kSqdiff;
+    if (s == "sub") return kSub;
+    if (s == "expsub") return kExpsub;
+    return -1;
+}
+
+int parse_agg(const std::string& s) {
+    if (s == "sum") return kSum;
+    if (s == "max") return kMax;
+    if (s == "min") return kMin;
+    if (s == "lse") return kLse;
+    if (s == "none") return kNone;
+    return -1;
+}
+
+}  // namespace
+
+void layout_operand(Operand& t, const Plan& p) {
+    t.sub = 1;
+    t.nkeys = 1;
+    for (int i = 0; i < t.rank; ++i) {
+        const int l = t.label[i];
+        t.d[i] = p.D[l];
+        t.shape[i] = p.B[l];
+        t.sub *= p.B[l] / p.D[l];
+        t.nkeys *= p.D[l];
+    }
+    t.total = t.sub * t.nkeys;
+    int64_t ls = 1, ks = t.sub;
+    for (int i = t.rank - 1; i >= 0; --i) {
+        const int l = t.label[i];
+        t.loc_stride[i] = ls;
+        t.key_stride[i] = ks;
+        ls *= p.B[l] / p.D[l];
+        ks *= p.D[l];
+    }
+}
+
+RoleMap role_map(const Plan& p, const Operand& t, int role) {
+    RoleMap m;
+    memset(&m, 0, sizeof(m));
+    uint64_t div = 1;
+    for (int l : p.comp[role]) {
+        const int i = t.pos_of(l);
+        if (i >= 0) {
+            Term& tm = m.t[m.n++];
+            tm.div = (uint32_t)div;
+            tm.ext = (uint32_t)p.B[l];
+            tm.sub = (uint32_t)(p.B[l] / p.D[l]);
+            tm.key_stride = t.key_stride[i];
+            tm.loc_stride = t.loc_stride[i];
+        }
+        div *= (uint64_t)p.B[l];
+    }
+    return m;
+}
+
+int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int32_t* d, int n_d, Plan* p) {
+    if (!spec || !p) return fail(TRA_ERR_ARG, "null spec or plan");
+    p->spec = spec;
+    std::vector<std::string> parts = split(spec, ':');
+    const std::string eq = parts[0];
+    const size_t arrow = eq.find("->");
+    if (arrow == std::string::npos) return fail(TRA_ERR_PARSE, "spec '%s': missing '->'", spec);
+    const std::string lhs = eq.substr(0, arrow), rhs = eq.substr(arrow + 2);
+    std::vector<std::string> ins = split(lhs, ',');
+    if (ins.size() < 1 || ins.size() > 2) return fail(TRA_ERR_PARSE, "spec '%s': one or two operands expected", spec);
+    p->unary = ins.size() == 1;
+    if (parts.size() < 3) return fail(TRA_ERR_PARSE, "spec '%s': expected '<eq>:<op>:<agg>'", spec);
+    if (p->unary) {
+        if (!parts[1].empty()) return fail(TRA_ERR_PARSE, "spec '%s': a unary EinSum takes no op", spec);
+        p->op = kId;
+    } else {
+        p->op = parse_op(parts[1]);
+        if (p->op < 0) return fail(TRA_ERR_PARSE, "spec '%s': unknown op '%s'", spec, parts[1].c_str());
+    }
+    p->agg = parse_agg(parts[2]);
+    if (p->agg < 0) return fail(TRA_ERR_PARSE, "spec '%s': unknown aggregation '%s'", spec, parts[2].c_str());
+    for (size_t i = 3; i < parts.size(); ++i) {
+        const std::string& o = parts[i];
+        const size_t eqp = o.find('=');
+        if (eqp == std::string::npos) return fail(TRA_ERR_PARSE, "spec '%s': option '%s' needs '='", spec, o.c_str());
+        const std::string k = o.substr(0, eqp), v = o.substr(eqp + 1);
+        if (k == "in" && (v == "f32" || v == "bf16")) p->in_bf16 = v == "bf16";
+        else if (k == "out" && (v == "f32" || v == "bf16")) p->out_bf16 = v == "bf16";
+        else if (k == "mode" && (v == "fused" || v == "literal")) p->literal = v == "literal";
+        else if (k == "sqdiff" && (v == "direct" || v == "expand")) p->sqdiff_expand = v == "expand";
+        else if (k == "alpha") {
+            char* end = nullptr;
+            errno = 0;
+            p->alpha = strtod(v.c_str(), &end);
+            if (errno || !end || *end || v.empty() || !std::isfinite(p->alpha))
+                return fail(TRA_ERR_PARSE, "spec '%s': bad alpha '%s'", spec, v.c_str());
+        } else {
+            return fail(TRA_ERR_PARSE, "spec '%s': unknown option '%s'", spec, o.c_str());
+        }
+    }
+
+    // labels, first appearance X then Y
+    std::string order;
+    Operand* ops[2] = {&p->X, &p->Y};
+    for (size_t a = 0; a < ins.size(); ++a) {
+        const std::string& s = ins[a];
+        if (s.empty() || (int)s.size() > TRA_MAX_RANK)
+            return fail(TRA_ERR_RANK, "operand '%s': rank must be 1..%d", s.c_str(), TRA_MAX_RANK);
+        ops[a]->rank = (int)s.size();
+        for (size_t i = 0; i < s.size(); ++i) {
+            const char c = s[i];
+            if (!std::isalpha((unsigned char)c)) return fail(TRA_ERR_PARSE, "label '%c' is not a letter", c);
+            if (s.find(c) != i) return fail(TRA_ERR_PARSE, "label '%c' repeats inside operand '%s'", c, s.c_str());
+            size_t pos = order.find(c);
+            if (pos == std::string::npos) {
+                if ((int)order.size() >= TRA_MAX_LABELS) return fail(TRA_ERR_RANK, "more than %d labels", TRA_MAX_LABELS);
+                order.push_back(c);
+                pos = order.size() - 1;
+            }
+            ops[a]->label[i] = (int)pos;
+        }
+    }
+    if ((int)rhs.size() > TRA_MAX_RANK) return fail(TRA_ERR_RANK, "output rank above %d", TRA_MAX_RANK);
+    p->Z.rank = (int)rhs.size();
+    for (size_t i = 0; i < rhs.size(); ++i) {
+        const char c = rhs[i];
+        const size_t pos = order.find(c);
+        if (pos == std::string::npos) return fail(TRA_ERR_PARSE, "output label '%c' is in no operand", c);
+        if (rhs.find(c) != i) return fail(TRA_ERR_PARSE, "output label '%c' repeats", c);
+        p->Z.label[i] = (int)pos;
+    }
+    p->n_labels = (int)order.size();
+    for (int l = 0; l < p->n_labels; ++l) p->name[l] = order[l];
+
+    if (!bounds || n_bounds != p->n_labels)
+        return fail(TRA_ERR_RANK, "%d bounds given, %d labels in '%s'", n_bounds, p->n_labels, spec);
+    const int nd_want = p->X.rank + (p->unary ? 0 : p->Y.rank);
+    if (!d || n_d != nd_want) return fail(TRA_ERR_RANK, "%d partition counts given, %d index positions", n_d, nd_want);
+    for (int l = 0; l < p->n_labels; ++l) {
+        if (bounds[l] < 1 || bounds[l] > 0x7fffffffLL)
+            return fail(TRA_ERR_ARG, "bound of '%c' out of range", p->name[l]);
+        p->B[l] = bounds[l];
+        p->D[l] = 0;
+    }
+    int di = 0;
+    for (size_t a = 0; a < ins.size(); ++a) {
+        for (int i = 0; i < ops[a]->rank; ++i, ++di) {
+            const int l = ops[a]->label[i];
+            if (d[di] < 1) return fail(TRA_ERR_ARG, "partition count %d < 1", d[di]);
+            if (p->B[l] % d[di])
+                return fail(TRA_ERR_DIVISIBILITY, "D=%d does not divide B=%lld for label '%c'", d[di],
+                            (long long)p->B[l], p->name[l]);
+            if (p->D[l] && p->D[l] != d[di])
+                return fail(TRA_ERR_SHARED_LABEL_D, "label '%c' partitioned %d ways in X and %d in Y", p->name[l],
+                            p->D[l], d[di]);
+            p->D[l] = d[di];
+        }
+    }
+
+    // roles
+    bool inx[TRA_MAX_LABELS] = {}, iny[TRA_MAX_LABELS] = {}, inz[TRA_MAX_LABELS] = {};
+    for (int i = 0; i < p->X.rank; ++i) inx[p->X.label[i]] = true;
+    if (!p->unary)
+        for (int i = 0; i < p->Y.rank; ++i) iny[p->Y.label[i]] = true;
+    for (int i = 0; i < p->Z.rank; ++i) inz[p->Z.label[i]] = true;
+    for (int l = 0; l < p->n_labels; ++l) {
+        if (!inz[l]) p->role[l] = kK;
+        else if (inx[l] && iny[l]) p->role[l] = kBatch;
+        else if (inx[l]) p->role[l] = kM;
+        else p->role[l] = kN;
+        if (!inz[l]) p->contracted.push_back(l);
+    }
+    if (p->agg == kNone && !p->contracted.empty())
+        return fail(TRA_ERR_PARSE, "aggregation 'none' with contracted label '%c'", p->name[p->contracted[0]]);
+    if (p->agg != kNone && p->contracted.empty())
+        return fail(TRA_ERR_PARSE, "no contracted label: use aggregation 'none'");
+
+    layout_operand(p->X, *p);
+    if (!p->unary) layout_operand(p->Y, *p);
+    layout_operand(p->Z, *p);
+    const int64_t lim = 0x7fffffffLL;
+    if (p->X.total > lim || p->Y.total > lim || p->Z.total > lim)
+        return fail(TRA_ERR_UNSUPPORTED, "tensors above 2^31-1 elements are not supported");
+
+    // composite order (innermost first): M by X's memory order, N by Y's, K by X's
+    // then Y-only contracted labels by Y's, batch by Z's
+    for (int r = 0; r < 4; ++r) p->comp[r].clear();
+    for (int i = p->Z.rank - 1; i >= 0; --i)
+        if (p->role[p->Z.label[i]] == kBatch) p->comp[kBatch].push_back(p->Z.label[i]);
+    for (int i = p->X.rank - 1; i >= 0; --i) {
+        const int l = p->X.label[i];
+        if (p->role[l] == kM) p->comp[kM].push_back(l);
+        if (p->role[l] == kK) p->comp[kK].push_back(l);
+    }
+    if (!p->unary)
+        for (int i = p->Y.rank - 1; i >= 0; --i) {
+            const int l = p->Y.label[i];
+            if (p->role[l] == kN) p->comp[kN].push_back(l);
+            if (p->role[l] == kK && !inx[l]) p->comp[kK].push_back(l);
+        }
+    for (int r = 0; r < 4; ++r) {
+        uint64_t e = 1;
+        for (int l : p->comp[r]) e *= (uint64_t)p->B[l];
+        if (e > 0x7fffffffull) return fail(TRA_ERR_UNSUPPORTED, "a composite extent exceeds 2^31-1");
+        p->ext[r] = e;
+    }
+
+    // task count and cost terms
+    p->n_tasks = 1;
+    p->n_groups = 1;
+    for (int l = 0; l < p->n_labels; ++l) {
+        p->n_tasks *= (uint64_t)p->D[l];
+        if (inz[l]) p->n_groups *= (uint64_t)p->D[l];
+    }
+    p->n_agg = p->n_tasks / p->n_groups;
+    const uint64_t xs = (uint64_t)p->X.sub, ys = p->unary ? 0 : (uint64_t)p->Y.sub, zs = (uint64_t)p->Z.sub;
+    p->cost_join = p->n_tasks * (xs + ys);
+    p->cost_agg = (p->n_tasks / p->n_agg) * (p->n_agg - 1) * zs;
+
+    // kernel choice and workspace
+    p->ws_bytes = 0;
+    if (p->literal && p->agg != kNone) {
+        p->kernel = TRA_KERNEL_LITERAL;
+        p->ws_bytes = align256(p->n_tasks * zs * sizeof(float));
+    } else if (p->agg == kNone) {
+        p->kernel = TRA_KERNEL_ELEMENTWISE;
+    } else if (p->unary) {
+        p->kernel = TRA_KERNEL_ROW_REDUCE;
+    } else if (p->op == kAdd && p->agg == kLse) {
+        p->kernel = TRA_KERNEL_LSE_FACTORED;
+        const uint64_t nb = p->ext[kBatch];
+        p->ws_bytes = align256((uint64_t)p->X.total * 4) + align256((uint64_t)p->Y.total * 4) +
+                      align256(nb * p->ext[kM] * 4) + align256(nb * p->ext[kN] * 4);
+    } else if (p->op == kMul && p->agg == kSum && p->in_bf16 && tc_plan(p)) {
+        p->kernel = TRA_KERNEL_TC_BF16;
+    } else {
+        p->kernel = TRA_KERNEL_SEMIRING_F32;
+        if (p->op == kSqdiff && p->agg == kSum && p->sqdiff_expand) {
+            if (p->in_bf16) return fail(TRA_ERR_UNSUPPORTED, "sqdiff=expand needs fp32 inputs");
+            const uint64_t nb = p->ext[kBatch];
+            p->ws_bytes = align256(nb * p->ext[kM] * 4) + align256(nb * p->ext[kN] * 4);
+        }
+    }
+    return TRA_OK;
+}
+
+// Join tuples in canonical order: Z key row-major, then the contracted labels' key
+// components (first-appearance order) row-major.  Row = X key, Y key, Z key.
+void fill_keys(const Plan& p, int32_t* out) {
+    const int w = p.X.rank + (p.unary ? 0 : p.Y.rank) + p.Z.rank;
+    int32_t comp[TRA_MAX_LABELS];
+    uint64_t row = 0;
+    for (uint64_t g = 0; g < p.n_groups; ++g) {
+        uint64_t t = g;
+        for (int i = p.Z.rank - 1; i >= 0; --i) {
+            comp[p.Z.label[i]] = (int32_t)(t % (uint64_t)p.D[p.Z.label[i]]);
+            t /= (uint64_t)p.D[p.Z.label[i]];
+        }
+        for (uint64_t c = 0; c < p.n_agg; ++c, ++row) {
+            uint64_t u = c;
+            for (int i = (int)p.contracted.size() - 1; i >= 0; --i) {
+                const int l = p.contracted[i];
+                comp[l] = (int32_t)(u % (uint64_t)p.D[l]);
+                u /= (uint64_t)p.D[l];
+            }
+            int32_t* r = out + row * w;
+            int o = 0;
+            for (int i = 0; i < p.X.rank; ++i) r[o++] = comp[p.X.label[i]];
+            if (!p.unary)
+                for (int i = 0; i < p.Y.rank; ++i) r[o++] = comp[p.Y.label[i]];
+            for (int i = 0; i < p.Z.rank; ++i) r[o++] = comp[p.Z.label[i]];
+        }
+    }
+}
+
+}  // namespace tra

@@ -1,0 +1,80 @@
+// Host planner of libtra.so: turns (spec, bounds, d) into a TRA plan.
+// "EinDecomp ... tensor relational algebra": section 2.2 (partition vector,
+// key -> index range, EinSum -> TRA lowering) and sections 3.1 / 3.2 (task
+// triple, cost model, task count).
+#pragma once
+
+#include <string>
+#include <vector>
+
+#include "tra_internal.h"
+
+namespace tra {
+
+struct Operand {
+    int rank = 0;
+    int label[TRA_MAX_RANK] = {};
+    int32_t d[TRA_MAX_RANK] = {};
+    int64_t shape[TRA_MAX_RANK] = {};
+    int64_t sub = 1;    // elements per sub-tensor
+    int64_t nkeys = 1;  // number of sub-tensors
+    int64_t total = 1;  // elements
+    int64_t key_stride[TRA_MAX_RANK] = {};
+    int64_t loc_stride[TRA_MAX_RANK] = {};
+    int pos_of(int l) const {
+        for (int i = 0; i < rank; ++i)
+            if (label[i] == l) return i;
+        return -1;
+    }
+};
+
+struct TcPlan;  // tensor-core launch description (k_tc.cu)
+
+struct Plan {
+    std::string spec;
+    int op = kMul, agg = kSum;
+    double alpha = 1.0;
+    int in_bf16 = 0, out_bf16 = 0;
+    int literal = 0;
+    int sqdiff_expand = 0;
+    bool unary = false;
+
+    int n_labels = 0;
+    char name[TRA_MAX_LABELS] = {};
+    int64_t B[TRA_MAX_LABELS] = {};
+    int32_t D[TRA_MAX_LABELS] = {};
+    int role[TRA_MAX_LABELS] = {};
+    std::vector<int> contracted;  // first-appearance order
+
+    Operand X, Y, Z;
+    std::vector<int> comp[4];  // labels per role, composite order (innermost first)
+    uint64_t ext[4] = {1, 1, 1, 1};
+
+    uint64_t n_tasks = 0, n_groups = 0, n_agg = 0;
+    uint64_t cost_join = 0, cost_agg = 0;
+    int kernel = 0;
+    uint64_t ws_bytes = 0;
+
+    TcPlan* tc = nullptr;
+    ~Plan();
+};
+
+// Error reporting (thread-local message, returned code).
+int fail(int code, const char* fmt, ...);
+void clear_error();
+const char* last_error();
+
+int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int32_t* d, int n_d, Plan* p);
+void layout_operand(Operand& t, const Plan& p);
+RoleMap role_map(const Plan& p, const Operand& t, int role);
+void fill_keys(const Plan& p, int32_t* out);
+
+// Tensor-core planning (k_tc.cu): returns true and sets p->tc when the BF16
+// sum-of-products can run on tcgen05 with TMA tiles that stay inside blocks.
+bool tc_plan(Plan* p);
+void tc_free(TcPlan* t);
+int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_t s);
+
+uint64_t align256(uint64_t v);
+
+}  // namespace tra

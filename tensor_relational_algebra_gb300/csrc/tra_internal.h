@@ -1,0 +1,179 @@
+// Internal structures shared by the host planner and the CUDA kernels of libtra.so.
+//
+// Addressing model.  Every label l of a plan has a global extent B_l, a
+// partition count D_l and a block-local extent b_l = B_l / D_l.  In the
+// relation ("blocked") layout of an operand with labels l_0..l_{r-1}, the
+// element with global indices g_l sits at
+//     sum_i (g_i / b_i) * key_stride_i + (g_i % b_i) * loc_stride_i
+// with loc_stride_i = prod_{j>i} b_j and key_stride_i = (prod_{j>i} D_j) * |sub|
+// (key k -> index range [k*b, (k+1)*b) of the key definition in section 2.2 of
+// the EinDecomp page).  Labels are grouped into roles -- batch (X, Y and Z), M
+// (X and Z), N (Y and Z), K (contracted) -- and each role's labels are folded
+// into one composite index; a RoleMap turns a composite index into that role's
+// part of an operand offset.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/tra.h"
+#include "fastdiv.h"
+
+#ifdef __CUDACC__
+#define TRA_HD __host__ __device__ __forceinline__
+#else
+#define TRA_HD inline
+#endif
+
+namespace tra {
+
+constexpr int kMaxTerms = 8;
+
+enum Role { kBatch = 0, kM = 1, kN = 2, kK = 3 };
+enum Op { kMul = 0, kAdd = 1, kSqdiff = 2, kSub = 3, kExpsub = 4, kId = 5 };
+enum Agg { kSum = 0, kMax = 1, kMin = 2, kLse = 3, kNone = 4 };
+
+struct Term {
+    uint32_t div;        // composite stride of the label inside its role
+    uint32_t ext;        // extent of the label inside the composite
+    uint32_t sub;        // block-local extent (ext when the label is not split)
+    uint32_t pad_;
+    int64_t key_stride;  // elements per key step
+    int64_t loc_stride;  // elements per local step
+};
+
+struct RoleMap {
+    int32_t n;
+    int32_t pad_;
+    Term t[kMaxTerms];
+};
+
+TRA_HD int64_t role_offset(const RoleMap& r, uint32_t idx) {
+    int64_t off = 0;
+    for (int i = 0; i < r.n; ++i) {
+        uint32_t g = (idx / r.t[i].div) % r.t[i].ext;
+        uint32_t k = g / r.t[i].sub;
+        uint32_t l = g - k * r.t[i].sub;
+        off += (int64_t)k * r.t[i].key_stride + (int64_t)l * r.t[i].loc_stride;
+    }
+    return off;
+}
+
+// Stride of consecutive composite indices when the whole run [idx, idx+len) stays
+// affine in this operand: returns the element stride, or 0 when not affine.
+inline int64_t affine_stride(const RoleMap& r) {
+    if (r.n == 0) return 0;
+    const Term& t = r.t[0];
+    if (t.div != 1) return 0;
+    return t.loc_stride;
+}
+
+// Join + aggregate on CUDA cores (register-tiled).  Operands may be fp32 or bf16.
+struct SemiringParams {
+    const void* x;
+    const void* y;
+    void* z;
+    RoleMap xb, xm, xk;
+    RoleMap yb, yn, yk;
+    RoleMap zb, zm, zn;
+    uint32_t nb, M, N, K;
+    int32_t op, agg;
+    float alpha;
+    int32_t in_bf16, out_bf16;
+    int32_t x_kcontig, x_mcontig, y_ncontig, y_kcontig;
+    // logsumexp factored form: the operands are exp(x - rowmax) and exp(y - colmax)
+    // (fp32 scratch), and the epilogue adds rowmax + colmax + log(sum).
+    const float* rowmax;  // [nb * M] or null
+    const float* colmax;  // [nb * N] or null
+    const void* x_raw;    // original operands for the underflow fallback
+    const void* y_raw;
+    // squared distance by expansion: the epilogue forms xn + yn - 2*sum
+    const float* xnorm;   // [nb * M] or null
+    const float* ynorm;   // [nb * N] or null
+};
+
+// Per-operand row-max / exp-shift preparation of the factored logsumexp.
+struct LsePrepParams {
+    const void* src;      // operand (fp32 or bf16)
+    float* dst;           // exp(v - max) in the same layout as src (fp32)
+    float* rmax;          // [nb * R]
+    RoleMap b, r, k;      // batch, row (M or N) and contracted maps of this operand
+    uint32_t nb, R, K;
+    int32_t in_bf16;
+    int32_t mode;         // 0: row max + exp shift;  1: sum of squares (for sqdiff expansion)
+};
+
+// Unary aggregation over the contracted labels (row reduction).
+struct RowReduceParams {
+    const void* x;
+    void* z;
+    RoleMap xr, xk;       // X: output-row composite (all Z labels), contracted composite
+    RoleMap zr;           // Z: output-row composite
+    uint32_t R, K;
+    int32_t agg;
+    float alpha;
+    int32_t in_bf16, out_bf16;
+    int32_t k_affine;     // the contracted composite is contiguous (stride 1) over all of [0, K)
+};
+
+// Join with aggregation "none": every output element is op(x, y); operands may broadcast.
+// The kernel walks Z in its physical (blocked) order, one run of I contiguous
+// elements (the innermost label's block-local extent) at a time.  Every label
+// of X and Y is a label of Z with the same partition count, so an operand's
+// offset is sum_i key_i * ks[i] + loc_i * ls[i] over Z's index positions i
+// (ks = ls = 0 where the operand lacks that label).
+struct ElementwiseParams {
+    const void* x;
+    const void* y;      // null for a unary (identity) join
+    void* z;
+    int32_t rank;       // rank of Z
+    int32_t op;
+    float alpha;
+    int32_t in_bf16, out_bf16;
+    uint32_t I;         // run length (elements)
+    uint64_t n_runs;
+    FastDiv sub_total;  // elements per Z block
+    FastDiv grid[TRA_MAX_RANK], sub[TRA_MAX_RANK];
+    int64_t x_ks[TRA_MAX_RANK], x_ls[TRA_MAX_RANK];
+    int64_t y_ks[TRA_MAX_RANK], y_ls[TRA_MAX_RANK];
+};
+
+// Repartition (permute copy) between two relation layouts of one tensor: walks the
+// destination in physical order, vec_elems elements per thread; a vector never
+// leaves a run that is contiguous in both layouts.
+struct RepartParams {
+    const void* src;
+    void* dst;
+    int32_t rank;
+    int32_t elem_bytes;
+    int32_t vec_elems;
+    int32_t vec_bytes;
+    uint64_t n_vec;
+    FastDiv dst_sub_total;
+    FastDiv dst_grid[TRA_MAX_RANK], dst_sub[TRA_MAX_RANK], src_sub[TRA_MAX_RANK];
+    int64_t src_key_stride[TRA_MAX_RANK], src_loc_stride[TRA_MAX_RANK];
+};
+
+// Ordered combine of per-join-tuple partials (literal mode).
+struct CombineParams {
+    const float* partials;  // [n_groups][n_agg][z_sub]
+    void* z;                // Z relation layout: group g's block at g * z_sub
+    uint64_t n_groups, n_agg, z_sub;
+    int32_t agg;
+    float alpha;
+    int32_t out_bf16;
+};
+
+cudaError_t launch_semiring(const SemiringParams& p, cudaStream_t s);
+cudaError_t launch_semiring_simple(const SemiringParams& p, cudaStream_t s);
+cudaError_t launch_lse_prep(const LsePrepParams& p, cudaStream_t s);
+cudaError_t launch_row_reduce(const RowReduceParams& p, cudaStream_t s);
+cudaError_t launch_elementwise(const ElementwiseParams& p, cudaStream_t s);
+cudaError_t launch_repartition(const RepartParams& p, cudaStream_t s);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
+
+// Device status word written by bounded waits that give up (TRA_ERR_TIMEOUT).
+cudaError_t read_and_clear_status(int* value, cudaStream_t s);
+
+}  // namespace tra

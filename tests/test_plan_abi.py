@@ -1,0 +1,150 @@
+"""C-ABI library without a GPU: symbols, planner facts and error paths.
+
+The planner's key space, task counts and cost terms ("EinDecomp ... tensor
+relational algebra", sections 2.2, 3.1, 3.2) must equal the oracle's brute-force
+enumeration bit for bit.
+"""
+import ctypes
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import tra as otra
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLD = os.path.join(ROOT, "tests", "golden")
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "tra.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:int|void|const char\*)\s+(ein_\w+)\s*\(", src, re.M)))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = ctypes.CDLL(os.path.join(ROOT, "tensor_relational_algebra_gb300", "libtra.so"))
+    syms = declared_symbols()
+    assert len(syms) >= 9
+    for s in syms:
+        assert hasattr(so, s), s
+
+
+CASES = [
+    ("ij,jk->ik", {"i": 64, "j": 64, "k": 64}, [4, 1, 1, 4]),
+    ("ij,jk->ik", {"i": 64, "j": 64, "k": 64}, [1, 4, 4, 1]),
+    ("ij,jk->ik", {"i": 64, "j": 64, "k": 64}, [2, 2, 2, 2]),
+    ("ij,jk->ik", {"i": 8192, "j": 256, "k": 8192}, [8, 1, 1, 8]),
+    ("abef,cfed->abcd", {c: 64 for c in "abefcd"}, [4, 1, 1, 1, 4, 1, 1, 1]),
+    ("abef,cfed->abcd", {c: 8 for c in "abefcd"}, [2, 1, 2, 4, 2, 4, 2, 1]),
+    ("ij,jk->ik", {"i": 16384, "j": 16384, "k": 16384}, [4, 2, 2, 2]),
+    ("ij,jk->ik", {"i": 16384, "j": 16384, "k": 16384}, [1, 8, 8, 1]),
+    ("sa,ahd->shd", {"s": 64, "a": 32, "h": 4, "d": 16}, [2, 2, 2, 4, 1]),
+    ("shd,thd->hst", {"s": 64, "h": 4, "d": 16, "t": 32}, [1, 4, 2, 2, 4, 2]),
+    ("hst,thd->shd", {"h": 4, "s": 64, "t": 32, "d": 16}, [4, 2, 2, 2, 4, 1]),
+    ("shd,ahd->sa", {"s": 64, "h": 4, "d": 16, "a": 32}, [1, 2, 4, 2, 2, 4]),
+    ("hst,hs->hst", {"h": 4, "s": 8, "t": 16}, [2, 4, 1, 2, 4]),
+    ("ijl,jk->ik", {"i": 4, "j": 6, "l": 2, "k": 4}, [2, 3, 2, 3, 2]),
+]
+
+
+def spec_for(eq):
+    if eq == "hst,hs->hst":
+        return eq + ":expsub:none"
+    return eq + ":mul:sum"
+
+
+@pytest.mark.parametrize("eq,bounds,d", CASES)
+def test_plan_matches_bruteforce(lib, eq, bounds, d):
+    p = lib.Plan(spec_for(eq), bounds, d)
+    ref = otra.plan_bruteforce(eq, bounds, d)
+    for k in ("n_tasks", "n_groups", "n_agg", "cost_join", "cost_agg"):
+        assert getattr(p, k) == ref[k], k
+    assert p.info.x_sub == ref["x_sub"] and p.info.y_sub == ref["y_sub"] and p.info.z_sub == ref["z_sub"]
+    assert p.dvec("z") == ref["dz"]
+    if ref["n_tasks"] <= 4096:
+        assert p.keys() == ref["tasks"]
+
+
+def test_plan_golden(lib):
+    g = json.load(open(os.path.join(GOLD, "cost_terms.json")))
+    for c in g["cases"]:
+        p = lib.Plan(spec_for(c["eq"]), c["bounds"], c["d"])
+        for k in ("n_tasks", "n_groups", "n_agg", "cost_join", "cost_agg"):
+            assert getattr(p, k) == c[k], (c["eq"], c["d"], k)
+
+
+def test_unary_plan(lib):
+    p = lib.Plan("hst->hs::lse", {"h": 32, "s": 64, "t": 128}, [4, 2, 1])
+    ref = otra.plan_bruteforce("hst->hs", {"h": 32, "s": 64, "t": 128}, [4, 2, 1])
+    assert (p.n_tasks, p.n_groups, p.n_agg, p.cost_join, p.cost_agg) == (
+        ref["n_tasks"], ref["n_groups"], ref["n_agg"], ref["cost_join"], ref["cost_agg"])
+    assert p.kernel == "row_reduce"
+
+
+def test_kernel_choice(lib):
+    assert lib.Plan("ij,jk->ik:sqdiff:sum", [64, 64, 64], [1, 1, 1, 1]).kernel == "semiring_f32"
+    assert lib.Plan("ij,jk->ik:add:lse", [64, 64, 64], [1, 1, 1, 1]).kernel == "lse_factored"
+    assert lib.Plan("ij,jk->ik:add:max:mode=literal", [64, 64, 64], [1, 2, 2, 1]).kernel == "literal"
+    assert lib.Plan("hst,hs->hst:expsub:none:out=bf16", [2, 4, 8], [1, 1, 1, 1, 1]).kernel == "elementwise"
+    p = lib.Plan("ij,jk->ik:add:lse", [64, 32, 16], [2, 1, 1, 2])
+    assert p.workspace_bytes >= (64 * 32 + 32 * 16 + 64 + 16) * 4
+    assert lib.Plan("ij,jk->ik:mul:sum", [64, 64, 64], [1, 1, 1, 1]).workspace_bytes == 0
+
+
+@pytest.mark.parametrize("spec,bounds,d,code", [
+    ("ij,jk->ik:mul:sum", [64, 64, 64], [3, 1, 1, 1], "TRA_ERR_DIVISIBILITY"),
+    ("ij,jk->ik:mul:sum", [64, 64, 64], [1, 2, 4, 1], "TRA_ERR_SHARED_LABEL_D"),
+    ("ij,jk->ik:mul:sum", [64, 64], [1, 1, 1, 1], "TRA_ERR_RANK"),
+    ("ij,jk->ik:mul:sum", [64, 64, 64], [1, 1, 1], "TRA_ERR_RANK"),
+    ("ij,jk->ik:pow:sum", [64, 64, 64], [1, 1, 1, 1], "TRA_ERR_PARSE"),
+    ("ij,jk->ik:mul:avg", [64, 64, 64], [1, 1, 1, 1], "TRA_ERR_PARSE"),
+    ("ij,jk:mul:sum", [64, 64, 64], [1, 1, 1, 1], "TRA_ERR_PARSE"),
+    ("ii,ik->ik:mul:sum", [64, 64], [1, 1, 1, 1], "TRA_ERR_PARSE"),
+    ("ij,jk->iz:mul:sum", [64, 64, 64], [1, 1, 1, 1], "TRA_ERR_PARSE"),
+    ("ij,jk->ik:mul:none", [64, 64, 64], [1, 1, 1, 1], "TRA_ERR_PARSE"),
+    ("ij,jk->ik:mul:sum:alpha=x", [64, 64, 64], [1, 1, 1, 1], "TRA_ERR_PARSE"),
+    ("ij,jk->ik:mul:sum:foo=1", [64, 64, 64], [1, 1, 1, 1], "TRA_ERR_PARSE"),
+    ("ij,jk->ik:mul:sum", [64, 0, 64], [1, 1, 1, 1], "TRA_ERR_ARG"),
+])
+def test_plan_errors(lib, spec, bounds, d, code):
+    with pytest.raises(lib.TraError) as e:
+        lib.Plan(spec, bounds, d)
+    assert code in str(e.value)
+    assert lib.ein_last_error() != ""
+
+
+def test_repartition_cost_matches_bruteforce(lib):
+    shape = (4, 4, 4, 4)
+    ds = [[4, 1, 4, 1], [1, 4, 1, 4], [2, 2, 2, 2], [1, 1, 1, 1], [4, 4, 1, 1], [2, 1, 1, 4]]
+    for a in ds:
+        for b in ds:
+            assert lib.repartition_cost(shape, a, b) == otra.repartition_cost_bruteforce(shape, a, b)
+    shape = (6, 4, 10)
+    for a, b in [([3, 2, 5], [1, 4, 2]), ([2, 1, 1], [6, 4, 10]), ([1, 2, 5], [3, 1, 1])]:
+        assert lib.repartition_cost(shape, a, b) == otra.repartition_cost_bruteforce(shape, a, b)
+    # the 4-D contraction's output, 64^4 under [4,1,4,1] -> [1,4,1,4]
+    assert lib.repartition_cost((64,) * 4, [4, 1, 4, 1], [1, 4, 1, 4]) == 16777216 - 16 * 16 ** 4
+    with pytest.raises(lib.TraError):
+        lib.repartition_cost((6, 4), [4, 1], [1, 1])
+
+
+def test_execute_argument_errors(lib):
+    p = lib.Plan("ij,jk->ik:add:lse", [64, 64, 64], [1, 1, 1, 1])
+    with pytest.raises(lib.TraError) as e:
+        lib.ein_execute(p.handle, 0x1000, 0x2000, 0x3000, None, 0, 0)
+    assert "TRA_ERR_WORKSPACE" in str(e.value)
+    with pytest.raises(lib.TraError) as e:
+        lib.ein_execute(p.handle, None, 0x2000, 0x3000, None, 0, 0)
+    assert "TRA_ERR_ARG" in str(e.value)
+    q = lib.Plan("ij,jk->ik:mul:sum", [64, 64, 64], [1, 1, 1, 1])
+    with pytest.raises(lib.TraError) as e:
+        lib.ein_execute(q.handle, 0x1000, None, 0x3000, None, 0, 0)
+    assert "TRA_ERR_ARG" in str(e.value)
+    with pytest.raises(lib.TraError) as e:
+        lib.ein_repartition([6, 4], [4, 1], [1, 1], 4, 0x1000, 0x2000, 0)
+    assert "TRA_ERR_DIVISIBILITY" in str(e.value)
+    with pytest.raises(lib.TraError) as e:
+        lib.ein_repartition([6, 4], [1, 1], [2, 1], 3, 0x1000, 0x2000, 0)
+    assert "TRA_ERR_ARG" in str(e.value)
