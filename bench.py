@@ -116,8 +116,13 @@ class Step:
 
 
 def kernel_launches(plan) -> int:
-    return {"semiring_f32": 1, "tc_bf16": 1, "row_reduce": 1, "elementwise": 1, "lse_factored": 3,
-            "literal": 2}[plan.kernel] + (2 if ":sqdiff=expand" in plan.spec else 0)
+    """Kernels one ein_execute of this plan launches."""
+    n = {"semiring_f32": 1, "tc_bf16": 1, "row_reduce": 1, "elementwise": 1, "lse_factored": 3,
+         "literal": 2}[plan.kernel]
+    spec = plan.spec
+    if plan.kernel == "semiring_f32" and ":sqdiff:sum" in spec and "sqdiff=direct" not in spec and "in=bf16" not in spec:
+        n += 2  # row / column norms of the squared-distance expansion
+    return n
 
 
 def device_relation(tra, torch, dense_dev, shape, d):

@@ -150,6 +150,13 @@ int ein_repartition_cost(int rank, const int64_t* shape, const int32_t* src_d, c
  * TRA_ERR_TIMEOUT or TRA_ERR_CUDA. */
 int ein_status(tra_stream_t stream);
 
+/* ein_selftest_wait_timeout -- test hook for the bounded device waits: launches one
+ * thread that waits on an mbarrier nothing arrives on, with the same bounded wait the
+ * tensor-core kernel uses, giving up after timeout_ns.  A following ein_status() on
+ * the same stream must return TRA_ERR_TIMEOUT; the context stays usable.
+ * Errors: TRA_ERR_CUDA (launch failure). */
+int ein_selftest_wait_timeout(uint64_t timeout_ns, tra_stream_t stream);
+
 /* ein_plan_destroy -- release a plan (NULL is ignored). */
 void ein_plan_destroy(tra_plan_t plan);
 

@@ -17,7 +17,8 @@ from ._build import LIB as _LIB_PATH, build as _build_lib
 
 __all__ = [
     "TraError", "build_library", "load", "Plan", "ein_plan", "ein_plan_info", "ein_plan_keys", "ein_execute",
-    "ein_repartition", "ein_repartition_cost", "ein_status", "ein_plan_destroy", "ein_last_error",
+    "ein_repartition", "ein_repartition_cost", "ein_status", "ein_selftest_wait_timeout", "ein_plan_destroy",
+    "ein_last_error",
     "repartition", "repartition_cost", "KERNELS", "ROLES",
 ]
 
@@ -82,6 +83,8 @@ def load():
     lib.ein_repartition.argtypes = [i32, vp, vp, vp, i32, vp, vp, vp]
     lib.ein_repartition_cost.argtypes = [i32, vp, vp, vp, u64p]
     lib.ein_status.argtypes = [vp]
+    lib.ein_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+    lib.ein_selftest_wait_timeout.restype = ctypes.c_int
     lib.ein_plan_destroy.argtypes = [vp]
     lib.ein_plan_destroy.restype = None
     lib.ein_last_error.restype = ctypes.c_char_p
@@ -161,6 +164,10 @@ def ein_repartition_cost(shape, src_d, dst_d) -> int:
 
 def ein_status(stream=None):
     _check(load().ein_status(_stream(stream)))
+
+
+def ein_selftest_wait_timeout(timeout_ns: int, stream=None):
+    _check(load().ein_selftest_wait_timeout(timeout_ns, _stream(stream)))
 
 
 def ein_plan_destroy(plan: int):
@@ -252,6 +259,16 @@ class Plan:
         return [(r[:rx], r[rx:rx + ry], r[rx + ry:]) for r in rows]
 
     def execute(self, x, y, z, workspace=None, stream=None):
+        """Run the plan on device tensors in the relation layout of d.  When the plan needs
+        scratch and none is given, a torch buffer is allocated once and kept with the plan."""
+        if workspace is None and self.info.workspace_bytes:
+            ws = getattr(self, "_workspace", None)
+            if ws is None or ws.device != z.device:
+                import torch
+
+                ws = torch.empty(self.info.workspace_bytes, dtype=torch.uint8, device=z.device)
+                self._workspace = ws
+            workspace = ws
         ws_bytes = 0
         if workspace is not None:
             ws_bytes = workspace.numel() * workspace.element_size()

@@ -12,6 +12,21 @@ int cuda_fail(cudaError_t e, const char* what) {
     return fail(TRA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// A map supports 4-wide vector loads when its innermost label is the operand's
+// innermost memory dimension with a block-local extent divisible by 4: then every
+// 4 consecutive composite indices starting at a multiple of 4 are contiguous and
+// 16-byte (fp32) / 8-byte (bf16) aligned, given an aligned base pointer.
+bool vec4_ok(const RoleMap& m, const void* base, int bf16) {
+    if (m.n == 0 || m.t[0].div != 1 || m.t[0].loc_stride != 1) return false;
+    if (m.t[0].sub % 4 != 0 || m.t[0].ext % 4 != 0) return false;
+    return ((uintptr_t)base % (bf16 ? 8 : 16)) == 0;
+}
+
+void set_load_modes(SemiringParams& sp, int bf16) {
+    sp.x_mode = vec4_ok(sp.xk, sp.x, bf16) ? 1 : (vec4_ok(sp.xm, sp.x, bf16) ? 2 : 0);
+    sp.y_mode = vec4_ok(sp.yn, sp.y, bf16) ? 2 : (vec4_ok(sp.yk, sp.y, bf16) ? 1 : 0);
+}
+
 SemiringParams semiring_params(const Plan& p, const void* x, const void* y, void* z) {
     SemiringParams sp;
     memset(&sp, 0, sizeof(sp));
@@ -40,6 +55,7 @@ SemiringParams semiring_params(const Plan& p, const void* x, const void* y, void
     sp.x_mcontig = affine_stride(sp.xm) == 1;
     sp.y_ncontig = affine_stride(sp.yn) == 1;
     sp.y_kcontig = affine_stride(sp.yk) == 1;
+    set_load_modes(sp, p.in_bf16);
     return sp;
 }
 
@@ -110,6 +126,7 @@ int execute_literal(const Plan& p, const void* x, const void* y, void* z, void* 
     sp.out_bf16 = 0;
     sp.x_kcontig = affine_stride(sp.xk) == 1;
     sp.y_kcontig = affine_stride(sp.yk) == 1;
+    set_load_modes(sp, p.in_bf16);
     cudaError_t e = launch_semiring(sp, s);
     if (e != cudaSuccess) return cuda_fail(e, "literal join");
     CombineParams cp;
@@ -147,6 +164,7 @@ int execute_plan(const Plan& p, const void* x, const void* y, void* z, void* ws,
                 sp.op = kMul;
                 sp.xnorm = xn;
                 sp.ynorm = yn;
+                set_load_modes(sp, 0);
             }
             e = launch_semiring(sp, s);
             break;
@@ -175,6 +193,7 @@ int execute_plan(const Plan& p, const void* x, const void* y, void* z, void* ws,
             sp.y_raw = y;
             sp.x = ex;
             sp.y = ey;
+            set_load_modes(sp, 0);
             sp.rowmax = rmax;
             sp.colmax = cmax;
             sp.op = kMul;
@@ -424,6 +443,12 @@ int ein_status(tra_stream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e, "status read");
     if (v) return fail(v, "a bounded device wait gave up (status %d)", v);
     return TRA_OK;
+}
+
+int ein_selftest_wait_timeout(uint64_t timeout_ns, tra_stream_t stream) {
+    clear_error();
+    cudaError_t e = launch_wait_timeout_probe(timeout_ns, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TRA_OK : cuda_fail(e, "wait probe launch");
 }
 
 void ein_plan_destroy(tra_plan_t plan) { delete reinterpret_cast<Plan*>(plan); }

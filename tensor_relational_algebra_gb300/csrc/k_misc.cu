@@ -15,8 +15,6 @@
 
 namespace tra {
 
-__device__ int g_status;  // TRA_ERR_* set by a bounded wait that gave up; 0 otherwise
-
 namespace {
 
 __device__ __forceinline__ float ld_f(const void* p, int64_t off, int bf16) {
@@ -241,17 +239,6 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
     if (total == 0) return cudaSuccess;
     combine_kernel<<<grid_for(total, 256), 256, 0, s>>>(p);
     return cudaGetLastError();
-}
-
-cudaError_t read_and_clear_status(int* value, cudaStream_t s) {
-    cudaError_t e = cudaMemcpyFromSymbolAsync(value, g_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s);
-    if (e != cudaSuccess) return e;
-    e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return e;
-    const int zero = 0;
-    e = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return e;
-    return cudaStreamSynchronize(s);
 }
 
 }  // namespace tra

@@ -3,13 +3,21 @@
 // associative aggregation -- sum, max, min, logsumexp -- over any binary scalar
 // function -- multiply, add, (x-y)^2).
 //
-// Each CTA owns one 128 x 128 output tile of one batch index.  A tile never
-// straddles two output keys in the sense that matters here: every element is
-// addressed through the relation layout (RoleMap), so the tile walks the whole
-// contracted range -- all contracted keys, then the local indices inside each
-// -- and the aggregation across join tuples of one output key (section 2.2,
+// Each CTA owns one 128 x 128 output tile of one batch index and walks the whole
+// contracted range -- every contracted key, then the local indices inside it --
+// so the aggregation across the join tuples of one output key (section 2.2,
 // aggregation) happens in the same registers as the aggregation inside one
-// sub-tensor.
+// sub-tensor.  Every element is addressed through the relation layout
+// (RoleMap), so one kernel serves every binary EinSum and every partition vector.
+//
+// Per thread: an 8 x 8 register tile; K is staged through shared memory 16 at a
+// time (double-buffered, prefetched into registers during the math).  Operands
+// are loaded as float4 / 4 x bf16 when the layout makes 4 consecutive indices
+// contiguous, else gathered element by element.  The K tail is padded with
+// values whose join is the aggregation's identity, so the inner loop never
+// branches.  For max-plus / min-plus the inner step works on pairs of
+// consecutive k: one packed add (add.rn.f32x2) and one 3-input max/min per two
+// join tuples.
 #include <cuda_bf16.h>
 
 #include <cfloat>
@@ -21,16 +29,32 @@ namespace tra {
 namespace {
 
 constexpr int BM = 128, BN = 128, BK = 16, NT = 256;
+enum { kEpiPlain = 0, kEpiLse = 1, kEpiSqExpand = 2 };
+enum { kLoadGather = 0, kLoadVecK = 1, kLoadVecMN = 2 };
 
 template <typename T>
-__device__ __forceinline__ float ld_in(const void* p, int64_t off);
+__device__ __forceinline__ float ld1(const void* p, int64_t off);
 template <>
-__device__ __forceinline__ float ld_in<float>(const void* p, int64_t off) {
+__device__ __forceinline__ float ld1<float>(const void* p, int64_t off) {
     return __ldg(reinterpret_cast<const float*>(p) + off);
 }
 template <>
-__device__ __forceinline__ float ld_in<__nv_bfloat16>(const void* p, int64_t off) {
+__device__ __forceinline__ float ld1<__nv_bfloat16>(const void* p, int64_t off) {
     return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[off]);
+}
+
+// four consecutive elements starting at a multiple of 4 (16-byte / 8-byte aligned)
+template <typename T>
+__device__ __forceinline__ float4 ld4(const void* p, int64_t off);
+template <>
+__device__ __forceinline__ float4 ld4<float>(const void* p, int64_t off) {
+    return __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p) + off));
+}
+template <>
+__device__ __forceinline__ float4 ld4<__nv_bfloat16>(const void* p, int64_t off) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p) + off));
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xffff0000u));
 }
 
 __device__ __forceinline__ void st_out(void* p, int64_t off, float v, int bf16) {
@@ -51,34 +75,77 @@ __device__ __forceinline__ float apply_op(int op, float x, float y) {
     }
 }
 
+// packed pair helpers
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float lo_of(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi_of(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float min3(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // ---------------------------------------------------------------- semiring functors
+// pad_x / pad_y: operand values for k beyond K whose join is the aggregation's identity
 struct MulSum {
-    static __host__ __device__ constexpr float init() { return 0.f; }
-    static __device__ __forceinline__ float step(float acc, float x, float y) { return fmaf(x, y, acc); }
+    static constexpr bool kPacked = false;
+    static __device__ __forceinline__ float init() { return 0.f; }
+    static __device__ __forceinline__ float pad_x() { return 0.f; }
+    static __device__ __forceinline__ float pad_y() { return 0.f; }
+    static __device__ __forceinline__ void step(float& acc, float x, float y) { acc = fmaf(x, y, acc); }
+    static __device__ __forceinline__ void step2(float&, uint64_t, uint64_t) {}
 };
 struct SqdiffSum {
-    static __host__ __device__ constexpr float init() { return 0.f; }
-    static __device__ __forceinline__ float step(float acc, float x, float y) {
-        float t = x - y;
-        return fmaf(t, t, acc);
+    static constexpr bool kPacked = false;
+    static __device__ __forceinline__ float init() { return 0.f; }
+    static __device__ __forceinline__ float pad_x() { return 0.f; }
+    static __device__ __forceinline__ float pad_y() { return 0.f; }
+    static __device__ __forceinline__ void step(float& acc, float x, float y) {
+        const float t = x - y;
+        acc = fmaf(t, t, acc);
     }
+    static __device__ __forceinline__ void step2(float&, uint64_t, uint64_t) {}
 };
 struct AddMax {
-    static __host__ __device__ constexpr float init() { return -INFINITY; }
-    static __device__ __forceinline__ float step(float acc, float x, float y) { return fmaxf(acc, x + y); }
+    static constexpr bool kPacked = true;
+    static __device__ __forceinline__ float init() { return -INFINITY; }
+    static __device__ __forceinline__ float pad_x() { return -INFINITY; }
+    static __device__ __forceinline__ float pad_y() { return 0.f; }
+    static __device__ __forceinline__ void step(float& acc, float x, float y) { acc = fmaxf(acc, x + y); }
+    static __device__ __forceinline__ void step2(float& acc, uint64_t x2, uint64_t y2) {
+        const uint64_t t = add2(x2, y2);
+        acc = max3(acc, lo_of(t), hi_of(t));
+    }
 };
 struct AddMin {
-    static __host__ __device__ constexpr float init() { return INFINITY; }
-    static __device__ __forceinline__ float step(float acc, float x, float y) { return fminf(acc, x + y); }
+    static constexpr bool kPacked = true;
+    static __device__ __forceinline__ float init() { return INFINITY; }
+    static __device__ __forceinline__ float pad_x() { return INFINITY; }
+    static __device__ __forceinline__ float pad_y() { return 0.f; }
+    static __device__ __forceinline__ void step(float& acc, float x, float y) { acc = fminf(acc, x + y); }
+    static __device__ __forceinline__ void step2(float& acc, uint64_t x2, uint64_t y2) {
+        const uint64_t t = add2(x2, y2);
+        acc = min3(acc, lo_of(t), hi_of(t));
+    }
 };
 
 // Online logsumexp of one output over the contracted range, read straight from the
-// operands (used by the factored form when its sum underflows, and by the simple kernel).
+// operands (the factored form's fallback when its sum underflows; the simple kernel).
 template <typename TIn>
-__device__ float direct_lse(const SemiringParams& p, const void* x, const void* y, int64_t xo, int64_t yo) {
+__device__ __noinline__ float direct_lse(const SemiringParams& p, const void* x, const void* y, int64_t xo,
+                                         int64_t yo) {
     float m = -INFINITY, s = 0.f;
     for (uint32_t k = 0; k < p.K; ++k) {
-        float v = ld_in<TIn>(x, xo + role_offset(p.xk, k)) + ld_in<TIn>(y, yo + role_offset(p.yk, k));
+        float v = ld1<TIn>(x, xo + role_offset(p.xk, k)) + ld1<TIn>(y, yo + role_offset(p.yk, k));
         if (v > m) {
             s = s * expf(m - v) + 1.f;
             m = v;
@@ -89,12 +156,26 @@ __device__ float direct_lse(const SemiringParams& p, const void* x, const void* 
     return m == -INFINITY ? m : m + logf(s);
 }
 
+__device__ __noinline__ float lse_fallback(const SemiringParams& p, uint32_t b, uint32_t m, uint32_t n) {
+    const int64_t xo = role_offset(p.xb, b) + role_offset(p.xm, m);
+    const int64_t yo = role_offset(p.yb, b) + role_offset(p.yn, n);
+    return p.in_bf16 ? direct_lse<__nv_bfloat16>(p, p.x_raw, p.y_raw, xo, yo)
+                     : direct_lse<float>(p, p.x_raw, p.y_raw, xo, yo);
+}
+
+// shared-memory index of (k, row) in the unpacked [k][row] or packed [k/2][row][k%2] layout
+template <bool P>
+__device__ __forceinline__ int sidx(int k, int r) {
+    return P ? (((k >> 1) * BM + r) << 1) + (k & 1) : k * BM + r;
+}
+
 // ---------------------------------------------------------------- tiled kernel
-template <class S, typename TIn>
+template <class S, typename TIn, int EPI>
 __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ SemiringParams p) {
-    __shared__ __align__(16) float Xs[2][BK][BM];
-    __shared__ __align__(16) float Ys[2][BK][BN];
-    __shared__ int64_t rowX[BM], colY[BN], rowZ[BM], colZ[BN];
+    constexpr bool P = S::kPacked;
+    __shared__ __align__(16) float Xs[2][BK * BM];
+    __shared__ __align__(16) float Ys[2][BK * BN];
+    __shared__ int64_t rowX[BM], colY[BN];
     __shared__ int64_t kX[2][BK], kY[2][BK];
 
     const int tid = threadIdx.x;
@@ -106,61 +187,140 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
     const uint32_t b = t / tiles_m;
     const uint32_t m0 = tm * BM, n0 = tn * BN;
 
-    const int64_t xb = role_offset(p.xb, b), yb = role_offset(p.yb, b), zb = role_offset(p.zb, b);
     if (tid < BM) {
-        uint32_t m = min(m0 + tid, p.M - 1);
-        rowX[tid] = xb + role_offset(p.xm, m);
-        rowZ[tid] = zb + role_offset(p.zm, m);
+        rowX[tid] = role_offset(p.xb, b) + role_offset(p.xm, min(m0 + tid, p.M - 1));
     } else {
-        uint32_t n = min(n0 + (tid - BM), p.N - 1);
-        colY[tid - BM] = yb + role_offset(p.yn, n);
-        colZ[tid - BM] = role_offset(p.zn, n);
+        colY[tid - BM] = role_offset(p.yb, b) + role_offset(p.yn, min(n0 + (tid - BM), p.N - 1));
     }
-    const uint32_t nkt = (p.K + BK - 1) / BK;
-    if (tid < BK) {
-        uint32_t k = min((uint32_t)tid, p.K - 1);
-        kX[0][tid] = role_offset(p.xk, k);
-    } else if (tid < 2 * BK) {
-        uint32_t k = min((uint32_t)(tid - BK), p.K - 1);
-        kY[0][tid - BK] = role_offset(p.yk, k);
-    }
+    if (tid < BK) kX[0][tid] = role_offset(p.xk, min((uint32_t)tid, p.K - 1));
+    else if (tid < 2 * BK) kY[0][tid - BK] = role_offset(p.yk, min((uint32_t)(tid - BK), p.K - 1));
     __syncthreads();
 
-    // global -> register staging of one K-tile
+    const int xmode = p.x_mode, ymode = p.y_mode;
     float rx[8], ry[8];
-    const bool xk_map = p.x_kcontig;
-    const bool yk_map = p.y_kcontig && !p.y_ncontig;
-    auto load_tile = [&](int buf, uint32_t k0) {
-        const uint32_t kv = min((uint32_t)BK, p.K - k0);
+
+    // ---- global -> registers for the K-tile starting at k0 (offsets in kX/kY[buf])
+    auto load = [&](int buf, uint32_t k0) {
+        const int kv = (int)min((uint32_t)BK, p.K - k0);
+        const float px = S::pad_x(), py = S::pad_y();
+        if (xmode == kLoadVecK) {
+            const int m = tid & (BM - 1);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            int m, k;
-            if (xk_map) { k = tid % BK; m = tid / BK + 16 * i; }
-            else { m = tid % BM; k = tid / BM + 2 * i; }
-            rx[i] = (uint32_t)k < kv ? ld_in<TIn>(p.x, rowX[m] + kX[buf][k]) : 0.f;
+            for (int i = 0; i < 2; ++i) {
+                const int k = ((tid >> 7) + 2 * i) * 4;
+                float4 v = k < kv ? ld4<TIn>(p.x, rowX[m] + kX[buf][k]) : make_float4(px, px, px, px);
+                rx[4 * i] = v.x, rx[4 * i + 1] = v.y, rx[4 * i + 2] = v.z, rx[4 * i + 3] = v.w;
+            }
+        } else if (xmode == kLoadVecMN) {
+            const int m = (tid & 31) * 4;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int k = (tid >> 5) + 8 * i;
+                float4 v = k < kv ? ld4<TIn>(p.x, rowX[m] + kX[buf][k]) : make_float4(px, px, px, px);
+                rx[4 * i] = v.x, rx[4 * i + 1] = v.y, rx[4 * i + 2] = v.z, rx[4 * i + 3] = v.w;
+            }
+        } else {
+            const int m = tid & (BM - 1);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k = (tid >> 7) + 2 * i;
+                rx[i] = k < kv ? ld1<TIn>(p.x, rowX[m] + kX[buf][k]) : px;
+            }
         }
+        if (ymode == kLoadVecMN) {
+            const int n = (tid & 31) * 4;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            int n, k;
-            if (yk_map) { k = tid % BK; n = tid / BK + 16 * i; }
-            else { n = tid % BN; k = tid / BN + 2 * i; }
-            ry[i] = (uint32_t)k < kv ? ld_in<TIn>(p.y, colY[n] + kY[buf][k]) : 0.f;
+            for (int i = 0; i < 2; ++i) {
+                // packed layout: rows 2*kp and 2*kp+1; unpacked: rows kk and kk+8
+                const int k = P ? 2 * (tid >> 5) + i : (tid >> 5) + 8 * i;
+                float4 v = k < kv ? ld4<TIn>(p.y, colY[n] + kY[buf][k]) : make_float4(py, py, py, py);
+                ry[4 * i] = v.x, ry[4 * i + 1] = v.y, ry[4 * i + 2] = v.z, ry[4 * i + 3] = v.w;
+            }
+        } else if (ymode == kLoadVecK) {
+            const int n = tid & (BN - 1);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int k = ((tid >> 7) + 2 * i) * 4;
+                float4 v = k < kv ? ld4<TIn>(p.y, colY[n] + kY[buf][k]) : make_float4(py, py, py, py);
+                ry[4 * i] = v.x, ry[4 * i + 1] = v.y, ry[4 * i + 2] = v.z, ry[4 * i + 3] = v.w;
+            }
+        } else {
+            const int n = tid & (BN - 1);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int k = (tid >> 7) + 2 * i;
+                ry[i] = k < kv ? ld1<TIn>(p.y, colY[n] + kY[buf][k]) : py;
+            }
         }
     };
-    auto store_tile = [&](int buf) {
+
+    // ---- registers -> shared memory
+    auto store = [&](int buf) {
+        float* xs = Xs[buf];
+        float* ys = Ys[buf];
+        if (xmode == kLoadVecK) {
+            const int m = tid & (BM - 1);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            int m, k;
-            if (xk_map) { k = tid % BK; m = tid / BK + 16 * i; }
-            else { m = tid % BM; k = tid / BM + 2 * i; }
-            Xs[buf][k][m] = rx[i];
+            for (int i = 0; i < 2; ++i) {
+                const int k = ((tid >> 7) + 2 * i) * 4;
+                if (P) {
+                    *reinterpret_cast<float2*>(&xs[sidx<P>(k, m)]) = make_float2(rx[4 * i], rx[4 * i + 1]);
+                    *reinterpret_cast<float2*>(&xs[sidx<P>(k + 2, m)]) = make_float2(rx[4 * i + 2], rx[4 * i + 3]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) xs[sidx<P>(k + c, m)] = rx[4 * i + c];
+                }
+            }
+        } else if (xmode == kLoadVecMN) {
+            const int m = (tid & 31) * 4;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int k = (tid >> 5) + 8 * i;
+                if (P) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) xs[sidx<P>(k, m + c)] = rx[4 * i + c];
+                } else {
+                    *reinterpret_cast<float4*>(&xs[sidx<P>(k, m)]) =
+                        make_float4(rx[4 * i], rx[4 * i + 1], rx[4 * i + 2], rx[4 * i + 3]);
+                }
+            }
+        } else {
+            const int m = tid & (BM - 1);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) xs[sidx<P>((tid >> 7) + 2 * i, m)] = rx[i];
         }
+        if (ymode == kLoadVecMN) {
+            const int n = (tid & 31) * 4;
+            if (P) {
+                const int kp = tid >> 5;  // rows 2kp (ry[0..3]) and 2kp+1 (ry[4..7])
+                float4* dst = reinterpret_cast<float4*>(&ys[((kp * BN + n) << 1)]);
+                dst[0] = make_float4(ry[0], ry[4], ry[1], ry[5]);
+                dst[1] = make_float4(ry[2], ry[6], ry[3], ry[7]);
+            } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            int n, k;
-            if (yk_map) { k = tid % BK; n = tid / BK + 16 * i; }
-            else { n = tid % BN; k = tid / BN + 2 * i; }
-            Ys[buf][k][n] = ry[i];
+                for (int i = 0; i < 2; ++i) {
+                    const int k = (tid >> 5) + 8 * i;
+                    *reinterpret_cast<float4*>(&ys[sidx<P>(k, n)]) =
+                        make_float4(ry[4 * i], ry[4 * i + 1], ry[4 * i + 2], ry[4 * i + 3]);
+                }
+            }
+        } else if (ymode == kLoadVecK) {
+            const int n = tid & (BN - 1);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int k = ((tid >> 7) + 2 * i) * 4;
+                if (P) {
+                    *reinterpret_cast<float2*>(&ys[sidx<P>(k, n)]) = make_float2(ry[4 * i], ry[4 * i + 1]);
+                    *reinterpret_cast<float2*>(&ys[sidx<P>(k + 2, n)]) = make_float2(ry[4 * i + 2], ry[4 * i + 3]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) ys[sidx<P>(k + c, n)] = ry[4 * i + c];
+                }
+            }
+        } else {
+            const int n = tid & (BN - 1);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ys[sidx<P>((tid >> 7) + 2 * i, n)] = ry[i];
         }
     };
 
@@ -170,90 +330,87 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = S::init();
 
-    const int ty = tid / 16, tx = tid % 16;
-    load_tile(0, 0);
-    store_tile(0);
+    const int ty = tid >> 4, tx = tid & 15;
+    load(0, 0);
+    store(0);
     __syncthreads();
 
+    const uint32_t nkt = (p.K + BK - 1) / BK;
     for (uint32_t kt = 0; kt < nkt; ++kt) {
         const int buf = kt & 1;
-        const uint32_t k0 = kt * BK;
         const bool has_next = kt + 1 < nkt;
         if (has_next) {
-            // offsets of the next K-tile, then its loads (overlap with the math below)
-            const uint32_t k1 = k0 + BK;
-            if (tid < BK) {
-                uint32_t k = min(k1 + tid, p.K - 1);
-                kX[buf ^ 1][tid] = role_offset(p.xk, k);
-            } else if (tid < 2 * BK) {
-                uint32_t k = min(k1 + tid - BK, p.K - 1);
-                kY[buf ^ 1][tid - BK] = role_offset(p.yk, k);
-            }
+            const uint32_t k1 = (kt + 1) * BK;
+            if (tid < BK) kX[buf ^ 1][tid] = role_offset(p.xk, min(k1 + tid, p.K - 1));
+            else if (tid < 2 * BK) kY[buf ^ 1][tid - BK] = role_offset(p.yk, min(k1 + tid - BK, p.K - 1));
         }
         __syncthreads();
-        if (has_next) load_tile(buf ^ 1, k0 + BK);
-        const uint32_t kv = min((uint32_t)BK, p.K - k0);
-        if (kv == BK) {
+        if (has_next) load(buf ^ 1, (kt + 1) * BK);
+        const float* xs = Xs[buf];
+        const float* ys = Ys[buf];
+        if constexpr (P) {
 #pragma unroll
-            for (int k = 0; k < BK; ++k) {
-                float4 a0 = *reinterpret_cast<const float4*>(&Xs[buf][k][ty * 4]);
-                float4 a1 = *reinterpret_cast<const float4*>(&Xs[buf][k][64 + ty * 4]);
-                float4 b0 = *reinterpret_cast<const float4*>(&Ys[buf][k][tx * 4]);
-                float4 b1 = *reinterpret_cast<const float4*>(&Ys[buf][k][64 + tx * 4]);
-                float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            for (int kp = 0; kp < BK / 2; ++kp) {
+                // x pairs for rows ty*4..+3 and 64+ty*4..+3; y pairs for columns g*32 + tx*2 + {0,1}
+                uint64_t xa[8], yb[8];
+                const ulonglong2* xr0 = reinterpret_cast<const ulonglong2*>(&xs[((kp * BM + ty * 4) << 1)]);
+                const ulonglong2* xr1 = reinterpret_cast<const ulonglong2*>(&xs[((kp * BM + 64 + ty * 4) << 1)]);
+                const ulonglong2 q0 = xr0[0], q1 = xr0[1], q2 = xr1[0], q3 = xr1[1];
+                xa[0] = q0.x, xa[1] = q0.y, xa[2] = q1.x, xa[3] = q1.y;
+                xa[4] = q2.x, xa[5] = q2.y, xa[6] = q3.x, xa[7] = q3.y;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const ulonglong2 w = *reinterpret_cast<const ulonglong2*>(&ys[((kp * BN + g * 32 + tx * 2) << 1)]);
+                    yb[2 * g] = w.x, yb[2 * g + 1] = w.y;
+                }
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[i][j] = S::step(acc[i][j], a[i], bb[j]);
+                    for (int j = 0; j < 8; ++j) S::step2(acc[i][j], xa[i], yb[j]);
             }
         } else {
-            for (uint32_t k = 0; k < kv; ++k) {
-                float4 a0 = *reinterpret_cast<const float4*>(&Xs[buf][k][ty * 4]);
-                float4 a1 = *reinterpret_cast<const float4*>(&Xs[buf][k][64 + ty * 4]);
-                float4 b0 = *reinterpret_cast<const float4*>(&Ys[buf][k][tx * 4]);
-                float4 b1 = *reinterpret_cast<const float4*>(&Ys[buf][k][64 + tx * 4]);
-                float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int k = 0; k < BK; ++k) {
+                const float4 a0 = *reinterpret_cast<const float4*>(&xs[k * BM + ty * 4]);
+                const float4 a1 = *reinterpret_cast<const float4*>(&xs[k * BM + 64 + ty * 4]);
+                const float4 b0 = *reinterpret_cast<const float4*>(&ys[k * BN + tx * 4]);
+                const float4 b1 = *reinterpret_cast<const float4*>(&ys[k * BN + 64 + tx * 4]);
+                const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[i][j] = S::step(acc[i][j], a[i], bb[j]);
+                    for (int j = 0; j < 8; ++j) S::step(acc[i][j], a[i], bb[j]);
             }
         }
-        if (has_next) store_tile(buf ^ 1);
+        if (has_next) store(buf ^ 1);
         __syncthreads();
     }
 
-    // epilogue
+    // ---- epilogue: output offsets through Z's relation layout
+    const int64_t zb = role_offset(p.zb, b);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int mi = (i < 4) ? ty * 4 + i : 64 + ty * 4 + (i - 4);
         const uint32_t m = m0 + mi;
         if (m >= p.M) continue;
-        const float rmax = p.rowmax ? p.rowmax[(uint64_t)b * p.M + m] : 0.f;
-        const float xn = p.xnorm ? p.xnorm[(uint64_t)b * p.M + m] : 0.f;
+        const int64_t zrow = zb + role_offset(p.zm, m);
+        float rterm = 0.f;
+        if (EPI == kEpiLse) rterm = p.rowmax[(uint64_t)b * p.M + m];
+        if (EPI == kEpiSqExpand) rterm = p.xnorm[(uint64_t)b * p.M + m];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const int nj = (j < 4) ? tx * 4 + j : 64 + tx * 4 + (j - 4);
+            const int nj = P ? (j >> 1) * 32 + tx * 2 + (j & 1) : ((j < 4) ? tx * 4 + j : 64 + tx * 4 + (j - 4));
             const uint32_t n = n0 + nj;
             if (n >= p.N) continue;
             float v = acc[i][j];
-            if (p.rowmax) {
-                const float cmax = p.colmax[(uint64_t)b * p.N + n];
-                if (v > 1e-30f) {
-                    v = rmax + cmax + logf(v);
-                } else {
-                    // every shifted term underflowed: evaluate this output directly
-                    const int64_t xo = role_offset(p.xb, b) + role_offset(p.xm, m);
-                    const int64_t yo = role_offset(p.yb, b) + role_offset(p.yn, n);
-                    v = p.in_bf16 ? direct_lse<__nv_bfloat16>(p, p.x_raw, p.y_raw, xo, yo)
-                                  : direct_lse<float>(p, p.x_raw, p.y_raw, xo, yo);
-                }
-            } else if (p.xnorm) {
-                v = fmaxf(xn + p.ynorm[(uint64_t)b * p.N + n] - 2.f * v, 0.f);
+            if (EPI == kEpiLse) {
+                if (v > 1e-30f) v = rterm + p.colmax[(uint64_t)b * p.N + n] + logf(v);
+                else v = lse_fallback(p, b, m, n);  // every exp-shifted product underflowed
+            } else if (EPI == kEpiSqExpand) {
+                v = fmaxf(rterm + p.ynorm[(uint64_t)b * p.N + n] - 2.f * v, 0.f);
             }
-            st_out(p.z, rowZ[mi] + colZ[nj], p.alpha * v, p.out_bf16);
+            st_out(p.z, zrow + role_offset(p.zn, n), p.alpha * v, p.out_bf16);
         }
     }
 }
@@ -274,8 +431,8 @@ __global__ void semiring_simple(const __grid_constant__ SemiringParams p) {
         if (p.agg == kLse) {
             float mx = -INFINITY, s = 0.f;
             for (uint32_t k = 0; k < p.K; ++k) {
-                float v = apply_op(p.op, ld_in<TIn>(p.x, xo + role_offset(p.xk, k)),
-                                   ld_in<TIn>(p.y, yo + role_offset(p.yk, k)));
+                float v = apply_op(p.op, ld1<TIn>(p.x, xo + role_offset(p.xk, k)),
+                                   ld1<TIn>(p.y, yo + role_offset(p.yk, k)));
                 if (v > mx) {
                     s = s * expf(mx - v) + 1.f;
                     mx = v;
@@ -287,8 +444,8 @@ __global__ void semiring_simple(const __grid_constant__ SemiringParams p) {
         } else {
             acc = p.agg == kMax ? -INFINITY : (p.agg == kMin ? INFINITY : 0.f);
             for (uint32_t k = 0; k < p.K; ++k) {
-                float v = apply_op(p.op, ld_in<TIn>(p.x, xo + role_offset(p.xk, k)),
-                                   ld_in<TIn>(p.y, yo + role_offset(p.yk, k)));
+                float v = apply_op(p.op, ld1<TIn>(p.x, xo + role_offset(p.xk, k)),
+                                   ld1<TIn>(p.y, yo + role_offset(p.yk, k)));
                 if (p.agg == kMax) acc = fmaxf(acc, v);
                 else if (p.agg == kMin) acc = fminf(acc, v);
                 else acc += v;
@@ -305,14 +462,15 @@ template <typename TIn>
 __global__ void lse_prep_kernel(const __grid_constant__ LsePrepParams p, int row_per_thread) {
     if (!row_per_thread) {
         // one warp per row (contracted index contiguous in memory)
-        const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
+        const uint64_t warp = (blockIdx.x * (uint64_t)blockDim.x + threadIdx.x) / 32;
+        const uint32_t lane = threadIdx.x % 32;
         const uint64_t rows = (uint64_t)p.nb * p.R;
         if (warp >= rows) return;
         const uint32_t r = warp % p.R, b = warp / p.R;
         const int64_t base = role_offset(p.b, b) + role_offset(p.r, r);
         float m = p.mode == 0 ? -INFINITY : 0.f;
         for (uint32_t k = lane; k < p.K; k += 32) {
-            float v = ld_in<TIn>(p.src, base + role_offset(p.k, k));
+            float v = ld1<TIn>(p.src, base + role_offset(p.k, k));
             m = p.mode == 0 ? fmaxf(m, v) : fmaf(v, v, m);
         }
         for (int o = 16; o; o >>= 1) {
@@ -323,7 +481,7 @@ __global__ void lse_prep_kernel(const __grid_constant__ LsePrepParams p, int row
         if (p.mode == 0)
             for (uint32_t k = lane; k < p.K; k += 32) {
                 int64_t off = base + role_offset(p.k, k);
-                p.dst[off] = expf(ld_in<TIn>(p.src, off) - m);
+                p.dst[off] = expf(ld1<TIn>(p.src, off) - m);
             }
     } else {
         // one thread per row (rows contiguous in memory): coalesced across the warp
@@ -333,16 +491,22 @@ __global__ void lse_prep_kernel(const __grid_constant__ LsePrepParams p, int row
         const int64_t base = role_offset(p.b, b) + role_offset(p.r, r);
         float m = p.mode == 0 ? -INFINITY : 0.f;
         for (uint32_t k = 0; k < p.K; ++k) {
-            float v = ld_in<TIn>(p.src, base + role_offset(p.k, k));
+            float v = ld1<TIn>(p.src, base + role_offset(p.k, k));
             m = p.mode == 0 ? fmaxf(m, v) : fmaf(v, v, m);
         }
         p.rmax[row] = m;
         if (p.mode == 0)
             for (uint32_t k = 0; k < p.K; ++k) {
                 int64_t off = base + role_offset(p.k, k);
-                p.dst[off] = expf(ld_in<TIn>(p.src, off) - m);
+                p.dst[off] = expf(ld1<TIn>(p.src, off) - m);
             }
     }
+}
+
+template <class S, typename TIn, int EPI>
+cudaError_t launch_tiled(const SemiringParams& p, unsigned grid, cudaStream_t s) {
+    semiring_tiled<S, TIn, EPI><<<grid, NT, 0, s>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -350,36 +514,28 @@ __global__ void lse_prep_kernel(const __grid_constant__ LsePrepParams p, int row
 cudaError_t launch_semiring(const SemiringParams& p, cudaStream_t s) {
     if (p.nb == 0 || p.M == 0 || p.N == 0) return cudaSuccess;
     if (p.K == 0) return cudaErrorInvalidValue;
-    const uint64_t grid = (uint64_t)p.nb * ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
-    if (grid > 0x7fffffffull) return cudaErrorInvalidValue;
+    const uint64_t grid64 = (uint64_t)p.nb * ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
+    if (grid64 > 0x7fffffffull) return cudaErrorInvalidValue;
+    const unsigned grid = (unsigned)grid64;
     const bool bf = p.in_bf16;
-    if (p.rowmax || p.xnorm) {
-        // factored logsumexp / squared-distance expansion: the operands are fp32 here
-        // (exp-shifted scratch, or the fp32 inputs); in_bf16 describes x_raw / y_raw
-        semiring_tiled<MulSum, float><<<(unsigned)grid, NT, 0, s>>>(p);
-        return cudaGetLastError();
-    }
+    if (p.rowmax) return launch_tiled<MulSum, float, kEpiLse>(p, grid, s);       // fp32 exp-shifted scratch
+    if (p.xnorm) return launch_tiled<MulSum, float, kEpiSqExpand>(p, grid, s);   // fp32 inputs
     switch (p.op * 8 + p.agg) {
         case kMul * 8 + kSum:
-            if (bf) semiring_tiled<MulSum, __nv_bfloat16><<<(unsigned)grid, NT, 0, s>>>(p);
-            else semiring_tiled<MulSum, float><<<(unsigned)grid, NT, 0, s>>>(p);
-            break;
+            return bf ? launch_tiled<MulSum, __nv_bfloat16, kEpiPlain>(p, grid, s)
+                      : launch_tiled<MulSum, float, kEpiPlain>(p, grid, s);
         case kSqdiff * 8 + kSum:
-            if (bf) semiring_tiled<SqdiffSum, __nv_bfloat16><<<(unsigned)grid, NT, 0, s>>>(p);
-            else semiring_tiled<SqdiffSum, float><<<(unsigned)grid, NT, 0, s>>>(p);
-            break;
+            return bf ? launch_tiled<SqdiffSum, __nv_bfloat16, kEpiPlain>(p, grid, s)
+                      : launch_tiled<SqdiffSum, float, kEpiPlain>(p, grid, s);
         case kAdd * 8 + kMax:
-            if (bf) semiring_tiled<AddMax, __nv_bfloat16><<<(unsigned)grid, NT, 0, s>>>(p);
-            else semiring_tiled<AddMax, float><<<(unsigned)grid, NT, 0, s>>>(p);
-            break;
+            return bf ? launch_tiled<AddMax, __nv_bfloat16, kEpiPlain>(p, grid, s)
+                      : launch_tiled<AddMax, float, kEpiPlain>(p, grid, s);
         case kAdd * 8 + kMin:
-            if (bf) semiring_tiled<AddMin, __nv_bfloat16><<<(unsigned)grid, NT, 0, s>>>(p);
-            else semiring_tiled<AddMin, float><<<(unsigned)grid, NT, 0, s>>>(p);
-            break;
+            return bf ? launch_tiled<AddMin, __nv_bfloat16, kEpiPlain>(p, grid, s)
+                      : launch_tiled<AddMin, float, kEpiPlain>(p, grid, s);
         default:
             return launch_semiring_simple(p, s);
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_semiring_simple(const SemiringParams& p, cudaStream_t s) {

@@ -1,14 +1,675 @@
-// Tensor-core (tcgen05 / TMEM / TMA) join + aggregate for BF16 sum-of-products.
+// BF16 sum-of-products join + aggregate on the 5th-generation tensor cores
+// (tcgen05.mma with the accumulator in tensor memory, operands staged by TMA).
+//
+// "EinDecomp ... tensor relational algebra", section 2.2: under a partition
+// vector every join tuple multiplies one X sub-tensor with one key-matched Y
+// sub-tensor, and the aggregation sums the tuples that share an output key.
+// Here each CTA tile of the output lies inside one output key; its K loop walks
+// every contracted key (one more run of K-steps at another block coordinate),
+// so the aggregation across join tuples is the TMEM accumulation itself.
+//
+// Relations are addressed through rank-5 TMA tensor maps over the blocked
+// layout: the dimensions are the block-local and the key parts of each label
+// (unit dimensions dropped), and a tile coordinate along a dimension is
+// (composite index / div) % mod.  The planner accepts a shape only when every
+// tile is one TMA box, which keeps every load inside one sub-tensor.
+//
+// Kernel: persistent, one CTA per SM, 6 warps: warp 0 issues TMA loads, warp 1
+// owns tensor memory and issues tcgen05.mma (M = 128, N = BLOCK_N <= 256,
+// K = 16 per instruction, fp32 accumulate), warps 2-5 drain the double-buffered
+// accumulator (tcgen05.ld) into global memory while the next tile is computed.
+// Every mbarrier wait is bounded; a wait that gives up sets the device status
+// word (TRA_ERR_TIMEOUT) and makes the whole CTA leave after its copies and
+// MMAs in flight have landed.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
 #include "plan.h"
 
 namespace tra {
 
-struct TcPlan {};
+__device__ int g_status;  // TRA_ERR_* set by a bounded wait that gave up; 0 otherwise
 
-bool tc_plan(Plan*) { return false; }
+namespace {
+
+constexpr int kBlockM = 128;
+constexpr int kBlockK = 64;  // one 128-byte swizzle row of bf16
+constexpr int kThreads = 192;
+constexpr uint32_t kMaxSmem = 227 * 1024;
+
+struct TcOpDev {
+    int32_t mn_major;  // 1: innermost dimension is M (X) / N (Y); 0: innermost is K
+    int32_t n_loads;   // TMA loads per stage (MN-major: one per 64 rows of M/N)
+    int32_t role[5];
+    uint32_t div[5], mod[5];
+};
+
+struct TcParams {
+    TcOpDev a, b;
+    uint32_t nb, M, N, K;
+    uint32_t tiles_m, tiles_n, n_tiles, group_m;
+    uint32_t block_n, stages, num_kb, tmem_cols;
+    uint32_t idesc;
+    uint32_t a_bytes, b_bytes;
+    RoleMap zb, zm, zn;
+    void* z;
+    float alpha;
+    int32_t out_bf16;
+    uint64_t timeout_ns;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of the given parity.  Gives up (returns false) when
+// the CTA's abort flag is set or after timeout_ns; the latter records
+// TRA_ERR_TIMEOUT in the device status word and raises the abort flag.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, uint64_t timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 63) == 0) {
+            if (*abort) return false;
+            if (globaltimer() - t0 > timeout_ns) {
+                *abort = 1;
+                atomicExch(&g_status, (int)TRA_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar, const int c[5]) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4]), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading / stride
+// byte offsets, fixed version bits 46-48 = 0b001, 128-byte swizzle (mode 2).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tile_coords(const TcOpDev& o, uint32_t cb, uint32_t cm, uint32_t cn, uint32_t ck,
+                                            int c[5]) {
+#pragma unroll
+    for (int j = 0; j < 5; ++j) {
+        const uint32_t v = o.role[j] == kBatch ? cb : (o.role[j] == kM ? cm : (o.role[j] == kN ? cn : ck));
+        c[j] = (int)((v / o.div[j]) % o.mod[j]);
+    }
+}
+
+__device__ __forceinline__ void tile_of(const TcParams& p, uint32_t t, uint32_t& b, uint32_t& mt, uint32_t& nt) {
+    const uint32_t per = p.tiles_m * p.tiles_n;
+    b = t / per;
+    const uint32_t r = t % per;
+    const uint32_t gsize = p.group_m * p.tiles_n;
+    const uint32_t g = r / gsize;
+    const uint32_t first = g * p.group_m;
+    const uint32_t gm = min(p.group_m, p.tiles_m - first);
+    const uint32_t w = r % gsize;
+    mt = first + w % gm;
+    nt = w / gm;
+}
+
+// ------------------------------------------------------------------ the kernel
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+            const __grid_constant__ TcParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t stage_bytes = p.a_bytes + p.b_bytes;
+    const uint32_t bar0 = base + p.stages * stage_bytes;
+    // barrier block: full[S], empty[S], tfull[2], tempty[2], done, then tmem slot and abort flag
+    const uint32_t full0 = bar0, empty0 = bar0 + 8 * p.stages, tfull0 = bar0 + 16 * p.stages;
+    const uint32_t tempty0 = tfull0 + 16, done_bar = tempty0 + 16;
+    uint8_t* gbase = smem_raw + (base - raw);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (done_bar + 8 - base));
+    volatile int* abort = reinterpret_cast<volatile int*>(gbase + (done_bar + 12 - base));
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < p.stages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull0 + 8 * a, 1);
+            mbar_init(tempty0 + 8 * a, 128);
+        }
+        mbar_init(done_bar, 1);
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(p.tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            uint32_t issued_phase[8];
+            bool issued[8] = {false, false, false, false, false, false, false, false};
+            bool ok = true;
+            for (uint32_t t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+                uint32_t b, mt, nt;
+                tile_of(p, t, b, mt, nt);
+                const uint32_t m0 = mt * kBlockM, n0 = nt * p.block_n;
+                for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full0 + 8 * stage;
+                    mbar_expect_tx(fb, stage_bytes);
+                    const uint32_t sa = base + stage * stage_bytes, sb = sa + p.a_bytes;
+                    const uint32_t k0 = kb * kBlockK;
+                    int c[5];
+                    for (int l = 0; l < p.a.n_loads; ++l) {
+                        tile_coords(p.a, b, m0 + 64u * l, 0, k0, c);
+                        tma_load_5d(sa + 8192u * l, &map_a, fb, c);
+                    }
+                    for (int l = 0; l < p.b.n_loads; ++l) {
+                        tile_coords(p.b, b, 0, n0 + 64u * l, k0, c);
+                        tma_load_5d(sb + 8192u * l, &map_b, fb, c);
+                    }
+                    issued[stage] = true;
+                    issued_phase[stage] = phase;
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                // let every copy already issued land before the CTA leaves
+                for (uint32_t s = 0; s < p.stages; ++s)
+                    if (issued[s]) {
+                        volatile int never = 0;
+                        mbar_wait(full0 + 8 * s, issued_phase[s], &never, p.timeout_ns);
+                    }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            const uint32_t a_lbo = p.a.mn_major ? 8192u : 16u, b_lbo = p.b.mn_major ? 8192u : 16u;
+            const uint32_t a_kstep = p.a.mn_major ? 2048u : 32u, b_kstep = p.b.mn_major ? 2048u : 32u;
+            for (uint32_t t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+                if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * p.block_n;
+                for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait(full0 + 8 * stage, phase, abort, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base + stage * stage_bytes, sb = sa + p.a_bytes;
+#pragma unroll
+                    for (uint32_t k = 0; k < kBlockK / 16; ++k) {
+                        const uint64_t ad = smem_desc(sa + k * a_kstep, a_lbo, 1024);
+                        const uint64_t bd = smem_desc(sb + k * b_kstep, b_lbo, 1024);
+                        tc_mma(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
+                    }
+                    tc_commit(empty0 + 8 * stage);  // frees the stage once these MMAs have read it
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(tfull0 + 8 * acc);  // accumulator ready for the epilogue
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1;
+                }
+            }
+            // every MMA issued so far has completed once this commit arrives
+            tc_commit(done_bar);
+            volatile int never = 0;
+            mbar_wait(done_bar, 0, &never, p.timeout_ns);
+        }
+    } else {
+        // ---------------------------------------------------------------- epilogue (warps 2-5)
+        const uint32_t q = warp & 3;  // TMEM lane quarter this warp may access
+        uint32_t acc = 0, acc_phase = 0;
+        for (uint32_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
+            uint32_t b, mt, nt;
+            tile_of(p, t, b, mt, nt);
+            if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort, p.timeout_ns)) break;
+            tc_fence_after();
+            const uint32_t row = q * 32 + lane;
+            const uint32_t m = mt * kBlockM + row;
+            const uint32_t n0 = nt * p.block_n;
+            const int64_t zrow = role_offset(p.zb, b) + role_offset(p.zm, min(m, p.M - 1));
+            for (uint32_t c = 0; c < p.block_n / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem_base + ((q * 32u) << 16) + acc * p.block_n + c * 32u, r);
+                const uint32_t n = n0 + c * 32u;
+                if (m >= p.M || n >= p.N) continue;
+                const int64_t off = zrow + role_offset(p.zn, n);
+                if (p.out_bf16) {
+                    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.z) + off);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const __nv_bfloat162 pr = __floats2bfloat162_rn(p.alpha * __uint_as_float(r[8 * v + 2 * h]),
+                                                                           p.alpha * __uint_as_float(r[8 * v + 2 * h + 1]));
+                            w[h] = *reinterpret_cast<const uint32_t*>(&pr);
+                        }
+                        dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.z) + off);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        dst[v] = make_float4(p.alpha * __uint_as_float(r[4 * v]), p.alpha * __uint_as_float(r[4 * v + 1]),
+                                             p.alpha * __uint_as_float(r[4 * v + 2]),
+                                             p.alpha * __uint_as_float(r[4 * v + 3]));
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(tempty0 + 8 * acc);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(p.tmem_cols)
+                     : "memory");
+    }
+}
+
+// Test hook: one thread waits on an mbarrier that nothing arrives on; the bounded
+// wait must give up after timeout_ns and record TRA_ERR_TIMEOUT.
+__global__ void wait_timeout_probe(uint64_t timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_wait(smem_u32(&bar), 0, &abort, timeout_ns);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+}  // namespace
+
+struct TcDim {
+    int role;
+    uint32_t div, mod, box;
+    uint64_t extent, stride;  // stride in elements
+};
+
+struct TcOperandPlan {
+    int ndims = 0;
+    TcDim dims[5];
+    TcOpDev dev;
+};
+
+struct TcPlan {
+    TcOperandPlan a, b;
+    uint32_t block_n = 0, stages = 0, tiles_m = 0, tiles_n = 0, n_tiles = 0, num_kb = 0, tmem_cols = 0;
+    uint32_t idesc = 0, smem = 0;
+};
+
 void tc_free(TcPlan* t) { delete t; }
-int tc_execute(const Plan&, const void*, const void*, void*, cudaStream_t) {
-    return fail(TRA_ERR_UNSUPPORTED, "tensor-core path not available");
+
+namespace {
+
+// Physical dimensions of an operand's blocked layout, innermost first: the local
+// part of every label (last index first), then the key part; unit dimensions dropped.
+bool operand_dims(const Plan& p, const Operand& t, int mn_role, uint32_t mn_tile, int mn_loads, TcOperandPlan& out) {
+    struct Phys {
+        int label, key;
+        uint64_t extent, stride;
+    };
+    Phys ph[2 * TRA_MAX_RANK];
+    int n = 0;
+    for (int i = t.rank - 1; i >= 0; --i) {
+        const int l = t.label[i];
+        if (p.B[l] / p.D[l] > 1) ph[n++] = {l, 0, (uint64_t)(p.B[l] / p.D[l]), (uint64_t)t.loc_stride[i]};
+    }
+    for (int i = t.rank - 1; i >= 0; --i) {
+        const int l = t.label[i];
+        if (p.D[l] > 1) ph[n++] = {l, 1, (uint64_t)p.D[l], (uint64_t)t.key_stride[i]};
+    }
+    if (n == 0 || n > 5) return false;
+    if (ph[0].stride != 1 || ph[0].key) return false;
+    for (int j = 1; j < n; ++j)
+        if ((ph[j].stride * 2) % 16) return false;
+    // composite stride of every label in its role
+    uint64_t div[TRA_MAX_LABELS] = {};
+    for (int r = 0; r < 4; ++r) {
+        uint64_t d = 1;
+        for (int l : p.comp[r]) {
+            div[l] = d;
+            d *= (uint64_t)p.B[l];
+        }
+    }
+    out.ndims = n;
+    for (int j = 0; j < n; ++j) {
+        const int l = ph[j].label;
+        TcDim& dm = out.dims[j];
+        dm.role = p.role[l];
+        dm.extent = ph[j].extent;
+        dm.stride = ph[j].stride;
+        const uint64_t b = (uint64_t)(p.B[l] / p.D[l]);
+        dm.div = (uint32_t)(ph[j].key ? div[l] * b : div[l]);
+        dm.mod = (uint32_t)ph[j].extent;
+        dm.box = 1;
+    }
+    // boxes: walk each role's labels innermost first with the tile extent
+    const uint32_t tiles[4] = {1u, mn_role == kM ? mn_tile : 1u, mn_role == kN ? mn_tile : 1u, (uint32_t)kBlockK};
+    for (int r = 0; r < 4; ++r) {
+        if ((r == kM || r == kN) && r != mn_role) continue;
+        uint64_t rem = tiles[r];
+        int last_dim = -1;
+        for (int l : p.comp[r]) {
+            if (t.pos_of(l) < 0) {
+                if (rem != 1) return false;  // the tile would span a label this operand lacks
+                continue;
+            }
+            for (int key = 0; key < 2; ++key) {
+                int j = -1;
+                for (int q = 0; q < n; ++q)
+                    if (ph[q].label == l && ph[q].key == key) j = q;
+                if (j < 0) continue;  // unit dimension
+                const uint64_t ext = ph[j].extent;
+                uint64_t box;
+                if (rem >= ext) {
+                    if (rem % ext) return false;
+                    box = ext;
+                } else {
+                    if (ext % rem) return false;
+                    box = rem;
+                }
+                rem /= box;
+                out.dims[j].box = (uint32_t)box;
+                if (box > 1) {
+                    if (j <= last_dim) return false;  // box order must follow the composite order
+                    last_dim = j;
+                }
+            }
+        }
+        if (rem != 1) return false;
+    }
+    // shared-memory layout: K-major (innermost K, 64 wide; the other boxes are the M/N rows)
+    // or MN-major (innermost M/N, 64 wide per load; the other boxes are K rows)
+    const int r0 = out.dims[0].role;
+    if (out.dims[0].box != 64 || out.dims[0].extent % 64) return false;
+    if (r0 == kK) {
+        if (mn_loads != 1) return false;
+        for (int j = 1; j < n; ++j)
+            if (out.dims[j].box > 1 && out.dims[j].role != mn_role) return false;
+        out.dev.mn_major = 0;
+        out.dev.n_loads = 1;
+    } else if (r0 == mn_role) {
+        for (int j = 1; j < n; ++j)
+            if (out.dims[j].box > 1 && out.dims[j].role != kK) return false;
+        out.dev.mn_major = 1;
+        out.dev.n_loads = mn_loads;
+    } else {
+        return false;
+    }
+    for (int j = 0; j < 5; ++j) {
+        out.dev.role[j] = j < n ? out.dims[j].role : kK;
+        out.dev.div[j] = j < n ? out.dims[j].div : 1u;
+        out.dev.mod[j] = j < n ? out.dims[j].mod : 1u;
+    }
+    return true;
+}
+
+}  // namespace
+
+bool tc_plan(Plan* p) {
+    if (p->unary || p->op != kMul || p->agg != kSum || !p->in_bf16 || p->literal) return false;
+    const uint64_t M = p->ext[kM], N = p->ext[kN], K = p->ext[kK];
+    if (M % kBlockM || K % kBlockK || N % 64) return false;
+    uint32_t bn = N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : 64);
+    // output: 32 consecutive columns contiguous (innermost label of Z is the innermost N label)
+    if (p->comp[kN].empty()) return false;
+    const int zl = p->Z.label[p->Z.rank - 1];
+    if (zl != p->comp[kN][0] || (p->B[zl] / p->D[zl]) % 32) return false;
+    TcPlan* t = new TcPlan();
+    // X: K-major (one load of 128 rows) or M-major (two loads of 64 columns)
+    bool ok = operand_dims(*p, p->X, kM, kBlockM, 1, t->a);
+    if (!ok || t->a.dev.mn_major) {
+        t->a = TcOperandPlan();
+        ok = operand_dims(*p, p->X, kM, 64, kBlockM / 64, t->a) && t->a.dev.mn_major;
+    }
+    bool okb = ok && operand_dims(*p, p->Y, kN, bn, 1, t->b);
+    if (ok && (!okb || t->b.dev.mn_major)) {
+        t->b = TcOperandPlan();
+        okb = operand_dims(*p, p->Y, kN, 64, bn / 64, t->b) && t->b.dev.mn_major;
+    }
+    if (!ok || !okb) {
+        delete t;
+        return false;
+    }
+    t->block_n = bn;
+    const uint32_t stage = (uint32_t)(kBlockM * kBlockK * 2 + bn * kBlockK * 2);
+    t->stages = (kMaxSmem - 2048) / stage;
+    if (t->stages > 8) t->stages = 8;
+    if (t->stages < 2) {
+        delete t;
+        return false;
+    }
+    t->smem = t->stages * stage + 1024 + 256;
+    t->tiles_m = (uint32_t)(M / kBlockM);
+    t->tiles_n = (uint32_t)(N / bn);
+    t->n_tiles = (uint32_t)(p->ext[kBatch] * t->tiles_m * t->tiles_n);
+    t->num_kb = (uint32_t)(K / kBlockK);
+    t->tmem_cols = 2 * bn <= 128 ? 128 : (2 * bn <= 256 ? 256 : 512);
+    t->idesc = (1u << 4)                                   // D: fp32
+               | (1u << 7) | (1u << 10)                    // A, B: bf16
+               | ((uint32_t)t->a.dev.mn_major << 15)       // A major-ness
+               | ((uint32_t)t->b.dev.mn_major << 16)       // B major-ness
+               | ((bn >> 3) << 17)                         // N / 8
+               | ((uint32_t)(kBlockM >> 4) << 24);         // M / 16
+    p->tc = t;
+    return true;
+}
+
+namespace {
+
+bool encode(const TcOperandPlan& o, const void* base, CUtensorMap* map) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[5], strides[4];
+    cuuint32_t box[5], estr[5] = {1, 1, 1, 1, 1};
+    uint64_t last = 1;
+    for (int j = 0; j < 5; ++j) {
+        if (j < o.ndims) {
+            dims[j] = o.dims[j].extent;
+            box[j] = o.dims[j].box;
+            if (j > 0) strides[j - 1] = o.dims[j].stride * 2;
+            last = o.dims[j].stride * o.dims[j].extent;
+        } else {
+            dims[j] = 1;
+            box[j] = 1;
+            if (j > 0) strides[j - 1] = ((last * 2 + 15) / 16) * 16;
+        }
+    }
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+}  // namespace
+
+int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_t s) {
+    const TcPlan& t = *p.tc;
+    if (((uintptr_t)x | (uintptr_t)y | (uintptr_t)z) % 16) return fail(TRA_ERR_ARG, "tensor-core path needs 16-byte aligned buffers");
+    CUtensorMap ma, mb;
+    if (!encode(t.a, x, &ma) || !encode(t.b, y, &mb)) return fail(TRA_ERR_CUDA, "tensor map encoding failed");
+    TcParams tp;
+    memset(&tp, 0, sizeof(tp));
+    tp.a = t.a.dev;
+    tp.b = t.b.dev;
+    tp.nb = (uint32_t)p.ext[kBatch];
+    tp.M = (uint32_t)p.ext[kM];
+    tp.N = (uint32_t)p.ext[kN];
+    tp.K = (uint32_t)p.ext[kK];
+    tp.tiles_m = t.tiles_m;
+    tp.tiles_n = t.tiles_n;
+    tp.n_tiles = t.n_tiles;
+    tp.group_m = 16;
+    tp.block_n = t.block_n;
+    tp.stages = t.stages;
+    tp.num_kb = t.num_kb;
+    tp.tmem_cols = t.tmem_cols;
+    tp.idesc = t.idesc;
+    tp.a_bytes = kBlockM * kBlockK * 2;
+    tp.b_bytes = t.block_n * kBlockK * 2;
+    tp.zb = role_map(p, p.Z, kBatch);
+    tp.zm = role_map(p, p.Z, kM);
+    tp.zn = role_map(p, p.Z, kN);
+    tp.z = z;
+    tp.alpha = (float)p.alpha;
+    tp.out_bf16 = p.out_bf16;
+    tp.timeout_ns = 2000000000ull;  // 2 s per wait
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)t.smem);
+    if (e != cudaSuccess) return fail(TRA_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(e));
+    const int sms = sm_count();
+    if (sms <= 0) return fail(TRA_ERR_CUDA, "no device");
+    const unsigned grid = (unsigned)(t.n_tiles < (uint32_t)sms ? t.n_tiles : (uint32_t)sms);
+    tc_gemm<<<grid, kThreads, t.smem, s>>>(ma, mb, tp);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? TRA_OK : fail(TRA_ERR_CUDA, "tensor-core launch: %s", cudaGetErrorString(e));
+}
+
+cudaError_t read_and_clear_status(int* value, cudaStream_t s) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(value, g_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    const int zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return e;
+    return cudaStreamSynchronize(s);
+}
+
+cudaError_t launch_wait_timeout_probe(uint64_t timeout_ns, cudaStream_t s) {
+    wait_timeout_probe<<<1, 32, 0, s>>>(timeout_ns);
+    return cudaGetLastError();
 }
 
 }  // namespace tra

@@ -122,6 +122,7 @@ RoleMap role_map(const Plan& p, const Operand& t, int role) {
 int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int32_t* d, int n_d, Plan* p) {
     if (!spec || !p) return fail(TRA_ERR_ARG, "null spec or plan");
     p->spec = spec;
+    p->sqdiff_expand = -1;  // not given: expansion for fp32 inputs, direct for bf16
     std::vector<std::string> parts = split(spec, ':');
     const std::string eq = parts[0];
     const size_t arrow = eq.find("->");
@@ -148,7 +149,7 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
         if (k == "in" && (v == "f32" || v == "bf16")) p->in_bf16 = v == "bf16";
         else if (k == "out" && (v == "f32" || v == "bf16")) p->out_bf16 = v == "bf16";
         else if (k == "mode" && (v == "fused" || v == "literal")) p->literal = v == "literal";
-        else if (k == "sqdiff" && (v == "direct" || v == "expand")) p->sqdiff_expand = v == "expand";
+        else if (k == "sqdiff" && (v == "direct" || v == "expand")) p->sqdiff_expand = v == "expand" ? 1 : 0;
         else if (k == "alpha") {
             char* end = nullptr;
             errno = 0;
@@ -217,6 +218,8 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
             p->D[l] = d[di];
         }
     }
+
+    if (p->sqdiff_expand < 0) p->sqdiff_expand = p->in_bf16 ? 0 : 1;
 
     // roles
     bool inx[TRA_MAX_LABELS] = {}, iny[TRA_MAX_LABELS] = {}, inz[TRA_MAX_LABELS] = {};

@@ -82,6 +82,8 @@ struct SemiringParams {
     float alpha;
     int32_t in_bf16, out_bf16;
     int32_t x_kcontig, x_mcontig, y_ncontig, y_kcontig;
+    // loader of each operand: 0 generic gather, 1 float4 along K, 2 float4 along M (X) / N (Y)
+    int32_t x_mode, y_mode;
     // logsumexp factored form: the operands are exp(x - rowmax) and exp(y - colmax)
     // (fp32 scratch), and the epilogue adds rowmax + colmax + log(sum).
     const float* rowmax;  // [nb * M] or null
@@ -175,5 +177,6 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 
 // Device status word written by bounded waits that give up (TRA_ERR_TIMEOUT).
 cudaError_t read_and_clear_status(int* value, cudaStream_t s);
+cudaError_t launch_wait_timeout_probe(uint64_t timeout_ns, cudaStream_t s);
 
 }  // namespace tra

@@ -121,13 +121,25 @@ def test_semiring_literal_mode(lib, cuda, op, agg):
         check(op, agg, g, r, S)
 
 
-def test_sqdiff_expansion(lib, cuda):
+@pytest.mark.parametrize("form", ["expand", "direct"])
+@pytest.mark.parametrize("d", [[2, 1, 1, 2], [1, 4, 4, 1]])
+def test_sqdiff_forms(lib, cuda, form, d):
     M, K, N = 200, 256, 130
     X = gen((M, K), 5, 0)
     Y = gen((K, N), 5, 1)
-    _, g = run_plan(lib, MM + ":sqdiff:sum:sqdiff=expand", [M, K, N], [2, 1, 1, 2], X, Y)
+    _, g = run_plan(lib, MM + ":sqdiff:sum:sqdiff=" + form, [M, K, N], d, X, Y)
     r, _ = ref_full(MM, X, Y, "sqdiff", "sum")
     check_rel(g, r, FP32_REL)
+
+
+def test_sqdiff_full_output_pair_workload(lib, cuda):
+    # every one of the 8192 x 8192 outputs of the squared-distance workload, both forms
+    X = gen((8192, 256), 0, 0)
+    Y = gen((256, 8192), 1, 0)
+    r = oracle.einsum(MM, X, Y, op="sqdiff", agg="sum")
+    for form in ("expand", "direct"):
+        _, g = run_plan(lib, MM + ":sqdiff:sum:sqdiff=" + form, [8192, 256, 8192], [8, 1, 1, 8], X, Y)
+        check_rel(g, r, FP32_REL)
 
 
 def test_lse_underflow_fallback(lib, cuda):

@@ -1,0 +1,93 @@
+"""Tensor-core (tcgen05) BF16 sum-of-products path against the oracle, and the bounded-wait hook.
+
+"EinDecomp ... tensor relational algebra", section 2.2: the join of key-matched
+BF16 sub-tensors through multiply and the sum aggregation over contracted keys.
+Shapes here are small but span several tiles, both operand majors (K innermost
+or M / N innermost), split contracted keys, batch labels, alpha and bf16 output.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import rounding
+
+from gpu_helpers import BF16_SUM_REL, FP32_REL, as_f64, check_bf16_bar, check_sum, gen, run_plan
+
+pytestmark = pytest.mark.gpu
+
+
+def labels_of(eq):
+    ins, out = eq.split("->")[0].split(","), eq.split("->")[1]
+    order = []
+    for c in "".join(ins):
+        if c not in order:
+            order.append(c)
+    return ins, out, order
+
+
+CASES = [
+    # eq, bounds (first-appearance order), d, options
+    ("ij,jk->ik", [256, 192, 128], [2, 3, 3, 2], ""),               # K-major A, N-major B, split K keys
+    ("ij,jk->ik", [384, 256, 512], [1, 1, 1, 1], ""),               # N tile 256
+    ("ji,jk->ik", [128, 256, 192], [2, 1, 2, 3], ""),               # M-major A
+    ("ij,kj->ik", [256, 128, 256], [2, 2, 2, 2], ""),               # K-major B
+    ("ji,kj->ik", [128, 256, 128], [1, 2, 1, 1], ""),               # both MN / K majors swapped
+    ("bij,bjk->bik", [3, 128, 128, 192], [3, 1, 2, 3, 2, 3], ""),   # batch label split into keys
+    ("abef,cfed->abcd", [4, 32, 8, 64, 4, 64], [2, 1, 1, 1, 2, 1, 1, 1], ""),
+    ("sa,ahd->shd", [256, 128, 2, 128], [2, 1, 1, 1, 1], ":out=bf16"),
+    ("shd,thd->hst", [256, 2, 128, 256], [1, 2, 1, 1, 2, 1], ":alpha=0.08838834764831845"),
+    ("hst,thd->shd", [2, 256, 256, 128], [2, 1, 1, 1, 2, 1], ":out=bf16"),
+    ("shd,ahd->sa", [256, 2, 128, 128], [1, 1, 1, 1, 1, 1], ""),
+]
+
+
+@pytest.mark.parametrize("eq,bounds,d,opts", CASES)
+def test_tc_parity(lib, cuda, eq, bounds, d, opts):
+    ins, out, order = labels_of(eq)
+    B = dict(zip(order, bounds))
+    X = gen(tuple(B[c] for c in ins[0]), 9, 0, bf16=True)
+    Y = gen(tuple(B[c] for c in ins[1]), 9, 1, bf16=True)
+    spec = f"{eq}:mul:sum:in=bf16{opts}"
+    alpha = 1.0
+    if "alpha=" in opts:
+        alpha = float(opts.split("alpha=")[1].split(":")[0])
+    p, g = run_plan(lib, spec, bounds, d, X, Y, out_bf16=":out=bf16" in opts)
+    assert p.kernel == "tc_bf16"
+    r = oracle.einsum(eq, as_f64(X), as_f64(Y), alpha=alpha)
+    S = oracle.einsum(eq, np.abs(as_f64(X)), np.abs(as_f64(Y))) * abs(alpha)
+    check_bf16_bar(g, r)
+    if ":out=bf16" in opts:
+        # one bf16 rounding of the fp32 accumulator: within half a bf16 ulp plus the sum error
+        assert np.all(np.abs(g - r) <= 2.0 ** -8 * np.abs(r) + FP32_REL * S)
+    else:
+        check_sum(g, r, S, FP32_REL)
+
+
+def test_tc_repeat_and_stream(lib, cuda):
+    # back-to-back launches on a side stream reuse the persistent schedule correctly
+    import torch
+
+    X = gen((512, 256), 10, 0, bf16=True)
+    Y = gen((256, 512), 10, 1, bf16=True)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        outs = [run_plan(lib, "ij,jk->ik:mul:sum:in=bf16", [512, 256, 512], [2, 2, 2, 2], X, Y)[1] for _ in range(3)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        np.testing.assert_array_equal(o, outs[0])
+    r = oracle.einsum("ij,jk->ik", as_f64(X), as_f64(Y))
+    check_sum(outs[0], r, oracle.einsum("ij,jk->ik", np.abs(as_f64(X)), np.abs(as_f64(Y))), FP32_REL)
+
+
+def test_bounded_wait_gives_up(lib, cuda):
+    lib.ein_status()  # clean status word
+    lib.ein_selftest_wait_timeout(2_000_000)  # 2 ms on a barrier nothing arrives on
+    with pytest.raises(lib.TraError) as e:
+        lib.ein_status()
+    assert "TRA_ERR_TIMEOUT" in str(e.value)
+    lib.ein_status()  # cleared; the context is still usable
+    X = gen((128, 64), 11, 0, bf16=True)
+    Y = gen((64, 128), 11, 1, bf16=True)
+    _, g = run_plan(lib, "ij,jk->ik:mul:sum:in=bf16", [128, 64, 128], [1, 1, 1, 1], X, Y)
+    check_sum(g, oracle.einsum("ij,jk->ik", as_f64(X), as_f64(Y)),
+              oracle.einsum("ij,jk->ik", np.abs(as_f64(X)), np.abs(as_f64(Y))), FP32_REL)
