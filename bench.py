@@ -139,8 +139,11 @@ class PairWorkload:
     name = "semiring pair: sqdist (x-y)^2/sum + max-plus (x+y)/max, X 8192x256, Y 256x8192 fp32, d=[8,1,1,8]"
     M, K, N = 8192, 256, 8192
     d = [8, 1, 1, 8]
+    dtype = "f32"
+    cpu_default = 1024  # output rows
+    ref_default = 32
 
-    def __init__(self, seed_offset=0):
+    def __init__(self, seed_offset=0, d=None):
         self.seed_offset = seed_offset
 
     def host_inputs(self):
@@ -195,7 +198,246 @@ class PairWorkload:
         return ("k_semiring.cu", ["repartition", "semiring sqdiff/sum", "semiring add/max"][j])
 
 
-WORKLOADS = {"pair": PairWorkload}
+class _PointsWorkload:
+    """Shared pieces: inputs resident in relation layout, one or more plans per step, oracle on points."""
+
+    cpu_default = 64  # output points per oracle sample
+    ref_default = 8
+    dtype = "bf16"
+
+    def __init__(self, seed_offset=0, d=None):
+        self.seed_offset = seed_offset
+        if d is not None:
+            self.d = list(d)
+
+    def oracle_points(self, eq, X, Y, op, agg, zshape, r0, n, alpha=1.0):
+        import oracle
+
+        total = int(np.prod(zshape))
+        pts = (np.arange(n, dtype=np.int64) + r0 * n) % total
+        oracle.einsum_points(eq, X, Y, pts, op=op, agg=agg, alpha=alpha)
+        K = 1
+        return pts.size, K
+
+
+def _bf16_host(shape, seed, tensor, sigma=1.0):
+    import datagen
+
+    return datagen.normal_bf16(shape, seed, tensor, 0.0, sigma)
+
+
+def _dev_bf16(torch, bits):
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda().reshape(-1)
+
+
+class C1Workload(_PointsWorkload):
+    dtype = "f32"
+    name = "matmul 64x64x64 fp32 U[-1,1], d in {[4,1,1,4],[1,4,4,1],[2,2,2,2]} (three executions per step)"
+    d = [[4, 1, 1, 4], [1, 4, 4, 1], [2, 2, 2, 2]]
+
+    def host_inputs(self):
+        import datagen
+
+        return [datagen.uniform_f32((64, 64), 0 + self.seed_offset, 0), datagen.uniform_f32((64, 64), 0 + self.seed_offset, 1)]
+
+    def setup(self, tra, torch, inputs):
+        X, Y = inputs
+        self.Xd = torch.from_numpy(X).cuda().reshape(-1)
+        self.Yd = torch.from_numpy(Y).cuda().reshape(-1)
+        self.steps, self.outputs_dev = [], []
+        for d in self.d:
+            p = tra.Plan("ij,jk->ik:mul:sum", [64, 64, 64], d)
+            xr, yr = torch.empty_like(self.Xd), torch.empty_like(self.Yd)
+            z = torch.empty(64 * 64, dtype=torch.float32, device="cuda")
+            self.outputs_dev.append(z)
+
+            def run(p=p, xr=xr, yr=yr, z=z, d=d):
+                tra.repartition(self.Xd, xr, [64, 64], [1, 1], d[:2])
+                tra.repartition(self.Yd, yr, [64, 64], [1, 1], d[2:])
+                p.execute(xr, yr, z)
+
+            self.steps.append(Step(f"partition + join+agg d={d}", run, 2 * 64 ** 3, "flop", "alu",
+                                   kernel_launches(p) + 2))
+        self.inputs_dev = [self.Xd, self.Yd]
+
+    def ops_per_step(self):
+        return 3 * 2 * 64 ** 3
+
+    def oracle_sample(self, inputs, r0, n):
+        X, Y = [a.astype(np.float64) for a in inputs]
+        import oracle
+
+        for _ in self.d:
+            oracle.einsum("ij,jk->ik", X, Y)
+        return 3 * 2 * 64 ** 3
+
+    def sample_text(self, n):
+        return "the whole workload (three 64^3 EinSums)"
+
+
+class C3Workload(_PointsWorkload):
+    name = "4-D contraction C[a,b,c,d]=sum_e,f A[a,b,e,f]B[c,f,e,d], 64^6 BF16 in / FP32 out, d=[4,1,1,1,4,1,1,1]; + repartition of C [4,1,4,1]->[1,4,1,4]"
+    d = [4, 1, 1, 1, 4, 1, 1, 1]
+    cpu_default = 256
+
+    def host_inputs(self):
+        return [_bf16_host((64,) * 4, 0 + self.seed_offset, 0), _bf16_host((64,) * 4, 0 + self.seed_offset, 1)]
+
+    def setup(self, tra, torch, inputs):
+        A, B = inputs
+        self.Ad, self.Bd = _dev_bf16(torch, A), _dev_bf16(torch, B)  # [4,1,1,1] relation == dense
+        self.p = tra.Plan("abef,cfed->abcd:mul:sum:in=bf16", [64] * 6, self.d)
+        self.C = torch.empty(64 ** 4, dtype=torch.float32, device="cuda")
+        self.C2 = torch.empty_like(self.C)
+        self.steps = [
+            Step("join+agg 4-D contraction (tcgen05)", lambda: self.p.execute(self.Ad, self.Bd, self.C), 2 * 64 ** 6,
+                 "flop", "tensor", kernel_launches(self.p)),
+            Step("repartition C [4,1,4,1]->[1,4,1,4]",
+                 lambda: tra.repartition(self.C, self.C2, [64] * 4, [4, 1, 4, 1], [1, 4, 1, 4]), 2 * 64 ** 4 * 4,
+                 "bytes", "hbm", 1),
+        ]
+        self.inputs_dev = [self.Ad, self.Bd]
+        self.outputs_dev = [self.C2]
+
+    def ops_per_step(self):
+        return 2 * 64 ** 6
+
+    def oracle_sample(self, inputs, r0, n):
+        from datagen import bf16_bits_to_f32
+
+        A, B = [bf16_bits_to_f32(a).astype(np.float64) for a in inputs]
+        self.oracle_points("abef,cfed->abcd", A, B, "mul", "sum", (64,) * 4, r0, n)
+        return 2 * n * 64 * 64
+
+    def sample_text(self, n):
+        return f"{n} of 64^4 outputs of the contraction"
+
+    def traffic_key(self, j):
+        return ("k_tc.cu", "tc_gemm 4-D contraction") if j == 0 else ("k_misc.cu", "repartition 64^4 fp32")
+
+
+class C4Workload(_PointsWorkload):
+    name = "multi-head attention EinGraph s=4096 a=4096 h=32 d=128, BF16 activations N(0,1), weights N(0,0.02)"
+    d = "projections all-ones; scores/lse/exp/A.V split h=32; repartitions between"
+    cpu_default = 256
+
+    def host_inputs(self):
+        s, a, h, d = 4096, 4096, 32, 128
+        o = self.seed_offset
+        return ([_bf16_host((s, a), 0 + o, t) for t in range(3)] +
+                [_bf16_host((a, h, d), 0 + o, 3 + t, 0.02) for t in range(4)])
+
+    def setup(self, tra, torch, inputs):
+        from tensor_relational_algebra_gb300.attention import AttentionGraph
+
+        self.g = AttentionGraph(4096, 4096, 32, 128)
+        self.dev = [_dev_bf16(torch, x) for x in inputs]
+        self.steps = [Step(*n) for n in self.g.nodes(*self.dev)]
+        self.inputs_dev = self.dev
+        self.outputs_dev = [self.g.out]
+
+    def ops_per_step(self):
+        return self.g.flops()
+
+    def oracle_sample(self, inputs, r0, n):
+        from datagen import bf16_bits_to_f32
+
+        Q, WQ = bf16_bits_to_f32(inputs[0]).astype(np.float64), bf16_bits_to_f32(inputs[3]).astype(np.float64)
+        self.oracle_points("sa,ahd->shd", Q, WQ, "mul", "sum", (4096, 32, 128), r0, n)
+        return 2 * n * 4096
+
+    def sample_text(self, n):
+        return f"{n} outputs of the Q projection node (4096 terms each)"
+
+
+class C5Workload(_PointsWorkload):
+    name_fmt = "BF16 matmul 16384^3 (FP32 accumulate), d={}"
+    d = [1, 1, 1, 1]
+    cpu_default = 64
+
+    @property
+    def name(self):
+        return self.name_fmt.format(self.d)
+
+    def host_inputs(self):
+        n = 16384
+        return [_bf16_host((n, n), 0 + self.seed_offset, 0), _bf16_host((n, n), 0 + self.seed_offset, 1)]
+
+    def setup(self, tra, torch, inputs):
+        n = 16384
+        X, Y = inputs
+        self.Xd, self.Yd = _dev_bf16(torch, X), _dev_bf16(torch, Y)
+        self.Xr, self.Yr = device_relation(tra, torch, self.Xd, [n, n], self.d[:2]), device_relation(
+            tra, torch, self.Yd, [n, n], self.d[2:])
+        torch.cuda.synchronize()
+        self.p = tra.Plan("ij,jk->ik:mul:sum:in=bf16", [n, n, n], self.d)
+        self.Z = torch.empty(n * n, dtype=torch.float32, device="cuda")
+        self.steps = [Step(f"join+agg matmul d={self.d} (tcgen05)", lambda: self.p.execute(self.Xr, self.Yr, self.Z),
+                           2 * n ** 3, "flop", "tensor", kernel_launches(self.p))]
+        self.inputs_dev = [self.Xr, self.Yr]
+        self.outputs_dev = [self.Z]
+
+    def ops_per_step(self):
+        return 2 * 16384 ** 3
+
+    def oracle_sample(self, inputs, r0, n):
+        from datagen import bf16_bits_to_f32
+
+        X, Y = [bf16_bits_to_f32(a).astype(np.float64) for a in inputs]
+        self.oracle_points("ij,jk->ik", X, Y, "mul", "sum", (16384, 16384), r0, n)
+        return 2 * n * 16384
+
+    def sample_text(self, n):
+        return f"{n} of 16384^2 outputs"
+
+    def traffic_key(self, j):
+        return ("k_tc.cu", f"tc_gemm 16384^3 d={self.d}")
+
+
+class C5bWorkload(_PointsWorkload):
+    dtype = "f32"
+    name_fmt = "logsumexp-aggregated Z[i,k]=lse_j(X[i,j]+Y[j,k]) 8192^3 fp32, d={}"
+    d = [1, 1, 1, 1]
+    cpu_default = 64
+
+    @property
+    def name(self):
+        return self.name_fmt.format(self.d)
+
+    def host_inputs(self):
+        import datagen
+
+        n = 8192
+        return [datagen.normal_f32((n, n), 0 + self.seed_offset, 0), datagen.normal_f32((n, n), 0 + self.seed_offset, 1)]
+
+    def setup(self, tra, torch, inputs):
+        n = 8192
+        X, Y = inputs
+        self.Xd, self.Yd = torch.from_numpy(X).cuda().reshape(-1), torch.from_numpy(Y).cuda().reshape(-1)
+        self.Xr, self.Yr = device_relation(tra, torch, self.Xd, [n, n], self.d[:2]), device_relation(
+            tra, torch, self.Yd, [n, n], self.d[2:])
+        self.p = tra.Plan("ij,jk->ik:add:lse", [n, n, n], self.d)
+        self.ws = torch.empty(self.p.workspace_bytes, dtype=torch.uint8, device="cuda")
+        self.Z = torch.empty(n * n, dtype=torch.float32, device="cuda")
+        self.steps = [Step(f"join+agg (x+y)/logsumexp d={self.d}", lambda: self.p.execute(self.Xr, self.Yr, self.Z, self.ws),
+                           2 * n ** 3, "flop", "alu", kernel_launches(self.p))]
+        self.inputs_dev = [self.Xr, self.Yr]
+        self.outputs_dev = [self.Z]
+
+    def ops_per_step(self):
+        return 2 * 8192 ** 3
+
+    def oracle_sample(self, inputs, r0, n):
+        X, Y = [a.astype(np.float64) for a in inputs]
+        self.oracle_points("ij,jk->ik", X, Y, "add", "lse", (8192, 8192), r0, n)
+        return 2 * n * 8192
+
+    def sample_text(self, n):
+        return f"{n} of 8192^2 outputs"
+
+
+WORKLOADS = {"pair": PairWorkload, "c1": C1Workload, "c3": C3Workload, "c4": C4Workload, "c5": C5Workload,
+             "c5b": C5bWorkload}
 
 
 # ----------------------------------------------------------------------------- measurement
@@ -276,7 +518,7 @@ def run_ours(args):
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
     tra.load()
-    wl = WORKLOADS[args.workload](seed_offset=rank)
+    wl = WORKLOADS[args.workload](seed_offset=rank, d=args.d)
     host = wl.host_inputs()
     wl.setup(tra, torch, host)
     flush_buf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
@@ -367,7 +609,7 @@ def run_ours(args):
     if world == 1 and not args.no_cpu_baseline:
         import oracle
 
-        rows = args.cpu_rows
+        rows = args.cpu_rows or wl.cpu_default
         t0 = time.perf_counter()
         work = wl.oracle_sample(host, 0, rows)
         dt = time.perf_counter() - t0
@@ -377,7 +619,7 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (Philox-4x32-10 N(0,1), seeded)",
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (Philox-4x32-10, seeded)",
         "config": {"workload": wl.name, "d": wl.d, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between steps (512 MiB write outside the step's events)",
                    "per_launch_group_ms": {s.name: round(m, 4) for s, m in zip(wl.steps, means)}},
@@ -405,9 +647,9 @@ def run_reference(args):
         return
     import oracle
 
-    wl = WORKLOADS[args.workload]()
+    wl = WORKLOADS[args.workload](d=args.d)
     host = wl.host_inputs()
-    rows = args.ref_rows
+    rows = args.ref_rows or wl.ref_default
     for s in range(args.warmup):
         wl.oracle_sample(host, s * rows, rows)
     t0 = time.perf_counter()
@@ -437,8 +679,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="pair")
-    ap.add_argument("--cpu-rows", type=int, default=1024, help="output rows the CPU-baseline oracle computes")
-    ap.add_argument("--ref-rows", type=int, default=32, help="output rows per reference-arm step")
+    ap.add_argument("--d", type=lambda v: [int(x) for x in v.split(",")], default=None,
+                    help="partition vector for c5 / c5b, e.g. 4,2,2,2")
+    ap.add_argument("--cpu-rows", type=int, default=None, help="oracle sample size of the CPU baseline")
+    ap.add_argument("--ref-rows", type=int, default=None, help="oracle sample size per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -1,0 +1,78 @@
+"""The multi-head-attention EinGraph of "EinDecomp ... tensor relational algebra" section 2.1,
+run node by node through the C ABI (one ein_execute or ein_repartition per node).
+
+  Q_proj[s,h,d] = sum_a Q[s,a] W_Q[a,h,d]        (K, V alike)        d = all ones
+  repartition   Q/K/V_proj [1,1,1] -> [1,h,1]                         (head-major relations)
+  S[h,s,t]      = (1/sqrt(d)) sum_d Q_proj[s,h,d] K_proj[t,h,d]        split h ways
+  L[h,s]        = logsumexp_t S[h,s,t]                                 split h ways
+  A[h,s,t]      = exp(S[h,s,t] - L[h,s])                               split h ways (bf16)
+  O[s,h,d]      = sum_t A[h,s,t] V_proj[t,h,d]                         split h ways (bf16)
+  repartition   O [1,h,1] -> [1,1,1]
+  Out[s,a]      = sum_h sum_d O[s,h,d] W_O[a,h,d]                      d = all ones
+
+The printed Scores[h,s,s] is read with a second sequence index t; the scale is applied
+after the sum over d; there is no mask.  Buffers are allocated once (torch) and reused.
+"""
+from __future__ import annotations
+
+import math
+
+from . import Plan, repartition
+
+
+class AttentionGraph:
+    def __init__(self, s: int, a: int, h: int, d: int, device="cuda"):
+        import torch
+
+        self.s, self.a, self.h, self.d = s, a, h, d
+        t = s
+        self.p_proj = Plan("sa,ahd->shd:mul:sum:in=bf16:out=bf16", [s, a, h, d], [1, 1, 1, 1, 1])
+        self.p_scores = Plan(f"shd,thd->hst:mul:sum:in=bf16:alpha={1.0 / math.sqrt(d)!r}", [s, h, d, t],
+                             [1, h, 1, 1, h, 1])
+        self.p_lse = Plan("hst->hs::lse", [h, s, t], [h, 1, 1])
+        self.p_exp = Plan("hst,hs->hst:expsub:none:out=bf16", [h, s, t], [h, 1, 1, h, 1])
+        self.p_pv = Plan("hst,thd->shd:mul:sum:in=bf16:out=bf16", [h, s, t, d], [h, 1, 1, 1, h, 1])
+        self.p_out = Plan("shd,ahd->sa:mul:sum:in=bf16", [s, h, d, a], [1, 1, 1, 1, 1, 1])
+        bf, f32 = torch.bfloat16, torch.float32
+        e = lambda n, dt: torch.empty(n, dtype=dt, device=device)  # noqa: E731
+        self.qp, self.kp, self.vp = e(s * h * d, bf), e(s * h * d, bf), e(s * h * d, bf)
+        self.qr, self.kr, self.vr = e(s * h * d, bf), e(s * h * d, bf), e(s * h * d, bf)
+        self.S = e(h * s * t, f32)
+        self.L = e(h * s, f32)
+        self.A = e(h * s * t, bf)
+        self.Oh = e(s * h * d, bf)
+        self.O = e(s * h * d, bf)
+        self.out = e(s * a, f32)
+
+    def nodes(self, Q, K, V, WQ, WK, WV, WO):
+        """(name, callable, work, unit, bound, kernel launches) per node, in execution order."""
+        s, a, h, d = self.s, self.a, self.h, self.d
+        shd = [s, h, d]
+        gemm = 2 * s * a * h * d
+        att = 2 * h * s * s * d
+        return [
+            ("proj Q", lambda: self.p_proj.execute(Q, WQ, self.qp), gemm, "flop", "tensor", 1),
+            ("proj K", lambda: self.p_proj.execute(K, WK, self.kp), gemm, "flop", "tensor", 1),
+            ("proj V", lambda: self.p_proj.execute(V, WV, self.vp), gemm, "flop", "tensor", 1),
+            ("repartition QKV -> head-major", lambda: (repartition(self.qp, self.qr, shd, [1, 1, 1], [1, h, 1]),
+                                                        repartition(self.kp, self.kr, shd, [1, 1, 1], [1, h, 1]),
+                                                        repartition(self.vp, self.vr, shd, [1, 1, 1], [1, h, 1])),
+             3 * 2 * s * h * d * 2, "bytes", "hbm", 3),
+            ("scores", lambda: self.p_scores.execute(self.qr, self.kr, self.S), att, "flop", "tensor", 1),
+            ("logsumexp", lambda: self.p_lse.execute(self.S, None, self.L), h * s * s * 4 + h * s * 4, "bytes", "hbm", 1),
+            ("exp(S-L)", lambda: self.p_exp.execute(self.S, self.L, self.A), h * s * s * (4 + 2) + h * s * 4, "bytes",
+             "hbm", 1),
+            ("A.V", lambda: self.p_pv.execute(self.A, self.vr, self.Oh), att, "flop", "tensor", 1),
+            ("repartition O -> dense", lambda: repartition(self.Oh, self.O, shd, [1, h, 1], [1, 1, 1]),
+             2 * s * h * d * 2, "bytes", "hbm", 1),
+            ("out proj", lambda: self.p_out.execute(self.O, WO, self.out), gemm, "flop", "tensor", 1),
+        ]
+
+    def __call__(self, Q, K, V, WQ, WK, WV, WO):
+        for n in self.nodes(Q, K, V, WQ, WK, WV, WO):
+            n[1]()
+        return self.out
+
+    def flops(self) -> int:
+        s, a, h, d = self.s, self.a, self.h, self.d
+        return 4 * (2 * s * a * h * d) + 2 * (2 * h * s * s * d) + 2 * (2 * h * s * s)

@@ -12,19 +12,13 @@ int cuda_fail(cudaError_t e, const char* what) {
     return fail(TRA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-// A map supports 4-wide vector loads when its innermost label is the operand's
-// innermost memory dimension with a block-local extent divisible by 4: then every
-// 4 consecutive composite indices starting at a multiple of 4 are contiguous and
-// 16-byte (fp32) / 8-byte (bf16) aligned, given an aligned base pointer.
-bool vec4_ok(const RoleMap& m, const void* base, int bf16) {
-    if (m.n == 0 || m.t[0].div != 1 || m.t[0].loc_stride != 1) return false;
-    if (m.t[0].sub % 4 != 0 || m.t[0].ext % 4 != 0) return false;
-    return ((uintptr_t)base % (bf16 ? 8 : 16)) == 0;
-}
-
-void set_load_modes(SemiringParams& sp, int bf16) {
-    sp.x_mode = vec4_ok(sp.xk, sp.x, bf16) ? 1 : (vec4_ok(sp.xm, sp.x, bf16) ? 2 : 0);
-    sp.y_mode = vec4_ok(sp.yn, sp.y, bf16) ? 2 : (vec4_ok(sp.yk, sp.y, bf16) ? 1 : 0);
+// Vector loads only where the plan-time scan proved every 4-wide address aligned and
+// contiguous, and the base pointer is 16-byte (fp32) / 8-byte (bf16) aligned.
+void set_load_modes(SemiringParams& sp, int bf16, const int flags[4]) {
+    const size_t a = bf16 ? 8 : 16;
+    const bool xa = (uintptr_t)sp.x % a == 0, ya = (uintptr_t)sp.y % a == 0;
+    sp.x_mode = xa && flags[0] ? 1 : (xa && flags[1] ? 2 : 0);
+    sp.y_mode = ya && flags[2] ? 2 : (ya && flags[3] ? 1 : 0);
 }
 
 SemiringParams semiring_params(const Plan& p, const void* x, const void* y, void* z) {
@@ -55,7 +49,7 @@ SemiringParams semiring_params(const Plan& p, const void* x, const void* y, void
     sp.x_mcontig = affine_stride(sp.xm) == 1;
     sp.y_ncontig = affine_stride(sp.yn) == 1;
     sp.y_kcontig = affine_stride(sp.yk) == 1;
-    set_load_modes(sp, p.in_bf16);
+    set_load_modes(sp, p.in_bf16, p.vec_flags);
     return sp;
 }
 
@@ -126,7 +120,9 @@ int execute_literal(const Plan& p, const void* x, const void* y, void* z, void* 
     sp.out_bf16 = 0;
     sp.x_kcontig = affine_stride(sp.xk) == 1;
     sp.y_kcontig = affine_stride(sp.yk) == 1;
-    set_load_modes(sp, p.in_bf16);
+    int flags[4];
+    scan_vec_flags(sp.xb, sp.xm, sp.xk, sp.yb, sp.yn, sp.yk, sp.nb, sp.M, sp.N, sp.K, flags);
+    set_load_modes(sp, p.in_bf16, flags);
     cudaError_t e = launch_semiring(sp, s);
     if (e != cudaSuccess) return cuda_fail(e, "literal join");
     CombineParams cp;
@@ -164,7 +160,7 @@ int execute_plan(const Plan& p, const void* x, const void* y, void* z, void* ws,
                 sp.op = kMul;
                 sp.xnorm = xn;
                 sp.ynorm = yn;
-                set_load_modes(sp, 0);
+                set_load_modes(sp, 0, p.vec_flags);
             }
             e = launch_semiring(sp, s);
             break;
@@ -193,7 +189,7 @@ int execute_plan(const Plan& p, const void* x, const void* y, void* z, void* ws,
             sp.y_raw = y;
             sp.x = ex;
             sp.y = ey;
-            set_load_modes(sp, 0);
+            set_load_modes(sp, 0, p.vec_flags);
             sp.rowmax = rmax;
             sp.colmax = cmax;
             sp.op = kMul;

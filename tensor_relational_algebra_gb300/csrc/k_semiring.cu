@@ -188,9 +188,10 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
     const uint32_t m0 = tm * BM, n0 = tn * BN;
 
     if (tid < BM) {
-        rowX[tid] = role_offset(p.xb, b) + role_offset(p.xm, min(m0 + tid, p.M - 1));
+        rowX[tid] = role_offset(p.xb, b) + role_offset(p.xm, clamp_row(m0 + tid, p.M, p.x_mode == kLoadVecMN));
     } else {
-        colY[tid - BM] = role_offset(p.yb, b) + role_offset(p.yn, min(n0 + (tid - BM), p.N - 1));
+        colY[tid - BM] =
+            role_offset(p.yb, b) + role_offset(p.yn, clamp_row(n0 + (tid - BM), p.N, p.y_mode == kLoadVecMN));
     }
     if (tid < BK) kX[0][tid] = role_offset(p.xk, min((uint32_t)tid, p.K - 1));
     else if (tid < 2 * BK) kY[0][tid - BK] = role_offset(p.yk, min((uint32_t)(tid - BK), p.K - 1));

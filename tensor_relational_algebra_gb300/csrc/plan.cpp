@@ -305,7 +305,46 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
             p->ws_bytes = align256(nb * p->ext[kM] * 4) + align256(nb * p->ext[kN] * 4);
         }
     }
+    if (!p->unary && p->kernel != TRA_KERNEL_TC_BF16 && p->kernel != TRA_KERNEL_ELEMENTWISE)
+        scan_vec_flags(role_map(*p, p->X, kBatch), role_map(*p, p->X, kM), role_map(*p, p->X, kK),
+                       role_map(*p, p->Y, kBatch), role_map(*p, p->Y, kN), role_map(*p, p->Y, kK),
+                       (uint32_t)p->ext[kBatch], (uint32_t)p->ext[kM], (uint32_t)p->ext[kN], (uint32_t)p->ext[kK],
+                       p->vec_flags);
     return TRA_OK;
+}
+
+namespace {
+
+bool groups_of_four(const RoleMap& m, uint32_t ext) {
+    if (ext % 4) return false;
+    for (uint32_t i = 0; i < ext; i += 4) {
+        const int64_t o = role_offset(m, i);
+        if (o % 4) return false;
+        for (uint32_t c = 1; c < 4; ++c)
+            if (role_offset(m, i + c) != o + c) return false;
+    }
+    return true;
+}
+
+bool all_multiples_of_four(const RoleMap& m, uint32_t ext) {
+    for (uint32_t i = 0; i < ext; ++i)
+        if (role_offset(m, i) % 4) return false;
+    return true;
+}
+
+}  // namespace
+
+void scan_vec_flags(const RoleMap& xb, const RoleMap& xm, const RoleMap& xk, const RoleMap& yb, const RoleMap& yn,
+                    const RoleMap& yk, uint32_t nb, uint32_t M, uint32_t N, uint32_t K, int flags[4]) {
+    const bool xb4 = all_multiples_of_four(xb, nb), yb4 = all_multiples_of_four(yb, nb);
+    const bool xk_in = xk.n > 0 && xk.t[0].div == 1 && xk.t[0].loc_stride == 1;
+    const bool xm_in = xm.n > 0 && xm.t[0].div == 1 && xm.t[0].loc_stride == 1;
+    const bool yn_in = yn.n > 0 && yn.t[0].div == 1 && yn.t[0].loc_stride == 1;
+    const bool yk_in = yk.n > 0 && yk.t[0].div == 1 && yk.t[0].loc_stride == 1;
+    flags[0] = xb4 && xk_in && groups_of_four(xk, K) && all_multiples_of_four(xm, M);
+    flags[1] = xb4 && xm_in && groups_of_four(xm, M) && all_multiples_of_four(xk, K);
+    flags[2] = yb4 && yn_in && groups_of_four(yn, N) && all_multiples_of_four(yk, K);
+    flags[3] = yb4 && yk_in && groups_of_four(yk, K) && all_multiples_of_four(yn, N);
 }
 
 // Join tuples in canonical order: Z key row-major, then the contracted labels' key

@@ -37,6 +37,8 @@ struct Plan {
     int in_bf16 = 0, out_bf16 = 0;
     int literal = 0;
     int sqdiff_expand = 0;
+    // vector-load eligibility of the semiring kernel's operands (host scan, see scan_vec_flags)
+    int vec_flags[4] = {0, 0, 0, 0};  // X along K, X along M, Y along N, Y along K
     bool unary = false;
 
     int n_labels = 0;
@@ -76,5 +78,13 @@ void tc_free(TcPlan* t);
 int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_t s);
 
 uint64_t align256(uint64_t v);
+
+// Exhaustive host check of the semiring kernel's 4-wide loads: an operand may load
+// 4 consecutive indices of a role at once only if every 4-aligned group of that role
+// maps to 4 contiguous elements at a multiple of 4, and every other offset that is
+// added to it (the other role, the batch) is a multiple of 4.  flags: X along K,
+// X along M, Y along N, Y along K.
+void scan_vec_flags(const RoleMap& xb, const RoleMap& xm, const RoleMap& xk, const RoleMap& yb, const RoleMap& yn,
+                    const RoleMap& yk, uint32_t nb, uint32_t M, uint32_t N, uint32_t K, int flags[4]);
 
 }  // namespace tra

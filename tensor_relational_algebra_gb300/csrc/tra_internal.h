@@ -60,6 +60,14 @@ TRA_HD int64_t role_offset(const RoleMap& r, uint32_t idx) {
     return off;
 }
 
+// Row index a tile uses for loads: itself when in range; past the end, the last row
+// (scalar loader) or the start of the last 4-aligned group (vector loader), so a
+// clamped row keeps the vector loader's alignment.
+TRA_HD uint32_t clamp_row(uint32_t idx, uint32_t ext, bool vec) {
+    if (idx < ext) return idx;
+    return vec ? ((ext - 1u) & ~3u) : ext - 1u;
+}
+
 // Stride of consecutive composite indices when the whole run [idx, idx+len) stays
 // affine in this operand: returns the element stride, or 0 when not affine.
 inline int64_t affine_stride(const RoleMap& r) {
