@@ -83,13 +83,27 @@ static int build_shape(or_shape* s, int n_labels, const int64_t* bounds, int rx,
     return 0;
 }
 
-/* One output element: idx[] holds the value of every output label. */
+/* One output element: idx[] holds the value of every output label.  The contracted
+ * tuples are visited in row-major order (an odometer over the contracted labels, the
+ * last one fastest); the operand offsets follow the odometer incrementally. */
 static double eval_one(const or_shape* s, int64_t* idx, const double* X, const double* Y, int op, int agg,
                        double alpha) {
-    int64_t n_ctr = 1;
-    for (int c = 0; c < s->n_c; ++c) n_ctr *= s->bounds[s->lc[c]];
     int unary = s->ry < 0 || Y == NULL;
-    double acc, m = -INFINITY;
+    int64_t ox0 = 0, oy0 = 0;
+    for (int i = 0; i < s->rz; ++i) {
+        int l = s->lz[i];
+        ox0 += idx[l] * s->sx[l];
+        oy0 += idx[l] * s->sy[l];
+    }
+    int64_t n_outer = 1, n_inner = 1, sxi = 0, syi = 0;
+    if (s->n_c > 0) {
+        int li = s->lc[s->n_c - 1];
+        n_inner = s->bounds[li];
+        sxi = s->sx[li];
+        syi = s->sy[li];
+        for (int c = 0; c < s->n_c - 1; ++c) n_outer *= s->bounds[s->lc[c]];
+    }
+    double acc = 0.0, m = -INFINITY;
     int pass_count = (agg == OR_AGG_LSE) ? 2 : 1;
     for (int pass = 0; pass < pass_count; ++pass) {
         if (agg == OR_AGG_SUM || agg == OR_AGG_NONE) acc = 0.0;
@@ -97,22 +111,27 @@ static double eval_one(const or_shape* s, int64_t* idx, const double* X, const d
         else if (agg == OR_AGG_MIN) acc = INFINITY;
         else acc = (pass == 0) ? -INFINITY : 0.0;
         for (int c = 0; c < s->n_c; ++c) idx[s->lc[c]] = 0;
-        for (int64_t t = 0; t < n_ctr; ++t) {
-            int64_t ox = 0, oy = 0;
-            for (int l = 0; l < s->n_labels; ++l) { ox += idx[l] * s->sx[l]; oy += idx[l] * s->sy[l]; }
-            double v = unary ? X[ox] : apply_op(op, X[ox], Y[oy]);
-            switch (agg) {
-                case OR_AGG_SUM: case OR_AGG_NONE: acc += v; break;
-                case OR_AGG_MAX: if (v > acc) acc = v; break;
-                case OR_AGG_MIN: if (v < acc) acc = v; break;
-                default:
-                    if (pass == 0) { if (v > acc) acc = v; }
-                    else acc += exp(v - m);
+        int64_t ox = ox0, oy = oy0;
+        for (int64_t t = 0; t < n_outer; ++t) {
+            for (int64_t u = 0; u < n_inner; ++u) {
+                double v = unary ? X[ox + u * sxi] : apply_op(op, X[ox + u * sxi], Y[oy + u * syi]);
+                switch (agg) {
+                    case OR_AGG_SUM: case OR_AGG_NONE: acc += v; break;
+                    case OR_AGG_MAX: if (v > acc) acc = v; break;
+                    case OR_AGG_MIN: if (v < acc) acc = v; break;
+                    default:
+                        if (pass == 0) { if (v > acc) acc = v; }
+                        else acc += exp(v - m);
+                }
             }
-            /* row-major odometer over the contracted labels */
-            for (int c = s->n_c - 1; c >= 0; --c) {
+            /* row-major odometer over the outer contracted labels */
+            for (int c = s->n_c - 2; c >= 0; --c) {
                 int l = s->lc[c];
+                ox += s->sx[l];
+                oy += s->sy[l];
                 if (++idx[l] < s->bounds[l]) break;
+                ox -= s->sx[l] * s->bounds[l];
+                oy -= s->sy[l] * s->bounds[l];
                 idx[l] = 0;
             }
         }

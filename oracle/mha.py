@@ -13,9 +13,13 @@ over d.  The softmax is written as two EinSums: L[h,s] = logsumexp_t Scores
 (an aggregation whose evaluation takes the row maximum first) and
 Attn = exp(Scores - L) (an element-wise join with a broadcast operand).
 
-Each node is evaluated in double by the oracle's EinSum and then rounded to the
-storage type the GPU chain uses: bf16 for tensors that feed a BF16 contraction
-(projections, Attn, O), fp32 for Scores, L and Output.
+Each node is evaluated in double and then rounded to the storage type the GPU
+chain uses: bf16 for tensors that feed a BF16 contraction (projections, Attn,
+O), fp32 for Scores, L and Output.  Two engines compute the nodes:
+  "loops" -- the oracle's nested-loop EinSum (einsum_ref.c) for every node;
+  "blas"  -- the contractions as a library matmul (numpy float64 einsum) and the
+             softmax nodes as numpy reductions, for sizes the loops cannot reach
+             in seconds; pinned against "loops" on small shapes in the tests.
 """
 from __future__ import annotations
 
@@ -25,28 +29,48 @@ from .einsum import einsum
 from .rounding import to_bf16, to_f32
 
 
-def projections(Q, K, V, WQ, WK, WV):
-    qp = to_bf16(einsum("sa,ahd->shd", Q, WQ))
-    kp = to_bf16(einsum("sa,ahd->shd", K, WK))
-    vp = to_bf16(einsum("sa,ahd->shd", V, WV))
+def _contract(eq, X, Y, alpha, engine):
+    if engine == "loops":
+        return einsum(eq, X, Y, alpha=alpha)
+    return alpha * np.einsum(eq, np.asarray(X, np.float64), np.asarray(Y, np.float64), optimize=True)
+
+
+def _lse(S, engine):
+    if engine == "loops":
+        return einsum("hst->hs", S, agg="lse")
+    S = np.asarray(S, np.float64)
+    m = S.max(axis=-1)
+    return m + np.log(np.exp(S - m[..., None]).sum(axis=-1))
+
+
+def _expsub(S, L, engine):
+    if engine == "loops":
+        return einsum("hst,hs->hst", S, L, op="expsub", agg="none")
+    return np.exp(np.asarray(S, np.float64) - np.asarray(L, np.float64)[..., None])
+
+
+def projections(Q, K, V, WQ, WK, WV, engine="loops"):
+    qp = to_bf16(_contract("sa,ahd->shd", Q, WQ, 1.0, engine))
+    kp = to_bf16(_contract("sa,ahd->shd", K, WK, 1.0, engine))
+    vp = to_bf16(_contract("sa,ahd->shd", V, WV, 1.0, engine))
     return qp, kp, vp
 
 
-def attention_rows(qp_rows, kp, vp, WO, scale):
+def attention_rows(qp_rows, kp, vp, WO, scale, engine="loops"):
     """The chain from Scores on, for a set of query rows (all of s, or a sample)."""
-    S = to_f32(einsum("shd,thd->hst", qp_rows, kp, alpha=scale))
-    L = to_f32(einsum("hst->hs", S, agg="lse"))
-    A = to_bf16(einsum("hst,hs->hst", S, L, op="expsub", agg="none"))
-    O = to_bf16(einsum("hst,thd->shd", A, vp))
-    out = to_f32(einsum("shd,ahd->sa", O, WO))
+    S = to_f32(_contract("shd,thd->hst", qp_rows, kp, scale, engine))
+    L = to_f32(_lse(S, engine))
+    A = to_bf16(_expsub(S, L, engine))
+    O = to_bf16(_contract("hst,thd->shd", A, vp, 1.0, engine))
+    out = to_f32(_contract("shd,ahd->sa", O, WO, 1.0, engine))
     return {"S": S, "L": L, "A": A, "O": O, "out": out}
 
 
-def chain(Q, K, V, WQ, WK, WV, WO, rows=None):
+def chain(Q, K, V, WQ, WK, WV, WO, rows=None, engine="loops"):
     """Whole chain; ``rows`` restricts the query positions (sampled check)."""
     scale = 1.0 / np.sqrt(WQ.shape[2])
-    qp, kp, vp = projections(Q if rows is None else Q[rows], K, V, WQ, WK, WV)
-    res = attention_rows(qp, kp, vp, WO, scale)
+    qp, kp, vp = projections(Q if rows is None else Q[rows], K, V, WQ, WK, WV, engine)
+    res = attention_rows(qp, kp, vp, WO, scale, engine)
     res.update({"Qp": qp, "Kp": kp, "Vp": vp})
     return res
 

@@ -19,6 +19,21 @@ void set_load_modes(SemiringParams& sp, int bf16, const int flags[4]) {
     const bool xa = (uintptr_t)sp.x % a == 0, ya = (uintptr_t)sp.y % a == 0;
     sp.x_mode = xa && flags[0] ? 1 : (xa && flags[1] ? 2 : 0);
     sp.y_mode = ya && flags[2] ? 2 : (ya && flags[3] ? 1 : 0);
+    // single-label contracted composite: the kernel divides by the block extent with a
+    // multiply-high instead of walking the role map
+    auto simple = [&](const RoleMap& m) { return m.n == 1 && m.t[0].div == 1 && m.t[0].ext == sp.K; };
+    sp.xk_simple = simple(sp.xk);
+    sp.yk_simple = simple(sp.yk);
+    if (sp.xk_simple) {
+        sp.xk_sub = FastDiv(sp.xk.t[0].sub);
+        sp.xk_ks = sp.xk.t[0].key_stride;
+        sp.xk_ls = sp.xk.t[0].loc_stride;
+    }
+    if (sp.yk_simple) {
+        sp.yk_sub = FastDiv(sp.yk.t[0].sub);
+        sp.yk_ks = sp.yk.t[0].key_stride;
+        sp.yk_ls = sp.yk.t[0].loc_stride;
+    }
 }
 
 SemiringParams semiring_params(const Plan& p, const void* x, const void* y, void* z) {

@@ -163,6 +163,23 @@ __device__ __noinline__ float lse_fallback(const SemiringParams& p, uint32_t b, 
                      : direct_lse<float>(p, p.x_raw, p.y_raw, xo, yo);
 }
 
+// offset of contracted index k in X / Y: one multiply-high division when the contracted
+// composite is a single label, the general role map otherwise
+__device__ __forceinline__ int64_t koff_x(const SemiringParams& p, uint32_t k) {
+    if (p.xk_simple) {
+        const uint32_t q = fdiv(k, p.xk_sub);
+        return (int64_t)q * p.xk_ks + (int64_t)(k - q * p.xk_sub.d) * p.xk_ls;
+    }
+    return role_offset(p.xk, k);
+}
+__device__ __forceinline__ int64_t koff_y(const SemiringParams& p, uint32_t k) {
+    if (p.yk_simple) {
+        const uint32_t q = fdiv(k, p.yk_sub);
+        return (int64_t)q * p.yk_ks + (int64_t)(k - q * p.yk_sub.d) * p.yk_ls;
+    }
+    return role_offset(p.yk, k);
+}
+
 // shared-memory index of (k, row) in the unpacked [k][row] or packed [k/2][row][k%2] layout
 template <bool P>
 __device__ __forceinline__ int sidx(int k, int r) {
@@ -176,7 +193,6 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
     __shared__ __align__(16) float Xs[2][BK * BM];
     __shared__ __align__(16) float Ys[2][BK * BN];
     __shared__ int64_t rowX[BM], colY[BN];
-    __shared__ int64_t kX[2][BK], kY[2][BK];
 
     const int tid = threadIdx.x;
     const uint32_t tiles_m = (p.M + BM - 1) / BM, tiles_n = (p.N + BN - 1) / BN;
@@ -193,15 +209,13 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
         colY[tid - BM] =
             role_offset(p.yb, b) + role_offset(p.yn, clamp_row(n0 + (tid - BM), p.N, p.y_mode == kLoadVecMN));
     }
-    if (tid < BK) kX[0][tid] = role_offset(p.xk, min((uint32_t)tid, p.K - 1));
-    else if (tid < 2 * BK) kY[0][tid - BK] = role_offset(p.yk, min((uint32_t)(tid - BK), p.K - 1));
     __syncthreads();
 
     const int xmode = p.x_mode, ymode = p.y_mode;
     float rx[8], ry[8];
 
-    // ---- global -> registers for the K-tile starting at k0 (offsets in kX/kY[buf])
-    auto load = [&](int buf, uint32_t k0) {
+    // ---- global -> registers for the K-tile starting at k0 (each thread maps its own k)
+    auto load = [&](uint32_t k0) {
         const int kv = (int)min((uint32_t)BK, p.K - k0);
         const float px = S::pad_x(), py = S::pad_y();
         if (xmode == kLoadVecK) {
@@ -209,7 +223,7 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int k = ((tid >> 7) + 2 * i) * 4;
-                float4 v = k < kv ? ld4<TIn>(p.x, rowX[m] + kX[buf][k]) : make_float4(px, px, px, px);
+                float4 v = k < kv ? ld4<TIn>(p.x, rowX[m] + koff_x(p, k0 + k)) : make_float4(px, px, px, px);
                 rx[4 * i] = v.x, rx[4 * i + 1] = v.y, rx[4 * i + 2] = v.z, rx[4 * i + 3] = v.w;
             }
         } else if (xmode == kLoadVecMN) {
@@ -217,7 +231,7 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int k = (tid >> 5) + 8 * i;
-                float4 v = k < kv ? ld4<TIn>(p.x, rowX[m] + kX[buf][k]) : make_float4(px, px, px, px);
+                float4 v = k < kv ? ld4<TIn>(p.x, rowX[m] + koff_x(p, k0 + k)) : make_float4(px, px, px, px);
                 rx[4 * i] = v.x, rx[4 * i + 1] = v.y, rx[4 * i + 2] = v.z, rx[4 * i + 3] = v.w;
             }
         } else {
@@ -225,7 +239,7 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int k = (tid >> 7) + 2 * i;
-                rx[i] = k < kv ? ld1<TIn>(p.x, rowX[m] + kX[buf][k]) : px;
+                rx[i] = k < kv ? ld1<TIn>(p.x, rowX[m] + koff_x(p, k0 + k)) : px;
             }
         }
         if (ymode == kLoadVecMN) {
@@ -234,7 +248,7 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
             for (int i = 0; i < 2; ++i) {
                 // packed layout: rows 2*kp and 2*kp+1; unpacked: rows kk and kk+8
                 const int k = P ? 2 * (tid >> 5) + i : (tid >> 5) + 8 * i;
-                float4 v = k < kv ? ld4<TIn>(p.y, colY[n] + kY[buf][k]) : make_float4(py, py, py, py);
+                float4 v = k < kv ? ld4<TIn>(p.y, colY[n] + koff_y(p, k0 + k)) : make_float4(py, py, py, py);
                 ry[4 * i] = v.x, ry[4 * i + 1] = v.y, ry[4 * i + 2] = v.z, ry[4 * i + 3] = v.w;
             }
         } else if (ymode == kLoadVecK) {
@@ -242,7 +256,7 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int k = ((tid >> 7) + 2 * i) * 4;
-                float4 v = k < kv ? ld4<TIn>(p.y, colY[n] + kY[buf][k]) : make_float4(py, py, py, py);
+                float4 v = k < kv ? ld4<TIn>(p.y, colY[n] + koff_y(p, k0 + k)) : make_float4(py, py, py, py);
                 ry[4 * i] = v.x, ry[4 * i + 1] = v.y, ry[4 * i + 2] = v.z, ry[4 * i + 3] = v.w;
             }
         } else {
@@ -250,7 +264,7 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int k = (tid >> 7) + 2 * i;
-                ry[i] = k < kv ? ld1<TIn>(p.y, colY[n] + kY[buf][k]) : py;
+                ry[i] = k < kv ? ld1<TIn>(p.y, colY[n] + koff_y(p, k0 + k)) : py;
             }
         }
     };
@@ -332,7 +346,7 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
         for (int j = 0; j < 8; ++j) acc[i][j] = S::init();
 
     const int ty = tid >> 4, tx = tid & 15;
-    load(0, 0);
+    load(0);
     store(0);
     __syncthreads();
 
@@ -340,20 +354,16 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
     for (uint32_t kt = 0; kt < nkt; ++kt) {
         const int buf = kt & 1;
         const bool has_next = kt + 1 < nkt;
-        if (has_next) {
-            const uint32_t k1 = (kt + 1) * BK;
-            if (tid < BK) kX[buf ^ 1][tid] = role_offset(p.xk, min(k1 + tid, p.K - 1));
-            else if (tid < 2 * BK) kY[buf ^ 1][tid - BK] = role_offset(p.yk, min(k1 + tid - BK, p.K - 1));
-        }
-        __syncthreads();
-        if (has_next) load(buf ^ 1, (kt + 1) * BK);
+        // one barrier per K-tile: this tile computes from buf while the next one is
+        // loaded into registers and then stored to buf ^ 1
+        if (has_next) load((kt + 1) * BK);
         const float* xs = Xs[buf];
         const float* ys = Ys[buf];
         if constexpr (P) {
-#pragma unroll
+#pragma unroll 2
             for (int kp = 0; kp < BK / 2; ++kp) {
                 // x pairs for rows ty*4..+3 and 64+ty*4..+3; y pairs for columns g*32 + tx*2 + {0,1}
-                uint64_t xa[8], yb[8];
+                uint64_t xa[8];
                 const ulonglong2* xr0 = reinterpret_cast<const ulonglong2*>(&xs[((kp * BM + ty * 4) << 1)]);
                 const ulonglong2* xr1 = reinterpret_cast<const ulonglong2*>(&xs[((kp * BM + 64 + ty * 4) << 1)]);
                 const ulonglong2 q0 = xr0[0], q1 = xr0[1], q2 = xr1[0], q3 = xr1[1];
@@ -361,16 +371,17 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
                 xa[4] = q2.x, xa[5] = q2.y, xa[6] = q3.x, xa[7] = q3.y;
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
+                    // one group of two y pairs at a time keeps fewer values live
                     const ulonglong2 w = *reinterpret_cast<const ulonglong2*>(&ys[((kp * BN + g * 32 + tx * 2) << 1)]);
-                    yb[2 * g] = w.x, yb[2 * g + 1] = w.y;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        S::step2(acc[i][2 * g], xa[i], w.x);
+                        S::step2(acc[i][2 * g + 1], xa[i], w.y);
+                    }
                 }
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) S::step2(acc[i][j], xa[i], yb[j]);
             }
         } else {
-#pragma unroll
+#pragma unroll 8
             for (int k = 0; k < BK; ++k) {
                 const float4 a0 = *reinterpret_cast<const float4*>(&xs[k * BM + ty * 4]);
                 const float4 a1 = *reinterpret_cast<const float4*>(&xs[k * BM + 64 + ty * 4]);

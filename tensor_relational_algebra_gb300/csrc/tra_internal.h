@@ -92,6 +92,10 @@ struct SemiringParams {
     int32_t x_kcontig, x_mcontig, y_ncontig, y_kcontig;
     // loader of each operand: 0 generic gather, 1 float4 along K, 2 float4 along M (X) / N (Y)
     int32_t x_mode, y_mode;
+    // contracted composite made of one label (div 1): offset = (k / sub) * ks + (k % sub) * ls
+    int32_t xk_simple, yk_simple;
+    FastDiv xk_sub, yk_sub;
+    int64_t xk_ks, xk_ls, yk_ks, yk_ls;
     // logsumexp factored form: the operands are exp(x - rowmax) and exp(y - colmax)
     // (fp32 scratch), and the epilogue adds rowmax + colmax + log(sum).
     const float* rowmax;  // [nb * M] or null

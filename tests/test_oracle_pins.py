@@ -276,3 +276,16 @@ def test_attention_chain_against_plain_softmax():
     rows = np.array([0, 5, 15])
     rr = mha.chain(Q, K, V, WQ, WK, WV, WO, rows=rows)
     np.testing.assert_array_equal(rr["out"], r["out"][rows])
+
+
+def test_attention_engines_agree():
+    # the library-matmul engine (used at full size) against the nested-loop engine
+    s, a, h, d = 24, 32, 2, 16
+    Q, K, V = [datagen.bf16_bits_to_f32(datagen.normal_bf16((s, a), 1, t)) for t in range(3)]
+    WQ, WK, WV, WO = [datagen.bf16_bits_to_f32(datagen.normal_bf16((a, h, d), 1, 3 + t, 0, 0.2)) for t in range(4)]
+    lo = mha.chain(Q, K, V, WQ, WK, WV, WO, engine="loops")
+    bl = mha.chain(Q, K, V, WQ, WK, WV, WO, engine="blas")
+    for k in ("Qp", "Kp", "Vp", "A", "O"):
+        assert np.mean(lo[k] == bl[k]) > 0.99, k  # bf16 roundings agree except at rare ties
+    np.testing.assert_allclose(bl["S"], lo["S"], rtol=1e-2, atol=1e-3)
+    assert np.abs(bl["out"] - lo["out"]).max() <= 1e-2 * np.abs(lo["out"]).max()
