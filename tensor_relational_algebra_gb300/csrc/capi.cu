@@ -14,11 +14,12 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 // Vector loads only where the plan-time scan proved every 4-wide address aligned and
 // contiguous, and the base pointer is 16-byte (fp32) / 8-byte (bf16) aligned.
-void set_load_modes(SemiringParams& sp, int bf16, const int flags[4]) {
+void set_load_modes(SemiringParams& sp, int bf16, const int flags[5]) {
     const size_t a = bf16 ? 8 : 16;
     const bool xa = (uintptr_t)sp.x % a == 0, ya = (uintptr_t)sp.y % a == 0;
     sp.x_mode = xa && flags[0] ? 1 : (xa && flags[1] ? 2 : 0);
     sp.y_mode = ya && flags[2] ? 2 : (ya && flags[3] ? 1 : 0);
+    sp.z_vec4 = flags[4] && (uintptr_t)sp.z % (sp.out_bf16 ? 8 : 16) == 0;
     // single-label contracted composite: the kernel divides by the block extent with a
     // multiply-high instead of walking the role map
     auto simple = [&](const RoleMap& m) { return m.n == 1 && m.t[0].div == 1 && m.t[0].ext == sp.K; };
@@ -135,8 +136,8 @@ int execute_literal(const Plan& p, const void* x, const void* y, void* z, void* 
     sp.out_bf16 = 0;
     sp.x_kcontig = affine_stride(sp.xk) == 1;
     sp.y_kcontig = affine_stride(sp.yk) == 1;
-    int flags[4];
-    scan_vec_flags(sp.xb, sp.xm, sp.xk, sp.yb, sp.yn, sp.yk, sp.nb, sp.M, sp.N, sp.K, flags);
+    int flags[5];
+    scan_vec_flags(sp.xb, sp.xm, sp.xk, sp.yb, sp.yn, sp.yk, sp.zb, sp.zm, sp.zn, sp.nb, sp.M, sp.N, sp.K, flags);
     set_load_modes(sp, p.in_bf16, flags);
     cudaError_t e = launch_semiring(sp, s);
     if (e != cudaSuccess) return cuda_fail(e, "literal join");

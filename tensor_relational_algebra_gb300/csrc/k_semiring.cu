@@ -399,30 +399,65 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
         __syncthreads();
     }
 
-    // ---- epilogue: output offsets through Z's relation layout
-    const int64_t zb = role_offset(p.zb, b);
+    // ---- epilogue: output offsets through Z's relation layout.  The row / column offset
+    // tables reuse rowX / colY (every thread is past its last load: the loop ends on a barrier).
+    if (tid < BM) {
+        rowX[tid] = role_offset(p.zb, b) + role_offset(p.zm, min(m0 + tid, p.M - 1));
+    } else {
+        colY[tid - BM] = role_offset(p.zn, min(n0 + (tid - BM), p.N - 1));
+    }
+    __syncthreads();
+    constexpr int G = P ? 2 : 4;  // consecutive output columns a thread owns
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int mi = (i < 4) ? ty * 4 + i : 64 + ty * 4 + (i - 4);
         const uint32_t m = m0 + mi;
         if (m >= p.M) continue;
-        const int64_t zrow = zb + role_offset(p.zm, m);
+        const int64_t zrow = rowX[mi];
         float rterm = 0.f;
         if (EPI == kEpiLse) rterm = p.rowmax[(uint64_t)b * p.M + m];
         if (EPI == kEpiSqExpand) rterm = p.xnorm[(uint64_t)b * p.M + m];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int nj = P ? (j >> 1) * 32 + tx * 2 + (j & 1) : ((j < 4) ? tx * 4 + j : 64 + tx * 4 + (j - 4));
-            const uint32_t n = n0 + nj;
-            if (n >= p.N) continue;
-            float v = acc[i][j];
-            if (EPI == kEpiLse) {
-                if (v > 1e-30f) v = rterm + p.colmax[(uint64_t)b * p.N + n] + logf(v);
-                else v = lse_fallback(p, b, m, n);  // every exp-shifted product underflowed
-            } else if (EPI == kEpiSqExpand) {
-                v = fmaxf(rterm + p.ynorm[(uint64_t)b * p.N + n] - 2.f * v, 0.f);
+        for (int g = 0; g < 8 / G; ++g) {
+            const int nb = P ? g * 32 + tx * 2 : g * 64 + tx * 4;
+            const uint32_t n = n0 + nb;
+            float v[G];
+#pragma unroll
+            for (int c = 0; c < G; ++c) {
+                float a = acc[i][g * G + c];
+                if (EPI == kEpiLse) {
+                    if (n + c < p.N) {
+                        if (a > 1e-30f) a = rterm + p.colmax[(uint64_t)b * p.N + n + c] + logf(a);
+                        else a = lse_fallback(p, b, m, n + c);  // every exp-shifted product underflowed
+                    }
+                } else if (EPI == kEpiSqExpand) {
+                    if (n + c < p.N) a = fmaxf(rterm + p.ynorm[(uint64_t)b * p.N + n + c] - 2.f * a, 0.f);
+                }
+                v[c] = p.alpha * a;
             }
-            st_out(p.z, zrow + role_offset(p.zn, n), p.alpha * v, p.out_bf16);
+            if (p.z_vec4 && n + G - 1 < p.N) {
+                const int64_t off = zrow + colY[nb];
+                if (p.out_bf16) {
+                    uint32_t w[G / 2];
+#pragma unroll
+                    for (int h = 0; h < G / 2; ++h) {
+                        const __nv_bfloat162 pr = __floats2bfloat162_rn(v[2 * h], v[2 * h + 1]);
+                        w[h] = *reinterpret_cast<const uint32_t*>(&pr);
+                    }
+                    if (G == 4)
+                        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.z) + off) = make_uint2(w[0], w[G / 2 - 1]);
+                    else
+                        *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(p.z) + off) = w[0];
+                } else if (G == 4) {
+                    *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.z) + off) = make_float4(v[0], v[1 % G], v[2 % G], v[3 % G]);
+                } else {
+                    *reinterpret_cast<float2*>(reinterpret_cast<float*>(p.z) + off) = make_float2(v[0], v[1 % G]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < G; ++c)
+                    if (n + c < p.N) st_out(p.z, zrow + colY[nb + c], v[c], p.out_bf16);
+            }
         }
     }
 }
@@ -468,6 +503,14 @@ __global__ void semiring_simple(const __grid_constant__ SemiringParams p) {
 }
 
 // ---------------------------------------------------------------- factored-logsumexp / norm preparation
+__device__ __forceinline__ int64_t prep_koff(const LsePrepParams& p, uint32_t k) {
+    if (p.k_simple) {
+        const uint32_t q = fdiv(k, p.k_sub);
+        return (int64_t)q * p.k_ks + (int64_t)(k - q * p.k_sub.d) * p.k_ls;
+    }
+    return role_offset(p.k, k);
+}
+
 // mode 0: per row, max over the contracted range, then dst = exp(v - max) for every element.
 // mode 1: per row, sum of squares over the contracted range (squared-distance expansion).
 template <typename TIn>
@@ -482,7 +525,7 @@ __global__ void lse_prep_kernel(const __grid_constant__ LsePrepParams p, int row
         const int64_t base = role_offset(p.b, b) + role_offset(p.r, r);
         float m = p.mode == 0 ? -INFINITY : 0.f;
         for (uint32_t k = lane; k < p.K; k += 32) {
-            float v = ld1<TIn>(p.src, base + role_offset(p.k, k));
+            float v = ld1<TIn>(p.src, base + prep_koff(p, k));
             m = p.mode == 0 ? fmaxf(m, v) : fmaf(v, v, m);
         }
         for (int o = 16; o; o >>= 1) {
@@ -492,24 +535,37 @@ __global__ void lse_prep_kernel(const __grid_constant__ LsePrepParams p, int row
         if (lane == 0) p.rmax[warp] = m;
         if (p.mode == 0)
             for (uint32_t k = lane; k < p.K; k += 32) {
-                int64_t off = base + role_offset(p.k, k);
+                int64_t off = base + prep_koff(p, k);
                 p.dst[off] = expf(ld1<TIn>(p.src, off) - m);
             }
     } else {
-        // one thread per row (rows contiguous in memory): coalesced across the warp
-        const uint64_t row = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x;
-        if (row >= (uint64_t)p.nb * p.R) return;
-        const uint32_t r = row % p.R, b = row / p.R;
+        // rows contiguous in memory: 32 consecutive rows per CTA (one per lane, coalesced
+        // across the warp), the 8 warps split the contracted range, shared-memory reduction
+        __shared__ float red[8][32];
+        const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+        const uint64_t rows = (uint64_t)p.nb * p.R;
+        const uint64_t row = blockIdx.x * 32ull + lane;
+        const bool valid = row < rows;
+        const uint32_t r = valid ? (uint32_t)(row % p.R) : 0u, b = valid ? (uint32_t)(row / p.R) : 0u;
         const int64_t base = role_offset(p.b, b) + role_offset(p.r, r);
         float m = p.mode == 0 ? -INFINITY : 0.f;
-        for (uint32_t k = 0; k < p.K; ++k) {
-            float v = ld1<TIn>(p.src, base + role_offset(p.k, k));
-            m = p.mode == 0 ? fmaxf(m, v) : fmaf(v, v, m);
+        if (valid)
+            for (uint32_t k = w; k < p.K; k += 8) {
+                const float v = ld1<TIn>(p.src, base + prep_koff(p, k));
+                m = p.mode == 0 ? fmaxf(m, v) : fmaf(v, v, m);
+            }
+        red[w][lane] = m;
+        __syncthreads();
+        if (w == 0) {
+            for (int q = 1; q < 8; ++q) m = p.mode == 0 ? fmaxf(m, red[q][lane]) : m + red[q][lane];
+            red[0][lane] = m;
+            if (valid) p.rmax[row] = m;
         }
-        p.rmax[row] = m;
-        if (p.mode == 0)
-            for (uint32_t k = 0; k < p.K; ++k) {
-                int64_t off = base + role_offset(p.k, k);
+        __syncthreads();
+        m = red[0][lane];
+        if (p.mode == 0 && valid)
+            for (uint32_t k = w; k < p.K; k += 8) {
+                const int64_t off = base + prep_koff(p, k);
                 p.dst[off] = expf(ld1<TIn>(p.src, off) - m);
             }
     }
@@ -559,13 +615,19 @@ cudaError_t launch_semiring_simple(const SemiringParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_lse_prep(const LsePrepParams& p, cudaStream_t s) {
+cudaError_t launch_lse_prep(const LsePrepParams& pin, cudaStream_t s) {
+    LsePrepParams p = pin;
+    p.k_simple = p.k.n == 1 && p.k.t[0].div == 1 && p.k.t[0].ext == p.K;
+    if (p.k_simple) {
+        p.k_sub = FastDiv(p.k.t[0].sub);
+        p.k_ks = p.k.t[0].key_stride;
+        p.k_ls = p.k.t[0].loc_stride;
+    }
     const uint64_t rows = (uint64_t)p.nb * p.R;
     if (rows == 0) return cudaSuccess;
     // rows contiguous (the contracted index is not the fastest-moving one): thread per row
     const bool rpt = !(p.k.n > 0 && p.k.t[0].div == 1 && p.k.t[0].loc_stride == 1);
-    const uint64_t threads = rpt ? rows : rows * 32;
-    const unsigned blocks = (unsigned)((threads + 255) / 256);
+    const unsigned blocks = (unsigned)(rpt ? (rows + 31) / 32 : (rows * 32 + 255) / 256);
     if (p.in_bf16) lse_prep_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(p, rpt);
     else lse_prep_kernel<float><<<blocks, 256, 0, s>>>(p, rpt);
     return cudaGetLastError();

@@ -45,7 +45,7 @@ struct TcOpDev {
     int32_t mn_major;  // 1: innermost dimension is M (X) / N (Y); 0: innermost is K
     int32_t n_loads;   // TMA loads per stage (MN-major: one per 64 rows of M/N)
     int32_t role[5];
-    uint32_t div[5], mod[5];
+    FastDiv div[5], mod[5];  // coordinate along dimension j = (composite / div) % mod
 };
 
 struct TcParams {
@@ -160,13 +160,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void tile_coords(const TcOpDev& o, uint32_t cb, uint32_t cm, uint32_t cn, uint32_t ck,
-                                            int c[5]) {
+__device__ __forceinline__ int dim_coord(const TcOpDev& o, int j, uint32_t v) {
+    const uint32_t q = fdiv(v, o.div[j]);
+    return (int)(q - fdiv(q, o.mod[j]) * o.mod[j].d);
+}
+
+// Coordinates of the dimensions that do not move along K (batch and M or N): once per tile.
+__device__ __forceinline__ void fixed_coords(const TcOpDev& o, uint32_t cb, uint32_t cmn, int c[5]) {
 #pragma unroll
-    for (int j = 0; j < 5; ++j) {
-        const uint32_t v = o.role[j] == kBatch ? cb : (o.role[j] == kM ? cm : (o.role[j] == kN ? cn : ck));
-        c[j] = (int)((v / o.div[j]) % o.mod[j]);
-    }
+    for (int j = 0; j < 5; ++j) c[j] = o.role[j] == kK ? 0 : dim_coord(o, j, o.role[j] == kBatch ? cb : cmn);
+}
+
+// Coordinates of the contracted dimensions at composite K index ck: once per K step.
+__device__ __forceinline__ void k_coords(const TcOpDev& o, uint32_t ck, int c[5]) {
+#pragma unroll
+    for (int j = 0; j < 5; ++j) c[j] = o.role[j] == kK ? dim_coord(o, j, ck) : 0;
 }
 
 __device__ __forceinline__ void tile_of(const TcParams& p, uint32_t t, uint32_t& b, uint32_t& mt, uint32_t& nt) {
@@ -234,6 +242,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t b, mt, nt;
                 tile_of(p, t, b, mt, nt);
                 const uint32_t m0 = mt * kBlockM, n0 = nt * p.block_n;
+                // per load, the coordinates that stay fixed over the K loop (at most 2 loads of
+                // A and 4 of B per stage)
+                int fa[2][5], fbx[4][5];
+#pragma unroll
+                for (int l = 0; l < 2; ++l)
+                    if (l < p.a.n_loads) fixed_coords(p.a, b, m0 + 64u * l, fa[l]);
+#pragma unroll
+                for (int l = 0; l < 4; ++l)
+                    if (l < p.b.n_loads) fixed_coords(p.b, b, n0 + 64u * l, fbx[l]);
                 for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort, p.timeout_ns)) {
                         ok = false;
@@ -243,15 +260,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_expect_tx(fb, stage_bytes);
                     const uint32_t sa = base + stage * stage_bytes, sb = sa + p.a_bytes;
                     const uint32_t k0 = kb * kBlockK;
-                    int c[5];
-                    for (int l = 0; l < p.a.n_loads; ++l) {
-                        tile_coords(p.a, b, m0 + 64u * l, 0, k0, c);
-                        tma_load_5d(sa + 8192u * l, &map_a, fb, c);
-                    }
-                    for (int l = 0; l < p.b.n_loads; ++l) {
-                        tile_coords(p.b, b, 0, n0 + 64u * l, k0, c);
-                        tma_load_5d(sb + 8192u * l, &map_b, fb, c);
-                    }
+                    int ka[5], kbc[5], c[5];
+                    k_coords(p.a, k0, ka);
+                    k_coords(p.b, k0, kbc);
+#pragma unroll
+                    for (int l = 0; l < 2; ++l)
+                        if (l < p.a.n_loads) {
+#pragma unroll
+                            for (int j = 0; j < 5; ++j) c[j] = fa[l][j] + ka[j];
+                            tma_load_5d(sa + 8192u * l, &map_a, fb, c);
+                        }
+#pragma unroll
+                    for (int l = 0; l < 4; ++l)
+                        if (l < p.b.n_loads) {
+#pragma unroll
+                            for (int j = 0; j < 5; ++j) c[j] = fbx[l][j] + kbc[j];
+                            tma_load_5d(sb + 8192u * l, &map_b, fb, c);
+                        }
                     issued[stage] = true;
                     issued_phase[stage] = phase;
                     if (++stage == p.stages) {
@@ -523,8 +548,8 @@ bool operand_dims(const Plan& p, const Operand& t, int mn_role, uint32_t mn_tile
     }
     for (int j = 0; j < 5; ++j) {
         out.dev.role[j] = j < n ? out.dims[j].role : kK;
-        out.dev.div[j] = j < n ? out.dims[j].div : 1u;
-        out.dev.mod[j] = j < n ? out.dims[j].mod : 1u;
+        out.dev.div[j] = FastDiv(j < n ? out.dims[j].div : 1u);
+        out.dev.mod[j] = FastDiv(j < n ? out.dims[j].mod : 1u);
     }
     return true;
 }

@@ -308,6 +308,7 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
     if (!p->unary && p->kernel != TRA_KERNEL_TC_BF16 && p->kernel != TRA_KERNEL_ELEMENTWISE)
         scan_vec_flags(role_map(*p, p->X, kBatch), role_map(*p, p->X, kM), role_map(*p, p->X, kK),
                        role_map(*p, p->Y, kBatch), role_map(*p, p->Y, kN), role_map(*p, p->Y, kK),
+                       role_map(*p, p->Z, kBatch), role_map(*p, p->Z, kM), role_map(*p, p->Z, kN),
                        (uint32_t)p->ext[kBatch], (uint32_t)p->ext[kM], (uint32_t)p->ext[kN], (uint32_t)p->ext[kK],
                        p->vec_flags);
     return TRA_OK;
@@ -335,7 +336,8 @@ bool all_multiples_of_four(const RoleMap& m, uint32_t ext) {
 }  // namespace
 
 void scan_vec_flags(const RoleMap& xb, const RoleMap& xm, const RoleMap& xk, const RoleMap& yb, const RoleMap& yn,
-                    const RoleMap& yk, uint32_t nb, uint32_t M, uint32_t N, uint32_t K, int flags[4]) {
+                    const RoleMap& yk, const RoleMap& zb, const RoleMap& zm, const RoleMap& zn, uint32_t nb,
+                    uint32_t M, uint32_t N, uint32_t K, int flags[5]) {
     const bool xb4 = all_multiples_of_four(xb, nb), yb4 = all_multiples_of_four(yb, nb);
     const bool xk_in = xk.n > 0 && xk.t[0].div == 1 && xk.t[0].loc_stride == 1;
     const bool xm_in = xm.n > 0 && xm.t[0].div == 1 && xm.t[0].loc_stride == 1;
@@ -345,6 +347,8 @@ void scan_vec_flags(const RoleMap& xb, const RoleMap& xm, const RoleMap& xk, con
     flags[1] = xb4 && xm_in && groups_of_four(xm, M) && all_multiples_of_four(xk, K);
     flags[2] = yb4 && yn_in && groups_of_four(yn, N) && all_multiples_of_four(yk, K);
     flags[3] = yb4 && yk_in && groups_of_four(yk, K) && all_multiples_of_four(yn, N);
+    const bool zn_in = zn.n > 0 && zn.t[0].div == 1 && zn.t[0].loc_stride == 1;
+    flags[4] = zn_in && groups_of_four(zn, N) && all_multiples_of_four(zm, M) && all_multiples_of_four(zb, nb);
 }
 
 // Join tuples in canonical order: Z key row-major, then the contracted labels' key

@@ -38,7 +38,7 @@ struct Plan {
     int literal = 0;
     int sqdiff_expand = 0;
     // vector-load eligibility of the semiring kernel's operands (host scan, see scan_vec_flags)
-    int vec_flags[4] = {0, 0, 0, 0};  // X along K, X along M, Y along N, Y along K
+    int vec_flags[5] = {0, 0, 0, 0, 0};  // X along K, X along M, Y along N, Y along K, Z along N
     bool unary = false;
 
     int n_labels = 0;
@@ -83,8 +83,9 @@ uint64_t align256(uint64_t v);
 // 4 consecutive indices of a role at once only if every 4-aligned group of that role
 // maps to 4 contiguous elements at a multiple of 4, and every other offset that is
 // added to it (the other role, the batch) is a multiple of 4.  flags: X along K,
-// X along M, Y along N, Y along K.
+// X along M, Y along N, Y along K, Z along N (vector stores of the output).
 void scan_vec_flags(const RoleMap& xb, const RoleMap& xm, const RoleMap& xk, const RoleMap& yb, const RoleMap& yn,
-                    const RoleMap& yk, uint32_t nb, uint32_t M, uint32_t N, uint32_t K, int flags[4]);
+                    const RoleMap& yk, const RoleMap& zb, const RoleMap& zm, const RoleMap& zn, uint32_t nb,
+                    uint32_t M, uint32_t N, uint32_t K, int flags[5]);
 
 }  // namespace tra

@@ -92,6 +92,8 @@ struct SemiringParams {
     int32_t x_kcontig, x_mcontig, y_ncontig, y_kcontig;
     // loader of each operand: 0 generic gather, 1 float4 along K, 2 float4 along M (X) / N (Y)
     int32_t x_mode, y_mode;
+    // output: every 4-aligned group of 4 consecutive N indices is contiguous and 4-aligned
+    int32_t z_vec4;
     // contracted composite made of one label (div 1): offset = (k / sub) * ks + (k % sub) * ls
     int32_t xk_simple, yk_simple;
     FastDiv xk_sub, yk_sub;
@@ -116,6 +118,10 @@ struct LsePrepParams {
     uint32_t nb, R, K;
     int32_t in_bf16;
     int32_t mode;         // 0: row max + exp shift;  1: sum of squares (for sqdiff expansion)
+    // contracted composite made of one label (set by the launcher)
+    int32_t k_simple;
+    FastDiv k_sub;
+    int64_t k_ks, k_ls;
 };
 
 // Unary aggregation over the contracted labels (row reduction).
