@@ -150,6 +150,23 @@ int ein_repartition_cost(int rank, const int64_t* shape, const int32_t* src_d, c
  * TRA_ERR_TIMEOUT or TRA_ERR_CUDA. */
 int ein_status(tra_stream_t stream);
 
+/* ein_execute_sqdist_noalloc -- ein_execute for an fp32 squared-distance plan
+ * ("...:sqdiff:sum", expanded form) that needs no caller workspace.  The EinDecomp page
+ * has no counterpart: this entry point exists for callers that cannot allocate device
+ * memory on their path (memory owned by another allocator or a fixed budget, plugins
+ * that may not allocate, paths that must not pay for an allocation and the device
+ * synchronisation a free implies).  The row / column norms go to a fixed 1 MiB device
+ * array inside libtra.so that every GPU loading the library holds until process exit.
+ * in0/in1/out: as for ein_execute.  The first call on a device (with that device
+ * current) looks up the array's device address; make that first call before any
+ * stream capture.  All calls share the array: calls whose kernels may overlap on the
+ * GPU (unordered streams) race.  Nothing is allocated; no clearing is needed (every
+ * norm is rewritten before it is read).
+ * Errors: TRA_ERR_UNSUPPORTED (not an fp32 expanded squared-distance plan),
+ * TRA_ERR_WORKSPACE (norms need more than 1 MiB: use ein_execute), TRA_ERR_ARG,
+ * TRA_ERR_CUDA. */
+int ein_execute_sqdist_noalloc(tra_plan_t plan, const void* in0, const void* in1, void* out, tra_stream_t stream);
+
 /* ein_selftest_wait_timeout -- test hook for the bounded device waits: launches one
  * thread that waits on an mbarrier nothing arrives on, with the same bounded wait the
  * tensor-core kernel uses, giving up after timeout_ns.  A following ein_status() on
