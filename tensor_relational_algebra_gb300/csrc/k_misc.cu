@@ -160,6 +160,29 @@ __global__ void elementwise_kernel(const __grid_constant__ ElementwiseParams p) 
     }
     const int last = p.rank - 1;
     const int64_t xs = p.x_ls[last], ys = p.y_ls[last];
+    // fp32 operands, X contiguous along the run, Y contiguous or broadcast, everything
+    // 4-aligned: 16-byte loads, 4 outputs per lane per step
+    if (!p.in_bf16 && xs == 1 && (ys == 0 || ys == 1 || !p.y) && (p.I & 3) == 0 && (e & 3) == 0 &&
+        (xo & 3) == 0 && (ys != 1 || (yo & 3) == 0) && ((uintptr_t)p.x & 15) == 0 &&
+        (!p.y || ys != 1 || ((uintptr_t)p.y & 15) == 0) && ((uintptr_t)p.z & (p.out_bf16 ? 7 : 15)) == 0) {
+        const float* xr = reinterpret_cast<const float*>(p.x) + xo;
+        const float* yr = p.y ? reinterpret_cast<const float*>(p.y) + yo : nullptr;
+        const float yb = (p.y && ys == 0) ? yr[0] : 0.f;
+        for (uint32_t j = lane * 4; j < p.I; j += 128) {
+            const float4 xv = __ldcs(reinterpret_cast<const float4*>(xr + j));
+            const float4 yv = (p.y && ys == 1) ? __ldg(reinterpret_cast<const float4*>(yr + j)) : make_float4(yb, yb, yb, yb);
+            const float r0 = p.alpha * ew_op(p.op, xv.x, yv.x), r1 = p.alpha * ew_op(p.op, xv.y, yv.y);
+            const float r2 = p.alpha * ew_op(p.op, xv.z, yv.z), r3 = p.alpha * ew_op(p.op, xv.w, yv.w);
+            if (p.out_bf16) {
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(r0, r1), hi = __floats2bfloat162_rn(r2, r3);
+                __stcs(reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.z) + e + j),
+                       make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi)));
+            } else {
+                __stcs(reinterpret_cast<float4*>(reinterpret_cast<float*>(p.z) + e + j), make_float4(r0, r1, r2, r3));
+            }
+        }
+        return;
+    }
     for (uint32_t j = lane; j < p.I; j += 32) {
         const float x = ld_f(p.x, xo + (int64_t)j * xs, p.in_bf16);
         const float y = p.y ? ld_f(p.y, yo + (int64_t)j * ys, p.in_bf16) : 0.f;

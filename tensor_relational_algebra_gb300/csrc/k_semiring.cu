@@ -10,14 +10,16 @@
 // sub-tensor.  Every element is addressed through the relation layout
 // (RoleMap), so one kernel serves every binary EinSum and every partition vector.
 //
-// Per thread: an 8 x 8 register tile; K is staged through shared memory 16 at a
-// time (double-buffered, prefetched into registers during the math).  Operands
-// are loaded as float4 / 4 x bf16 when the layout makes 4 consecutive indices
-// contiguous, else gathered element by element.  The K tail is padded with
-// values whose join is the aggregation's identity, so the inner loop never
-// branches.  For max-plus / min-plus the inner step works on pairs of
-// consecutive k: one packed add (add.rn.f32x2) and one 3-input max/min per two
-// join tuples.
+// Per thread: an 8 x 8 register tile.  Two kernels share the tile mapping and the
+// epilogue:
+//  * semiring_async -- fp32 operands laid out K-contiguous (X) and N-contiguous (Y)
+//    in runs of 4: a 3-stage cp.async pipeline of 32-deep K tiles, no register
+//    staging, one barrier per tile;
+//  * semiring_tiled -- every other layout / bf16: 16-deep K tiles staged through
+//    registers (float4 / 4 x bf16 loads where the layout allows, gathers otherwise).
+// The K tail is padded with values whose join is the aggregation's identity, so the
+// inner loop never branches.  Tuples are taken in pairs of consecutive k: max-plus and
+// min-plus become two FADD and one 3-input FMNMX per two tuples.
 #include <cuda_bf16.h>
 
 #include <cfloat>
@@ -29,6 +31,8 @@ namespace tra {
 namespace {
 
 constexpr int BM = 128, BN = 128, BK = 16, NT = 256;
+constexpr int ABK = 32, ASTAGES = 3;  // async kernel: K-tile depth and pipeline stages
+constexpr size_t kAsyncSmem = (size_t)ASTAGES * (BM * ABK + ABK * BN) * sizeof(float);
 enum { kEpiPlain = 0, kEpiLse = 1, kEpiSqExpand = 2 };
 enum { kLoadGather = 0, kLoadVecK = 1, kLoadVecMN = 2 };
 
@@ -75,14 +79,6 @@ __device__ __forceinline__ float apply_op(int op, float x, float y) {
     }
 }
 
-// packed pair helpers
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ float lo_of(uint64_t v) { return __uint_as_float((uint32_t)v); }
-__device__ __forceinline__ float hi_of(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
@@ -94,47 +90,51 @@ __device__ __forceinline__ float min3(float a, float b, float c) {
     return r;
 }
 
+__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ---------------------------------------------------------------- semiring functors
-// pad_x / pad_y: operand values for k beyond K whose join is the aggregation's identity
+// step: one join tuple; step2: two tuples of the same output (consecutive k).
+// pad_x / pad_y: operand values for k beyond K whose join is the aggregation's identity.
 struct MulSum {
-    static constexpr bool kPacked = false;
     static __device__ __forceinline__ float init() { return 0.f; }
     static __device__ __forceinline__ float pad_x() { return 0.f; }
     static __device__ __forceinline__ float pad_y() { return 0.f; }
-    static __device__ __forceinline__ void step(float& acc, float x, float y) { acc = fmaf(x, y, acc); }
-    static __device__ __forceinline__ void step2(float&, uint64_t, uint64_t) {}
+    static __device__ __forceinline__ void step2(float& acc, float x0, float y0, float x1, float y1) {
+        acc = fmaf(x1, y1, fmaf(x0, y0, acc));
+    }
 };
 struct SqdiffSum {
-    static constexpr bool kPacked = false;
     static __device__ __forceinline__ float init() { return 0.f; }
     static __device__ __forceinline__ float pad_x() { return 0.f; }
     static __device__ __forceinline__ float pad_y() { return 0.f; }
-    static __device__ __forceinline__ void step(float& acc, float x, float y) {
-        const float t = x - y;
-        acc = fmaf(t, t, acc);
+    static __device__ __forceinline__ void step2(float& acc, float x0, float y0, float x1, float y1) {
+        const float t0 = x0 - y0, t1 = x1 - y1;
+        acc = fmaf(t1, t1, fmaf(t0, t0, acc));
     }
-    static __device__ __forceinline__ void step2(float&, uint64_t, uint64_t) {}
 };
 struct AddMax {
-    static constexpr bool kPacked = true;
     static __device__ __forceinline__ float init() { return -INFINITY; }
     static __device__ __forceinline__ float pad_x() { return -INFINITY; }
     static __device__ __forceinline__ float pad_y() { return 0.f; }
-    static __device__ __forceinline__ void step(float& acc, float x, float y) { acc = fmaxf(acc, x + y); }
-    static __device__ __forceinline__ void step2(float& acc, uint64_t x2, uint64_t y2) {
-        const uint64_t t = add2(x2, y2);
-        acc = max3(acc, lo_of(t), hi_of(t));
+    static __device__ __forceinline__ void step2(float& acc, float x0, float y0, float x1, float y1) {
+        acc = max3(acc, x0 + y0, x1 + y1);
     }
 };
 struct AddMin {
-    static constexpr bool kPacked = true;
     static __device__ __forceinline__ float init() { return INFINITY; }
     static __device__ __forceinline__ float pad_x() { return INFINITY; }
     static __device__ __forceinline__ float pad_y() { return 0.f; }
-    static __device__ __forceinline__ void step(float& acc, float x, float y) { acc = fminf(acc, x + y); }
-    static __device__ __forceinline__ void step2(float& acc, uint64_t x2, uint64_t y2) {
-        const uint64_t t = add2(x2, y2);
-        acc = min3(acc, lo_of(t), hi_of(t));
+    static __device__ __forceinline__ void step2(float& acc, float x0, float y0, float x1, float y1) {
+        acc = min3(acc, x0 + y0, x1 + y1);
     }
 };
 
@@ -180,29 +180,190 @@ __device__ __forceinline__ int64_t koff_y(const SemiringParams& p, uint32_t k) {
     return role_offset(p.yk, k);
 }
 
-// shared-memory index of (k, row) in the unpacked [k][row] or packed [k/2][row][k%2] layout
-template <bool P>
-__device__ __forceinline__ int sidx(int k, int r) {
-    return P ? (((k >> 1) * BM + r) << 1) + (k & 1) : k * BM + r;
-}
-
-// ---------------------------------------------------------------- tiled kernel
-template <class S, typename TIn, int EPI>
-__global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ SemiringParams p) {
-    constexpr bool P = S::kPacked;
-    __shared__ __align__(16) float Xs[2][BK * BM];
-    __shared__ __align__(16) float Ys[2][BK * BN];
-    __shared__ int64_t rowX[BM], colY[BN];
-
-    const int tid = threadIdx.x;
+__device__ __forceinline__ void decode_tile(const SemiringParams& p, uint32_t& b, uint32_t& m0, uint32_t& n0) {
     const uint32_t tiles_m = (p.M + BM - 1) / BM, tiles_n = (p.N + BN - 1) / BN;
     uint32_t t = blockIdx.x;
     const uint32_t tn = t % tiles_n;
     t /= tiles_n;
     const uint32_t tm = t % tiles_m;
-    const uint32_t b = t / tiles_m;
-    const uint32_t m0 = tm * BM, n0 = tn * BN;
+    b = t / tiles_m;
+    m0 = tm * BM;
+    n0 = tn * BN;
+}
 
+// Thread (ty, tx) owns rows ty*4+{0..3}, 64+ty*4+{0..3} and columns tx*4+{0..3},
+// 64+tx*4+{0..3} of the tile.  The caller guarantees every shared buffer passed here is
+// free (all threads past their last read of it).
+template <int EPI>
+__device__ __forceinline__ void tile_epilogue(const SemiringParams& p, float (&acc)[8][8], uint32_t b, uint32_t m0,
+                                              uint32_t n0, int64_t* rowZ, int64_t* colZ, float* rterms,
+                                              float* cterms) {
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    if (tid < BM) {
+        const uint32_t m = min(m0 + tid, p.M - 1);
+        rowZ[tid] = role_offset(p.zb, b) + role_offset(p.zm, m);
+        if (EPI == kEpiLse) rterms[tid] = p.rowmax[(uint64_t)b * p.M + m];
+        if (EPI == kEpiSqExpand) rterms[tid] = p.xnorm[(uint64_t)b * p.M + m];
+    } else {
+        const uint32_t n = min(n0 + (tid - BM), p.N - 1);
+        colZ[tid - BM] = role_offset(p.zn, n);
+        if (EPI == kEpiLse) cterms[tid - BM] = p.colmax[(uint64_t)b * p.N + n];
+        if (EPI == kEpiSqExpand) cterms[tid - BM] = p.ynorm[(uint64_t)b * p.N + n];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int mi = (i < 4) ? ty * 4 + i : 64 + ty * 4 + (i - 4);
+        const uint32_t m = m0 + mi;
+        if (m >= p.M) continue;
+        const int64_t zrow = rowZ[mi];
+        const float rterm = EPI == kEpiPlain ? 0.f : rterms[mi];
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            const int nb = g * 64 + tx * 4;
+            const uint32_t n = n0 + nb;
+            float v[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float a = acc[i][g * 4 + c];
+                if (EPI == kEpiLse) {
+                    // every exp-shifted product underflowed: mark the output, lse_fixup recomputes it
+                    a = a > 1e-30f ? rterm + cterms[nb + c] + logf(a) : __int_as_float(0x7fc00000);
+                } else if (EPI == kEpiSqExpand) {
+                    a = fmaxf(rterm + cterms[nb + c] - 2.f * a, 0.f);
+                }
+                v[c] = p.alpha * a;
+            }
+            if (p.z_vec4 && n + 3 < p.N) {
+                const int64_t off = zrow + colZ[nb];
+                if (p.out_bf16) {
+                    const __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
+                    const __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
+                    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.z) + off) =
+                        make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+                } else {
+                    *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.z) + off) = make_float4(v[0], v[1], v[2], v[3]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (n + c < p.N) st_out(p.z, zrow + colZ[nb + c], v[c], p.out_bf16);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- cp.async pipelined kernel
+// X tile in shared memory as [m][k] (32 floats per row, copied straight from the
+// K-contiguous operand), Y tile as [k][n].  Per thread per 4 k: 8 LDS.128 of X (one per
+// owned row), 2 LDS.128 of Y per k.
+template <class S, int EPI>
+__global__ void __launch_bounds__(NT, 2) semiring_async(const __grid_constant__ SemiringParams p) {
+    extern __shared__ __align__(16) float dsm[];
+    float* Xs = dsm;                          // [ASTAGES][BM * ABK]
+    float* Ys = dsm + ASTAGES * BM * ABK;     // [ASTAGES][ABK * BN]
+    __shared__ int64_t rowX[BM], colY[BN];
+
+    const int tid = threadIdx.x;
+    uint32_t b, m0, n0;
+    decode_tile(p, b, m0, n0);
+    if (tid < BM) {
+        rowX[tid] = role_offset(p.xb, b) + role_offset(p.xm, clamp_row(m0 + tid, p.M, false));
+    } else {
+        colY[tid - BM] = role_offset(p.yb, b) + role_offset(p.yn, clamp_row(n0 + (tid - BM), p.N, true));
+    }
+    __syncthreads();
+
+    const float* __restrict__ xg = reinterpret_cast<const float*>(p.x);
+    const float* __restrict__ yg = reinterpret_cast<const float*>(p.y);
+    // copy assignment: X chunk (row (tid>>3) + 32i, k (tid&7)*4); Y chunk (k row (tid>>5) + 8i, n (tid&31)*4)
+    const int xk = (tid & 7) * 4, xr = tid >> 3;
+    const int yn = (tid & 31) * 4, yr = tid >> 5;
+    auto issue = [&](int stage, uint32_t k0) {
+        float* xs = Xs + stage * (BM * ABK);
+        float* ys = Ys + stage * (ABK * BN);
+        if (k0 + xk < p.K) {
+            const int64_t ko = koff_x(p, k0 + xk);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) cp_async16(&xs[(xr + 32 * i) * ABK + xk], xg + rowX[xr + 32 * i] + ko);
+        } else {
+            const float px = S::pad_x();
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<float4*>(&xs[(xr + 32 * i) * ABK + xk]) = make_float4(px, px, px, px);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int kr = yr + 8 * i;
+            if (k0 + kr < p.K) {
+                cp_async16(&ys[kr * BN + yn], yg + colY[yn] + koff_y(p, k0 + kr));
+            } else {
+                const float py = S::pad_y();
+                *reinterpret_cast<float4*>(&ys[kr * BN + yn]) = make_float4(py, py, py, py);
+            }
+        }
+        cp_async_commit();
+    };
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = S::init();
+
+    const int ty = tid >> 4, tx = tid & 15;
+    const uint32_t nkt = (p.K + ABK - 1) / ABK;
+    issue(0, 0);
+    if (nkt > 1) issue(1, ABK);
+    else cp_async_commit();
+    for (uint32_t kt = 0; kt < nkt; ++kt) {
+        cp_async_wait<ASTAGES - 2>();  // this thread's copies of tile kt have landed
+        __syncthreads();               // everyone's have, and tile kt-1's buffer is free
+        if (kt + 2 < nkt) issue((kt + 2) % ASTAGES, (kt + 2) * ABK);
+        else cp_async_commit();
+        const int st = kt % ASTAGES;
+        const float4* xs4 = reinterpret_cast<const float4*>(Xs + st * (BM * ABK));
+        const float4* ys4 = reinterpret_cast<const float4*>(Ys + st * (ABK * BN));
+#pragma unroll 2
+        for (int kq = 0; kq < ABK / 4; ++kq) {
+            float4 a[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = (i < 4) ? ty * 4 + i : 64 + ty * 4 + (i - 4);
+                a[i] = xs4[r * (ABK / 4) + kq];
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int k = kq * 4 + 2 * h;
+                const float4 b0 = ys4[k * (BN / 4) + tx], b1 = ys4[k * (BN / 4) + 16 + tx];
+                const float4 d0 = ys4[(k + 1) * (BN / 4) + tx], d1 = ys4[(k + 1) * (BN / 4) + 16 + tx];
+                const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float x0 = h == 0 ? a[i].x : a[i].z;
+                    const float x1 = h == 0 ? a[i].y : a[i].w;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) S::step2(acc[i][j], x0, bb[j], x1, dd[j]);
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+    tile_epilogue<EPI>(p, acc, b, m0, n0, rowX, colY, Xs, Ys);
+}
+
+// ---------------------------------------------------------------- register-staged kernel
+template <class S, typename TIn, int EPI>
+__global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ SemiringParams p) {
+    __shared__ __align__(16) float Xs[2][BK * BM];
+    __shared__ __align__(16) float Ys[2][BK * BN];
+    __shared__ int64_t rowX[BM], colY[BN];
+
+    const int tid = threadIdx.x;
+    uint32_t b, m0, n0;
+    decode_tile(p, b, m0, n0);
     if (tid < BM) {
         rowX[tid] = role_offset(p.xb, b) + role_offset(p.xm, clamp_row(m0 + tid, p.M, p.x_mode == kLoadVecMN));
     } else {
@@ -246,8 +407,7 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
             const int n = (tid & 31) * 4;
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-                // packed layout: rows 2*kp and 2*kp+1; unpacked: rows kk and kk+8
-                const int k = P ? 2 * (tid >> 5) + i : (tid >> 5) + 8 * i;
+                const int k = (tid >> 5) + 8 * i;
                 float4 v = k < kv ? ld4<TIn>(p.y, colY[n] + koff_y(p, k0 + k)) : make_float4(py, py, py, py);
                 ry[4 * i] = v.x, ry[4 * i + 1] = v.y, ry[4 * i + 2] = v.z, ry[4 * i + 3] = v.w;
             }
@@ -269,7 +429,7 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
         }
     };
 
-    // ---- registers -> shared memory
+    // ---- registers -> shared memory, [k][row] layout
     auto store = [&](int buf) {
         float* xs = Xs[buf];
         float* ys = Ys[buf];
@@ -278,64 +438,40 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int k = ((tid >> 7) + 2 * i) * 4;
-                if (P) {
-                    *reinterpret_cast<float2*>(&xs[sidx<P>(k, m)]) = make_float2(rx[4 * i], rx[4 * i + 1]);
-                    *reinterpret_cast<float2*>(&xs[sidx<P>(k + 2, m)]) = make_float2(rx[4 * i + 2], rx[4 * i + 3]);
-                } else {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) xs[sidx<P>(k + c, m)] = rx[4 * i + c];
-                }
+                for (int c = 0; c < 4; ++c) xs[(k + c) * BM + m] = rx[4 * i + c];
             }
         } else if (xmode == kLoadVecMN) {
             const int m = (tid & 31) * 4;
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int k = (tid >> 5) + 8 * i;
-                if (P) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) xs[sidx<P>(k, m + c)] = rx[4 * i + c];
-                } else {
-                    *reinterpret_cast<float4*>(&xs[sidx<P>(k, m)]) =
-                        make_float4(rx[4 * i], rx[4 * i + 1], rx[4 * i + 2], rx[4 * i + 3]);
-                }
+                *reinterpret_cast<float4*>(&xs[k * BM + m]) = make_float4(rx[4 * i], rx[4 * i + 1], rx[4 * i + 2], rx[4 * i + 3]);
             }
         } else {
             const int m = tid & (BM - 1);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) xs[sidx<P>((tid >> 7) + 2 * i, m)] = rx[i];
+            for (int i = 0; i < 8; ++i) xs[((tid >> 7) + 2 * i) * BM + m] = rx[i];
         }
         if (ymode == kLoadVecMN) {
             const int n = (tid & 31) * 4;
-            if (P) {
-                const int kp = tid >> 5;  // rows 2kp (ry[0..3]) and 2kp+1 (ry[4..7])
-                float4* dst = reinterpret_cast<float4*>(&ys[((kp * BN + n) << 1)]);
-                dst[0] = make_float4(ry[0], ry[4], ry[1], ry[5]);
-                dst[1] = make_float4(ry[2], ry[6], ry[3], ry[7]);
-            } else {
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int k = (tid >> 5) + 8 * i;
-                    *reinterpret_cast<float4*>(&ys[sidx<P>(k, n)]) =
-                        make_float4(ry[4 * i], ry[4 * i + 1], ry[4 * i + 2], ry[4 * i + 3]);
-                }
+            for (int i = 0; i < 2; ++i) {
+                const int k = (tid >> 5) + 8 * i;
+                *reinterpret_cast<float4*>(&ys[k * BN + n]) = make_float4(ry[4 * i], ry[4 * i + 1], ry[4 * i + 2], ry[4 * i + 3]);
             }
         } else if (ymode == kLoadVecK) {
             const int n = tid & (BN - 1);
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int k = ((tid >> 7) + 2 * i) * 4;
-                if (P) {
-                    *reinterpret_cast<float2*>(&ys[sidx<P>(k, n)]) = make_float2(ry[4 * i], ry[4 * i + 1]);
-                    *reinterpret_cast<float2*>(&ys[sidx<P>(k + 2, n)]) = make_float2(ry[4 * i + 2], ry[4 * i + 3]);
-                } else {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) ys[sidx<P>(k + c, n)] = ry[4 * i + c];
-                }
+                for (int c = 0; c < 4; ++c) ys[(k + c) * BN + n] = ry[4 * i + c];
             }
         } else {
             const int n = tid & (BN - 1);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) ys[sidx<P>((tid >> 7) + 2 * i, n)] = ry[i];
+            for (int i = 0; i < 8; ++i) ys[((tid >> 7) + 2 * i) * BN + n] = ry[i];
         }
     };
 
@@ -357,109 +493,28 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
         // one barrier per K-tile: this tile computes from buf while the next one is
         // loaded into registers and then stored to buf ^ 1
         if (has_next) load((kt + 1) * BK);
-        const float* xs = Xs[buf];
-        const float* ys = Ys[buf];
-        if constexpr (P) {
-#pragma unroll 2
-            for (int kp = 0; kp < BK / 2; ++kp) {
-                // x pairs for rows ty*4..+3 and 64+ty*4..+3; y pairs for columns g*32 + tx*2 + {0,1}
-                uint64_t xa[8];
-                const ulonglong2* xr0 = reinterpret_cast<const ulonglong2*>(&xs[((kp * BM + ty * 4) << 1)]);
-                const ulonglong2* xr1 = reinterpret_cast<const ulonglong2*>(&xs[((kp * BM + 64 + ty * 4) << 1)]);
-                const ulonglong2 q0 = xr0[0], q1 = xr0[1], q2 = xr1[0], q3 = xr1[1];
-                xa[0] = q0.x, xa[1] = q0.y, xa[2] = q1.x, xa[3] = q1.y;
-                xa[4] = q2.x, xa[5] = q2.y, xa[6] = q3.x, xa[7] = q3.y;
+        const float4* xs4 = reinterpret_cast<const float4*>(Xs[buf]);
+        const float4* ys4 = reinterpret_cast<const float4*>(Ys[buf]);
+#pragma unroll 4
+        for (int k = 0; k < BK; k += 2) {
+            const float4 a0 = xs4[k * (BM / 4) + ty], a1 = xs4[k * (BM / 4) + 16 + ty];
+            const float4 c0 = xs4[(k + 1) * (BM / 4) + ty], c1 = xs4[(k + 1) * (BM / 4) + 16 + ty];
+            const float4 b0 = ys4[k * (BN / 4) + tx], b1 = ys4[k * (BN / 4) + 16 + tx];
+            const float4 d0 = ys4[(k + 1) * (BN / 4) + tx], d1 = ys4[(k + 1) * (BN / 4) + 16 + tx];
+            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    // one group of two y pairs at a time keeps fewer values live
-                    const ulonglong2 w = *reinterpret_cast<const ulonglong2*>(&ys[((kp * BN + g * 32 + tx * 2) << 1)]);
+            for (int i = 0; i < 8; ++i)
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        S::step2(acc[i][2 * g], xa[i], w.x);
-                        S::step2(acc[i][2 * g + 1], xa[i], w.y);
-                    }
-                }
-            }
-        } else {
-#pragma unroll 8
-            for (int k = 0; k < BK; ++k) {
-                const float4 a0 = *reinterpret_cast<const float4*>(&xs[k * BM + ty * 4]);
-                const float4 a1 = *reinterpret_cast<const float4*>(&xs[k * BM + 64 + ty * 4]);
-                const float4 b0 = *reinterpret_cast<const float4*>(&ys[k * BN + tx * 4]);
-                const float4 b1 = *reinterpret_cast<const float4*>(&ys[k * BN + 64 + tx * 4]);
-                const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) S::step(acc[i][j], a[i], bb[j]);
-            }
+                for (int j = 0; j < 8; ++j) S::step2(acc[i][j], a[i], bb[j], c[i], dd[j]);
         }
         if (has_next) store(buf ^ 1);
         __syncthreads();
     }
-
-    // ---- epilogue: output offsets through Z's relation layout.  The row / column offset
-    // tables reuse rowX / colY (every thread is past its last load: the loop ends on a barrier).
-    if (tid < BM) {
-        rowX[tid] = role_offset(p.zb, b) + role_offset(p.zm, min(m0 + tid, p.M - 1));
-    } else {
-        colY[tid - BM] = role_offset(p.zn, min(n0 + (tid - BM), p.N - 1));
-    }
-    __syncthreads();
-    constexpr int G = P ? 2 : 4;  // consecutive output columns a thread owns
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int mi = (i < 4) ? ty * 4 + i : 64 + ty * 4 + (i - 4);
-        const uint32_t m = m0 + mi;
-        if (m >= p.M) continue;
-        const int64_t zrow = rowX[mi];
-        float rterm = 0.f;
-        if (EPI == kEpiLse) rterm = p.rowmax[(uint64_t)b * p.M + m];
-        if (EPI == kEpiSqExpand) rterm = p.xnorm[(uint64_t)b * p.M + m];
-#pragma unroll
-        for (int g = 0; g < 8 / G; ++g) {
-            const int nb = P ? g * 32 + tx * 2 : g * 64 + tx * 4;
-            const uint32_t n = n0 + nb;
-            float v[G];
-#pragma unroll
-            for (int c = 0; c < G; ++c) {
-                float a = acc[i][g * G + c];
-                if (EPI == kEpiLse) {
-                    if (n + c < p.N) {
-                        if (a > 1e-30f) a = rterm + p.colmax[(uint64_t)b * p.N + n + c] + logf(a);
-                        else a = lse_fallback(p, b, m, n + c);  // every exp-shifted product underflowed
-                    }
-                } else if (EPI == kEpiSqExpand) {
-                    if (n + c < p.N) a = fmaxf(rterm + p.ynorm[(uint64_t)b * p.N + n + c] - 2.f * a, 0.f);
-                }
-                v[c] = p.alpha * a;
-            }
-            if (p.z_vec4 && n + G - 1 < p.N) {
-                const int64_t off = zrow + colY[nb];
-                if (p.out_bf16) {
-                    uint32_t w[G / 2];
-#pragma unroll
-                    for (int h = 0; h < G / 2; ++h) {
-                        const __nv_bfloat162 pr = __floats2bfloat162_rn(v[2 * h], v[2 * h + 1]);
-                        w[h] = *reinterpret_cast<const uint32_t*>(&pr);
-                    }
-                    if (G == 4)
-                        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.z) + off) = make_uint2(w[0], w[G / 2 - 1]);
-                    else
-                        *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(p.z) + off) = w[0];
-                } else if (G == 4) {
-                    *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.z) + off) = make_float4(v[0], v[1 % G], v[2 % G], v[3 % G]);
-                } else {
-                    *reinterpret_cast<float2*>(reinterpret_cast<float*>(p.z) + off) = make_float2(v[0], v[1 % G]);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < G; ++c)
-                    if (n + c < p.N) st_out(p.z, zrow + colY[nb + c], v[c], p.out_bf16);
-            }
-        }
-    }
+    // every thread is past its last read of Xs / Ys / rowX / colY (the loop ends on a barrier)
+    tile_epilogue<EPI>(p, acc, b, m0, n0, rowX, colY, Xs[0], Ys[0]);
 }
 
 // ---------------------------------------------------------------- generic fallback
@@ -499,6 +554,34 @@ __global__ void semiring_simple(const __grid_constant__ SemiringParams p) {
             }
         }
         st_out(p.z, role_offset(p.zb, b) + role_offset(p.zm, m) + role_offset(p.zn, n), p.alpha * acc, p.out_bf16);
+    }
+}
+
+// ---------------------------------------------------------------- factored-logsumexp underflow fix-up
+// Outputs whose exp-shifted sum underflowed carry a NaN mark from the tiled kernel; this pass
+// (same 128 x 128 tiling) finds them and recomputes each with an online max / sum straight
+// from the operands.  With finite inputs no true result is NaN.
+__global__ void __launch_bounds__(NT) lse_fixup_kernel(const __grid_constant__ SemiringParams p) {
+    __shared__ int64_t rowZ[BM], colZ[BN];
+    const int tid = threadIdx.x;
+    const uint32_t tiles_m = (p.M + BM - 1) / BM, tiles_n = (p.N + BN - 1) / BN;
+    uint32_t t = blockIdx.x;
+    const uint32_t tn = t % tiles_n;
+    t /= tiles_n;
+    const uint32_t tm = t % tiles_m;
+    const uint32_t b = t / tiles_m;
+    const uint32_t m0 = tm * BM, n0 = tn * BN;
+    if (tid < BM) rowZ[tid] = role_offset(p.zb, b) + role_offset(p.zm, min(m0 + tid, p.M - 1));
+    else colZ[tid - BM] = role_offset(p.zn, min(n0 + (tid - BM), p.N - 1));
+    __syncthreads();
+    const int c = tid & (BN - 1);
+    if (n0 + c >= p.N) return;
+    for (int r = tid >> 7; r < BM && m0 + r < p.M; r += NT / BN) {
+        const int64_t off = rowZ[r] + colZ[c];
+        const float v = p.out_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.z)[off])
+                                   : reinterpret_cast<const float*>(p.z)[off];
+        if (v == v) continue;
+        st_out(p.z, off, p.alpha * lse_fallback(p, b, m0 + r, n0 + c), p.out_bf16);
     }
 }
 
@@ -573,6 +656,14 @@ __global__ void lse_prep_kernel(const __grid_constant__ LsePrepParams p, int row
 
 template <class S, typename TIn, int EPI>
 cudaError_t launch_tiled(const SemiringParams& p, unsigned grid, cudaStream_t s) {
+    if (!p.in_bf16 && p.x_mode == kLoadVecK && p.y_mode == kLoadVecMN) {
+        // fp32, X contiguous along K and Y along N: the cp.async pipelined kernel
+        cudaError_t e = cudaFuncSetAttribute(semiring_async<S, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kAsyncSmem);
+        if (e != cudaSuccess) return e;
+        semiring_async<S, EPI><<<grid, NT, kAsyncSmem, s>>>(p);
+        return cudaGetLastError();
+    }
     semiring_tiled<S, TIn, EPI><<<grid, NT, 0, s>>>(p);
     return cudaGetLastError();
 }
@@ -586,8 +677,15 @@ cudaError_t launch_semiring(const SemiringParams& p, cudaStream_t s) {
     if (grid64 > 0x7fffffffull) return cudaErrorInvalidValue;
     const unsigned grid = (unsigned)grid64;
     const bool bf = p.in_bf16;
-    if (p.rowmax) return launch_tiled<MulSum, float, kEpiLse>(p, grid, s);       // fp32 exp-shifted scratch
-    if (p.xnorm) return launch_tiled<MulSum, float, kEpiSqExpand>(p, grid, s);   // fp32 inputs
+    if (p.rowmax) {  // fp32 exp-shifted scratch, then the underflow fix-up
+        SemiringParams q = p;
+        q.in_bf16 = 0;
+        cudaError_t e = launch_tiled<MulSum, float, kEpiLse>(q, grid, s);
+        if (e != cudaSuccess) return e;
+        lse_fixup_kernel<<<grid, NT, 0, s>>>(p);
+        return cudaGetLastError();
+    }
+    if (p.xnorm) return launch_tiled<MulSum, float, kEpiSqExpand>(p, grid, s);  // fp32 inputs
     switch (p.op * 8 + p.agg) {
         case kMul * 8 + kSum:
             return bf ? launch_tiled<MulSum, __nv_bfloat16, kEpiPlain>(p, grid, s)
