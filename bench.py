@@ -504,6 +504,23 @@ def traffic_for(kernel_file: str, kernel_name: str, units_scale: float = 1.0):
     return rec["dram_bytes_per_launch"] * units_scale
 
 
+def max_over_ranks(value_ms: float, world: int, device: str = "cuda") -> float:
+    """Largest per-rank elapsed time (the job's time) -- an all-reduce MAX across ranks."""
+    if world <= 1:
+        return value_ms
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(ops_per_step: int, steps: int, world: int, job_ms: float) -> float:
+    """Whole-job TFLOP/s: every rank processed its own replica of the workload (weak scaling)."""
+    return world * ops_per_step * steps / (job_ms * 1e-3) / 1e12
+
+
 def run_ours(args):
     import torch
 
@@ -538,15 +555,9 @@ def run_ours(args):
     sampler = ClockSampler(local) if rank == 0 else None
     step_ms, per, wall, clocks = time_steps(torch, wl, args.steps, args.warmup, flush, sampler)
     barrier()
-    total_ms = sum(step_ms)
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world)
     ops = wl.ops_per_step()
-    value = world * ops * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_throughput(ops, args.steps, world, total_ms)
 
     # end to end: pinned host inputs -> device, the step, results -> pinned host
     pinned_in = [torch.from_numpy(h).reshape(-1).pin_memory() for h in host]
@@ -564,15 +575,9 @@ def run_ours(args):
     e2e_ms, _, _, _ = time_steps(torch, wl, max(3, args.steps // 4), args.warmup, flush, None,
                                  {"h2d": h2d, "d2h": d2h})
     barrier()
-    e2e_total = sum(e2e_ms)
     n_e2e = max(3, args.steps // 4)
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([e2e_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
-    e2e_value = world * ops * n_e2e / (e2e_total * 1e-3) / 1e12
+    e2e_total = max_over_ranks(sum(e2e_ms), world)
+    e2e_value = job_throughput(ops, n_e2e, world, e2e_total)
     h2d_bytes = sum(t.numel() * t.element_size() for t in pinned_in)
     d2h_bytes = sum(t.numel() * t.element_size() for t in pinned_out)
 
