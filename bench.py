@@ -117,7 +117,7 @@ class Step:
 
 def kernel_launches(plan) -> int:
     """Kernels one ein_execute of this plan launches."""
-    n = {"semiring_f32": 1, "tc_bf16": 1, "row_reduce": 1, "elementwise": 1, "lse_factored": 4,
+    n = {"semiring_f32": 1, "tc_bf16": 1, "tc_bf16_pair": 1, "row_reduce": 1, "elementwise": 1, "lse_factored": 4,
          "literal": 2}[plan.kernel]
     spec = plan.spec
     if plan.kernel == "semiring_f32" and ":sqdiff:sum" in spec and "sqdiff=direct" not in spec and "in=bf16" not in spec:

@@ -89,7 +89,8 @@ enum {
     TRA_KERNEL_ROW_REDUCE = 3,    /* unary aggregation over the contracted labels */
     TRA_KERNEL_ELEMENTWISE = 4,   /* join with AGG = none (broadcast operands allowed) */
     TRA_KERNEL_LSE_FACTORED = 5,  /* logsumexp of a sum: max-shifted exp, then sum-of-products */
-    TRA_KERNEL_LITERAL = 6        /* one partial per join tuple, then ordered combine */
+    TRA_KERNEL_LITERAL = 6,       /* one partial per join tuple, then ordered combine */
+    TRA_KERNEL_TC_BF16_PAIR = 7   /* as TC_BF16, one 256 x 256 tile per cluster of two CTAs */
 };
 
 /* ein_plan -- build the TRA plan of one EinSum under partition vector d
@@ -102,7 +103,10 @@ enum {
  *         contracted.  Options: in=f32|bf16 (both inputs, default f32),
  *         out=f32|bf16 (default f32), alpha=<float> (scales the aggregated value),
  *         mode=fused|literal (literal materialises one partial per join tuple and
- *         combines them in canonical order), sqdiff=direct|expand.
+ *         combines them in canonical order), sqdiff=direct|expand,
+ *         tc=pair|single (BF16 sum-of-products on tensor cores: a 256 x 256 tile
+ *         shared by a cluster of two CTAs, or a 128-row tile per CTA; default pair
+ *         when the output rows and columns are multiples of 256).
  * bounds: B_l for every distinct label in first-appearance order (X then Y);
  *         n_bounds must equal the number of distinct labels.
  * d:      partition counts per operand index position, X's then Y's (n_d =

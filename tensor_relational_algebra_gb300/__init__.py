@@ -28,7 +28,8 @@ ERRORS = {
     -1: "TRA_ERR_PARSE", -2: "TRA_ERR_DIVISIBILITY", -3: "TRA_ERR_SHARED_LABEL_D", -4: "TRA_ERR_RANK",
     -5: "TRA_ERR_UNSUPPORTED", -6: "TRA_ERR_WORKSPACE", -7: "TRA_ERR_CUDA", -8: "TRA_ERR_TIMEOUT", -9: "TRA_ERR_ARG",
 }
-KERNELS = {1: "semiring_f32", 2: "tc_bf16", 3: "row_reduce", 4: "elementwise", 5: "lse_factored", 6: "literal"}
+KERNELS = {1: "semiring_f32", 2: "tc_bf16", 3: "row_reduce", 4: "elementwise", 5: "lse_factored", 6: "literal",
+           7: "tc_bf16_pair"}
 ROLES = {0: "batch", 1: "M", 2: "N", 3: "contracted"}
 
 

@@ -258,6 +258,7 @@ int execute_plan(const Plan& p, const void* x, const void* y, void* z, void* ws,
             break;
         }
         case TRA_KERNEL_TC_BF16:
+        case TRA_KERNEL_TC_BF16_PAIR:
             return tc_execute(p, x, y, z, s);
         case TRA_KERNEL_LITERAL:
             return execute_literal(p, x, y, z, ws, s);

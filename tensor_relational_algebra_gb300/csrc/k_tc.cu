@@ -399,6 +399,281 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ------------------------------------------------------------------ CTA-pair kernel
+// Two CTAs of a cluster share one 256 x 256 output tile: tcgen05.mma.cta_group::2
+// (M = 256, N = 256) issued by the even CTA reads A rows 0-127 and B rows 0-127 from its
+// own shared memory and A rows 128-255 / B rows 128-255 from the odd CTA's, and writes
+// accumulator rows 0-127 to the even CTA's tensor memory, rows 128-255 to the odd CTA's.
+// Each SM therefore loads half of B per K step (32 KB instead of 48 KB for the same MMA
+// work), which is what the L2 -> SM delivery rate limits.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// bounded wait on a barrier that other CTAs of the cluster signal (cluster-scope acquire)
+__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, volatile int* abort, uint64_t timeout_ns) {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait_cl(bar, parity)) return true;
+        if ((n & 63) == 0) {
+            if (*abort) return false;
+            if (globaltimer() - t0 > timeout_ns) {
+                *abort = 1;
+                atomicExch(&g_status, (int)TRA_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
+}
+// TMA load into this CTA's shared memory whose completion is counted on a barrier that may
+// live in the peer CTA of the pair
+__device__ __forceinline__ void tma_load_5d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                 const int c[5]) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4]), "r"(bar_cluster)
+        : "memory");
+}
+__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// arrive once on the barrier at this shared offset in every CTA of ctamask, when the MMAs
+// issued so far have completed
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t ctamask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(ctamask)
+        : "memory");
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    tc_gemm_2sm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                const __grid_constant__ TcParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t stage_bytes = p.a_bytes + p.b_bytes;  // this CTA's half of one K step
+    const uint32_t bar0 = base + p.stages * stage_bytes;
+    const uint32_t full0 = bar0, empty0 = bar0 + 8 * p.stages, tfull0 = bar0 + 16 * p.stages;
+    const uint32_t tempty0 = tfull0 + 16, done_bar = tempty0 + 16;
+    uint8_t* gbase = smem_raw + (base - raw);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (done_bar + 8 - base));
+    volatile int* abort = reinterpret_cast<volatile int*>(gbase + (done_bar + 12 - base));
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const uint32_t pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < p.stages; ++s) {
+            mbar_init(full0 + 8 * s, 1);   // the even CTA's producer arrives; both CTAs' bytes count
+            mbar_init(empty0 + 8 * s, 1);  // one multicast commit
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull0 + 8 * a, 1);
+            mbar_init(tempty0 + 8 * a, 8);  // one lane of each epilogue warp of both CTAs
+        }
+        mbar_init(done_bar, 1);
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(p.tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers exist before anyone signals across the pair
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer (both CTAs)
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            for (uint32_t t = pair; t < p.n_tiles && ok; t += n_pairs) {
+                uint32_t b, mt, nt;
+                tile_of(p, t, b, mt, nt);
+                const uint32_t m0 = mt * 2 * kBlockM + rank * kBlockM, n0 = nt * p.block_n + rank * (p.block_n / 2);
+                int fa[2][5], fbx[2][5];
+#pragma unroll
+                for (int l = 0; l < 2; ++l) {
+                    if (l < p.a.n_loads) fixed_coords(p.a, b, m0 + 64u * l, fa[l]);
+                    if (l < p.b.n_loads) fixed_coords(p.b, b, n0 + 64u * l, fbx[l]);
+                }
+                for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait_cl(empty0 + 8 * stage, phase ^ 1, abort, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full0 + 8 * stage;
+                    if (leader) mbar_expect_tx(fb, 2 * stage_bytes);
+                    const uint32_t fb_leader = mapa_shared(fb, 0);
+                    const uint32_t sa = base + stage * stage_bytes, sb = sa + p.a_bytes;
+                    const uint32_t k0 = kb * kBlockK;
+                    int ka[5], kbc[5], c[5];
+                    k_coords(p.a, k0, ka);
+                    k_coords(p.b, k0, kbc);
+#pragma unroll
+                    for (int l = 0; l < 2; ++l) {
+                        if (l < p.a.n_loads) {
+#pragma unroll
+                            for (int j = 0; j < 5; ++j) c[j] = fa[l][j] + ka[j];
+                            tma_load_5d_pair(sa + 8192u * l, &map_a, fb_leader, c);
+                        }
+                        if (l < p.b.n_loads) {
+#pragma unroll
+                            for (int j = 0; j < 5; ++j) c[j] = fbx[l][j] + kbc[j];
+                            tma_load_5d_pair(sb + 8192u * l, &map_b, fb_leader, c);
+                        }
+                    }
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) __nanosleep(20000);  // let copies already issued land before leaving
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer (even CTA)
+        if (lane == 0 && leader) {
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            const uint32_t a_lbo = p.a.mn_major ? 8192u : 16u, b_lbo = p.b.mn_major ? 8192u : 16u;
+            const uint32_t a_kstep = p.a.mn_major ? 2048u : 32u, b_kstep = p.b.mn_major ? 2048u : 32u;
+            for (uint32_t t = pair; t < p.n_tiles && ok; t += n_pairs) {
+                if (!mbar_wait_cl(tempty0 + 8 * acc, acc_phase ^ 1, abort, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * p.block_n;
+                for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait_cl(full0 + 8 * stage, phase, abort, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base + stage * stage_bytes, sb = sa + p.a_bytes;
+#pragma unroll
+                    for (uint32_t k = 0; k < kBlockK / 16; ++k) {
+                        const uint64_t ad = smem_desc(sa + k * a_kstep, a_lbo, 1024);
+                        const uint64_t bd = smem_desc(sb + k * b_kstep, b_lbo, 1024);
+                        tc_mma_pair(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
+                    }
+                    tc_commit_pair(empty0 + 8 * stage, 3);  // frees this stage in both CTAs
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit_pair(tfull0 + 8 * acc, 3);  // accumulator ready in both CTAs
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1;
+                }
+            }
+            tc_commit_pair(done_bar, 1);  // all MMAs issued so far have completed
+            volatile int never = 0;
+            mbar_wait_cl(done_bar, 0, &never, p.timeout_ns);
+        }
+    } else {
+        // ---------------------------------------------------------------- epilogue (warps 2-5, both CTAs)
+        const uint32_t q = warp & 3;
+        uint32_t acc = 0, acc_phase = 0;
+        for (uint32_t t = pair; t < p.n_tiles; t += n_pairs) {
+            uint32_t b, mt, nt;
+            tile_of(p, t, b, mt, nt);
+            if (!mbar_wait_cl(tfull0 + 8 * acc, acc_phase, abort, p.timeout_ns)) break;
+            tc_fence_after();
+            const uint32_t m = mt * 2 * kBlockM + rank * kBlockM + q * 32 + lane;
+            const uint32_t n0 = nt * p.block_n;
+            const int64_t zrow = role_offset(p.zb, b) + role_offset(p.zm, min(m, p.M - 1));
+            for (uint32_t c = 0; c < p.block_n / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem_base + ((q * 32u) << 16) + acc * p.block_n + c * 32u, r);
+                const uint32_t n = n0 + c * 32u;
+                if (m >= p.M || n >= p.N) continue;
+                const int64_t off = zrow + role_offset(p.zn, n);
+                if (p.out_bf16) {
+                    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.z) + off);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const __nv_bfloat162 pr = __floats2bfloat162_rn(p.alpha * __uint_as_float(r[8 * v + 2 * h]),
+                                                                           p.alpha * __uint_as_float(r[8 * v + 2 * h + 1]));
+                            w[h] = *reinterpret_cast<const uint32_t*>(&pr);
+                        }
+                        dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.z) + off);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        dst[v] = make_float4(p.alpha * __uint_as_float(r[4 * v]), p.alpha * __uint_as_float(r[4 * v + 1]),
+                                             p.alpha * __uint_as_float(r[4 * v + 2]),
+                                             p.alpha * __uint_as_float(r[4 * v + 3]));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty0 + 8 * acc, 0));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the even CTA's MMAs have finished with the odd CTA's memory
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(p.tmem_cols)
+                     : "memory");
+    }
+}
+
 // Test hook: one thread waits on an mbarrier that nothing arrives on; the bounded
 // wait must give up after timeout_ns and record TRA_ERR_TIMEOUT.
 __global__ void wait_timeout_probe(uint64_t timeout_ns) {
@@ -443,6 +718,8 @@ struct TcOperandPlan {
 
 struct TcPlan {
     TcOperandPlan a, b;
+    bool pair = false;  // 256 x 256 tile on a cluster of two CTAs
+    uint32_t b_rows = 0;  // rows of Y one CTA loads per K step
     uint32_t block_n = 0, stages = 0, tiles_m = 0, tiles_n = 0, n_tiles = 0, num_kb = 0, tmem_cols = 0;
     uint32_t idesc = 0, smem = 0;
 };
@@ -556,33 +833,55 @@ bool operand_dims(const Plan& p, const Operand& t, int mn_role, uint32_t mn_tile
 
 }  // namespace
 
+namespace {
+
+// Operand tilings for one CTA: A holds a_rows output rows x 64 K, B holds b_rows output
+// columns x 64 K.  Either may be K-major (one box) or M/N-major (boxes of 64 rows).
+bool plan_operands(const Plan& p, uint32_t a_rows, uint32_t b_rows, TcPlan* t) {
+    bool ok = operand_dims(p, p.X, kM, a_rows, 1, t->a);
+    if (!ok || t->a.dev.mn_major) {
+        t->a = TcOperandPlan();
+        ok = operand_dims(p, p.X, kM, 64, a_rows / 64, t->a) && t->a.dev.mn_major;
+    }
+    if (!ok) return false;
+    bool okb = operand_dims(p, p.Y, kN, b_rows, 1, t->b);
+    if (!okb || t->b.dev.mn_major) {
+        t->b = TcOperandPlan();
+        okb = operand_dims(p, p.Y, kN, 64, b_rows / 64, t->b) && t->b.dev.mn_major;
+    }
+    return okb;
+}
+
+}  // namespace
+
 bool tc_plan(Plan* p) {
     if (p->unary || p->op != kMul || p->agg != kSum || !p->in_bf16 || p->literal) return false;
     const uint64_t M = p->ext[kM], N = p->ext[kN], K = p->ext[kK];
     if (M % kBlockM || K % kBlockK || N % 64) return false;
-    uint32_t bn = N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : 64);
     // output: 32 consecutive columns contiguous (innermost label of Z is the innermost N label)
     if (p->comp[kN].empty()) return false;
     const int zl = p->Z.label[p->Z.rank - 1];
     if (zl != p->comp[kN][0] || (p->B[zl] / p->D[zl]) % 32) return false;
     TcPlan* t = new TcPlan();
-    // X: K-major (one load of 128 rows) or M-major (two loads of 64 columns)
-    bool ok = operand_dims(*p, p->X, kM, kBlockM, 1, t->a);
-    if (!ok || t->a.dev.mn_major) {
-        t->a = TcOperandPlan();
-        ok = operand_dims(*p, p->X, kM, 64, kBlockM / 64, t->a) && t->a.dev.mn_major;
+    // a CTA pair: 256 x 256 output tile, each CTA loads 128 rows of X and 128 rows of Y
+    bool ok = false;
+    if (p->tc_pair != 0 && M % 256 == 0 && N % 256 == 0) {
+        ok = plan_operands(*p, kBlockM, 128, t);
+        t->pair = ok;
     }
-    bool okb = ok && operand_dims(*p, p->Y, kN, bn, 1, t->b);
-    if (ok && (!okb || t->b.dev.mn_major)) {
-        t->b = TcOperandPlan();
-        okb = operand_dims(*p, p->Y, kN, 64, bn / 64, t->b) && t->b.dev.mn_major;
+    uint32_t bn = 256;
+    if (!ok && p->tc_pair != 1) {
+        bn = N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : 64);
+        *t = TcPlan();
+        ok = plan_operands(*p, kBlockM, bn, t);
     }
-    if (!ok || !okb) {
+    if (!ok) {
         delete t;
         return false;
     }
     t->block_n = bn;
-    const uint32_t stage = (uint32_t)(kBlockM * kBlockK * 2 + bn * kBlockK * 2);
+    t->b_rows = t->pair ? bn / 2 : bn;
+    const uint32_t stage = (uint32_t)(kBlockM * kBlockK * 2 + t->b_rows * kBlockK * 2);
     t->stages = (kMaxSmem - 2048) / stage;
     if (t->stages > 8) t->stages = 8;
     if (t->stages < 2) {
@@ -590,7 +889,8 @@ bool tc_plan(Plan* p) {
         return false;
     }
     t->smem = t->stages * stage + 1024 + 256;
-    t->tiles_m = (uint32_t)(M / kBlockM);
+    const uint32_t tile_m = t->pair ? 2 * kBlockM : kBlockM;
+    t->tiles_m = (uint32_t)(M / tile_m);
     t->tiles_n = (uint32_t)(N / bn);
     t->n_tiles = (uint32_t)(p->ext[kBatch] * t->tiles_m * t->tiles_n);
     t->num_kb = (uint32_t)(K / kBlockK);
@@ -600,8 +900,9 @@ bool tc_plan(Plan* p) {
                | ((uint32_t)t->a.dev.mn_major << 15)       // A major-ness
                | ((uint32_t)t->b.dev.mn_major << 16)       // B major-ness
                | ((bn >> 3) << 17)                         // N / 8
-               | ((uint32_t)(kBlockM >> 4) << 24);         // M / 16
+               | ((tile_m >> 4) << 24);                    // M / 16
     p->tc = t;
+    p->kernel = t->pair ? TRA_KERNEL_TC_BF16_PAIR : TRA_KERNEL_TC_BF16;
     return true;
 }
 
@@ -663,7 +964,7 @@ int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_
     tp.tmem_cols = t.tmem_cols;
     tp.idesc = t.idesc;
     tp.a_bytes = kBlockM * kBlockK * 2;
-    tp.b_bytes = t.block_n * kBlockK * 2;
+    tp.b_bytes = t.b_rows * kBlockK * 2;
     tp.zb = role_map(p, p.Z, kBatch);
     tp.zm = role_map(p, p.Z, kM);
     tp.zn = role_map(p, p.Z, kN);
@@ -671,12 +972,32 @@ int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_
     tp.alpha = (float)p.alpha;
     tp.out_bf16 = p.out_bf16;
     tp.timeout_ns = 2000000000ull;  // 2 s per wait
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)t.smem);
-    if (e != cudaSuccess) return fail(TRA_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(e));
     const int sms = sm_count();
     if (sms <= 0) return fail(TRA_ERR_CUDA, "no device");
-    const unsigned grid = (unsigned)(t.n_tiles < (uint32_t)sms ? t.n_tiles : (uint32_t)sms);
-    tc_gemm<<<grid, kThreads, t.smem, s>>>(ma, mb, tp);
+    cudaError_t e;
+    if (t.pair) {
+        e = cudaFuncSetAttribute(tc_gemm_2sm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)t.smem);
+        if (e != cudaSuccess) return fail(TRA_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(e));
+        // persistent: one cluster per co-resident SM pair, at most one per tile
+        uint32_t clusters = (uint32_t)sms / 2;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * clusters);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = t.smem;
+        cfg.stream = s;
+        int active = 0;
+        if (cudaOccupancyMaxActiveClusters(&active, tc_gemm_2sm, &cfg) == cudaSuccess && active > 0)
+            clusters = (uint32_t)active < clusters ? (uint32_t)active : clusters;
+        else
+            (void)cudaGetLastError();
+        if (clusters > t.n_tiles) clusters = t.n_tiles;
+        tc_gemm_2sm<<<2 * clusters, kThreads, t.smem, s>>>(ma, mb, tp);
+    } else {
+        e = cudaFuncSetAttribute(tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)t.smem);
+        if (e != cudaSuccess) return fail(TRA_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(e));
+        const unsigned grid = (unsigned)(t.n_tiles < (uint32_t)sms ? t.n_tiles : (uint32_t)sms);
+        tc_gemm<<<grid, kThreads, t.smem, s>>>(ma, mb, tp);
+    }
     e = cudaGetLastError();
     return e == cudaSuccess ? TRA_OK : fail(TRA_ERR_CUDA, "tensor-core launch: %s", cudaGetErrorString(e));
 }

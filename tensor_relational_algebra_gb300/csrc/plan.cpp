@@ -150,6 +150,7 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
         else if (k == "out" && (v == "f32" || v == "bf16")) p->out_bf16 = v == "bf16";
         else if (k == "mode" && (v == "fused" || v == "literal")) p->literal = v == "literal";
         else if (k == "sqdiff" && (v == "direct" || v == "expand")) p->sqdiff_expand = v == "expand" ? 1 : 0;
+        else if (k == "tc" && (v == "pair" || v == "single")) p->tc_pair = v == "pair" ? 1 : 0;
         else if (k == "alpha") {
             char* end = nullptr;
             errno = 0;
@@ -296,8 +297,10 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
         p->ws_bytes = align256((uint64_t)p->X.total * 4) + align256((uint64_t)p->Y.total * 4) +
                       align256(nb * p->ext[kM] * 4) + align256(nb * p->ext[kN] * 4);
     } else if (p->op == kMul && p->agg == kSum && p->in_bf16 && tc_plan(p)) {
-        p->kernel = TRA_KERNEL_TC_BF16;
+        // tc_plan chose TRA_KERNEL_TC_BF16 or TRA_KERNEL_TC_BF16_PAIR
     } else {
+        if (p->tc_pair == 1 && p->op == kMul && p->agg == kSum && p->in_bf16)
+            return fail(TRA_ERR_UNSUPPORTED, "tc=pair: no 256 x 256 tensor-core tiling for this plan");
         p->kernel = TRA_KERNEL_SEMIRING_F32;
         if (p->op == kSqdiff && p->agg == kSum && p->sqdiff_expand) {
             if (p->in_bf16) return fail(TRA_ERR_UNSUPPORTED, "sqdiff=expand needs fp32 inputs");
@@ -305,7 +308,8 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
             p->ws_bytes = align256(nb * p->ext[kM] * 4) + align256(nb * p->ext[kN] * 4);
         }
     }
-    if (!p->unary && p->kernel != TRA_KERNEL_TC_BF16 && p->kernel != TRA_KERNEL_ELEMENTWISE)
+    if (!p->unary && p->kernel != TRA_KERNEL_TC_BF16 && p->kernel != TRA_KERNEL_TC_BF16_PAIR &&
+        p->kernel != TRA_KERNEL_ELEMENTWISE)
         scan_vec_flags(role_map(*p, p->X, kBatch), role_map(*p, p->X, kM), role_map(*p, p->X, kK),
                        role_map(*p, p->Y, kBatch), role_map(*p, p->Y, kN), role_map(*p, p->Y, kK),
                        role_map(*p, p->Z, kBatch), role_map(*p, p->Z, kM), role_map(*p, p->Z, kN),

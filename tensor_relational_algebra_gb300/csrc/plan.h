@@ -37,6 +37,7 @@ struct Plan {
     int in_bf16 = 0, out_bf16 = 0;
     int literal = 0;
     int sqdiff_expand = 0;
+    int tc_pair = -1;  // tensor-core tile: 1 CTA pair (256 x 256), 0 single CTA, -1 pair when shapes allow
     // vector-load eligibility of the semiring kernel's operands (host scan, see scan_vec_flags)
     int vec_flags[5] = {0, 0, 0, 0, 0};  // X along K, X along M, Y along N, Y along K, Z along N
     bool unary = false;

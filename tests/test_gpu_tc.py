@@ -40,9 +40,24 @@ CASES = [
     ("shd,ahd->sa", [256, 2, 128, 128], [1, 1, 1, 1, 1, 1], ""),
 ]
 
+# 256 x 256 tiles on a cluster of two CTAs: each CTA loads half of the X rows and half of
+# the Y rows of a tile; the tensor-core instruction reads both CTAs' shared memory.
+PAIR_CASES = [
+    ("ij,jk->ik", [256, 192, 256], [2, 3, 3, 2], ""),               # one Y key block per CTA
+    ("ij,jk->ik", [512, 256, 768], [1, 1, 1, 1], ""),               # 2 x 3 tiles
+    ("ji,jk->ik", [128, 256, 256], [2, 1, 2, 2], ""),               # M-major A
+    ("ij,kj->ik", [256, 128, 256], [2, 2, 2, 2], ""),               # K-major B
+    ("ji,kj->ik", [64, 256, 512], [1, 2, 1, 1], ""),                # both majors swapped
+    ("bij,bjk->bik", [3, 256, 128, 256], [3, 1, 2, 3, 2, 1], ""),   # batch label split into keys
+    ("bij,bjk->bik", [24, 512, 64, 512], [1, 1, 1, 1, 1, 1], ""),   # 96 tiles: clusters take several
+    ("abef,cfed->abcd", [4, 64, 8, 64, 4, 64], [2, 1, 1, 1, 2, 1, 1, 1], ""),
+    ("sa,ahd->shd", [256, 128, 2, 128], [2, 1, 1, 1, 1], ":out=bf16"),
+    ("shd,thd->hst", [256, 2, 128, 256], [1, 2, 1, 1, 2, 1], ":alpha=0.08838834764831845"),
+    ("shd,ahd->sa", [256, 2, 128, 256], [1, 1, 1, 1, 1, 1], ""),
+]
 
-@pytest.mark.parametrize("eq,bounds,d,opts", CASES)
-def test_tc_parity(lib, cuda, eq, bounds, d, opts):
+
+def _tc_case(lib, eq, bounds, d, opts, kernel):
     ins, out, order = labels_of(eq)
     B = dict(zip(order, bounds))
     X = gen(tuple(B[c] for c in ins[0]), 9, 0, bf16=True)
@@ -52,7 +67,7 @@ def test_tc_parity(lib, cuda, eq, bounds, d, opts):
     if "alpha=" in opts:
         alpha = float(opts.split("alpha=")[1].split(":")[0])
     p, g = run_plan(lib, spec, bounds, d, X, Y, out_bf16=":out=bf16" in opts)
-    assert p.kernel == "tc_bf16"
+    assert p.kernel == kernel
     r = oracle.einsum(eq, as_f64(X), as_f64(Y), alpha=alpha)
     S = oracle.einsum(eq, np.abs(as_f64(X)), np.abs(as_f64(Y))) * abs(alpha)
     check_bf16_bar(g, r)
@@ -61,6 +76,16 @@ def test_tc_parity(lib, cuda, eq, bounds, d, opts):
         assert np.all(np.abs(g - r) <= 2.0 ** -8 * np.abs(r) + FP32_REL * S)
     else:
         check_sum(g, r, S, FP32_REL)
+
+
+@pytest.mark.parametrize("eq,bounds,d,opts", CASES)
+def test_tc_parity(lib, cuda, eq, bounds, d, opts):
+    _tc_case(lib, eq, bounds, d, opts + ":tc=single", "tc_bf16")
+
+
+@pytest.mark.parametrize("eq,bounds,d,opts", PAIR_CASES)
+def test_tc_pair_parity(lib, cuda, eq, bounds, d, opts):
+    _tc_case(lib, eq, bounds, d, opts + ":tc=pair", "tc_bf16_pair")
 
 
 def test_tc_repeat_and_stream(lib, cuda):

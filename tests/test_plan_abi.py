@@ -91,6 +91,11 @@ def test_kernel_choice(lib):
     p = lib.Plan("ij,jk->ik:add:lse", [64, 32, 16], [2, 1, 1, 2])
     assert p.workspace_bytes >= (64 * 32 + 32 * 16 + 64 + 16) * 4
     assert lib.Plan("ij,jk->ik:mul:sum", [64, 64, 64], [1, 1, 1, 1]).workspace_bytes == 0
+    # BF16 sum-of-products: a 256 x 256 tile per CTA pair when rows and columns allow it
+    assert lib.Plan("ij,jk->ik:mul:sum:in=bf16", [512, 128, 256], [2, 1, 1, 1]).kernel == "tc_bf16_pair"
+    assert lib.Plan("ij,jk->ik:mul:sum:in=bf16:tc=single", [512, 128, 256], [2, 1, 1, 1]).kernel == "tc_bf16"
+    assert lib.Plan("ij,jk->ik:mul:sum:in=bf16", [384, 128, 256], [1, 1, 1, 1]).kernel == "tc_bf16"
+    assert lib.Plan("ij,jk->ik:mul:sum:in=bf16", [256, 128, 192], [1, 1, 1, 1]).kernel == "tc_bf16"
 
 
 @pytest.mark.parametrize("spec,bounds,d,code", [
@@ -107,6 +112,8 @@ def test_kernel_choice(lib):
     ("ij,jk->ik:mul:sum:alpha=x", [64, 64, 64], [1, 1, 1, 1], "TRA_ERR_PARSE"),
     ("ij,jk->ik:mul:sum:foo=1", [64, 64, 64], [1, 1, 1, 1], "TRA_ERR_PARSE"),
     ("ij,jk->ik:mul:sum", [64, 0, 64], [1, 1, 1, 1], "TRA_ERR_ARG"),
+    ("ij,jk->ik:mul:sum:in=bf16:tc=pair", [384, 128, 256], [1, 1, 1, 1], "TRA_ERR_UNSUPPORTED"),
+    ("ij,jk->ik:mul:sum:tc=both", [256, 128, 256], [1, 1, 1, 1], "TRA_ERR_PARSE"),
 ])
 def test_plan_errors(lib, spec, bounds, d, code):
     with pytest.raises(lib.TraError) as e:
