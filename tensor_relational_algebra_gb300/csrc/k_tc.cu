@@ -38,8 +38,18 @@ namespace {
 
 constexpr int kBlockM = 128;
 constexpr int kBlockK = 64;  // one 128-byte swizzle row of bf16
-constexpr int kThreads = 192;
+// Warp roles: 0-3 TMA producers (global K step g goes to producer g % kProducers: the
+// copy engine completes the copies of one issuing thread in order, so a single issuing
+// thread caps a CTA at one box per L2 round trip), 4 MMA issuer, 5-8 epilogue.
+constexpr int kProducers = 4;
+constexpr int kMmaWarp = kProducers;
+constexpr int kThreads = 32 * (kProducers + 1 + 4);
 constexpr uint32_t kMaxSmem = 227 * 1024;
+// Epilogue staging per epilogue warp: a 32 x 32 fp32 tile (16-byte groups swizzled by row)
+// and 32 row offsets.
+constexpr uint32_t kEpiTile = 32 * 32 * 4;
+constexpr uint32_t kEpiWarpBytes = kEpiTile + 32 * 8;
+constexpr uint32_t kEpiBytes = 4 * kEpiWarpBytes;
 
 struct TcOpDev {
     int32_t mn_major;  // 1: innermost dimension is M (X) / N (Y); 0: innermost is K
@@ -190,222 +200,6 @@ __device__ __forceinline__ void tile_of(const TcParams& p, uint32_t t, uint32_t&
     nt = w / gm;
 }
 
-// ------------------------------------------------------------------ the kernel
-__global__ void __launch_bounds__(kThreads, 1)
-    tc_gemm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-            const __grid_constant__ TcParams p) {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t stage_bytes = p.a_bytes + p.b_bytes;
-    const uint32_t bar0 = base + p.stages * stage_bytes;
-    // barrier block: full[S], empty[S], tfull[2], tempty[2], done, then tmem slot and abort flag
-    const uint32_t full0 = bar0, empty0 = bar0 + 8 * p.stages, tfull0 = bar0 + 16 * p.stages;
-    const uint32_t tempty0 = tfull0 + 16, done_bar = tempty0 + 16;
-    uint8_t* gbase = smem_raw + (base - raw);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (done_bar + 8 - base));
-    volatile int* abort = reinterpret_cast<volatile int*>(gbase + (done_bar + 12 - base));
-
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    if (threadIdx.x == 0) {
-        for (uint32_t s = 0; s < p.stages; ++s) {
-            mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
-        }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(tfull0 + 8 * a, 1);
-            mbar_init(tempty0 + 8 * a, 128);
-        }
-        mbar_init(done_bar, 1);
-        *abort = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(p.tmem_cols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
-
-    if (warp == 0) {
-        // ---------------------------------------------------------------- TMA producer
-        if (lane == 0) {
-            uint32_t stage = 0, phase = 0;
-            uint32_t issued_phase[8];
-            bool issued[8] = {false, false, false, false, false, false, false, false};
-            bool ok = true;
-            for (uint32_t t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
-                uint32_t b, mt, nt;
-                tile_of(p, t, b, mt, nt);
-                const uint32_t m0 = mt * kBlockM, n0 = nt * p.block_n;
-                // per load, the coordinates that stay fixed over the K loop (at most 2 loads of
-                // A and 4 of B per stage)
-                int fa[2][5], fbx[4][5];
-#pragma unroll
-                for (int l = 0; l < 2; ++l)
-                    if (l < p.a.n_loads) fixed_coords(p.a, b, m0 + 64u * l, fa[l]);
-#pragma unroll
-                for (int l = 0; l < 4; ++l)
-                    if (l < p.b.n_loads) fixed_coords(p.b, b, n0 + 64u * l, fbx[l]);
-                for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
-                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort, p.timeout_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb = full0 + 8 * stage;
-                    mbar_expect_tx(fb, stage_bytes);
-                    const uint32_t sa = base + stage * stage_bytes, sb = sa + p.a_bytes;
-                    const uint32_t k0 = kb * kBlockK;
-                    int ka[5], kbc[5], c[5];
-                    k_coords(p.a, k0, ka);
-                    k_coords(p.b, k0, kbc);
-#pragma unroll
-                    for (int l = 0; l < 2; ++l)
-                        if (l < p.a.n_loads) {
-#pragma unroll
-                            for (int j = 0; j < 5; ++j) c[j] = fa[l][j] + ka[j];
-                            tma_load_5d(sa + 8192u * l, &map_a, fb, c);
-                        }
-#pragma unroll
-                    for (int l = 0; l < 4; ++l)
-                        if (l < p.b.n_loads) {
-#pragma unroll
-                            for (int j = 0; j < 5; ++j) c[j] = fbx[l][j] + kbc[j];
-                            tma_load_5d(sb + 8192u * l, &map_b, fb, c);
-                        }
-                    issued[stage] = true;
-                    issued_phase[stage] = phase;
-                    if (++stage == p.stages) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
-                }
-            }
-            if (!ok) {
-                // let every copy already issued land before the CTA leaves
-                for (uint32_t s = 0; s < p.stages; ++s)
-                    if (issued[s]) {
-                        volatile int never = 0;
-                        mbar_wait(full0 + 8 * s, issued_phase[s], &never, p.timeout_ns);
-                    }
-            }
-        }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-            bool ok = true;
-            const uint32_t a_lbo = p.a.mn_major ? 8192u : 16u, b_lbo = p.b.mn_major ? 8192u : 16u;
-            const uint32_t a_kstep = p.a.mn_major ? 2048u : 32u, b_kstep = p.b.mn_major ? 2048u : 32u;
-            for (uint32_t t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
-                if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort, p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * p.block_n;
-                for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
-                    if (!mbar_wait(full0 + 8 * stage, phase, abort, p.timeout_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t sa = base + stage * stage_bytes, sb = sa + p.a_bytes;
-#pragma unroll
-                    for (uint32_t k = 0; k < kBlockK / 16; ++k) {
-                        const uint64_t ad = smem_desc(sa + k * a_kstep, a_lbo, 1024);
-                        const uint64_t bd = smem_desc(sb + k * b_kstep, b_lbo, 1024);
-                        tc_mma(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
-                    }
-                    tc_commit(empty0 + 8 * stage);  // frees the stage once these MMAs have read it
-                    if (++stage == p.stages) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
-                }
-                if (!ok) break;
-                tc_commit(tfull0 + 8 * acc);  // accumulator ready for the epilogue
-                if (++acc == 2) {
-                    acc = 0;
-                    acc_phase ^= 1;
-                }
-            }
-            // every MMA issued so far has completed once this commit arrives
-            tc_commit(done_bar);
-            volatile int never = 0;
-            mbar_wait(done_bar, 0, &never, p.timeout_ns);
-        }
-    } else {
-        // ---------------------------------------------------------------- epilogue (warps 2-5)
-        const uint32_t q = warp & 3;  // TMEM lane quarter this warp may access
-        uint32_t acc = 0, acc_phase = 0;
-        for (uint32_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
-            uint32_t b, mt, nt;
-            tile_of(p, t, b, mt, nt);
-            if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort, p.timeout_ns)) break;
-            tc_fence_after();
-            const uint32_t row = q * 32 + lane;
-            const uint32_t m = mt * kBlockM + row;
-            const uint32_t n0 = nt * p.block_n;
-            const int64_t zrow = role_offset(p.zb, b) + role_offset(p.zm, min(m, p.M - 1));
-            for (uint32_t c = 0; c < p.block_n / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tmem_base + ((q * 32u) << 16) + acc * p.block_n + c * 32u, r);
-                const uint32_t n = n0 + c * 32u;
-                if (m >= p.M || n >= p.N) continue;
-                const int64_t off = zrow + role_offset(p.zn, n);
-                if (p.out_bf16) {
-                    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.z) + off);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) {
-                            const __nv_bfloat162 pr = __floats2bfloat162_rn(p.alpha * __uint_as_float(r[8 * v + 2 * h]),
-                                                                           p.alpha * __uint_as_float(r[8 * v + 2 * h + 1]));
-                            w[h] = *reinterpret_cast<const uint32_t*>(&pr);
-                        }
-                        dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
-                } else {
-                    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.z) + off);
-#pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        dst[v] = make_float4(p.alpha * __uint_as_float(r[4 * v]), p.alpha * __uint_as_float(r[4 * v + 1]),
-                                             p.alpha * __uint_as_float(r[4 * v + 2]),
-                                             p.alpha * __uint_as_float(r[4 * v + 3]));
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(tempty0 + 8 * acc);
-            if (++acc == 2) {
-                acc = 0;
-                acc_phase ^= 1;
-            }
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        __syncwarp();
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(p.tmem_cols)
-                     : "memory");
-    }
-}
-
-// ------------------------------------------------------------------ CTA-pair kernel
-// Two CTAs of a cluster share one 256 x 256 output tile: tcgen05.mma.cta_group::2
-// (M = 256, N = 256) issued by the even CTA reads A rows 0-127 and B rows 0-127 from its
-// own shared memory and A rows 128-255 / B rows 128-255 from the odd CTA's, and writes
-// accumulator rows 0-127 to the even CTA's tensor memory, rows 128-255 to the odd CTA's.
-// Each SM therefore loads half of B per K step (32 KB instead of 48 KB for the same MMA
-// work), which is what the L2 -> SM delivery rate limits.
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -477,6 +271,291 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t ctamask) {
         : "memory");
 }
 
+// One producer thread's share of the K steps of every tile this CTA (or CTA pair) owns:
+// steps g = pw, pw + kProducers, ...  Stage g % stages, phase (g / stages) & 1.  A parity
+// wait cannot alias an older phase because stages >= kProducers: when this thread reaches
+// step g it has seen step g - kProducers - stages released, and releases are in order.
+// PAIR: the copy of this CTA's half counts on the even CTA's full barrier (cta_group::2).
+template <bool PAIR>
+__device__ __forceinline__ void producer_steps(const CUtensorMap* map_a, const CUtensorMap* map_b, const TcParams& p,
+                                               uint32_t pw, uint32_t first_tile, uint32_t tile_step, uint32_t rank,
+                                               uint32_t base, uint32_t full0, uint32_t empty0, volatile int* abort) {
+    const uint32_t stage_bytes = p.a_bytes + p.b_bytes;
+    const uint32_t n_local = first_tile < p.n_tiles ? (p.n_tiles - first_tile + tile_step - 1) / tile_step : 0u;
+    const uint32_t total = n_local * p.num_kb;
+    uint32_t cur = 0xffffffffu;
+    int fa[2][5], fbx[4][5];
+    uint32_t pend_stage[2] = {0, 0}, pend_phase[2] = {0, 0}, n_pend = 0;
+    bool ok = true;
+    for (uint32_t g = pw; g < total; g += kProducers) {
+        const uint32_t i = g / p.num_kb, kb = g - i * p.num_kb;
+        if (i != cur) {
+            cur = i;
+            uint32_t b, mt, nt;
+            tile_of(p, first_tile + i * tile_step, b, mt, nt);
+            const uint32_t m0 = PAIR ? mt * 2 * kBlockM + rank * kBlockM : mt * kBlockM;
+            const uint32_t n0 = PAIR ? nt * p.block_n + rank * (p.block_n / 2) : nt * p.block_n;
+#pragma unroll
+            for (int l = 0; l < 2; ++l)
+                if (l < p.a.n_loads) fixed_coords(p.a, b, m0 + 64u * l, fa[l]);
+#pragma unroll
+            for (int l = 0; l < 4; ++l)
+                if (l < p.b.n_loads) fixed_coords(p.b, b, n0 + 64u * l, fbx[l]);
+        }
+        const uint32_t stage = g % p.stages, phase = (g / p.stages) & 1u;
+        const bool got = PAIR ? mbar_wait_cl(empty0 + 8 * stage, phase ^ 1, abort, p.timeout_ns)
+                              : mbar_wait(empty0 + 8 * stage, phase ^ 1, abort, p.timeout_ns);
+        if (!got) {
+            ok = false;
+            break;
+        }
+        const uint32_t fb = full0 + 8 * stage;
+        uint32_t fb_sig = fb;
+        if (PAIR) {
+            if (rank == 0) mbar_expect_tx(fb, 2 * stage_bytes);  // both CTAs' bytes land on the even CTA's barrier
+            fb_sig = mapa_shared(fb, 0);
+        } else {
+            mbar_expect_tx(fb, stage_bytes);
+        }
+        const uint32_t sa = base + stage * stage_bytes, sb = sa + p.a_bytes;
+        const uint32_t k0 = kb * kBlockK;
+        int ka[5], kbc[5], c[5];
+        k_coords(p.a, k0, ka);
+        k_coords(p.b, k0, kbc);
+#pragma unroll
+        for (int l = 0; l < 2; ++l)
+            if (l < p.a.n_loads) {
+#pragma unroll
+                for (int j = 0; j < 5; ++j) c[j] = fa[l][j] + ka[j];
+                if (PAIR) tma_load_5d_pair(sa + 8192u * l, map_a, fb_sig, c);
+                else tma_load_5d(sa + 8192u * l, map_a, fb_sig, c);
+            }
+#pragma unroll
+        for (int l = 0; l < 4; ++l)
+            if (l < p.b.n_loads) {
+#pragma unroll
+                for (int j = 0; j < 5; ++j) c[j] = fbx[l][j] + kbc[j];
+                if (PAIR) tma_load_5d_pair(sb + 8192u * l, map_b, fb_sig, c);
+                else tma_load_5d(sb + 8192u * l, map_b, fb_sig, c);
+            }
+        pend_stage[n_pend & 1] = stage;
+        pend_phase[n_pend & 1] = phase;
+        ++n_pend;
+    }
+    if (!ok) {
+        // let the copies this thread issued land before the CTA leaves (at most
+        // ceil(stages / kProducers) <= 2 are outstanding)
+        if (PAIR) {
+            __nanosleep(20000);  // the pair's copies count on the even CTA's barriers
+        } else {
+            volatile int never = 0;
+            for (uint32_t j = 0; j < 2 && j < n_pend; ++j) mbar_wait(full0 + 8 * pend_stage[j], pend_phase[j], &never, p.timeout_ns);
+        }
+    }
+}
+
+// tcgen05.ld of 32 consecutive accumulator columns for this warp's 32 lanes (no wait)
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+// Store one 32 x 32 accumulator block (thread = row, r = its 32 columns starting at n).
+// The block goes through shared memory as 16-byte groups, group g of row w at slot
+// g ^ (w & 7): the row-wise writes (8 rows per phase) and the column-wise reads (one row
+// per 8 lanes) are both conflict-free, and each global store instruction of the warp writes
+// whole row segments (4 rows x 128 bytes fp32, or 8 rows x 64 bytes bf16).
+__device__ __forceinline__ void store_block(const TcParams& p, float4* stg, const int64_t* zr, int lane,
+                                            const uint32_t (&r)[32], uint32_t n) {
+    if (n >= p.N) return;  // uniform over the warp
+    const int64_t zc = role_offset(p.zn, n);
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+        stg[lane * 8 + (g ^ (lane & 7))] =
+            make_float4(p.alpha * __uint_as_float(r[4 * g]), p.alpha * __uint_as_float(r[4 * g + 1]),
+                        p.alpha * __uint_as_float(r[4 * g + 2]), p.alpha * __uint_as_float(r[4 * g + 3]));
+    __syncwarp();
+    if (p.out_bf16) {
+        __nv_bfloat16* z = reinterpret_cast<__nv_bfloat16*>(p.z);
+        const int sub = lane & 3;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int row = 8 * i + (lane >> 2);
+            const float4 v0 = stg[row * 8 + ((2 * sub) ^ (row & 7))];
+            const float4 v1 = stg[row * 8 + ((2 * sub + 1) ^ (row & 7))];
+            const int64_t o = zr[row];
+            __nv_bfloat162 h[4] = {__floats2bfloat162_rn(v0.x, v0.y), __floats2bfloat162_rn(v0.z, v0.w),
+                                   __floats2bfloat162_rn(v1.x, v1.y), __floats2bfloat162_rn(v1.z, v1.w)};
+            if (o >= 0) *reinterpret_cast<uint4*>(z + o + zc + 8 * sub) = *reinterpret_cast<const uint4*>(h);
+        }
+    } else {
+        float* z = reinterpret_cast<float*>(p.z);
+        const int g = lane & 7;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int row = 4 * i + (lane >> 3);
+            const float4 v = stg[row * 8 + (g ^ (row & 7))];
+            const int64_t o = zr[row];
+            if (o >= 0) *reinterpret_cast<float4*>(z + o + zc + 4 * g) = v;
+        }
+    }
+    __syncwarp();
+}
+
+// Epilogue of one tile for one epilogue warp: TMEM lane quarter q holds 32 rows of the
+// accumulator (thread = row m); the columns n0 .. n0 + block_n - 1 go out two 32-column
+// blocks at a time (both TMEM loads in flight before the wait).
+__device__ __forceinline__ void epilogue_tile(const TcParams& p, uint8_t* epi, uint32_t tmem_acc, uint32_t q, int lane,
+                                              uint32_t b, uint32_t m, uint32_t n0) {
+    float4* stg = reinterpret_cast<float4*>(epi + q * kEpiWarpBytes);
+    int64_t* zr = reinterpret_cast<int64_t*>(epi + q * kEpiWarpBytes + kEpiTile);
+    zr[lane] = m < p.M ? role_offset(p.zb, b) + role_offset(p.zm, m) : (int64_t)-1;
+    __syncwarp();
+    const uint32_t taddr = tmem_acc + ((q * 32u) << 16);
+    for (uint32_t c = 0; c < p.block_n / 32; c += 2) {  // block_n is a multiple of 64
+        uint32_t ra[32], rb[32];
+        tmem_ld32_nowait(taddr + c * 32u, ra);
+        tmem_ld32_nowait(taddr + c * 32u + 32u, rb);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        store_block(p, stg, zr, lane, ra, n0 + c * 32u);
+        store_block(p, stg, zr, lane, rb, n0 + c * 32u + 32u);
+    }
+}
+
+// ------------------------------------------------------------------ the kernel
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+            const __grid_constant__ TcParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t stage_bytes = p.a_bytes + p.b_bytes;
+    const uint32_t bar0 = base + p.stages * stage_bytes;
+    // barrier block: full[S], empty[S], tfull[2], tempty[2], done, then tmem slot and abort flag
+    const uint32_t full0 = bar0, empty0 = bar0 + 8 * p.stages, tfull0 = bar0 + 16 * p.stages;
+    const uint32_t tempty0 = tfull0 + 16, done_bar = tempty0 + 16;
+    uint8_t* gbase = smem_raw + (base - raw);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (done_bar + 8 - base));
+    volatile int* abort = reinterpret_cast<volatile int*>(gbase + (done_bar + 12 - base));
+    uint8_t* epi = gbase + (bar0 + 256 - base);  // epilogue staging (kEpiBytes)
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < p.stages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull0 + 8 * a, 1);
+            mbar_init(tempty0 + 8 * a, 128);
+        }
+        mbar_init(done_bar, 1);
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(p.tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp < kProducers) {
+        // ---------------------------------------------------------------- TMA producers
+        if (lane == 0)
+            producer_steps<false>(&map_a, &map_b, p, (uint32_t)warp, blockIdx.x, gridDim.x, 0u, base, full0, empty0, abort);
+    } else if (warp == kMmaWarp) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            const uint32_t a_lbo = p.a.mn_major ? 8192u : 16u, b_lbo = p.b.mn_major ? 8192u : 16u;
+            const uint32_t a_kstep = p.a.mn_major ? 2048u : 32u, b_kstep = p.b.mn_major ? 2048u : 32u;
+            for (uint32_t t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+                if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * p.block_n;
+                for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait(full0 + 8 * stage, phase, abort, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base + stage * stage_bytes, sb = sa + p.a_bytes;
+#pragma unroll
+                    for (uint32_t k = 0; k < kBlockK / 16; ++k) {
+                        const uint64_t ad = smem_desc(sa + k * a_kstep, a_lbo, 1024);
+                        const uint64_t bd = smem_desc(sb + k * b_kstep, b_lbo, 1024);
+                        tc_mma(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
+                    }
+                    tc_commit(empty0 + 8 * stage);  // frees the stage once these MMAs have read it
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(tfull0 + 8 * acc);  // accumulator ready for the epilogue
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1;
+                }
+            }
+            // every MMA issued so far has completed once this commit arrives
+            tc_commit(done_bar);
+            volatile int never = 0;
+            mbar_wait(done_bar, 0, &never, p.timeout_ns);
+        }
+    } else {
+        // ---------------------------------------------------------------- epilogue (warps 5-8)
+        const uint32_t q = warp & 3;  // TMEM lane quarter this warp may access
+        uint32_t acc = 0, acc_phase = 0;
+        for (uint32_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
+            uint32_t b, mt, nt;
+            tile_of(p, t, b, mt, nt);
+            if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort, p.timeout_ns)) break;
+            tc_fence_after();
+            epilogue_tile(p, epi, tmem_base + acc * p.block_n, q, lane, b, mt * kBlockM + q * 32 + lane, nt * p.block_n);
+            tc_fence_before();
+            mbar_arrive(tempty0 + 8 * acc);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(p.tmem_cols)
+                     : "memory");
+    }
+}
+
+// ------------------------------------------------------------------ CTA-pair kernel
+// Two CTAs of a cluster share one 256 x 256 output tile: tcgen05.mma.cta_group::2
+// (M = 256, N = 256) issued by the even CTA reads A rows 0-127 and B rows 0-127 from its
+// own shared memory and A rows 128-255 / B rows 128-255 from the odd CTA's, and writes
+// accumulator rows 0-127 to the even CTA's tensor memory, rows 128-255 to the odd CTA's.
+// Each SM therefore loads half of B per K step (32 KB instead of 48 KB for the same MMA
+// work).
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_gemm_2sm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                 const __grid_constant__ TcParams p) {
@@ -490,6 +569,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint8_t* gbase = smem_raw + (base - raw);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (done_bar + 8 - base));
     volatile int* abort = reinterpret_cast<volatile int*>(gbase + (done_bar + 12 - base));
+    uint8_t* epi = gbase + (bar0 + 256 - base);  // epilogue staging (kEpiBytes)
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t rank = cluster_rank();
@@ -508,7 +588,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(p.tmem_cols)
                      : "memory");
@@ -520,56 +600,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 0) {
-        // ---------------------------------------------------------------- TMA producer (both CTAs)
-        if (lane == 0) {
-            uint32_t stage = 0, phase = 0;
-            bool ok = true;
-            for (uint32_t t = pair; t < p.n_tiles && ok; t += n_pairs) {
-                uint32_t b, mt, nt;
-                tile_of(p, t, b, mt, nt);
-                const uint32_t m0 = mt * 2 * kBlockM + rank * kBlockM, n0 = nt * p.block_n + rank * (p.block_n / 2);
-                int fa[2][5], fbx[2][5];
-#pragma unroll
-                for (int l = 0; l < 2; ++l) {
-                    if (l < p.a.n_loads) fixed_coords(p.a, b, m0 + 64u * l, fa[l]);
-                    if (l < p.b.n_loads) fixed_coords(p.b, b, n0 + 64u * l, fbx[l]);
-                }
-                for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
-                    if (!mbar_wait_cl(empty0 + 8 * stage, phase ^ 1, abort, p.timeout_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb = full0 + 8 * stage;
-                    if (leader) mbar_expect_tx(fb, 2 * stage_bytes);
-                    const uint32_t fb_leader = mapa_shared(fb, 0);
-                    const uint32_t sa = base + stage * stage_bytes, sb = sa + p.a_bytes;
-                    const uint32_t k0 = kb * kBlockK;
-                    int ka[5], kbc[5], c[5];
-                    k_coords(p.a, k0, ka);
-                    k_coords(p.b, k0, kbc);
-#pragma unroll
-                    for (int l = 0; l < 2; ++l) {
-                        if (l < p.a.n_loads) {
-#pragma unroll
-                            for (int j = 0; j < 5; ++j) c[j] = fa[l][j] + ka[j];
-                            tma_load_5d_pair(sa + 8192u * l, &map_a, fb_leader, c);
-                        }
-                        if (l < p.b.n_loads) {
-#pragma unroll
-                            for (int j = 0; j < 5; ++j) c[j] = fbx[l][j] + kbc[j];
-                            tma_load_5d_pair(sb + 8192u * l, &map_b, fb_leader, c);
-                        }
-                    }
-                    if (++stage == p.stages) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
-                }
-            }
-            if (!ok) __nanosleep(20000);  // let copies already issued land before leaving
-        }
-    } else if (warp == 1) {
+    if (warp < kProducers) {
+        // ---------------------------------------------------------------- TMA producers (both CTAs)
+        if (lane == 0)
+            producer_steps<true>(&map_a, &map_b, p, (uint32_t)warp, pair, n_pairs, rank, base, full0, empty0, abort);
+    } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer (even CTA)
         if (lane == 0 && leader) {
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
@@ -614,7 +649,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_wait_cl(done_bar, 0, &never, p.timeout_ns);
         }
     } else {
-        // ---------------------------------------------------------------- epilogue (warps 2-5, both CTAs)
+        // ---------------------------------------------------------------- epilogue (warps 5-8, both CTAs)
         const uint32_t q = warp & 3;
         uint32_t acc = 0, acc_phase = 0;
         for (uint32_t t = pair; t < p.n_tiles; t += n_pairs) {
@@ -622,37 +657,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tile_of(p, t, b, mt, nt);
             if (!mbar_wait_cl(tfull0 + 8 * acc, acc_phase, abort, p.timeout_ns)) break;
             tc_fence_after();
-            const uint32_t m = mt * 2 * kBlockM + rank * kBlockM + q * 32 + lane;
-            const uint32_t n0 = nt * p.block_n;
-            const int64_t zrow = role_offset(p.zb, b) + role_offset(p.zm, min(m, p.M - 1));
-            for (uint32_t c = 0; c < p.block_n / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tmem_base + ((q * 32u) << 16) + acc * p.block_n + c * 32u, r);
-                const uint32_t n = n0 + c * 32u;
-                if (m >= p.M || n >= p.N) continue;
-                const int64_t off = zrow + role_offset(p.zn, n);
-                if (p.out_bf16) {
-                    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.z) + off);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) {
-                            const __nv_bfloat162 pr = __floats2bfloat162_rn(p.alpha * __uint_as_float(r[8 * v + 2 * h]),
-                                                                           p.alpha * __uint_as_float(r[8 * v + 2 * h + 1]));
-                            w[h] = *reinterpret_cast<const uint32_t*>(&pr);
-                        }
-                        dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
-                } else {
-                    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.z) + off);
-#pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        dst[v] = make_float4(p.alpha * __uint_as_float(r[4 * v]), p.alpha * __uint_as_float(r[4 * v + 1]),
-                                             p.alpha * __uint_as_float(r[4 * v + 2]),
-                                             p.alpha * __uint_as_float(r[4 * v + 3]));
-                }
-            }
+            epilogue_tile(p, epi, tmem_base + acc * p.block_n, q, lane, b, mt * 2 * kBlockM + rank * kBlockM + q * 32 + lane,
+                          nt * p.block_n);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty0 + 8 * acc, 0));
@@ -666,7 +672,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // the even CTA's MMAs have finished with the odd CTA's memory
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         __syncwarp();
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(p.tmem_cols)
@@ -882,18 +888,22 @@ bool tc_plan(Plan* p) {
     t->block_n = bn;
     t->b_rows = t->pair ? bn / 2 : bn;
     const uint32_t stage = (uint32_t)(kBlockM * kBlockK * 2 + t->b_rows * kBlockK * 2);
-    t->stages = (kMaxSmem - 2048) / stage;
+    t->stages = (kMaxSmem - 1024 - 256 - kEpiBytes) / stage;
     if (t->stages > 8) t->stages = 8;
-    if (t->stages < 2) {
+    if (t->stages < (uint32_t)kProducers) {  // the producers' parity waits need stages >= kProducers
         delete t;
         return false;
     }
-    t->smem = t->stages * stage + 1024 + 256;
+    t->smem = t->stages * stage + 1024 + 256 + kEpiBytes;
     const uint32_t tile_m = t->pair ? 2 * kBlockM : kBlockM;
     t->tiles_m = (uint32_t)(M / tile_m);
     t->tiles_n = (uint32_t)(N / bn);
     t->n_tiles = (uint32_t)(p->ext[kBatch] * t->tiles_m * t->tiles_n);
     t->num_kb = (uint32_t)(K / kBlockK);
+    if ((uint64_t)t->n_tiles * t->num_kb >= (1ull << 31)) {  // K steps are counted in 32 bits
+        delete t;
+        return false;
+    }
     t->tmem_cols = 2 * bn <= 128 ? 128 : (2 * bn <= 256 ? 256 : 512);
     t->idesc = (1u << 4)                                   // D: fp32
                | (1u << 7) | (1u << 10)                    // A, B: bf16
