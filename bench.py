@@ -48,9 +48,10 @@ def measured_peaks():
 
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi samples (every 50 ms, stamped by nvidia-smi itself) of SM clock and throttle
+    reasons; only the samples stamped inside the timed region count."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -65,46 +66,72 @@ class ClockSampler:
             pass
         self.proc = None
         self.lines = []
+        self.region = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except OSError:
             self.proc = None
+            return
+        t0 = time.time()  # wait (at most 3 s) for the first sample so the region is covered
+        while not self.lines and time.time() - t0 < 3.0:
+            time.sleep(0.01)
 
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def mark(self, t_begin: float, t_end: float):
+        """Wall-clock (time.time()) bounds of the timed region."""
+        self.region = (t_begin, t_end)
+
+    @staticmethod
+    def _stamp(text):
+        import datetime
+
+        try:
+            return datetime.datetime.strptime(text.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.25)
+        time.sleep(0.12)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                rows.append((self._stamp(parts[0]), float(parts[2]), float(parts[3]), parts[6:10]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
+        inside = rows
+        if self.region:
+            lo, hi = self.region
+            inside = [r for r in rows if r[0] is not None and lo - 0.025 <= r[0] <= hi + 0.025]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for n, v in zip(names, r[3]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        sm = [r[1] for r in inside]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(r[2] for r in rows) if rows else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "sm_mhz_min": min(sm) if sm else None, "sampled": "nvidia-smi every 50 ms inside the timed region"}
 
 
 # ----------------------------------------------------------------------------- workloads
@@ -475,11 +502,14 @@ def time_steps(torch, wl, steps, warmup, flush, sampler=None, e2e_io=None):
         sampler.start()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
+    w0 = time.time()
     for _ in range(steps):
         recs.append(one_step(True))
         flush()
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
+    if sampler:
+        sampler.mark(w0, time.time())
     clocks = sampler.stop() if sampler else None
     step_ms = [r[0].elapsed_time(r[-1]) for r in recs]
     off = 1 if e2e_io else 0
@@ -595,19 +625,22 @@ def run_ours(args):
     means = [statistics.mean(p) for p in per]
     dom = max(range(len(wl.steps)), key=lambda j: means[j])
     st = wl.steps[dom]
-    dur_s = means[dom] * 1e-3 / st.launches if st.launches else means[dom] * 1e-3
-    if st.bound == "alu":
-        peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
-        achieved = st.work / (means[dom] * 1e-3) / 1e12
-        unit = "TFLOP/s"
-    elif st.bound == "tensor":
-        peak = float(peaks.get("bf16_tflops", 1900.0))
-        achieved = st.work / (means[dom] * 1e-3) / 1e12
-        unit = "TFLOP/s"
-    else:
-        peak = float(peaks.get("hbm_gbs", 6800.0))
-        achieved = st.work / (means[dom] * 1e-3) / 1e9
-        unit = "GB/s"
+
+    def roof(step, ms):
+        """(achieved, peak, unit) of one launch group from its mean device time."""
+        if step.bound == "alu":
+            pk = props.multi_processor_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+            return step.work / (ms * 1e-3) / 1e12, pk, "TFLOP/s"
+        if step.bound == "tensor":
+            return step.work / (ms * 1e-3) / 1e12, float(peaks.get("bf16_tflops", 1900.0)), "TFLOP/s"
+        return step.work / (ms * 1e-3) / 1e9, float(peaks.get("hbm_gbs", 6800.0)), "GB/s"
+
+    achieved, peak, unit = roof(st, means[dom])
+    nodes = []
+    for step, ms in zip(wl.steps, means):
+        a, pk, u = roof(step, ms)
+        nodes.append({"name": step.name, "bound": step.bound, "ms": round(ms, 4), "achieved": round(a, 1),
+                      "unit": u, "frac": round(a / pk, 3)})
     traffic = traffic_for(*wl.traffic_key(dom)) if hasattr(wl, "traffic_key") else None
 
     cpu = None
@@ -632,6 +665,12 @@ def run_ours(args):
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": ("derived: SMs x 128 FP32 lanes x 2 x max SM clock (MEASURED_PEAKS sm_max_mhz)"
                                      if st.bound == "alu" else "MEASURED_PEAKS.json (of measured)")},
+        "roofline_nodes": nodes,
+        "alu_peak_at_sampled_clock": (
+            {"sm_mhz": clocks["sm_mhz"],
+             "peak": props.multi_processor_count * FP32_LANES_PER_SM * 2 * clocks["sm_mhz"] * 1e6 / 1e12,
+             "frac": achieved / (props.multi_processor_count * FP32_LANES_PER_SM * 2 * clocks["sm_mhz"] * 1e6 / 1e12)}
+            if st.bound == "alu" and clocks and clocks.get("sm_mhz") else None),
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d_bytes,
                 "d2h_bytes_per_step": d2h_bytes},

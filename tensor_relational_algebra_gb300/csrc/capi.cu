@@ -408,6 +408,8 @@ int ein_repartition(int rank, const int64_t* shape, const int32_t* src_d, const 
     rp.vec_bytes = vb;
     rp.vec_elems = vb / elem_bytes;
     rp.n_vec = (uint64_t)total / rp.vec_elems;
+    const int64_t run_vec = run / rp.vec_elems;  // vectors over which both layouts stay contiguous
+    rp.group = run_vec % 4 == 0 ? 4 : (run_vec % 2 == 0 ? 2 : 1);
     cudaError_t e = launch_repartition(rp, s);
     return e == cudaSuccess ? TRA_OK : cuda_fail(e, "repartition launch");
 }

@@ -29,29 +29,70 @@ __device__ __forceinline__ void st_f(void* p, int64_t off, float v, int bf16) {
 }
 
 // ---------------------------------------------------------------- repartition
-template <typename V>
-__global__ void repartition_kernel(const __grid_constant__ RepartParams p) {
+// Source offset (in elements) of the element that sits at destination position e:
+// decode e into (destination key, local index) per dimension, rebuild the global index
+// g, and re-encode g under the source partition.
+__device__ __forceinline__ int64_t repart_src_offset(const RepartParams& p, uint32_t e) {
+    uint32_t key = fdiv(e, p.dst_sub_total);
+    uint32_t loc = e - key * p.dst_sub_total.d;
+    int64_t so = 0;
+    for (int i = p.rank - 1; i >= 0; --i) {
+        const uint32_t kq = fdiv(key, p.dst_grid[i]);
+        const uint32_t ki = key - kq * p.dst_grid[i].d;
+        key = kq;
+        const uint32_t lq = fdiv(loc, p.dst_sub[i]);
+        const uint32_t li = loc - lq * p.dst_sub[i].d;
+        loc = lq;
+        const uint32_t g = ki * p.dst_sub[i].d + li;
+        const uint32_t sq = fdiv(g, p.src_sub[i]);
+        so += (int64_t)sq * p.src_key_stride[i] + (int64_t)(g - sq * p.src_sub[i].d) * p.src_loc_stride[i];
+    }
+    return so;
+}
+
+// Destination-ordered copy.  A warp takes chunks of 128 consecutive destination vectors
+// (V = up to 16 bytes).  The source is contiguous over runs of G vectors (G = 1, 2 or 4
+// divides the run length shared by both layouts), so each lane decodes the source offset
+// of 4 / G segments and the lanes that copy a segment read its offset by shuffle.  Copy
+// instruction j of the warp then reads segments 32j / G .. and writes 32 consecutive
+// vectors, and each lane has 4 loads in flight before its stores.  Grid: persistent.
+template <typename V, int G>
+__global__ void __launch_bounds__(256) repartition_kernel(const __grid_constant__ RepartParams p) {
     const V* __restrict__ src = reinterpret_cast<const V*>(p.src);
     V* __restrict__ dst = reinterpret_cast<V*>(p.dst);
-    for (uint64_t v = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; v < p.n_vec;
-         v += (uint64_t)gridDim.x * blockDim.x) {
-        const uint32_t e = (uint32_t)(v * p.vec_elems);  // first element, destination physical order
-        uint32_t key = fdiv(e, p.dst_sub_total);
-        uint32_t loc = e - key * p.dst_sub_total.d;
-        int64_t so = 0;
-        for (int i = p.rank - 1; i >= 0; --i) {
-            const uint32_t kq = fdiv(key, p.dst_grid[i]);
-            const uint32_t ki = key - kq * p.dst_grid[i].d;
-            key = kq;
-            const uint32_t lq = fdiv(loc, p.dst_sub[i]);
-            const uint32_t li = loc - lq * p.dst_sub[i].d;
-            loc = lq;
-            const uint32_t g = ki * p.dst_sub[i].d + li;
-            const uint32_t sq = fdiv(g, p.src_sub[i]);
-            so += (int64_t)sq * p.src_key_stride[i] + (int64_t)(g - sq * p.src_sub[i].d) * p.src_loc_stride[i];
+    const int lane = threadIdx.x & 31;
+    const int vsh = __ffs(p.vec_elems) - 1;  // vec_elems is a power of two; segments start on vectors
+    const uint64_t n_chunks = (p.n_vec + 127) / 128;
+    const uint64_t warps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
+    for (uint64_t chunk = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; chunk < n_chunks; chunk += warps) {
+        const uint64_t c0 = chunk * 128;
+        int64_t seg[4 / G];
+#pragma unroll
+        for (int i = 0; i < 4 / G; ++i) {
+            const uint64_t v = c0 + (uint64_t)(lane + 32 * i) * G;
+            seg[i] = v < p.n_vec ? repart_src_offset(p, (uint32_t)(v << vsh)) >> vsh : 0;
         }
-        dst[v] = src[so / p.vec_elems];
+        V val[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int pos = 32 * j + lane;
+            const int64_t so = __shfl_sync(0xffffffffu, seg[(32 * j) / (32 * G)], (pos / G) & 31) + pos % G;
+            if (c0 + pos < p.n_vec) val[j] = __ldcs(src + so);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (c0 + 32 * j + lane < p.n_vec) dst[c0 + 32 * j + lane] = val[j];
     }
+}
+
+template <typename V>
+cudaError_t launch_repartition_v(const RepartParams& p, unsigned g, cudaStream_t s) {
+    switch (p.group) {
+        case 4: repartition_kernel<V, 4><<<g, 256, 0, s>>>(p); break;
+        case 2: repartition_kernel<V, 2><<<g, 256, 0, s>>>(p); break;
+        default: repartition_kernel<V, 1><<<g, 256, 0, s>>>(p); break;
+    }
+    return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- unary aggregation
@@ -221,20 +262,38 @@ unsigned grid_for(uint64_t work, unsigned per_block) {
     return (unsigned)(b ? b : 1);
 }
 
+// CTAs for a grid-stride kernel: enough to fill every SM at its occupancy, no more than
+// the work needs.
+template <typename K>
+unsigned persistent_grid(uint64_t work, unsigned per_block, K kernel, int max_per_sm = 64) {
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0) != cudaSuccess || per_sm < 1) {
+        (void)cudaGetLastError();
+        per_sm = 4;
+    }
+    if (per_sm > max_per_sm) per_sm = max_per_sm;
+    const uint64_t need = (work + per_block - 1) / per_block;
+    const uint64_t full = (uint64_t)(sms > 0 ? sms : 1) * per_sm;
+    return (unsigned)(need < full ? (need ? need : 1) : full);
+}
+
 }  // namespace
 
 cudaError_t launch_repartition(const RepartParams& p, cudaStream_t s) {
     if (p.n_vec == 0) return cudaSuccess;
-    const unsigned g = grid_for(p.n_vec, 256);
+    // 4 CTAs (32 warps) per SM keep 64 KB of loads in flight per SM and give every warp
+    // several 2 KB chunks, so the last round is a small share of the copy
+    const unsigned g = persistent_grid(p.n_vec, 256 * 4, repartition_kernel<uint4, 4>, 4);
     switch (p.vec_bytes) {
-        case 16: repartition_kernel<uint4><<<g, 256, 0, s>>>(p); break;
-        case 8: repartition_kernel<uint2><<<g, 256, 0, s>>>(p); break;
-        case 4: repartition_kernel<uint32_t><<<g, 256, 0, s>>>(p); break;
-        case 2: repartition_kernel<uint16_t><<<g, 256, 0, s>>>(p); break;
-        case 1: repartition_kernel<uint8_t><<<g, 256, 0, s>>>(p); break;
+        case 16: return launch_repartition_v<uint4>(p, g, s);
+        case 8: return launch_repartition_v<uint2>(p, g, s);
+        case 4: return launch_repartition_v<uint32_t>(p, g, s);
+        case 2: return launch_repartition_v<uint16_t>(p, g, s);
+        case 1: return launch_repartition_v<uint8_t>(p, g, s);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_row_reduce(const RowReduceParams& p, cudaStream_t s) {

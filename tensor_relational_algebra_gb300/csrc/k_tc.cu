@@ -869,13 +869,19 @@ bool tc_plan(Plan* p) {
     const int zl = p->Z.label[p->Z.rank - 1];
     if (zl != p->comp[kN][0] || (p->B[zl] / p->D[zl]) % 32) return false;
     TcPlan* t = new TcPlan();
-    // a CTA pair: 256 x 256 output tile, each CTA loads 128 rows of X and 128 rows of Y
+    // a CTA pair: 256 x bn output tile (bn = 256 or 128), each CTA loads 128 rows of X and
+    // bn / 2 rows of Y
     bool ok = false;
-    if (p->tc_pair != 0 && M % 256 == 0 && N % 256 == 0) {
-        ok = plan_operands(*p, kBlockM, 128, t);
+    uint32_t bn = N % 256 == 0 ? 256 : 128;
+    if (p->tc_pair != 0 && M % 256 == 0 && N % 128 == 0) {
+        ok = plan_operands(*p, kBlockM, bn / 2, t);
+        if (!ok && bn == 256) {
+            bn = 128;
+            *t = TcPlan();
+            ok = plan_operands(*p, kBlockM, bn / 2, t);
+        }
         t->pair = ok;
     }
-    uint32_t bn = 256;
     if (!ok && p->tc_pair != 1) {
         bn = N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : 64);
         *t = TcPlan();
@@ -905,7 +911,7 @@ bool tc_plan(Plan* p) {
         return false;
     }
     t->tmem_cols = 2 * bn <= 128 ? 128 : (2 * bn <= 256 ? 256 : 512);
-    t->idesc = (1u << 4)                                   // D: fp32
+    t->idesc = (1u << 4)                                   // D: fp32 (M = 256 for a pair: two CTAs' rows)
                | (1u << 7) | (1u << 10)                    // A, B: bf16
                | ((uint32_t)t->a.dev.mn_major << 15)       // A major-ness
                | ((uint32_t)t->b.dev.mn_major << 16)       // B major-ness

@@ -169,6 +169,7 @@ struct RepartParams {
     int32_t elem_bytes;
     int32_t vec_elems;
     int32_t vec_bytes;
+    int32_t group;  // vectors per decoded segment (1, 2 or 4): a power of two dividing the common run
     uint64_t n_vec;
     FastDiv dst_sub_total;
     FastDiv dst_grid[TRA_MAX_RANK], dst_sub[TRA_MAX_RANK], src_sub[TRA_MAX_RANK];

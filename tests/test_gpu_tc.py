@@ -54,6 +54,10 @@ PAIR_CASES = [
     ("sa,ahd->shd", [256, 128, 2, 128], [2, 1, 1, 1, 1], ":out=bf16"),
     ("shd,thd->hst", [256, 2, 128, 256], [1, 2, 1, 1, 2, 1], ":alpha=0.08838834764831845"),
     ("shd,ahd->sa", [256, 2, 128, 256], [1, 1, 1, 1, 1, 1], ""),
+    # 256 x 128 tiles: each CTA loads 64 rows of Y per K step
+    ("ij,jk->ik", [256, 128, 128], [2, 1, 1, 2], ""),               # N-major B, one 64-wide box
+    ("ij,kj->ik", [512, 192, 384], [1, 3, 1, 3], ""),               # K-major B, 3 column tiles
+    ("hst,thd->shd", [2, 256, 256, 128], [2, 1, 1, 1, 2, 1], ":out=bf16"),  # attention A.V
 ]
 
 

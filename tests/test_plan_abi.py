@@ -96,6 +96,7 @@ def test_kernel_choice(lib):
     assert lib.Plan("ij,jk->ik:mul:sum:in=bf16:tc=single", [512, 128, 256], [2, 1, 1, 1]).kernel == "tc_bf16"
     assert lib.Plan("ij,jk->ik:mul:sum:in=bf16", [384, 128, 256], [1, 1, 1, 1]).kernel == "tc_bf16"
     assert lib.Plan("ij,jk->ik:mul:sum:in=bf16", [256, 128, 192], [1, 1, 1, 1]).kernel == "tc_bf16"
+    assert lib.Plan("ij,jk->ik:mul:sum:in=bf16", [256, 128, 384], [1, 1, 1, 1]).kernel == "tc_bf16_pair"
 
 
 @pytest.mark.parametrize("spec,bounds,d,code", [
