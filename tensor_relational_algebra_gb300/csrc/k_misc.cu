@@ -283,9 +283,7 @@ unsigned persistent_grid(uint64_t work, unsigned per_block, K kernel, int max_pe
 
 cudaError_t launch_repartition(const RepartParams& p, cudaStream_t s) {
     if (p.n_vec == 0) return cudaSuccess;
-    // 4 CTAs (32 warps) per SM keep 64 KB of loads in flight per SM and give every warp
-    // several 2 KB chunks, so the last round is a small share of the copy
-    const unsigned g = persistent_grid(p.n_vec, 256 * 4, repartition_kernel<uint4, 4>, 4);
+    const unsigned g = persistent_grid(p.n_vec, 256 * 4, repartition_kernel<uint4, 4>);
     switch (p.vec_bytes) {
         case 16: return launch_repartition_v<uint4>(p, g, s);
         case 8: return launch_repartition_v<uint2>(p, g, s);
