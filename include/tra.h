@@ -104,9 +104,11 @@ enum {
  *         out=f32|bf16 (default f32), alpha=<float> (scales the aggregated value),
  *         mode=fused|literal (literal materialises one partial per join tuple and
  *         combines them in canonical order), sqdiff=direct|expand,
- *         tc=pair|single (BF16 sum-of-products on tensor cores: a 256 x 256 tile
+ *         tc=pair|single (BF16 sum-of-products on tensor cores: a 256-row tile
  *         shared by a cluster of two CTAs, or a 128-row tile per CTA; default pair
- *         when the output rows and columns are multiples of 256).
+ *         when the output rows are a multiple of 256 and the columns of 128),
+ *         tc_n=256|128 (width of the pair tile; by default 256 where the columns
+ *         allow, else 128).
  * bounds: B_l for every distinct label in first-appearance order (X then Y);
  *         n_bounds must equal the number of distinct labels.
  * d:      partition counts per operand index position, X's then Y's (n_d =

@@ -724,7 +724,7 @@ struct TcOperandPlan {
 
 struct TcPlan {
     TcOperandPlan a, b;
-    bool pair = false;  // 256 x 256 tile on a cluster of two CTAs
+    bool pair = false;  // 256 x block_n tile on a cluster of two CTAs
     uint32_t b_rows = 0;  // rows of Y one CTA loads per K step
     uint32_t block_n = 0, stages = 0, tiles_m = 0, tiles_n = 0, n_tiles = 0, num_kb = 0, tmem_cols = 0;
     uint32_t idesc = 0, smem = 0;
@@ -860,6 +860,39 @@ bool plan_operands(const Plan& p, uint32_t a_rows, uint32_t b_rows, TcPlan* t) {
 
 }  // namespace
 
+namespace {
+
+// Fill t for one tiling: a CTA pair (256 x bn tile, each CTA loading 128 rows of X and bn / 2
+// rows of Y) or a single CTA (128 x bn).  False when the operands cannot be boxed that way.
+bool build_tc(const Plan& p, bool pair, uint32_t bn, TcPlan* t) {
+    *t = TcPlan();
+    if (!plan_operands(p, kBlockM, pair ? bn / 2 : bn, t)) return false;
+    t->pair = pair;
+    t->block_n = bn;
+    t->b_rows = pair ? bn / 2 : bn;
+    const uint32_t stage = (uint32_t)(kBlockM * kBlockK * 2 + t->b_rows * kBlockK * 2);
+    t->stages = (kMaxSmem - 1024 - 256 - kEpiBytes) / stage;
+    if (t->stages > 8) t->stages = 8;
+    if (t->stages < (uint32_t)kProducers) return false;  // the producers' parity waits need stages >= kProducers
+    t->smem = t->stages * stage + 1024 + 256 + kEpiBytes;
+    const uint32_t tile_m = pair ? 2 * kBlockM : kBlockM;
+    t->tiles_m = (uint32_t)(p.ext[kM] / tile_m);
+    t->tiles_n = (uint32_t)(p.ext[kN] / bn);
+    t->n_tiles = (uint32_t)(p.ext[kBatch] * t->tiles_m * t->tiles_n);
+    t->num_kb = (uint32_t)(p.ext[kK] / kBlockK);
+    if ((uint64_t)t->n_tiles * t->num_kb >= (1ull << 31)) return false;  // K steps are counted in 32 bits
+    t->tmem_cols = 2 * bn <= 128 ? 128 : (2 * bn <= 256 ? 256 : 512);
+    t->idesc = (1u << 4)                                   // D: fp32 (M = 256 for a pair: two CTAs' rows)
+               | (1u << 7) | (1u << 10)                    // A, B: bf16
+               | ((uint32_t)t->a.dev.mn_major << 15)       // A major-ness
+               | ((uint32_t)t->b.dev.mn_major << 16)       // B major-ness
+               | ((bn >> 3) << 17)                         // N / 8
+               | ((tile_m >> 4) << 24);                    // M / 16
+    return true;
+}
+
+}  // namespace
+
 bool tc_plan(Plan* p) {
     if (p->unary || p->op != kMul || p->agg != kSum || !p->in_bf16 || p->literal) return false;
     const uint64_t M = p->ext[kM], N = p->ext[kN], K = p->ext[kK];
@@ -869,54 +902,18 @@ bool tc_plan(Plan* p) {
     const int zl = p->Z.label[p->Z.rank - 1];
     if (zl != p->comp[kN][0] || (p->B[zl] / p->D[zl]) % 32) return false;
     TcPlan* t = new TcPlan();
-    // a CTA pair: 256 x bn output tile (bn = 256 or 128), each CTA loads 128 rows of X and
-    // bn / 2 rows of Y
     bool ok = false;
-    uint32_t bn = N % 256 == 0 ? 256 : 128;
     if (p->tc_pair != 0 && M % 256 == 0 && N % 128 == 0) {
-        ok = plan_operands(*p, kBlockM, bn / 2, t);
-        if (!ok && bn == 256) {
-            bn = 128;
-            *t = TcPlan();
-            ok = plan_operands(*p, kBlockM, bn / 2, t);
-        }
-        t->pair = ok;
+        // 256-wide tiles where the columns allow: a 256 x 128 tile moves 3/4 of the bytes of a
+        // 256 x 256 one per K step for half the MMA work, and measured ~1.7x slower per flop
+        if (N % 256 == 0 && p->tc_n != 128) ok = build_tc(*p, true, 256, t);
+        if (!ok && p->tc_n != 256) ok = build_tc(*p, true, 128, t);
     }
-    if (!ok && p->tc_pair != 1) {
-        bn = N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : 64);
-        *t = TcPlan();
-        ok = plan_operands(*p, kBlockM, bn, t);
-    }
+    if (!ok && p->tc_pair != 1) ok = build_tc(*p, false, N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : 64), t);
     if (!ok) {
         delete t;
         return false;
     }
-    t->block_n = bn;
-    t->b_rows = t->pair ? bn / 2 : bn;
-    const uint32_t stage = (uint32_t)(kBlockM * kBlockK * 2 + t->b_rows * kBlockK * 2);
-    t->stages = (kMaxSmem - 1024 - 256 - kEpiBytes) / stage;
-    if (t->stages > 8) t->stages = 8;
-    if (t->stages < (uint32_t)kProducers) {  // the producers' parity waits need stages >= kProducers
-        delete t;
-        return false;
-    }
-    t->smem = t->stages * stage + 1024 + 256 + kEpiBytes;
-    const uint32_t tile_m = t->pair ? 2 * kBlockM : kBlockM;
-    t->tiles_m = (uint32_t)(M / tile_m);
-    t->tiles_n = (uint32_t)(N / bn);
-    t->n_tiles = (uint32_t)(p->ext[kBatch] * t->tiles_m * t->tiles_n);
-    t->num_kb = (uint32_t)(K / kBlockK);
-    if ((uint64_t)t->n_tiles * t->num_kb >= (1ull << 31)) {  // K steps are counted in 32 bits
-        delete t;
-        return false;
-    }
-    t->tmem_cols = 2 * bn <= 128 ? 128 : (2 * bn <= 256 ? 256 : 512);
-    t->idesc = (1u << 4)                                   // D: fp32 (M = 256 for a pair: two CTAs' rows)
-               | (1u << 7) | (1u << 10)                    // A, B: bf16
-               | ((uint32_t)t->a.dev.mn_major << 15)       // A major-ness
-               | ((uint32_t)t->b.dev.mn_major << 16)       // B major-ness
-               | ((bn >> 3) << 17)                         // N / 8
-               | ((tile_m >> 4) << 24);                    // M / 16
     p->tc = t;
     p->kernel = t->pair ? TRA_KERNEL_TC_BF16_PAIR : TRA_KERNEL_TC_BF16;
     return true;
@@ -955,11 +952,53 @@ int sm_count() {
     return n;
 }
 
+// Co-resident clusters of tc_gemm_2sm at this dynamic shared memory size on the current device
+// (cached: the occupancy query costs more than a launch).
+uint32_t pair_clusters(int sms, uint32_t smem) {
+    static std::mutex mu;
+    static int cache_dev[64];
+    static uint32_t cache_smem[64], cache_val[64];
+    static int n = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return (uint32_t)sms / 2;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        for (int i = 0; i < n; ++i)
+            if (cache_dev[i] == dev && cache_smem[i] == smem) return cache_val[i];
+    }
+    uint32_t clusters = (uint32_t)sms / 2;
+    if (cudaFuncSetAttribute(tc_gemm_2sm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * clusters);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        int active = 0;
+        if (cudaOccupancyMaxActiveClusters(&active, tc_gemm_2sm, &cfg) == cudaSuccess && active > 0)
+            clusters = (uint32_t)active < clusters ? (uint32_t)active : clusters;
+    }
+    (void)cudaGetLastError();
+    std::lock_guard<std::mutex> lk(mu);
+    if (n < 64) {
+        cache_dev[n] = dev;
+        cache_smem[n] = smem;
+        cache_val[n] = clusters;
+        ++n;
+    }
+    return clusters;
+}
+
 }  // namespace
 
 int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_t s) {
-    const TcPlan& t = *p.tc;
     if (((uintptr_t)x | (uintptr_t)y | (uintptr_t)z) % 16) return fail(TRA_ERR_ARG, "tensor-core path needs 16-byte aligned buffers");
+    const int sms = sm_count();
+    if (sms <= 0) return fail(TRA_ERR_CUDA, "no device");
+    const TcPlan& t = *p.tc;
+    uint32_t clusters = 0;
+    if (t.pair) {
+        clusters = pair_clusters(sms, t.smem);
+        if (clusters == 0) return fail(TRA_ERR_CUDA, "no co-resident pair of SMs for the pair kernel");
+    }
     CUtensorMap ma, mb;
     if (!encode(t.a, x, &ma) || !encode(t.b, y, &mb)) return fail(TRA_ERR_CUDA, "tensor map encoding failed");
     TcParams tp;
@@ -988,26 +1027,13 @@ int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_
     tp.alpha = (float)p.alpha;
     tp.out_bf16 = p.out_bf16;
     tp.timeout_ns = 2000000000ull;  // 2 s per wait
-    const int sms = sm_count();
-    if (sms <= 0) return fail(TRA_ERR_CUDA, "no device");
     cudaError_t e;
     if (t.pair) {
         e = cudaFuncSetAttribute(tc_gemm_2sm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)t.smem);
         if (e != cudaSuccess) return fail(TRA_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(e));
         // persistent: one cluster per co-resident SM pair, at most one per tile
-        uint32_t clusters = (uint32_t)sms / 2;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2 * clusters);
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = t.smem;
-        cfg.stream = s;
-        int active = 0;
-        if (cudaOccupancyMaxActiveClusters(&active, tc_gemm_2sm, &cfg) == cudaSuccess && active > 0)
-            clusters = (uint32_t)active < clusters ? (uint32_t)active : clusters;
-        else
-            (void)cudaGetLastError();
-        if (clusters > t.n_tiles) clusters = t.n_tiles;
-        tc_gemm_2sm<<<2 * clusters, kThreads, t.smem, s>>>(ma, mb, tp);
+        const uint32_t c = clusters < t.n_tiles ? clusters : t.n_tiles;
+        tc_gemm_2sm<<<2 * c, kThreads, t.smem, s>>>(ma, mb, tp);
     } else {
         e = cudaFuncSetAttribute(tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)t.smem);
         if (e != cudaSuccess) return fail(TRA_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(e));

@@ -151,6 +151,7 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
         else if (k == "mode" && (v == "fused" || v == "literal")) p->literal = v == "literal";
         else if (k == "sqdiff" && (v == "direct" || v == "expand")) p->sqdiff_expand = v == "expand" ? 1 : 0;
         else if (k == "tc" && (v == "pair" || v == "single")) p->tc_pair = v == "pair" ? 1 : 0;
+        else if (k == "tc_n" && (v == "256" || v == "128")) p->tc_n = v == "256" ? 256 : 128;
         else if (k == "alpha") {
             char* end = nullptr;
             errno = 0;

@@ -87,9 +87,16 @@ def test_tc_parity(lib, cuda, eq, bounds, d, opts):
     _tc_case(lib, eq, bounds, d, opts + ":tc=single", "tc_bf16")
 
 
+@pytest.mark.parametrize("width", ["", ":tc_n=256", ":tc_n=128"])
 @pytest.mark.parametrize("eq,bounds,d,opts", PAIR_CASES)
-def test_tc_pair_parity(lib, cuda, eq, bounds, d, opts):
-    _tc_case(lib, eq, bounds, d, opts + ":tc=pair", "tc_bf16_pair")
+def test_tc_pair_parity(lib, cuda, eq, bounds, d, opts, width):
+    # default width and both forced widths
+    try:
+        lib.Plan(f"{eq}:mul:sum:in=bf16{opts}:tc=pair{width}", bounds, d)
+    except lib.TraError as e:
+        assert "TRA_ERR_UNSUPPORTED" in str(e)
+        pytest.skip("no pair tiling of this width")
+    _tc_case(lib, eq, bounds, d, opts + ":tc=pair" + width, "tc_bf16_pair")
 
 
 def test_tc_repeat_and_stream(lib, cuda):

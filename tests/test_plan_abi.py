@@ -115,6 +115,8 @@ def test_kernel_choice(lib):
     ("ij,jk->ik:mul:sum", [64, 0, 64], [1, 1, 1, 1], "TRA_ERR_ARG"),
     ("ij,jk->ik:mul:sum:in=bf16:tc=pair", [384, 128, 256], [1, 1, 1, 1], "TRA_ERR_UNSUPPORTED"),
     ("ij,jk->ik:mul:sum:tc=both", [256, 128, 256], [1, 1, 1, 1], "TRA_ERR_PARSE"),
+    ("ij,jk->ik:mul:sum:tc_n=64", [256, 128, 256], [1, 1, 1, 1], "TRA_ERR_PARSE"),
+    ("ij,jk->ik:mul:sum:in=bf16:tc=pair:tc_n=256", [256, 128, 384], [1, 1, 1, 1], "TRA_ERR_UNSUPPORTED"),
 ])
 def test_plan_errors(lib, spec, bounds, d, code):
     with pytest.raises(lib.TraError) as e:
