@@ -37,6 +37,27 @@ void set_load_modes(SemiringParams& sp, int bf16, const int flags[5]) {
     }
 }
 
+// Elementwise joins whose fp32 X has Z's labels in Z's order share Z's relation layout, so
+// element e of Z reads X at e; Y either has that layout too (or is absent) or is Z without
+// its innermost label, unsplit, and then is read at e / extent.  Chunks of 8 elements need
+// the sizes and the buffers' alignment below.
+int flat_mode(const Plan& p, const void* x, const void* y, const void* z) {
+    if (p.in_bf16 || p.X.rank != p.Z.rank) return 0;
+    for (int i = 0; i < p.Z.rank; ++i)
+        if (p.X.label[i] != p.Z.label[i]) return 0;
+    if (p.Z.total % 8 || ((uintptr_t)x | (uintptr_t)z) % 16) return 0;
+    if (p.unary) return 1;
+    bool same = p.Y.rank == p.Z.rank, minus_last = p.Y.rank == p.Z.rank - 1;
+    for (int i = 0; i < p.Y.rank; ++i) {
+        same = same && p.Y.label[i] == p.Z.label[i];
+        minus_last = minus_last && p.Y.label[i] == p.Z.label[i];
+    }
+    if (same) return (uintptr_t)y % 16 ? 0 : 1;
+    const int last = p.Z.rank - 1;
+    if (minus_last && p.Z.d[last] == 1 && p.Z.shape[last] % 8 == 0) return 2;
+    return 0;
+}
+
 SemiringParams semiring_params(const Plan& p, const void* x, const void* y, void* z) {
     SemiringParams sp;
     memset(&sp, 0, sizeof(sp));
@@ -254,6 +275,9 @@ int execute_plan(const Plan& p, const void* x, const void* y, void* z, void* ws,
             }
             ep.I = (uint32_t)(p.Z.shape[p.Z.rank - 1] / p.Z.d[p.Z.rank - 1]);
             ep.n_runs = (uint64_t)p.Z.total / ep.I;
+            ep.total = (uint64_t)p.Z.total;
+            ep.flat = flat_mode(p, x, y, z);
+            ep.y_div = (uint32_t)p.Z.shape[p.Z.rank - 1];
             e = launch_elementwise(ep, s);
             break;
         }

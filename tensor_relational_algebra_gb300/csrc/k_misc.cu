@@ -119,6 +119,11 @@ __device__ __forceinline__ void agg_merge(float& m, float& s, float m2, float s2
     if (AGG == kLse) {
         const float mm = fmaxf(m, m2);
         if (mm == -INFINITY) return;
+        if (mm == INFINITY) {
+            m = INFINITY;
+            s = 1.f;
+            return;
+        }
         s = s * __expf(m - mm) + s2 * __expf(m2 - mm);
         m = mm;
     } else if (AGG == kMax) {
@@ -127,6 +132,34 @@ __device__ __forceinline__ void agg_merge(float& m, float& s, float m2, float s2
         m = fminf(m, m2);
     } else {
         s += s2;
+    }
+}
+
+template <int AGG>
+__device__ __forceinline__ void agg_group16(float& m, float& s, const float4 (&v)[4]) {
+    if (AGG == kLse) {
+        float cm = m;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) cm = fmaxf(cm, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));
+        if (cm == -INFINITY) return;  // nothing but empty / -inf values so far
+        if (cm == INFINITY) {         // the result is +inf from here on
+            m = INFINITY;
+            s = 1.f;
+            return;
+        }
+        s *= __expf(m - cm);  // m == -inf gives 0
+        m = cm;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            s += (__expf(v[u].x - m) + __expf(v[u].y - m)) + (__expf(v[u].z - m) + __expf(v[u].w - m));
+    } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            agg_step<AGG>(m, s, v[u].x);
+            agg_step<AGG>(m, s, v[u].y);
+            agg_step<AGG>(m, s, v[u].z);
+            agg_step<AGG>(m, s, v[u].w);
+        }
     }
 }
 
@@ -140,13 +173,18 @@ __global__ void row_reduce_kernel(const __grid_constant__ RowReduceParams p) {
     const int64_t xo = role_offset(p.xr, r);
     float m = AGG == kMin ? INFINITY : -INFINITY, s = 0.f;
     if (p.k_affine && !p.in_bf16 && (xo % 4) == 0 && (p.K % 4) == 0 && ((uintptr_t)p.x % 16) == 0) {
+        // 4 float4 loads in flight per lane; each group of 16 values folds in at once (for
+        // logsumexp: one rescale per group, one exp per value); padding is the identity of the
+        // aggregation
         const float4* row = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.x) + xo);
-        for (uint32_t k = lane; k < p.K / 4; k += 32) {
-            float4 v = __ldcs(row + k);
-            agg_step<AGG>(m, s, v.x);
-            agg_step<AGG>(m, s, v.y);
-            agg_step<AGG>(m, s, v.z);
-            agg_step<AGG>(m, s, v.w);
+        const uint32_t K4 = p.K / 4;
+        const float pad = AGG == kMin ? INFINITY : (AGG == kSum ? 0.f : -INFINITY);
+        for (uint32_t k0 = lane; k0 < K4; k0 += 128) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                v[u] = k0 + 32 * u < K4 ? __ldcs(row + k0 + 32 * u) : make_float4(pad, pad, pad, pad);
+            agg_group16<AGG>(m, s, v);
         }
     } else if (p.k_affine) {
         for (uint32_t k = lane; k < p.K; k += 32) agg_step<AGG>(m, s, ld_f(p.x, xo + k, p.in_bf16));
@@ -231,6 +269,49 @@ __global__ void elementwise_kernel(const __grid_constant__ ElementwiseParams p) 
     }
 }
 
+// Flat form of the join above (see ElementwiseParams::flat): one thread per 8 consecutive
+// elements of Z, two 16-byte loads of X (and of Y when laid out as Z), one store of 8 results.
+template <int OP, bool OUT_BF16>
+__global__ void __launch_bounds__(256) elementwise_flat_kernel(const __grid_constant__ ElementwiseParams p) {
+    const uint64_t c = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x;
+    if (c * 8 >= p.total) return;
+    const uint64_t e = c * 8;
+    const float* xr = reinterpret_cast<const float*>(p.x) + e;
+    const float4 x0 = *reinterpret_cast<const float4*>(xr), x1 = *reinterpret_cast<const float4*>(xr + 4);
+    float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
+    if (p.y) {
+        if (p.flat == 1) {
+            const float* yr = reinterpret_cast<const float*>(p.y) + e;
+            y0 = *reinterpret_cast<const float4*>(yr);
+            y1 = *reinterpret_cast<const float4*>(yr + 4);
+        } else {
+            const float yb = __ldg(reinterpret_cast<const float*>(p.y) + e / p.y_div);
+            y0 = y1 = make_float4(yb, yb, yb, yb);
+        }
+    }
+    const float r[8] = {p.alpha * ew_op(OP, x0.x, y0.x), p.alpha * ew_op(OP, x0.y, y0.y), p.alpha * ew_op(OP, x0.z, y0.z),
+                        p.alpha * ew_op(OP, x0.w, y0.w), p.alpha * ew_op(OP, x1.x, y1.x), p.alpha * ew_op(OP, x1.y, y1.y),
+                        p.alpha * ew_op(OP, x1.z, y1.z), p.alpha * ew_op(OP, x1.w, y1.w)};
+    if (OUT_BF16) {
+        __nv_bfloat162 h[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(r[2 * i], r[2 * i + 1]);
+        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.z) + e) = *reinterpret_cast<const uint4*>(h);
+    } else {
+        float* zr = reinterpret_cast<float*>(p.z) + e;
+        *reinterpret_cast<float4*>(zr) = make_float4(r[0], r[1], r[2], r[3]);
+        *reinterpret_cast<float4*>(zr + 4) = make_float4(r[4], r[5], r[6], r[7]);
+    }
+}
+
+template <int OP>
+cudaError_t launch_flat(const ElementwiseParams& p, cudaStream_t s) {
+    const unsigned blocks = (unsigned)((p.total / 8 + 255) / 256);
+    if (p.out_bf16) elementwise_flat_kernel<OP, true><<<blocks, 256, 0, s>>>(p);
+    else elementwise_flat_kernel<OP, false><<<blocks, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- ordered combine of partials
 __global__ void combine_kernel(const __grid_constant__ CombineParams p) {
     const uint64_t total = p.n_groups * p.z_sub;
@@ -309,6 +390,17 @@ cudaError_t launch_row_reduce(const RowReduceParams& p, cudaStream_t s) {
 
 cudaError_t launch_elementwise(const ElementwiseParams& p, cudaStream_t s) {
     if (p.n_runs == 0) return cudaSuccess;
+    if (p.flat && p.total / 8 <= 0xffffffffull * 256) {
+        switch (p.op) {
+            case kMul: return launch_flat<kMul>(p, s);
+            case kAdd: return launch_flat<kAdd>(p, s);
+            case kSqdiff: return launch_flat<kSqdiff>(p, s);
+            case kSub: return launch_flat<kSub>(p, s);
+            case kExpsub: return launch_flat<kExpsub>(p, s);
+            case kId: return launch_flat<kId>(p, s);
+            default: break;
+        }
+    }
     const uint64_t threads = p.n_runs * 32;
     elementwise_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(p);
     return cudaGetLastError();

@@ -157,6 +157,11 @@ struct ElementwiseParams {
     FastDiv grid[TRA_MAX_RANK], sub[TRA_MAX_RANK];
     int64_t x_ks[TRA_MAX_RANK], x_ls[TRA_MAX_RANK];
     int64_t y_ks[TRA_MAX_RANK], y_ls[TRA_MAX_RANK];
+    // flat fast path (fp32 X laid out exactly as Z): 0 off; 1 Y absent or laid out as Z;
+    // 2 Y laid out as Z without its innermost label (unsplit, extent y_div)
+    int32_t flat;
+    uint32_t y_div;
+    uint64_t total;
 };
 
 // Repartition (permute copy) between two relation layouts of one tensor: walks the

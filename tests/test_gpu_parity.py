@@ -197,6 +197,53 @@ def test_row_reduce(lib, cuda, agg, d):
         check_rel(g, r, FP32_REL, floor=1.0)
 
 
+@pytest.mark.parametrize("agg", ["lse", "max"])
+def test_row_reduce_long_rows_with_masked_entries(lib, cuda, agg):
+    # rows of 1100: several 512-value rounds per lane group and a ragged last round; -inf
+    # entries (masked scores) contribute nothing
+    S = gen((4, 6, 1100), 17, 0, b=4.0)
+    S[0, 0, ::7] = -np.inf
+    S[3, 5, 1:] = -np.inf
+    _, g = run_plan(lib, "hst->hs::" + agg, [4, 6, 1100], [1, 1, 1], S)
+    r = oracle.einsum("hst->hs", as_f64(S), agg=agg)
+    if agg == "max":
+        np.testing.assert_array_equal(g, r)
+    else:
+        check_rel(g, r, FP32_REL, floor=1.0)
+
+
+def test_broadcast_expsub_long_rows(lib, cuda):
+    S = gen((4, 6, 1100), 18, 0, b=3.0)
+    L = gen((4, 6), 18, 1, b=3.0)
+    _, g = run_plan(lib, "hst,hs->hst:expsub:none:out=bf16", [4, 6, 1100], [1, 1, 1, 1, 1], S, L, out_bf16=True)
+    r = oracle.einsum("hst,hs->hst", as_f64(S), as_f64(L), op="expsub", agg="none")
+    check_rel(g, rounding.to_bf16(r).astype(np.float64), 2 ** -7)
+
+
+@pytest.mark.parametrize("d", [[1, 1, 1, 1, 1], [2, 3, 1, 2, 3], [2, 3, 4, 2, 3]])
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_broadcast_expsub_flat(lib, cuda, d, out):
+    # innermost extent a multiple of 8: the flat kernel when the innermost label is unsplit
+    S = gen((4, 6, 1024), 19, 0, b=3.0)
+    L = gen((4, 6), 19, 1, b=3.0)
+    bf = out == "bf16"
+    _, g = run_plan(lib, f"hst,hs->hst:expsub:none:out={out}", [4, 6, 1024], d, S, L, out_bf16=bf)
+    r = oracle.einsum("hst,hs->hst", as_f64(S), as_f64(L), op="expsub", agg="none")
+    if bf:
+        check_rel(g, rounding.to_bf16(r).astype(np.float64), 2 ** -7)
+    else:
+        check_rel(g, r, 1e-5)
+
+
+@pytest.mark.parametrize("op", ["mul", "add", "sub", "sqdiff"])
+def test_same_layout_join_flat(lib, cuda, op):
+    X = gen((3, 10, 64), 20, 0)
+    Y = gen((3, 10, 64), 20, 1)
+    _, g = run_plan(lib, f"hst,hst->hst:{op}:none:alpha=0.5", [3, 10, 64], [3, 2, 1, 3, 2, 1], X, Y)
+    r = oracle.einsum("hst,hst->hst", as_f64(X), as_f64(Y), op=op, agg="none", alpha=0.5)
+    check_rel(g, r, 1e-6, floor=1e-3)
+
+
 @pytest.mark.parametrize("d", [[1, 1, 1, 1, 1], [4, 2, 3, 4, 2]])
 def test_broadcast_expsub(lib, cuda, d):
     S = gen((8, 20, 300), 8, 0, b=3.0)
