@@ -14,10 +14,12 @@
 // (composite index / div) % mod.  The planner accepts a shape only when every
 // tile is one TMA box, which keeps every load inside one sub-tensor.
 //
-// Kernel: persistent, one CTA per SM, 6 warps: warp 0 issues TMA loads, warp 1
-// owns tensor memory and issues tcgen05.mma (M = 128, N = BLOCK_N <= 256,
-// K = 16 per instruction, fp32 accumulate), warps 2-5 drain the double-buffered
-// accumulator (tcgen05.ld) into global memory while the next tile is computed.
+// Kernels: persistent, one CTA per SM, 13 warps: warps 0-3 issue TMA loads,
+// warp 4 owns tensor memory and issues tcgen05.mma (fp32 accumulate, K = 16 per
+// instruction), warps 5-12 drain the double-buffered accumulator (tcgen05.ld)
+// into global memory while the next tile is computed.  tc_gemm: one CTA per
+// 128 x BLOCK_N tile.  tc_gemm_2sm: a cluster of two CTAs per 256 x BLOCK_N tile
+// (cta_group::2 instructions issued by the even CTA).
 // Every mbarrier wait is bounded; a wait that gives up sets the device status
 // word (TRA_ERR_TIMEOUT) and makes the whole CTA leave after its copies and
 // MMAs in flight have landed.
@@ -40,16 +42,16 @@ constexpr int kBlockM = 128;
 constexpr int kBlockK = 64;  // one 128-byte swizzle row of bf16
 // Warp roles: 0-3 TMA producers (global K step g goes to producer g % kProducers: the
 // copy engine completes the copies of one issuing thread in order, so a single issuing
-// thread caps a CTA at one box per L2 round trip), 4 MMA issuer, 5-8 epilogue.
+// thread caps a CTA at one box per L2 round trip), 4 MMA issuer, 5-12 epilogue (two warps
+// per TMEM lane quarter, each taking half of the tile's columns).
 constexpr int kProducers = 4;
 constexpr int kMmaWarp = kProducers;
-constexpr int kThreads = 32 * (kProducers + 1 + 4);
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (kProducers + 1 + kEpiWarps);
 constexpr uint32_t kMaxSmem = 227 * 1024;
-// Epilogue staging per epilogue warp: a 32 x 32 fp32 tile (16-byte groups swizzled by row)
-// and 32 row offsets.
+// Epilogue staging per epilogue warp: a 32 x 32 fp32 tile (16-byte groups swizzled by row).
 constexpr uint32_t kEpiTile = 32 * 32 * 4;
-constexpr uint32_t kEpiWarpBytes = kEpiTile + 32 * 8;
-constexpr uint32_t kEpiBytes = 4 * kEpiWarpBytes;
+constexpr uint32_t kEpiBytes = kEpiWarps * kEpiTile;
 
 struct TcOpDev {
     int32_t mn_major;  // 1: innermost dimension is M (X) / N (Y); 0: innermost is K
@@ -367,15 +369,15 @@ __device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[3
         : "r"(taddr));
 }
 
-// Store one 32 x 32 accumulator block (thread = row, r = its 32 columns starting at n).
+// Store one 32 x 32 accumulator block (thread = row, r = its 32 columns starting at n; zr =
+// this lane's row offset in Z, -1 for a row past the end; zc = the block's column offset).
 // The block goes through shared memory as 16-byte groups, group g of row w at slot
 // g ^ (w & 7): the row-wise writes (8 rows per phase) and the column-wise reads (one row
 // per 8 lanes) are both conflict-free, and each global store instruction of the warp writes
 // whole row segments (4 rows x 128 bytes fp32, or 8 rows x 64 bytes bf16).
-__device__ __forceinline__ void store_block(const TcParams& p, float4* stg, const int64_t* zr, int lane,
+__device__ __forceinline__ void store_block(const TcParams& p, float4* stg, int64_t zr, int64_t zc, int lane,
                                             const uint32_t (&r)[32], uint32_t n) {
     if (n >= p.N) return;  // uniform over the warp
-    const int64_t zc = role_offset(p.zn, n);
 #pragma unroll
     for (int g = 0; g < 8; ++g)
         stg[lane * 8 + (g ^ (lane & 7))] =
@@ -390,7 +392,7 @@ __device__ __forceinline__ void store_block(const TcParams& p, float4* stg, cons
             const int row = 8 * i + (lane >> 2);
             const float4 v0 = stg[row * 8 + ((2 * sub) ^ (row & 7))];
             const float4 v1 = stg[row * 8 + ((2 * sub + 1) ^ (row & 7))];
-            const int64_t o = zr[row];
+            const int64_t o = __shfl_sync(0xffffffffu, zr, row);
             __nv_bfloat162 h[4] = {__floats2bfloat162_rn(v0.x, v0.y), __floats2bfloat162_rn(v0.z, v0.w),
                                    __floats2bfloat162_rn(v1.x, v1.y), __floats2bfloat162_rn(v1.z, v1.w)};
             if (o >= 0) *reinterpret_cast<uint4*>(z + o + zc + 8 * sub) = *reinterpret_cast<const uint4*>(h);
@@ -402,7 +404,7 @@ __device__ __forceinline__ void store_block(const TcParams& p, float4* stg, cons
         for (int i = 0; i < 8; ++i) {
             const int row = 4 * i + (lane >> 3);
             const float4 v = stg[row * 8 + (g ^ (row & 7))];
-            const int64_t o = zr[row];
+            const int64_t o = __shfl_sync(0xffffffffu, zr, row);
             if (o >= 0) *reinterpret_cast<float4*>(z + o + zc + 4 * g) = v;
         }
     }
@@ -410,22 +412,24 @@ __device__ __forceinline__ void store_block(const TcParams& p, float4* stg, cons
 }
 
 // Epilogue of one tile for one epilogue warp: TMEM lane quarter q holds 32 rows of the
-// accumulator (thread = row m); the columns n0 .. n0 + block_n - 1 go out two 32-column
-// blocks at a time (both TMEM loads in flight before the wait).
-__device__ __forceinline__ void epilogue_tile(const TcParams& p, uint8_t* epi, uint32_t tmem_acc, uint32_t q, int lane,
-                                              uint32_t b, uint32_t m, uint32_t n0) {
-    float4* stg = reinterpret_cast<float4*>(epi + q * kEpiWarpBytes);
-    int64_t* zr = reinterpret_cast<int64_t*>(epi + q * kEpiWarpBytes + kEpiTile);
-    zr[lane] = m < p.M ? role_offset(p.zb, b) + role_offset(p.zm, m) : (int64_t)-1;
-    __syncwarp();
+// accumulator (thread = row m).  The tile's columns go out in pairs of 32-column blocks (both
+// TMEM loads in flight before the wait); the two warps of a quarter (half 0 / 1) take
+// alternate pairs.  Row and column offsets are computed once per tile, one per lane, and
+// passed by shuffle.
+__device__ __forceinline__ void epilogue_tile(const TcParams& p, uint8_t* epi, uint32_t tmem_acc, uint32_t q,
+                                              uint32_t half, int lane, uint32_t b, uint32_t m, uint32_t n0) {
+    float4* stg = reinterpret_cast<float4*>(epi + (q + 4 * half) * kEpiTile);
+    const int64_t zr = m < p.M ? role_offset(p.zb, b) + role_offset(p.zm, m) : (int64_t)-1;
+    const uint32_t nblk = p.block_n / 32;  // block_n is a multiple of 64
+    const int64_t zc_lane = (uint32_t)lane < nblk && n0 + 32u * lane < p.N ? role_offset(p.zn, n0 + 32u * lane) : 0;
     const uint32_t taddr = tmem_acc + ((q * 32u) << 16);
-    for (uint32_t c = 0; c < p.block_n / 32; c += 2) {  // block_n is a multiple of 64
+    for (uint32_t c = 2 * half; c < nblk; c += 4) {
         uint32_t ra[32], rb[32];
         tmem_ld32_nowait(taddr + c * 32u, ra);
         tmem_ld32_nowait(taddr + c * 32u + 32u, rb);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        store_block(p, stg, zr, lane, ra, n0 + c * 32u);
-        store_block(p, stg, zr, lane, rb, n0 + c * 32u + 32u);
+        store_block(p, stg, zr, __shfl_sync(0xffffffffu, zc_lane, c), lane, ra, n0 + c * 32u);
+        store_block(p, stg, zr, __shfl_sync(0xffffffffu, zc_lane, c + 1), lane, rb, n0 + c * 32u + 32u);
     }
 }
 
@@ -444,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* gbase = smem_raw + (base - raw);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (done_bar + 8 - base));
     volatile int* abort = reinterpret_cast<volatile int*>(gbase + (done_bar + 12 - base));
-    uint8_t* epi = gbase + (bar0 + 256 - base);  // epilogue staging (kEpiBytes)
+    uint8_t* epi = gbase + (bar0 + 256 - base);  // epilogue staging (kEpiBytes, 16-byte aligned)
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
@@ -454,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull0 + 8 * a, 1);
-            mbar_init(tempty0 + 8 * a, 128);
+            mbar_init(tempty0 + 8 * a, 32 * kEpiWarps);
         }
         mbar_init(done_bar, 1);
         *abort = 0;
@@ -521,15 +525,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(done_bar, 0, &never, p.timeout_ns);
         }
     } else {
-        // ---------------------------------------------------------------- epilogue (warps 5-8)
+        // ---------------------------------------------------------------- epilogue (warps 5-12)
         const uint32_t q = warp & 3;  // TMEM lane quarter this warp may access
+        const uint32_t half = (uint32_t)(warp - kMmaWarp - 1) >> 2;
         uint32_t acc = 0, acc_phase = 0;
         for (uint32_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
             uint32_t b, mt, nt;
             tile_of(p, t, b, mt, nt);
             if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort, p.timeout_ns)) break;
             tc_fence_after();
-            epilogue_tile(p, epi, tmem_base + acc * p.block_n, q, lane, b, mt * kBlockM + q * 32 + lane, nt * p.block_n);
+            epilogue_tile(p, epi, tmem_base + acc * p.block_n, q, half, lane, b, mt * kBlockM + q * 32 + lane,
+                          nt * p.block_n);
             tc_fence_before();
             mbar_arrive(tempty0 + 8 * acc);
             if (++acc == 2) {
@@ -569,7 +575,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint8_t* gbase = smem_raw + (base - raw);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (done_bar + 8 - base));
     volatile int* abort = reinterpret_cast<volatile int*>(gbase + (done_bar + 12 - base));
-    uint8_t* epi = gbase + (bar0 + 256 - base);  // epilogue staging (kEpiBytes)
+    uint8_t* epi = gbase + (bar0 + 256 - base);  // epilogue staging (kEpiBytes, 16-byte aligned)
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t rank = cluster_rank();
@@ -582,7 +588,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull0 + 8 * a, 1);
-            mbar_init(tempty0 + 8 * a, 8);  // one lane of each epilogue warp of both CTAs
+            mbar_init(tempty0 + 8 * a, 2 * kEpiWarps);  // one lane of each epilogue warp of both CTAs
         }
         mbar_init(done_bar, 1);
         *abort = 0;
@@ -649,16 +655,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_wait_cl(done_bar, 0, &never, p.timeout_ns);
         }
     } else {
-        // ---------------------------------------------------------------- epilogue (warps 5-8, both CTAs)
+        // ---------------------------------------------------------------- epilogue (warps 5-12, both CTAs)
         const uint32_t q = warp & 3;
+        const uint32_t half = (uint32_t)(warp - kMmaWarp - 1) >> 2;
         uint32_t acc = 0, acc_phase = 0;
         for (uint32_t t = pair; t < p.n_tiles; t += n_pairs) {
             uint32_t b, mt, nt;
             tile_of(p, t, b, mt, nt);
             if (!mbar_wait_cl(tfull0 + 8 * acc, acc_phase, abort, p.timeout_ns)) break;
             tc_fence_after();
-            epilogue_tile(p, epi, tmem_base + acc * p.block_n, q, lane, b, mt * 2 * kBlockM + rank * kBlockM + q * 32 + lane,
-                          nt * p.block_n);
+            epilogue_tile(p, epi, tmem_base + acc * p.block_n, q, half, lane, b,
+                          mt * 2 * kBlockM + rank * kBlockM + q * 32 + lane, nt * p.block_n);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty0 + 8 * acc, 0));
