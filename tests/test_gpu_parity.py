@@ -160,6 +160,15 @@ def test_lse_underflow_fallback(lib, cuda):
     ("ijl,jk->ik", [12, 10, 3, 14], [2, 5, 1, 5, 7], "add", "max"),
     ("ij,jk->ik", [1, 1, 1], [1, 1, 1, 1], "mul", "sum"),
     ("ij,jk->ik", [1, 300, 1], [1, 3, 3, 1], "sqdiff", "sum"),
+    # degenerate forms: full contraction to a scalar, rank-1 operands, an outer product
+    # (no contracted label), every block 1 x 1, a batch label split into keys with lse
+    ("ij,ij->", [12, 20], [3, 4, 3, 4], "mul", "sum"),
+    ("ij,ij->", [12, 20], [3, 4, 3, 4], "add", "max"),
+    ("i,i->", [300], [3, 3], "add", "lse"),
+    ("i,j->ij", [7, 9], [7, 3], "mul", "none"),
+    ("ij,jk->ik", [4, 6, 8], [4, 6, 6, 8], "add", "max"),
+    ("ij,jk->ik", [4, 6, 8], [4, 6, 6, 8], "mul", "sum"),
+    ("bij,bjk->bik", [2, 3, 5, 7], [2, 3, 5, 2, 5, 7], "add", "lse"),
 ])
 def test_general_einsums(lib, cuda, eq, bounds, d, op, agg):
     ins, out = eq.split("->")[0].split(","), eq.split("->")[1]
