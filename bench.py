@@ -267,13 +267,15 @@ class C1Workload(_PointsWorkload):
 
         return [datagen.uniform_f32((64, 64), 0 + self.seed_offset, 0), datagen.uniform_f32((64, 64), 0 + self.seed_offset, 1)]
 
+    mode = "fused"
+
     def setup(self, tra, torch, inputs):
         X, Y = inputs
         self.Xd = torch.from_numpy(X).cuda().reshape(-1)
         self.Yd = torch.from_numpy(Y).cuda().reshape(-1)
         self.steps, self.outputs_dev = [], []
         for d in self.d:
-            p = tra.Plan("ij,jk->ik:mul:sum", [64, 64, 64], d)
+            p = tra.Plan(f"ij,jk->ik:mul:sum:mode={self.mode}", [64, 64, 64], d)
             xr, yr = torch.empty_like(self.Xd), torch.empty_like(self.Yd)
             z = torch.empty(64 * 64, dtype=torch.float32, device="cuda")
             self.outputs_dev.append(z)
@@ -300,6 +302,14 @@ class C1Workload(_PointsWorkload):
 
     def sample_text(self, n):
         return "the whole workload (three 64^3 EinSums)"
+
+
+class C1LiteralWorkload(C1Workload):
+    """Config 1 executed as the literal TRA: one partial sub-tensor per join tuple, then the
+    aggregation combines each output key's partials in canonical order (combine kernel)."""
+    name = ("matmul 64x64x64 fp32 U[-1,1], d in {[4,1,1,4],[1,4,4,1],[2,2,2,2]}, literal TRA "
+            "(one partial per join tuple, ordered combine; three executions per step)")
+    mode = "literal"
 
 
 class C3Workload(_PointsWorkload):
@@ -463,7 +473,7 @@ class C5bWorkload(_PointsWorkload):
         return f"{n} of 8192^2 outputs"
 
 
-WORKLOADS = {"pair": PairWorkload, "c1": C1Workload, "c3": C3Workload, "c4": C4Workload, "c5": C5Workload,
+WORKLOADS = {"pair": PairWorkload, "c1": C1Workload, "c1l": C1LiteralWorkload, "c3": C3Workload, "c4": C4Workload, "c5": C5Workload,
              "c5b": C5bWorkload}
 
 
