@@ -108,7 +108,8 @@ enum {
  *         shared by a cluster of two CTAs, or a 128-row tile per CTA; default pair
  *         when the output rows are a multiple of 256 and the columns of 128),
  *         tc_n=256|128 (width of the pair tile; by default 256 where the columns
- *         allow, else 128).
+ *         allow, else 128), tc_store=tma|lsu (tensor-core epilogue: TMA stores
+ *         through an output tensor map, the default where one fits, or warp stores).
  * bounds: B_l for every distinct label in first-appearance order (X then Y);
  *         n_bounds must equal the number of distinct labels.
  * d:      partition counts per operand index position, X's then Y's (n_d =

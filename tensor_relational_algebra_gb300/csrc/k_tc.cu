@@ -61,6 +61,8 @@ struct TcOpDev {
 };
 
 struct TcParams {
+    TcOpDev zt;     // output tensor-map dimensions (TMA-store epilogue)
+    uint32_t z_tma;  // 1: the epilogue stores through the output tensor map
     TcOpDev a, b;
     uint32_t nb, M, N, K;
     uint32_t tiles_m, tiles_n, n_tiles, group_m;
@@ -157,19 +159,6 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
     d |= (uint64_t)1 << 46;
     d |= (uint64_t)2 << 61;
     return d;
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ int dim_coord(const TcOpDev& o, int j, uint32_t v) {
@@ -369,6 +358,26 @@ __device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[3
         : "r"(taddr));
 }
 
+// TMA store of one box from this CTA's shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_5d(const CUtensorMap* map, const int c[5], uint32_t src) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4, %5}], [%6];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4]), "r"(src)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Output tensor-map coordinates of the box starting at (b, m, n).
+__device__ __forceinline__ void z_coords(const TcOpDev& o, uint32_t b, uint32_t m, uint32_t n, int c[5]) {
+#pragma unroll
+    for (int j = 0; j < 5; ++j)
+        c[j] = o.role[j] == kK ? 0 : dim_coord(o, j, o.role[j] == kBatch ? b : (o.role[j] == kM ? m : n));
+}
+
 // Store one 32 x 32 accumulator block (thread = row, r = its 32 columns starting at n; zr =
 // this lane's row offset in Z, -1 for a row past the end; zc = the block's column offset).
 // The block goes through shared memory as 16-byte groups, group g of row w at slot
@@ -414,15 +423,75 @@ __device__ __forceinline__ void store_block(const TcParams& p, float4* stg, int6
 // Epilogue of one tile for one epilogue warp: TMEM lane quarter q holds 32 rows of the
 // accumulator (thread = row m).  The tile's columns go out in pairs of 32-column blocks (both
 // TMEM loads in flight before the wait); the two warps of a quarter (half 0 / 1) take
-// alternate pairs.  Row and column offsets are computed once per tile, one per lane, and
-// passed by shuffle.
-__device__ __forceinline__ void epilogue_tile(const TcParams& p, uint8_t* epi, uint32_t tmem_acc, uint32_t q,
-                                              uint32_t half, int lane, uint32_t b, uint32_t m, uint32_t n0) {
+// alternate pairs.  With an output tensor map the blocks leave by TMA stores; otherwise by
+// warp stores, with row and column offsets computed once per tile, one per lane, and passed
+// by shuffle.
+__device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorMap* map_z, uint8_t* epi,
+                                              uint32_t tmem_acc, uint32_t q, uint32_t half, int lane, uint32_t b,
+                                              uint32_t m, uint32_t n0) {
     float4* stg = reinterpret_cast<float4*>(epi + (q + 4 * half) * kEpiTile);
-    const int64_t zr = m < p.M ? role_offset(p.zb, b) + role_offset(p.zm, m) : (int64_t)-1;
     const uint32_t nblk = p.block_n / 32;  // block_n is a multiple of 64
-    const int64_t zc_lane = (uint32_t)lane < nblk && n0 + 32u * lane < p.N ? role_offset(p.zn, n0 + 32u * lane) : 0;
     const uint32_t taddr = tmem_acc + ((q * 32u) << 16);
+    if (p.z_tma) {
+        // TMA stores: the warp writes its 32 rows into its (1024-aligned) staging tile in the
+        // 128-byte swizzle the output map uses, then one lane stores the box.  fp32: one box
+        // per 32 columns; bf16: one box per 64 columns.  The tile is rewritten once the previous
+        // box has left shared memory.  (A second staging tile per warp measured no faster and
+        // costs the pair kernel a pipeline stage.)
+        const uint32_t row0 = m - (uint32_t)lane;
+        auto next_tile = [&]() -> float4* {
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            return stg;
+        };
+        auto store_tile = [&](float4* t, uint32_t n) {
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                int cc[5];
+                z_coords(p.zt, b, row0, n, cc);
+                tma_store_5d(map_z, cc, smem_u32(t));
+                bulk_commit();
+            }
+        };
+        for (uint32_t c = 2 * half; c < nblk; c += 4) {
+            uint32_t ra[32], rb[32];
+            tmem_ld32_nowait(taddr + c * 32u, ra);
+            tmem_ld32_nowait(taddr + c * 32u + 32u, rb);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            if (!p.out_bf16) {
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+                    float4* t = next_tile();
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        const uint32_t* r = blk ? rb : ra;
+                        t[lane * 8 + (g ^ (lane & 7))] = make_float4(
+                            p.alpha * __uint_as_float(r[4 * g]), p.alpha * __uint_as_float(r[4 * g + 1]),
+                            p.alpha * __uint_as_float(r[4 * g + 2]), p.alpha * __uint_as_float(r[4 * g + 3]));
+                    }
+                    store_tile(t, n0 + (c + blk) * 32u);
+                }
+            } else {
+                float4* t = next_tile();
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    const uint32_t* r = g < 4 ? ra : rb;
+                    const int o = 8 * (g & 3);
+                    __nv_bfloat162 h[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        h[i] = __floats2bfloat162_rn(p.alpha * __uint_as_float(r[o + 2 * i]),
+                                                     p.alpha * __uint_as_float(r[o + 2 * i + 1]));
+                    t[lane * 8 + (g ^ (lane & 7))] = *reinterpret_cast<const float4*>(h);
+                }
+                store_tile(t, n0 + c * 32u);
+            }
+        }
+        return;
+    }
+    const int64_t zr = m < p.M ? role_offset(p.zb, b) + role_offset(p.zm, m) : (int64_t)-1;
+    const int64_t zc_lane = (uint32_t)lane < nblk && n0 + 32u * lane < p.N ? role_offset(p.zn, n0 + 32u * lane) : 0;
     for (uint32_t c = 2 * half; c < nblk; c += 4) {
         uint32_t ra[32], rb[32];
         tmem_ld32_nowait(taddr + c * 32u, ra);
@@ -436,19 +505,20 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, uint8_t* epi, u
 // ------------------------------------------------------------------ the kernel
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-            const __grid_constant__ TcParams p) {
+            const __grid_constant__ CUtensorMap map_z, const __grid_constant__ TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t stage_bytes = p.a_bytes + p.b_bytes;
-    const uint32_t bar0 = base + p.stages * stage_bytes;
+    const uint32_t epi_s = base + p.stages * stage_bytes;  // epilogue staging, 1024-aligned (TMA swizzle)
+    const uint32_t bar0 = epi_s + kEpiBytes;
     // barrier block: full[S], empty[S], tfull[2], tempty[2], done, then tmem slot and abort flag
     const uint32_t full0 = bar0, empty0 = bar0 + 8 * p.stages, tfull0 = bar0 + 16 * p.stages;
     const uint32_t tempty0 = tfull0 + 16, done_bar = tempty0 + 16;
     uint8_t* gbase = smem_raw + (base - raw);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (done_bar + 8 - base));
     volatile int* abort = reinterpret_cast<volatile int*>(gbase + (done_bar + 12 - base));
-    uint8_t* epi = gbase + (bar0 + 256 - base);  // epilogue staging (kEpiBytes, 16-byte aligned)
+    uint8_t* epi = gbase + (epi_s - base);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
@@ -534,8 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tile_of(p, t, b, mt, nt);
             if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort, p.timeout_ns)) break;
             tc_fence_after();
-            epilogue_tile(p, epi, tmem_base + acc * p.block_n, q, half, lane, b, mt * kBlockM + q * 32 + lane,
-                          nt * p.block_n);
+            epilogue_tile(p, &map_z, epi, tmem_base + acc * p.block_n, q, half, lane, b,
+                          mt * kBlockM + q * 32 + lane, nt * p.block_n);
             tc_fence_before();
             mbar_arrive(tempty0 + 8 * acc);
             if (++acc == 2) {
@@ -543,6 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc_phase ^= 1;
             }
         }
+        if (lane == 0) bulk_wait_all();  // this warp's TMA stores have completed
     }
 
     tc_fence_before();
@@ -564,18 +635,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 // work).
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_gemm_2sm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                const __grid_constant__ TcParams p) {
+                const __grid_constant__ CUtensorMap map_z, const __grid_constant__ TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t stage_bytes = p.a_bytes + p.b_bytes;  // this CTA's half of one K step
-    const uint32_t bar0 = base + p.stages * stage_bytes;
+    const uint32_t epi_s = base + p.stages * stage_bytes;  // epilogue staging, 1024-aligned (TMA swizzle)
+    const uint32_t bar0 = epi_s + kEpiBytes;
     const uint32_t full0 = bar0, empty0 = bar0 + 8 * p.stages, tfull0 = bar0 + 16 * p.stages;
     const uint32_t tempty0 = tfull0 + 16, done_bar = tempty0 + 16;
     uint8_t* gbase = smem_raw + (base - raw);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (done_bar + 8 - base));
     volatile int* abort = reinterpret_cast<volatile int*>(gbase + (done_bar + 12 - base));
-    uint8_t* epi = gbase + (bar0 + 256 - base);  // epilogue staging (kEpiBytes, 16-byte aligned)
+    uint8_t* epi = gbase + (epi_s - base);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t rank = cluster_rank();
@@ -664,7 +736,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tile_of(p, t, b, mt, nt);
             if (!mbar_wait_cl(tfull0 + 8 * acc, acc_phase, abort, p.timeout_ns)) break;
             tc_fence_after();
-            epilogue_tile(p, epi, tmem_base + acc * p.block_n, q, half, lane, b,
+            epilogue_tile(p, &map_z, epi, tmem_base + acc * p.block_n, q, half, lane, b,
                           mt * 2 * kBlockM + rank * kBlockM + q * 32 + lane, nt * p.block_n);
             tc_fence_before();
             __syncwarp();
@@ -674,6 +746,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 acc_phase ^= 1;
             }
         }
+        if (lane == 0) bulk_wait_all();  // this warp's TMA stores have completed
     }
 
     tc_fence_before();
@@ -731,6 +804,8 @@ struct TcOperandPlan {
 
 struct TcPlan {
     TcOperandPlan a, b;
+    TcOperandPlan z;     // output tensor map (TMA-store epilogue), valid when z_tma
+    bool z_tma = false;
     bool pair = false;  // 256 x block_n tile on a cluster of two CTAs
     uint32_t b_rows = 0;  // rows of Y one CTA loads per K step
     uint32_t block_n = 0, stages = 0, tiles_m = 0, tiles_n = 0, n_tiles = 0, num_kb = 0, tmem_cols = 0;
@@ -741,9 +816,10 @@ void tc_free(TcPlan* t) { delete t; }
 
 namespace {
 
-// Physical dimensions of an operand's blocked layout, innermost first: the local
-// part of every label (last index first), then the key part; unit dimensions dropped.
-bool operand_dims(const Plan& p, const Operand& t, int mn_role, uint32_t mn_tile, int mn_loads, TcOperandPlan& out) {
+// Physical dimensions of a relation's blocked layout, innermost first: the local part of every
+// label (last index first), then the key part; unit dimensions dropped.  Boxes: tiles[role]
+// consecutive composite indices of each role, one TMA box that stays inside one block.
+bool box_dims(const Plan& p, const Operand& t, const uint32_t (&tiles)[4], int elem_bytes, TcOperandPlan& out) {
     struct Phys {
         int label, key;
         uint64_t extent, stride;
@@ -761,7 +837,7 @@ bool operand_dims(const Plan& p, const Operand& t, int mn_role, uint32_t mn_tile
     if (n == 0 || n > 5) return false;
     if (ph[0].stride != 1 || ph[0].key) return false;
     for (int j = 1; j < n; ++j)
-        if ((ph[j].stride * 2) % 16) return false;
+        if ((ph[j].stride * (uint64_t)elem_bytes) % 16) return false;
     // composite stride of every label in its role
     uint64_t div[TRA_MAX_LABELS] = {};
     for (int r = 0; r < 4; ++r) {
@@ -783,10 +859,8 @@ bool operand_dims(const Plan& p, const Operand& t, int mn_role, uint32_t mn_tile
         dm.mod = (uint32_t)ph[j].extent;
         dm.box = 1;
     }
-    // boxes: walk each role's labels innermost first with the tile extent
-    const uint32_t tiles[4] = {1u, mn_role == kM ? mn_tile : 1u, mn_role == kN ? mn_tile : 1u, (uint32_t)kBlockK};
+    // boxes: walk each role's labels innermost first with the tile extent (1: box 1 everywhere)
     for (int r = 0; r < 4; ++r) {
-        if ((r == kM || r == kN) && r != mn_role) continue;
         uint64_t rem = tiles[r];
         int last_dim = -1;
         for (int l : p.comp[r]) {
@@ -818,6 +892,15 @@ bool operand_dims(const Plan& p, const Operand& t, int mn_role, uint32_t mn_tile
         }
         if (rem != 1) return false;
     }
+    return true;
+}
+
+// Physical dimensions and TMA boxes of an operand: a tile of mn_tile rows along M (X) or N (Y)
+// and kBlockK along K, loaded in mn_loads boxes.
+bool operand_dims(const Plan& p, const Operand& t, int mn_role, uint32_t mn_tile, int mn_loads, TcOperandPlan& out) {
+    const uint32_t tiles[4] = {1u, mn_role == kM ? mn_tile : 1u, mn_role == kN ? mn_tile : 1u, (uint32_t)kBlockK};
+    if (!box_dims(p, t, tiles, 2, out)) return false;
+    const int n = out.ndims;
     // shared-memory layout: K-major (innermost K, 64 wide; the other boxes are the M/N rows)
     // or MN-major (innermost M/N, 64 wide per load; the other boxes are K rows)
     const int r0 = out.dims[0].role;
@@ -847,6 +930,21 @@ bool operand_dims(const Plan& p, const Operand& t, int mn_role, uint32_t mn_tile
 }  // namespace
 
 namespace {
+
+// The output's tensor map for TMA stores from the epilogue: boxes of 32 rows (M) by n_tile
+// columns (N), the innermost dimension being the innermost N label (n_tile wide, 128 bytes).
+bool z_dims(const Plan& p, uint32_t n_tile, TcOperandPlan& out) {
+    const uint32_t tiles[4] = {1u, 32u, n_tile, 1u};
+    const int eb = p.out_bf16 ? 2 : 4;
+    if (!box_dims(p, p.Z, tiles, eb, out)) return false;
+    if (out.dims[0].role != kN || out.dims[0].box != n_tile || n_tile * (uint32_t)eb != 128) return false;
+    for (int j = 0; j < 5; ++j) {
+        out.dev.role[j] = j < out.ndims ? out.dims[j].role : kK;
+        out.dev.div[j] = FastDiv(j < out.ndims ? out.dims[j].div : 1u);
+        out.dev.mod[j] = FastDiv(j < out.ndims ? out.dims[j].mod : 1u);
+    }
+    return true;
+}
 
 // Operand tilings for one CTA: A holds a_rows output rows x 64 K, B holds b_rows output
 // columns x 64 K.  Either may be K-major (one box) or M/N-major (boxes of 64 rows).
@@ -888,6 +986,9 @@ bool build_tc(const Plan& p, bool pair, uint32_t bn, TcPlan* t) {
     t->n_tiles = (uint32_t)(p.ext[kBatch] * t->tiles_m * t->tiles_n);
     t->num_kb = (uint32_t)(p.ext[kK] / kBlockK);
     if ((uint64_t)t->n_tiles * t->num_kb >= (1ull << 31)) return false;  // K steps are counted in 32 bits
+    // TMA-store epilogue: boxes of 32 rows x 128 bytes of the output
+    t->z_tma = p.tc_store != 0 && z_dims(p, p.out_bf16 ? 64u : 32u, t->z);
+    if (p.tc_store == 1 && !t->z_tma) return false;  // TMA stores asked for and no output map fits
     t->tmem_cols = 2 * bn <= 128 ? 128 : (2 * bn <= 256 ? 256 : 512);
     t->idesc = (1u << 4)                                   // D: fp32 (M = 256 for a pair: two CTAs' rows)
                | (1u << 7) | (1u << 10)                    // A, B: bf16
@@ -928,7 +1029,8 @@ bool tc_plan(Plan* p) {
 
 namespace {
 
-bool encode(const TcOperandPlan& o, const void* base, CUtensorMap* map) {
+bool encode(const TcOperandPlan& o, const void* base, CUtensorMap* map,
+            CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, int elem = 2) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[5], strides[4];
@@ -938,15 +1040,15 @@ bool encode(const TcOperandPlan& o, const void* base, CUtensorMap* map) {
         if (j < o.ndims) {
             dims[j] = o.dims[j].extent;
             box[j] = o.dims[j].box;
-            if (j > 0) strides[j - 1] = o.dims[j].stride * 2;
+            if (j > 0) strides[j - 1] = o.dims[j].stride * (uint64_t)elem;
             last = o.dims[j].stride * o.dims[j].extent;
         } else {
             dims[j] = 1;
             box[j] = 1;
-            if (j > 0) strides[j - 1] = ((last * 2 + 15) / 16) * 16;
+            if (j > 0) strides[j - 1] = ((last * (uint64_t)elem + 15) / 16) * 16;
         }
     }
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
+    const CUresult r = fn(map, dtype, 5, const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -1006,12 +1108,18 @@ int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_
         clusters = pair_clusters(sms, t.smem);
         if (clusters == 0) return fail(TRA_ERR_CUDA, "no co-resident pair of SMs for the pair kernel");
     }
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mz;
     if (!encode(t.a, x, &ma) || !encode(t.b, y, &mb)) return fail(TRA_ERR_CUDA, "tensor map encoding failed");
+    memset(&mz, 0, sizeof(mz));
+    if (t.z_tma && !encode(t.z, z, &mz, p.out_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                           p.out_bf16 ? 2 : 4))
+        return fail(TRA_ERR_CUDA, "output tensor map encoding failed");
     TcParams tp;
     memset(&tp, 0, sizeof(tp));
     tp.a = t.a.dev;
     tp.b = t.b.dev;
+    tp.zt = t.z.dev;
+    tp.z_tma = t.z_tma ? 1u : 0u;
     tp.nb = (uint32_t)p.ext[kBatch];
     tp.M = (uint32_t)p.ext[kM];
     tp.N = (uint32_t)p.ext[kN];
@@ -1040,12 +1148,12 @@ int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_
         if (e != cudaSuccess) return fail(TRA_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(e));
         // persistent: one cluster per co-resident SM pair, at most one per tile
         const uint32_t c = clusters < t.n_tiles ? clusters : t.n_tiles;
-        tc_gemm_2sm<<<2 * c, kThreads, t.smem, s>>>(ma, mb, tp);
+        tc_gemm_2sm<<<2 * c, kThreads, t.smem, s>>>(ma, mb, mz, tp);
     } else {
         e = cudaFuncSetAttribute(tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)t.smem);
         if (e != cudaSuccess) return fail(TRA_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(e));
         const unsigned grid = (unsigned)(t.n_tiles < (uint32_t)sms ? t.n_tiles : (uint32_t)sms);
-        tc_gemm<<<grid, kThreads, t.smem, s>>>(ma, mb, tp);
+        tc_gemm<<<grid, kThreads, t.smem, s>>>(ma, mb, mz, tp);
     }
     e = cudaGetLastError();
     return e == cudaSuccess ? TRA_OK : fail(TRA_ERR_CUDA, "tensor-core launch: %s", cudaGetErrorString(e));

@@ -152,6 +152,7 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
         else if (k == "sqdiff" && (v == "direct" || v == "expand")) p->sqdiff_expand = v == "expand" ? 1 : 0;
         else if (k == "tc" && (v == "pair" || v == "single")) p->tc_pair = v == "pair" ? 1 : 0;
         else if (k == "tc_n" && (v == "256" || v == "128")) p->tc_n = v == "256" ? 256 : 128;
+        else if (k == "tc_store" && (v == "tma" || v == "lsu")) p->tc_store = v == "tma" ? 1 : 0;
         else if (k == "alpha") {
             char* end = nullptr;
             errno = 0;
@@ -302,6 +303,8 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
     } else {
         if (p->tc_pair == 1 && p->op == kMul && p->agg == kSum && p->in_bf16)
             return fail(TRA_ERR_UNSUPPORTED, "tc=pair: no 256 x 256 tensor-core tiling for this plan");
+        if (p->tc_store == 1 && p->op == kMul && p->agg == kSum && p->in_bf16)
+            return fail(TRA_ERR_UNSUPPORTED, "tc_store=tma: no tensor-core tiling with an output tensor map");
         p->kernel = TRA_KERNEL_SEMIRING_F32;
         if (p->op == kSqdiff && p->agg == kSum && p->sqdiff_expand) {
             if (p->in_bf16) return fail(TRA_ERR_UNSUPPORTED, "sqdiff=expand needs fp32 inputs");

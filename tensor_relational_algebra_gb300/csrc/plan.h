@@ -39,6 +39,7 @@ struct Plan {
     int sqdiff_expand = 0;
     int tc_pair = -1;  // tensor-core tile: 1 CTA pair (256 x 256), 0 single CTA, -1 pair when shapes allow
     int tc_n = 0;      // width of a pair tile: 256, 128, or 0 (256 where the columns allow)
+    int tc_store = -1; // tensor-core epilogue: 1 TMA stores, 0 warp stores, -1 TMA where the output map fits
     // vector-load eligibility of the semiring kernel's operands (host scan, see scan_vec_flags)
     int vec_flags[5] = {0, 0, 0, 0, 0};  // X along K, X along M, Y along N, Y along K, Z along N
     bool unary = false;

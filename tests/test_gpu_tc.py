@@ -82,21 +82,29 @@ def _tc_case(lib, eq, bounds, d, opts, kernel):
         check_sum(g, r, S, FP32_REL)
 
 
-@pytest.mark.parametrize("eq,bounds,d,opts", CASES)
-def test_tc_parity(lib, cuda, eq, bounds, d, opts):
-    _tc_case(lib, eq, bounds, d, opts + ":tc=single", "tc_bf16")
-
-
-@pytest.mark.parametrize("width", ["", ":tc_n=256", ":tc_n=128"])
-@pytest.mark.parametrize("eq,bounds,d,opts", PAIR_CASES)
-def test_tc_pair_parity(lib, cuda, eq, bounds, d, opts, width):
-    # default width and both forced widths
+def _store_or_skip(lib, spec, bounds, d):
     try:
-        lib.Plan(f"{eq}:mul:sum:in=bf16{opts}:tc=pair{width}", bounds, d)
+        lib.Plan(spec, bounds, d)
     except lib.TraError as e:
         assert "TRA_ERR_UNSUPPORTED" in str(e)
-        pytest.skip("no pair tiling of this width")
-    _tc_case(lib, eq, bounds, d, opts + ":tc=pair" + width, "tc_bf16_pair")
+        pytest.skip("no tiling with this epilogue / width")
+
+
+@pytest.mark.parametrize("store", [":tc_store=tma", ":tc_store=lsu"])
+@pytest.mark.parametrize("eq,bounds,d,opts", CASES)
+def test_tc_parity(lib, cuda, eq, bounds, d, opts, store):
+    # the epilogue stores through an output tensor map (TMA) or with warp stores
+    _store_or_skip(lib, f"{eq}:mul:sum:in=bf16{opts}:tc=single{store}", bounds, d)
+    _tc_case(lib, eq, bounds, d, opts + ":tc=single" + store, "tc_bf16")
+
+
+@pytest.mark.parametrize("store", [":tc_store=tma", ":tc_store=lsu"])
+@pytest.mark.parametrize("width", ["", ":tc_n=256", ":tc_n=128"])
+@pytest.mark.parametrize("eq,bounds,d,opts", PAIR_CASES)
+def test_tc_pair_parity(lib, cuda, eq, bounds, d, opts, width, store):
+    # default width and both forced widths, each with both epilogues
+    _store_or_skip(lib, f"{eq}:mul:sum:in=bf16{opts}:tc=pair{width}{store}", bounds, d)
+    _tc_case(lib, eq, bounds, d, opts + ":tc=pair" + width + store, "tc_bf16_pair")
 
 
 def test_tc_repeat_and_stream(lib, cuda):
