@@ -1127,7 +1127,10 @@ int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_
     tp.tiles_m = t.tiles_m;
     tp.tiles_n = t.tiles_n;
     tp.n_tiles = t.n_tiles;
-    tp.group_m = 16;
+    // tile raster: groups of 16 M-tiles keep the operand panels of concurrent tiles in L2 for a
+    // long K loop; with a short one (write-bound: the output dominates the bytes) N runs
+    // fastest, so concurrent tiles write neighbouring output rows' segments
+    tp.group_m = t.num_kb <= 8 ? 1u : 16u;
     tp.block_n = t.block_n;
     tp.stages = t.stages;
     tp.num_kb = t.num_kb;
