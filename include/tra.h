@@ -152,6 +152,50 @@ int ein_repartition(int rank, const int64_t* shape, const int32_t* src_d, const 
 int ein_repartition_cost(int rank, const int64_t* shape, const int32_t* src_d, const int32_t* dst_d,
                          uint64_t* cost);
 
+/* ein_graph_decompose -- EinDecomp's optimiser (sections 3.1 and 3.2): choose one
+ * partition vector per node of an EinGraph so that the summed cost of section 3.1
+ * (every node's join + aggregation cost, plus the repartition cost of every edge
+ * whose producer output and consumer input are partitioned differently) is small.
+ * Host only.
+ *
+ * Candidates per node: one partition count D_l per distinct label, each a divisor of
+ * B_l (a power of two with TRA_DP_POW2), shared labels equal, with
+ * p_min <= n_tasks <= p_max (n_tasks = join tuples; the pages' parallelism
+ * constraint asks for at least P, usually exactly P: p_min = p_max = P).
+ * Dynamic programme in node order: DP[v][d] = cost(v, d) + sum over v's inputs that
+ * are nodes u of min over d' (DP[u][d'] + repartition(u's output under d' -> v's
+ * input under d)); the last node is the output; the choice is read back from it.
+ * Graph inputs (input -1) arrive in whatever partition their consumer asks for.
+ * Where a node feeds two consumers the programme counts its subgraph once per
+ * consumer and keeps the choice the later consumer made; total_cost is then
+ * recounted with every node and edge once.
+ *
+ * nodes:  n_nodes entries in topological order (an input index names an earlier node).
+ * d_out:  receives every node's vector (X's positions then Y's), nodes in order;
+ *         n_d_out must equal the sum of the nodes' ranks.
+ * node_cost (may be NULL): receives per node join + aggregation + the repartition cost
+ *         of its input edges under the chosen vectors.
+ * Errors: TRA_ERR_ARG (NULL, bad input index, node order, output/input shape mismatch,
+ *         n_d_out), TRA_ERR_PARSE / TRA_ERR_RANK (a node's spec), TRA_ERR_UNSUPPORTED
+ *         (a node has no candidate, or more than 65536). */
+typedef struct {
+    const char* spec;        /* the node's EinSum as for ein_plan (options are ignored) */
+    const int64_t* bounds;   /* B_l per distinct label, first-appearance order X then Y */
+    int32_t n_bounds;
+    int32_t input[2];        /* producing node of X and of Y, or -1 for a graph input */
+} tra_graph_node;
+
+typedef struct {
+    uint64_t total_cost;     /* nodes + edges under the chosen vectors, each counted once */
+    uint64_t dp_cost;        /* the programme's value at the output node */
+    uint64_t n_candidates;   /* partition vectors kept after pruning, over all nodes */
+} tra_graph_result;
+
+enum { TRA_DP_POW2 = 1 };
+
+int ein_graph_decompose(const tra_graph_node* nodes, int n_nodes, int64_t p_min, int64_t p_max, int flags,
+                        int32_t* d_out, int n_d_out, uint64_t* node_cost, tra_graph_result* result);
+
 /* ein_status -- synchronise the stream, then read and clear the device status word
  * that bounded waits inside the kernels set when they give up.  Returns TRA_OK,
  * TRA_ERR_TIMEOUT or TRA_ERR_CUDA. */

@@ -18,8 +18,8 @@ from ._build import LIB as _LIB_PATH, build as _build_lib
 __all__ = [
     "TraError", "build_library", "load", "Plan", "ein_plan", "ein_plan_info", "ein_plan_keys", "ein_execute",
     "ein_repartition", "ein_repartition_cost", "ein_status", "ein_selftest_wait_timeout", "ein_plan_destroy",
-    "ein_last_error",
-    "repartition", "repartition_cost", "KERNELS", "ROLES",
+    "ein_last_error", "ein_graph_decompose",
+    "repartition", "repartition_cost", "decompose", "KERNELS", "ROLES",
 ]
 
 TRA_MAX_RANK = 8
@@ -60,6 +60,17 @@ class tra_plan_info(ctypes.Structure):
     ]
 
 
+class tra_graph_node(ctypes.Structure):
+    _fields_ = [("spec", ctypes.c_char_p), ("bounds", ctypes.POINTER(ctypes.c_int64)), ("n_bounds", ctypes.c_int32),
+                ("input", ctypes.c_int32 * 2)]
+
+
+class tra_graph_result(ctypes.Structure):
+    _fields_ = [("total_cost", ctypes.c_uint64), ("dp_cost", ctypes.c_uint64), ("n_candidates", ctypes.c_uint64)]
+
+
+TRA_DP_POW2 = 1
+
 _lib = None
 
 
@@ -89,8 +100,10 @@ def load():
     lib.ein_plan_destroy.argtypes = [vp]
     lib.ein_plan_destroy.restype = None
     lib.ein_last_error.restype = ctypes.c_char_p
+    lib.ein_graph_decompose.argtypes = [ctypes.POINTER(tra_graph_node), i32, i64, i64, i32, vp, i32, u64p,
+                                        ctypes.POINTER(tra_graph_result)]
     for f in ("ein_plan", "ein_plan_info", "ein_plan_keys", "ein_execute", "ein_repartition",
-              "ein_repartition_cost", "ein_status"):
+              "ein_repartition_cost", "ein_status", "ein_graph_decompose"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -161,6 +174,31 @@ def ein_repartition_cost(shape, src_d, dst_d) -> int:
     c = ctypes.c_uint64()
     _check(load().ein_repartition_cost(len(shape), _i64(shape), _i32(src_d), _i32(dst_d), ctypes.byref(c)))
     return c.value
+
+
+def ein_graph_decompose(nodes, p_min: int, p_max: int, flags: int = 0):
+    """nodes: sequence of (spec, bounds, (input_x, input_y)) with -1 for a graph input.
+    Returns (d per node, cost per node, total_cost, dp_cost, n_candidates)."""
+    keep, arr = [], (tra_graph_node * len(nodes))()
+    ranks = []
+    for i, (spec, bounds, inputs) in enumerate(nodes):
+        b = _i64(bounds)
+        e = spec.encode()
+        keep += [b, e]
+        arr[i].spec, arr[i].bounds, arr[i].n_bounds = e, ctypes.cast(b, ctypes.POINTER(ctypes.c_int64)), len(bounds)
+        arr[i].input[0], arr[i].input[1] = (list(inputs) + [-1, -1])[:2]
+        lhs = spec.split("->")[0]
+        ranks.append([len(x) for x in lhs.split(",")])
+    n_d = sum(sum(r) for r in ranks)
+    d = (ctypes.c_int32 * max(1, n_d))()
+    costs = (ctypes.c_uint64 * len(nodes))()
+    res = tra_graph_result()
+    _check(load().ein_graph_decompose(arr, len(nodes), p_min, p_max, flags, d, n_d, costs, ctypes.byref(res)))
+    out, pos = [], 0
+    for r in ranks:
+        out.append(list(d[pos:pos + sum(r)]))
+        pos += sum(r)
+    return out, list(costs), res.total_cost, res.dp_cost, res.n_candidates
 
 
 def ein_status(stream=None):
@@ -283,3 +321,14 @@ def repartition(src, dst, shape, src_d, dst_d, stream=None):
 
 def repartition_cost(shape, src_d, dst_d) -> int:
     return ein_repartition_cost(shape, src_d, dst_d)
+
+
+def decompose(nodes, P: int, p_max: int = None, pow2: bool = False):
+    """EinDecomp over an EinGraph (host only): a partition vector for every node with
+    P..p_max join tuples (p_max defaults to P), minimising join + aggregation +
+    repartition cost.  nodes: (spec, bounds, (input_x, input_y)) in topological order,
+    -1 marking a graph input.  Returns a dict with "d", "node_cost", "total_cost",
+    "dp_cost", "n_candidates"."""
+    d, costs, total, dp, n = ein_graph_decompose(nodes, P, P if p_max is None else p_max,
+                                                 TRA_DP_POW2 if pow2 else 0)
+    return {"d": d, "node_cost": costs, "total_cost": total, "dp_cost": dp, "n_candidates": n}

@@ -448,30 +448,7 @@ int ein_repartition_cost(int rank, const int64_t* shape, const int32_t* src_d, c
         if (src_d[i] < 1 || dst_d[i] < 1 || shape[i] % src_d[i] || shape[i] % dst_d[i])
             return fail(TRA_ERR_DIVISIBILITY, "partition count does not divide extent %lld", (long long)shape[i]);
     }
-    uint64_t total = 1, ns = 1, nd = 1;
-    for (int i = 0; i < rank; ++i) {
-        total *= (uint64_t)shape[i];
-        ns *= (uint64_t)src_d[i];
-        nd *= (uint64_t)dst_d[i];
-    }
-    // blocks are owned by their row-major linear key id L; elements in
-    // block_L(src) n block_L(dst) stay, all others move
-    uint64_t stay = 0;
-    const uint64_t n = ns < nd ? ns : nd;
-    for (uint64_t L = 0; L < n; ++L) {
-        uint64_t ls = L, ld = L, inter = 1;
-        for (int i = rank - 1; i >= 0 && inter; --i) {
-            const uint64_t ks = ls % (uint64_t)src_d[i], kd = ld % (uint64_t)dst_d[i];
-            ls /= (uint64_t)src_d[i];
-            ld /= (uint64_t)dst_d[i];
-            const uint64_t bs = (uint64_t)shape[i] / src_d[i], bd = (uint64_t)shape[i] / dst_d[i];
-            const uint64_t lo = ks * bs > kd * bd ? ks * bs : kd * bd;
-            const uint64_t hi = (ks + 1) * bs < (kd + 1) * bd ? (ks + 1) * bs : (kd + 1) * bd;
-            inter *= hi > lo ? hi - lo : 0;
-        }
-        stay += inter;
-    }
-    *cost = total - stay;
+    *cost = repartition_cost_elems(rank, shape, src_d, dst_d);
     return TRA_OK;
 }
 

@@ -41,6 +41,34 @@ const char* last_error() { return g_err.c_str(); }
 
 uint64_t align256(uint64_t v) { return (v + 255) & ~uint64_t(255); }
 
+// Elements whose owning block changes between two partitions of one tensor, blocks being
+// owned by their row-major linear key id L: |T| - sum_L |block_L(src) n block_L(dst)|.
+// Arguments already validated (every d divides its extent).
+uint64_t repartition_cost_elems(int rank, const int64_t* shape, const int32_t* src_d, const int32_t* dst_d) {
+    uint64_t total = 1, ns = 1, nd = 1;
+    for (int i = 0; i < rank; ++i) {
+        total *= (uint64_t)shape[i];
+        ns *= (uint64_t)src_d[i];
+        nd *= (uint64_t)dst_d[i];
+    }
+    uint64_t stay = 0;
+    const uint64_t n = ns < nd ? ns : nd;
+    for (uint64_t L = 0; L < n; ++L) {
+        uint64_t ls = L, ld = L, inter = 1;
+        for (int i = rank - 1; i >= 0 && inter; --i) {
+            const uint64_t ks = ls % (uint64_t)src_d[i], kd = ld % (uint64_t)dst_d[i];
+            ls /= (uint64_t)src_d[i];
+            ld /= (uint64_t)dst_d[i];
+            const uint64_t bs = (uint64_t)shape[i] / src_d[i], bd = (uint64_t)shape[i] / dst_d[i];
+            const uint64_t lo = ks * bs > kd * bd ? ks * bs : kd * bd;
+            const uint64_t hi = (ks + 1) * bs < (kd + 1) * bd ? (ks + 1) * bs : (kd + 1) * bd;
+            inter *= hi > lo ? hi - lo : 0;
+        }
+        stay += inter;
+    }
+    return total - stay;
+}
+
 Plan::~Plan() {
     if (tc) tc_free(tc);
 }

@@ -81,6 +81,7 @@ void tc_free(TcPlan* t);
 int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_t s);
 
 uint64_t align256(uint64_t v);
+uint64_t repartition_cost_elems(int rank, const int64_t* shape, const int32_t* src_d, const int32_t* dst_d);
 
 // Exhaustive host check of the semiring kernel's 4-wide loads: an operand may load
 // 4 consecutive indices of a role at once only if every 4-aligned group of that role
