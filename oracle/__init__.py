@@ -15,6 +15,8 @@ summation + tensor relational algebra".
   plan enumeration and the communication-cost terms of section 3.1, and a
   literal TRA execution (relation dictionaries, join, GROUP BY aggregate).
 * ``mha`` -- the multi-head-attention EinGraph of section 2.1, node by node.
+* ``decomp`` -- the partition-vector choice of sections 3.1-3.2 by exhaustive search
+  over every combination of every node's candidates (tiny graphs).
 * ``rounding`` -- fp32 / bf16 round-to-nearest-even.
 
 Parity pins: every function above is checked in ``tests/test_oracle_pins.py``
