@@ -196,6 +196,23 @@ enum { TRA_DP_POW2 = 1 };
 int ein_graph_decompose(const tra_graph_node* nodes, int n_nodes, int64_t p_min, int64_t p_max, int flags,
                         int32_t* d_out, int n_d_out, uint64_t* node_cost, tra_graph_result* result);
 
+/* ein_attention -- the attention chain of the multi-head-attention EinGraph (section 2.1)
+ * fused into one kernel: Scores[h,s,t] = scale * sum_d Q K, L[h,s] = logsumexp_t Scores,
+ * Attn = exp(Scores - L), O[s,h,d] = sum_t Attn V -- without writing Scores or Attn
+ * (running max / sum over blocks of 128 keys, O rescaled as the max moves).
+ *
+ * q:     bf16 [h][s][d]  (the relation of Q_proj under d = [1, h, 1]: head-major)
+ * k, v:  bf16 [h][t][d]
+ * o:     bf16 [s][h][d]  (dense, as the output projection reads it)
+ * lse:   fp32 [h][s] receives L (may be NULL)
+ * d must be 128; s and t multiples of 128; device buffers 16-byte aligned (lse 4).
+ * Asynchronous on stream; no workspace.  The result is the unfused chain's within the BF16
+ * bar: P = Attn is rounded to bf16 before the A.V contraction, as the unfused chain's
+ * bf16 Attn is, but against the running max rather than the final L.
+ * Errors: TRA_ERR_ARG, TRA_ERR_UNSUPPORTED (shape), TRA_ERR_CUDA. */
+int ein_attention(int s, int t, int h, int d, float scale, const void* q, const void* k, const void* v, void* o,
+                  void* lse, tra_stream_t stream);
+
 /* ein_status -- synchronise the stream, then read and clear the device status word
  * that bounded waits inside the kernels set when they give up.  Returns TRA_OK,
  * TRA_ERR_TIMEOUT or TRA_ERR_CUDA. */

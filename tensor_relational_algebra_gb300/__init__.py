@@ -18,7 +18,7 @@ from ._build import LIB as _LIB_PATH, build as _build_lib
 __all__ = [
     "TraError", "build_library", "load", "Plan", "ein_plan", "ein_plan_info", "ein_plan_keys", "ein_execute",
     "ein_repartition", "ein_repartition_cost", "ein_status", "ein_selftest_wait_timeout", "ein_plan_destroy",
-    "ein_last_error", "ein_graph_decompose",
+    "ein_last_error", "ein_graph_decompose", "ein_attention", "attention",
     "repartition", "repartition_cost", "decompose", "KERNELS", "ROLES",
 ]
 
@@ -102,8 +102,9 @@ def load():
     lib.ein_last_error.restype = ctypes.c_char_p
     lib.ein_graph_decompose.argtypes = [ctypes.POINTER(tra_graph_node), i32, i64, i64, i32, vp, i32, u64p,
                                         ctypes.POINTER(tra_graph_result)]
+    lib.ein_attention.argtypes = [i32, i32, i32, i32, ctypes.c_float, vp, vp, vp, vp, vp, vp]
     for f in ("ein_plan", "ein_plan_info", "ein_plan_keys", "ein_execute", "ein_repartition",
-              "ein_repartition_cost", "ein_status", "ein_graph_decompose"):
+              "ein_repartition_cost", "ein_status", "ein_graph_decompose", "ein_attention"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -199,6 +200,15 @@ def ein_graph_decompose(nodes, p_min: int, p_max: int, flags: int = 0):
         out.append(list(d[pos:pos + sum(r)]))
         pos += sum(r)
     return out, list(costs), res.total_cost, res.dp_cost, res.n_candidates
+
+
+def ein_attention(s: int, t: int, h: int, d: int, scale: float, q, k, v, o, lse=None, stream=None):
+    _check(load().ein_attention(s, t, h, d, scale, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _stream(stream)))
+
+
+def attention(q, k, v, o, s: int, t: int, h: int, d: int = 128, scale: float = None, lse=None, stream=None):
+    """Fused Scores -> logsumexp -> exp -> A.V on device tensors (see ein_attention)."""
+    ein_attention(s, t, h, d, (1.0 / d ** 0.5) if scale is None else scale, q, k, v, o, lse, stream)
 
 
 def ein_status(stream=None):

@@ -12,19 +12,23 @@ run node by node through the C ABI (one ein_execute or ein_repartition per node)
 
 The printed Scores[h,s,s] is read with a second sequence index t; the scale is applied
 after the sum over d; there is no mask.  Buffers are allocated once (torch) and reused.
+
+With fused=True the four nodes Scores -> L -> A -> O and the repartition of O run as one
+kernel (ein_attention), which writes O dense and L, never the scores or A.
 """
 from __future__ import annotations
 
 import math
 
-from . import Plan, repartition
+from . import Plan, attention, repartition
 
 
 class AttentionGraph:
-    def __init__(self, s: int, a: int, h: int, d: int, device="cuda"):
+    def __init__(self, s: int, a: int, h: int, d: int, device="cuda", fused: bool = False):
         import torch
 
         self.s, self.a, self.h, self.d = s, a, h, d
+        self.fused = fused
         t = s
         self.p_proj = Plan("sa,ahd->shd:mul:sum:in=bf16:out=bf16", [s, a, h, d], [1, 1, 1, 1, 1])
         self.p_scores = Plan(f"shd,thd->hst:mul:sum:in=bf16:alpha={1.0 / math.sqrt(d)!r}", [s, h, d, t],
@@ -37,9 +41,9 @@ class AttentionGraph:
         e = lambda n, dt: torch.empty(n, dtype=dt, device=device)  # noqa: E731
         self.qp, self.kp, self.vp = e(s * h * d, bf), e(s * h * d, bf), e(s * h * d, bf)
         self.qr, self.kr, self.vr = e(s * h * d, bf), e(s * h * d, bf), e(s * h * d, bf)
-        self.S = e(h * s * t, f32)
+        self.S = None if fused else e(h * s * t, f32)
         self.L = e(h * s, f32)
-        self.A = e(h * s * t, bf)
+        self.A = None if fused else e(h * s * t, bf)
         self.Oh = e(s * h * d, bf)
         self.O = e(s * h * d, bf)
         self.out = e(s * a, f32)
@@ -58,6 +62,11 @@ class AttentionGraph:
                                                         repartition(self.kp, self.kr, shd, [1, 1, 1], [1, h, 1]),
                                                         repartition(self.vp, self.vr, shd, [1, 1, 1], [1, h, 1])),
              3 * 2 * s * h * d * 2, "bytes", "hbm", 3),
+        ] + ([
+            ("attention (Scores -> L -> exp -> A.V fused)",
+             lambda: attention(self.qr, self.kr, self.vr, self.O, s, s, h, d, lse=self.L),
+             2 * att, "flop", "tensor", 1),
+        ] if self.fused else [
             ("scores", lambda: self.p_scores.execute(self.qr, self.kr, self.S), att, "flop", "tensor", 1),
             ("logsumexp", lambda: self.p_lse.execute(self.S, None, self.L), h * s * s * 4 + h * s * 4, "bytes", "hbm", 1),
             ("exp(S-L)", lambda: self.p_exp.execute(self.S, self.L, self.A), h * s * s * (4 + 2) + h * s * 4, "bytes",
@@ -65,6 +74,7 @@ class AttentionGraph:
             ("A.V", lambda: self.p_pv.execute(self.A, self.vr, self.Oh), att, "flop", "tensor", 1),
             ("repartition O -> dense", lambda: repartition(self.Oh, self.O, shd, [1, h, 1], [1, 1, 1]),
              2 * s * h * d * 2, "bytes", "hbm", 1),
+        ]) + [
             ("out proj", lambda: self.p_out.execute(self.O, WO, self.out), gemm, "flop", "tensor", 1),
         ]
 

@@ -454,10 +454,11 @@ int ein_repartition_cost(int rank, const int64_t* shape, const int32_t* src_d, c
 
 int ein_status(tra_stream_t stream) {
     clear_error();
-    int v = 0;
+    int v = 0, va = 0;
     cudaError_t e = read_and_clear_status(&v, reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = read_and_clear_attn_status(&va, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "status read");
-    if (v) return fail(v, "a bounded device wait gave up (status %d)", v);
+    if (v || va) return fail(v ? v : va, "a bounded device wait gave up (status %d)", v ? v : va);
     return TRA_OK;
 }
 

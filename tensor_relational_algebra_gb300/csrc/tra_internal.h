@@ -201,6 +201,7 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 
 // Device status word written by bounded waits that give up (TRA_ERR_TIMEOUT).
 cudaError_t read_and_clear_status(int* value, cudaStream_t s);
+cudaError_t read_and_clear_attn_status(int* value, cudaStream_t s);
 cudaError_t launch_wait_timeout_probe(uint64_t timeout_ns, cudaStream_t s);
 
 }  // namespace tra

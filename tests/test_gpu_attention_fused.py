@@ -1,0 +1,83 @@
+"""The attention chain fused into one kernel (ein_attention) against the oracle and against
+the unfused EinGraph nodes ("EinDecomp ... tensor relational algebra", section 2.1).
+
+O is compared at the BF16 bar (2e-2 of max|ref|) with the oracle's chain evaluated in double
+(S, L = logsumexp_t S, A = exp(S - L), O = A.V); L within 1e-4 of max(|L|, 1).  The cases
+cover one key block, an odd number of key blocks with s != t, several heads, and the whole
+attention EinGraph with the fused node against the unfused one.
+"""
+import numpy as np
+import pytest
+
+import datagen
+import oracle
+from oracle import mha
+
+from gpu_helpers import as_f64, check_bf16_bar, from_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(lib, s, t, h, seed):
+    import torch
+
+    d = 128
+    q = datagen.normal_bf16((h, s, d), seed, 0)
+    k = datagen.normal_bf16((h, t, d), seed, 1)
+    v = datagen.normal_bf16((h, t, d), seed, 2)
+    dev = [torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda().reshape(-1) for a in (q, k, v)]
+    o = torch.empty(s * h * d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(h * s, dtype=torch.float32, device="cuda")
+    lib.attention(dev[0], dev[1], dev[2], o, s, t, h, d, lse=lse)
+    lib.ein_status()
+    f = [datagen.bf16_bits_to_f32(a).astype(np.float64) for a in (q, k, v)]
+    qs, ks, vs = (np.transpose(a, (1, 0, 2)) for a in f)  # [s|t][h][d]
+    S = oracle.einsum("shd,thd->hst", qs, ks, alpha=1.0 / np.sqrt(d))
+    L = oracle.einsum("hst->hs", S, agg="lse")
+    A = oracle.einsum("hst,hs->hst", S, L, op="expsub", agg="none")
+    O = oracle.einsum("hst,thd->shd", A, vs)
+    return as_f64(from_dev(o)).reshape(s, h, d), as_f64(from_dev(lse)).reshape(h, s), O, L
+
+
+@pytest.mark.parametrize("s,t,h", [(128, 128, 1), (256, 384, 3), (384, 1024, 2)])
+def test_fused_attention_against_oracle(lib, cuda, s, t, h):
+    o, lse, O, L = _run(lib, s, t, h, 40 + s + t + h)
+    check_bf16_bar(o, O)
+    assert np.all(np.abs(lse - L) <= 1e-4 * np.maximum(np.abs(L), 1.0))
+
+
+def test_fused_node_in_the_attention_eingraph(lib, cuda):
+    import torch
+
+    from tensor_relational_algebra_gb300.attention import AttentionGraph
+
+    s, a, h, d = 512, 256, 2, 128
+    acts = [datagen.normal_bf16((s, a), 41, t) for t in range(3)]
+    ws = [datagen.normal_bf16((a, h, d), 41, 3 + t, 0.0, 0.02) for t in range(4)]
+    dev = [torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda().reshape(-1) for b in acts + ws]
+    unfused = AttentionGraph(s, a, h, d)
+    fused = AttentionGraph(s, a, h, d, fused=True)
+    unfused(*dev)
+    fused(*dev)
+    torch.cuda.synchronize()
+    lib.ein_status()
+    ref = mha.chain(*[datagen.bf16_bits_to_f32(b) for b in acts + ws], engine="blas")
+    check_bf16_bar(as_f64(from_dev(fused.O)).reshape(s, h, d), ref["O"])
+    check_bf16_bar(as_f64(from_dev(fused.out)).reshape(s, a), ref["out"])
+    # against the unfused nodes on the same device inputs
+    check_bf16_bar(as_f64(from_dev(fused.O)), as_f64(from_dev(unfused.O)))
+    Lf, Lu = as_f64(from_dev(fused.L)), as_f64(from_dev(unfused.L))
+    assert np.all(np.abs(Lf - Lu) <= 1e-4 * np.maximum(np.abs(Lu), 1.0))
+
+
+@pytest.mark.parametrize("args,code", [((128, 128, 1, 64), "TRA_ERR_UNSUPPORTED"),
+                                       ((100, 128, 1, 128), "TRA_ERR_UNSUPPORTED"),
+                                       ((128, 200, 1, 128), "TRA_ERR_UNSUPPORTED")])
+def test_fused_attention_rejects_shapes(lib, cuda, args, code):
+    import torch
+
+    buf = torch.zeros(1 << 20, dtype=torch.bfloat16, device="cuda")
+    s, t, h, d = args
+    with pytest.raises(lib.TraError) as e:
+        lib.ein_attention(s, t, h, d, 0.1, buf, buf, buf, buf)
+    assert code in str(e.value)
