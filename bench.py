@@ -10,7 +10,8 @@ relation), then both join + aggregate EinSums.
 
 Other workloads (``--workload``): c1 (64^3 fp32 matmul under three d), c3 (4-D
 BF16 contraction + repartition of its output), c4 (multi-head-attention
-EinGraph), c5 (16384^3 BF16 matmul, ``--d``), c5b (8192^3 logsumexp).
+EinGraph; c4f the same with the attention chain fused into one kernel), c5
+(16384^3 BF16 matmul, ``--d``), c5b (8192^3 logsumexp).
 
 ``--impl reference`` times the CPU oracle on a bounded sample of the same
 workload (the reference arm).  Under torchrun (N > 1) every rank runs an
@@ -388,6 +389,24 @@ class C4Workload(_PointsWorkload):
         return f"{n} outputs of the Q projection node (4096 terms each)"
 
 
+class C4fWorkload(C4Workload):
+    name = ("multi-head attention EinGraph s=4096 a=4096 h=32 d=128, BF16 activations N(0,1), weights N(0,0.02), "
+            "Scores -> L -> exp -> A.V -> repartition O fused in one kernel")
+    d = "projections all-ones; fused attention split over (s/128 row blocks) x h; repartitions of Q/K/V before"
+
+    def setup(self, tra, torch, inputs):
+        from tensor_relational_algebra_gb300.attention import AttentionGraph
+
+        self.g = AttentionGraph(4096, 4096, 32, 128, fused=True)
+        self.dev = [_dev_bf16(torch, x) for x in inputs]
+        self.steps = [Step(*n) for n in self.g.nodes(*self.dev)]
+        self.inputs_dev = self.dev
+        self.outputs_dev = [self.g.out]
+
+    def traffic_key(self, j):
+        return ("k_attn.cu", "attention s=4096 h=32 d=128" if self.steps[j].name.startswith("attention") else "-")
+
+
 class C5Workload(_PointsWorkload):
     name_fmt = "BF16 matmul 16384^3 (FP32 accumulate), d={}"
     d = [1, 1, 1, 1]
@@ -474,7 +493,7 @@ class C5bWorkload(_PointsWorkload):
         return f"{n} of 8192^2 outputs"
 
 
-WORKLOADS = {"pair": PairWorkload, "c1": C1Workload, "c1l": C1LiteralWorkload, "c3": C3Workload, "c4": C4Workload, "c5": C5Workload,
+WORKLOADS = {"pair": PairWorkload, "c1": C1Workload, "c1l": C1LiteralWorkload, "c3": C3Workload, "c4": C4Workload, "c4f": C4fWorkload, "c5": C5Workload,
              "c5b": C5bWorkload}
 
 
