@@ -4,18 +4,22 @@
 // "EinDecomp ... tensor relational algebra", section 2.1 (multi-head attention as EinSums):
 //   S[h,s,t] = scale * sum_d Q[h,s,d] K[h,t,d],  L[h,s] = logsumexp_t S[h,s,t],
 //   A[h,s,t] = exp(S[h,s,t] - L[h,s]),           O[s,h,d] = sum_t A[h,s,t] V[h,t,d].
-// Here the t axis is walked in blocks of 128 keys with a running maximum m and running sum
-// l per query row (the logsumexp of the blocks seen so far is m + log l); O is rescaled by
-// exp(m_old - m_new) whenever m moves, so after the last block O / l is the chained result
-// and m + log l is L.
+// Here the t axis is walked in blocks of 128 keys with a reference maximum m and running sum
+// l per query row (the logsumexp of the blocks seen so far is m + log l).  m moves only when
+// a block's maximum exceeds it by more than 2^8 (so every exponent stays below 2^8); then l
+// and O are rescaled by exp(m_old - m_new).  After the last block O / l is the chained
+// result and m + log l is L.
 //
-// One CTA per (head, 128 query rows); 7 warps:
-//   warp 0   TMA loads of Q (once) and of each K block,   warp 1   TMA loads of each V block,
+// One CTA per (head, 128 query rows); 11 warps:
+//   warp 0   TMA loads of Q (once) and of each K block (three slots, each freed once S_j is
+//            computed), one 32 KB copy per tile,
+//   warp 1   TMA loads of each V block (two slots, freed once P_j V_j is computed),
 //   warp 2   tensor memory and the MMAs: S_j = Q K_j^T into one of two TMEM buffers, then
-//            O += P_j V_j with P_j (bf16) read from shared memory,
-//   warps 3-6 (TMEM lane quarter warp % 4, one query row per thread): the softmax update,
-//            P_j in the 128-byte-swizzled K-major layout the MMA reads, the rescale of O, and
-//            the epilogue (O / l as bf16 in [s][h][d]; L as fp32 in [h][s]).
+//            O += P_j V_j with P_j (bf16) read from tensor memory (one buffer),
+//   warps 3-10 (TMEM lane quarter warp % 4, one query row per thread, key half (warp - 3) / 4):
+//            the softmax update of that half (the halves share each block's row maximum), its
+//            P_j columns stored to tensor memory, the rescale of O, and the epilogue (O as bf16
+//            in [s][h][d]; L as fp32 in [h][s]).
 // Every mbarrier wait is bounded; a wait that gives up records TRA_ERR_TIMEOUT in this unit's
 // status word (read by ein_status), raises the CTA's abort flag and the CTA leaves after its
 // copies and MMAs in flight have landed.
@@ -39,11 +43,14 @@ namespace {
 constexpr int kHead = 128;     // head dimension d
 constexpr int kRows = 128;     // query rows per CTA
 constexpr int kKeys = 128;     // keys per block
-constexpr int kThreadsA = 7 * 32;
+constexpr int kThreadsA = 11 * 32;
 constexpr uint32_t kTile = 128 * 128 * 2;   // one 128 x 128 bf16 operand tile (two 16 KB boxes)
 constexpr uint32_t kHalf = kTile / 2;       // one box: 64 columns x 128 rows
-// shared memory: Q | K0 V0 | K1 V1 | P0 | P1 | barriers (all tiles 1024-aligned)
-constexpr uint32_t kSmemA = 7 * kTile + 1024 + 256;
+constexpr uint32_t kKStages = 3;            // K tiles in flight; V has two
+constexpr uint32_t kTiles = 1 + kKStages + 2;
+// shared memory: Q | K0 K1 K2 | V0 V1 | barriers, TMEM slot, abort flag (256 B) | the softmax
+// warps' exchange array (2 KB); tiles 1024-aligned
+constexpr uint32_t kSmemA = kTiles * kTile + 1024 + 256 + 2048;
 
 struct AttnParams {
     uint32_t s, t, h, nb;   // query rows, keys, heads, key blocks
@@ -57,8 +64,10 @@ __device__ __forceinline__ bool wait_a(uint32_t bar, uint32_t parity, volatile i
     return mbar_wait_status(bar, parity, abort, ns, &g_attn_status);
 }
 
-__device__ __forceinline__ void tma_load_rows(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int row) {
-    const int c[5] = {x, row, 0, 0, 0};
+// one 128-row x 128-column bf16 tile: the map's box covers both 64-column halves, the
+// second landing 16 KB after the first
+__device__ __forceinline__ void tma_load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar, int row) {
+    const int c[5] = {0, row, 0, 0, 0};
     tma_load_5d(dst, map, bar, c);
 }
 
@@ -80,6 +89,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 __global__ void __launch_bounds__(kThreadsA, 1)
     attn_fwd(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
              const __grid_constant__ CUtensorMap map_v, const __grid_constant__ AttnParams p) {
@@ -87,31 +101,39 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t sq = base;
-    auto sk = [&](uint32_t st) { return base + kTile + st * 2 * kTile; };
-    auto sv = [&](uint32_t st) { return base + 2 * kTile + st * 2 * kTile; };
-    auto sp = [&](uint32_t b) { return base + 5 * kTile + b * kTile; };
-    const uint32_t bar = base + 7 * kTile;
-    // barriers: q_full, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full[2], o_done, mma_done,
-    // then the TMEM slot and the abort flag
-    const uint32_t q_full = bar, kv_full = bar + 8, kv_empty = bar + 24, s_full = bar + 40, s_free = bar + 56,
-                   p_full = bar + 72, o_done = bar + 88, mma_done = bar + 96;
+    auto sk = [&](uint32_t st) { return base + (1 + st) * kTile; };
+    auto sv = [&](uint32_t st) { return base + (1 + kKStages + st) * kTile; };
+    const uint32_t bar = base + kTiles * kTile;
+    // barriers: q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], s_free[2], p_full,
+    // o_done[2], mma_done, xch[2][4]; then the TMEM slot, the abort flag and the exchange array
+    const uint32_t q_full = bar, k_full = bar + 8, k_empty = bar + 32, v_full = bar + 56, v_empty = bar + 72,
+                   s_full = bar + 88, s_free = bar + 104, p_full = bar + 120, o_done = bar + 128,
+                   mma_done = bar + 144, xbar = bar + 152;
     uint8_t* gbase = smem_raw + (base - raw);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar + 104 - base));
-    volatile int* abort = reinterpret_cast<volatile int*>(gbase + (bar + 108 - base));
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar + 216 - base));
+    volatile int* abort = reinterpret_cast<volatile int*>(gbase + (bar + 220 - base));
+    float* xval = reinterpret_cast<float*>(gbase + (bar + 256 - base));  // [2 slots][2 halves][128 rows]
 
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    // warp index and tensor-memory base made provably warp-uniform (shuffled from lane 0), so the
+    // tcgen05 operands derived from them live in uniform registers
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x / 32), 0), lane = threadIdx.x % 32;
     const uint32_t hd = blockIdx.y, q0 = blockIdx.x * kRows;
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(kv_full + 8 * i, 2);   // the K and the V producer each arrive with their bytes
-            mbar_init(kv_empty + 8 * i, 1);  // MMA commit after the block's P.V
-            mbar_init(s_full + 8 * i, 1);    // MMA commit after S_j
-            mbar_init(s_free + 8 * i, 4);    // one lane of each softmax warp
-            mbar_init(p_full + 8 * i, 4);
+        for (int i = 0; i < kKStages; ++i) {
+            mbar_init(k_full + 8 * i, 1);   // the K producer's arrive with its bytes
+            mbar_init(k_empty + 8 * i, 1);  // MMA commit after S_j (K_j read)
         }
-        mbar_init(o_done, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(v_full + 8 * i, 1);
+            mbar_init(v_empty + 8 * i, 1);  // MMA commit after P_j V_j
+            mbar_init(s_full + 8 * i, 1);   // MMA commit after S_j
+            mbar_init(s_free + 8 * i, 8);   // one lane of each softmax warp: S_j is in registers
+            mbar_init(o_done + 8 * i, 1);   // MMA commit after P_j V_j
+        }
+        mbar_init(p_full, 8);               // one lane of each softmax warp: P_j stored, O rescaled
         mbar_init(mma_done, 1);
+        for (int i = 0; i < 8; ++i) mbar_init(xbar + 8 * i, 64);  // both warps of a lane quarter
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -124,79 +146,110 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t t_s0 = tmem, t_o = tmem + 256;  // S buffers at columns 0 and 128, O at 256
+    const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
+    // columns: S buffers 0-127 and 128-255 (fp32), O 256-383 (fp32), P 384-447 (bf16 pairs:
+    // column c holds keys 2c and 2c + 1)
+    const uint32_t t_s0 = tmem, t_o = tmem + 256, t_p = tmem + 384;
 
+    // producer and MMA warps run their loops with the whole warp (waits taken by every lane, the
+    // result shuffled from lane 0 so that control flow stays uniform); one elected lane issues
+    auto wait_u = [&](uint32_t b_, uint32_t parity) {
+        return __shfl_sync(0xffffffffu, (int)wait_a(b_, parity, abort, p.timeout_ns), 0) != 0;
+    };
     if (warp <= 1) {
-        // ------------------------------------------------------------------ producers
-        if (lane == 0) {
-            const CUtensorMap* map = warp == 0 ? &map_k : &map_v;
-            if (warp == 0) {
+        // ------------------------------------------------------------------ producers (K: warp 0, V: warp 1)
+        // one 32 KB copy per tile (both 64-column halves)
+        if (warp == 0) {
+            if (elect_one()) {
                 mbar_expect_tx(q_full, kTile);
-                tma_load_rows(sq, &map_q, q_full, 0, (int)(hd * p.s + q0));
-                tma_load_rows(sq + kHalf, &map_q, q_full, 64, (int)(hd * p.s + q0));
+                tma_load_tile(sq, &map_q, q_full, (int)(hd * p.s + q0));
             }
             for (uint32_t j = 0; j < p.nb; ++j) {
-                const uint32_t st = j & 1, ph = (j >> 1) & 1;
-                if (!wait_a(kv_empty + 8 * st, ph ^ 1, abort, p.timeout_ns)) break;
-                mbar_expect_tx(kv_full + 8 * st, kTile);
-                const uint32_t dst = warp == 0 ? sk(st) : sv(st);
-                const int row = (int)(hd * p.t + j * kKeys);
-                tma_load_rows(dst, map, kv_full + 8 * st, 0, row);
-                tma_load_rows(dst + kHalf, map, kv_full + 8 * st, 64, row);
+                const uint32_t st = j % kKStages, ph = (j / kKStages) & 1;
+                if (!wait_u(k_empty + 8 * st, ph ^ 1)) break;
+                if (elect_one()) {
+                    mbar_expect_tx(k_full + 8 * st, kTile);
+                    tma_load_tile(sk(st), &map_k, k_full + 8 * st, (int)(hd * p.t + j * kKeys));
+                }
+                __syncwarp();
             }
-            if (*abort) __nanosleep(20000);  // let copies already issued land before leaving
+        } else {
+            for (uint32_t j = 0; j < p.nb; ++j) {
+                const uint32_t st = j & 1, ph = (j >> 1) & 1;
+                if (!wait_u(v_empty + 8 * st, ph ^ 1)) break;
+                if (elect_one()) {
+                    mbar_expect_tx(v_full + 8 * st, kTile);
+                    tma_load_tile(sv(st), &map_v, v_full + 8 * st, (int)(hd * p.t + j * kKeys));
+                }
+                __syncwarp();
+            }
         }
+        if (*abort) __nanosleep(20000);  // let copies already issued land before leaving
     } else if (warp == 2) {
         // ------------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            // S = Q K^T: M = 128, N = 128 keys, both K-major; O += P V: M = 128, N = 128, P K-major,
-            // V M/N-major (d innermost; its two 64-column boxes are 16 KB apart)
-            const uint32_t id_s = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
-            const uint32_t id_o = id_s | (1u << 16);
-            bool ok = wait_a(q_full, 0, abort, p.timeout_ns);
-            auto issue_s = [&](uint32_t j) {
-                const uint32_t st = j & 1;
-                if (!wait_a(kv_full + 8 * st, (j >> 1) & 1, abort, p.timeout_ns)) return false;
-                tc_fence_after();
-                for (uint32_t kk = 0; kk < kHead / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    tc_mma(t_s0 + st * 128, smem_desc(sq + off, 16, 1024), smem_desc(sk(st) + off, 16, 1024), id_s,
-                           kk != 0);
-                }
-                tc_commit(s_full + 8 * st);
-                return true;
-            };
-            if (ok) ok = issue_s(0);
-            if (ok && p.nb > 1) ok = issue_s(1);
-            for (uint32_t j = 0; ok && j < p.nb; ++j) {
-                const uint32_t b = j & 1, ph = (j >> 1) & 1;
-                if (!wait_a(p_full + 8 * b, ph, abort, p.timeout_ns)) break;
-                tc_fence_after();
-                for (uint32_t kk = 0; kk < kKeys / 16; ++kk) {
-                    const uint64_t ad = smem_desc(sp(b) + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd = smem_desc(sv(b) + kk * 2048, kHalf, 1024);
-                    tc_mma(t_o, ad, bd, id_o, (j | kk) != 0);
-                }
-                tc_commit(o_done);
-                tc_commit(kv_empty + 8 * b);
-                if (j + 2 < p.nb) {
-                    // S_{j+2} reuses S buffer b once the softmax warps have read S_j
-                    if (!wait_a(s_free + 8 * b, ph, abort, p.timeout_ns)) break;
-                    if (!issue_s(j + 2)) break;
-                }
+        // S = Q K^T: M = 128, N = 128 keys, Q and K K-major in shared memory.
+        // O += P V: M = 128, N = 128, P (A) in tensor memory, V M/N-major in shared memory
+        // (d innermost; its two 64-column boxes are 16 KB apart).  Descriptors are formed once;
+        // a tile or K-step offset is added to the start-address field (addresses stay below
+        // 2^18, so the field does not carry).
+        const uint32_t id_s = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+        const uint32_t id_o = id_s | (1u << 16);
+        const uint64_t dq = smem_desc(sq, 16, 1024), dk = smem_desc(sk(0), 16, 1024), dv = smem_desc(sv(0), kHalf, 1024);
+        bool ok = wait_u(q_full, 0);
+        auto issue_s = [&](uint32_t j) {
+            const uint32_t st = j % kKStages, b = j & 1;
+            if (!wait_u(k_full + 8 * st, (j / kKStages) & 1)) return false;
+            tc_fence_after();
+            const uint64_t dks = dk + ((st * kTile) >> 4);
+#pragma unroll
+            for (uint32_t kk = 0; kk < kHead / 16; ++kk) {
+                const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                tc_mma_elect(t_s0 + b * 128, dq + off, dks + off, id_s, kk != 0);
             }
-            // every MMA issued so far has completed once this commit arrives
-            tc_commit(mma_done);
-            volatile int never = 0;
-            mbar_wait_status(mma_done, 0, &never, p.timeout_ns, &g_attn_status);
+            tc_commit_elect(s_full + 8 * b);
+            tc_commit_elect(k_empty + 8 * st);
+            return true;
+        };
+        if (ok) ok = issue_s(0);
+        if (ok && p.nb > 1) ok = issue_s(1);
+        for (uint32_t j = 0; ok && j < p.nb; ++j) {
+            const uint32_t b = j & 1, ph = (j >> 1) & 1;
+            if (!wait_u(p_full, j & 1)) break;
+            if (!wait_u(v_full + 8 * b, ph)) break;
+            tc_fence_after();
+            const uint64_t dvb = dv + ((b * kTile) >> 4);
+#pragma unroll
+            for (uint32_t kk = 0; kk < kKeys / 16; ++kk)  // keys 16kk..16kk+15: P columns 8kk..8kk+7
+                tc_mma_ts_elect(t_o, t_p + kk * 8, dvb + ((kk * 2048) >> 4), id_o, (j | kk) != 0);
+            tc_commit_elect(o_done + 8 * b);
+            tc_commit_elect(v_empty + 8 * b);
+            if (j + 2 < p.nb) {
+                // S_{j+2} reuses S buffer b once the softmax warps have read S_j
+                if (!wait_u(s_free + 8 * b, ph)) break;
+                if (!issue_s(j + 2)) break;
+            }
         }
+        // every MMA issued so far has completed once this commit arrives
+        tc_commit_elect(mma_done);
+        volatile int never = 0;
+        mbar_wait_status(mma_done, 0, &never, p.timeout_ns, &g_attn_status);
+        __syncwarp();
     } else {
         // ------------------------------------------------------------------ softmax, rescale, epilogue
-        const uint32_t qr = warp & 3;                 // TMEM lane quarter
-        const uint32_t row = qr * 32 + lane;          // query row inside the tile
+        // Warps 3-10: TMEM lane quarter warp % 4 (one query row per thread), key half
+        // hf = (warp - 3) / 4 of every block.  The two warps of a quarter exchange their
+        // halves' maxima through shared memory each block (so both use one reference maximum
+        // m per row) and keep partial sums l_hf; O is shared.  m moves only when a block's
+        // maximum exceeds it by more than 8 (log2 units): P stays below 2^8, and O is rescaled
+        // through tensor memory (each warp its 64 columns) only on such blocks.  P_j is stored
+        // to tensor memory once P V_{j-1} has completed (one P buffer), which is also when O
+        // may be rescaled.  The parity waits on o_done stay unambiguous: P V_j cannot complete
+        // before P_j is published.
+        const uint32_t qr = warp & 3;                   // TMEM lane quarter
+        const uint32_t hf = (uint32_t)(warp - 3) >> 2;  // key half
+        const uint32_t row = qr * 32 + lane;            // query row inside the tile
         const uint32_t lanebase = (qr * 32u) << 16;
-        float m = -INFINITY, l = 0.f;
+        float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (uint32_t j = 0; j < p.nb; ++j) {
             const uint32_t b = j & 1, ph = (j >> 1) & 1;
@@ -205,81 +258,95 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                 break;
             }
             tc_fence_after();
-            uint32_t sr[4][32];
+            uint32_t sr[2][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32_nowait(t_s0 + lanebase + b * 128 + c * 32, sr[c]);
+            for (int c = 0; c < 2; ++c) tmem_ld32_nowait(t_s0 + lanebase + b * 128 + hf * 64 + c * 32, sr[c]);
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free + 8 * b);  // S buffer b may be overwritten
-            float mx = -INFINITY;
+            float mc[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t* v = &sr[c >> 1][(c & 1) * 16];
+                float x = max3f(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
 #pragma unroll
-                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
-            const float m_new = fmaxf(m, mx * p.scale_log2);
-            const float corr = fast_exp2(m - m_new);  // 0 on the first block (m = -inf)
-            // P_j as bf16 pairs in registers while P V_{j-1} may still run
-            uint32_t pk[64];
-            float sum = 0.f;
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float p0 = fast_exp2(__uint_as_float(sr[c][2 * i]) * p.scale_log2 - m_new);
-                    const float p1 = fast_exp2(__uint_as_float(sr[c][2 * i + 1]) * p.scale_log2 - m_new);
-                    sum += p0 + p1;
-                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-                    pk[c * 16 + i] = *reinterpret_cast<const uint32_t*>(&h2);
-                }
-            // the P buffer b was last read by P V_{j-2}, and O is rescaled after P V_{j-1}: wait for
-            // P V_{j-1} (they complete in order)
-            if (j > 0 && !wait_a(o_done, (j - 1) & 1, abort, p.timeout_ns)) {
+                for (int i = 3; i < 15; i += 2) x = max3f(x, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                mc[c] = fmaxf(x, __uint_as_float(v[15]));
+            }
+            // the row maximum over both halves
+            xval[(b * 2 + hf) * 128 + row] = max3f(mc[0], mc[1], fmaxf(mc[2], mc[3]));
+            mbar_arrive(xbar + 8 * (b * 4 + qr));
+            if (!wait_a(xbar + 8 * (b * 4 + qr), ph, abort, p.timeout_ns)) {
                 ok = false;
                 break;
             }
-            const uint32_t pbase = sp(b) + row * 128;
+            const float m_blk =
+                fmaxf(xval[(b * 2 + hf) * 128 + row], xval[(b * 2 + (hf ^ 1)) * 128 + row]) * p.scale_log2;
+            const bool need = m_blk > m_used + 8.f;
+            const float m_use = need ? m_blk : m_used;
+            const float corr = fast_exp2(m_used - m_use);  // 1 when m_used stays; 0 on the first block
+            uint32_t pk[32];
+            float sc[2];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 2; ++c) {
+                float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    // keys 32c + 8u .. +7: 64-key chunk c / 2, 16-byte unit (c % 2) * 4 + u, swizzled by row
-                    const uint32_t unit = (uint32_t)((c & 1) * 4 + u);
-                    const uint32_t addr = pbase + (uint32_t)(c >> 1) * kHalf + ((unit ^ (row & 7u)) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[c * 16 + 4 * u]),
-                                 "r"(pk[c * 16 + 4 * u + 1]), "r"(pk[c * 16 + 4 * u + 2]), "r"(pk[c * 16 + 4 * u + 3])
-                                 : "memory");
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c][2 * i]), p.scale_log2, -m_use));
+                    const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c][2 * i + 1]), p.scale_log2, -m_use));
+                    s0 += p0;
+                    s1 += p1;
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+                    pk[c * 16 + i] = *reinterpret_cast<const uint32_t*>(&h2);
                 }
-            l = l * corr + sum;
-            m = m_new;
-            if (j > 0) {
-                // O *= corr (PV_{j-1} has completed: waited above)
-                tc_fence_after();
+                sc[c] = s0 + s1;
+            }
+            if (j >= 1 && !wait_a(o_done + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, abort, p.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            tmem_st32(t_p + lanebase + hf * 32, pk);  // this half's 64 keys
+            l = fmaf(l, corr, sc[0] + sc[1]);
+            m_used = m_use;
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                // O *= corr, this warp's 64 columns (P V_{j-1} has completed; rows whose m_used
+                // stayed multiply by 1)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     uint32_t orr[32];
-                    tmem_ld32_nowait(t_o + lanebase + c * 32, orr);
+                    tmem_ld32_nowait(t_o + lanebase + hf * 64 + c * 32, orr);
                     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
                     for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * corr);
-                    tmem_st32(t_o + lanebase + c * 32, orr);
+                    tmem_st32(t_o + lanebase + hf * 64 + c * 32, orr);
                 }
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             }
-            fence_async_smem();  // P_j visible to the tensor core's (async proxy) reads
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full + 8 * b);
+            if (lane == 0) mbar_arrive(p_full);
         }
-        // epilogue: O / l and L
-        if (ok && wait_a(o_done, (p.nb - 1) & 1, abort, p.timeout_ns)) {
+        // epilogue, once the last P V has completed (they complete in order): the two halves
+        // add their partial sums (exchange slot nb % 2), then warp half hf writes output
+        // columns 64hf..64hf+63 of O / l, and L = (m ln 2) + log(l).
+        const uint32_t jl = p.nb - 1, bx = p.nb & 1;
+        ok = ok && wait_a(o_done + 8 * (jl & 1), (jl >> 1) & 1, abort, p.timeout_ns);
+        if (ok) {
+            xval[(bx * 2 + hf) * 128 + row] = l;
+            mbar_arrive(xbar + 8 * (bx * 4 + qr));
+            ok = wait_a(xbar + 8 * (bx * 4 + qr), (p.nb >> 1) & 1, abort, p.timeout_ns);
+        }
+        if (ok) {
+            const float lt = l + xval[(bx * 2 + (hf ^ 1)) * 128 + row];
+            const float inv = 1.f / lt;
             tc_fence_after();
-            const float inv = 1.f / l;
-            __nv_bfloat16* orow = p.o + ((uint64_t)(q0 + row) * p.h + hd) * kHead;
+            __nv_bfloat16* orow = p.o + ((uint64_t)(q0 + row) * p.h + hd) * kHead + hf * 64;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t orr[32];
-                tmem_ld32_nowait(t_o + lanebase + c * 32, orr);
+                tmem_ld32_nowait(t_o + lanebase + hf * 64 + c * 32, orr);
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
@@ -293,7 +360,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                     *reinterpret_cast<uint4*>(orow + c * 32 + v * 8) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
-            if (p.lse) p.lse[(uint64_t)hd * p.s + q0 + row] = m * 0.6931471805599453f + logf(l);
+            if (p.lse && hf == 0) p.lse[(uint64_t)hd * p.s + q0 + row] = m_used * 0.6931471805599453f + logf(lt);
         }
     }
     tc_fence_before();
@@ -319,13 +386,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn_a() {
     return fn;
 }
 
-// rows x 128 bf16 (row pitch 256 bytes), boxes of 64 columns x 128 rows, 128-byte swizzle
+// rows x 128 bf16 (row pitch 256 bytes) seen as [2 column halves][rows][64 columns]: the box
+// {64 columns, 128 rows, 2 halves} is one 32 KB copy, 128-byte swizzle
 bool encode_rows(const void* base, uint64_t rows, CUtensorMap* map) {
     auto fn = encode_fn_a();
     if (!fn) return false;
-    cuuint64_t dims[5] = {(cuuint64_t)kHead, rows, 1, 1, 1};
-    cuuint64_t strides[4] = {kHead * 2, rows * kHead * 2, rows * kHead * 2, rows * kHead * 2};
-    cuuint32_t box[5] = {64, 128, 1, 1, 1}, es[5] = {1, 1, 1, 1, 1};
+    cuuint64_t dims[5] = {64, rows, 2, 1, 1};
+    cuuint64_t strides[4] = {kHead * 2, 128, rows * kHead * 2, rows * kHead * 2};
+    cuuint32_t box[5] = {64, 128, 2, 1, 1}, es[5] = {1, 1, 1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;

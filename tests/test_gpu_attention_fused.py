@@ -3,8 +3,9 @@ the unfused EinGraph nodes ("EinDecomp ... tensor relational algebra", section 2
 
 O is compared at the BF16 bar (2e-2 of max|ref|) with the oracle's chain evaluated in double
 (S, L = logsumexp_t S, A = exp(S - L), O = A.V); L within 1e-4 of max(|L|, 1).  The cases
-cover one key block, an odd number of key blocks with s != t, several heads, and the whole
-attention EinGraph with the fused node against the unfused one.
+cover one key block, an odd number of key blocks with s != t, several heads, key blocks
+whose maxima grow (the kernel's reference maximum moves) or fall, and the whole attention
+EinGraph with the fused node against the unfused one.
 """
 import numpy as np
 import pytest
@@ -18,13 +19,24 @@ from gpu_helpers import as_f64, check_bf16_bar, from_dev
 pytestmark = pytest.mark.gpu
 
 
-def _run(lib, s, t, h, seed):
+def _scale_key_blocks(k, factors):
+    """k (bf16 bits [h][t][d]) with key block j (128 keys) multiplied by factors[j], a power of
+    two, so the product stays exact in bf16."""
+    f = datagen.bf16_bits_to_f32(k).copy()
+    for j, g in enumerate(factors):
+        f[:, 128 * j:128 * (j + 1)] *= np.float32(g)
+    return (f.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def _run(lib, s, t, h, seed, key_scale=None):
     import torch
 
     d = 128
     q = datagen.normal_bf16((h, s, d), seed, 0)
     k = datagen.normal_bf16((h, t, d), seed, 1)
     v = datagen.normal_bf16((h, t, d), seed, 2)
+    if key_scale is not None:
+        k = _scale_key_blocks(k, key_scale)
     dev = [torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda().reshape(-1) for a in (q, k, v)]
     o = torch.empty(s * h * d, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(h * s, dtype=torch.float32, device="cuda")
@@ -42,6 +54,15 @@ def _run(lib, s, t, h, seed):
 @pytest.mark.parametrize("s,t,h", [(128, 128, 1), (256, 384, 3), (384, 1024, 2)])
 def test_fused_attention_against_oracle(lib, cuda, s, t, h):
     o, lse, O, L = _run(lib, s, t, h, 40 + s + t + h)
+    check_bf16_bar(o, O)
+    assert np.all(np.abs(lse - L) <= 1e-4 * np.maximum(np.abs(L), 1.0))
+
+
+@pytest.mark.parametrize("factors", [[1, 2, 4, 8, 8, 16, 1, 16], [16, 8, 4, 2, 1, 1, 1, 1]])
+def test_fused_attention_growing_and_falling_block_maxima(lib, cuda, factors):
+    """Key blocks scaled so the row maxima jump by more than 2^8 between blocks (the reference
+    maximum moves and O is rescaled, for some rows of a warp but not others) or only fall."""
+    o, lse, O, L = _run(lib, 256, 1024, 2, 77, key_scale=factors)
     check_bf16_bar(o, O)
     assert np.all(np.abs(lse - L) <= 1e-4 * np.maximum(np.abs(L), 1.0))
 
