@@ -165,20 +165,24 @@ __device__ __forceinline__ void tma_load_5d_pair(uint32_t dst, const CUtensorMap
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4]), "r"(bar_cluster)
         : "memory");
 }
-__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t acc) {
+// tcgen05.mma / commit with cta_group::2 (M = 256 across the pair), issued by the elected lane
+// of a converged warp (see tc_mma_elect); the commit arrives once on the barrier at this shared
+// offset in every CTA of ctamask when the MMAs issued so far have completed
+__device__ __forceinline__ void tc_mma_pair_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                  uint32_t acc) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
         : "memory");
 }
-// arrive once on the barrier at this shared offset in every CTA of ctamask, when the MMAs
-// issued so far have completed
-__device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t ctamask) {
+__device__ __forceinline__ void tc_commit_pair_elect(uint32_t bar, uint16_t ctamask) {
     asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(bar),
         "h"(ctamask)
         : "memory");
 }
@@ -415,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort = reinterpret_cast<volatile int*>(gbase + (done_bar + 12 - base));
     uint8_t* epi = gbase + (epi_s - base);
 
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x / 32), 0), lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < p.stages; ++s) {
             mbar_init(full0 + 8 * s, 1);
@@ -438,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t tmem_base = __shfl_sync(0xffffffffu, *tmem_slot, 0);  // warp-uniform
 
     if (warp < kProducers) {
         // ---------------------------------------------------------------- TMA producers
@@ -446,49 +450,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             producer_steps<false>(&map_a, &map_b, p, (uint32_t)warp, blockIdx.x, gridDim.x, 0u, base, full0, empty0, abort);
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-            bool ok = true;
-            const uint32_t a_lbo = p.a.mn_major ? 8192u : 16u, b_lbo = p.b.mn_major ? 8192u : 16u;
-            const uint32_t a_kstep = p.a.mn_major ? 2048u : 32u, b_kstep = p.b.mn_major ? 2048u : 32u;
-            for (uint32_t t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
-                if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort, p.timeout_ns)) {
+        // The whole warp runs the loop (waits by every lane, results shuffled from lane 0 so
+        // that control flow and operands stay warp-uniform); the elected lane issues.
+        // Descriptors are formed once; stage and K-step offsets go into the start-address
+        // field (shared addresses stay below 2^18, so the field does not carry).
+        auto wait_u = [&](uint32_t b_, uint32_t parity) {
+            return __shfl_sync(0xffffffffu, (int)mbar_wait(b_, parity, abort, p.timeout_ns), 0) != 0;
+        };
+        uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+        bool ok = true;
+        const uint32_t a_lbo = p.a.mn_major ? 8192u : 16u, b_lbo = p.b.mn_major ? 8192u : 16u;
+        const uint32_t a_kstep = (p.a.mn_major ? 2048u : 32u) >> 4, b_kstep = (p.b.mn_major ? 2048u : 32u) >> 4;
+        const uint64_t da0 = smem_desc(base, a_lbo, 1024), db0 = smem_desc(base + p.a_bytes, b_lbo, 1024);
+        for (uint32_t t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+            if (!wait_u(tempty0 + 8 * acc, acc_phase ^ 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + acc * p.block_n;
+            for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+                if (!wait_u(full0 + 8 * stage, phase)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * p.block_n;
-                for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
-                    if (!mbar_wait(full0 + 8 * stage, phase, abort, p.timeout_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t sa = base + stage * stage_bytes, sb = sa + p.a_bytes;
+                const uint32_t so = (stage * stage_bytes) >> 4;
 #pragma unroll
-                    for (uint32_t k = 0; k < kBlockK / 16; ++k) {
-                        const uint64_t ad = smem_desc(sa + k * a_kstep, a_lbo, 1024);
-                        const uint64_t bd = smem_desc(sb + k * b_kstep, b_lbo, 1024);
-                        tc_mma(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
-                    }
-                    tc_commit(empty0 + 8 * stage);  // frees the stage once these MMAs have read it
-                    if (++stage == p.stages) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
-                }
-                if (!ok) break;
-                tc_commit(tfull0 + 8 * acc);  // accumulator ready for the epilogue
-                if (++acc == 2) {
-                    acc = 0;
-                    acc_phase ^= 1;
+                for (uint32_t k = 0; k < kBlockK / 16; ++k)
+                    tc_mma_elect(d_tmem, da0 + so + k * a_kstep, db0 + so + k * b_kstep, p.idesc, (kb | k) != 0);
+                tc_commit_elect(empty0 + 8 * stage);  // frees the stage once these MMAs have read it
+                if (++stage == p.stages) {
+                    stage = 0;
+                    phase ^= 1;
                 }
             }
-            // every MMA issued so far has completed once this commit arrives
-            tc_commit(done_bar);
-            volatile int never = 0;
-            mbar_wait(done_bar, 0, &never, p.timeout_ns);
+            if (!ok) break;
+            tc_commit_elect(tfull0 + 8 * acc);  // accumulator ready for the epilogue
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
         }
+        // every MMA issued so far has completed once this commit arrives
+        tc_commit_elect(done_bar);
+        volatile int never = 0;
+        mbar_wait(done_bar, 0, &never, p.timeout_ns);
+        __syncwarp();
     } else {
         // ---------------------------------------------------------------- epilogue (warps 5-12)
         const uint32_t q = warp & 3;  // TMEM lane quarter this warp may access
@@ -544,7 +552,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     volatile int* abort = reinterpret_cast<volatile int*>(gbase + (done_bar + 12 - base));
     uint8_t* epi = gbase + (epi_s - base);
 
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x / 32), 0), lane = threadIdx.x % 32;
     const uint32_t rank = cluster_rank();
     const bool leader = rank == 0;
     const uint32_t pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
@@ -571,7 +579,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncthreads();
     cluster_sync();  // both CTAs' barriers exist before anyone signals across the pair
     tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t tmem_base = __shfl_sync(0xffffffffu, *tmem_slot, 0);  // warp-uniform
 
     if (warp < kProducers) {
         // ---------------------------------------------------------------- TMA producers (both CTAs)
@@ -579,47 +587,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             producer_steps<true>(&map_a, &map_b, p, (uint32_t)warp, pair, n_pairs, rank, base, full0, empty0, abort);
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer (even CTA)
-        if (lane == 0 && leader) {
+        // whole warp, uniform waits, elected issue, descriptors formed once (as in tc_gemm)
+        if (leader) {
+            auto wait_u = [&](uint32_t b_, uint32_t parity) {
+                return __shfl_sync(0xffffffffu, (int)mbar_wait_cl(b_, parity, abort, p.timeout_ns), 0) != 0;
+            };
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             const uint32_t a_lbo = p.a.mn_major ? 8192u : 16u, b_lbo = p.b.mn_major ? 8192u : 16u;
-            const uint32_t a_kstep = p.a.mn_major ? 2048u : 32u, b_kstep = p.b.mn_major ? 2048u : 32u;
+            const uint32_t a_kstep = (p.a.mn_major ? 2048u : 32u) >> 4, b_kstep = (p.b.mn_major ? 2048u : 32u) >> 4;
+            const uint64_t da0 = smem_desc(base, a_lbo, 1024), db0 = smem_desc(base + p.a_bytes, b_lbo, 1024);
             for (uint32_t t = pair; t < p.n_tiles && ok; t += n_pairs) {
-                if (!mbar_wait_cl(tempty0 + 8 * acc, acc_phase ^ 1, abort, p.timeout_ns)) {
+                if (!wait_u(tempty0 + 8 * acc, acc_phase ^ 1)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * p.block_n;
                 for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
-                    if (!mbar_wait_cl(full0 + 8 * stage, phase, abort, p.timeout_ns)) {
+                    if (!wait_u(full0 + 8 * stage, phase)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = base + stage * stage_bytes, sb = sa + p.a_bytes;
+                    const uint32_t so = (stage * stage_bytes) >> 4;
 #pragma unroll
-                    for (uint32_t k = 0; k < kBlockK / 16; ++k) {
-                        const uint64_t ad = smem_desc(sa + k * a_kstep, a_lbo, 1024);
-                        const uint64_t bd = smem_desc(sb + k * b_kstep, b_lbo, 1024);
-                        tc_mma_pair(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
-                    }
-                    tc_commit_pair(empty0 + 8 * stage, 3);  // frees this stage in both CTAs
+                    for (uint32_t k = 0; k < kBlockK / 16; ++k)
+                        tc_mma_pair_elect(d_tmem, da0 + so + k * a_kstep, db0 + so + k * b_kstep, p.idesc,
+                                          (kb | k) != 0);
+                    tc_commit_pair_elect(empty0 + 8 * stage, 3);  // frees this stage in both CTAs
                     if (++stage == p.stages) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
                 if (!ok) break;
-                tc_commit_pair(tfull0 + 8 * acc, 3);  // accumulator ready in both CTAs
+                tc_commit_pair_elect(tfull0 + 8 * acc, 3);  // accumulator ready in both CTAs
                 if (++acc == 2) {
                     acc = 0;
                     acc_phase ^= 1;
                 }
             }
-            tc_commit_pair(done_bar, 1);  // all MMAs issued so far have completed
+            tc_commit_pair_elect(done_bar, 1);  // all MMAs issued so far have completed
             volatile int never = 0;
             mbar_wait_cl(done_bar, 0, &never, p.timeout_ns);
+            __syncwarp();
         }
     } else {
         // ---------------------------------------------------------------- epilogue (warps 5-12, both CTAs)
