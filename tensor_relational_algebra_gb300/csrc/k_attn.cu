@@ -196,10 +196,9 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         const uint32_t id_o = id_s | (1u << 16);
         const uint64_t dq = smem_desc(sq, 16, 1024), dk = smem_desc(sk(0), 16, 1024), dv = smem_desc(sv(0), kHalf, 1024);
         bool ok = wait_u(q_full, 0);
+        // S_j = Q K_j^T into S buffer j % 2 (its K slot must have landed)
         auto issue_s = [&](uint32_t j) {
             const uint32_t st = j % kKStages, b = j & 1;
-            if (!wait_u(k_full + 8 * st, (j / kKStages) & 1)) return false;
-            tc_fence_after();
             const uint64_t dks = dk + ((st * kTile) >> 4);
 #pragma unroll
             for (uint32_t kk = 0; kk < kHead / 16; ++kk) {
@@ -208,14 +207,24 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             }
             tc_commit_elect(s_full + 8 * b);
             tc_commit_elect(k_empty + 8 * st);
-            return true;
         };
-        if (ok) ok = issue_s(0);
-        if (ok && p.nb > 1) ok = issue_s(1);
+        for (uint32_t j = 0; ok && j < 2 && j < p.nb; ++j) {
+            ok = wait_u(k_full + 8 * (j % kKStages), (j / kKStages) & 1);
+            if (ok) {
+                tc_fence_after();
+                issue_s(j);
+            }
+        }
+        // Per block j every wait comes first (P_j published, V_j landed, and for S_{j+2} its S
+        // buffer read and K slot landed), then P V_j and S_{j+2} go out as one run of MMAs:
+        // a wait placed after a run of MMAs stalls until they have drained.
         for (uint32_t j = 0; ok && j < p.nb; ++j) {
             const uint32_t b = j & 1, ph = (j >> 1) & 1;
-            if (!wait_u(p_full, j & 1)) break;
-            if (!wait_u(v_full + 8 * b, ph)) break;
+            const bool more = j + 2 < p.nb;
+            if (!wait_u(p_full, j & 1) || !wait_u(v_full + 8 * b, ph)) break;
+            if (more && (!wait_u(s_free + 8 * b, ph) ||
+                         !wait_u(k_full + 8 * ((j + 2) % kKStages), ((j + 2) / kKStages) & 1)))
+                break;
             tc_fence_after();
             const uint64_t dvb = dv + ((b * kTile) >> 4);
 #pragma unroll
@@ -223,11 +232,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                 tc_mma_ts_elect(t_o, t_p + kk * 8, dvb + ((kk * 2048) >> 4), id_o, (j | kk) != 0);
             tc_commit_elect(o_done + 8 * b);
             tc_commit_elect(v_empty + 8 * b);
-            if (j + 2 < p.nb) {
-                // S_{j+2} reuses S buffer b once the softmax warps have read S_j
-                if (!wait_u(s_free + 8 * b, ph)) break;
-                if (!issue_s(j + 2)) break;
-            }
+            if (more) issue_s(j + 2);  // into S buffer b, which the softmax warps have read
         }
         // every MMA issued so far has completed once this commit arrives
         tc_commit_elect(mma_done);
