@@ -11,7 +11,8 @@ relation), then both join + aggregate EinSums.
 Other workloads (``--workload``): c1 (64^3 fp32 matmul under three d), c3 (4-D
 BF16 contraction + repartition of its output), c4 (multi-head-attention
 EinGraph; c4f the same with the attention chain fused into one kernel), c5
-(16384^3 BF16 matmul, ``--d``), c5b (8192^3 logsumexp).
+(16384^3 BF16 matmul, ``--d``), c5b (8192^3 logsumexp); c2s and c5bs run the squared
+distance of the pair and the 8192^3 logsumexp with split=bf16x3 (tensor cores).
 
 ``--impl reference`` times the CPU oracle on a bounded sample of the same
 workload (the reference arm).  Under torchrun (N > 1) every rank runs an
@@ -146,7 +147,9 @@ class Step:
 def kernel_launches(plan) -> int:
     """Kernels one ein_execute of this plan launches."""
     n = {"semiring_f32": 1, "tc_bf16": 1, "tc_bf16_pair": 1, "row_reduce": 1, "elementwise": 1, "lse_factored": 4,
-         "literal": 2}[plan.kernel]
+         "literal": 2, "tc_split3": 5}[plan.kernel]
+    if plan.kernel == "tc_split3" and ":add:lse" in plan.spec:
+        n += 1  # the underflow fix-up pass
     spec = plan.spec
     if plan.kernel == "semiring_f32" and ":sqdiff:sum" in spec and "sqdiff=direct" not in spec and "in=bf16" not in spec:
         n += 2  # row / column norms of the squared-distance expansion
@@ -493,8 +496,70 @@ class C5bWorkload(_PointsWorkload):
         return f"{n} of 8192^2 outputs"
 
 
-WORKLOADS = {"pair": PairWorkload, "c1": C1Workload, "c1l": C1LiteralWorkload, "c3": C3Workload, "c4": C4Workload, "c4f": C4fWorkload, "c5": C5Workload,
-             "c5b": C5bWorkload}
+class C2sWorkload(PairWorkload):
+    """Squared distance only, X 8192x256, Y 256x8192 fp32, d = [8,1,1,8], with split=bf16x3: the
+    expansion's x.y on BF16 tensor cores as hi.hi + hi.lo + lo.hi (K' = 768)."""
+
+    name = "squared distance (x-y)^2/sum, X 8192x256, Y 256x8192 fp32, d=[8,1,1,8], split=bf16x3 on tensor cores"
+
+    def setup(self, tra, torch, inputs):
+        X, Y = inputs
+        dev = torch.device("cuda")
+        self.Xd = torch.from_numpy(X).to(dev).reshape(-1)
+        self.Yd = torch.from_numpy(Y).to(dev).reshape(-1)
+        self.Yr = torch.empty_like(self.Yd)
+        self.p_sq = tra.Plan("ij,jk->ik:sqdiff:sum:split=bf16x3", [self.M, self.K, self.N], self.d)
+        self.ws = torch.empty(self.p_sq.workspace_bytes, dtype=torch.uint8, device=dev)
+        self.Zs = torch.empty(self.M * self.N, dtype=torch.float32, device=dev)
+        # work of the split step: the GEMM's BF16 flops over K' = 3K (the EinSum's own 2MKN is the
+        # headline value)
+        self.steps = [
+            Step("repartition Y [1,1]->[1,8]", lambda: tra.repartition(self.Yd, self.Yr, [self.K, self.N], [1, 1], [1, 8]),
+                 2 * self.K * self.N * 4, "bytes", "hbm", 1),
+            Step("join+agg (x-y)^2/sum, split bf16x3 (tcgen05)", lambda: self.p_sq.execute(self.Xd, self.Yr, self.Zs, self.ws),
+                 3 * 2 * self.M * self.K * self.N, "flop", "tensor", kernel_launches(self.p_sq)),
+        ]
+        self.inputs_dev = [self.Xd, self.Yd]
+        self.outputs_dev = [self.Zs]
+        self.output_steps = [1]
+
+    def ops_per_step(self):
+        return 2 * self.M * self.K * self.N
+
+    def oracle_sample(self, inputs, r0, rows):
+        import oracle
+
+        X, Y = inputs
+        pts = (np.arange(rows, dtype=np.int64)[:, None] % self.M + r0) % self.M * self.N + np.arange(self.N)[None, :]
+        oracle.einsum_points("ij,jk->ik", X.astype(np.float64), Y.astype(np.float64), pts.reshape(-1), op="sqdiff",
+                             agg="sum")
+        return 2 * pts.size * self.K
+
+    def sample_text(self, rows):
+        return f"{rows} of 8192 output rows (all 8192 columns)"
+
+
+class C5bsWorkload(C5bWorkload):
+    name_fmt = "logsumexp-aggregated Z[i,k]=lse_j(X[i,j]+Y[j,k]) 8192^3 fp32, d={}, split=bf16x3 on tensor cores"
+
+    def setup(self, tra, torch, inputs):
+        n = 8192
+        X, Y = inputs
+        self.Xd, self.Yd = torch.from_numpy(X).cuda().reshape(-1), torch.from_numpy(Y).cuda().reshape(-1)
+        self.Xr, self.Yr = device_relation(tra, torch, self.Xd, [n, n], self.d[:2]), device_relation(
+            tra, torch, self.Yd, [n, n], self.d[2:])
+        self.p = tra.Plan("ij,jk->ik:add:lse:split=bf16x3", [n, n, n], self.d)
+        self.ws = torch.empty(self.p.workspace_bytes, dtype=torch.uint8, device="cuda")
+        self.Z = torch.empty(n * n, dtype=torch.float32, device="cuda")
+        self.steps = [Step(f"join+agg (x+y)/logsumexp d={self.d}, split bf16x3 (tcgen05)",
+                           lambda: self.p.execute(self.Xr, self.Yr, self.Z, self.ws), 3 * 2 * n ** 3, "flop", "tensor",
+                           kernel_launches(self.p))]
+        self.inputs_dev = [self.Xr, self.Yr]
+        self.outputs_dev = [self.Z]
+
+
+WORKLOADS = {"pair": PairWorkload, "c1": C1Workload, "c1l": C1LiteralWorkload, "c2s": C2sWorkload, "c3": C3Workload,
+             "c4": C4Workload, "c4f": C4fWorkload, "c5": C5Workload, "c5b": C5bWorkload, "c5bs": C5bsWorkload}
 
 
 # ----------------------------------------------------------------------------- measurement

@@ -90,7 +90,8 @@ enum {
     TRA_KERNEL_ELEMENTWISE = 4,   /* join with AGG = none (broadcast operands allowed) */
     TRA_KERNEL_LSE_FACTORED = 5,  /* logsumexp of a sum: max-shifted exp, then sum-of-products */
     TRA_KERNEL_LITERAL = 6,       /* one partial per join tuple, then ordered combine */
-    TRA_KERNEL_TC_BF16_PAIR = 7   /* as TC_BF16, one 256 x 256 tile per cluster of two CTAs */
+    TRA_KERNEL_TC_BF16_PAIR = 7,  /* as TC_BF16, one 256 x 256 tile per cluster of two CTAs */
+    TRA_KERNEL_TC_SPLIT3 = 8      /* split=bf16x3: squared distance / logsumexp on tensor cores */
 };
 
 /* ein_plan -- build the TRA plan of one EinSum under partition vector d
@@ -109,7 +110,13 @@ enum {
  *         when the output rows are a multiple of 256 and the columns of 128),
  *         tc_n=256|128 (width of the pair tile; by default 256 where the columns
  *         allow, else 128), tc_store=tma|lsu (tensor-core epilogue: TMA stores
- *         through an output tensor map, the default where one fits, or warp stores).
+ *         through an output tensor map, the default where one fits, or warp stores),
+ *         split=bf16x3|none (fp32 "sqdiff:sum" and "add:lse" only: the squared-distance
+ *         expansion |x|^2 + |y|^2 - 2 x.y, or the factored logsumexp
+ *         mx + my + log sum e^(x-mx) e^(y-my), with the sum of products on BF16 tensor cores,
+ *         each fp32 operand split as hi + lo bf16 and the product taken as
+ *         hi.hi + hi.lo + lo.hi; per product the relative error is at most 3 * 2^-16.
+ *         Default none: these semirings run on CUDA cores).
  * bounds: B_l for every distinct label in first-appearance order (X then Y);
  *         n_bounds must equal the number of distinct labels.
  * d:      partition counts per operand index position, X's then Y's (n_d =

@@ -284,6 +284,59 @@ int execute_plan(const Plan& p, const void* x, const void* y, void* z, void* ws,
         case TRA_KERNEL_TC_BF16:
         case TRA_KERNEL_TC_BF16_PAIR:
             return tc_execute(p, x, y, z, s);
+        case TRA_KERNEL_TC_SPLIT3: {
+            // norms (squared distance) or row / column maxima (logsumexp) of the fp32 operands,
+            // the hi / lo split into the GEMM's operands, the GEMM with the rank-one epilogue
+            // writing Z in its relation layout, and for logsumexp the underflow fix-up
+            SemiringParams sp = semiring_params(p, x, y, z);
+            const bool lse = p.op == kAdd;
+            const uint64_t nb = sp.nb, M = sp.M, N = sp.N, K = sp.K;
+            const uint64_t Mp = split3_pad(M, 128), Np = split3_pad(N, 64), K3p = split3_pad(3 * K, 64);
+            char* w = reinterpret_cast<char*>(ws);
+            __nv_bfloat16* a3 = reinterpret_cast<__nv_bfloat16*>(w);
+            w += align256(nb * Mp * K3p * 2);
+            __nv_bfloat16* b3 = reinterpret_cast<__nv_bfloat16*>(w);
+            w += align256(nb * Np * K3p * 2);
+            float* rt = reinterpret_cast<float*>(w);
+            w += align256(nb * M * 4);
+            float* ct = reinterpret_cast<float*>(w);
+            LsePrepParams lp;
+            memset(&lp, 0, sizeof(lp));
+            lp.mode = lse ? 0 : 1;
+            lp.dst = nullptr;
+            lp.nb = sp.nb;
+            lp.K = sp.K;
+            lp.src = x, lp.rmax = rt, lp.b = sp.xb, lp.r = sp.xm, lp.k = sp.xk, lp.R = sp.M;
+            if ((e = launch_lse_prep(lp, s)) != cudaSuccess) return cuda_fail(e, "row terms of X");
+            lp.src = y, lp.rmax = ct, lp.b = sp.yb, lp.r = sp.yn, lp.k = sp.yk, lp.R = sp.N;
+            if ((e = launch_lse_prep(lp, s)) != cudaSuccess) return cuda_fail(e, "column terms of Y");
+            Split3Params s3;
+            memset(&s3, 0, sizeof(s3));
+            s3.src = reinterpret_cast<const float*>(x), s3.dst = a3, s3.shift = lse ? rt : nullptr;
+            s3.b = sp.xb, s3.r = sp.xm, s3.k = sp.xk, s3.nb = sp.nb, s3.R = sp.M, s3.K = sp.K, s3.is_y = 0;
+            s3.Rp = (uint32_t)Mp, s3.K3p = (uint32_t)K3p;
+            if ((e = launch_split3(s3, s)) != cudaSuccess) return cuda_fail(e, "split of X");
+            s3.src = reinterpret_cast<const float*>(y), s3.dst = b3, s3.shift = lse ? ct : nullptr;
+            s3.b = sp.yb, s3.r = sp.yn, s3.k = sp.yk, s3.R = sp.N, s3.is_y = 1, s3.Rp = (uint32_t)Np;
+            if ((e = launch_split3(s3, s)) != cudaSuccess) return cuda_fail(e, "split of Y");
+            TcExtra ex;
+            ex.epi = lse ? 2 : 1;
+            ex.row_term = rt;
+            ex.col_term = ct;
+            ex.alpha = (float)p.alpha;
+            ex.z_override = true;
+            ex.zb = sp.zb;
+            ex.zm = sp.zm;
+            ex.zn = sp.zn;
+            ex.M = sp.M;
+            ex.N = sp.N;
+            const int rc = tc_execute(*p.inner, a3, b3, z, s, &ex);
+            if (rc != TRA_OK || !lse) return rc;
+            sp.x_raw = x;
+            sp.y_raw = y;
+            e = launch_lse_fixup(sp, s);
+            break;
+        }
         case TRA_KERNEL_LITERAL:
             return execute_literal(p, x, y, z, ws, s);
         default:

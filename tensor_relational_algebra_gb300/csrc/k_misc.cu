@@ -406,6 +406,61 @@ cudaError_t launch_elementwise(const ElementwiseParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+namespace {
+
+// One CTA per 32 rows x 32 contracted indices of one batch: the tile is read along the index
+// that is contiguous in the operand (k when k_fast), staged in shared memory, and written
+// along k, so both sides coalesce whatever the operand's relation layout.
+__global__ void __launch_bounds__(256) split3_kernel(const __grid_constant__ Split3Params p) {
+    __shared__ float t[32][33];
+    const uint32_t tiles_k = (p.K + 31) / 32, tiles_r = (p.R + 31) / 32;
+    const uint32_t kt = blockIdx.x % tiles_k, rest = blockIdx.x / tiles_k;
+    const uint32_t rt = rest % tiles_r, b = rest / tiles_r;
+    const uint32_t r0 = rt * 32, k0 = kt * 32;
+    const uint32_t tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int64_t bo = role_offset(p.b, b);
+#pragma unroll
+    for (uint32_t i = 0; i < 4; ++i) {
+        const uint32_t rl = p.k_fast ? ty + 8 * i : tx, kl = p.k_fast ? tx : ty + 8 * i;
+        const uint32_t r = r0 + rl, k = k0 + kl;
+        if (r < p.R && k < p.K) {
+            float v = p.src[bo + role_offset(p.r, r) + role_offset(p.k, k)];
+            if (p.shift) v = expf(v - p.shift[(uint64_t)b * p.R + r]);
+            t[rl][kl] = v;
+        }
+    }
+    __syncthreads();
+    const uint64_t K = p.K;
+#pragma unroll
+    for (uint32_t i = 0; i < 4; ++i) {
+        const uint32_t r = r0 + ty + 8 * i, k = k0 + tx;
+        if (r >= p.R) continue;
+        __nv_bfloat16* out = p.dst + ((uint64_t)b * p.Rp + r) * p.K3p;
+        if (k < p.K) {
+            const float v = t[ty + 8 * i][tx];
+            const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+            out[k] = hi;
+            out[K + k] = p.is_y ? lo : hi;
+            out[2 * K + k] = p.is_y ? hi : lo;
+        }
+        if (kt == tiles_k - 1)  // the row's zero padding
+            for (uint64_t j = 3 * K + tx; j < p.K3p; j += 32) out[j] = __float2bfloat16_rn(0.f);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_split3(const Split3Params& pin, cudaStream_t s) {
+    Split3Params p = pin;
+    p.k_fast = p.k.n > 0 && p.k.t[0].div == 1 && p.k.t[0].loc_stride == 1;
+    const uint64_t ctas = (uint64_t)p.nb * ((p.R + 31) / 32) * ((p.K + 31) / 32);
+    if (ctas == 0) return cudaSuccess;
+    if (ctas > 0x7fffffffull) return cudaErrorInvalidValue;
+    split3_kernel<<<(unsigned)ctas, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
     const uint64_t total = p.n_groups * p.z_sub;
     if (total == 0) return cudaSuccess;

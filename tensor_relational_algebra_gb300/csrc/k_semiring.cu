@@ -616,7 +616,7 @@ __global__ void lse_prep_kernel(const __grid_constant__ LsePrepParams p, int row
             m = p.mode == 0 ? fmaxf(m, w) : m + w;
         }
         if (lane == 0) p.rmax[warp] = m;
-        if (p.mode == 0)
+        if (p.mode == 0 && p.dst)
             for (uint32_t k = lane; k < p.K; k += 32) {
                 int64_t off = base + prep_koff(p, k);
                 p.dst[off] = expf(ld1<TIn>(p.src, off) - m);
@@ -646,7 +646,7 @@ __global__ void lse_prep_kernel(const __grid_constant__ LsePrepParams p, int row
         }
         __syncthreads();
         m = red[0][lane];
-        if (p.mode == 0 && valid)
+        if (p.mode == 0 && p.dst && valid)
             for (uint32_t k = w; k < p.K; k += 8) {
                 const int64_t off = base + prep_koff(p, k);
                 p.dst[off] = expf(ld1<TIn>(p.src, off) - m);
@@ -710,6 +710,14 @@ cudaError_t launch_semiring_simple(const SemiringParams& p, cudaStream_t s) {
     const unsigned blocks = (unsigned)((total + 255) / 256 < 65536 ? (total + 255) / 256 : 65536);
     if (p.in_bf16) semiring_simple<__nv_bfloat16><<<blocks, 256, 0, s>>>(p);
     else semiring_simple<float><<<blocks, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_lse_fixup(const SemiringParams& p, cudaStream_t s) {
+    if (p.nb == 0 || p.M == 0 || p.N == 0) return cudaSuccess;
+    const uint64_t grid64 = (uint64_t)p.nb * ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
+    if (grid64 > 0x7fffffffull) return cudaErrorInvalidValue;
+    lse_fixup_kernel<<<(unsigned)grid64, NT, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -75,6 +75,12 @@ struct TcParams {
     float alpha;
     int32_t out_bf16;
     uint64_t timeout_ns;
+    // epilogue terms (TcExtra): 0 plain; 1 max(r[m] + c[n] - 2 acc, 0); 2 r[m] + c[n] + log(acc),
+    // NaN where acc <= 1e-30 (the caller's fix-up recomputes those); r, c indexed b * M + m, b * N + n
+    uint32_t epi;
+    const float* row_term;
+    const float* col_term;
+    uint32_t zM, zN;  // output rows / columns stored (M, N unless the operands are padded)
 };
 
 // ------------------------------------------------------------------ PTX wrappers (tc_ptx.h)
@@ -285,7 +291,7 @@ __device__ __forceinline__ void z_coords(const TcOpDev& o, uint32_t b, uint32_t 
 // whole row segments (4 rows x 128 bytes fp32, or 8 rows x 64 bytes bf16).
 __device__ __forceinline__ void store_block(const TcParams& p, float4* stg, int64_t zr, int64_t zc, int lane,
                                             const uint32_t (&r)[32], uint32_t n) {
-    if (n >= p.N) return;  // uniform over the warp
+    if (n >= p.zN) return;  // uniform over the warp
 #pragma unroll
     for (int g = 0; g < 8; ++g)
         stg[lane * 8 + (g ^ (lane & 7))] =
@@ -325,12 +331,31 @@ __device__ __forceinline__ void store_block(const TcParams& p, float4* stg, int6
 // alternate pairs.  With an output tensor map the blocks leave by TMA stores; otherwise by
 // warp stores, with row and column offsets computed once per tile, one per lane, and passed
 // by shuffle.
+// Rank-one epilogue terms of the rewritten non-sum semirings, applied to one 32-column block
+// (this lane's row m, columns n .. n + 31) before the stores scale by alpha.
+template <int EPI>
+__device__ __forceinline__ void apply_terms(const TcParams& p, uint32_t (&r)[32], float rt, uint32_t b, uint32_t n) {
+    if (EPI == 0) return;
+    const float* ct = p.col_term + (uint64_t)b * p.zN;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const float c = __ldg(ct + min(n + (uint32_t)i, p.zN - 1));
+        const float a = __uint_as_float(r[i]);
+        float v;
+        if (EPI == 1) v = fmaxf(rt + c - 2.f * a, 0.f);
+        else v = a > 1e-30f ? rt + c + logf(a) : __int_as_float(0x7fc00000);
+        r[i] = __float_as_uint(v);
+    }
+}
+
+template <int EPI>
 __device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorMap* map_z, uint8_t* epi,
                                               uint32_t tmem_acc, uint32_t q, uint32_t half, int lane, uint32_t b,
                                               uint32_t m, uint32_t n0) {
     float4* stg = reinterpret_cast<float4*>(epi + (q + 4 * half) * kEpiTile);
     const uint32_t nblk = p.block_n / 32;  // block_n is a multiple of 64
     const uint32_t taddr = tmem_acc + ((q * 32u) << 16);
+    const float rt = EPI ? __ldg(p.row_term + (uint64_t)b * p.zM + min(m, p.zM - 1)) : 0.f;
     if (p.z_tma) {
         // TMA stores: the warp writes its 32 rows into its (1024-aligned) staging tile in the
         // 128-byte swizzle the output map uses, then one lane stores the box.  fp32: one box
@@ -358,6 +383,8 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorM
             tmem_ld32_nowait(taddr + c * 32u, ra);
             tmem_ld32_nowait(taddr + c * 32u + 32u, rb);
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            apply_terms<EPI>(p, ra, rt, b, n0 + c * 32u);
+            apply_terms<EPI>(p, rb, rt, b, n0 + c * 32u + 32u);
             if (!p.out_bf16) {
 #pragma unroll
                 for (int blk = 0; blk < 2; ++blk) {
@@ -389,13 +416,15 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorM
         }
         return;
     }
-    const int64_t zr = m < p.M ? role_offset(p.zb, b) + role_offset(p.zm, m) : (int64_t)-1;
-    const int64_t zc_lane = (uint32_t)lane < nblk && n0 + 32u * lane < p.N ? role_offset(p.zn, n0 + 32u * lane) : 0;
+    const int64_t zr = m < p.zM ? role_offset(p.zb, b) + role_offset(p.zm, m) : (int64_t)-1;
+    const int64_t zc_lane = (uint32_t)lane < nblk && n0 + 32u * lane < p.zN ? role_offset(p.zn, n0 + 32u * lane) : 0;
     for (uint32_t c = 2 * half; c < nblk; c += 4) {
         uint32_t ra[32], rb[32];
         tmem_ld32_nowait(taddr + c * 32u, ra);
         tmem_ld32_nowait(taddr + c * 32u + 32u, rb);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        apply_terms<EPI>(p, ra, rt, b, n0 + c * 32u);
+        apply_terms<EPI>(p, rb, rt, b, n0 + c * 32u + 32u);
         store_block(p, stg, zr, __shfl_sync(0xffffffffu, zc_lane, c), lane, ra, n0 + c * 32u);
         store_block(p, stg, zr, __shfl_sync(0xffffffffu, zc_lane, c + 1), lane, rb, n0 + c * 32u + 32u);
     }
@@ -507,8 +536,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tile_of(p, t, b, mt, nt);
             if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort, p.timeout_ns)) break;
             tc_fence_after();
-            epilogue_tile(p, &map_z, epi, tmem_base + acc * p.block_n, q, half, lane, b,
-                          mt * kBlockM + q * 32 + lane, nt * p.block_n);
+            const uint32_t mrow = mt * kBlockM + q * 32 + lane;
+            if (p.epi == 0) epilogue_tile<0>(p, &map_z, epi, tmem_base + acc * p.block_n, q, half, lane, b, mrow, nt * p.block_n);
+            else if (p.epi == 1) epilogue_tile<1>(p, &map_z, epi, tmem_base + acc * p.block_n, q, half, lane, b, mrow, nt * p.block_n);
+            else epilogue_tile<2>(p, &map_z, epi, tmem_base + acc * p.block_n, q, half, lane, b, mrow, nt * p.block_n);
             tc_fence_before();
             mbar_arrive(tempty0 + 8 * acc);
             if (++acc == 2) {
@@ -643,8 +674,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tile_of(p, t, b, mt, nt);
             if (!mbar_wait_cl(tfull0 + 8 * acc, acc_phase, abort, p.timeout_ns)) break;
             tc_fence_after();
-            epilogue_tile(p, &map_z, epi, tmem_base + acc * p.block_n, q, half, lane, b,
-                          mt * 2 * kBlockM + rank * kBlockM + q * 32 + lane, nt * p.block_n);
+            const uint32_t mrow = mt * 2 * kBlockM + rank * kBlockM + q * 32 + lane;
+            if (p.epi == 0) epilogue_tile<0>(p, &map_z, epi, tmem_base + acc * p.block_n, q, half, lane, b, mrow, nt * p.block_n);
+            else if (p.epi == 1) epilogue_tile<1>(p, &map_z, epi, tmem_base + acc * p.block_n, q, half, lane, b, mrow, nt * p.block_n);
+            else epilogue_tile<2>(p, &map_z, epi, tmem_base + acc * p.block_n, q, half, lane, b, mrow, nt * p.block_n);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty0 + 8 * acc, 0));
@@ -1005,7 +1038,7 @@ uint32_t pair_clusters(int sms, uint32_t smem) {
 
 }  // namespace
 
-int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_t s) {
+int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_t s, const TcExtra* ex) {
     if (((uintptr_t)x | (uintptr_t)y | (uintptr_t)z) % 16) return fail(TRA_ERR_ARG, "tensor-core path needs 16-byte aligned buffers");
     const int sms = sm_count();
     if (sms <= 0) return fail(TRA_ERR_CUDA, "no device");
@@ -1052,6 +1085,28 @@ int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_
     tp.alpha = (float)p.alpha;
     tp.out_bf16 = p.out_bf16;
     tp.timeout_ns = 2000000000ull;  // 2 s per wait
+    tp.zM = tp.M;
+    tp.zN = tp.N;
+    if (ex) {
+        if (ex->z_override) {
+            if (t.z_tma) return fail(TRA_ERR_UNSUPPORTED, "output addressing override needs warp stores");
+            if (ex->M > tp.M || ex->N > tp.N) return fail(TRA_ERR_ARG, "output bounds exceed the product");
+            // the warp stores write runs of 32 columns: the map must keep each run contiguous
+            if (ex->zn.n < 1 || ex->zn.t[0].div != 1 || ex->zn.t[0].loc_stride != 1 || ex->zn.t[0].sub % 32 ||
+                ex->N % 32)
+                return fail(TRA_ERR_UNSUPPORTED, "output map is not contiguous along N in runs of 32");
+            tp.zb = ex->zb;
+            tp.zm = ex->zm;
+            tp.zn = ex->zn;
+            tp.zM = ex->M;
+            tp.zN = ex->N;
+        }
+        tp.epi = (uint32_t)ex->epi;
+        tp.row_term = ex->row_term;
+        tp.col_term = ex->col_term;
+        tp.alpha = ex->alpha;
+        if (tp.epi && (!tp.row_term || !tp.col_term)) return fail(TRA_ERR_ARG, "epilogue terms missing");
+    }
     cudaError_t e;
     if (t.pair) {
         e = cudaFuncSetAttribute(tc_gemm_2sm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)t.smem);

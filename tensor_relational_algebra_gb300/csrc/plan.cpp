@@ -71,6 +71,7 @@ uint64_t repartition_cost_elems(int rank, const int64_t* shape, const int32_t* s
 
 Plan::~Plan() {
     if (tc) tc_free(tc);
+    delete inner;
 }
 
 namespace {
@@ -181,6 +182,7 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
         else if (k == "tc" && (v == "pair" || v == "single")) p->tc_pair = v == "pair" ? 1 : 0;
         else if (k == "tc_n" && (v == "256" || v == "128")) p->tc_n = v == "256" ? 256 : 128;
         else if (k == "tc_store" && (v == "tma" || v == "lsu")) p->tc_store = v == "tma" ? 1 : 0;
+        else if (k == "split" && (v == "bf16x3" || v == "none")) p->split3 = v == "bf16x3";
         else if (k == "alpha") {
             char* end = nullptr;
             errno = 0;
@@ -321,6 +323,42 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
         p->kernel = TRA_KERNEL_ELEMENTWISE;
     } else if (p->unary) {
         p->kernel = TRA_KERNEL_ROW_REDUCE;
+    } else if (p->split3) {
+        // Squared distance sum_k (x - y)^2 = |x|^2 + |y|^2 - 2 x.y, and the factored logsumexp
+        // lse_k (x + y) = mx + my + log sum_k e^(x - mx) e^(y - my): the sum of products runs as
+        // one BF16 GEMM over K' = 3K with each fp32 operand split into hi + lo bf16 terms
+        // (hi.hi + hi.lo + lo.hi); the rank-one terms go into its epilogue.
+        if (p->in_bf16) return fail(TRA_ERR_UNSUPPORTED, "split=bf16x3 takes fp32 inputs");
+        if (!((p->op == kSqdiff && p->agg == kSum) || (p->op == kAdd && p->agg == kLse)))
+            return fail(TRA_ERR_UNSUPPORTED, "split=bf16x3 applies to sqdiff:sum and add:lse");
+        const uint64_t nb = p->ext[kBatch], M = p->ext[kM], N = p->ext[kN], K = p->ext[kK];
+        if (3 * K + 64 > 0x7fffffffull) return fail(TRA_ERR_UNSUPPORTED, "split=bf16x3: 3K exceeds 2^31-1");
+        // the GEMM's warp-store epilogue writes runs of 32 output columns: Z must be contiguous
+        // along N in such runs (its last label is N's innermost, with a block extent that is a
+        // multiple of 32)
+        const int zl = p->Z.rank ? p->Z.label[p->Z.rank - 1] : -1;
+        if (p->comp[kN].empty() || zl != p->comp[kN][0] || (p->B[zl] / p->D[zl]) % 32)
+            return fail(TRA_ERR_UNSUPPORTED,
+                        "split=bf16x3: the output's last label must be an N label with a block extent that is a multiple of 32");
+        // the GEMM's tiles take M, K' and N in multiples of 128, 64 and 64: the split operands
+        // are padded (rows past M / N are never stored; the K' padding is zero)
+        const uint64_t Mp = split3_pad(M, 128), Np = split3_pad(N, 64), K3p = split3_pad(3 * K, 64);
+        std::string ispec = nb > 1 ? "bmk,bnk->bmn" : "mk,nk->mn";
+        ispec += ":mul:sum:in=bf16:tc_store=lsu";
+        if (p->out_bf16) ispec += ":out=bf16";
+        const int64_t ib[4] = {(int64_t)nb, (int64_t)Mp, (int64_t)K3p, (int64_t)Np};  // labels b, m, k, n
+        const int32_t ones[6] = {1, 1, 1, 1, 1, 1};
+        Plan* in = new Plan();
+        const int rc = nb > 1 ? build_plan(ispec.c_str(), ib, 4, ones, 6, in) : build_plan(ispec.c_str(), ib + 1, 3, ones, 4, in);
+        if (rc != TRA_OK || (in->kernel != TRA_KERNEL_TC_BF16 && in->kernel != TRA_KERNEL_TC_BF16_PAIR)) {
+            delete in;
+            return fail(TRA_ERR_UNSUPPORTED, "split=bf16x3: no tensor-core tiling for the %llu x %llu x %llu product",
+                        (unsigned long long)M, (unsigned long long)(3 * K), (unsigned long long)N);
+        }
+        p->inner = in;
+        p->kernel = TRA_KERNEL_TC_SPLIT3;
+        p->ws_bytes = align256(nb * Mp * K3p * 2) + align256(nb * Np * K3p * 2) + align256(nb * M * 4) +
+                      align256(nb * N * 4);
     } else if (p->op == kAdd && p->agg == kLse) {
         p->kernel = TRA_KERNEL_LSE_FACTORED;
         const uint64_t nb = p->ext[kBatch];
@@ -341,7 +379,7 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
         }
     }
     if (!p->unary && p->kernel != TRA_KERNEL_TC_BF16 && p->kernel != TRA_KERNEL_TC_BF16_PAIR &&
-        p->kernel != TRA_KERNEL_ELEMENTWISE)
+        p->kernel != TRA_KERNEL_ELEMENTWISE && p->kernel != TRA_KERNEL_TC_SPLIT3)
         scan_vec_flags(role_map(*p, p->X, kBatch), role_map(*p, p->X, kM), role_map(*p, p->X, kK),
                        role_map(*p, p->Y, kBatch), role_map(*p, p->Y, kN), role_map(*p, p->Y, kK),
                        role_map(*p, p->Z, kBatch), role_map(*p, p->Z, kM), role_map(*p, p->Z, kN),

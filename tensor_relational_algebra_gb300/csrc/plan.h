@@ -40,6 +40,8 @@ struct Plan {
     int tc_pair = -1;  // tensor-core tile: 1 CTA pair (256 x 256), 0 single CTA, -1 pair when shapes allow
     int tc_n = 0;      // width of a pair tile: 256, 128, or 0 (256 where the columns allow)
     int tc_store = -1; // tensor-core epilogue: 1 TMA stores, 0 warp stores, -1 TMA where the output map fits
+    int split3 = 0;    // split=bf16x3: squared distance / logsumexp rewritten onto BF16 tensor cores
+    Plan* inner = nullptr;  // split3: the GEMM plan over the split operands (owned)
     // vector-load eligibility of the semiring kernel's operands (host scan, see scan_vec_flags)
     int vec_flags[5] = {0, 0, 0, 0, 0};  // X along K, X along M, Y along N, Y along K, Z along N
     bool unary = false;
@@ -78,9 +80,22 @@ void fill_keys(const Plan& p, int32_t* out);
 // sum-of-products can run on tcgen05 with TMA tiles that stay inside blocks.
 bool tc_plan(Plan* p);
 void tc_free(TcPlan* t);
-int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_t s);
+// Optional epilogue of tc_execute for the rewritten non-sum semirings (split=bf16x3): rank-one
+// terms per output row / column, and the output addressed through another plan's Z role maps
+// (the caller's relation layout) instead of the GEMM plan's own.
+struct TcExtra {
+    int epi = 0;  // 0 plain, 1 squared-distance expansion, 2 factored logsumexp
+    const float* row_term = nullptr;
+    const float* col_term = nullptr;
+    float alpha = 1.f;
+    bool z_override = false;
+    RoleMap zb, zm, zn;
+    uint32_t M = 0, N = 0;  // with z_override: the rows / columns stored (the product may be padded)
+};
+int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_t s, const TcExtra* ex = nullptr);
 
 uint64_t align256(uint64_t v);
+inline uint64_t split3_pad(uint64_t v, uint64_t q) { return (v + q - 1) / q * q; }
 uint64_t repartition_cost_elems(int rank, const int64_t* shape, const int32_t* src_d, const int32_t* dst_d);
 
 // Exhaustive host check of the semiring kernel's 4-wide loads: an operand may load

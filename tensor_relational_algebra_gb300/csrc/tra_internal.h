@@ -15,6 +15,7 @@
 
 #include <cstdint>
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "../../include/tra.h"
@@ -117,11 +118,29 @@ struct LsePrepParams {
     RoleMap b, r, k;      // batch, row (M or N) and contracted maps of this operand
     uint32_t nb, R, K;
     int32_t in_bf16;
-    int32_t mode;         // 0: row max + exp shift;  1: sum of squares (for sqdiff expansion)
+    int32_t mode;         // 0: row max, and dst = exp(v - max) unless dst is null;
+                          // 1: sum of squares (for sqdiff expansion)
     // contracted composite made of one label (set by the launcher)
     int32_t k_simple;
     FastDiv k_sub;
     int64_t k_ks, k_ls;
+};
+
+// One fp32 operand of a sum-of-products split for three BF16 products (split=bf16x3):
+// v = src (or exp(src - shift[row]) when shift is set) becomes hi = bf16(v), lo = bf16(v - hi),
+// written dense, one row of pitch K3p >= 3K per row index r (M for X, N for Y) of batch b:
+// dst[(b Rp + r) K3p + s K + k] = hi, hi, lo for X (is_y = 0) and hi, lo, hi for Y, s = 0, 1, 2,
+// and zeros in [3K, K3p); rows R .. Rp - 1 are left as they are (they feed only outputs that
+// are not stored).  hi.hi + hi.lo + lo.hi then runs as one GEMM over the tripled index.
+struct Split3Params {
+    const float* src;
+    __nv_bfloat16* dst;
+    const float* shift;   // [nb * R] or null
+    RoleMap b, r, k;      // batch, row (M or N) and contracted maps of the operand
+    uint32_t nb, R, K;
+    uint32_t Rp, K3p;     // padded row count and row pitch of dst
+    int32_t is_y;
+    int32_t k_fast;       // set by the launcher: the innermost contracted label is contiguous
 };
 
 // Unary aggregation over the contracted labels (row reduction).
@@ -194,6 +213,10 @@ struct CombineParams {
 cudaError_t launch_semiring(const SemiringParams& p, cudaStream_t s);
 cudaError_t launch_semiring_simple(const SemiringParams& p, cudaStream_t s);
 cudaError_t launch_lse_prep(const LsePrepParams& p, cudaStream_t s);
+// Outputs of the factored logsumexp marked NaN (their exp-shifted sum underflowed) are
+// recomputed straight from p.x_raw / p.y_raw through p's role maps.
+cudaError_t launch_lse_fixup(const SemiringParams& p, cudaStream_t s);
+cudaError_t launch_split3(const Split3Params& p, cudaStream_t s);
 cudaError_t launch_row_reduce(const RowReduceParams& p, cudaStream_t s);
 cudaError_t launch_elementwise(const ElementwiseParams& p, cudaStream_t s);
 cudaError_t launch_repartition(const RepartParams& p, cudaStream_t s);

@@ -99,6 +99,42 @@ def test_kernel_choice(lib):
     assert lib.Plan("ij,jk->ik:mul:sum:in=bf16", [256, 128, 384], [1, 1, 1, 1]).kernel == "tc_bf16_pair"
 
 
+def test_split3_plans(lib):
+    # split=bf16x3: the dense split operands (K tripled, bf16) and one fp32 term per row and column
+    a = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    p = lib.Plan("ij,jk->ik:sqdiff:sum:split=bf16x3", [8192, 256, 8192], [8, 1, 1, 8])
+    assert p.kernel == "tc_split3"
+    assert p.workspace_bytes == a(8192 * 768 * 2) + a(8192 * 768 * 2) + a(8192 * 4) + a(8192 * 4)
+    assert lib.Plan("ij,jk->ik:add:lse:split=bf16x3", [256, 64, 384], [2, 2, 2, 3]).kernel == "tc_split3"
+    p = lib.Plan("bij,bjk->bik:sqdiff:sum:split=bf16x3", [3, 130, 24, 96], [3, 2, 1, 3, 1, 3])
+    assert p.kernel == "tc_split3"
+    # padded to the GEMM's tiles: M 130 -> 256, N 96 -> 128, 3K = 72 -> 128
+    assert p.workspace_bytes == a(3 * 256 * 128 * 2) + a(3 * 128 * 128 * 2) + a(3 * 130 * 4) + a(3 * 96 * 4)
+    # the cost terms are the plan's own (the split changes how, not what, is computed)
+    q = lib.Plan("ij,jk->ik:sqdiff:sum", [8192, 256, 8192], [8, 1, 1, 8])
+    p = lib.Plan("ij,jk->ik:sqdiff:sum:split=bf16x3", [8192, 256, 8192], [8, 1, 1, 8])
+    assert (p.n_tasks, p.cost_join, p.cost_agg) == (q.n_tasks, q.cost_join, q.cost_agg)
+    assert lib.Plan("ij,jk->ik:sqdiff:sum:split=none", [64, 64, 64], [1, 1, 1, 1]).kernel == "semiring_f32"
+
+
+@pytest.mark.parametrize("spec,bounds,d,code", [
+    ("ij,jk->ik:sqdiff:sum:in=bf16:split=bf16x3", [64, 64, 64], [1, 1, 1, 1], "TRA_ERR_UNSUPPORTED"),
+    ("ij,jk->ik:mul:sum:split=bf16x3", [64, 64, 64], [1, 1, 1, 1], "TRA_ERR_UNSUPPORTED"),
+    ("ij,jk->ik:add:max:split=bf16x3", [64, 64, 64], [1, 1, 1, 1], "TRA_ERR_UNSUPPORTED"),
+    ("ij,jk->ik:sqdiff:sum:split=bf16x2", [64, 64, 64], [1, 1, 1, 1], "TRA_ERR_PARSE"),
+    ("ij,jk->ik:sqdiff:sum:split=bf16x3", [300, 96, 200], [2, 1, 1, 2], "TRA_ERR_UNSUPPORTED"),  # N blocks of 100
+    ("ij,jk->ki:add:lse:split=bf16x3", [64, 64, 64], [1, 1, 1, 1], "TRA_ERR_UNSUPPORTED"),  # Z contiguous along M
+    ("ij,jk->ik:add:lse:split=bf16x3:mode=literal", [64, 64, 64], [1, 1, 1, 1], None),
+])
+def test_split3_plan_errors(lib, spec, bounds, d, code):
+    if code is None:  # literal mode takes precedence: the pages' two-phase form
+        assert lib.Plan(spec, bounds, d).kernel == "literal"
+        return
+    with pytest.raises(lib.TraError) as e:
+        lib.Plan(spec, bounds, d)
+    assert code in str(e.value)
+
+
 @pytest.mark.parametrize("spec,bounds,d,code", [
     ("ij,jk->ik:mul:sum", [64, 64, 64], [3, 1, 1, 1], "TRA_ERR_DIVISIBILITY"),
     ("ij,jk->ik:mul:sum", [64, 64, 64], [1, 2, 4, 1], "TRA_ERR_SHARED_LABEL_D"),
