@@ -300,16 +300,22 @@ int execute_plan(const Plan& p, const void* x, const void* y, void* z, void* ws,
             float* rt = reinterpret_cast<float*>(w);
             w += align256(nb * M * 4);
             float* ct = reinterpret_cast<float*>(w);
-            LsePrepParams lp;
-            memset(&lp, 0, sizeof(lp));
-            lp.mode = lse ? 0 : 1;
-            lp.dst = nullptr;
-            lp.nb = sp.nb;
-            lp.K = sp.K;
-            lp.src = x, lp.rmax = rt, lp.b = sp.xb, lp.r = sp.xm, lp.k = sp.xk, lp.R = sp.M;
-            if ((e = launch_lse_prep(lp, s)) != cudaSuccess) return cuda_fail(e, "row terms of X");
-            lp.src = y, lp.rmax = ct, lp.b = sp.yb, lp.r = sp.yn, lp.k = sp.yk, lp.R = sp.N;
-            if ((e = launch_lse_prep(lp, s)) != cudaSuccess) return cuda_fail(e, "column terms of Y");
+            w += align256(nb * N * 4);
+            int* marks = reinterpret_cast<int*>(w);
+            w += 256;
+            float* parts = reinterpret_cast<float*>(w);
+            Split3StatsParams st;
+            memset(&st, 0, sizeof(st));
+            st.mode = lse ? 0 : 1;
+            st.nb = sp.nb;
+            st.K = sp.K;
+            st.partials = parts;
+            st.src = reinterpret_cast<const float*>(x), st.out = rt, st.b = sp.xb, st.r = sp.xm, st.k = sp.xk, st.R = sp.M;
+            st.kc = split3_stats_chunks(nb * M, K);
+            if ((e = launch_split3_stats(st, s)) != cudaSuccess) return cuda_fail(e, "row terms of X");
+            st.src = reinterpret_cast<const float*>(y), st.out = ct, st.b = sp.yb, st.r = sp.yn, st.k = sp.yk, st.R = sp.N;
+            st.kc = split3_stats_chunks(nb * N, K);
+            if ((e = launch_split3_stats(st, s)) != cudaSuccess) return cuda_fail(e, "column terms of Y");
             Split3Params s3;
             memset(&s3, 0, sizeof(s3));
             s3.src = reinterpret_cast<const float*>(x), s3.dst = a3, s3.shift = lse ? rt : nullptr;
@@ -324,16 +330,21 @@ int execute_plan(const Plan& p, const void* x, const void* y, void* z, void* ws,
             ex.row_term = rt;
             ex.col_term = ct;
             ex.alpha = (float)p.alpha;
-            ex.z_override = true;
+            ex.z_override = !p.split3_direct;
             ex.zb = sp.zb;
             ex.zm = sp.zm;
             ex.zn = sp.zn;
             ex.M = sp.M;
             ex.N = sp.N;
+            if (lse) {
+                ex.mark_count = marks;
+                if ((e = cudaMemsetAsync(marks, 0, sizeof(int), s)) != cudaSuccess) return cuda_fail(e, "mark count");
+            }
             const int rc = tc_execute(*p.inner, a3, b3, z, s, &ex);
             if (rc != TRA_OK || !lse) return rc;
             sp.x_raw = x;
             sp.y_raw = y;
+            sp.mark_count = marks;
             e = launch_lse_fixup(sp, s);
             break;
         }

@@ -408,53 +408,210 @@ cudaError_t launch_elementwise(const ElementwiseParams& p, cudaStream_t s) {
 
 namespace {
 
-// One CTA per 32 rows x 32 contracted indices of one batch: the tile is read along the index
-// that is contiguous in the operand (k when k_fast), staged in shared memory, and written
-// along k, so both sides coalesce whatever the operand's relation layout.
+// One CTA per 32 rows x 128 contracted indices of one batch: the tile's row and contracted
+// offsets are formed once (shared memory), the tile is read along the index that is contiguous
+// in the operand (k when k_fast), staged in shared memory, and written along k as bf16 pairs,
+// so both sides coalesce whatever the operand's relation layout.
+constexpr uint32_t kSplitTR = 32, kSplitTK = 128;
+
 __global__ void __launch_bounds__(256) split3_kernel(const __grid_constant__ Split3Params p) {
-    __shared__ float t[32][33];
-    const uint32_t tiles_k = (p.K + 31) / 32, tiles_r = (p.R + 31) / 32;
+    constexpr uint32_t TR = kSplitTR, TK = kSplitTK;
+    __shared__ float t[TR][TK + 1];
+    __shared__ int64_t roff[TR], koff[TK];
+    __shared__ float rsh[TR];
+    const uint32_t tiles_k = (p.K + TK - 1) / TK, tiles_r = (p.R + TR - 1) / TR;
     const uint32_t kt = blockIdx.x % tiles_k, rest = blockIdx.x / tiles_k;
     const uint32_t rt = rest % tiles_r, b = rest / tiles_r;
-    const uint32_t r0 = rt * 32, k0 = kt * 32;
-    const uint32_t tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    const int64_t bo = role_offset(p.b, b);
+    const uint32_t r0 = rt * TR, k0 = kt * TK;
+    const uint32_t tid = threadIdx.x;
+    if (tid < TR) {
+        const uint32_t r = min(r0 + tid, p.R - 1);
+        roff[tid] = role_offset(p.b, b) + role_offset(p.r, r);
+        rsh[tid] = p.shift ? p.shift[(uint64_t)b * p.R + r] : 0.f;
+    } else if (tid < TR + TK && !p.k_dense) {
+        koff[tid - TR] = role_offset(p.k, min(k0 + tid - TR, p.K - 1));
+    }
+    __syncthreads();
+    const uint32_t lane = tid & 31, w = tid >> 5;
+    if (p.k_fast) {
+        // warp w reads rows w, w + 8, ...; lanes along k
 #pragma unroll
-    for (uint32_t i = 0; i < 4; ++i) {
-        const uint32_t rl = p.k_fast ? ty + 8 * i : tx, kl = p.k_fast ? tx : ty + 8 * i;
-        const uint32_t r = r0 + rl, k = k0 + kl;
-        if (r < p.R && k < p.K) {
-            float v = p.src[bo + role_offset(p.r, r) + role_offset(p.k, k)];
-            if (p.shift) v = expf(v - p.shift[(uint64_t)b * p.R + r]);
-            t[rl][kl] = v;
+        for (uint32_t i = 0; i < TR / 8; ++i) {
+            const uint32_t rl = w + 8 * i;
+            if (r0 + rl >= p.R) continue;
+            const float* row = p.src + roff[rl];
+#pragma unroll
+            for (uint32_t h = 0; h < TK / 32; ++h) {
+                const uint32_t kl = lane + 32 * h;
+                if (k0 + kl < p.K) t[rl][kl] = row[p.k_dense ? (int64_t)(k0 + kl) : koff[kl]];
+            }
+        }
+    } else {
+        // lanes along the rows
+        const bool rv = r0 + lane < p.R;
+        const float* row = p.src + roff[lane];
+#pragma unroll 4
+        for (uint32_t i = 0; i < TK / 8; ++i) {
+            const uint32_t kl = w + 8 * i;
+            if (rv && k0 + kl < p.K) t[lane][kl] = row[p.k_dense ? (int64_t)(k0 + kl) * p.k_ls : koff[kl]];
         }
     }
     __syncthreads();
+    // write: warp w, rows w, w + 8, ...; lane holds k = 2 lane, 2 lane + 1 of each 64
     const uint64_t K = p.K;
 #pragma unroll
-    for (uint32_t i = 0; i < 4; ++i) {
-        const uint32_t r = r0 + ty + 8 * i, k = k0 + tx;
+    for (uint32_t i = 0; i < TR / 8; ++i) {
+        const uint32_t rl = w + 8 * i, r = r0 + rl;
         if (r >= p.R) continue;
         __nv_bfloat16* out = p.dst + ((uint64_t)b * p.Rp + r) * p.K3p;
-        if (k < p.K) {
-            const float v = t[ty + 8 * i][tx];
-            const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-            const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-            out[k] = hi;
-            out[K + k] = p.is_y ? lo : hi;
-            out[2 * K + k] = p.is_y ? hi : lo;
+#pragma unroll
+        for (uint32_t h = 0; h < TK / 64; ++h) {
+            const uint32_t kl = 2 * lane + 64 * h, k = k0 + kl;
+            if (k >= p.K) continue;
+            float v0 = t[rl][kl], v1 = k + 1 < p.K ? t[rl][kl + 1] : 0.f;
+            if (p.shift) {
+                v0 = expf(v0 - rsh[rl]);
+                v1 = k + 1 < p.K ? expf(v1 - rsh[rl]) : 0.f;
+            }
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(v0, v1);
+            const float2 hf = __bfloat1622float2(hi);
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(v0 - hf.x, v1 - hf.y);
+            if ((K & 1) == 0) {  // k even, so every pair is 4-byte aligned
+                *reinterpret_cast<__nv_bfloat162*>(out + k) = hi;
+                *reinterpret_cast<__nv_bfloat162*>(out + K + k) = p.is_y ? lo : hi;
+                *reinterpret_cast<__nv_bfloat162*>(out + 2 * K + k) = p.is_y ? hi : lo;
+            } else {
+                const __nv_bfloat16 e[3][2] = {{hi.x, hi.y}, {p.is_y ? lo.x : hi.x, p.is_y ? lo.y : hi.y},
+                                               {p.is_y ? hi.x : lo.x, p.is_y ? hi.y : lo.y}};
+                for (int sgm = 0; sgm < 3; ++sgm) {
+                    out[sgm * K + k] = e[sgm][0];
+                    if (k + 1 < p.K) out[sgm * K + k + 1] = e[sgm][1];
+                }
+            }
         }
         if (kt == tiles_k - 1)  // the row's zero padding
-            for (uint64_t j = 3 * K + tx; j < p.K3p; j += 32) out[j] = __float2bfloat16_rn(0.f);
+            for (uint64_t j = 3 * K + lane; j < p.K3p; j += 32) out[j] = __float2bfloat16_rn(0.f);
     }
 }
 
 }  // namespace
 
+namespace {
+
+// Phase 1 of the row statistics: one CTA per 32 rows x one chunk of the contracted range.
+// k_fast: warp w takes rows w, w + 8, w + 16, w + 24 with its lanes along k; otherwise the lanes
+// take the 32 rows and the 8 warps split the chunk.  Loads are unrolled for memory parallelism.
+constexpr uint32_t kStatsChunk = 2048;  // contracted indices per phase-1 CTA at most
+
+__global__ void __launch_bounds__(256) split3_stats_kernel(const __grid_constant__ Split3StatsParams p) {
+    __shared__ float red[8][32];
+    __shared__ int64_t koff[kStatsChunk];
+    const uint32_t tiles_r = (p.R + 31) / 32;
+    const uint32_t c = blockIdx.x % p.kc, rest = blockIdx.x / p.kc;
+    const uint32_t rt = rest % tiles_r, b = rest / tiles_r;
+    const uint32_t r0 = rt * 32;
+    const uint32_t per = (p.K + p.kc - 1) / p.kc, k_lo = c * per, k_hi = min(p.K, k_lo + per);
+    const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const float init = p.mode == 0 ? -INFINITY : 0.f;
+    const int64_t bo = role_offset(p.b, b);
+    auto acc = [&](float a, float v) { return p.mode == 0 ? fmaxf(a, v) : fmaf(v, v, a); };
+    const uint64_t rows = (uint64_t)p.nb * p.R;
+    for (uint32_t k = k_lo + threadIdx.x; k < k_hi; k += blockDim.x) koff[k - k_lo] = role_offset(p.k, k);
+    __syncthreads();
+    const int64_t* ko = koff - k_lo;  // indexed by k
+    if (p.k_fast) {
+#pragma unroll
+        for (uint32_t i = 0; i < 4; ++i) {
+            const uint32_t r = r0 + w + 8 * i;
+            float a0 = init, a1 = init;
+            if (r < p.R) {
+                const float* row = p.src + bo + role_offset(p.r, r);
+                uint32_t k = k_lo + lane;
+#pragma unroll 4
+                for (; k + 32 < k_hi; k += 64) {
+                    a0 = acc(a0, row[ko[k]]);
+                    a1 = acc(a1, row[ko[k + 32]]);
+                }
+                if (k < k_hi) a0 = acc(a0, row[ko[k]]);
+            }
+            float a = p.mode == 0 ? fmaxf(a0, a1) : a0 + a1;
+            for (int o = 16; o; o >>= 1) {
+                const float v = __shfl_xor_sync(0xffffffffu, a, o);
+                a = p.mode == 0 ? fmaxf(a, v) : a + v;
+            }
+            if (lane == 0 && r < p.R) p.partials[(uint64_t)c * rows + (uint64_t)b * p.R + r] = a;
+        }
+    } else {
+        const uint32_t r = r0 + lane;
+        float a0 = init, a1 = init;
+        if (r < p.R) {
+            const float* row = p.src + bo + role_offset(p.r, r);
+            uint32_t k = k_lo + w;
+#pragma unroll 4
+            for (; k + 8 < k_hi; k += 16) {
+                a0 = acc(a0, row[ko[k]]);
+                a1 = acc(a1, row[ko[k + 8]]);
+            }
+            if (k < k_hi) a0 = acc(a0, row[ko[k]]);
+        }
+        red[w][lane] = p.mode == 0 ? fmaxf(a0, a1) : a0 + a1;
+        __syncthreads();
+        if (w == 0 && r < p.R) {
+            float a = red[0][lane];
+            for (int q = 1; q < 8; ++q) a = p.mode == 0 ? fmaxf(a, red[q][lane]) : a + red[q][lane];
+            p.partials[(uint64_t)c * rows + (uint64_t)b * p.R + r] = a;
+        }
+    }
+}
+
+__global__ void split3_stats_combine(const __grid_constant__ Split3StatsParams p) {
+    const uint64_t rows = (uint64_t)p.nb * p.R;
+    const uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x;
+    if (i >= rows) return;
+    float a = p.partials[i];
+    for (uint32_t c = 1; c < p.kc; ++c) {
+        const float v = p.partials[(uint64_t)c * rows + i];
+        a = p.mode == 0 ? fmaxf(a, v) : a + v;
+    }
+    p.out[i] = a;
+}
+
+}  // namespace
+
+uint32_t split3_stats_chunks(uint64_t rows, uint64_t K) {
+    // about 2048 CTAs in phase 1, and at least 256 contracted indices per chunk
+    const uint64_t tiles = (rows + 31) / 32;
+    uint64_t kc = (2048 + tiles - 1) / tiles;
+    const uint64_t kmax = (K + 255) / 256;
+    if (kc > kmax) kc = kmax;
+    const uint64_t kmin = (K + kStatsChunk - 1) / kStatsChunk;  // chunks fit the offset table
+    if (kc < kmin) kc = kmin;
+    if (kc < 1) kc = 1;
+    return (uint32_t)kc;
+}
+
+cudaError_t launch_split3_stats(const Split3StatsParams& pin, cudaStream_t s) {
+    Split3StatsParams p = pin;
+    p.k_fast = p.k.n > 0 && p.k.t[0].div == 1 && p.k.t[0].loc_stride == 1;
+    const uint64_t rows = (uint64_t)p.nb * p.R;
+    if (rows == 0) return cudaSuccess;
+    if (p.kc < 1 || p.kc != split3_stats_chunks(rows, p.K)) return cudaErrorInvalidValue;
+    const uint64_t ctas = (uint64_t)p.nb * ((p.R + 31) / 32) * p.kc;
+    if (ctas > 0x7fffffffull) return cudaErrorInvalidValue;
+    split3_stats_kernel<<<(unsigned)ctas, 256, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    split3_stats_combine<<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_split3(const Split3Params& pin, cudaStream_t s) {
     Split3Params p = pin;
     p.k_fast = p.k.n > 0 && p.k.t[0].div == 1 && p.k.t[0].loc_stride == 1;
-    const uint64_t ctas = (uint64_t)p.nb * ((p.R + 31) / 32) * ((p.K + 31) / 32);
+    // one contracted label, not split into keys: offset = k * its local stride
+    p.k_dense = p.k.n == 1 && p.k.t[0].div == 1 && p.k.t[0].sub == p.K && p.k.t[0].ext == p.K;
+    p.k_ls = p.k_dense ? p.k.t[0].loc_stride : 0;
+    const uint64_t ctas = (uint64_t)p.nb * ((p.R + kSplitTR - 1) / kSplitTR) * ((p.K + kSplitTK - 1) / kSplitTK);
     if (ctas == 0) return cudaSuccess;
     if (ctas > 0x7fffffffull) return cudaErrorInvalidValue;
     split3_kernel<<<(unsigned)ctas, 256, 0, s>>>(p);

@@ -563,6 +563,7 @@ __global__ void semiring_simple(const __grid_constant__ SemiringParams p) {
 // from the operands.  With finite inputs no true result is NaN.
 __global__ void __launch_bounds__(NT) lse_fixup_kernel(const __grid_constant__ SemiringParams p) {
     __shared__ int64_t rowZ[BM], colZ[BN];
+    if (p.mark_count && *p.mark_count == 0) return;  // the producer counted its marks: none
     const int tid = threadIdx.x;
     const uint32_t tiles_m = (p.M + BM - 1) / BM, tiles_n = (p.N + BN - 1) / BN;
     uint32_t t = blockIdx.x;
@@ -607,6 +608,7 @@ __global__ void lse_prep_kernel(const __grid_constant__ LsePrepParams p, int row
         const uint32_t r = warp % p.R, b = warp / p.R;
         const int64_t base = role_offset(p.b, b) + role_offset(p.r, r);
         float m = p.mode == 0 ? -INFINITY : 0.f;
+#pragma unroll 8
         for (uint32_t k = lane; k < p.K; k += 32) {
             float v = ld1<TIn>(p.src, base + prep_koff(p, k));
             m = p.mode == 0 ? fmaxf(m, v) : fmaf(v, v, m);
@@ -633,6 +635,7 @@ __global__ void lse_prep_kernel(const __grid_constant__ LsePrepParams p, int row
         const int64_t base = role_offset(p.b, b) + role_offset(p.r, r);
         float m = p.mode == 0 ? -INFINITY : 0.f;
         if (valid)
+#pragma unroll 8
             for (uint32_t k = w; k < p.K; k += 8) {
                 const float v = ld1<TIn>(p.src, base + prep_koff(p, k));
                 m = p.mode == 0 ? fmaxf(m, v) : fmaf(v, v, m);

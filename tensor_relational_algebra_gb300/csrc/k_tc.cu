@@ -81,6 +81,7 @@ struct TcParams {
     const float* row_term;
     const float* col_term;
     uint32_t zM, zN;  // output rows / columns stored (M, N unless the operands are padded)
+    int* mark_count;  // epilogue 2: incremented once per output marked NaN (may be null)
 };
 
 // ------------------------------------------------------------------ PTX wrappers (tc_ptx.h)
@@ -342,8 +343,14 @@ __device__ __forceinline__ void apply_terms(const TcParams& p, uint32_t (&r)[32]
         const float c = __ldg(ct + min(n + (uint32_t)i, p.zN - 1));
         const float a = __uint_as_float(r[i]);
         float v;
-        if (EPI == 1) v = fmaxf(rt + c - 2.f * a, 0.f);
-        else v = a > 1e-30f ? rt + c + logf(a) : __int_as_float(0x7fc00000);
+        if (EPI == 1) {
+            v = fmaxf(rt + c - 2.f * a, 0.f);
+        } else if (a > 1e-30f) {
+            v = rt + c + logf(a);
+        } else {
+            v = __int_as_float(0x7fc00000);
+            if (p.mark_count) atomicAdd(p.mark_count, 1);
+        }
         r[i] = __float_as_uint(v);
     }
 }
@@ -753,6 +760,7 @@ struct TcPlan {
 };
 
 void tc_free(TcPlan* t) { delete t; }
+bool tc_tma_store(const TcPlan* t) { return t && t->z_tma; }
 
 namespace {
 
@@ -1104,6 +1112,7 @@ int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_
         tp.epi = (uint32_t)ex->epi;
         tp.row_term = ex->row_term;
         tp.col_term = ex->col_term;
+        tp.mark_count = ex->mark_count;
         tp.alpha = ex->alpha;
         if (tp.epi && (!tp.row_term || !tp.col_term)) return fail(TRA_ERR_ARG, "epilogue terms missing");
     }

@@ -19,6 +19,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
+#include <algorithm>
 #include <cstring>
 
 namespace tra {
@@ -343,22 +344,45 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
         // the GEMM's tiles take M, K' and N in multiples of 128, 64 and 64: the split operands
         // are padded (rows past M / N are never stored; the K' padding is zero)
         const uint64_t Mp = split3_pad(M, 128), Np = split3_pad(N, 64), K3p = split3_pad(3 * K, 64);
-        std::string ispec = nb > 1 ? "bmk,bnk->bmn" : "mk,nk->mn";
-        ispec += ":mul:sum:in=bf16:tc_store=lsu";
-        if (p->out_bf16) ispec += ":out=bf16";
-        const int64_t ib[4] = {(int64_t)nb, (int64_t)Mp, (int64_t)K3p, (int64_t)Np};  // labels b, m, k, n
-        const int32_t ones[6] = {1, 1, 1, 1, 1, 1};
-        Plan* in = new Plan();
-        const int rc = nb > 1 ? build_plan(ispec.c_str(), ib, 4, ones, 6, in) : build_plan(ispec.c_str(), ib + 1, 3, ones, 4, in);
-        if (rc != TRA_OK || (in->kernel != TRA_KERNEL_TC_BF16 && in->kernel != TRA_KERNEL_TC_BF16_PAIR)) {
-            delete in;
-            return fail(TRA_ERR_UNSUPPORTED, "split=bf16x3: no tensor-core tiling for the %llu x %llu x %llu product",
-                        (unsigned long long)M, (unsigned long long)(3 * K), (unsigned long long)N);
+        const std::string out_opt = p->out_bf16 ? ":out=bf16" : "";
+        auto is_tc = [](const Plan* q) { return q->kernel == TRA_KERNEL_TC_BF16 || q->kernel == TRA_KERNEL_TC_BF16_PAIR; };
+        // Direct form: one M and one N label, no padding.  The GEMM "mk,nk->mn" takes this plan's
+        // partition of m and n; with k' unsplit, the split operands' row-major layout is their
+        // relation layout, and the GEMM's output relation is this plan's Z, so its TMA-store
+        // epilogue writes Z directly.
+        if (nb == 1 && p->comp[kM].size() == 1 && p->comp[kN].size() == 1 && p->Z.rank == 2 && Mp == M && Np == N) {
+            const std::string dspec = "mk,nk->mn:mul:sum:in=bf16" + out_opt;
+            const int64_t db[3] = {(int64_t)M, (int64_t)K3p, (int64_t)N};
+            const int32_t dd[4] = {p->D[p->comp[kM][0]], 1, p->D[p->comp[kN][0]], 1};
+            Plan* in = new Plan();
+            if (build_plan(dspec.c_str(), db, 3, dd, 4, in) == TRA_OK && is_tc(in) && tc_tma_store(in->tc)) {
+                p->inner = in;
+                p->split3_direct = 1;
+            } else {
+                delete in;
+                clear_error();
+            }
         }
-        p->inner = in;
+        // General form: dense operands, the output addressed through this plan's Z role maps.
+        if (!p->inner) {
+            std::string ispec = nb > 1 ? "bmk,bnk->bmn" : "mk,nk->mn";
+            ispec += ":mul:sum:in=bf16:tc_store=lsu" + out_opt;
+            const int64_t ib[4] = {(int64_t)nb, (int64_t)Mp, (int64_t)K3p, (int64_t)Np};  // labels b, m, k, n
+            const int32_t ones[6] = {1, 1, 1, 1, 1, 1};
+            Plan* in = new Plan();
+            const int rc = nb > 1 ? build_plan(ispec.c_str(), ib, 4, ones, 6, in) : build_plan(ispec.c_str(), ib + 1, 3, ones, 4, in);
+            if (rc != TRA_OK || !is_tc(in)) {
+                delete in;
+                return fail(TRA_ERR_UNSUPPORTED, "split=bf16x3: no tensor-core tiling for the %llu x %llu x %llu product",
+                            (unsigned long long)M, (unsigned long long)(3 * K), (unsigned long long)N);
+            }
+            p->inner = in;
+        }
         p->kernel = TRA_KERNEL_TC_SPLIT3;
+        const uint64_t parts = std::max<uint64_t>(split3_stats_chunks(nb * M, K) * nb * M, split3_stats_chunks(nb * N, K) * nb * N);
+        // operands, row / column terms, the fix-up's mark count (256 bytes), the statistics' partials
         p->ws_bytes = align256(nb * Mp * K3p * 2) + align256(nb * Np * K3p * 2) + align256(nb * M * 4) +
-                      align256(nb * N * 4);
+                      align256(nb * N * 4) + 256 + align256(parts * 4);
     } else if (p->op == kAdd && p->agg == kLse) {
         p->kernel = TRA_KERNEL_LSE_FACTORED;
         const uint64_t nb = p->ext[kBatch];

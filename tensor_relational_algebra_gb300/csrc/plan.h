@@ -42,6 +42,7 @@ struct Plan {
     int tc_store = -1; // tensor-core epilogue: 1 TMA stores, 0 warp stores, -1 TMA where the output map fits
     int split3 = 0;    // split=bf16x3: squared distance / logsumexp rewritten onto BF16 tensor cores
     Plan* inner = nullptr;  // split3: the GEMM plan over the split operands (owned)
+    int split3_direct = 0;  // split3: inner's output layout is this plan's (no override, TMA stores)
     // vector-load eligibility of the semiring kernel's operands (host scan, see scan_vec_flags)
     int vec_flags[5] = {0, 0, 0, 0, 0};  // X along K, X along M, Y along N, Y along K, Z along N
     bool unary = false;
@@ -80,6 +81,7 @@ void fill_keys(const Plan& p, int32_t* out);
 // sum-of-products can run on tcgen05 with TMA tiles that stay inside blocks.
 bool tc_plan(Plan* p);
 void tc_free(TcPlan* t);
+bool tc_tma_store(const TcPlan* t);  // the plan's epilogue stores through an output tensor map
 // Optional epilogue of tc_execute for the rewritten non-sum semirings (split=bf16x3): rank-one
 // terms per output row / column, and the output addressed through another plan's Z role maps
 // (the caller's relation layout) instead of the GEMM plan's own.
@@ -91,6 +93,7 @@ struct TcExtra {
     bool z_override = false;
     RoleMap zb, zm, zn;
     uint32_t M = 0, N = 0;  // with z_override: the rows / columns stored (the product may be padded)
+    int* mark_count = nullptr;  // epi 2: count of outputs marked for the underflow fix-up
 };
 int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_t s, const TcExtra* ex = nullptr);
 

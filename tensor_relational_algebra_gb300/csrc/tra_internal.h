@@ -108,6 +108,9 @@ struct SemiringParams {
     // squared distance by expansion: the epilogue forms xn + yn - 2*sum
     const float* xnorm;   // [nb * M] or null
     const float* ynorm;   // [nb * N] or null
+    // the underflow fix-up returns at once when this count (written by the producer of the
+    // marks) is zero; null: scan every output
+    const int* mark_count;
 };
 
 // Per-operand row-max / exp-shift preparation of the factored logsumexp.
@@ -132,6 +135,21 @@ struct LsePrepParams {
 // dst[(b Rp + r) K3p + s K + k] = hi, hi, lo for X (is_y = 0) and hi, lo, hi for Y, s = 0, 1, 2,
 // and zeros in [3K, K3p); rows R .. Rp - 1 are left as they are (they feed only outputs that
 // are not stored).  hi.hi + hi.lo + lo.hi then runs as one GEMM over the tripled index.
+// Row statistics of one fp32 operand for split=bf16x3: per row r of batch b the maximum
+// (mode 0) or the sum of squares (mode 1) over the contracted index.  Phase 1: CTAs over 32 rows
+// x one of kc chunks of the contracted range write partials[c][b R + r]; phase 2 combines the kc
+// partials of each row in chunk order into out (deterministic).
+struct Split3StatsParams {
+    const float* src;
+    float* partials;      // [kc][nb * R]
+    float* out;           // [nb * R]
+    RoleMap b, r, k;
+    uint32_t nb, R, K, kc;
+    int32_t mode;
+    int32_t k_fast;       // set by the launcher
+};
+uint32_t split3_stats_chunks(uint64_t rows, uint64_t K);  // kc for nb * R rows
+
 struct Split3Params {
     const float* src;
     __nv_bfloat16* dst;
@@ -141,6 +159,8 @@ struct Split3Params {
     uint32_t Rp, K3p;     // padded row count and row pitch of dst
     int32_t is_y;
     int32_t k_fast;       // set by the launcher: the innermost contracted label is contiguous
+    int32_t k_dense;      // set by the launcher: one unsplit contracted label (offset k * k_ls)
+    int64_t k_ls;
 };
 
 // Unary aggregation over the contracted labels (row reduction).
@@ -217,6 +237,7 @@ cudaError_t launch_lse_prep(const LsePrepParams& p, cudaStream_t s);
 // recomputed straight from p.x_raw / p.y_raw through p's role maps.
 cudaError_t launch_lse_fixup(const SemiringParams& p, cudaStream_t s);
 cudaError_t launch_split3(const Split3Params& p, cudaStream_t s);
+cudaError_t launch_split3_stats(const Split3StatsParams& p, cudaStream_t s);
 cudaError_t launch_row_reduce(const RowReduceParams& p, cudaStream_t s);
 cudaError_t launch_elementwise(const ElementwiseParams& p, cudaStream_t s);
 cudaError_t launch_repartition(const RepartParams& p, cudaStream_t s);

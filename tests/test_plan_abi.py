@@ -104,12 +104,13 @@ def test_split3_plans(lib):
     a = lambda v: (v + 255) // 256 * 256  # noqa: E731
     p = lib.Plan("ij,jk->ik:sqdiff:sum:split=bf16x3", [8192, 256, 8192], [8, 1, 1, 8])
     assert p.kernel == "tc_split3"
-    assert p.workspace_bytes == a(8192 * 768 * 2) + a(8192 * 768 * 2) + a(8192 * 4) + a(8192 * 4)
+    # + the statistics' partials: 256 row tiles of 32, 8 chunks of the 256 contracted indices at most -> 1
+    assert p.workspace_bytes == a(8192 * 768 * 2) + a(8192 * 768 * 2) + a(8192 * 4) + a(8192 * 4) + 256 + a(8192 * 4)
     assert lib.Plan("ij,jk->ik:add:lse:split=bf16x3", [256, 64, 384], [2, 2, 2, 3]).kernel == "tc_split3"
     p = lib.Plan("bij,bjk->bik:sqdiff:sum:split=bf16x3", [3, 130, 24, 96], [3, 2, 1, 3, 1, 3])
     assert p.kernel == "tc_split3"
     # padded to the GEMM's tiles: M 130 -> 256, N 96 -> 128, 3K = 72 -> 128
-    assert p.workspace_bytes == a(3 * 256 * 128 * 2) + a(3 * 128 * 128 * 2) + a(3 * 130 * 4) + a(3 * 96 * 4)
+    assert p.workspace_bytes == a(3 * 256 * 128 * 2) + a(3 * 128 * 128 * 2) + a(3 * 130 * 4) + a(3 * 96 * 4) + 256 + a(3 * 130 * 4)
     # the cost terms are the plan's own (the split changes how, not what, is computed)
     q = lib.Plan("ij,jk->ik:sqdiff:sum", [8192, 256, 8192], [8, 1, 1, 8])
     p = lib.Plan("ij,jk->ik:sqdiff:sum:split=bf16x3", [8192, 256, 8192], [8, 1, 1, 8])
