@@ -81,6 +81,10 @@ typedef struct {
     uint64_t workspace_bytes;          /* device scratch ein_execute needs (0 = none) */
     int32_t in_dtype, out_dtype;       /* 0 = fp32, 1 = bf16 */
     int32_t kernel;                    /* TRA_KERNEL_* chosen for ein_execute */
+    /* terms of the cost-model variants (section 4.3 of the EinDecomp page, see tra_cost_model) */
+    uint64_t msg_join;                 /* n_tasks * (number of operands): sub-tensors sent to tasks */
+    uint64_t msg_agg;                  /* (n_tasks/n_agg) * (n_agg-1): partials sent to be combined */
+    uint64_t mem_elems;                /* |Z| + (n_agg > 1 ? n_tasks * z_sub : 0): output + partials */
 } tra_plan_info;
 
 enum {
@@ -159,6 +163,29 @@ int ein_repartition(int rank, const int64_t* shape, const int32_t* src_d, const 
 int ein_repartition_cost(int rank, const int64_t* shape, const int32_t* src_d, const int32_t* dst_d,
                          uint64_t* cost);
 
+/* ein_repartition_messages -- the repartition's number of communication operations, for the
+ * latency term of the cost-model variants: the (source block, destination block) pairs that
+ * share at least one element and have different linear key ids.  Host only. */
+int ein_repartition_messages(int rank, const int64_t* shape, const int32_t* src_d, const int32_t* dst_d,
+                             uint64_t* messages);
+
+/* Cost-model variants (section 4.3 of the EinDecomp page, "troubleshooting"), each off at 0:
+ *   latency        added per communication operation: a node's msg_join + msg_agg (see
+ *                  tra_plan_info) and an edge's repartition messages; penalises many small tasks
+ *   min_block      minimum task granularity: every label's block extent B_l / D_l must be at
+ *                  least min(min_block, B_l)
+ *   mem_limit      memory-aware pruning: a node's mem_elems may not exceed this many elements
+ *   mem_weight     memory-aware cost: mem_weight * mem_elems is added to the node's cost
+ *   task_multiple  load balance: n_tasks must be a multiple of this (e.g. the device count)
+ * Costs stay in elements; latency and mem_weight convert messages and memory into elements. */
+typedef struct {
+    uint64_t latency;
+    int64_t min_block;
+    uint64_t mem_limit;
+    uint64_t mem_weight;
+    int64_t task_multiple;
+} tra_cost_model;
+
 /* ein_graph_decompose -- EinDecomp's optimiser (sections 3.1 and 3.2): choose one
  * partition vector per node of an EinGraph so that the summed cost of section 3.1
  * (every node's join + aggregation cost, plus the repartition cost of every edge
@@ -180,8 +207,10 @@ int ein_repartition_cost(int rank, const int64_t* shape, const int32_t* src_d, c
  * nodes:  n_nodes entries in topological order (an input index names an earlier node).
  * d_out:  receives every node's vector (X's positions then Y's), nodes in order;
  *         n_d_out must equal the sum of the nodes' ranks.
+ * model (may be NULL: the pages' base model): the cost-model variants above, applied to
+ *         the candidates (min_block, task_multiple, mem_limit) and to every node and edge cost.
  * node_cost (may be NULL): receives per node join + aggregation + the repartition cost
- *         of its input edges under the chosen vectors.
+ *         of its input edges under the chosen vectors (with the model's terms).
  * Errors: TRA_ERR_ARG (NULL, bad input index, node order, output/input shape mismatch,
  *         n_d_out), TRA_ERR_PARSE / TRA_ERR_RANK (a node's spec), TRA_ERR_UNSUPPORTED
  *         (a node has no candidate, or more than 65536). */
@@ -201,7 +230,8 @@ typedef struct {
 enum { TRA_DP_POW2 = 1 };
 
 int ein_graph_decompose(const tra_graph_node* nodes, int n_nodes, int64_t p_min, int64_t p_max, int flags,
-                        int32_t* d_out, int n_d_out, uint64_t* node_cost, tra_graph_result* result);
+                        const tra_cost_model* model, int32_t* d_out, int n_d_out, uint64_t* node_cost,
+                        tra_graph_result* result);
 
 /* ein_attention -- the attention chain of the multi-head-attention EinGraph (section 2.1)
  * fused into one kernel: Scores[h,s,t] = scale * sum_d Q K, L[h,s] = logsumexp_t Scores,

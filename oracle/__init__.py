@@ -16,7 +16,8 @@ summation + tensor relational algebra".
   literal TRA execution (relation dictionaries, join, GROUP BY aggregate).
 * ``mha`` -- the multi-head-attention EinGraph of section 2.1, node by node.
 * ``decomp`` -- the partition-vector choice of sections 3.1-3.2 by exhaustive search
-  over every combination of every node's candidates (tiny graphs).
+  over every combination of every node's candidates (tiny graphs), with the cost-model
+  variants of section 4.3 counted from their definitions (messages element by element).
 * ``rounding`` -- fp32 / bf16 round-to-nearest-even.
 
 Parity pins: every function above is checked in ``tests/test_oracle_pins.py``

@@ -18,8 +18,8 @@ from ._build import LIB as _LIB_PATH, build as _build_lib
 __all__ = [
     "TraError", "build_library", "load", "Plan", "ein_plan", "ein_plan_info", "ein_plan_keys", "ein_execute",
     "ein_repartition", "ein_repartition_cost", "ein_status", "ein_selftest_wait_timeout", "ein_plan_destroy",
-    "ein_last_error", "ein_graph_decompose", "ein_attention", "attention",
-    "repartition", "repartition_cost", "decompose", "KERNELS", "ROLES",
+    "ein_last_error", "ein_graph_decompose", "ein_attention", "attention", "ein_repartition_messages",
+    "repartition", "repartition_cost", "repartition_messages", "decompose", "KERNELS", "ROLES",
 ]
 
 TRA_MAX_RANK = 8
@@ -57,6 +57,7 @@ class tra_plan_info(ctypes.Structure):
         ("workspace_bytes", ctypes.c_uint64),
         ("in_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
         ("kernel", ctypes.c_int32),
+        ("msg_join", ctypes.c_uint64), ("msg_agg", ctypes.c_uint64), ("mem_elems", ctypes.c_uint64),
     ]
 
 
@@ -67,6 +68,11 @@ class tra_graph_node(ctypes.Structure):
 
 class tra_graph_result(ctypes.Structure):
     _fields_ = [("total_cost", ctypes.c_uint64), ("dp_cost", ctypes.c_uint64), ("n_candidates", ctypes.c_uint64)]
+
+
+class tra_cost_model(ctypes.Structure):
+    _fields_ = [("latency", ctypes.c_uint64), ("min_block", ctypes.c_int64), ("mem_limit", ctypes.c_uint64),
+                ("mem_weight", ctypes.c_uint64), ("task_multiple", ctypes.c_int64)]
 
 
 TRA_DP_POW2 = 1
@@ -94,17 +100,20 @@ def load():
     lib.ein_execute.argtypes = [vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
     lib.ein_repartition.argtypes = [i32, vp, vp, vp, i32, vp, vp, vp]
     lib.ein_repartition_cost.argtypes = [i32, vp, vp, vp, u64p]
+    lib.ein_repartition_messages.argtypes = [i32, vp, vp, vp, u64p]
     lib.ein_status.argtypes = [vp]
     lib.ein_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     lib.ein_selftest_wait_timeout.restype = ctypes.c_int
     lib.ein_plan_destroy.argtypes = [vp]
     lib.ein_plan_destroy.restype = None
     lib.ein_last_error.restype = ctypes.c_char_p
-    lib.ein_graph_decompose.argtypes = [ctypes.POINTER(tra_graph_node), i32, i64, i64, i32, vp, i32, u64p,
+    lib.ein_graph_decompose.argtypes = [ctypes.POINTER(tra_graph_node), i32, i64, i64, i32,
+                                        ctypes.POINTER(tra_cost_model), vp, i32, u64p,
                                         ctypes.POINTER(tra_graph_result)]
     lib.ein_attention.argtypes = [i32, i32, i32, i32, ctypes.c_float, vp, vp, vp, vp, vp, vp]
     for f in ("ein_plan", "ein_plan_info", "ein_plan_keys", "ein_execute", "ein_repartition",
-              "ein_repartition_cost", "ein_status", "ein_graph_decompose", "ein_attention"):
+              "ein_repartition_cost", "ein_repartition_messages", "ein_status", "ein_graph_decompose",
+              "ein_attention"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -177,9 +186,26 @@ def ein_repartition_cost(shape, src_d, dst_d) -> int:
     return c.value
 
 
-def ein_graph_decompose(nodes, p_min: int, p_max: int, flags: int = 0):
+def ein_repartition_messages(shape, src_d, dst_d) -> int:
+    c = ctypes.c_uint64()
+    _check(load().ein_repartition_messages(len(shape), _i64(shape), _i32(src_d), _i32(dst_d), ctypes.byref(c)))
+    return c.value
+
+
+def _cost_model(model):
+    if model is None:
+        return None
+    unknown = set(model) - {f for f, _ in tra_cost_model._fields_}
+    if unknown:
+        raise ValueError(f"unknown cost-model fields {sorted(unknown)}")
+    return tra_cost_model(**model)
+
+
+def ein_graph_decompose(nodes, p_min: int, p_max: int, flags: int = 0, model=None):
     """nodes: sequence of (spec, bounds, (input_x, input_y)) with -1 for a graph input.
-    Returns (d per node, cost per node, total_cost, dp_cost, n_candidates)."""
+    model: None or a dict of tra_cost_model fields (latency, min_block, mem_limit,
+    mem_weight, task_multiple).  Returns (d per node, cost per node, total_cost, dp_cost,
+    n_candidates)."""
     keep, arr = [], (tra_graph_node * len(nodes))()
     ranks = []
     for i, (spec, bounds, inputs) in enumerate(nodes):
@@ -194,7 +220,9 @@ def ein_graph_decompose(nodes, p_min: int, p_max: int, flags: int = 0):
     d = (ctypes.c_int32 * max(1, n_d))()
     costs = (ctypes.c_uint64 * len(nodes))()
     res = tra_graph_result()
-    _check(load().ein_graph_decompose(arr, len(nodes), p_min, p_max, flags, d, n_d, costs, ctypes.byref(res)))
+    cm = _cost_model(model)
+    _check(load().ein_graph_decompose(arr, len(nodes), p_min, p_max, flags, ctypes.byref(cm) if cm else None, d, n_d,
+                                      costs, ctypes.byref(res)))
     out, pos = [], 0
     for r in ranks:
         out.append(list(d[pos:pos + sum(r)]))
@@ -281,6 +309,18 @@ class Plan:
         return self.info.cost_agg
 
     @property
+    def msg_join(self):
+        return self.info.msg_join
+
+    @property
+    def msg_agg(self):
+        return self.info.msg_agg
+
+    @property
+    def mem_elems(self):
+        return self.info.mem_elems
+
+    @property
     def workspace_bytes(self):
         return self.info.workspace_bytes
 
@@ -333,12 +373,17 @@ def repartition_cost(shape, src_d, dst_d) -> int:
     return ein_repartition_cost(shape, src_d, dst_d)
 
 
-def decompose(nodes, P: int, p_max: int = None, pow2: bool = False):
+def repartition_messages(shape, src_d, dst_d) -> int:
+    return ein_repartition_messages(shape, src_d, dst_d)
+
+
+def decompose(nodes, P: int, p_max: int = None, pow2: bool = False, model=None):
     """EinDecomp over an EinGraph (host only): a partition vector for every node with
     P..p_max join tuples (p_max defaults to P), minimising join + aggregation +
-    repartition cost.  nodes: (spec, bounds, (input_x, input_y)) in topological order,
-    -1 marking a graph input.  Returns a dict with "d", "node_cost", "total_cost",
-    "dp_cost", "n_candidates"."""
+    repartition cost (plus the terms of the cost-model variants in model, a dict of
+    tra_cost_model fields).  nodes: (spec, bounds, (input_x, input_y)) in topological
+    order, -1 marking a graph input.  Returns a dict with "d", "node_cost",
+    "total_cost", "dp_cost", "n_candidates"."""
     d, costs, total, dp, n = ein_graph_decompose(nodes, P, P if p_max is None else p_max,
-                                                 TRA_DP_POW2 if pow2 else 0)
+                                                 TRA_DP_POW2 if pow2 else 0, model)
     return {"d": d, "node_cost": costs, "total_cost": total, "dp_cost": dp, "n_candidates": n}

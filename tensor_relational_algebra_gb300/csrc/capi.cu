@@ -418,6 +418,9 @@ int ein_plan_info(tra_plan_t plan, tra_plan_info* o) {
     o->in_dtype = p.in_bf16;
     o->out_dtype = p.out_bf16;
     o->kernel = p.kernel;
+    o->msg_join = p.msg_join;
+    o->msg_agg = p.msg_agg;
+    o->mem_elems = p.mem_elems;
     return TRA_OK;
 }
 
@@ -513,6 +516,20 @@ int ein_repartition_cost(int rank, const int64_t* shape, const int32_t* src_d, c
             return fail(TRA_ERR_DIVISIBILITY, "partition count does not divide extent %lld", (long long)shape[i]);
     }
     *cost = repartition_cost_elems(rank, shape, src_d, dst_d);
+    return TRA_OK;
+}
+
+int ein_repartition_messages(int rank, const int64_t* shape, const int32_t* src_d, const int32_t* dst_d,
+                             uint64_t* messages) {
+    clear_error();
+    if (rank < 1 || rank > TRA_MAX_RANK) return fail(TRA_ERR_RANK, "rank %d outside 1..%d", rank, TRA_MAX_RANK);
+    if (!shape || !src_d || !dst_d || !messages) return fail(TRA_ERR_ARG, "NULL argument");
+    for (int i = 0; i < rank; ++i) {
+        if (shape[i] < 1) return fail(TRA_ERR_ARG, "extent < 1");
+        if (src_d[i] < 1 || dst_d[i] < 1 || shape[i] % src_d[i] || shape[i] % dst_d[i])
+            return fail(TRA_ERR_DIVISIBILITY, "partition count does not divide extent %lld", (long long)shape[i]);
+    }
+    *messages = repartition_messages(rank, shape, src_d, dst_d);
     return TRA_OK;
 }
 

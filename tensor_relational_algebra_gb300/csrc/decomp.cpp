@@ -10,6 +10,10 @@
 //    DP[v][d_v] = min over d_u of (DP[u][d_u] + repartition(d_u, d_v)) + cost(v, d_v),
 //    read back from the output node.  A node with two inputs adds one such minimum per
 //    input.
+//  * section 4.3 (troubleshooting) -- the cost-model variants of tra_cost_model: a latency
+//    charge per message (node: msg_join + msg_agg; edge: repartition messages), a minimum
+//    block extent per label, a memory limit and weight on the node's output plus partials,
+//    and task counts restricted to multiples of a given number.
 // Host only; no device is touched.
 #include <cstring>
 #include <limits>
@@ -44,11 +48,29 @@ void spec_ranks(const char* spec, int& rx, int& ry) {
     }
 }
 
+struct Model {
+    uint64_t latency = 0, mem_limit = 0, mem_weight = 0;
+    int64_t min_block = 0, task_multiple = 0;
+};
+
+// the node's memory under D: its output plus the join's partials when they are aggregated
+uint64_t node_memory(const Plan& p, const int32_t* D) {
+    uint64_t tasks = 1, n_agg = 1, z_sub = 1;
+    for (int l = 0; l < p.n_labels; ++l) {
+        tasks *= (uint64_t)D[l];
+        if (p.role[l] == kK) n_agg *= (uint64_t)D[l];
+    }
+    for (int i = 0; i < p.Z.rank; ++i) z_sub *= (uint64_t)(p.B[p.Z.label[i]] / D[p.Z.label[i]]);
+    return (uint64_t)p.Z.total + (n_agg > 1 ? tasks * z_sub : 0);
+}
+
 void enumerate(const Plan& p, int l, Candidate& c, uint64_t prod, int64_t p_min, int64_t p_max, bool pow2,
-               std::vector<Candidate>& out, bool& overflow) {
+               const Model& m, std::vector<Candidate>& out, bool& overflow) {
     if (overflow) return;
     if (l == p.n_labels) {
         if (prod < (uint64_t)p_min) return;
+        if (m.task_multiple > 1 && prod % (uint64_t)m.task_multiple) return;
+        if (m.mem_limit && node_memory(p, c.D) > m.mem_limit) return;
         if (out.size() >= kMaxCandidates) {
             overflow = true;
             return;
@@ -57,16 +79,18 @@ void enumerate(const Plan& p, int l, Candidate& c, uint64_t prod, int64_t p_min,
         return;
     }
     const int64_t B = p.B[l];
+    const int64_t gmin = m.min_block > 1 ? (m.min_block < B ? m.min_block : B) : 1;
     for (int64_t D = 1; D <= B; ++D) {
         if (B % D) continue;
         if (pow2 && (D & (D - 1))) continue;
         if (prod * (uint64_t)D > (uint64_t)p_max) break;
+        if (B / D < gmin) break;  // block extents only shrink as D grows
         c.D[l] = (int32_t)D;
-        enumerate(p, l + 1, c, prod * (uint64_t)D, p_min, p_max, pow2, out, overflow);
+        enumerate(p, l + 1, c, prod * (uint64_t)D, p_min, p_max, pow2, m, out, overflow);
     }
 }
 
-uint64_t node_cost(const Plan& p, const int32_t* D) {
+uint64_t node_cost(const Plan& p, const int32_t* D, const Model& m) {
     uint64_t tasks = 1, x_sub = 1, y_sub = 0, z_sub = 1, n_agg = 1;
     for (int l = 0; l < p.n_labels; ++l) {
         tasks *= (uint64_t)D[l];
@@ -78,13 +102,16 @@ uint64_t node_cost(const Plan& p, const int32_t* D) {
         for (int i = 0; i < p.Y.rank; ++i) y_sub *= (uint64_t)(p.B[p.Y.label[i]] / D[p.Y.label[i]]);
     }
     for (int i = 0; i < p.Z.rank; ++i) z_sub *= (uint64_t)(p.B[p.Z.label[i]] / D[p.Z.label[i]]);
-    return tasks * (x_sub + y_sub) + (tasks / n_agg) * (n_agg - 1) * z_sub;
+    uint64_t c = tasks * (x_sub + y_sub) + (tasks / n_agg) * (n_agg - 1) * z_sub;
+    if (m.latency) c += m.latency * (tasks * (p.unary ? 1u : 2u) + (tasks / n_agg) * (n_agg - 1));
+    if (m.mem_weight) c += m.mem_weight * node_memory(p, D);
+    return c;
 }
 
 const Operand& input_operand(const Plan& p, int k) { return k == 0 ? p.X : p.Y; }
 
 // Repartition cost of producer u's output (candidate cu) into consumer v's input k (candidate cv).
-uint64_t edge_cost(const Plan& u, const Candidate& cu, const Plan& v, int k, const Candidate& cv) {
+uint64_t edge_cost(const Plan& u, const Candidate& cu, const Plan& v, int k, const Candidate& cv, const Model& m) {
     const Operand& in = input_operand(v, k);
     int64_t shape[TRA_MAX_RANK];
     int32_t src[TRA_MAX_RANK], dst[TRA_MAX_RANK];
@@ -93,7 +120,9 @@ uint64_t edge_cost(const Plan& u, const Candidate& cu, const Plan& v, int k, con
         dst[i] = cv.D[in.label[i]];
         src[i] = cu.D[u.Z.label[i]];
     }
-    return repartition_cost_elems(in.rank, shape, src, dst);
+    uint64_t c = repartition_cost_elems(in.rank, shape, src, dst);
+    if (m.latency && c) c += m.latency * repartition_messages(in.rank, shape, src, dst);
+    return c;
 }
 
 }  // namespace
@@ -102,11 +131,21 @@ uint64_t edge_cost(const Plan& u, const Candidate& cu, const Plan& v, int k, con
 using namespace tra;
 
 extern "C" int ein_graph_decompose(const tra_graph_node* nodes, int n_nodes, int64_t p_min, int64_t p_max, int flags,
-                                   int32_t* d_out, int n_d_out, uint64_t* node_cost_out, tra_graph_result* result) {
+                                   const tra_cost_model* model, int32_t* d_out, int n_d_out, uint64_t* node_cost_out,
+                                   tra_graph_result* result) {
     clear_error();
     if (!nodes || n_nodes < 1 || !d_out || !result) return fail(TRA_ERR_ARG, "NULL argument or empty graph");
     if (p_min < 1 || p_max < p_min) return fail(TRA_ERR_ARG, "task bounds must satisfy 1 <= p_min <= p_max");
     const bool pow2 = (flags & TRA_DP_POW2) != 0;
+    Model m;
+    if (model) {
+        if (model->min_block < 0 || model->task_multiple < 0) return fail(TRA_ERR_ARG, "negative cost-model parameter");
+        m.latency = model->latency;
+        m.min_block = model->min_block;
+        m.mem_limit = model->mem_limit;
+        m.mem_weight = model->mem_weight;
+        m.task_multiple = model->task_multiple;
+    }
     std::vector<Node> g(n_nodes);
     int d_total = 0;
     for (int v = 0; v < n_nodes; ++v) {
@@ -136,12 +175,12 @@ extern "C" int ein_graph_decompose(const tra_graph_node* nodes, int n_nodes, int
         Candidate c;
         memset(&c, 0, sizeof(c));
         bool overflow = false;
-        enumerate(p, 0, c, 1, p_min, p_max, pow2, g[v].cand, overflow);
+        enumerate(p, 0, c, 1, p_min, p_max, pow2, m, g[v].cand, overflow);
         if (overflow) return fail(TRA_ERR_UNSUPPORTED, "node %d: more than %zu candidate partition vectors", v, kMaxCandidates);
         if (g[v].cand.empty())
-            return fail(TRA_ERR_UNSUPPORTED, "node %d: no partition vector gives %lld..%lld tasks", v, (long long)p_min,
-                        (long long)p_max);
-        for (Candidate& cc : g[v].cand) cc.cost = node_cost(p, cc.D);
+            return fail(TRA_ERR_UNSUPPORTED, "node %d: no partition vector gives %lld..%lld tasks under the cost model",
+                        v, (long long)p_min, (long long)p_max);
+        for (Candidate& cc : g[v].cand) cc.cost = node_cost(p, cc.D, m);
     }
     if (n_d_out != d_total) return fail(TRA_ERR_ARG, "d_out holds %d entries, the graph needs %d", n_d_out, d_total);
 
@@ -162,7 +201,7 @@ extern "C" int ein_graph_decompose(const tra_graph_node* nodes, int n_nodes, int
                 uint64_t best = std::numeric_limits<uint64_t>::max();
                 int best_i = 0;
                 for (size_t cu = 0; cu < nu.cand.size(); ++cu) {
-                    const uint64_t t = nu.dp[cu] + edge_cost(nu.plan, nu.cand[cu], nv.plan, k, nv.cand[c]);
+                    const uint64_t t = nu.dp[cu] + edge_cost(nu.plan, nu.cand[cu], nv.plan, k, nv.cand[c], m);
                     if (t < best) {
                         best = t;
                         best_i = (int)cu;
@@ -199,7 +238,7 @@ extern "C" int ein_graph_decompose(const tra_graph_node* nodes, int n_nodes, int
         uint64_t own = cv.cost;
         for (int k = 0; k < 2; ++k) {
             const int u = nodes[v].input[k];
-            if (u >= 0) own += edge_cost(g[u].plan, g[u].cand[choice[u]], p, k, cv);
+            if (u >= 0) own += edge_cost(g[u].plan, g[u].cand[choice[u]], p, k, cv, m);
         }
         total += own;
         if (node_cost_out) node_cost_out[v] = own;

@@ -70,6 +70,39 @@ uint64_t repartition_cost_elems(int rank, const int64_t* shape, const int32_t* s
     return total - stay;
 }
 
+uint64_t repartition_messages(int rank, const int64_t* shape, const int32_t* src_d, const int32_t* dst_d) {
+    // overlapping (source block, destination block) pairs: per dimension the union of the two
+    // sets of block boundaries cuts [0, B) into Ds + Dd - gcd(Ds, Dd) segments, one per pair;
+    // minus the pairs whose two blocks have the same linear id (nothing moves between them)
+    uint64_t pairs = 1, ns = 1, nd = 1;
+    for (int i = 0; i < rank; ++i) {
+        uint64_t a = (uint64_t)src_d[i], b = (uint64_t)dst_d[i];
+        while (b) {
+            const uint64_t t = a % b;
+            a = b;
+            b = t;
+        }
+        pairs *= (uint64_t)src_d[i] + (uint64_t)dst_d[i] - a;
+        ns *= (uint64_t)src_d[i];
+        nd *= (uint64_t)dst_d[i];
+    }
+    uint64_t same = 0;
+    const uint64_t n = ns < nd ? ns : nd;
+    for (uint64_t L = 0; L < n; ++L) {
+        uint64_t ls = L, ld = L;
+        bool meet = true;
+        for (int i = rank - 1; i >= 0 && meet; --i) {
+            const uint64_t ks = ls % (uint64_t)src_d[i], kd = ld % (uint64_t)dst_d[i];
+            ls /= (uint64_t)src_d[i];
+            ld /= (uint64_t)dst_d[i];
+            const uint64_t bs = (uint64_t)shape[i] / src_d[i], bd = (uint64_t)shape[i] / dst_d[i];
+            meet = ks * bs < (kd + 1) * bd && kd * bd < (ks + 1) * bs;
+        }
+        same += meet;
+    }
+    return pairs - same;
+}
+
 Plan::~Plan() {
     if (tc) tc_free(tc);
     delete inner;
@@ -314,6 +347,11 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
     const uint64_t xs = (uint64_t)p->X.sub, ys = p->unary ? 0 : (uint64_t)p->Y.sub, zs = (uint64_t)p->Z.sub;
     p->cost_join = p->n_tasks * (xs + ys);
     p->cost_agg = (p->n_tasks / p->n_agg) * (p->n_agg - 1) * zs;
+    // cost-model variants: one message per sub-tensor moved, and the node's memory (its output
+    // plus the join's partial results when they are aggregated)
+    p->msg_join = p->n_tasks * (p->unary ? 1u : 2u);
+    p->msg_agg = (p->n_tasks / p->n_agg) * (p->n_agg - 1);
+    p->mem_elems = (uint64_t)p->Z.total + (p->n_agg > 1 ? p->n_tasks * zs : 0);
 
     // kernel choice and workspace
     p->ws_bytes = 0;

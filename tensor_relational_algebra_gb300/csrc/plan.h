@@ -60,6 +60,7 @@ struct Plan {
 
     uint64_t n_tasks = 0, n_groups = 0, n_agg = 0;
     uint64_t cost_join = 0, cost_agg = 0;
+    uint64_t msg_join = 0, msg_agg = 0, mem_elems = 0;
     int kernel = 0;
     uint64_t ws_bytes = 0;
 
@@ -100,6 +101,7 @@ int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_
 uint64_t align256(uint64_t v);
 inline uint64_t split3_pad(uint64_t v, uint64_t q) { return (v + q - 1) / q * q; }
 uint64_t repartition_cost_elems(int rank, const int64_t* shape, const int32_t* src_d, const int32_t* dst_d);
+uint64_t repartition_messages(int rank, const int64_t* shape, const int32_t* src_d, const int32_t* dst_d);
 
 // Exhaustive host check of the semiring kernel's 4-wide loads: an operand may load
 // 4 consecutive indices of a role at once only if every 4-aligned group of that role

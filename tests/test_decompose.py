@@ -112,3 +112,93 @@ def test_attention_eingraph_full_size(lib):
         assert edge >= 0
         total += own
     assert total == r["total_cost"]
+
+
+# ---------------------------------------------------------------- cost-model variants (page section 4.3)
+
+@pytest.mark.parametrize("shape,src,dst,want", [
+    # [0,2),[2,4) -> [0,1),[1,2),[2,3),[3,4): overlapping pairs (0,0),(0,1),(1,2),(1,3); (0,0) keeps
+    # its id -> 3 messages
+    ([4], [2], [4], 3),
+    # [0,3),[3,6) -> [0,2),[2,4),[4,6): pairs (0,0),(0,1),(1,1),(1,2); same-id (0,0),(1,1) -> 2
+    ([6], [2], [3], 2),
+    # row halves -> column halves of a 4 x 4: all four pairs overlap, ids 0->0 and 1->1 stay -> 2
+    ([4, 4], [2, 1], [1, 2], 2),
+    ([8, 6], [2, 3], [2, 3], 0),  # unchanged partition: nothing moves
+])
+def test_repartition_messages_hand_derived(lib, shape, src, dst, want):
+    assert odec.repartition_messages_bruteforce(shape, src, dst) == want
+    assert lib.repartition_messages(shape, src, dst) == want
+
+
+def test_repartition_messages_match_bruteforce(lib):
+    import numpy as np
+
+    rng = np.random.default_rng(5)
+    for _ in range(60):
+        rank = int(rng.integers(1, 4))
+        shape = [int(v) for v in rng.choice([2, 3, 4, 6, 8, 12], size=rank)]
+        divs = lambda n: [v for v in range(1, n + 1) if n % v == 0]  # noqa: E731
+        src = [int(rng.choice(divs(n))) for n in shape]
+        dst = [int(rng.choice(divs(n))) for n in shape]
+        assert lib.repartition_messages(shape, src, dst) == odec.repartition_messages_bruteforce(shape, src, dst), \
+            (shape, src, dst)
+
+
+@pytest.mark.parametrize("eq,bounds,d", [
+    ("ij,jk->ik", [4, 6, 4], [2, 3, 3, 2]),
+    ("ij,jk->ik", [4, 6, 4], [4, 1, 1, 2]),
+    ("abef,cfed->abcd", [2, 2, 2, 4, 2, 2], [1, 2, 2, 2, 2, 2, 2, 1]),
+    ("hst->hs", [2, 4, 6], [2, 2, 3]),
+    ("i,j->ij", [4, 6], [2, 3]),
+])
+def test_plan_messages_and_memory_match_bruteforce(lib, eq, bounds, d):
+    spec = eq + (":mul:sum" if "," in eq and "->ij" not in eq else "::sum" if "," not in eq else ":mul:none")
+    p = lib.Plan(spec, bounds, d)
+    _, D = _tasks(eq, bounds, d)
+    assert p.msg_join + p.msg_agg == odec.node_messages(eq, bounds, D)
+    assert p.mem_elems == odec.node_memory(eq, bounds, D)
+
+
+MODELS = [
+    {"latency": 3},
+    {"min_block": 2},
+    {"mem_weight": 2},
+    {"mem_limit": 40},
+    {"task_multiple": 4},
+    {"latency": 5, "min_block": 2, "mem_weight": 1, "task_multiple": 2},
+]
+
+
+@pytest.mark.parametrize("model", MODELS, ids=lambda m: ",".join(f"{k}={v}" for k, v in m.items()))
+@pytest.mark.parametrize("graph", [CHAIN, TREE], ids=["chain", "binary-tree"])
+def test_variants_match_exhaustive_search(lib, graph, model):
+    p_min, p_max = 2, 8
+    r = lib.decompose(graph, p_min, p_max, model=model)
+    best, _ = odec.search(graph, p_min, p_max, model=model)
+    assert r["total_cost"] == best
+    eqs = [(s.split(":")[0], b, i) for s, b, i in graph]
+    choice = [_tasks(eq, b, d)[1] for (eq, b, _), d in zip(eqs, r["d"])]
+    assert odec.graph_cost(eqs, choice, model) == r["total_cost"]
+    for (eq, b, _), d in zip(eqs, r["d"]):
+        n, D = _tasks(eq, b, d)
+        assert D in odec.candidates(eq, b, p_min, p_max, model=model)
+
+
+def test_variant_terms_take_effect(lib):
+    # the latency and memory terms raise the optimum by at least their smallest possible value
+    base = lib.decompose(CHAIN, 2, 8)["total_cost"]
+    assert lib.decompose(CHAIN, 2, 8, model={"latency": 7})["total_cost"] >= base + 7 * 3 * 2 * 2
+    # outputs of 4x4, 4x2 and 4x4 elements: at least 40 of memory (partials only add)
+    assert lib.decompose(CHAIN, 2, 8, model={"mem_weight": 1})["total_cost"] >= base + 16 + 8 + 16
+    # minimum granularity equal to the bounds leaves one task per node
+    with pytest.raises(lib.TraError) as e:
+        lib.decompose(CHAIN, 2, 8, model={"min_block": 4})
+    assert "TRA_ERR_UNSUPPORTED" in str(e.value)
+    r = lib.decompose(CHAIN, 1, 8, model={"min_block": 4})
+    assert all(v == 1 for d in r["d"] for v in d)
+    # a memory limit below every output prunes everything
+    with pytest.raises(lib.TraError):
+        lib.decompose(CHAIN, 2, 8, model={"mem_limit": 8})
+    with pytest.raises(ValueError):
+        lib.decompose(CHAIN, 2, 8, model={"latncy": 1})
