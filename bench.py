@@ -360,17 +360,19 @@ class C3Workload(_PointsWorkload):
 
 class C4Workload(_PointsWorkload):
     name = "multi-head attention EinGraph s=4096 a=4096 h=32 d=128, BF16 activations N(0,1), weights N(0,0.02)"
-    d = "projections all-ones; scores/lse/exp/A.V split h=32; repartitions between"
+    d = "projections split h=32 (head-major outputs); scores/lse/exp/A.V split h=32; repartition of O to dense"
     cpu_default = 256
 
     def host_inputs(self):
         s, a, h, d = 4096, 4096, 32, 128
         o = self.seed_offset
-        return ([_bf16_host((s, a), 0 + o, t) for t in range(3)] +
-                [_bf16_host((a, h, d), 0 + o, 3 + t, 0.02) for t in range(4)])
+        ws = [_bf16_host((a, h, d), 0 + o, 3 + t, 0.02) for t in range(4)]
+        # W_Q, W_K, W_V as the projections' relations under [1, h, 1]: stored [h][a][d]
+        ws[:3] = [np.ascontiguousarray(w.reshape(a, h, d).transpose(1, 0, 2)).reshape(-1) for w in ws[:3]]
+        return [_bf16_host((s, a), 0 + o, t) for t in range(3)] + ws
 
     def setup(self, tra, torch, inputs):
-        from tensor_relational_algebra_gb300.attention import AttentionGraph
+        from tensor_relational_algebra_gb300.eingraph import AttentionGraph
 
         self.g = AttentionGraph(4096, 4096, 32, 128)
         self.dev = [_dev_bf16(torch, x) for x in inputs]
@@ -384,7 +386,8 @@ class C4Workload(_PointsWorkload):
     def oracle_sample(self, inputs, r0, n):
         from datagen import bf16_bits_to_f32
 
-        Q, WQ = bf16_bits_to_f32(inputs[0]).astype(np.float64), bf16_bits_to_f32(inputs[3]).astype(np.float64)
+        Q = bf16_bits_to_f32(inputs[0]).astype(np.float64)
+        WQ = bf16_bits_to_f32(inputs[3]).astype(np.float64).reshape(32, 4096, 128).transpose(1, 0, 2)  # dense [a][h][d]
         self.oracle_points("sa,ahd->shd", Q, WQ, "mul", "sum", (4096, 32, 128), r0, n)
         return 2 * n * 4096
 
@@ -395,10 +398,10 @@ class C4Workload(_PointsWorkload):
 class C4fWorkload(C4Workload):
     name = ("multi-head attention EinGraph s=4096 a=4096 h=32 d=128, BF16 activations N(0,1), weights N(0,0.02), "
             "Scores -> L -> exp -> A.V -> repartition O fused in one kernel")
-    d = "projections all-ones; fused attention split over (s/128 row blocks) x h; repartitions of Q/K/V before"
+    d = "projections split h=32 (head-major outputs); fused attention over (s/128 row blocks) x h"
 
     def setup(self, tra, torch, inputs):
-        from tensor_relational_algebra_gb300.attention import AttentionGraph
+        from tensor_relational_algebra_gb300.eingraph import AttentionGraph
 
         self.g = AttentionGraph(4096, 4096, 32, 128, fused=True)
         self.dev = [_dev_bf16(torch, x) for x in inputs]

@@ -1,8 +1,7 @@
 """The multi-head-attention EinGraph of "EinDecomp ... tensor relational algebra" section 2.1,
 run node by node through the C ABI (one ein_execute or ein_repartition per node).
 
-  Q_proj[s,h,d] = sum_a Q[s,a] W_Q[a,h,d]        (K, V alike)        d = all ones
-  repartition   Q/K/V_proj [1,1,1] -> [1,h,1]                         (head-major relations)
+  Q_proj[s,h,d] = sum_a Q[s,a] W_Q[a,h,d]        (K, V alike)        h split h ways
   S[h,s,t]      = (1/sqrt(d)) sum_d Q_proj[s,h,d] K_proj[t,h,d]        split h ways
   L[h,s]        = logsumexp_t S[h,s,t]                                 split h ways
   A[h,s,t]      = exp(S[h,s,t] - L[h,s])                               split h ways (bf16)
@@ -12,6 +11,12 @@ run node by node through the C ABI (one ein_execute or ein_repartition per node)
 
 The printed Scores[h,s,s] is read with a second sequence index t; the scale is applied
 after the sum over d; there is no mask.  Buffers are allocated once (torch) and reused.
+
+The projections take the partition vector that splits h (X = Q: [1, 1]; Y = W_Q: [1, h, 1]), as
+EinDecomp's search would pick to avoid a repartition: their output relation under [1, h, 1] is
+the head-major layout the next nodes read.  W_Q, W_K and W_V are therefore passed as relations
+under [1, h, 1] (stored [h][a][d]; projection_weight converts a dense [a][h][d] weight); W_O is
+dense [a][h][d].
 
 With fused=True the four nodes Scores -> L -> A -> O and the repartition of O run as one
 kernel (ein_attention), which writes O dense and L, never the scores or A.
@@ -30,7 +35,7 @@ class AttentionGraph:
         self.s, self.a, self.h, self.d = s, a, h, d
         self.fused = fused
         t = s
-        self.p_proj = Plan("sa,ahd->shd:mul:sum:in=bf16:out=bf16", [s, a, h, d], [1, 1, 1, 1, 1])
+        self.p_proj = Plan("sa,ahd->shd:mul:sum:in=bf16:out=bf16", [s, a, h, d], [1, 1, 1, h, 1])
         self.p_scores = Plan(f"shd,thd->hst:mul:sum:in=bf16:alpha={1.0 / math.sqrt(d)!r}", [s, h, d, t],
                              [1, h, 1, 1, h, 1])
         self.p_lse = Plan("hst->hs::lse", [h, s, t], [h, 1, 1])
@@ -39,8 +44,7 @@ class AttentionGraph:
         self.p_out = Plan("shd,ahd->sa:mul:sum:in=bf16", [s, h, d, a], [1, 1, 1, 1, 1, 1])
         bf, f32 = torch.bfloat16, torch.float32
         e = lambda n, dt: torch.empty(n, dtype=dt, device=device)  # noqa: E731
-        self.qp, self.kp, self.vp = e(s * h * d, bf), e(s * h * d, bf), e(s * h * d, bf)
-        self.qr, self.kr, self.vr = e(s * h * d, bf), e(s * h * d, bf), e(s * h * d, bf)
+        self.qp, self.kp, self.vp = e(s * h * d, bf), e(s * h * d, bf), e(s * h * d, bf)  # [h][s][d]
         self.S = None if fused else e(h * s * t, f32)
         self.L = e(h * s, f32)
         self.A = None if fused else e(h * s * t, bf)
@@ -58,25 +62,29 @@ class AttentionGraph:
             ("proj Q", lambda: self.p_proj.execute(Q, WQ, self.qp), gemm, "flop", "tensor", 1),
             ("proj K", lambda: self.p_proj.execute(K, WK, self.kp), gemm, "flop", "tensor", 1),
             ("proj V", lambda: self.p_proj.execute(V, WV, self.vp), gemm, "flop", "tensor", 1),
-            ("repartition QKV -> head-major", lambda: (repartition(self.qp, self.qr, shd, [1, 1, 1], [1, h, 1]),
-                                                        repartition(self.kp, self.kr, shd, [1, 1, 1], [1, h, 1]),
-                                                        repartition(self.vp, self.vr, shd, [1, 1, 1], [1, h, 1])),
-             3 * 2 * s * h * d * 2, "bytes", "hbm", 3),
         ] + ([
             ("attention (Scores -> L -> exp -> A.V fused)",
-             lambda: attention(self.qr, self.kr, self.vr, self.O, s, s, h, d, lse=self.L),
+             lambda: attention(self.qp, self.kp, self.vp, self.O, s, s, h, d, lse=self.L),
              2 * att, "flop", "tensor", 1),
         ] if self.fused else [
-            ("scores", lambda: self.p_scores.execute(self.qr, self.kr, self.S), att, "flop", "tensor", 1),
+            ("scores", lambda: self.p_scores.execute(self.qp, self.kp, self.S), att, "flop", "tensor", 1),
             ("logsumexp", lambda: self.p_lse.execute(self.S, None, self.L), h * s * s * 4 + h * s * 4, "bytes", "hbm", 1),
             ("exp(S-L)", lambda: self.p_exp.execute(self.S, self.L, self.A), h * s * s * (4 + 2) + h * s * 4, "bytes",
              "hbm", 1),
-            ("A.V", lambda: self.p_pv.execute(self.A, self.vr, self.Oh), att, "flop", "tensor", 1),
+            ("A.V", lambda: self.p_pv.execute(self.A, self.vp, self.Oh), att, "flop", "tensor", 1),
             ("repartition O -> dense", lambda: repartition(self.Oh, self.O, shd, [1, h, 1], [1, 1, 1]),
              2 * s * h * d * 2, "bytes", "hbm", 1),
         ]) + [
             ("out proj", lambda: self.p_out.execute(self.O, WO, self.out), gemm, "flop", "tensor", 1),
         ]
+
+    def projection_weight(self, W):
+        """The relation under [1, h, 1] of a dense [a][h][d] projection weight (device bf16)."""
+        import torch
+
+        out = torch.empty_like(W)
+        repartition(W, out, [self.a, self.h, self.d], [1, 1, 1], [1, self.h, 1])
+        return out
 
     def __call__(self, Q, K, V, WQ, WK, WV, WO):
         for n in self.nodes(Q, K, V, WQ, WK, WV, WO):

@@ -70,7 +70,7 @@ def test_fused_attention_growing_and_falling_block_maxima(lib, cuda, factors):
 def test_fused_node_in_the_attention_eingraph(lib, cuda):
     import torch
 
-    from tensor_relational_algebra_gb300.attention import AttentionGraph
+    from tensor_relational_algebra_gb300.eingraph import AttentionGraph
 
     s, a, h, d = 512, 256, 2, 128
     acts = [datagen.normal_bf16((s, a), 41, t) for t in range(3)]
@@ -78,6 +78,7 @@ def test_fused_node_in_the_attention_eingraph(lib, cuda):
     dev = [torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda().reshape(-1) for b in acts + ws]
     unfused = AttentionGraph(s, a, h, d)
     fused = AttentionGraph(s, a, h, d, fused=True)
+    dev[3:6] = [unfused.projection_weight(w) for w in dev[3:6]]  # relations under [1, h, 1]
     unfused(*dev)
     fused(*dev)
     torch.cuda.synchronize()

@@ -27,11 +27,12 @@ def _to_dev(torch, bits):
 def test_attention_step_graph_replay(lib, cuda):
     import torch
 
-    from tensor_relational_algebra_gb300.attention import AttentionGraph
+    from tensor_relational_algebra_gb300.eingraph import AttentionGraph
 
     s, a, h, d = 512, 256, 2, 128
     g = AttentionGraph(s, a, h, d)
     dev = _to_dev(torch, _inputs(s, a, h, d, 31))
+    dev[3:6] = [g.projection_weight(w) for w in dev[3:6]]  # relations under [1, h, 1]
     nodes = g.nodes(*dev)
 
     def step():
@@ -59,6 +60,7 @@ def test_attention_step_graph_replay(lib, cuda):
 
     # new inputs written into the captured buffers: the replay follows them
     fresh = _to_dev(torch, _inputs(s, a, h, d, 32))
+    fresh[3:6] = [g.projection_weight(w) for w in fresh[3:6]]
     for dst, src in zip(dev, fresh):
         dst.copy_(src)
     graph.replay()

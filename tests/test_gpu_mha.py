@@ -26,10 +26,11 @@ def inputs(s, a, h, d, seed):
 def run_gpu(lib, bits, s, a, h, d):
     import torch
 
-    from tensor_relational_algebra_gb300.attention import AttentionGraph
+    from tensor_relational_algebra_gb300.eingraph import AttentionGraph
 
     g = AttentionGraph(s, a, h, d)
     dev = [torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda().reshape(-1) for b in bits]
+    dev[3:6] = [g.projection_weight(w) for w in dev[3:6]]  # W_Q, W_K, W_V as relations under [1, h, 1]
     g(*dev)
     lib.ein_status()
     torch.cuda.synchronize()
@@ -45,9 +46,9 @@ def test_attention_small_every_node(lib, cuda):
     bits = inputs(s, a, h, d, 21)
     g = run_gpu(lib, bits, s, a, h, d)
     ref = mha.chain(*[f32(b) for b in bits], engine="blas")
-    # projections (dense [s,h,d]); head-major relations (repartitioned) match the dense ones
-    check_bf16_bar(as_f64(from_dev(g.qp)).reshape(s, h, d), ref["Qp"])
-    check_bf16_bar(as_f64(otra.unblock(from_dev(g.kr), (s, h, d), [1, h, 1])), ref["Kp"])
+    # projections: head-major relations under [1, h, 1] (h split in the projection's d)
+    check_bf16_bar(as_f64(otra.unblock(from_dev(g.qp), (s, h, d), [1, h, 1])), ref["Qp"])
+    check_bf16_bar(as_f64(otra.unblock(from_dev(g.kp), (s, h, d), [1, h, 1])), ref["Kp"])
     check_bf16_bar(as_f64(from_dev(g.S)).reshape(h, s, s), ref["S"])
     check_bf16_bar(as_f64(from_dev(g.L)).reshape(h, s), ref["L"])
     A = as_f64(from_dev(g.A)).reshape(h, s, s)

@@ -195,3 +195,14 @@ def test_execute_argument_errors(lib):
     with pytest.raises(lib.TraError) as e:
         lib.ein_repartition([6, 4], [1, 1], [2, 1], 3, 0x1000, 0x2000, 0)
     assert "TRA_ERR_ARG" in str(e.value)
+
+
+def test_attention_function_survives_the_eingraph_import(lib):
+    # the attention-EinGraph module is imported beside the package-level attention() call; the
+    # import must not rebind the name
+    import types
+
+    import tensor_relational_algebra_gb300.eingraph  # noqa: F401
+
+    assert callable(lib.attention) and not isinstance(lib.attention, types.ModuleType)
+
