@@ -95,7 +95,11 @@ enum {
     TRA_KERNEL_LSE_FACTORED = 5,  /* logsumexp of a sum: max-shifted exp, then sum-of-products */
     TRA_KERNEL_LITERAL = 6,       /* one partial per join tuple, then ordered combine */
     TRA_KERNEL_TC_BF16_PAIR = 7,  /* as TC_BF16, one 256 x 256 tile per cluster of two CTAs */
-    TRA_KERNEL_TC_SPLIT3 = 8      /* split=bf16x3: squared distance / logsumexp on tensor cores */
+    TRA_KERNEL_TC_SPLIT3 = 8,     /* split=bf16x3: squared distance / logsumexp on tensor cores */
+    TRA_KERNEL_EMPTY = 9,         /* an output label has extent 0: there is nothing to compute */
+    TRA_KERNEL_FILL = 10          /* a contracted label has extent 0: every output aggregates an
+                                     empty set, i.e. is agg's identity (0 for sum, -inf for max and
+                                     lse, +inf for min) times alpha */
 };
 
 /* ein_plan -- build the TRA plan of one EinSum under partition vector d
@@ -115,6 +119,10 @@ enum {
  *         tc_n=256|128 (width of the pair tile; by default 256 where the columns
  *         allow, else 128), tc_store=tma|lsu (tensor-core epilogue: TMA stores
  *         through an output tensor map, the default where one fits, or warp stores),
+ *         ksplit=auto|off (tensor-core path: by default the tiles of a last, partly
+ *         filled wave of the persistent grid have their K loop split into 2-4 runs on
+ *         otherwise idle SMs, the partial sums kept in the workspace and added in a fixed
+ *         order, so results stay deterministic; off keeps one worker per tile),
  *         split=bf16x3|none (fp32 "sqdiff:sum" and "add:lse" only: the squared-distance
  *         expansion |x|^2 + |y|^2 - 2 x.y, or the factored logsumexp
  *         mx + my + log sum e^(x-mx) e^(y-my), with the sum of products on BF16 tensor cores,
@@ -122,7 +130,10 @@ enum {
  *         hi.hi + hi.lo + lo.hi; per product the relative error is at most 3 * 2^-16.
  *         Default none: these semirings run on CUDA cores).
  * bounds: B_l for every distinct label in first-appearance order (X then Y);
- *         n_bounds must equal the number of distinct labels.
+ *         n_bounds must equal the number of distinct labels.  0 <= B_l < 2^31; an
+ *         extent of 0 gives an empty EinSum (kernel TRA_KERNEL_EMPTY or _FILL: the key
+ *         space, task counts and cost terms are still those of the formulas, with
+ *         sub-tensors of 0 elements).
  * d:      partition counts per operand index position, X's then Y's (n_d =
  *         rank_x + rank_y).  A label shared by X and Y must get equal counts.
  * out:    receives the plan; release it with ein_plan_destroy.
@@ -142,8 +153,12 @@ int ein_plan_keys(tra_plan_t plan, int32_t* xyz_keys, int64_t capacity);
 /* ein_execute -- run the plan: join key-matched sub-tensors through op and aggregate
  * with agg (section 2.2).  in0/in1/out are device buffers in the relation layout of
  * the plan's d (in1 = NULL for a unary EinSum); element types per the in=/out=
- * options.  workspace: device scratch of at least info.workspace_bytes (may be NULL
- * when that is 0); it is overwritten.  Asynchronous on stream.
+ * options (in0, in1 may be NULL for an empty plan, out too when the output has no
+ * elements).  workspace: device scratch of at least info.workspace_bytes (may be NULL
+ * when that is 0); it is overwritten.  Asynchronous on stream.  Calls that may overlap
+ * on the GPU need separate workspaces.  Tensor-core plans size their workspace at
+ * ein_plan for the device current then (partial sums and flags of the K-split tiles,
+ * see ksplit); on another device they run without the split when it does not fit.
  * Errors: TRA_ERR_ARG, TRA_ERR_WORKSPACE, TRA_ERR_CUDA (launch failure). */
 int ein_execute(tra_plan_t plan, const void* in0, const void* in1, void* out, void* workspace,
                 size_t workspace_bytes, tra_stream_t stream);
@@ -151,6 +166,7 @@ int ein_execute(tra_plan_t plan, const void* in0, const void* in1, void* out, vo
 /* ein_repartition -- section 2.2 repartition: copy a tensor of the given shape from the
  * relation layout under src_d to the relation layout under dst_d (either may be all
  * ones = dense row-major).  elem_bytes in {1,2,4,8}.  src and dst must not overlap.
+ * An extent may be 0 (nothing is copied; src and dst may then be NULL).
  * Asynchronous on stream.  Errors: TRA_ERR_RANK, TRA_ERR_DIVISIBILITY, TRA_ERR_ARG,
  * TRA_ERR_CUDA. */
 int ein_repartition(int rank, const int64_t* shape, const int32_t* src_d, const int32_t* dst_d, int elem_bytes,

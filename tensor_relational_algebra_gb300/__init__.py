@@ -29,7 +29,7 @@ ERRORS = {
     -5: "TRA_ERR_UNSUPPORTED", -6: "TRA_ERR_WORKSPACE", -7: "TRA_ERR_CUDA", -8: "TRA_ERR_TIMEOUT", -9: "TRA_ERR_ARG",
 }
 KERNELS = {1: "semiring_f32", 2: "tc_bf16", 3: "row_reduce", 4: "elementwise", 5: "lse_factored", 6: "literal",
-           7: "tc_bf16_pair", 8: "tc_split3"}
+           7: "tc_bf16_pair", 8: "tc_split3", 9: "empty", 10: "fill"}
 ROLES = {0: "batch", 1: "M", 2: "N", 3: "contracted"}
 
 

@@ -281,9 +281,17 @@ int execute_plan(const Plan& p, const void* x, const void* y, void* z, void* ws,
             e = launch_elementwise(ep, s);
             break;
         }
+        case TRA_KERNEL_EMPTY:
+            return TRA_OK;  // no output element
+        case TRA_KERNEL_FILL: {
+            // each output aggregates the empty set: agg's identity, then alpha, then one rounding
+            const double id = p.agg == kSum ? 0.0 : (p.agg == kMin ? HUGE_VAL : -HUGE_VAL);
+            e = launch_fill(z, (uint64_t)p.Z.total, (float)(p.alpha * id), p.out_bf16 != 0, s);
+            break;
+        }
         case TRA_KERNEL_TC_BF16:
         case TRA_KERNEL_TC_BF16_PAIR:
-            return tc_execute(p, x, y, z, s);
+            return tc_execute(p, x, y, z, s, nullptr, ws);
         case TRA_KERNEL_TC_SPLIT3: {
             // norms (squared distance) or row / column maxima (logsumexp) of the fp32 operands,
             // the hi / lo split into the GEMM's operands, the GEMM with the rank-one epilogue
@@ -359,7 +367,7 @@ int execute_plan(const Plan& p, const void* x, const void* y, void* z, void* ws,
 
 int check_partition(int rank, const int64_t* shape, const int32_t* d, const char* what) {
     for (int i = 0; i < rank; ++i) {
-        if (shape[i] < 1 || shape[i] > 0x7fffffffLL)
+        if (shape[i] < 0 || shape[i] > 0x7fffffffLL)
             return fail(TRA_ERR_ARG, "%s: extent %lld out of range", what, (long long)shape[i]);
         if (d[i] < 1 || shape[i] % d[i])
             return fail(TRA_ERR_DIVISIBILITY, "%s: D=%d does not divide B=%lld in dimension %d", what, d[i],
@@ -439,9 +447,14 @@ int ein_plan_keys(tra_plan_t plan, int32_t* xyz_keys, int64_t capacity) {
 int ein_execute(tra_plan_t plan, const void* in0, const void* in1, void* out, void* workspace, size_t ws_bytes,
                 tra_stream_t stream) {
     clear_error();
-    if (!plan || !in0 || !out) return fail(TRA_ERR_ARG, "NULL plan, input or output");
+    if (!plan) return fail(TRA_ERR_ARG, "NULL plan");
     const Plan& p = *reinterpret_cast<const Plan*>(plan);
-    if (!p.unary && !in1) return fail(TRA_ERR_ARG, "binary EinSum needs in1");
+    if (p.kernel == TRA_KERNEL_EMPTY) return TRA_OK;  // an output of no elements: nothing to read or write
+    if (!out) return fail(TRA_ERR_ARG, "NULL output");
+    if (p.kernel != TRA_KERNEL_FILL) {  // a fill reads no input
+        if (!in0) return fail(TRA_ERR_ARG, "NULL input");
+        if (!p.unary && !in1) return fail(TRA_ERR_ARG, "binary EinSum needs in1");
+    }
     if (p.ws_bytes && (!workspace || ws_bytes < p.ws_bytes))
         return fail(TRA_ERR_WORKSPACE, "workspace of %llu bytes needed, %llu given",
                     (unsigned long long)p.ws_bytes, (unsigned long long)(workspace ? ws_bytes : 0));
@@ -452,15 +465,18 @@ int ein_repartition(int rank, const int64_t* shape, const int32_t* src_d, const 
                     const void* src, void* dst, tra_stream_t stream) {
     clear_error();
     if (rank < 1 || rank > TRA_MAX_RANK) return fail(TRA_ERR_RANK, "rank %d outside 1..%d", rank, TRA_MAX_RANK);
-    if (!shape || !src_d || !dst_d || !src || !dst) return fail(TRA_ERR_ARG, "NULL argument");
+    if (!shape || !src_d || !dst_d) return fail(TRA_ERR_ARG, "NULL argument");
     if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8)
         return fail(TRA_ERR_ARG, "element size %d not in {1,2,4,8}", elem_bytes);
     int rc = check_partition(rank, shape, src_d, "source");
     if (rc == TRA_OK) rc = check_partition(rank, shape, dst_d, "destination");
     if (rc != TRA_OK) return rc;
+    for (int i = 0; i < rank; ++i)
+        if (shape[i] == 0) return TRA_OK;  // an extent of 0: nothing to copy
     int64_t total = 1;
-    for (int i = 0; i < rank; ++i) total *= shape[i];
+    for (int i = 0; i < rank; ++i) total = total >= 0x7fffffffLL ? total : total * shape[i];
     if (total >= 0x7fffffffLL) return fail(TRA_ERR_UNSUPPORTED, "tensors above 2^31-1 elements are not supported");
+    if (!src || !dst) return fail(TRA_ERR_ARG, "NULL buffer");
     if (((uintptr_t)src | (uintptr_t)dst) % elem_bytes) return fail(TRA_ERR_ARG, "misaligned buffer");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (total == 0) return TRA_OK;

@@ -618,6 +618,21 @@ cudaError_t launch_split3(const Split3Params& pin, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// Every element of z set to v (fp32, or bf16 rounded to nearest even): the outputs of an
+// EinSum whose contracted range is empty, each the identity of its aggregation times alpha.
+__global__ void fill_kernel(void* z, uint64_t n, float v, int bf16) {
+    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < n; i += (uint64_t)gridDim.x * blockDim.x) {
+        if (bf16) reinterpret_cast<__nv_bfloat16*>(z)[i] = __float2bfloat16_rn(v);
+        else reinterpret_cast<float*>(z)[i] = v;
+    }
+}
+
+cudaError_t launch_fill(void* z, uint64_t n, float v, bool bf16, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    fill_kernel<<<grid_for(n, 256), 256, 0, s>>>(z, n, v, bf16 ? 1 : 0);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
     const uint64_t total = p.n_groups * p.z_sub;
     if (total == 0) return cudaSuccess;

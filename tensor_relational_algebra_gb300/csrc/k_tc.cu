@@ -27,6 +27,8 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+#include <chrono>
 #include <cstring>
 #include <mutex>
 
@@ -82,7 +84,36 @@ struct TcParams {
     const float* col_term;
     uint32_t zM, zN;  // output rows / columns stored (M, N unless the operands are padded)
     int* mark_count;  // epilogue 2: incremented once per output marked NaN (may be null)
+    // Work units (see unit_of): tiles [0, n_full) whole; tiles [n_full, n_tiles) of the last,
+    // partly filled wave split into `split` runs of K steps on as many idle workers.  Parts
+    // 0 .. split-2 leave fp32 partial sums in `part`; each part waits for the one before it
+    // through one flag per (tile, epilogue warp), so the sum order is fixed.
+    uint32_t n_full, split, n_units;
+    float* part;                 // [tile - n_full][epilogue warp slot][column block][register][lane]
+    unsigned long long* flags;   // [tile - n_full][epilogue warp slot]: tag | parts done
+    unsigned long long tag;      // this launch's flag tag (the low 8 bits are zero)
 };
+
+constexpr uint32_t kWhole = 0xffffffffu;  // unit_of: the unit is a whole tile
+
+// Unit u -> its tile, its run of K steps [kb0, kb1) and its part (kWhole for a whole tile).
+// Worker w (CTA or CTA pair) takes units w, w + workers, ...; n_full is a multiple of the
+// worker count (or 0), so each worker owns at most one split unit, and it is its last.
+__device__ __forceinline__ void unit_of(const TcParams& p, uint32_t u, uint32_t& tile, uint32_t& kb0, uint32_t& kb1,
+                                        uint32_t& part) {
+    if (u < p.n_full) {
+        tile = u;
+        kb0 = 0;
+        kb1 = p.num_kb;
+        part = kWhole;
+        return;
+    }
+    const uint32_t v = u - p.n_full, j = v % p.split;
+    tile = p.n_full + v / p.split;
+    part = j;
+    kb0 = j * p.num_kb / p.split;
+    kb1 = (j + 1) * p.num_kb / p.split;
+}
 
 // ------------------------------------------------------------------ PTX wrappers (tc_ptx.h)
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, uint64_t timeout_ns) {
@@ -204,18 +235,32 @@ __device__ __forceinline__ void producer_steps(const CUtensorMap* map_a, const C
                                                uint32_t pw, uint32_t first_tile, uint32_t tile_step, uint32_t rank,
                                                uint32_t base, uint32_t full0, uint32_t empty0, volatile int* abort) {
     const uint32_t stage_bytes = p.a_bytes + p.b_bytes;
-    const uint32_t n_local = first_tile < p.n_tiles ? (p.n_tiles - first_tile + tile_step - 1) / tile_step : 0u;
-    const uint32_t total = n_local * p.num_kb;
+    // this worker's units: n_whole whole tiles, then at most one split unit (K steps skb0 .. skb1)
+    const uint32_t n_whole = first_tile < p.n_full ? (p.n_full - first_tile + tile_step - 1) / tile_step : 0u;
+    const uint32_t split_u = p.n_full + first_tile;
+    uint32_t stile = 0, skb0 = 0, skb1 = 0, spart = 0;
+    if (p.split > 1 && split_u < p.n_units) unit_of(p, split_u, stile, skb0, skb1, spart);
+    const uint32_t whole_steps = n_whole * p.num_kb;
+    const uint32_t total = whole_steps + (skb1 - skb0);
     uint32_t cur = 0xffffffffu;
     int fa[2][5], fbx[4][5];
     uint32_t pend_stage[2] = {0, 0}, pend_phase[2] = {0, 0}, n_pend = 0;
     bool ok = true;
     for (uint32_t g = pw; g < total; g += kProducers) {
-        const uint32_t i = g / p.num_kb, kb = g - i * p.num_kb;
+        uint32_t i, kb, tile;
+        if (g < whole_steps) {
+            i = g / p.num_kb;
+            kb = g - i * p.num_kb;
+            tile = first_tile + i * tile_step;
+        } else {
+            i = n_whole;
+            kb = skb0 + (g - whole_steps);
+            tile = stile;
+        }
         if (i != cur) {
             cur = i;
             uint32_t b, mt, nt;
-            tile_of(p, first_tile + i * tile_step, b, mt, nt);
+            tile_of(p, tile, b, mt, nt);
             const uint32_t m0 = PAIR ? mt * 2 * kBlockM + rank * kBlockM : mt * kBlockM;
             const uint32_t n0 = PAIR ? nt * p.block_n + rank * (p.block_n / 2) : nt * p.block_n;
 #pragma unroll
@@ -355,10 +400,78 @@ __device__ __forceinline__ void apply_terms(const TcParams& p, uint32_t (&r)[32]
     }
 }
 
+// Partial sums of a split tile, for one epilogue warp: column block c (32 columns) holds
+// register i of every lane at c * 1024 + i * 32 + lane, so each access of the warp is one
+// contiguous 128-byte line.  L2 only (the other parts run on other SMs).
+__device__ __forceinline__ void add_partial(uint32_t (&r)[32], const float* pw, uint32_t c, int lane) {
+    const float* s = pw + (size_t)c * 1024u + (uint32_t)lane;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __ldcg(s + 32 * i));
+}
+__device__ __forceinline__ void put_partial(const uint32_t (&r)[32], float* pw, uint32_t c, int lane) {
+    float* s = pw + (size_t)c * 1024u + (uint32_t)lane;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) __stcg(s + 32 * i, __uint_as_float(r[i]));
+}
+
+// Bounded wait, by every lane, until the flag holds `want` (acquire at GPU scope: the partial
+// sums written before the flag's release are visible afterwards).
+__device__ __forceinline__ bool wait_flag(const unsigned long long* f, unsigned long long want, volatile int* abort,
+                                          uint64_t timeout_ns) {
+    const uint64_t t0 = globaltimer();
+    bool ok = true;
+    for (uint32_t n = 0;; ++n) {
+        unsigned long long v;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(f) : "memory");
+        if (v == want) break;
+        if ((n & 15) == 15) {
+            if (*abort || globaltimer() - t0 > timeout_ns) {
+                if (!*abort) {
+                    *abort = 1;
+                    atomicExch(&g_status, (int)TRA_ERR_TIMEOUT);
+                }
+                ok = false;
+                break;
+            }
+        }
+        __nanosleep(100);
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+__device__ __forceinline__ void set_flag(unsigned long long* f, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(f), "l"(v) : "memory");
+}
+
+// A non-final part of a split tile: wait for the previous part (if any), add its partial
+// sums, leave this warp's running sums in the partial buffer, release the next part.
+__device__ __forceinline__ bool split_partial(const TcParams& p, uint32_t tmem_acc, uint32_t q, uint32_t half,
+                                              int lane, uint32_t part, float* pw, unsigned long long* flag,
+                                              volatile int* abort) {
+    if (part > 0 && !wait_flag(flag, p.tag | part, abort, p.timeout_ns)) return false;
+    const uint32_t nblk = p.block_n / 32;
+    const uint32_t taddr = tmem_acc + ((q * 32u) << 16);
+    for (uint32_t c = 2 * half; c < nblk; c += 4) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32_nowait(taddr + c * 32u, ra);
+        tmem_ld32_nowait(taddr + c * 32u + 32u, rb);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (part > 0) {
+            add_partial(ra, pw, c, lane);
+            add_partial(rb, pw, c + 1, lane);
+        }
+        put_partial(ra, pw, c, lane);
+        put_partial(rb, pw, c + 1, lane);
+    }
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) set_flag(flag, p.tag | (part + 1));
+    return true;
+}
+
 template <int EPI>
 __device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorMap* map_z, uint8_t* epi,
                                               uint32_t tmem_acc, uint32_t q, uint32_t half, int lane, uint32_t b,
-                                              uint32_t m, uint32_t n0) {
+                                              uint32_t m, uint32_t n0, const float* addp = nullptr) {
     float4* stg = reinterpret_cast<float4*>(epi + (q + 4 * half) * kEpiTile);
     const uint32_t nblk = p.block_n / 32;  // block_n is a multiple of 64
     const uint32_t taddr = tmem_acc + ((q * 32u) << 16);
@@ -390,6 +503,10 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorM
             tmem_ld32_nowait(taddr + c * 32u, ra);
             tmem_ld32_nowait(taddr + c * 32u + 32u, rb);
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            if (addp) {
+                add_partial(ra, addp, c, lane);
+                add_partial(rb, addp, c + 1, lane);
+            }
             apply_terms<EPI>(p, ra, rt, b, n0 + c * 32u);
             apply_terms<EPI>(p, rb, rt, b, n0 + c * 32u + 32u);
             if (!p.out_bf16) {
@@ -430,11 +547,40 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorM
         tmem_ld32_nowait(taddr + c * 32u, ra);
         tmem_ld32_nowait(taddr + c * 32u + 32u, rb);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (addp) {
+            add_partial(ra, addp, c, lane);
+            add_partial(rb, addp, c + 1, lane);
+        }
         apply_terms<EPI>(p, ra, rt, b, n0 + c * 32u);
         apply_terms<EPI>(p, rb, rt, b, n0 + c * 32u + 32u);
         store_block(p, stg, zr, __shfl_sync(0xffffffffu, zc_lane, c), lane, ra, n0 + c * 32u);
         store_block(p, stg, zr, __shfl_sync(0xffffffffu, zc_lane, c + 1), lane, rb, n0 + c * 32u + 32u);
     }
+}
+
+// One unit's epilogue for one epilogue warp.  A whole tile goes out as before.  Of a split tile
+// (plain epilogue only), parts before the last leave running sums in the partial buffer; the
+// last part adds them to its accumulator and stores the tile, then clears its flag.  rank: the
+// CTA's rank in its pair (0 for one CTA per tile); regions: TMEM lane quarters per tile (4 per
+// CTA).  False when a wait gave up.
+__device__ __forceinline__ bool epilogue_unit(const TcParams& p, const CUtensorMap* map_z, uint8_t* epi,
+                                              uint32_t tmem_acc, uint32_t q, uint32_t half, int lane, uint32_t b,
+                                              uint32_t mrow, uint32_t n0, uint32_t tile, uint32_t part, uint32_t rank,
+                                              uint32_t regions, volatile int* abort) {
+    if (part == kWhole) {
+        if (p.epi == 0) epilogue_tile<0>(p, map_z, epi, tmem_acc, q, half, lane, b, mrow, n0);
+        else if (p.epi == 1) epilogue_tile<1>(p, map_z, epi, tmem_acc, q, half, lane, b, mrow, n0);
+        else epilogue_tile<2>(p, map_z, epi, tmem_acc, q, half, lane, b, mrow, n0);
+        return true;
+    }
+    const uint32_t v = tile - p.n_full;
+    float* pw = p.part + ((size_t)v * regions + rank * 4u + q) * (size_t)(p.block_n * 32u);
+    unsigned long long* flag = p.flags + (size_t)v * (2u * regions) + rank * 8u + half * 4u + q;
+    if (part + 1 < p.split) return split_partial(p, tmem_acc, q, half, lane, part, pw, flag, abort);
+    if (!wait_flag(flag, p.tag | part, abort, p.timeout_ns)) return false;
+    epilogue_tile<0>(p, map_z, epi, tmem_acc, q, half, lane, b, mrow, n0, pw);
+    if (lane == 0) *reinterpret_cast<volatile unsigned long long*>(flag) = 0ull;  // ready for the next call
+    return true;
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -498,14 +644,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a_lbo = p.a.mn_major ? 8192u : 16u, b_lbo = p.b.mn_major ? 8192u : 16u;
         const uint32_t a_kstep = (p.a.mn_major ? 2048u : 32u) >> 4, b_kstep = (p.b.mn_major ? 2048u : 32u) >> 4;
         const uint64_t da0 = smem_desc(base, a_lbo, 1024), db0 = smem_desc(base + p.a_bytes, b_lbo, 1024);
-        for (uint32_t t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+        for (uint32_t u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+            uint32_t tile, kb0, kb1, part;
+            unit_of(p, u, tile, kb0, kb1, part);
             if (!wait_u(tempty0 + 8 * acc, acc_phase ^ 1)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + acc * p.block_n;
-            for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+            for (uint32_t kb = kb0; kb < kb1; ++kb) {
                 if (!wait_u(full0 + 8 * stage, phase)) {
                     ok = false;
                     break;
@@ -514,7 +662,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t so = (stage * stage_bytes) >> 4;
 #pragma unroll
                 for (uint32_t k = 0; k < kBlockK / 16; ++k)
-                    tc_mma_elect(d_tmem, da0 + so + k * a_kstep, db0 + so + k * b_kstep, p.idesc, (kb | k) != 0);
+                    tc_mma_elect(d_tmem, da0 + so + k * a_kstep, db0 + so + k * b_kstep, p.idesc,
+                                 (kb != kb0 || k != 0));
                 tc_commit_elect(empty0 + 8 * stage);  // frees the stage once these MMAs have read it
                 if (++stage == p.stages) {
                     stage = 0;
@@ -538,15 +687,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t q = warp & 3;  // TMEM lane quarter this warp may access
         const uint32_t half = (uint32_t)(warp - kMmaWarp - 1) >> 2;
         uint32_t acc = 0, acc_phase = 0;
-        for (uint32_t t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
-            uint32_t b, mt, nt;
-            tile_of(p, t, b, mt, nt);
+        for (uint32_t u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+            uint32_t tile, kb0, kb1, part, b, mt, nt;
+            unit_of(p, u, tile, kb0, kb1, part);
+            tile_of(p, tile, b, mt, nt);
             if (!mbar_wait(tfull0 + 8 * acc, acc_phase, abort, p.timeout_ns)) break;
             tc_fence_after();
             const uint32_t mrow = mt * kBlockM + q * 32 + lane;
-            if (p.epi == 0) epilogue_tile<0>(p, &map_z, epi, tmem_base + acc * p.block_n, q, half, lane, b, mrow, nt * p.block_n);
-            else if (p.epi == 1) epilogue_tile<1>(p, &map_z, epi, tmem_base + acc * p.block_n, q, half, lane, b, mrow, nt * p.block_n);
-            else epilogue_tile<2>(p, &map_z, epi, tmem_base + acc * p.block_n, q, half, lane, b, mrow, nt * p.block_n);
+            if (!epilogue_unit(p, &map_z, epi, tmem_base + acc * p.block_n, q, half, lane, b, mrow, nt * p.block_n, tile,
+                               part, 0u, 4u, abort))
+                break;
             tc_fence_before();
             mbar_arrive(tempty0 + 8 * acc);
             if (++acc == 2) {
@@ -635,14 +785,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t a_lbo = p.a.mn_major ? 8192u : 16u, b_lbo = p.b.mn_major ? 8192u : 16u;
             const uint32_t a_kstep = (p.a.mn_major ? 2048u : 32u) >> 4, b_kstep = (p.b.mn_major ? 2048u : 32u) >> 4;
             const uint64_t da0 = smem_desc(base, a_lbo, 1024), db0 = smem_desc(base + p.a_bytes, b_lbo, 1024);
-            for (uint32_t t = pair; t < p.n_tiles && ok; t += n_pairs) {
+            for (uint32_t u = pair; u < p.n_units && ok; u += n_pairs) {
+                uint32_t tile, kb0, kb1, part;
+                unit_of(p, u, tile, kb0, kb1, part);
                 if (!wait_u(tempty0 + 8 * acc, acc_phase ^ 1)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * p.block_n;
-                for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+                for (uint32_t kb = kb0; kb < kb1; ++kb) {
                     if (!wait_u(full0 + 8 * stage, phase)) {
                         ok = false;
                         break;
@@ -652,7 +804,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (uint32_t k = 0; k < kBlockK / 16; ++k)
                         tc_mma_pair_elect(d_tmem, da0 + so + k * a_kstep, db0 + so + k * b_kstep, p.idesc,
-                                          (kb | k) != 0);
+                                          (kb != kb0 || k != 0));
                     tc_commit_pair_elect(empty0 + 8 * stage, 3);  // frees this stage in both CTAs
                     if (++stage == p.stages) {
                         stage = 0;
@@ -676,15 +828,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t q = warp & 3;
         const uint32_t half = (uint32_t)(warp - kMmaWarp - 1) >> 2;
         uint32_t acc = 0, acc_phase = 0;
-        for (uint32_t t = pair; t < p.n_tiles; t += n_pairs) {
-            uint32_t b, mt, nt;
-            tile_of(p, t, b, mt, nt);
+        for (uint32_t u = pair; u < p.n_units; u += n_pairs) {
+            uint32_t tile, kb0, kb1, part, b, mt, nt;
+            unit_of(p, u, tile, kb0, kb1, part);
+            tile_of(p, tile, b, mt, nt);
             if (!mbar_wait_cl(tfull0 + 8 * acc, acc_phase, abort, p.timeout_ns)) break;
             tc_fence_after();
             const uint32_t mrow = mt * 2 * kBlockM + rank * kBlockM + q * 32 + lane;
-            if (p.epi == 0) epilogue_tile<0>(p, &map_z, epi, tmem_base + acc * p.block_n, q, half, lane, b, mrow, nt * p.block_n);
-            else if (p.epi == 1) epilogue_tile<1>(p, &map_z, epi, tmem_base + acc * p.block_n, q, half, lane, b, mrow, nt * p.block_n);
-            else epilogue_tile<2>(p, &map_z, epi, tmem_base + acc * p.block_n, q, half, lane, b, mrow, nt * p.block_n);
+            if (!epilogue_unit(p, &map_z, epi, tmem_base + acc * p.block_n, q, half, lane, b, mrow, nt * p.block_n, tile,
+                               part, rank, 8u, abort))
+                break;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty0 + 8 * acc, 0));
@@ -757,6 +910,10 @@ struct TcPlan {
     uint32_t b_rows = 0;  // rows of Y one CTA loads per K step
     uint32_t block_n = 0, stages = 0, tiles_m = 0, tiles_n = 0, n_tiles = 0, num_kb = 0, tmem_cols = 0;
     uint32_t idesc = 0, smem = 0;
+    // K split of the last wave's tiles, chosen for `workers` co-resident CTAs (one CTA per
+    // tile) or CTA pairs; split = 1 when it does not apply
+    uint32_t workers = 0, split = 1, n_full = 0;
+    uint64_t ws_part = 0, ws_flags = 0;  // workspace bytes of the partial sums and of the flags
 };
 
 void tc_free(TcPlan* t) { delete t; }
@@ -949,6 +1106,36 @@ bool build_tc(const Plan& p, bool pair, uint32_t bn, TcPlan* t) {
 
 }  // namespace
 
+namespace {
+int sm_count();
+uint32_t pair_clusters(int sms, uint32_t smem);
+
+// K split of the tiles of the last, partly filled wave: T tiles on C workers leave R = T mod C
+// tiles for the last wave; each is split into s = min(C / R, 4) runs of K steps (each run at
+// least 8 steps), so that the last wave keeps R * s workers busy for 1 / s of a tile's time.
+// Tiles [0, n_full) stay whole; n_full = T - R is a multiple of C.
+void split_config(uint32_t T, uint32_t C, uint32_t num_kb, uint32_t& n_full, uint32_t& s) {
+    n_full = T;
+    s = 1;
+    if (C == 0 || T == 0) return;
+    const uint32_t R = T % C;
+    if (R == 0) return;
+    uint32_t c = C / R;
+    if (c > 4) c = 4;
+    while (c > 1 && num_kb / c < 8) --c;
+    if (c < 2) return;
+    n_full = T - R;
+    s = c;
+}
+
+// Workers a launch of this tiling gets on the current device: co-resident CTA pairs, or SMs.
+uint32_t tc_workers(const TcPlan& t) {
+    const int sms = sm_count();
+    if (sms <= 0) return 0;
+    return t.pair ? pair_clusters(sms, t.smem) : (uint32_t)sms;
+}
+}  // namespace
+
 bool tc_plan(Plan* p) {
     if (p->unary || p->op != kMul || p->agg != kSum || !p->in_bf16 || p->literal) return false;
     const uint64_t M = p->ext[kM], N = p->ext[kN], K = p->ext[kK];
@@ -972,6 +1159,20 @@ bool tc_plan(Plan* p) {
     }
     p->tc = t;
     p->kernel = t->pair ? TRA_KERNEL_TC_BF16_PAIR : TRA_KERNEL_TC_BF16;
+    if (p->ksplit) {
+        t->workers = tc_workers(*t);
+        (void)cudaGetLastError();  // no device here: plan without the split
+        uint32_t n_full = 0, s = 1;
+        split_config(t->n_tiles, t->workers, t->num_kb, n_full, s);
+        if (s > 1) {
+            t->split = s;
+            t->n_full = n_full;
+            const uint64_t R = t->n_tiles - n_full, tile = (uint64_t)(t->pair ? 2 * kBlockM : kBlockM) * t->block_n;
+            t->ws_part = align256(R * tile * 4);
+            t->ws_flags = align256(R * (t->pair ? 16 : 8) * 8);
+            p->ws_bytes = t->ws_part + t->ws_flags;
+        }
+    }
     return true;
 }
 
@@ -1046,7 +1247,18 @@ uint32_t pair_clusters(int sms, uint32_t smem) {
 
 }  // namespace
 
-int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_t s, const TcExtra* ex) {
+namespace {
+// Flag tag of one launch: a fixed high byte and a per-process launch counter (started from the
+// clock), so that flags left by an earlier launch, or bytes the workspace held before, never
+// read as this launch's.  Bits 0-7 stay free for the count of parts done.
+unsigned long long next_split_tag() {
+    static std::atomic<unsigned long long> n{(unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count()};
+    const unsigned long long e = n.fetch_add(1) & 0xffffffffffull;
+    return (0xa5ull << 56) | (e << 8);
+}
+}  // namespace
+
+int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_t s, const TcExtra* ex, void* ws) {
     if (((uintptr_t)x | (uintptr_t)y | (uintptr_t)z) % 16) return fail(TRA_ERR_ARG, "tensor-core path needs 16-byte aligned buffers");
     const int sms = sm_count();
     if (sms <= 0) return fail(TRA_ERR_CUDA, "no device");
@@ -1116,17 +1328,38 @@ int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_
         tp.alpha = ex->alpha;
         if (tp.epi && (!tp.row_term || !tp.col_term)) return fail(TRA_ERR_ARG, "epilogue terms missing");
     }
+    // work units: the plan's K split of the last wave when the workspace is there, no epilogue
+    // terms are asked for, and this device gives the split no more workspace than planned
+    const uint32_t workers = t.pair ? clusters : (uint32_t)sms;
+    uint32_t n_full = t.n_tiles, split = 1;
+    if (t.split > 1 && !ex && ws) {
+        split_config(t.n_tiles, workers, t.num_kb, n_full, split);
+        const uint64_t R = t.n_tiles - n_full, tile = (uint64_t)(t.pair ? 2 * kBlockM : kBlockM) * t.block_n;
+        if (split > 1 && (align256(R * tile * 4) > t.ws_part || align256(R * (t.pair ? 16 : 8) * 8) > t.ws_flags)) {
+            split = 1;
+            n_full = t.n_tiles;
+        }
+    }
+    tp.n_full = n_full;
+    tp.split = split;
+    tp.n_units = n_full + (t.n_tiles - n_full) * split;
+    if (split > 1) {
+        tp.part = reinterpret_cast<float*>(ws);
+        tp.flags = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(ws) + t.ws_part);
+        tp.tag = next_split_tag();
+    }
     cudaError_t e;
     if (t.pair) {
         e = cudaFuncSetAttribute(tc_gemm_2sm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)t.smem);
         if (e != cudaSuccess) return fail(TRA_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(e));
-        // persistent: one cluster per co-resident SM pair, at most one per tile
-        const uint32_t c = clusters < t.n_tiles ? clusters : t.n_tiles;
+        // persistent: one cluster per co-resident SM pair, at most one per work unit (so that
+        // the whole tiles fill whole waves and every worker owns at most one split unit)
+        const uint32_t c = clusters < tp.n_units ? clusters : tp.n_units;
         tc_gemm_2sm<<<2 * c, kThreads, t.smem, s>>>(ma, mb, mz, tp);
     } else {
         e = cudaFuncSetAttribute(tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)t.smem);
         if (e != cudaSuccess) return fail(TRA_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(e));
-        const unsigned grid = (unsigned)(t.n_tiles < (uint32_t)sms ? t.n_tiles : (uint32_t)sms);
+        const unsigned grid = (unsigned)(tp.n_units < (uint32_t)sms ? tp.n_units : (uint32_t)sms);
         tc_gemm<<<grid, kThreads, t.smem, s>>>(ma, mb, mz, tp);
     }
     e = cudaGetLastError();

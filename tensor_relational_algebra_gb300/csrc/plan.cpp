@@ -216,6 +216,7 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
         else if (k == "tc" && (v == "pair" || v == "single")) p->tc_pair = v == "pair" ? 1 : 0;
         else if (k == "tc_n" && (v == "256" || v == "128")) p->tc_n = v == "256" ? 256 : 128;
         else if (k == "tc_store" && (v == "tma" || v == "lsu")) p->tc_store = v == "tma" ? 1 : 0;
+        else if (k == "ksplit" && (v == "auto" || v == "off")) p->ksplit = v == "auto" ? 1 : 0;
         else if (k == "split" && (v == "bf16x3" || v == "none")) p->split3 = v == "bf16x3";
         else if (k == "alpha") {
             char* end = nullptr;
@@ -266,7 +267,7 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
     const int nd_want = p->X.rank + (p->unary ? 0 : p->Y.rank);
     if (!d || n_d != nd_want) return fail(TRA_ERR_RANK, "%d partition counts given, %d index positions", n_d, nd_want);
     for (int l = 0; l < p->n_labels; ++l) {
-        if (bounds[l] < 1 || bounds[l] > 0x7fffffffLL)
+        if (bounds[l] < 0 || bounds[l] > 0x7fffffffLL)
             return fail(TRA_ERR_ARG, "bound of '%c' out of range", p->name[l]);
         p->B[l] = bounds[l];
         p->D[l] = 0;
@@ -355,6 +356,12 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
 
     // kernel choice and workspace
     p->ws_bytes = 0;
+    for (int l = 0; l < p->n_labels; ++l)
+        if (p->B[l] == 0) {
+            // an empty EinSum: no output element, or only empty aggregations (agg's identity)
+            p->kernel = p->Z.total == 0 ? TRA_KERNEL_EMPTY : TRA_KERNEL_FILL;
+            return TRA_OK;
+        }
     if (p->literal && p->agg != kNone) {
         p->kernel = TRA_KERNEL_LITERAL;
         p->ws_bytes = align256(p->n_tasks * zs * sizeof(float));
@@ -389,7 +396,7 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
         // relation layout, and the GEMM's output relation is this plan's Z, so its TMA-store
         // epilogue writes Z directly.
         if (nb == 1 && p->comp[kM].size() == 1 && p->comp[kN].size() == 1 && p->Z.rank == 2 && Mp == M && Np == N) {
-            const std::string dspec = "mk,nk->mn:mul:sum:in=bf16" + out_opt;
+            const std::string dspec = "mk,nk->mn:mul:sum:in=bf16:ksplit=off" + out_opt;
             const int64_t db[3] = {(int64_t)M, (int64_t)K3p, (int64_t)N};
             const int32_t dd[4] = {p->D[p->comp[kM][0]], 1, p->D[p->comp[kN][0]], 1};
             Plan* in = new Plan();
@@ -404,7 +411,7 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
         // General form: dense operands, the output addressed through this plan's Z role maps.
         if (!p->inner) {
             std::string ispec = nb > 1 ? "bmk,bnk->bmn" : "mk,nk->mn";
-            ispec += ":mul:sum:in=bf16:tc_store=lsu" + out_opt;
+            ispec += ":mul:sum:in=bf16:tc_store=lsu:ksplit=off" + out_opt;
             const int64_t ib[4] = {(int64_t)nb, (int64_t)Mp, (int64_t)K3p, (int64_t)Np};  // labels b, m, k, n
             const int32_t ones[6] = {1, 1, 1, 1, 1, 1};
             Plan* in = new Plan();

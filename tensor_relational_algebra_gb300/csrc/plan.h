@@ -40,6 +40,7 @@ struct Plan {
     int tc_pair = -1;  // tensor-core tile: 1 CTA pair (256 x 256), 0 single CTA, -1 pair when shapes allow
     int tc_n = 0;      // width of a pair tile: 256, 128, or 0 (256 where the columns allow)
     int tc_store = -1; // tensor-core epilogue: 1 TMA stores, 0 warp stores, -1 TMA where the output map fits
+    int ksplit = 1;    // tensor-core path: 1 split the K loop of the last wave's tiles over idle workers, 0 never
     int split3 = 0;    // split=bf16x3: squared distance / logsumexp rewritten onto BF16 tensor cores
     Plan* inner = nullptr;  // split3: the GEMM plan over the split operands (owned)
     int split3_direct = 0;  // split3: inner's output layout is this plan's (no override, TMA stores)
@@ -96,7 +97,10 @@ struct TcExtra {
     uint32_t M = 0, N = 0;  // with z_override: the rows / columns stored (the product may be padded)
     int* mark_count = nullptr;  // epi 2: count of outputs marked for the underflow fix-up
 };
-int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_t s, const TcExtra* ex = nullptr);
+// ws: the plan's workspace (tc->ws_part + tc->ws_flags bytes) for the K split of the last
+// wave's tiles; without it, or with ex, every tile runs on one worker.
+int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_t s, const TcExtra* ex = nullptr,
+               void* ws = nullptr);
 
 uint64_t align256(uint64_t v);
 inline uint64_t split3_pad(uint64_t v, uint64_t q) { return (v + q - 1) / q * q; }

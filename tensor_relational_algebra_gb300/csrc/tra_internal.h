@@ -242,6 +242,7 @@ cudaError_t launch_row_reduce(const RowReduceParams& p, cudaStream_t s);
 cudaError_t launch_elementwise(const ElementwiseParams& p, cudaStream_t s);
 cudaError_t launch_repartition(const RepartParams& p, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
+cudaError_t launch_fill(void* z, uint64_t n, float v, bool bf16, cudaStream_t s);
 
 // Device status word written by bounded waits that give up (TRA_ERR_TIMEOUT).
 cudaError_t read_and_clear_status(int* value, cudaStream_t s);

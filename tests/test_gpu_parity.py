@@ -315,3 +315,41 @@ def test_large_bf16_matmul(lib, cuda, d):
     X = gen((n, n), 0, 0, bf16=True)
     Y = gen((n, n), 0, 1, bf16=True)
     _sampled(lib, MM + ":mul:sum:in=bf16", [n] * 3, d, X, Y, "mul", "sum", n=2048, tile=(8100, 8100, 64), bf16=True)
+
+
+# ---------------------------------------------------------------- empty EinSums
+EMPTY_FILL = [
+    # a contracted label of extent 0 (binary and unary): each output aggregates the empty set
+    ("ij,jk->ik", [64, 0, 32], [4, 2, 2, 2]),
+    ("abef,cfed->abcd", [4, 2, 0, 3, 2, 4], [2, 1, 4, 3, 2, 3, 4, 2]),
+    ("hst->hs", [2, 8, 0], [2, 2, 1]),
+]
+
+
+@pytest.mark.parametrize("alpha", [1.0, -0.5])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+@pytest.mark.parametrize("agg", ["sum", "max", "min", "lse"])
+@pytest.mark.parametrize("eq,bounds,d", EMPTY_FILL)
+def test_empty_contraction(lib, cuda, eq, bounds, d, agg, out, alpha):
+    import torch
+
+    ins = eq.split("->")[0].split(",")
+    unary = len(ins) == 1
+    op = "" if unary else ("mul" if agg == "sum" else "add")
+    p = lib.Plan(f"{eq}:{op}:{agg}:out={out}:alpha={alpha}", bounds, d)
+    assert p.kernel == "fill"
+    order = []
+    for c in "".join(ins):
+        if c not in order:
+            order.append(c)
+    B = dict(zip(order, bounds))
+    X = np.zeros(tuple(B[c] for c in ins[0]), np.float32)
+    Y = None if unary else np.zeros(tuple(B[c] for c in ins[1]), np.float32)
+    z = torch.full((int(np.prod(p.shape("z"))),), 7.0, device="cuda",
+                   dtype=torch.bfloat16 if out == "bf16" else torch.float32)
+    p.execute(None, None, z)  # nothing is read
+    lib.ein_status()
+    g = as_f64(from_dev(z))
+    r = oracle.einsum(eq, X, Y, op=op or "mul", agg=agg, alpha=alpha).reshape(-1)
+    np.testing.assert_array_equal(g, r)  # 0 or an infinity, exactly
+    np.testing.assert_array_equal(np.signbit(g), np.signbit(r))

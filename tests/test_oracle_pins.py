@@ -139,6 +139,34 @@ def test_alpha_applies_after_aggregation():
     np.testing.assert_array_equal(oracle.einsum("ij,jk->ik", X, Y, op="add", agg="max", alpha=-1.0), -mx)
 
 
+@pytest.mark.parametrize("op,agg,lib_red", [
+    ("mul", "sum", lambda v: np.sum(v, axis=1)),
+    ("add", "max", lambda v: np.max(v, axis=1, initial=-np.inf)),
+    ("add", "min", lambda v: np.min(v, axis=1, initial=np.inf)),
+    ("add", "lse", None),
+])
+def test_empty_contraction_gives_the_identity(op, agg, lib_red):
+    # aggregating an empty set gives the aggregation's identity: numpy's empty sum is 0 and its
+    # max / min with an initial value return that value; logsumexp of nothing is log(0) = -inf
+    from scipy.special import logsumexp
+
+    X = np.zeros((3, 0), np.float32)
+    Y = np.zeros((0, 4), np.float32)
+    got = oracle.einsum("ij,jk->ik", X, Y, op=op, agg=agg)
+    v = X[:, :, None].astype(np.float64) + Y[None, :, :].astype(np.float64)
+    if lib_red is not None:
+        want = lib_red(v)
+    else:
+        with np.errstate(divide="ignore"):
+            want = logsumexp(v, axis=1)
+    assert got.shape == (3, 4)
+    np.testing.assert_array_equal(got, want)
+    np.testing.assert_array_equal(oracle.einsum("ij,jk->ik", X, Y, op=op, agg=agg, alpha=-2.0), -2.0 * want)
+    # an empty output label: no output element at all
+    assert oracle.einsum("ij,jk->ik", np.zeros((0, 5), np.float32), np.ones((5, 4), np.float32), op=op,
+                         agg=agg).shape == (0, 4)
+
+
 def test_points_equal_full():
     X, Y = rng_arrays((9, 5, 4), (7, 5, 4), seed=9)
     full = oracle.einsum("shd,thd->hst", X, Y, alpha=0.25)

@@ -67,6 +67,44 @@ def test_plan_matches_bruteforce(lib, eq, bounds, d):
         assert p.keys() == ref["tasks"]
 
 
+EMPTY_CASES = [
+    # a contracted label of extent 0: every output aggregates the empty set
+    ("ij,jk->ik", {"i": 64, "j": 0, "k": 32}, [4, 2, 2, 2], "fill"),
+    ("abef,cfed->abcd", {"a": 4, "b": 2, "e": 0, "f": 3, "c": 2, "d": 4}, [2, 1, 4, 3, 2, 3, 4, 2], "fill"),
+    # an output label of extent 0: nothing to compute
+    ("ij,jk->ik", {"i": 0, "j": 16, "k": 32}, [2, 4, 4, 2], "empty"),
+    ("sa,ahd->shd", {"s": 8, "a": 4, "h": 0, "d": 2}, [2, 2, 2, 1, 1], "empty"),
+]
+
+
+@pytest.mark.parametrize("eq,bounds,d,kernel", EMPTY_CASES)
+def test_empty_plan_matches_bruteforce(lib, eq, bounds, d, kernel):
+    # the key space and the cost formulas still hold, with sub-tensors of 0 elements
+    p = lib.Plan(eq + ":mul:sum", bounds, d)
+    assert p.kernel == kernel and p.workspace_bytes == 0
+    ref = otra.plan_bruteforce(eq, bounds, d)
+    for k in ("n_tasks", "n_groups", "n_agg", "cost_join", "cost_agg"):
+        assert getattr(p, k) == ref[k], k
+    assert p.info.x_sub == ref["x_sub"] and p.info.y_sub == ref["y_sub"] and p.info.z_sub == ref["z_sub"]
+    assert p.keys() == ref["tasks"]
+    for agg in ("max", "min", "lse"):
+        assert lib.Plan(f"{eq}:add:{agg}", bounds, d).kernel == kernel
+
+
+def test_empty_output_and_repartition_need_no_buffers(lib):
+    # an output of no elements launches nothing (no device needed); nor does a repartition of
+    # a tensor with an extent of 0
+    p = lib.Plan("ij,jk->ik:mul:sum", [0, 16, 32], [1, 1, 1, 1])
+    lib.ein_execute(p.handle, None, None, None, None, 0, 0)
+    lib.ein_repartition([0, 4], [1, 1], [1, 2], 4, None, None, 0)
+    with pytest.raises(lib.TraError) as e:
+        lib.ein_repartition([0, 4], [1, 1], [1, 3], 4, None, None, 0)
+    assert "TRA_ERR_DIVISIBILITY" in str(e.value)
+    with pytest.raises(lib.TraError) as e:
+        lib.ein_execute(lib.Plan("ij,jk->ik:mul:sum", [4, 0, 4], [1, 1, 1, 1]).handle, None, None, None, None, 0, 0)
+    assert "TRA_ERR_ARG" in str(e.value)  # a fill needs its output
+
+
 def test_plan_golden(lib):
     g = json.load(open(os.path.join(GOLD, "cost_terms.json")))
     for c in g["cases"]:
@@ -149,7 +187,8 @@ def test_split3_plan_errors(lib, spec, bounds, d, code):
     ("ij,jk->ik:mul:none", [64, 64, 64], [1, 1, 1, 1], "TRA_ERR_PARSE"),
     ("ij,jk->ik:mul:sum:alpha=x", [64, 64, 64], [1, 1, 1, 1], "TRA_ERR_PARSE"),
     ("ij,jk->ik:mul:sum:foo=1", [64, 64, 64], [1, 1, 1, 1], "TRA_ERR_PARSE"),
-    ("ij,jk->ik:mul:sum", [64, 0, 64], [1, 1, 1, 1], "TRA_ERR_ARG"),
+    ("ij,jk->ik:mul:sum", [64, -1, 64], [1, 1, 1, 1], "TRA_ERR_ARG"),
+    ("ij,jk->ik:mul:sum:ksplit=on", [64, 64, 64], [1, 1, 1, 1], "TRA_ERR_PARSE"),
     ("ij,jk->ik:mul:sum:in=bf16:tc=pair", [384, 128, 256], [1, 1, 1, 1], "TRA_ERR_UNSUPPORTED"),
     ("ij,jk->ik:mul:sum:tc=both", [256, 128, 256], [1, 1, 1, 1], "TRA_ERR_PARSE"),
     ("ij,jk->ik:mul:sum:tc_n=64", [256, 128, 256], [1, 1, 1, 1], "TRA_ERR_PARSE"),
