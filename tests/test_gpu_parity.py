@@ -110,6 +110,29 @@ def test_semiring_ragged(lib, cuda, op, agg, d):
     check(op, agg, g, r, S)
 
 
+# fp32 operands contiguous along K (X) and N (Y) in runs of 4: the cp.async pipelined kernel,
+# 9 tiles with ragged M / N tails, and 18 x 18 tiles (more CTAs than fit at once).
+@pytest.mark.parametrize("op,agg", SEMIRINGS)
+@pytest.mark.parametrize("d", [[1, 1, 1, 1], [2, 2, 2, 2]])
+def test_semiring_async_ragged(lib, cuda, op, agg, d):
+    M, K, N = 300, 96, 264
+    X = gen((M, K), 13, 0)
+    Y = gen((K, N), 13, 1)
+    _, g = run_plan(lib, f"{MM}:{op}:{agg}", [M, K, N], d, X, Y)
+    r, S = ref_full(MM, X, Y, op, agg)
+    check(op, agg, g, r, S)
+
+
+@pytest.mark.parametrize("op,agg", [("mul", "sum"), ("add", "max"), ("sqdiff", "sum")])
+def test_semiring_async_many_tiles(lib, cuda, op, agg):
+    M, K, N = 2304, 64, 2304
+    X = gen((M, K), 14, 0)
+    Y = gen((K, N), 14, 1)
+    _, g = run_plan(lib, f"{MM}:{op}:{agg}", [M, K, N], [1, 1, 1, 1], X, Y)
+    r, S = ref_full(MM, X, Y, op, agg)
+    check(op, agg, g, r, S)
+
+
 @pytest.mark.parametrize("op,agg", [("mul", "sum"), ("add", "max"), ("add", "lse"), ("sqdiff", "sum")])
 def test_semiring_literal_mode(lib, cuda, op, agg):
     M, K, N = 96, 60, 70
