@@ -646,6 +646,31 @@ def max_over_ranks(value_ms: float, world: int, device: str = "cuda") -> float:
     return float(t.item())
 
 
+def plan_times(tra, wl, reps: int = 20) -> dict:
+    """Host time (median of reps, ms) to build each plan the step executes: ein_plan runs once,
+    before the timed region, and is reported here apart from it."""
+    plans = []
+
+    def collect(obj, depth):
+        for v in vars(obj).values():
+            if isinstance(v, tra.Plan):
+                plans.append(v)
+            elif depth == 0 and type(v).__module__.startswith("tensor_relational_algebra_gb300"):
+                collect(v, 1)
+
+    collect(wl, 0)
+    out = {}
+    for p in plans:
+        ts = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            q = tra.Plan(p.spec, p.bounds, p.d)
+            ts.append(time.perf_counter() - t0)
+            del q
+        out[f"{p.spec} d={p.d}"] = round(sorted(ts)[len(ts) // 2] * 1e3, 4)
+    return out
+
+
 def job_throughput(ops_per_step: int, steps: int, world: int, job_ms: float) -> float:
     """Whole-job TFLOP/s: every rank processed its own replica of the workload (weak scaling)."""
     return world * ops_per_step * steps / (job_ms * 1e-3) / 1e12
@@ -788,6 +813,7 @@ def run_ours(args):
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d_bytes,
                 "d2h_bytes_per_step": d2h_bytes},
         "gpu_launches": args.steps * sum(s.launches for s in wl.steps),
+        "plan_ms": plan_times(tra, wl),
         "clocks": clocks,
         "wall_s": round(wall, 3),
     }

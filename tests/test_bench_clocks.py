@@ -54,3 +54,23 @@ def test_malformed_lines_are_ignored():
     lines = ["", "garbage", "a, b, c", _line(t0 + 0.1, 2070)]
     rec = _sampler(lines, (t0, t0 + 0.2)).stop()
     assert rec["samples"] == 1
+
+
+def test_plan_times_cover_every_plan_of_the_step(lib):
+    # the plans a workload holds directly or through its EinGraph object are timed apart from
+    # the step (no GPU needed: ein_plan is host code)
+    class Graph:
+        pass
+
+    Graph.__module__ = "tensor_relational_algebra_gb300.eingraph"
+
+    class Workload:
+        pass
+
+    wl = Workload()
+    wl.p = lib.Plan("ij,jk->ik:add:max", [256, 64, 256], [2, 1, 1, 2])
+    wl.g = Graph()
+    wl.g.p_proj = lib.Plan("sa,ahd->shd:mul:sum:in=bf16:out=bf16", [256, 256, 2, 128], [1, 1, 1, 2, 1])
+    t = bench.plan_times(lib, wl, reps=3)
+    assert set(t) == {"ij,jk->ik:add:max d=[2, 1, 1, 2]", "sa,ahd->shd:mul:sum:in=bf16:out=bf16 d=[1, 1, 1, 2, 1]"}
+    assert all(v >= 0 for v in t.values())
