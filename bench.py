@@ -208,6 +208,13 @@ class PairWorkload:
         self.outputs_dev = [self.Zs, self.Zm]
         self.output_steps = [1, 2]  # the launch group that produces each output
 
+    # end to end: the CUDA-core kernels store their results straight into pinned host memory
+    # (device-addressable over the host link), so no staging copy follows them
+    e2e_host_outputs = True
+
+    def redirect_outputs(self, outs):
+        self.Zs, self.Zm = outs
+
     def ops_per_step(self):
         return 2 * (2 * self.M * self.K * self.N)
 
@@ -738,6 +745,17 @@ def run_ours(args):
 
     def d2h():
         torch.cuda.current_stream().wait_stream(copy_stream)
+
+    if getattr(wl, "e2e_host_outputs", False):
+        # the step's kernels write pinned host memory themselves: the same bytes cross to the
+        # host, with no device-side staging buffer and no copy engine pass
+        wl.redirect_outputs(pinned_out)
+
+        def after(j):
+            return None
+
+        def d2h():
+            return None
 
     barrier()
     e2e_ms, _, _, _ = time_steps(torch, wl, max(3, args.steps // 4), args.warmup, flush, None,

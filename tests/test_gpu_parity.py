@@ -376,3 +376,28 @@ def test_empty_contraction(lib, cuda, eq, bounds, d, agg, out, alpha):
     r = oracle.einsum(eq, X, Y, op=op or "mul", agg=agg, alpha=alpha).reshape(-1)
     np.testing.assert_array_equal(g, r)  # 0 or an infinity, exactly
     np.testing.assert_array_equal(np.signbit(g), np.signbit(r))
+
+
+@pytest.mark.parametrize("spec,bounds,d", [
+    (MM + ":sqdiff:sum", [300, 96, 264], [2, 2, 2, 2]),
+    (MM + ":add:max", [300, 96, 264], [1, 1, 1, 1]),
+    ("hst->hs::lse", [4, 96, 200], [2, 3, 1]),
+])
+def test_output_in_pinned_host_memory(lib, cuda, spec, bounds, d):
+    # the CUDA-core kernels may store their result straight into pinned host memory (unified
+    # addressing): bit-identical to the result written to device memory
+    import torch
+
+    p = lib.Plan(spec, bounds, d)
+    n_in = len(p.operands)
+    xs = [torch.from_numpy(gen(tuple(p.shape(w)), 15, i)).reshape(-1).cuda() for i, w in enumerate("xy"[:n_in])]
+    if n_in == 1:
+        xs.append(None)
+    nz = int(np.prod(p.shape("z")))
+    zd = torch.empty(nz, device="cuda")
+    zh = torch.full((nz,), 7.0).pin_memory()
+    p.execute(xs[0], xs[1], zd)
+    p.execute(xs[0], xs[1], zh)
+    torch.cuda.synchronize()
+    lib.ein_status()
+    np.testing.assert_array_equal(zh.numpy(), zd.cpu().numpy())
