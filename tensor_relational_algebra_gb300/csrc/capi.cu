@@ -484,6 +484,11 @@ int ein_repartition(int rank, const int64_t* shape, const int32_t* src_d, const 
         cudaError_t e = cudaMemcpyAsync(dst, src, (size_t)total * elem_bytes, cudaMemcpyDeviceToDevice, s);
         return e == cudaSuccess ? TRA_OK : cuda_fail(e, "copy");
     }
+    {
+        const cudaError_t et = launch_repartition_tma(rank, shape, src_d, dst_d, elem_bytes, src, dst, s);
+        if (et == cudaSuccess) return TRA_OK;
+        if (et != cudaErrorNotSupported) return cuda_fail(et, "repartition launch");
+    }
     RepartParams rp;
     memset(&rp, 0, sizeof(rp));
     rp.src = src;
@@ -551,11 +556,13 @@ int ein_repartition_messages(int rank, const int64_t* shape, const int32_t* src_
 
 int ein_status(tra_stream_t stream) {
     clear_error();
-    int v = 0, va = 0;
+    int v = 0, va = 0, vr = 0;
     cudaError_t e = read_and_clear_status(&v, reinterpret_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) e = read_and_clear_attn_status(&va, reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = read_and_clear_rp_status(&vr, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "status read");
-    if (v || va) return fail(v ? v : va, "a bounded device wait gave up (status %d)", v ? v : va);
+    if (!v) v = va ? va : vr;
+    if (v) return fail(v, "a bounded device wait gave up (status %d)", v);
     return TRA_OK;
 }
 

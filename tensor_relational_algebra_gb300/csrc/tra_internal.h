@@ -241,6 +241,12 @@ cudaError_t launch_split3_stats(const Split3StatsParams& p, cudaStream_t s);
 cudaError_t launch_row_reduce(const RowReduceParams& p, cudaStream_t s);
 cudaError_t launch_elementwise(const ElementwiseParams& p, cudaStream_t s);
 cudaError_t launch_repartition(const RepartParams& p, cudaStream_t s);
+// TMA path of the repartition (k_repart.cu): cudaErrorNotSupported when the layouts do not fit
+// it (more than 4 dimensions of extent > 1, rows not on 16-byte boundaries, boxes under 4 KB);
+// the caller then runs launch_repartition.
+cudaError_t launch_repartition_tma(int rank, const int64_t* shape, const int32_t* src_d, const int32_t* dst_d,
+                                   int elem_bytes, const void* src, void* dst, cudaStream_t s);
+cudaError_t read_and_clear_rp_status(int* value, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_fill(void* z, uint64_t n, float v, bool bf16, cudaStream_t s);
 

@@ -54,12 +54,21 @@ def check(op, agg, g, r, S=None, bf16=False):
     ((7, 9), [7, 3], [1, 9], "f32"),
     ((16, 16), [2, 4], [8, 2], "f64"),
     ((1,), [1], [1], "f32"),
+    # the TMA path (at most 4 dimensions of extent > 1, 16-byte rows, boxes of 4-32 KB) for
+    # every element size, unit dimensions dropped; and a 5-dimensional case that falls back
+    ((64, 128, 256), [2, 1, 4], [4, 2, 1], "u8"),
+    ((1, 128, 64, 256), [1, 2, 1, 4], [1, 1, 4, 2], "f32"),
+    ((2, 1, 32, 64, 128), [2, 1, 2, 1, 4], [1, 1, 1, 4, 2], "bf16"),
+    ((256, 512), [4, 2], [2, 8], "f64"),
+    ((4, 4, 8, 16, 64), [2, 2, 2, 2, 2], [1, 4, 1, 8, 1], "f32"),
 ])
 def test_repartition_bit_exact(lib, cuda, shape, src_d, dst_d, dtype):
     import torch
 
     if dtype == "f64":
         dense = gen(shape, 0, 7).astype(np.float64)
+    elif dtype == "u8":
+        dense = (gen(shape, 0, 7) * 40).astype(np.int16).astype(np.uint8)
     else:
         dense = gen(shape, 0, 7, bf16=(dtype == "bf16"))
     src_blocked = otra.block(dense, src_d)
