@@ -362,7 +362,7 @@ class C3Workload(_PointsWorkload):
         return f"{n} of 64^4 outputs of the contraction"
 
     def traffic_key(self, j):
-        return ("k_tc.cu", "tc_gemm 4-D contraction") if j == 0 else ("k_misc.cu", "repartition 64^4 fp32")
+        return ("k_tc.cu", "tc_gemm 4-D contraction") if j == 0 else ("k_repart.cu", "repartition 64^4 fp32")
 
 
 class C4Workload(_PointsWorkload):
