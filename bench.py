@@ -365,6 +365,15 @@ class C3Workload(_PointsWorkload):
         return ("k_tc.cu", "tc_gemm 4-D contraction") if j == 0 else ("k_repart.cu", "repartition 64^4 fp32")
 
 
+def _packed_dev(torch, inputs):
+    """Q, K, V in one device buffer, back to back, and so the relations of W_Q, W_K, W_V (the graph then
+    runs the three projections as one EinSum); W_O on its own."""
+    qkv = _dev_bf16(torch, np.concatenate([x.reshape(-1) for x in inputs[:3]]))
+    w = _dev_bf16(torch, np.concatenate([x.reshape(-1) for x in inputs[3:6]]))
+    n, m = inputs[0].size, inputs[3].size
+    return [qkv[:n], qkv[n:2 * n], qkv[2 * n:], w[:m], w[m:2 * m], w[2 * m:], _dev_bf16(torch, inputs[6])]
+
+
 class C4Workload(_PointsWorkload):
     name = "multi-head attention EinGraph s=4096 a=4096 h=32 d=128, BF16 activations N(0,1), weights N(0,0.02)"
     d = "projections split h=32 (head-major outputs); scores/lse/exp/A.V split h=32; repartition of O to dense"
@@ -382,7 +391,7 @@ class C4Workload(_PointsWorkload):
         from tensor_relational_algebra_gb300.eingraph import AttentionGraph
 
         self.g = AttentionGraph(4096, 4096, 32, 128)
-        self.dev = [_dev_bf16(torch, x) for x in inputs]
+        self.dev = _packed_dev(torch, inputs)
         self.steps = [Step(*n) for n in self.g.nodes(*self.dev)]
         self.inputs_dev = self.dev
         self.outputs_dev = [self.g.out]
@@ -411,7 +420,7 @@ class C4fWorkload(C4Workload):
         from tensor_relational_algebra_gb300.eingraph import AttentionGraph
 
         self.g = AttentionGraph(4096, 4096, 32, 128, fused=True)
-        self.dev = [_dev_bf16(torch, x) for x in inputs]
+        self.dev = _packed_dev(torch, inputs)
         self.steps = [Step(*n) for n in self.g.nodes(*self.dev)]
         self.inputs_dev = self.dev
         self.outputs_dev = [self.g.out]

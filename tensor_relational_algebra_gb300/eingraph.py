@@ -20,6 +20,13 @@ dense [a][h][d].
 
 With fused=True the four nodes Scores -> L -> A -> O and the repartition of O run as one
 kernel (ein_attention), which writes O dense and L, never the scores or A.
+
+When Q, K, V lie back to back in one buffer, and so do the relations of W_Q, W_K, W_V, the three
+projections run as one EinSum with a batch label p of extent 3, split 3 ways:
+  QKV_proj[p,s,h,d] = sum_a QKV[p,s,a] W[p,a,h,d]      d = [3,1,1, 3,1,h,1]
+Its input and output relations are exactly the three separate ones laid end to end, so the
+result per element is the same EinSum; the tensor-core kernel sees 3x the tiles in one launch
+(fewer partly filled waves).
 """
 from __future__ import annotations
 
@@ -36,6 +43,7 @@ class AttentionGraph:
         self.fused = fused
         t = s
         self.p_proj = Plan("sa,ahd->shd:mul:sum:in=bf16:out=bf16", [s, a, h, d], [1, 1, 1, h, 1])
+        self.p_proj3 = Plan("psa,pahd->pshd:mul:sum:in=bf16:out=bf16", [3, s, a, h, d], [3, 1, 1, 3, 1, h, 1])
         self.p_scores = Plan(f"shd,thd->hst:mul:sum:in=bf16:alpha={1.0 / math.sqrt(d)!r}", [s, h, d, t],
                              [1, h, 1, 1, h, 1])
         self.p_lse = Plan("hst->hs::lse", [h, s, t], [h, 1, 1])
@@ -44,7 +52,9 @@ class AttentionGraph:
         self.p_out = Plan("shd,ahd->sa:mul:sum:in=bf16", [s, h, d, a], [1, 1, 1, 1, 1, 1])
         bf, f32 = torch.bfloat16, torch.float32
         e = lambda n, dt: torch.empty(n, dtype=dt, device=device)  # noqa: E731
-        self.qp, self.kp, self.vp = e(s * h * d, bf), e(s * h * d, bf), e(s * h * d, bf)  # [h][s][d]
+        self.qkvp = e(3 * s * h * d, bf)  # Q_proj, K_proj, V_proj back to back, each [h][s][d]
+        n = s * h * d
+        self.qp, self.kp, self.vp = self.qkvp[:n], self.qkvp[n:2 * n], self.qkvp[2 * n:]
         self.S = None if fused else e(h * s * t, f32)
         self.L = e(h * s, f32)
         self.A = None if fused else e(h * s * t, bf)
@@ -52,17 +62,29 @@ class AttentionGraph:
         self.O = e(s * h * d, bf)
         self.out = e(s * a, f32)
 
+    @staticmethod
+    def back_to_back(*ts) -> bool:
+        """True when the tensors are contiguous, of one dtype and size, and follow each other in memory."""
+        t0 = ts[0]
+        return all(t.is_contiguous() and t.dtype == t0.dtype and t.numel() == t0.numel() for t in ts) and all(
+            ts[i + 1].data_ptr() == ts[i].data_ptr() + ts[i].numel() * ts[i].element_size() for i in range(len(ts) - 1))
+
     def nodes(self, Q, K, V, WQ, WK, WV, WO):
         """(name, callable, work, unit, bound, kernel launches) per node, in execution order."""
         s, a, h, d = self.s, self.a, self.h, self.d
         shd = [s, h, d]
         gemm = 2 * s * a * h * d
         att = 2 * h * s * s * d
-        return [
-            ("proj Q", lambda: self.p_proj.execute(Q, WQ, self.qp), gemm, "flop", "tensor", 1),
-            ("proj K", lambda: self.p_proj.execute(K, WK, self.kp), gemm, "flop", "tensor", 1),
-            ("proj V", lambda: self.p_proj.execute(V, WV, self.vp), gemm, "flop", "tensor", 1),
-        ] + ([
+        if self.back_to_back(Q, K, V) and self.back_to_back(WQ, WK, WV):
+            proj = [("proj Q, K, V (one EinSum, p = 3)", lambda: self.p_proj3.execute(Q, WQ, self.qkvp), 3 * gemm,
+                     "flop", "tensor", 1)]
+        else:
+            proj = [
+                ("proj Q", lambda: self.p_proj.execute(Q, WQ, self.qp), gemm, "flop", "tensor", 1),
+                ("proj K", lambda: self.p_proj.execute(K, WK, self.kp), gemm, "flop", "tensor", 1),
+                ("proj V", lambda: self.p_proj.execute(V, WV, self.vp), gemm, "flop", "tensor", 1),
+            ]
+        return proj + ([
             ("attention (Scores -> L -> exp -> A.V fused)",
              lambda: attention(self.qp, self.kp, self.vp, self.O, s, s, h, d, lse=self.L),
              2 * att, "flop", "tensor", 1),

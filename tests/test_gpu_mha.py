@@ -70,3 +70,40 @@ def test_attention_full_size_sampled_rows(lib, cuda):
     check_bf16_bar(S, ref["S"])
     L = as_f64(from_dev(g.L)).reshape(h, s)[:, rows]
     check_bf16_bar(L, ref["L"])
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_packed_projections_one_einsum(lib, cuda, fused):
+    # Q, K, V (and the relations of W_Q, W_K, W_V) back to back in one buffer: the three
+    # projections run as one EinSum with a batch label p = 3 split 3 ways; every node still
+    # matches the oracle's chain, and the projections agree with the three separate launches
+    import torch
+
+    from tensor_relational_algebra_gb300.eingraph import AttentionGraph
+
+    s, a, h, d = 512, 512, 4, 128
+    bits = inputs(s, a, h, d, 22)
+    dev = [torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda().reshape(-1) for b in bits]
+    g_sep = AttentionGraph(s, a, h, d, fused=fused)
+    ws = [g_sep.projection_weight(w) for w in dev[3:6]]
+    qkv = torch.cat(dev[:3])
+    wqkv = torch.cat(ws)
+    n, m = s * a, a * h * d
+    packed = [qkv[:n], qkv[n:2 * n], qkv[2 * n:], wqkv[:m], wqkv[m:2 * m], wqkv[2 * m:], dev[6]]
+    g = AttentionGraph(s, a, h, d, fused=fused)
+    names = [nd[0] for nd in g.nodes(*packed)]
+    assert names[0].startswith("proj Q, K, V") and not any(x in ("proj K", "proj V") for x in names)
+    g(*packed)
+    g_sep(*dev[:3], *ws, dev[6])
+    lib.ein_status()
+    torch.cuda.synchronize()
+    ref = mha.chain(*[f32(b) for b in bits], engine="blas")
+    for t, key in ((g.qp, "Qp"), (g.kp, "Kp"), (g.vp, "Vp")):
+        check_bf16_bar(as_f64(otra.unblock(from_dev(t), (s, h, d), [1, h, 1])), ref[key])
+    check_bf16_bar(as_f64(from_dev(g.O)).reshape(s, h, d), ref["O"])
+    check_bf16_bar(as_f64(from_dev(g.out)).reshape(s, a), ref["out"])
+    # against the three separate projections: the same EinSum, summed in another order only in
+    # tiles whose K loop the last wave splits (bf16 outputs: within one bf16 rounding)
+    for t_p, t_s in ((g.qp, g_sep.qp), (g.kp, g_sep.kp), (g.vp, g_sep.vp)):
+        x, y = as_f64(from_dev(t_p)), as_f64(from_dev(t_s))
+        assert np.all(np.abs(x - y) <= 2.0 ** -7 * np.maximum(np.abs(x), np.abs(y)) + 1e-4 * np.abs(y).max())
