@@ -426,7 +426,10 @@ class C4fWorkload(C4Workload):
         self.outputs_dev = [self.g.out]
 
     def traffic_key(self, j):
-        return ("k_attn.cu", "attention s=4096 h=32 d=128" if self.steps[j].name.startswith("attention") else "-")
+        name = self.steps[j].name
+        if name.startswith("proj Q, K, V"):
+            return ("k_tc.cu", "tc_gemm projections QKV s=a=4096 h=32 d=128")
+        return ("k_attn.cu", "attention s=4096 h=32 d=128" if name.startswith("attention") else "-")
 
 
 class C5Workload(_PointsWorkload):
