@@ -273,6 +273,7 @@ class C1Workload(_PointsWorkload):
     dtype = "f32"
     name = "matmul 64x64x64 fp32 U[-1,1], d in {[4,1,1,4],[1,4,4,1],[2,2,2,2]} (three executions per step)"
     d = [[4, 1, 1, 4], [1, 4, 4, 1], [2, 2, 2, 2]]
+    single_core_baseline = True  # the oracle is timed on all host cores and on one
 
     def host_inputs(self):
         import datagen
@@ -821,6 +822,15 @@ def run_ours(args):
         dt = time.perf_counter() - t0
         cpu = {"value": work / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
                "sample": wl.sample_text(rows), "seconds": round(dt, 2)}
+        if getattr(wl, "single_core_baseline", False):
+            # the same sample on one host core as well
+            threads = oracle.num_threads()
+            oracle.set_num_threads(1)
+            t0 = time.perf_counter()
+            wl.oracle_sample(host, 0, rows)
+            dt1 = time.perf_counter() - t0
+            oracle.set_num_threads(threads)
+            cpu["single_core"] = {"value": work / dt1 / 1e12, "seconds": round(dt1, 3)}
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,

@@ -25,5 +25,5 @@ against closed forms, library routines on special cases, brute force and the
 pages' own formulas.  The repartition-cost term (section 3.1 gives no formula)
 is pinned by invariants only: "parity unpinned" for that one function.
 """
-from .einsum import OPS, AGGS, einsum, einsum_points, num_threads, build  # noqa: F401
+from .einsum import OPS, AGGS, einsum, einsum_points, num_threads, set_num_threads, build  # noqa: F401
 from . import tra, rounding, mha  # noqa: F401

@@ -48,6 +48,8 @@ def _load():
         lib.oracle_einsum_points.argtypes = [i32, vp, i32, vp, vp, i32, vp, vp, i32, vp, i64, vp, vp, i32, i32, dbl]
         lib.oracle_einsum_points.restype = i32
         lib.oracle_num_threads.restype = i32
+        lib.oracle_set_num_threads.argtypes = [i32]
+        lib.oracle_set_num_threads.restype = None
         _lib = lib
     return _lib
 
@@ -55,6 +57,11 @@ def _load():
 def num_threads() -> int:
     """Threads the oracle's OpenMP loops use on this host."""
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads for the oracle's OpenMP loops from now on (1: a single-core run)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def parse(eq: str):

@@ -193,3 +193,13 @@ int oracle_num_threads(void) {
     return 1;
 #endif
 }
+
+/* Threads for the OpenMP loops above (n >= 1); no effect without OpenMP. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    extern void omp_set_num_threads(int);
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
