@@ -245,3 +245,24 @@ def test_attention_function_survives_the_eingraph_import(lib):
 
     assert callable(lib.attention) and not isinstance(lib.attention, types.ModuleType)
 
+
+
+def test_maximum_sizes(lib):
+    # tensors of up to 2^31 - 1 elements plan; one element more is refused, as is a bound past
+    # 2^31 - 1; cost terms are 64-bit (n_tasks * (|X_sub| + |Y_sub|) passes 2^31 here)
+    big = 2 ** 31 - 1
+    p = lib.Plan("ij,jk->ik:add:max", [big, 1, 1], [1, 1, 1, 1])
+    assert p.info.x_sub == big and p.info.z_sub == big and p.cost_join == big + 1
+    q = lib.Plan("ij,jk->ik:mul:sum", [65536, 16384, 2], [8, 1, 1, 2])
+    assert q.n_tasks == 16 and q.cost_join == 16 * (8192 * 16384 + 16384) > 2 ** 31
+    for spec, bounds, d, code in [
+        ("ij,jk->ik:add:max", [2 ** 31, 1, 1], [1, 1, 1, 1], "TRA_ERR_ARG"),
+        ("ij,jk->ik:add:max", [65536, 32768, 1], [1, 1, 1, 1], "TRA_ERR_UNSUPPORTED"),
+        ("bij,bjk->bik:add:max", [2, 46341, 46341, 1], [1, 1, 1, 1, 1, 1], "TRA_ERR_UNSUPPORTED"),
+    ]:
+        with pytest.raises(lib.TraError) as e:
+            lib.Plan(spec, bounds, d)
+        assert code in str(e.value), (spec, bounds)
+    with pytest.raises(lib.TraError) as e:
+        lib.ein_repartition([65536, 32768], [1, 1], [2, 1], 4, 0x1000, 0x2000, 0)
+    assert "TRA_ERR_UNSUPPORTED" in str(e.value)
