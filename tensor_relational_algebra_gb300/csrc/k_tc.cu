@@ -86,11 +86,11 @@ struct TcParams {
     int* mark_count;  // epilogue 2: incremented once per output marked NaN (may be null)
     // Work units (see unit_of): tiles [0, n_full) whole; tiles [n_full, n_tiles) of the last,
     // partly filled wave split into `split` runs of K steps on as many idle workers.  Parts
-    // 0 .. split-2 leave fp32 partial sums in `part`; each part waits for the one before it
-    // through one flag per (tile, epilogue warp), so the sum order is fixed.
+    // 0 .. split-2 each leave fp32 partial sums in a slot of `part` and release them through one
+    // flag per (tile, part, epilogue warp); the last part adds them in part order.
     uint32_t n_full, split, n_units;
-    float* part;                 // [tile - n_full][epilogue warp slot][column block][register][lane]
-    unsigned long long* flags;   // [tile - n_full][epilogue warp slot]: tag | parts done
+    float* part;                 // [tile - n_full][part][lane quarter][column block][register][lane]
+    unsigned long long* flags;   // [tile - n_full][part][epilogue warp]: tag | 1 once released
     unsigned long long tag;      // this launch's flag tag (the low 8 bits are zero)
 };
 
@@ -442,12 +442,10 @@ __device__ __forceinline__ void set_flag(unsigned long long* f, unsigned long lo
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(f), "l"(v) : "memory");
 }
 
-// A non-final part of a split tile: wait for the previous part (if any), add its partial
-// sums, leave this warp's running sums in the partial buffer, release the next part.
-__device__ __forceinline__ bool split_partial(const TcParams& p, uint32_t tmem_acc, uint32_t q, uint32_t half,
-                                              int lane, uint32_t part, float* pw, unsigned long long* flag,
-                                              volatile int* abort) {
-    if (part > 0 && !wait_flag(flag, p.tag | part, abort, p.timeout_ns)) return false;
+// A part of a split tile other than the last: leave this warp's sums in the part's own slot of
+// the partial buffer and release them (no wait: every such part runs at once).
+__device__ __forceinline__ void split_partial(const TcParams& p, uint32_t tmem_acc, uint32_t q, uint32_t half,
+                                              int lane, float* pw, unsigned long long* flag) {
     const uint32_t nblk = p.block_n / 32;
     const uint32_t taddr = tmem_acc + ((q * 32u) << 16);
     for (uint32_t c = 2 * half; c < nblk; c += 4) {
@@ -455,23 +453,19 @@ __device__ __forceinline__ bool split_partial(const TcParams& p, uint32_t tmem_a
         tmem_ld32_nowait(taddr + c * 32u, ra);
         tmem_ld32_nowait(taddr + c * 32u + 32u, rb);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        if (part > 0) {
-            add_partial(ra, pw, c, lane);
-            add_partial(rb, pw, c + 1, lane);
-        }
         put_partial(ra, pw, c, lane);
         put_partial(rb, pw, c + 1, lane);
     }
     __threadfence();
     __syncwarp();
-    if (lane == 0) set_flag(flag, p.tag | (part + 1));
-    return true;
+    if (lane == 0) set_flag(flag, p.tag | 1u);
 }
 
 template <int EPI>
 __device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorMap* map_z, uint8_t* epi,
                                               uint32_t tmem_acc, uint32_t q, uint32_t half, int lane, uint32_t b,
-                                              uint32_t m, uint32_t n0, const float* addp = nullptr) {
+                                              uint32_t m, uint32_t n0, const float* addp = nullptr, uint32_t nadd = 0,
+                                              size_t add_stride = 0) {
     float4* stg = reinterpret_cast<float4*>(epi + (q + 4 * half) * kEpiTile);
     const uint32_t nblk = p.block_n / 32;  // block_n is a multiple of 64
     const uint32_t taddr = tmem_acc + ((q * 32u) << 16);
@@ -503,9 +497,9 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorM
             tmem_ld32_nowait(taddr + c * 32u, ra);
             tmem_ld32_nowait(taddr + c * 32u + 32u, rb);
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            if (addp) {
-                add_partial(ra, addp, c, lane);
-                add_partial(rb, addp, c + 1, lane);
+            for (uint32_t j = 0; j < nadd; ++j) {  // the other parts' sums, in part order
+                add_partial(ra, addp + j * add_stride, c, lane);
+                add_partial(rb, addp + j * add_stride, c + 1, lane);
             }
             apply_terms<EPI>(p, ra, rt, b, n0 + c * 32u);
             apply_terms<EPI>(p, rb, rt, b, n0 + c * 32u + 32u);
@@ -547,9 +541,9 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorM
         tmem_ld32_nowait(taddr + c * 32u, ra);
         tmem_ld32_nowait(taddr + c * 32u + 32u, rb);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        if (addp) {
-            add_partial(ra, addp, c, lane);
-            add_partial(rb, addp, c + 1, lane);
+        for (uint32_t j = 0; j < nadd; ++j) {
+            add_partial(ra, addp + j * add_stride, c, lane);
+            add_partial(rb, addp + j * add_stride, c + 1, lane);
         }
         apply_terms<EPI>(p, ra, rt, b, n0 + c * 32u);
         apply_terms<EPI>(p, rb, rt, b, n0 + c * 32u + 32u);
@@ -559,10 +553,11 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorM
 }
 
 // One unit's epilogue for one epilogue warp.  A whole tile goes out as before.  Of a split tile
-// (plain epilogue only), parts before the last leave running sums in the partial buffer; the
-// last part adds them to its accumulator and stores the tile, then clears its flag.  rank: the
-// CTA's rank in its pair (0 for one CTA per tile); regions: TMEM lane quarters per tile (4 per
-// CTA).  False when a wait gave up.
+// (plain epilogue only), the parts before the last each leave their sums in a slot of their
+// own; the last part waits for all of them, adds them to its accumulator in part order (a fixed
+// order: results are deterministic), stores the tile and clears the flags.  rank: the CTA's rank
+// in its pair (0 for one CTA per tile); regions: TMEM lane quarters per tile (4 per CTA).  False
+// when a wait gave up.
 __device__ __forceinline__ bool epilogue_unit(const TcParams& p, const CUtensorMap* map_z, uint8_t* epi,
                                               uint32_t tmem_acc, uint32_t q, uint32_t half, int lane, uint32_t b,
                                               uint32_t mrow, uint32_t n0, uint32_t tile, uint32_t part, uint32_t rank,
@@ -573,13 +568,20 @@ __device__ __forceinline__ bool epilogue_unit(const TcParams& p, const CUtensorM
         else epilogue_tile<2>(p, map_z, epi, tmem_acc, q, half, lane, b, mrow, n0);
         return true;
     }
-    const uint32_t v = tile - p.n_full;
-    float* pw = p.part + ((size_t)v * regions + rank * 4u + q) * (size_t)(p.block_n * 32u);
-    unsigned long long* flag = p.flags + (size_t)v * (2u * regions) + rank * 8u + half * 4u + q;
-    if (part + 1 < p.split) return split_partial(p, tmem_acc, q, half, lane, part, pw, flag, abort);
-    if (!wait_flag(flag, p.tag | part, abort, p.timeout_ns)) return false;
-    epilogue_tile<0>(p, map_z, epi, tmem_acc, q, half, lane, b, mrow, n0, pw);
-    if (lane == 0) *reinterpret_cast<volatile unsigned long long*>(flag) = 0ull;  // ready for the next call
+    // slot (tile, part j) of this warp's lane quarter: partial sums and one flag per epilogue warp
+    const uint32_t others = p.split - 1;
+    const size_t region = (size_t)p.block_n * 32u;
+    float* slot0 = p.part + ((size_t)(tile - p.n_full) * others * regions + rank * 4u + q) * region;
+    unsigned long long* flag0 = p.flags + (size_t)(tile - p.n_full) * others * (2u * regions) + rank * 8u + half * 4u + q;
+    if (part < others) {
+        split_partial(p, tmem_acc, q, half, lane, slot0 + part * regions * region, flag0 + part * 2u * regions);
+        return true;
+    }
+    for (uint32_t j = 0; j < others; ++j)
+        if (!wait_flag(flag0 + j * 2u * regions, p.tag | 1u, abort, p.timeout_ns)) return false;
+    epilogue_tile<0>(p, map_z, epi, tmem_acc, q, half, lane, b, mrow, n0, slot0, others, regions * region);
+    if (lane == 0)  // ready for the next call
+        for (uint32_t j = 0; j < others; ++j) *reinterpret_cast<volatile unsigned long long*>(flag0 + j * 2u * regions) = 0ull;
     return true;
 }
 
@@ -1168,8 +1170,8 @@ bool tc_plan(Plan* p) {
             t->split = s;
             t->n_full = n_full;
             const uint64_t R = t->n_tiles - n_full, tile = (uint64_t)(t->pair ? 2 * kBlockM : kBlockM) * t->block_n;
-            t->ws_part = align256(R * tile * 4);
-            t->ws_flags = align256(R * (t->pair ? 16 : 8) * 8);
+            t->ws_part = align256(R * (s - 1) * tile * 4);
+            t->ws_flags = align256(R * (s - 1) * (t->pair ? 16 : 8) * 8);
             p->ws_bytes = t->ws_part + t->ws_flags;
         }
     }
@@ -1335,7 +1337,8 @@ int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_
     if (t.split > 1 && !ex && ws) {
         split_config(t.n_tiles, workers, t.num_kb, n_full, split);
         const uint64_t R = t.n_tiles - n_full, tile = (uint64_t)(t.pair ? 2 * kBlockM : kBlockM) * t.block_n;
-        if (split > 1 && (align256(R * tile * 4) > t.ws_part || align256(R * (t.pair ? 16 : 8) * 8) > t.ws_flags)) {
+        if (split > 1 && (align256(R * (split - 1) * tile * 4) > t.ws_part ||
+                          align256(R * (split - 1) * (t.pair ? 16 : 8) * 8) > t.ws_flags)) {
             split = 1;
             n_full = t.n_tiles;
         }
