@@ -328,7 +328,7 @@ class C1LiteralWorkload(C1Workload):
 class C3Workload(_PointsWorkload):
     name = "4-D contraction C[a,b,c,d]=sum_e,f A[a,b,e,f]B[c,f,e,d], 64^6 BF16 in / FP32 out, d=[4,1,1,1,4,1,1,1]; + repartition of C [4,1,4,1]->[1,4,1,4]"
     d = [4, 1, 1, 1, 4, 1, 1, 1]
-    cpu_default = 65536  # contraction outputs (about 8 s of the oracle on 16 host cores)
+    cpu_default = 4194304  # contraction outputs (about 8 s of the oracle on 16 host cores)
 
     def host_inputs(self):
         return [_bf16_host((64,) * 4, 0 + self.seed_offset, 0), _bf16_host((64,) * 4, 0 + self.seed_offset, 1)]
@@ -378,7 +378,7 @@ def _packed_dev(torch, inputs):
 class C4Workload(_PointsWorkload):
     name = "multi-head attention EinGraph s=4096 a=4096 h=32 d=128, BF16 activations N(0,1), weights N(0,0.02)"
     d = "projections split h=32 (head-major outputs); scores/lse/exp/A.V split h=32; repartition of O to dense"
-    cpu_default = 49152  # Q-projection outputs (about 10 s of the oracle)
+    cpu_default = 2457600  # Q-projection outputs (about 8 s of the oracle on 16 host cores)
 
     def host_inputs(self):
         s, a, h, d = 4096, 4096, 32, 128
