@@ -87,6 +87,9 @@ SemiringParams semiring_params(const Plan& p, const void* x, const void* y, void
     sp.y_ncontig = affine_stride(sp.yn) == 1;
     sp.y_kcontig = affine_stride(sp.yk) == 1;
     set_load_modes(sp, p.in_bf16, p.vec_flags);
+    cudaPointerAttributes pa;
+    sp.z_device = z && cudaPointerGetAttributes(&pa, z) == cudaSuccess && pa.type == cudaMemoryTypeDevice;
+    (void)cudaGetLastError();
     return sp;
 }
 

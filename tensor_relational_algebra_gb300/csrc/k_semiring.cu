@@ -194,10 +194,15 @@ __device__ __forceinline__ void decode_tile(const SemiringParams& p, uint32_t& b
 // Thread (ty, tx) owns rows ty*4+{0..3}, 64+ty*4+{0..3} and columns tx*4+{0..3},
 // 64+tx*4+{0..3} of the tile.  The caller guarantees every shared buffer passed here is
 // free (all threads past their last read of it).
-template <int EPI>
+// stg (BULK): a free 64 KB of shared memory.  When the output is fp32 and each of the tile's
+// 128-column row segments is contiguous and 16-byte aligned in Z, the tile is staged there
+// and leaves as one 512-byte bulk copy per row: the CTA waits only until shared memory has
+// been read, and the writes to HBM drain while the next CTA on the SM computes (the CTAs of
+// a wave finish together, so direct stores would all stall on the same write burst).
+template <int EPI, bool BULK = false>
 __device__ __forceinline__ void tile_epilogue(const SemiringParams& p, float (&acc)[8][8], uint32_t b, uint32_t m0,
                                               uint32_t n0, int64_t* rowZ, int64_t* colZ, float* rterms,
-                                              float* cterms) {
+                                              float* cterms, float* stg = nullptr) {
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
     if (tid < BM) {
         const uint32_t m = min(m0 + tid, p.M - 1);
@@ -211,6 +216,47 @@ __device__ __forceinline__ void tile_epilogue(const SemiringParams& p, float (&a
         if (EPI == kEpiSqExpand) cterms[tid - BM] = p.ynorm[(uint64_t)b * p.N + n];
     }
     __syncthreads();
+    if (BULK) {
+        const bool rows_contiguous = __syncthreads_and(
+            !p.out_bf16 && p.z_vec4 && p.z_device && (reinterpret_cast<uintptr_t>(p.z) & 15) == 0 && n0 + BN <= p.N &&
+            (tid >= BN || colZ[tid] == colZ[0] + tid));
+        if (rows_contiguous) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int mi = (i < 4) ? ty * 4 + i : 64 + ty * 4 + (i - 4);
+                const float rterm = EPI == kEpiPlain ? 0.f : rterms[mi];
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    const int nb = g * 64 + tx * 4;
+                    float v[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        float a = acc[i][g * 4 + c];
+                        if (EPI == kEpiLse) {
+                            a = a > 1e-30f ? rterm + cterms[nb + c] + logf(a) : __int_as_float(0x7fc00000);
+                        } else if (EPI == kEpiSqExpand) {
+                            a = fmaxf(rterm + cterms[nb + c] - 2.f * a, 0.f);
+                        }
+                        v[c] = p.alpha * a;
+                    }
+                    *reinterpret_cast<float4*>(stg + mi * BN + nb) = make_float4(v[0], v[1], v[2], v[3]);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncthreads();
+            if (tid < BM) {
+                if (m0 + tid < p.M) {
+                    float* dst = reinterpret_cast<float*>(p.z) + rowZ[tid] + colZ[0];
+                    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                                 "r"((uint32_t)__cvta_generic_to_shared(stg + tid * BN)), "r"(BN * 4)
+                                 : "memory");
+                }
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            }
+            return;
+        }
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int mi = (i < 4) ? ty * 4 + i : 64 + ty * 4 + (i - 4);
@@ -351,7 +397,10 @@ __global__ void __launch_bounds__(NT, 2) semiring_async(const __grid_constant__ 
     }
     cp_async_wait<0>();
     __syncthreads();
-    tile_epilogue<EPI>(p, acc, b, m0, n0, rowX, colY, Xs, Ys);
+    // staging: the first 64 KB of the pipeline stages; row / column terms past it (in the last
+    // Y stage)
+    float* terms = Ys + 2 * (ABK * BN);
+    tile_epilogue<EPI, true>(p, acc, b, m0, n0, rowX, colY, terms, terms + BM, dsm);
 }
 
 // ---------------------------------------------------------------- register-staged kernel

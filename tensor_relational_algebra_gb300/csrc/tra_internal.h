@@ -111,6 +111,9 @@ struct SemiringParams {
     // the underflow fix-up returns at once when this count (written by the producer of the
     // marks) is zero; null: scan every output
     const int* mark_count;
+    // 1 when z is device memory (the bulk-copy epilogue writes only there; pinned host memory
+    // the device can address gets plain stores)
+    int32_t z_device;
 };
 
 // Per-operand row-max / exp-shift preparation of the factored logsumexp.
