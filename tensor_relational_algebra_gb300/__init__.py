@@ -349,7 +349,9 @@ class Plan:
 
     def execute(self, x, y, z, workspace=None, stream=None):
         """Run the plan on device tensors in the relation layout of d.  When the plan needs
-        scratch and none is given, a torch buffer is allocated once and kept with the plan."""
+        scratch and none is given, a torch buffer is allocated once and kept with the plan, so
+        calls of one plan that may overlap on the GPU (other streams) must each pass their own
+        workspace."""
         if workspace is None and self.info.workspace_bytes:
             ws = getattr(self, "_workspace", None)
             if ws is None or ws.device != z.device:
