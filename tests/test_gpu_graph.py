@@ -70,3 +70,50 @@ def test_attention_step_graph_replay(lib, cuda):
     torch.cuda.synchronize()
     assert torch.equal(replayed, g.out)
     assert not torch.equal(replayed, eager[3])
+
+
+def test_semiring_pair_graph_replay(lib, cuda):
+    # the default workload's step (repartition of Y, squared distance, max-plus) captured once;
+    # replays equal the eager run bit for bit and follow new inputs (the launch path queries
+    # the output's memory type, which must be allowed while capturing)
+    import torch
+
+    M, K, N = 512, 256, 640
+    d = [2, 1, 1, 2]
+    p_sq = lib.Plan("ij,jk->ik:sqdiff:sum", [M, K, N], d)
+    p_mx = lib.Plan("ij,jk->ik:add:max", [M, K, N], d)
+    ws = torch.empty(max(p_sq.workspace_bytes, 256), dtype=torch.uint8, device="cuda")
+    xs = [(datagen.normal_f32((M, K), s, 0), datagen.normal_f32((K, N), s, 1)) for s in (41, 42)]
+    x = torch.empty(M * K, device="cuda")
+    y = torch.empty(K * N, device="cuda")
+    yr = torch.empty_like(y)
+    zs = torch.empty(M * N, device="cuda")
+    zm = torch.empty_like(zs)
+
+    def step():
+        lib.repartition(y, yr, [K, N], [1, 1], [1, 2])
+        p_sq.execute(x, yr, zs, ws)
+        p_mx.execute(x, yr, zm)
+
+    eager = []
+    for X, Y in xs:
+        x.copy_(torch.from_numpy(X).reshape(-1))
+        y.copy_(torch.from_numpy(Y).reshape(-1))
+        step()
+        eager.append((zs.cpu().clone(), zm.cpu().clone()))
+    lib.ein_status()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        step()
+    for i in (1, 0, 1):
+        X, Y = xs[i]
+        x.copy_(torch.from_numpy(X).reshape(-1))
+        y.copy_(torch.from_numpy(Y).reshape(-1))
+        zs.zero_()
+        zm.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(zs.cpu(), eager[i][0]) and torch.equal(zm.cpu(), eager[i][1])
+    lib.ein_status()
