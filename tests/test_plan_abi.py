@@ -266,3 +266,20 @@ def test_maximum_sizes(lib):
     with pytest.raises(lib.TraError) as e:
         lib.ein_repartition([65536, 32768], [1, 1], [2, 1], 4, 0x1000, 0x2000, 0)
     assert "TRA_ERR_UNSUPPORTED" in str(e.value)
+
+
+def test_back_to_back_detection():
+    # the attention EinGraph batches its three projections only when Q, K, V (and the three
+    # weight relations) are contiguous views that follow each other in one buffer
+    import torch
+
+    from tensor_relational_algebra_gb300.eingraph import AttentionGraph
+
+    buf = torch.zeros(30, dtype=torch.bfloat16)
+    assert AttentionGraph.back_to_back(buf[:10], buf[10:20], buf[20:])
+    assert not AttentionGraph.back_to_back(buf[:10], buf[20:], buf[10:20])          # out of order
+    assert not AttentionGraph.back_to_back(buf[:10], buf[10:20], torch.zeros(10, dtype=torch.bfloat16))
+    assert not AttentionGraph.back_to_back(buf[:10], buf[10:19], buf[19:29])        # sizes differ
+    assert not AttentionGraph.back_to_back(buf[:10], buf[10:20].float(), buf[20:])  # dtypes differ
+    strided = torch.zeros(60, dtype=torch.bfloat16)[::2]
+    assert not AttentionGraph.back_to_back(strided[:10], strided[10:20], strided[20:])  # not contiguous
