@@ -22,8 +22,11 @@ summation + tensor relational algebra".
 
 Parity pins: every function above is checked in ``tests/test_oracle_pins.py``
 against closed forms, library routines on special cases, brute force and the
-pages' own formulas.  The repartition-cost term (section 3.1 gives no formula)
-is pinned by invariants only: "parity unpinned" for that one function.
+pages' own formulas.  The repartition-cost term (section 3.1 gives no formula) is
+pinned where the pages fix it -- between the centralized layout (d all ones) and N
+blocks, the Scatter / Gather traffic (N-1)/N * M of the communication-primitive
+table on rkmt.cn/news/51250.html -- and by invariants elsewhere: between two
+partitioned layouts it is "parity unpinned".
 """
 from .einsum import OPS, AGGS, einsum, einsum_points, num_threads, set_num_threads, build  # noqa: F401
 from . import tra, rounding, mha  # noqa: F401

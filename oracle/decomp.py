@@ -12,7 +12,8 @@ parallelism constraint (here p_min <= tasks <= p_max) and whose entries divide t
 This module enumerates every combination of every node's candidates and evaluates the
 whole cost from its definition: the join and aggregation terms come from the enumerated
 join (``tra.plan_bruteforce``), the repartition term from the element-wise count
-(``tra.repartition_cost_bruteforce``; parity of that term with the pages is unpinned).
+(``tra.repartition_cost_bruteforce``; pinned to the pages' Scatter / Gather traffic only
+between the centralized layout and a partitioned one).
 Exponential: tiny graphs only.  Graph inputs cost nothing (they arrive partitioned as their
 consumer asks).
 

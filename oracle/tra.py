@@ -29,8 +29,10 @@ Readings of points the pages leave open:
     and d);
   * n_agg is the product of the contracted labels' partition counts;
   * the repartition term (section 3.1 gives no formula): elements whose owner
-    changes when blocks are owned by their row-major linear key id.  Parity
-    unpinned: only invariants and brute force on tiny shapes check it.
+    changes when blocks are owned by their row-major linear key id.  Pinned to
+    the Scatter / Gather traffic (N-1)/N * M of rkmt.cn/news/51250.html (table of
+    traffic per communication primitive) between d all ones and N blocks; between
+    two partitioned layouts parity is unpinned (invariants and brute force only).
 Canonical task order (a tie-break the pages do not set): output key in
 row-major order, then the contracted labels' key components (first-appearance
 order, X then Y) in row-major order.  Keys are linearised row-major.

@@ -268,7 +268,74 @@ def test_literal_4d_contraction_and_unary():
                                logsumexp(S.astype(np.float64), axis=2), rtol=1e-13)
 
 
-# ---------------------------------------------------------------- repartition cost (parity unpinned)
+# ---------------------------------------------------------------- repartition cost
+def _divisor_vectors(shape):
+    out = [[]]
+    for B in shape:
+        out = [v + [D] for v in out for D in range(1, B + 1) if B % D == 0]
+    return out
+
+
+def test_repartition_cost_scatter_gather_pin():
+    # rkmt.cn/news/51250.html, traffic per communication primitive: Scatter (centralized ->
+    # partitioned) and Gather (partitioned -> centralized) each move (N-1)/N of the variable.
+    # d = all ones is the centralized tensor (one block, owned by block id 0); a d with
+    # N = prod(D) blocks spreads it over N owners.  Every divisor vector of three tiny shapes,
+    # both directions, element by element.
+    for shape in [(4, 6), (2, 3, 4), (4, 4, 4, 4), (12,)]:
+        ones = [1] * len(shape)
+        n = int(np.prod(shape))
+        for d in _divisor_vectors(shape):
+            N = int(np.prod(d))
+            want = (N - 1) * n // N
+            assert (N - 1) * n % N == 0
+            assert tra.repartition_cost_bruteforce(shape, ones, d) == want, (shape, d)
+            assert tra.repartition_cost_bruteforce(shape, d, ones) == want, (shape, d)
+    with open(os.path.join(GOLD, "repartition_scatter_gather.json")) as f:
+        gold = json.load(f)
+    for c in gold["cases"]:
+        if c["M"] <= 1024:  # the brute force walks every element
+            ones = [1] * len(c["shape"])
+            assert tra.repartition_cost_bruteforce(c["shape"], ones, c["d"]) == c["cost"]
+            assert tra.repartition_cost_bruteforce(c["shape"], c["d"], ones) == c["cost"]
+
+
+def test_repartition_cost_pin_rejects_plausible_mistakes():
+    # Negative controls for the pin above: rules a slip could produce, each evaluated by the
+    # same element walk, must miss (N-1)/N * M on some divisor vector.
+    def walk(shape, src, dst, rule):
+        n = int(np.prod(shape))
+        total = 0
+        blocks = set()
+        for flat in range(n):
+            idx = np.unravel_index(flat, shape)
+            own = []
+            for d in (src, dst):
+                key = [int(i) // (B // D) for i, B, D in zip(idx, shape, d)]
+                lin = 0
+                for k, D in zip(key, d):
+                    lin = lin * D + k
+                own.append((lin, int(np.prod(d))))
+            if rule == "owner_from_first_index":  # the linear id dropped every dimension but the first
+                k0 = [int(idx[0]) // (shape[0] // d[0]) for d in (src, dst)]
+                changed = k0[0] != k0[1]
+            else:
+                changed = own[0][0] != own[1][0]
+            if changed:
+                total += 1
+                blocks.add(own[1][0])
+        return len(blocks) if rule == "count_blocks" else (2 * total if rule == "both_sides" else total)
+
+    shape = (4, 6)
+    for rule in ("owner_from_first_index", "count_blocks", "both_sides"):
+        missed = False
+        for d in _divisor_vectors(shape):
+            N = int(np.prod(d))
+            if walk(shape, [1, 1], d, rule) != (N - 1) * 24 // N:
+                missed = True
+        assert missed, rule
+
+
 def test_repartition_cost_invariants():
     shape = (4, 4, 4, 4)
     ds = [[4, 1, 4, 1], [1, 4, 1, 4], [2, 2, 2, 2], [1, 1, 1, 1], [4, 4, 1, 1]]

@@ -216,6 +216,17 @@ def test_repartition_cost_matches_bruteforce(lib):
         lib.repartition_cost((6, 4), [4, 1], [1, 1])
 
 
+def test_repartition_cost_scatter_gather_golden(lib):
+    # rkmt.cn/news/51250.html: Scatter / Gather move (N-1)/N of the variable (M elements over N
+    # nodes); the library's term between the centralized layout (d all ones) and N blocks, both ways
+    with open(os.path.join(os.path.dirname(__file__), "golden", "repartition_scatter_gather.json")) as f:
+        gold = json.load(f)
+    for c in gold["cases"]:
+        ones = [1] * len(c["shape"])
+        assert lib.repartition_cost(c["shape"], ones, c["d"]) == c["cost"], c
+        assert lib.repartition_cost(c["shape"], c["d"], ones) == c["cost"], c
+
+
 def test_execute_argument_errors(lib):
     p = lib.Plan("ij,jk->ik:add:lse", [64, 64, 64], [1, 1, 1, 1])
     with pytest.raises(lib.TraError) as e:
