@@ -1,18 +1,20 @@
 #!/usr/bin/env python3
 """Throughput of the TRA join + aggregate hot path on one GB300 (one JSON line).
 
-Default workload: the extended-semiring pair of "EinDecomp ... tensor relational
-algebra" section 2.1 -- squared distance D[i,k] = sum_j (X[i,j]-Y[j,k])^2 and
-max-plus Z[i,k] = max_j (X[i,j]+Y[j,k]) -- with X 8192x256 and Y 256x8192 fp32
-N(0,1), partition vector d = [8,1,1,8] (64 join tuples).  One step = partition
-the dense Y into its relation (X under [8,1] is already laid out as its
-relation), then both join + aggregate EinSums.
+Default workload (``c5``): the largest single-GPU configuration, the matrix multiply of
+"EinDecomp ... tensor relational algebra" section 2.1 at 16384 x 16384 x 16384, BF16
+inputs N(0,1), FP32 accumulate, partition vector d = [1,1,1,1] (``--d`` for the others):
+one join + aggregate on the tcgen05 tensor cores per step.  In the same process, after
+the headline line's own measurement, the default run also times (device-resident, same
+timing rules) the extended-semiring pair (``pair``: squared distance and max-plus, X
+8192x256, Y 256x8192 fp32, d = [8,1,1,8]) and the 4-D contraction with the repartition
+of its output (``c3``); they are reported under ``extra_workloads`` (``--extra`` picks
+them, ``--extra none`` skips them).
 
-Other workloads (``--workload``): c1 (64^3 fp32 matmul under three d), c3 (4-D
-BF16 contraction + repartition of its output), c4 (multi-head-attention
-EinGraph; c4f the same with the attention chain fused into one kernel), c5
-(16384^3 BF16 matmul, ``--d``), c5b (8192^3 logsumexp); c2s and c5bs run the squared
-distance of the pair and the 8192^3 logsumexp with split=bf16x3 (tensor cores).
+Other workloads (``--workload``): pair, c1 (64^3 fp32 matmul under three d), c3, c4
+(multi-head-attention EinGraph; c4f the same with the attention chain fused into one
+kernel), c5b (8192^3 logsumexp); c2s and c5bs run the squared distance of the pair and
+the 8192^3 logsumexp with split=bf16x3 (tensor cores).
 
 ``--impl reference`` times the CPU oracle on a bounded sample of the same
 workload (the reference arm).  Under torchrun (N > 1) every rank runs an
@@ -249,6 +251,14 @@ class _PointsWorkload:
         if d is not None:
             self.d = list(d)
 
+    def f64_inputs(self, inputs, bf16=True):
+        """The oracle's double inputs, converted once (outside any timed oracle sample)."""
+        if getattr(self, "_f64", None) is None:
+            from datagen import bf16_bits_to_f32
+
+            self._f64 = [(bf16_bits_to_f32(a) if bf16 else a).astype(np.float64) for a in inputs]
+        return self._f64
+
     def oracle_points(self, eq, X, Y, op, agg, zshape, r0, n, alpha=1.0):
         import oracle
 
@@ -353,9 +363,7 @@ class C3Workload(_PointsWorkload):
         return 2 * 64 ** 6
 
     def oracle_sample(self, inputs, r0, n):
-        from datagen import bf16_bits_to_f32
-
-        A, B = [bf16_bits_to_f32(a).astype(np.float64) for a in inputs]
+        A, B = self.f64_inputs(inputs)
         self.oracle_points("abef,cfed->abcd", A, B, "mul", "sum", (64,) * 4, r0, n)
         return 2 * n * 64 * 64
 
@@ -434,9 +442,10 @@ class C4fWorkload(C4Workload):
 
 
 class C5Workload(_PointsWorkload):
-    name_fmt = "BF16 matmul 16384^3 (FP32 accumulate), d={}"
+    name_fmt = "BF16 matmul Z[i,k]=sum_j X[i,j]Y[j,k] 16384^3, inputs N(0,1), FP32 accumulate, d={}"
     d = [1, 1, 1, 1]
-    cpu_default = 64
+    cpu_default = 262144  # output points (about 10 s of the oracle on 16 host cores)
+    ref_default = 16384
 
     @property
     def name(self):
@@ -464,9 +473,7 @@ class C5Workload(_PointsWorkload):
         return 2 * 16384 ** 3
 
     def oracle_sample(self, inputs, r0, n):
-        from datagen import bf16_bits_to_f32
-
-        X, Y = [bf16_bits_to_f32(a).astype(np.float64) for a in inputs]
+        X, Y = self.f64_inputs(inputs)
         self.oracle_points("ij,jk->ik", X, Y, "mul", "sum", (16384, 16384), r0, n)
         return 2 * n * 16384
 
@@ -511,7 +518,7 @@ class C5bWorkload(_PointsWorkload):
         return 2 * 8192 ** 3
 
     def oracle_sample(self, inputs, r0, n):
-        X, Y = [a.astype(np.float64) for a in inputs]
+        X, Y = self.f64_inputs(inputs, bf16=False)
         self.oracle_points("ij,jk->ik", X, Y, "add", "lse", (8192, 8192), r0, n)
         return 2 * n * 8192
 
@@ -695,6 +702,64 @@ def plan_times(tra, wl, reps: int = 20) -> dict:
     return out
 
 
+def roofline_of(step, ms, peaks, props):
+    """(achieved, peak, unit) of one launch group from its mean device time."""
+    if step.bound == "alu":
+        sm_max = float(peaks.get("sm_max_mhz", 2070.0))
+        pk = props.multi_processor_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+        return step.work / (ms * 1e-3) / 1e12, pk, "TFLOP/s"
+    if step.bound == "tensor":
+        return step.work / (ms * 1e-3) / 1e12, float(peaks.get("bf16_tflops", 1900.0)), "TFLOP/s"
+    return step.work / (ms * 1e-3) / 1e9, float(peaks.get("hbm_gbs", 6800.0)), "GB/s"
+
+
+def roofline_nodes(wl, means, peaks, props):
+    nodes = []
+    for step, ms in zip(wl.steps, means):
+        a, pk, u = roofline_of(step, ms, peaks, props)
+        nodes.append({"name": step.name, "bound": step.bound, "ms": round(ms, 4), "achieved": round(a, 1),
+                      "unit": u, "frac": round(a / pk, 3)})
+    return nodes
+
+
+def peak_source(bound):
+    return ("derived: SMs x 128 FP32 lanes x 2 x max SM clock (MEASURED_PEAKS sm_max_mhz)" if bound == "alu"
+            else "MEASURED_PEAKS.json (of measured)")
+
+
+def extra_workload(torch, tra, name, args, flush, local):
+    """Device-resident timing of one more workload in this process (the same warm-up, step
+    count, L2 flush and clock sampling as the headline), for the extra_workloads record."""
+    wl = WORKLOADS[name]()
+    wl.setup(tra, torch, wl.host_inputs())
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    step_ms, per, wall, clocks = time_steps(torch, wl, args.steps, args.warmup, flush, sampler)
+    peaks, props = measured_peaks(), torch.cuda.get_device_properties(0)
+    means = [statistics.mean(p) for p in per]
+    dom = max(range(len(wl.steps)), key=lambda j: means[j])
+    st = wl.steps[dom]
+    achieved, peak, unit = roofline_of(st, means[dom], peaks, props)
+    total = sum(step_ms)
+    rec = {"workload": wl.name, "key": name, "d": wl.d, "dtype": wl.dtype, "steps": args.steps,
+           "ms_per_step": total / args.steps, "value": job_throughput(wl.ops_per_step(), args.steps, 1, total),
+           "unit": "TFLOP/s",
+           "roofline": {"bound": st.bound, "kernel": st.name, "achieved": achieved, "peak": peak, "unit": unit,
+                        "frac": achieved / peak,
+                        "traffic": traffic_for(*wl.traffic_key(dom)) if hasattr(wl, "traffic_key") else None,
+                        "peak_source": peak_source(st.bound)},
+           "roofline_nodes": roofline_nodes(wl, means, peaks, props),
+           "gpu_launches": args.steps * sum(s.launches for s in wl.steps),
+           "clocks": clocks, "wall_s": round(wall, 3)}
+    if st.bound == "alu" and clocks and clocks.get("sm_mhz"):
+        pk = props.multi_processor_count * FP32_LANES_PER_SM * 2 * clocks["sm_mhz"] * 1e6 / 1e12
+        rec["alu_peak_at_sampled_clock"] = {"sm_mhz": clocks["sm_mhz"], "peak": pk, "frac": achieved / pk}
+    del wl
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
+
+
 def job_throughput(ops_per_step: int, steps: int, world: int, job_ms: float) -> float:
     """Whole-job TFLOP/s: every rank processed its own replica of the workload (weak scaling)."""
     return world * ops_per_step * steps / (job_ms * 1e-3) / 1e12
@@ -794,27 +859,30 @@ def run_ours(args):
     # roofline of the dominant kernel
     peaks = measured_peaks()
     props = torch.cuda.get_device_properties(0)
-    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
     means = [statistics.mean(p) for p in per]
     dom = max(range(len(wl.steps)), key=lambda j: means[j])
     st = wl.steps[dom]
-
-    def roof(step, ms):
-        """(achieved, peak, unit) of one launch group from its mean device time."""
-        if step.bound == "alu":
-            pk = props.multi_processor_count * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
-            return step.work / (ms * 1e-3) / 1e12, pk, "TFLOP/s"
-        if step.bound == "tensor":
-            return step.work / (ms * 1e-3) / 1e12, float(peaks.get("bf16_tflops", 1900.0)), "TFLOP/s"
-        return step.work / (ms * 1e-3) / 1e9, float(peaks.get("hbm_gbs", 6800.0)), "GB/s"
-
-    achieved, peak, unit = roof(st, means[dom])
-    nodes = []
-    for step, ms in zip(wl.steps, means):
-        a, pk, u = roof(step, ms)
-        nodes.append({"name": step.name, "bound": step.bound, "ms": round(ms, 4), "achieved": round(a, 1),
-                      "unit": u, "frac": round(a / pk, 3)})
+    achieved, peak, unit = roofline_of(st, means[dom], peaks, props)
+    nodes = roofline_nodes(wl, means, peaks, props)
     traffic = traffic_for(*wl.traffic_key(dom)) if hasattr(wl, "traffic_key") else None
+    gpu_launches = args.steps * sum(s.launches for s in wl.steps)
+    plan_ms = plan_times(tra, wl)
+
+    # the other workloads of the default run, each with its own timed region (device-resident)
+    extras = []
+    names = [] if args.extra == "none" else [n for n in args.extra.split(",") if n and n != args.workload]
+    wl_name, wl_d, wl_dtype, wl_steps = wl.name, wl.d, wl.dtype, wl.steps
+    if world == 1 and names:
+        # release the headline workload's device and pinned buffers first (the oracle sample
+        # below needs only its host inputs)
+        for k, v in list(vars(wl).items()):
+            if isinstance(v, torch.Tensor) or (isinstance(v, list) and v and isinstance(v[0], torch.Tensor)):
+                delattr(wl, k)
+        pinned_in = pinned_out = None
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        for n in names:
+            extras.append(extra_workload(torch, tra, n, args, flush, local))
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -839,14 +907,12 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (Philox-4x32-10, seeded)",
-        "config": {"workload": wl.name, "d": wl.d, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        "scaling": "weak", "vs_baseline": None, "dtype": wl_dtype, "data": "synthetic (Philox-4x32-10, seeded)",
+        "config": {"workload": wl_name, "d": wl_d, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between steps (512 MiB write outside the step's events)",
-                   "per_launch_group_ms": {s.name: round(m, 4) for s, m in zip(wl.steps, means)}},
+                   "per_launch_group_ms": {s.name: round(m, 4) for s, m in zip(wl_steps, means)}},
         "roofline": {"bound": st.bound, "kernel": st.name, "achieved": achieved, "peak": peak, "unit": unit,
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": ("derived: SMs x 128 FP32 lanes x 2 x max SM clock (MEASURED_PEAKS sm_max_mhz)"
-                                     if st.bound == "alu" else "MEASURED_PEAKS.json (of measured)")},
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_source(st.bound)},
         "roofline_nodes": nodes,
         "alu_peak_at_sampled_clock": (
             {"sm_mhz": clocks["sm_mhz"],
@@ -856,11 +922,14 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d_bytes,
                 "d2h_bytes_per_step": d2h_bytes},
-        "gpu_launches": args.steps * sum(s.launches for s in wl.steps),
-        "plan_ms": plan_times(tra, wl),
+        "gpu_launches": gpu_launches,
+        "plan_ms": plan_ms,
         "clocks": clocks,
         "wall_s": round(wall, 3),
+        "extra_workloads": extras,
     }
+    if wl_dtype == "bf16" and st.bound == "tensor":
+        line["config"]["accumulate"] = "fp32"
     print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
@@ -905,7 +974,9 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="pair")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c5")
+    ap.add_argument("--extra", default="pair,c3",
+                    help="comma-separated workloads also timed (device-resident) in the same run, or 'none'")
     ap.add_argument("--d", type=lambda v: [int(x) for x in v.split(",")], default=None,
                     help="partition vector for c5 / c5b, e.g. 4,2,2,2")
     ap.add_argument("--cpu-rows", type=int, default=None, help="oracle sample size of the CPU baseline")

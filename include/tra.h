@@ -53,7 +53,8 @@ enum {
     TRA_ERR_WORKSPACE = -6,      /* workspace missing or smaller than ein_plan_info's */
     TRA_ERR_CUDA = -7,           /* a CUDA runtime / driver call failed */
     TRA_ERR_TIMEOUT = -8,        /* a bounded device wait gave up (see ein_status) */
-    TRA_ERR_ARG = -9             /* NULL pointer or invalid argument */
+    TRA_ERR_ARG = -9,            /* NULL pointer or invalid argument */
+    TRA_ERR_BOUNDS = -10         /* check builds only: a kernel skipped an index outside its buffer */
 };
 
 #define TRA_MAX_RANK 8
@@ -112,7 +113,13 @@ enum {
  *         contracted.  Options: in=f32|bf16 (both inputs, default f32),
  *         out=f32|bf16 (default f32), alpha=<float> (scales the aggregated value),
  *         mode=fused|literal (literal materialises one partial per join tuple and
- *         combines them in canonical order), sqdiff=direct|expand,
+ *         combines them in canonical order), sqdiff=direct|expand (squared distance as
+ *         sum (x - y)^2, or as |x|^2 + |y|^2 - 2 x.y with one FFMA per tuple; default expand
+ *         for fp32 inputs with a contracted extent K <= 3127, direct otherwise.  The
+ *         expansion cancels where points nearly coincide: every 128 x 128 output tile
+ *         holding an output below tau * (|x|^2 + |y|^2), tau = 3 sqrt(K) 2^-24 / 1e-5, is
+ *         recomputed in the direct form, so results stay within 1e-5 of D relative, down
+ *         to D = 0),
  *         tc=pair|single (BF16 sum-of-products on tensor cores: a 256-row tile
  *         shared by a cluster of two CTAs, or a 128-row tile per CTA; default pair
  *         when the output rows are a multiple of 256 and the columns of 128),
@@ -128,6 +135,8 @@ enum {
  *         mx + my + log sum e^(x-mx) e^(y-my), with the sum of products on BF16 tensor cores,
  *         each fp32 operand split as hi + lo bf16 and the product taken as
  *         hi.hi + hi.lo + lo.hi; per product the relative error is at most 3 * 2^-16.
+ *         The squared distance keeps the expansion's guard with tau = 4.5 sqrt(K) 2^-24 / 1e-5:
+ *         marked 128 x 128 tiles are recomputed on CUDA cores in the direct form.
  *         Default none: these semirings run on CUDA cores).
  * bounds: B_l for every distinct label in first-appearance order (X then Y);
  *         n_bounds must equal the number of distinct labels.  0 <= B_l < 2^31; an
@@ -271,7 +280,9 @@ int ein_attention(int s, int t, int h, int d, float scale, const void* q, const 
 
 /* ein_status -- synchronise the stream, then read and clear the device status word
  * that bounded waits inside the kernels set when they give up.  Returns TRA_OK,
- * TRA_ERR_TIMEOUT or TRA_ERR_CUDA. */
+ * TRA_ERR_TIMEOUT or TRA_ERR_CUDA; in a check build (see ein_build_flags) also
+ * TRA_ERR_BOUNDS when a kernel found an index outside its buffer (the message names the
+ * first check site; the access was skipped, nothing trapped). */
 int ein_status(tra_stream_t stream);
 
 /* ein_execute_sqdist_noalloc -- ein_execute for an fp32 squared-distance plan
@@ -279,16 +290,20 @@ int ein_status(tra_stream_t stream);
  * has no counterpart: this entry point exists for callers that cannot allocate device
  * memory on their path (memory owned by another allocator or a fixed budget, plugins
  * that may not allocate, paths that must not pay for an allocation and the device
- * synchronisation a free implies).  The row / column norms go to a fixed 1 MiB device
- * array inside libtra.so that every GPU loading the library holds until process exit.
+ * synchronisation a free implies).  The row / column norms and the expansion guard's
+ * words (one per 128 x 128 output tile) go to a fixed 1 MiB device array inside
+ * libtra.so that every GPU loading the library holds until process exit.
  * in0/in1/out: as for ein_execute.  The first call on a device (with that device
  * current) looks up the array's device address; make that first call before any
- * stream capture.  All calls share the array: calls whose kernels may overlap on the
- * GPU (unordered streams) race.  Nothing is allocated; no clearing is needed (every
- * norm is rewritten before it is read).
+ * stream capture.  The address is cached per device and context, and looked up again
+ * when the context has changed (after cudaDeviceReset).  All calls share the array:
+ * calls whose kernels may overlap on the GPU (unordered streams) race.  Nothing is
+ * allocated; no clearing is needed (every norm and guard word is rewritten before it
+ * is read).  A squared-distance plan with an empty range (TRA_KERNEL_EMPTY / _FILL)
+ * needs no scratch and runs as under ein_execute.
  * Errors: TRA_ERR_UNSUPPORTED (not an fp32 expanded squared-distance plan),
- * TRA_ERR_WORKSPACE (norms need more than 1 MiB: use ein_execute), TRA_ERR_ARG,
- * TRA_ERR_CUDA. */
+ * TRA_ERR_WORKSPACE (norms and guard words need more than 1 MiB: use ein_execute),
+ * TRA_ERR_ARG, TRA_ERR_CUDA. */
 int ein_execute_sqdist_noalloc(tra_plan_t plan, const void* in0, const void* in1, void* out, tra_stream_t stream);
 
 /* ein_selftest_wait_timeout -- test hook for the bounded device waits: launches one
@@ -297,6 +312,15 @@ int ein_execute_sqdist_noalloc(tra_plan_t plan, const void* in0, const void* in1
  * the same stream must return TRA_ERR_TIMEOUT; the context stays usable.
  * Errors: TRA_ERR_CUDA (launch failure). */
 int ein_selftest_wait_timeout(uint64_t timeout_ns, tra_stream_t stream);
+
+/* ein_build_flags -- how this library was built: TRA_BUILD_CHECK is set in the check build
+ * (libtra_check.so, compiled with -DTRA_CHECK).  There every plain global load and store of
+ * the CUDA-core semiring, reduction, element-wise, split and repartition kernels and the warp
+ * stores of the tensor-core epilogue first test the index against the buffer's extent (the
+ * plan's tensors, the workspace's regions); an access outside is skipped and recorded for
+ * ein_status.  TMA copies need no test: the tensor maps bound them. */
+enum { TRA_BUILD_CHECK = 1 };
+int ein_build_flags(void);
 
 /* ein_plan_destroy -- release a plan (NULL is ignored). */
 void ein_plan_destroy(tra_plan_t plan);

@@ -13,7 +13,11 @@ from __future__ import annotations
 import ctypes
 import os
 
-from ._build import LIB as _LIB_PATH, build as _build_lib
+from ._build import LIB as _LIB_DEFAULT, LIB_CHECK as _LIB_CHECK, build as _build_lib
+
+# TRA_CHECK=1 in the environment selects the check build (bounds tests in the kernels)
+CHECK_BUILD = os.environ.get("TRA_CHECK", "") not in ("", "0")
+_LIB_PATH = _LIB_CHECK if CHECK_BUILD else _LIB_DEFAULT
 
 __all__ = [
     "TraError", "build_library", "load", "Plan", "ein_plan", "ein_plan_info", "ein_plan_keys", "ein_execute",
@@ -27,6 +31,7 @@ TRA_MAX_LABELS = 12
 ERRORS = {
     -1: "TRA_ERR_PARSE", -2: "TRA_ERR_DIVISIBILITY", -3: "TRA_ERR_SHARED_LABEL_D", -4: "TRA_ERR_RANK",
     -5: "TRA_ERR_UNSUPPORTED", -6: "TRA_ERR_WORKSPACE", -7: "TRA_ERR_CUDA", -8: "TRA_ERR_TIMEOUT", -9: "TRA_ERR_ARG",
+    -10: "TRA_ERR_BOUNDS",
 }
 KERNELS = {1: "semiring_f32", 2: "tc_bf16", 3: "row_reduce", 4: "elementwise", 5: "lse_factored", 6: "literal",
            7: "tc_bf16_pair", 8: "tc_split3", 9: "empty", 10: "fill"}
@@ -80,9 +85,10 @@ TRA_DP_POW2 = 1
 _lib = None
 
 
-def build_library(force: bool = False) -> str:
-    """Compile libtra.so in-tree for sm_103a (no-op when up to date)."""
-    return _build_lib(force=force)
+def build_library(force: bool = False, both: bool = False) -> str:
+    """Compile libtra.so in-tree for sm_103a (no-op when up to date); under TRA_CHECK=1 the check
+    build libtra_check.so instead; both=True builds the two."""
+    return _build_lib(force=force, check=CHECK_BUILD, both=both)
 
 
 def load():
@@ -91,7 +97,7 @@ def load():
     if _lib is not None:
         return _lib
     if not os.path.exists(_LIB_PATH):
-        build_library()
+        _build_lib(check=CHECK_BUILD)
     lib = ctypes.CDLL(_LIB_PATH)
     vp, i32, i64, u64p = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.POINTER(ctypes.c_uint64)
     lib.ein_plan.argtypes = [ctypes.c_char_p, vp, i32, vp, i32, ctypes.POINTER(vp)]
@@ -111,6 +117,8 @@ def load():
                                         ctypes.POINTER(tra_cost_model), vp, i32, u64p,
                                         ctypes.POINTER(tra_graph_result)]
     lib.ein_attention.argtypes = [i32, i32, i32, i32, ctypes.c_float, vp, vp, vp, vp, vp, vp]
+    lib.ein_build_flags.argtypes = []
+    lib.ein_build_flags.restype = ctypes.c_int
     for f in ("ein_plan", "ein_plan_info", "ein_plan_keys", "ein_execute", "ein_repartition",
               "ein_repartition_cost", "ein_repartition_messages", "ein_status", "ein_graph_decompose",
               "ein_attention"):

@@ -87,6 +87,9 @@ SemiringParams semiring_params(const Plan& p, const void* x, const void* y, void
     sp.y_ncontig = affine_stride(sp.yn) == 1;
     sp.y_kcontig = affine_stride(sp.yk) == 1;
     set_load_modes(sp, p.in_bf16, p.vec_flags);
+    sp.x_elems = (uint64_t)p.X.total;
+    sp.y_elems = p.unary ? 0 : (uint64_t)p.Y.total;
+    sp.z_elems = (uint64_t)p.Z.total;
     cudaPointerAttributes pa;
     sp.z_device = z && cudaPointerGetAttributes(&pa, z) == cudaSuccess && pa.type == cudaMemoryTypeDevice;
     (void)cudaGetLastError();
@@ -158,6 +161,7 @@ int execute_literal(const Plan& p, const void* x, const void* y, void* z, void* 
     sp.nb = (uint32_t)div;
     sp.alpha = 1.f;
     sp.out_bf16 = 0;
+    sp.z_elems = p.n_tasks * zsub;  // one partial sub-tensor per join tuple
     sp.x_kcontig = affine_stride(sp.xk) == 1;
     sp.y_kcontig = affine_stride(sp.yk) == 1;
     int flags[5];
@@ -194,12 +198,18 @@ int execute_plan(const Plan& p, const void* x, const void* y, void* z, void* ws,
                 lp.nb = sp.nb;
                 lp.K = sp.K;
                 lp.src = x, lp.rmax = xn, lp.b = sp.xb, lp.r = sp.xm, lp.k = sp.xk, lp.R = sp.M;
+                lp.src_elems = sp.x_elems;
                 if ((e = launch_lse_prep(lp, s)) != cudaSuccess) return cuda_fail(e, "norms of X");
                 lp.src = y, lp.rmax = yn, lp.b = sp.yb, lp.r = sp.yn, lp.k = sp.yk, lp.R = sp.N;
+                lp.src_elems = sp.y_elems;
                 if ((e = launch_lse_prep(lp, s)) != cudaSuccess) return cuda_fail(e, "norms of Y");
                 sp.op = kMul;
                 sp.xnorm = xn;
                 sp.ynorm = yn;
+                sp.sq_tau = sqdist_guard_tau(sp.K, kSqGuardFp32);
+                sp.tile_mark = reinterpret_cast<uint32_t*>((char*)ws + align256((uint64_t)sp.nb * sp.M * 4) +
+                                                           align256((uint64_t)sp.nb * sp.N * 4));
+                sp.gate_tag = next_gate_tag();
                 set_load_modes(sp, 0, p.vec_flags);
             }
             e = launch_semiring(sp, s);
@@ -222,8 +232,10 @@ int execute_plan(const Plan& p, const void* x, const void* y, void* z, void* ws,
             lp.nb = sp.nb;
             lp.K = sp.K;
             lp.src = x, lp.dst = ex, lp.rmax = rmax, lp.b = sp.xb, lp.r = sp.xm, lp.k = sp.xk, lp.R = sp.M;
+            lp.src_elems = sp.x_elems;
             if ((e = launch_lse_prep(lp, s)) != cudaSuccess) return cuda_fail(e, "max-shift of X");
             lp.src = y, lp.dst = ey, lp.rmax = cmax, lp.b = sp.yb, lp.r = sp.yn, lp.k = sp.yk, lp.R = sp.N;
+            lp.src_elems = sp.y_elems;
             if ((e = launch_lse_prep(lp, s)) != cudaSuccess) return cuda_fail(e, "max-shift of Y");
             sp.x_raw = x;
             sp.y_raw = y;
@@ -252,6 +264,8 @@ int execute_plan(const Plan& p, const void* x, const void* y, void* z, void* ws,
             rp.in_bf16 = p.in_bf16;
             rp.out_bf16 = p.out_bf16;
             rp.k_affine = rp.xk.n == 1 && rp.xk.t[0].loc_stride == 1 && rp.xk.t[0].sub == rp.xk.t[0].ext;
+            rp.x_elems = (uint64_t)p.X.total;
+            rp.z_elems = (uint64_t)p.Z.total;
             e = launch_row_reduce(rp, s);
             break;
         }
@@ -281,6 +295,8 @@ int execute_plan(const Plan& p, const void* x, const void* y, void* z, void* ws,
             ep.total = (uint64_t)p.Z.total;
             ep.flat = flat_mode(p, x, y, z);
             ep.y_div = (uint32_t)p.Z.shape[p.Z.rank - 1];
+            ep.x_elems = (uint64_t)p.X.total;
+            ep.y_elems = p.unary ? 0 : (uint64_t)p.Y.total;
             e = launch_elementwise(ep, s);
             break;
         }
@@ -314,6 +330,11 @@ int execute_plan(const Plan& p, const void* x, const void* y, void* z, void* ws,
             w += align256(nb * N * 4);
             int* marks = reinterpret_cast<int*>(w);
             w += 256;
+            uint32_t* fix = nullptr;  // squared distance: guard words, one per 128 x 128 output tile
+            if (!lse) {
+                fix = reinterpret_cast<uint32_t*>(w);
+                w += align256(sqdist_guard_bytes(nb, M, N));
+            }
             float* parts = reinterpret_cast<float*>(w);
             Split3StatsParams st;
             memset(&st, 0, sizeof(st));
@@ -322,9 +343,11 @@ int execute_plan(const Plan& p, const void* x, const void* y, void* z, void* ws,
             st.K = sp.K;
             st.partials = parts;
             st.src = reinterpret_cast<const float*>(x), st.out = rt, st.b = sp.xb, st.r = sp.xm, st.k = sp.xk, st.R = sp.M;
+            st.src_elems = sp.x_elems;
             st.kc = split3_stats_chunks(nb * M, K);
             if ((e = launch_split3_stats(st, s)) != cudaSuccess) return cuda_fail(e, "row terms of X");
             st.src = reinterpret_cast<const float*>(y), st.out = ct, st.b = sp.yb, st.r = sp.yn, st.k = sp.yk, st.R = sp.N;
+            st.src_elems = sp.y_elems;
             st.kc = split3_stats_chunks(nb * N, K);
             if ((e = launch_split3_stats(st, s)) != cudaSuccess) return cuda_fail(e, "column terms of Y");
             Split3Params s3;
@@ -332,9 +355,11 @@ int execute_plan(const Plan& p, const void* x, const void* y, void* z, void* ws,
             s3.src = reinterpret_cast<const float*>(x), s3.dst = a3, s3.shift = lse ? rt : nullptr;
             s3.b = sp.xb, s3.r = sp.xm, s3.k = sp.xk, s3.nb = sp.nb, s3.R = sp.M, s3.K = sp.K, s3.is_y = 0;
             s3.Rp = (uint32_t)Mp, s3.K3p = (uint32_t)K3p;
+            s3.src_elems = sp.x_elems;
             if ((e = launch_split3(s3, s)) != cudaSuccess) return cuda_fail(e, "split of X");
             s3.src = reinterpret_cast<const float*>(y), s3.dst = b3, s3.shift = lse ? ct : nullptr;
             s3.b = sp.yb, s3.r = sp.yn, s3.k = sp.yk, s3.R = sp.N, s3.is_y = 1, s3.Rp = (uint32_t)Np;
+            s3.src_elems = sp.y_elems;
             if ((e = launch_split3(s3, s)) != cudaSuccess) return cuda_fail(e, "split of Y");
             TcExtra ex;
             ex.epi = lse ? 2 : 1;
@@ -347,12 +372,28 @@ int execute_plan(const Plan& p, const void* x, const void* y, void* z, void* ws,
             ex.zn = sp.zn;
             ex.M = sp.M;
             ex.N = sp.N;
+            ex.z_elems = sp.z_elems;
             if (lse) {
                 ex.mark_count = marks;
                 if ((e = cudaMemsetAsync(marks, 0, sizeof(int), s)) != cudaSuccess) return cuda_fail(e, "mark count");
+            } else {
+                ex.sq_tau = sqdist_guard_tau(K, kSqGuardSplit3);
+                ex.fix_flags = fix;
+                ex.fix_tiles_m = (uint32_t)((M + 127) / 128);
+                ex.fix_tiles_n = (uint32_t)((N + 127) / 128);
+                ex.fix_tag_index = semiring_tiles(nb, M, N);  // the word set to 1 when anything is marked
+                if ((e = cudaMemsetAsync(fix, 0, sqdist_guard_bytes(nb, M, N), s)) != cudaSuccess)
+                    return cuda_fail(e, "guard words");
             }
             const int rc = tc_execute(*p.inner, a3, b3, z, s, &ex);
-            if (rc != TRA_OK || !lse) return rc;
+            if (rc != TRA_OK) return rc;
+            if (!lse) {
+                // the outputs whose expansion cancelled too far: their tiles in the direct form
+                sp.tile_gate = fix;
+                sp.gate_tag = 1;
+                if ((e = launch_sqdist_fixup(sp, s)) != cudaSuccess) return cuda_fail(e, "guard pass");
+                return TRA_OK;
+            }
             sp.x_raw = x;
             sp.y_raw = y;
             sp.mark_count = marks;
@@ -566,6 +607,15 @@ int ein_status(tra_stream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e, "status read");
     if (!v) v = va ? va : vr;
     if (v) return fail(v, "a bounded device wait gave up (status %d)", v);
+    // check builds: the first out-of-range access site of each kernel unit (0 = none)
+    int c[3] = {0, 0, 0};
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    e = read_and_clear_check_semiring(&c[0], st);
+    if (e == cudaSuccess) e = read_and_clear_check_misc(&c[1], st);
+    if (e == cudaSuccess) e = read_and_clear_check_tc(&c[2], st);
+    if (e != cudaSuccess) return cuda_fail(e, "check word read");
+    for (int i = 0; i < 3; ++i)
+        if (c[i]) return fail(TRA_ERR_BOUNDS, "an index outside its buffer was skipped at check site %d", c[i]);
     return TRA_OK;
 }
 
@@ -576,6 +626,8 @@ int ein_selftest_wait_timeout(uint64_t timeout_ns, tra_stream_t stream) {
 }
 
 void ein_plan_destroy(tra_plan_t plan) { delete reinterpret_cast<Plan*>(plan); }
+
+int ein_build_flags(void) { return kCheckBuild ? TRA_BUILD_CHECK : 0; }
 
 const char* ein_last_error(void) { return last_error(); }
 

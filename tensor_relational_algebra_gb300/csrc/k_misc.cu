@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(256) repartition_kernel(const __grid_constant_
         for (int j = 0; j < 4; ++j) {
             const int pos = 32 * j + lane;
             const int64_t so = __shfl_sync(0xffffffffu, seg[(32 * j) / (32 * G)], (pos / G) & 31) + pos % G;
-            if (c0 + pos < p.n_vec) val[j] = __ldcs(src + so);
+            if (c0 + pos < p.n_vec) val[j] = chk(so, p.n_vec, 201) ? __ldcs(src + so) : V{};
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -172,7 +172,8 @@ __global__ void row_reduce_kernel(const __grid_constant__ RowReduceParams p) {
     const uint32_t r = (uint32_t)warp;
     const int64_t xo = role_offset(p.xr, r);
     float m = AGG == kMin ? INFINITY : -INFINITY, s = 0.f;
-    if (p.k_affine && !p.in_bf16 && (xo % 4) == 0 && (p.K % 4) == 0 && ((uintptr_t)p.x % 16) == 0) {
+    if (p.k_affine && !p.in_bf16 && (xo % 4) == 0 && (p.K % 4) == 0 && ((uintptr_t)p.x % 16) == 0 &&
+        chk(xo + (int64_t)p.K - 1, p.x_elems, 202)) {
         // 4 float4 loads in flight per lane; each group of 16 values folds in at once (for
         // logsumexp: one rescale per group, one exp per value); padding is the identity of the
         // aggregation
@@ -187,9 +188,13 @@ __global__ void row_reduce_kernel(const __grid_constant__ RowReduceParams p) {
             agg_group16<AGG>(m, s, v);
         }
     } else if (p.k_affine) {
-        for (uint32_t k = lane; k < p.K; k += 32) agg_step<AGG>(m, s, ld_f(p.x, xo + k, p.in_bf16));
+        for (uint32_t k = lane; k < p.K; k += 32)
+            if (chk(xo + k, p.x_elems, 203)) agg_step<AGG>(m, s, ld_f(p.x, xo + k, p.in_bf16));
     } else {
-        for (uint32_t k = lane; k < p.K; k += 32) agg_step<AGG>(m, s, ld_f(p.x, xo + role_offset(p.xk, k), p.in_bf16));
+        for (uint32_t k = lane; k < p.K; k += 32) {
+            const int64_t o = xo + role_offset(p.xk, k);
+            if (chk(o, p.x_elems, 203)) agg_step<AGG>(m, s, ld_f(p.x, o, p.in_bf16));
+        }
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
@@ -202,7 +207,8 @@ __global__ void row_reduce_kernel(const __grid_constant__ RowReduceParams p) {
         if (AGG == kLse) v = m == -INFINITY ? m : m + logf(s);
         else if (AGG == kSum) v = s;
         else v = m;
-        st_f(p.z, role_offset(p.zr, r), p.alpha * v, p.out_bf16);
+        const int64_t zo = role_offset(p.zr, r);
+        if (chk(zo, p.z_elems, 204)) st_f(p.z, zo, p.alpha * v, p.out_bf16);
     }
 }
 
@@ -243,7 +249,9 @@ __global__ void elementwise_kernel(const __grid_constant__ ElementwiseParams p) 
     // 4-aligned: 16-byte loads, 4 outputs per lane per step
     if (!p.in_bf16 && xs == 1 && (ys == 0 || ys == 1 || !p.y) && (p.I & 3) == 0 && (e & 3) == 0 &&
         (xo & 3) == 0 && (ys != 1 || (yo & 3) == 0) && ((uintptr_t)p.x & 15) == 0 &&
-        (!p.y || ys != 1 || ((uintptr_t)p.y & 15) == 0) && ((uintptr_t)p.z & (p.out_bf16 ? 7 : 15)) == 0) {
+        (!p.y || ys != 1 || ((uintptr_t)p.y & 15) == 0) && ((uintptr_t)p.z & (p.out_bf16 ? 7 : 15)) == 0 &&
+        chk(xo + p.I - 1, p.x_elems, 205) && (!p.y || chk(yo + (ys ? p.I - 1 : 0), p.y_elems, 206)) &&
+        chk((int64_t)e + p.I - 1, p.total, 207)) {
         const float* xr = reinterpret_cast<const float*>(p.x) + xo;
         const float* yr = p.y ? reinterpret_cast<const float*>(p.y) + yo : nullptr;
         const float yb = (p.y && ys == 0) ? yr[0] : 0.f;
@@ -263,8 +271,11 @@ __global__ void elementwise_kernel(const __grid_constant__ ElementwiseParams p) 
         return;
     }
     for (uint32_t j = lane; j < p.I; j += 32) {
-        const float x = ld_f(p.x, xo + (int64_t)j * xs, p.in_bf16);
-        const float y = p.y ? ld_f(p.y, yo + (int64_t)j * ys, p.in_bf16) : 0.f;
+        const int64_t xi = xo + (int64_t)j * xs, yi = yo + (int64_t)j * ys;
+        if (!chk(xi, p.x_elems, 205) || (p.y && !chk(yi, p.y_elems, 206)) || !chk((int64_t)e + j, p.total, 207))
+            continue;
+        const float x = ld_f(p.x, xi, p.in_bf16);
+        const float y = p.y ? ld_f(p.y, yi, p.in_bf16) : 0.f;
         st_f(p.z, (int64_t)e + j, p.alpha * ew_op(p.op, x, y), p.out_bf16);
     }
 }
@@ -276,6 +287,9 @@ __global__ void __launch_bounds__(256) elementwise_flat_kernel(const __grid_cons
     const uint64_t c = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x;
     if (c * 8 >= p.total) return;
     const uint64_t e = c * 8;
+    if (!chk((int64_t)e + 7, p.total, 208) || !chk((int64_t)e + 7, p.x_elems, 208) ||
+        (p.y && !chk(p.flat == 1 ? (int64_t)e + 7 : (int64_t)(e / p.y_div), p.y_elems, 209)))
+        return;
     const float* xr = reinterpret_cast<const float*>(p.x) + e;
     const float4 x0 = *reinterpret_cast<const float4*>(xr), x1 = *reinterpret_cast<const float4*>(xr + 4);
     float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
@@ -362,6 +376,8 @@ unsigned persistent_grid(uint64_t work, unsigned per_block, K kernel, int max_pe
 
 }  // namespace
 
+TRA_CHECK_READER(read_and_clear_check_misc)
+
 cudaError_t launch_repartition(const RepartParams& p, cudaStream_t s) {
     if (p.n_vec == 0) return cudaSuccess;
     const unsigned g = persistent_grid(p.n_vec, 256 * 4, repartition_kernel<uint4, 4>);
@@ -443,7 +459,8 @@ __global__ void __launch_bounds__(256) split3_kernel(const __grid_constant__ Spl
 #pragma unroll
             for (uint32_t h = 0; h < TK / 32; ++h) {
                 const uint32_t kl = lane + 32 * h;
-                if (k0 + kl < p.K) t[rl][kl] = row[p.k_dense ? (int64_t)(k0 + kl) : koff[kl]];
+                const int64_t o = p.k_dense ? (int64_t)(k0 + kl) : koff[kl];
+                if (k0 + kl < p.K) t[rl][kl] = chk(roff[rl] + o, p.src_elems, 210) ? row[o] : 0.f;
             }
         }
     } else {
@@ -453,7 +470,8 @@ __global__ void __launch_bounds__(256) split3_kernel(const __grid_constant__ Spl
 #pragma unroll 4
         for (uint32_t i = 0; i < TK / 8; ++i) {
             const uint32_t kl = w + 8 * i;
-            if (rv && k0 + kl < p.K) t[lane][kl] = row[p.k_dense ? (int64_t)(k0 + kl) * p.k_ls : koff[kl]];
+            const int64_t o = p.k_dense ? (int64_t)(k0 + kl) * p.k_ls : koff[kl];
+            if (rv && k0 + kl < p.K) t[lane][kl] = chk(roff[lane] + o, p.src_elems, 210) ? row[o] : 0.f;
         }
     }
     __syncthreads();
@@ -464,6 +482,7 @@ __global__ void __launch_bounds__(256) split3_kernel(const __grid_constant__ Spl
         const uint32_t rl = w + 8 * i, r = r0 + rl;
         if (r >= p.R) continue;
         __nv_bfloat16* out = p.dst + ((uint64_t)b * p.Rp + r) * p.K3p;
+        if (!chk(((int64_t)b * p.Rp + r) * p.K3p + p.K3p - 1, (uint64_t)p.nb * p.Rp * p.K3p, 211)) continue;
 #pragma unroll
         for (uint32_t h = 0; h < TK / 64; ++h) {
             const uint32_t kl = 2 * lane + 64 * h, k = k0 + kl;
@@ -519,12 +538,16 @@ __global__ void __launch_bounds__(256) split3_stats_kernel(const __grid_constant
     for (uint32_t k = k_lo + threadIdx.x; k < k_hi; k += blockDim.x) koff[k - k_lo] = role_offset(p.k, k);
     __syncthreads();
     const int64_t* ko = koff - k_lo;  // indexed by k
+    // check build: the chunk's offsets against the operand (a row's offset is added below)
+    int64_t kmax = 0;
+    if (kCheckBuild)
+        for (uint32_t k = k_lo; k < k_hi; ++k) kmax = kmax > ko[k] ? kmax : ko[k];
     if (p.k_fast) {
 #pragma unroll
         for (uint32_t i = 0; i < 4; ++i) {
             const uint32_t r = r0 + w + 8 * i;
             float a0 = init, a1 = init;
-            if (r < p.R) {
+            if (r < p.R && chk(bo + role_offset(p.r, r) + kmax, p.src_elems, 212)) {
                 const float* row = p.src + bo + role_offset(p.r, r);
                 uint32_t k = k_lo + lane;
 #pragma unroll 4
@@ -544,7 +567,7 @@ __global__ void __launch_bounds__(256) split3_stats_kernel(const __grid_constant
     } else {
         const uint32_t r = r0 + lane;
         float a0 = init, a1 = init;
-        if (r < p.R) {
+        if (r < p.R && chk(bo + role_offset(p.r, r) + kmax, p.src_elems, 212)) {
             const float* row = p.src + bo + role_offset(p.r, r);
             uint32_t k = k_lo + w;
 #pragma unroll 4

@@ -61,6 +61,16 @@ __device__ __forceinline__ float4 ld4<__nv_bfloat16>(const void* p, int64_t off)
                        __uint_as_float(u.y & 0xffff0000u));
 }
 
+// the loads above with the check build's bounds test (n elements; pad where it fails)
+template <typename T>
+__device__ __forceinline__ float ld1c(const void* p, int64_t off, uint64_t n, int site, float pad) {
+    return chk(off, n, site) ? ld1<T>(p, off) : pad;
+}
+template <typename T>
+__device__ __forceinline__ float4 ld4c(const void* p, int64_t off, uint64_t n, int site, float pad) {
+    return chk(off + 3, n, site) ? ld4<T>(p, off) : make_float4(pad, pad, pad, pad);
+}
+
 __device__ __forceinline__ void st_out(void* p, int64_t off, float v, int bf16) {
     if (bf16)
         reinterpret_cast<__nv_bfloat16*>(p)[off] = __float2bfloat16_rn(v);
@@ -145,7 +155,8 @@ __device__ __noinline__ float direct_lse(const SemiringParams& p, const void* x,
                                          int64_t yo) {
     float m = -INFINITY, s = 0.f;
     for (uint32_t k = 0; k < p.K; ++k) {
-        float v = ld1<TIn>(x, xo + role_offset(p.xk, k)) + ld1<TIn>(y, yo + role_offset(p.yk, k));
+        float v = ld1c<TIn>(x, xo + role_offset(p.xk, k), p.x_elems, 114, -INFINITY) +
+                  ld1c<TIn>(y, yo + role_offset(p.yk, k), p.y_elems, 114, 0.f);
         if (v > m) {
             s = s * expf(m - v) + 1.f;
             m = v;
@@ -180,9 +191,13 @@ __device__ __forceinline__ int64_t koff_y(const SemiringParams& p, uint32_t k) {
     return role_offset(p.yk, k);
 }
 
-__device__ __forceinline__ void decode_tile(const SemiringParams& p, uint32_t& b, uint32_t& m0, uint32_t& n0) {
+__device__ __forceinline__ uint32_t n_tiles(const SemiringParams& p) {
+    return p.nb * ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
+}
+
+__device__ __forceinline__ void decode_tile(const SemiringParams& p, uint32_t t, uint32_t& b, uint32_t& m0,
+                                            uint32_t& n0) {
     const uint32_t tiles_m = (p.M + BM - 1) / BM, tiles_n = (p.N + BN - 1) / BN;
-    uint32_t t = blockIdx.x;
     const uint32_t tn = t % tiles_n;
     t /= tiles_n;
     const uint32_t tm = t % tiles_m;
@@ -216,15 +231,22 @@ __device__ __forceinline__ void tile_epilogue(const SemiringParams& p, float (&a
         if (EPI == kEpiSqExpand) cterms[tid - BM] = p.ynorm[(uint64_t)b * p.N + n];
     }
     __syncthreads();
+    // squared-distance guard: this thread saw an output whose expansion cancelled
+    bool marked = false;
     if (BULK) {
         const bool rows_contiguous = __syncthreads_and(
             !p.out_bf16 && p.z_vec4 && p.z_device && (reinterpret_cast<uintptr_t>(p.z) & 15) == 0 && n0 + BN <= p.N &&
             (tid >= BN || colZ[tid] == colZ[0] + tid));
         if (rows_contiguous) {
+            // guard, bounded per thread: min over its outputs of d against tau * (largest row norm
+            // + largest column norm); this marks every tile the exact test would (and rows past M,
+            // computed from a clamped row, can only add a mark)
+            float dmin = INFINITY, rmx = 0.f, cmx = 0.f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int mi = (i < 4) ? ty * 4 + i : 64 + ty * 4 + (i - 4);
                 const float rterm = EPI == kEpiPlain ? 0.f : rterms[mi];
+                if (EPI == kEpiSqExpand) rmx = fmaxf(rmx, rterm);
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
                     const int nb = g * 64 + tx * 4;
@@ -235,7 +257,10 @@ __device__ __forceinline__ void tile_epilogue(const SemiringParams& p, float (&a
                         if (EPI == kEpiLse) {
                             a = a > 1e-30f ? rterm + cterms[nb + c] + logf(a) : __int_as_float(0x7fc00000);
                         } else if (EPI == kEpiSqExpand) {
-                            a = fmaxf(rterm + cterms[nb + c] - 2.f * a, 0.f);
+                            const float d = rterm + cterms[nb + c] - 2.f * a;
+                            dmin = fminf(dmin, d);
+                            if (i == 0) cmx = fmaxf(cmx, cterms[nb + c]);
+                            a = fmaxf(d, 0.f);
                         }
                         v[c] = p.alpha * a;
                     }
@@ -243,9 +268,17 @@ __device__ __forceinline__ void tile_epilogue(const SemiringParams& p, float (&a
                 }
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncthreads();
+            if (EPI == kEpiSqExpand) {
+                const int any = __syncthreads_or(dmin < p.sq_tau * (rmx + cmx));
+                if (tid == 0 && p.tile_mark) {
+                    p.tile_mark[blockIdx.x] = any ? 1u : 0u;
+                    if (any) p.tile_mark[gridDim.x] = p.gate_tag;  // this launch marked a tile
+                }
+            } else {
+                __syncthreads();
+            }
             if (tid < BM) {
-                if (m0 + tid < p.M) {
+                if (m0 + tid < p.M && chk(rowZ[tid] + colZ[0] + BN - 1, p.z_elems, 103)) {
                     float* dst = reinterpret_cast<float*>(p.z) + rowZ[tid] + colZ[0];
                     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
                                  "r"((uint32_t)__cvta_generic_to_shared(stg + tid * BN)), "r"(BN * 4)
@@ -276,12 +309,15 @@ __device__ __forceinline__ void tile_epilogue(const SemiringParams& p, float (&a
                     // every exp-shifted product underflowed: mark the output, lse_fixup recomputes it
                     a = a > 1e-30f ? rterm + cterms[nb + c] + logf(a) : __int_as_float(0x7fc00000);
                 } else if (EPI == kEpiSqExpand) {
-                    a = fmaxf(rterm + cterms[nb + c] - 2.f * a, 0.f);
+                    const float s = rterm + cterms[nb + c], d = s - 2.f * a;
+                    marked |= d < p.sq_tau * s && n + c < p.N;
+                    a = fmaxf(d, 0.f);
                 }
                 v[c] = p.alpha * a;
             }
             if (p.z_vec4 && n + 3 < p.N) {
                 const int64_t off = zrow + colZ[nb];
+                if (!chk(off + 3, p.z_elems, 104)) continue;
                 if (p.out_bf16) {
                     const __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
                     const __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
@@ -293,8 +329,16 @@ __device__ __forceinline__ void tile_epilogue(const SemiringParams& p, float (&a
             } else {
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    if (n + c < p.N) st_out(p.z, zrow + colZ[nb + c], v[c], p.out_bf16);
+                    if (n + c < p.N && chk(zrow + colZ[nb + c], p.z_elems, 105))
+                        st_out(p.z, zrow + colZ[nb + c], v[c], p.out_bf16);
             }
+        }
+    }
+    if (EPI == kEpiSqExpand) {
+        const int any = __syncthreads_or(marked);
+        if (tid == 0 && p.tile_mark) {
+            p.tile_mark[blockIdx.x] = any ? 1u : 0u;
+            if (any) p.tile_mark[gridDim.x] = p.gate_tag;
         }
     }
 }
@@ -304,7 +348,7 @@ __device__ __forceinline__ void tile_epilogue(const SemiringParams& p, float (&a
 // K-contiguous operand), Y tile as [k][n].  Per thread per 4 k: 8 LDS.128 of X (one per
 // owned row), 2 LDS.128 of Y per k.
 template <class S, int EPI>
-__global__ void __launch_bounds__(NT, 2) semiring_async(const __grid_constant__ SemiringParams p) {
+__device__ __forceinline__ void async_tile(const SemiringParams& p, uint32_t tile) {
     extern __shared__ __align__(16) float dsm[];
     float* Xs = dsm;                          // [ASTAGES][BM * ABK]
     float* Ys = dsm + ASTAGES * BM * ABK;     // [ASTAGES][ABK * BN]
@@ -312,7 +356,7 @@ __global__ void __launch_bounds__(NT, 2) semiring_async(const __grid_constant__ 
 
     const int tid = threadIdx.x;
     uint32_t b, m0, n0;
-    decode_tile(p, b, m0, n0);
+    decode_tile(p, tile, b, m0, n0);
     if (tid < BM) {
         rowX[tid] = role_offset(p.xb, b) + role_offset(p.xm, clamp_row(m0 + tid, p.M, false));
     } else {
@@ -331,7 +375,14 @@ __global__ void __launch_bounds__(NT, 2) semiring_async(const __grid_constant__ 
         if (k0 + xk < p.K) {
             const int64_t ko = koff_x(p, k0 + xk);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) cp_async16(&xs[(xr + 32 * i) * ABK + xk], xg + rowX[xr + 32 * i] + ko);
+            for (int i = 0; i < 4; ++i) {
+                if (chk(rowX[xr + 32 * i] + ko + 3, p.x_elems, 101)) {
+                    cp_async16(&xs[(xr + 32 * i) * ABK + xk], xg + rowX[xr + 32 * i] + ko);
+                } else {
+                    const float px = S::pad_x();
+                    *reinterpret_cast<float4*>(&xs[(xr + 32 * i) * ABK + xk]) = make_float4(px, px, px, px);
+                }
+            }
         } else {
             const float px = S::pad_x();
 #pragma unroll
@@ -341,7 +392,7 @@ __global__ void __launch_bounds__(NT, 2) semiring_async(const __grid_constant__ 
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int kr = yr + 8 * i;
-            if (k0 + kr < p.K) {
+            if (k0 + kr < p.K && chk(colY[yn] + koff_y(p, k0 + kr) + 3, p.y_elems, 102)) {
                 cp_async16(&ys[kr * BN + yn], yg + colY[yn] + koff_y(p, k0 + kr));
             } else {
                 const float py = S::pad_y();
@@ -403,16 +454,33 @@ __global__ void __launch_bounds__(NT, 2) semiring_async(const __grid_constant__ 
     tile_epilogue<EPI, true>(p, acc, b, m0, n0, rowX, colY, terms, terms + BM, dsm);
 }
 
+// One CTA per output tile; GATED (the squared-distance guard's fix-up pass): a persistent
+// sweep over the tiles, computing only those whose word in p.tile_gate is nonzero.
+template <class S, int EPI, bool GATED>
+__global__ void __launch_bounds__(NT, 2) semiring_async(const __grid_constant__ SemiringParams p) {
+    if (!GATED) {
+        async_tile<S, EPI>(p, blockIdx.x);
+        return;
+    }
+    const uint32_t n = n_tiles(p);
+    if (p.tile_gate[n] != p.gate_tag) return;  // the producing launch marked no tile
+    for (uint32_t t = blockIdx.x; t < n; t += gridDim.x) {
+        if (p.tile_gate[t] == 0) continue;
+        async_tile<S, EPI>(p, t);
+        __syncthreads();  // shared memory is free again (the epilogue's bulk reads are done)
+    }
+}
+
 // ---------------------------------------------------------------- register-staged kernel
 template <class S, typename TIn, int EPI>
-__global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ SemiringParams p) {
+__device__ __forceinline__ void tiled_tile(const SemiringParams& p, uint32_t tile) {
     __shared__ __align__(16) float Xs[2][BK * BM];
     __shared__ __align__(16) float Ys[2][BK * BN];
     __shared__ int64_t rowX[BM], colY[BN];
 
     const int tid = threadIdx.x;
     uint32_t b, m0, n0;
-    decode_tile(p, b, m0, n0);
+    decode_tile(p, tile, b, m0, n0);
     if (tid < BM) {
         rowX[tid] = role_offset(p.xb, b) + role_offset(p.xm, clamp_row(m0 + tid, p.M, p.x_mode == kLoadVecMN));
     } else {
@@ -433,7 +501,7 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int k = ((tid >> 7) + 2 * i) * 4;
-                float4 v = k < kv ? ld4<TIn>(p.x, rowX[m] + koff_x(p, k0 + k)) : make_float4(px, px, px, px);
+                float4 v = k < kv ? ld4c<TIn>(p.x, rowX[m] + koff_x(p, k0 + k), p.x_elems, 106, px) : make_float4(px, px, px, px);
                 rx[4 * i] = v.x, rx[4 * i + 1] = v.y, rx[4 * i + 2] = v.z, rx[4 * i + 3] = v.w;
             }
         } else if (xmode == kLoadVecMN) {
@@ -441,7 +509,7 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int k = (tid >> 5) + 8 * i;
-                float4 v = k < kv ? ld4<TIn>(p.x, rowX[m] + koff_x(p, k0 + k)) : make_float4(px, px, px, px);
+                float4 v = k < kv ? ld4c<TIn>(p.x, rowX[m] + koff_x(p, k0 + k), p.x_elems, 106, px) : make_float4(px, px, px, px);
                 rx[4 * i] = v.x, rx[4 * i + 1] = v.y, rx[4 * i + 2] = v.z, rx[4 * i + 3] = v.w;
             }
         } else {
@@ -449,7 +517,7 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int k = (tid >> 7) + 2 * i;
-                rx[i] = k < kv ? ld1<TIn>(p.x, rowX[m] + koff_x(p, k0 + k)) : px;
+                rx[i] = k < kv ? ld1c<TIn>(p.x, rowX[m] + koff_x(p, k0 + k), p.x_elems, 107, px) : px;
             }
         }
         if (ymode == kLoadVecMN) {
@@ -457,7 +525,7 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int k = (tid >> 5) + 8 * i;
-                float4 v = k < kv ? ld4<TIn>(p.y, colY[n] + koff_y(p, k0 + k)) : make_float4(py, py, py, py);
+                float4 v = k < kv ? ld4c<TIn>(p.y, colY[n] + koff_y(p, k0 + k), p.y_elems, 108, py) : make_float4(py, py, py, py);
                 ry[4 * i] = v.x, ry[4 * i + 1] = v.y, ry[4 * i + 2] = v.z, ry[4 * i + 3] = v.w;
             }
         } else if (ymode == kLoadVecK) {
@@ -465,7 +533,7 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int k = ((tid >> 7) + 2 * i) * 4;
-                float4 v = k < kv ? ld4<TIn>(p.y, colY[n] + koff_y(p, k0 + k)) : make_float4(py, py, py, py);
+                float4 v = k < kv ? ld4c<TIn>(p.y, colY[n] + koff_y(p, k0 + k), p.y_elems, 108, py) : make_float4(py, py, py, py);
                 ry[4 * i] = v.x, ry[4 * i + 1] = v.y, ry[4 * i + 2] = v.z, ry[4 * i + 3] = v.w;
             }
         } else {
@@ -473,7 +541,7 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int k = (tid >> 7) + 2 * i;
-                ry[i] = k < kv ? ld1<TIn>(p.y, colY[n] + koff_y(p, k0 + k)) : py;
+                ry[i] = k < kv ? ld1c<TIn>(p.y, colY[n] + koff_y(p, k0 + k), p.y_elems, 109, py) : py;
             }
         }
     };
@@ -566,6 +634,21 @@ __global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ 
     tile_epilogue<EPI>(p, acc, b, m0, n0, rowX, colY, Xs[0], Ys[0]);
 }
 
+template <class S, typename TIn, int EPI, bool GATED>
+__global__ void __launch_bounds__(NT, 2) semiring_tiled(const __grid_constant__ SemiringParams p) {
+    if (!GATED) {
+        tiled_tile<S, TIn, EPI>(p, blockIdx.x);
+        return;
+    }
+    const uint32_t n = n_tiles(p);
+    if (p.tile_gate[n] != p.gate_tag) return;
+    for (uint32_t t = blockIdx.x; t < n; t += gridDim.x) {
+        if (p.tile_gate[t] == 0) continue;
+        tiled_tile<S, TIn, EPI>(p, t);
+        __syncthreads();
+    }
+}
+
 // ---------------------------------------------------------------- generic fallback
 // One thread per output; any op / aggregation (logsumexp evaluated online).
 template <typename TIn>
@@ -582,8 +665,8 @@ __global__ void semiring_simple(const __grid_constant__ SemiringParams p) {
         if (p.agg == kLse) {
             float mx = -INFINITY, s = 0.f;
             for (uint32_t k = 0; k < p.K; ++k) {
-                float v = apply_op(p.op, ld1<TIn>(p.x, xo + role_offset(p.xk, k)),
-                                   ld1<TIn>(p.y, yo + role_offset(p.yk, k)));
+                float v = apply_op(p.op, ld1c<TIn>(p.x, xo + role_offset(p.xk, k), p.x_elems, 110, 0.f),
+                                   ld1c<TIn>(p.y, yo + role_offset(p.yk, k), p.y_elems, 111, 0.f));
                 if (v > mx) {
                     s = s * expf(mx - v) + 1.f;
                     mx = v;
@@ -595,14 +678,15 @@ __global__ void semiring_simple(const __grid_constant__ SemiringParams p) {
         } else {
             acc = p.agg == kMax ? -INFINITY : (p.agg == kMin ? INFINITY : 0.f);
             for (uint32_t k = 0; k < p.K; ++k) {
-                float v = apply_op(p.op, ld1<TIn>(p.x, xo + role_offset(p.xk, k)),
-                                   ld1<TIn>(p.y, yo + role_offset(p.yk, k)));
+                float v = apply_op(p.op, ld1c<TIn>(p.x, xo + role_offset(p.xk, k), p.x_elems, 110, 0.f),
+                                   ld1c<TIn>(p.y, yo + role_offset(p.yk, k), p.y_elems, 111, 0.f));
                 if (p.agg == kMax) acc = fmaxf(acc, v);
                 else if (p.agg == kMin) acc = fminf(acc, v);
                 else acc += v;
             }
         }
-        st_out(p.z, role_offset(p.zb, b) + role_offset(p.zm, m) + role_offset(p.zn, n), p.alpha * acc, p.out_bf16);
+        const int64_t zo = role_offset(p.zb, b) + role_offset(p.zm, m) + role_offset(p.zn, n);
+        if (chk(zo, p.z_elems, 112)) st_out(p.z, zo, p.alpha * acc, p.out_bf16);
     }
 }
 
@@ -628,6 +712,7 @@ __global__ void __launch_bounds__(NT) lse_fixup_kernel(const __grid_constant__ S
     if (n0 + c >= p.N) return;
     for (int r = tid >> 7; r < BM && m0 + r < p.M; r += NT / BN) {
         const int64_t off = rowZ[r] + colZ[c];
+        if (!chk(off, p.z_elems, 113)) continue;
         const float v = p.out_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.z)[off])
                                    : reinterpret_cast<const float*>(p.z)[off];
         if (v == v) continue;
@@ -659,7 +744,7 @@ __global__ void lse_prep_kernel(const __grid_constant__ LsePrepParams p, int row
         float m = p.mode == 0 ? -INFINITY : 0.f;
 #pragma unroll 8
         for (uint32_t k = lane; k < p.K; k += 32) {
-            float v = ld1<TIn>(p.src, base + prep_koff(p, k));
+            float v = ld1c<TIn>(p.src, base + prep_koff(p, k), p.src_elems, 115, p.mode == 0 ? -INFINITY : 0.f);
             m = p.mode == 0 ? fmaxf(m, v) : fmaf(v, v, m);
         }
         for (int o = 16; o; o >>= 1) {
@@ -670,7 +755,7 @@ __global__ void lse_prep_kernel(const __grid_constant__ LsePrepParams p, int row
         if (p.mode == 0 && p.dst)
             for (uint32_t k = lane; k < p.K; k += 32) {
                 int64_t off = base + prep_koff(p, k);
-                p.dst[off] = expf(ld1<TIn>(p.src, off) - m);
+                if (chk(off, p.src_elems, 116)) p.dst[off] = expf(ld1<TIn>(p.src, off) - m);
             }
     } else {
         // rows contiguous in memory: 32 consecutive rows per CTA (one per lane, coalesced
@@ -686,7 +771,7 @@ __global__ void lse_prep_kernel(const __grid_constant__ LsePrepParams p, int row
         if (valid)
 #pragma unroll 8
             for (uint32_t k = w; k < p.K; k += 8) {
-                const float v = ld1<TIn>(p.src, base + prep_koff(p, k));
+                const float v = ld1c<TIn>(p.src, base + prep_koff(p, k), p.src_elems, 115, p.mode == 0 ? -INFINITY : 0.f);
                 m = p.mode == 0 ? fmaxf(m, v) : fmaf(v, v, m);
             }
         red[w][lane] = m;
@@ -701,26 +786,28 @@ __global__ void lse_prep_kernel(const __grid_constant__ LsePrepParams p, int row
         if (p.mode == 0 && p.dst && valid)
             for (uint32_t k = w; k < p.K; k += 8) {
                 const int64_t off = base + prep_koff(p, k);
-                p.dst[off] = expf(ld1<TIn>(p.src, off) - m);
+                if (chk(off, p.src_elems, 116)) p.dst[off] = expf(ld1<TIn>(p.src, off) - m);
             }
     }
 }
 
-template <class S, typename TIn, int EPI>
+template <class S, typename TIn, int EPI, bool GATED = false>
 cudaError_t launch_tiled(const SemiringParams& p, unsigned grid, cudaStream_t s) {
     if (!p.in_bf16 && p.x_mode == kLoadVecK && p.y_mode == kLoadVecMN) {
         // fp32, X contiguous along K and Y along N: the cp.async pipelined kernel
-        cudaError_t e = cudaFuncSetAttribute(semiring_async<S, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kAsyncSmem);
+        cudaError_t e = cudaFuncSetAttribute(semiring_async<S, EPI, GATED>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAsyncSmem);
         if (e != cudaSuccess) return e;
-        semiring_async<S, EPI><<<grid, NT, kAsyncSmem, s>>>(p);
+        semiring_async<S, EPI, GATED><<<grid, NT, kAsyncSmem, s>>>(p);
         return cudaGetLastError();
     }
-    semiring_tiled<S, TIn, EPI><<<grid, NT, 0, s>>>(p);
+    semiring_tiled<S, TIn, EPI, GATED><<<grid, NT, 0, s>>>(p);
     return cudaGetLastError();
 }
 
 }  // namespace
+
+TRA_CHECK_READER(read_and_clear_check_semiring)
 
 cudaError_t launch_semiring(const SemiringParams& p, cudaStream_t s) {
     if (p.nb == 0 || p.M == 0 || p.N == 0) return cudaSuccess;
@@ -737,7 +824,16 @@ cudaError_t launch_semiring(const SemiringParams& p, cudaStream_t s) {
         lse_fixup_kernel<<<grid, NT, 0, s>>>(p);
         return cudaGetLastError();
     }
-    if (p.xnorm) return launch_tiled<MulSum, float, kEpiSqExpand>(p, grid, s);  // fp32 inputs
+    if (p.xnorm) {  // fp32 inputs: the expansion, then the direct form over the tiles it marked
+        cudaError_t e = launch_tiled<MulSum, float, kEpiSqExpand>(p, grid, s);
+        if (e != cudaSuccess || !p.tile_mark) return e;
+        SemiringParams q = p;
+        q.op = kSqdiff;
+        q.xnorm = q.ynorm = nullptr;
+        q.tile_gate = p.tile_mark;
+        q.tile_mark = nullptr;
+        return launch_sqdist_fixup(q, s);
+    }
     switch (p.op * 8 + p.agg) {
         case kMul * 8 + kSum:
             return bf ? launch_tiled<MulSum, __nv_bfloat16, kEpiPlain>(p, grid, s)
@@ -763,6 +859,21 @@ cudaError_t launch_semiring_simple(const SemiringParams& p, cudaStream_t s) {
     if (p.in_bf16) semiring_simple<__nv_bfloat16><<<blocks, 256, 0, s>>>(p);
     else semiring_simple<float><<<blocks, 256, 0, s>>>(p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_sqdist_fixup(const SemiringParams& p, cudaStream_t s) {
+    if (p.nb == 0 || p.M == 0 || p.N == 0) return cudaSuccess;
+    if (!p.tile_gate || p.in_bf16) return cudaErrorInvalidValue;
+    const uint64_t tiles = (uint64_t)p.nb * ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
+    if (tiles > 0x7fffffffull) return cudaErrorInvalidValue;
+    // persistent sweep: two CTAs per SM (the kernels' occupancy) walk the tiles' words and
+    // compute the marked tiles; with none marked the pass costs one read per tile
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t grid = tiles < 2ull * (uint64_t)sms ? tiles : 2ull * (uint64_t)sms;
+    return launch_tiled<SqdiffSum, float, kEpiPlain, true>(p, (unsigned)grid, s);
 }
 
 cudaError_t launch_lse_fixup(const SemiringParams& p, cudaStream_t s) {

@@ -84,6 +84,13 @@ struct TcParams {
     const float* col_term;
     uint32_t zM, zN;  // output rows / columns stored (M, N unless the operands are padded)
     int* mark_count;  // epilogue 2: incremented once per output marked NaN (may be null)
+    // epilogue 1: guard of the expansion (r + c - 2 acc < sq_tau (r + c) sets the word of the
+    // output's 128 x 128 tile in fix_flags; may be null)
+    float sq_tau;
+    uint32_t* fix_flags;
+    uint32_t fix_tiles_m, fix_tiles_n;
+    uint64_t fix_tag_index;  // fix_flags[fix_tag_index] = 1 once anything is marked
+    uint64_t z_elems;        // elements of z: the check build's bound on the warp stores
     // Work units (see unit_of): tiles [0, n_full) whole; tiles [n_full, n_tiles) of the last,
     // partly filled wave split into `split` runs of K steps on as many idle workers.  Parts
     // 0 .. split-2 each leave fp32 partial sums in a slot of `part` and release them through one
@@ -355,7 +362,8 @@ __device__ __forceinline__ void store_block(const TcParams& p, float4* stg, int6
             const int64_t o = __shfl_sync(0xffffffffu, zr, row);
             __nv_bfloat162 h[4] = {__floats2bfloat162_rn(v0.x, v0.y), __floats2bfloat162_rn(v0.z, v0.w),
                                    __floats2bfloat162_rn(v1.x, v1.y), __floats2bfloat162_rn(v1.z, v1.w)};
-            if (o >= 0) *reinterpret_cast<uint4*>(z + o + zc + 8 * sub) = *reinterpret_cast<const uint4*>(h);
+            if (o >= 0 && chk(o + zc + 8 * sub + 7, p.z_elems, 301))
+                *reinterpret_cast<uint4*>(z + o + zc + 8 * sub) = *reinterpret_cast<const uint4*>(h);
         }
     } else {
         float* z = reinterpret_cast<float*>(p.z);
@@ -365,7 +373,7 @@ __device__ __forceinline__ void store_block(const TcParams& p, float4* stg, int6
             const int row = 4 * i + (lane >> 3);
             const float4 v = stg[row * 8 + (g ^ (row & 7))];
             const int64_t o = __shfl_sync(0xffffffffu, zr, row);
-            if (o >= 0) *reinterpret_cast<float4*>(z + o + zc + 4 * g) = v;
+            if (o >= 0 && chk(o + zc + 4 * g + 3, p.z_elems, 302)) *reinterpret_cast<float4*>(z + o + zc + 4 * g) = v;
         }
     }
     __syncwarp();
@@ -380,16 +388,20 @@ __device__ __forceinline__ void store_block(const TcParams& p, float4* stg, int6
 // Rank-one epilogue terms of the rewritten non-sum semirings, applied to one 32-column block
 // (this lane's row m, columns n .. n + 31) before the stores scale by alpha.
 template <int EPI>
-__device__ __forceinline__ void apply_terms(const TcParams& p, uint32_t (&r)[32], float rt, uint32_t b, uint32_t n) {
+__device__ __forceinline__ void apply_terms(const TcParams& p, uint32_t (&r)[32], float rt, uint32_t b, uint32_t m,
+                                            uint32_t n) {
     if (EPI == 0) return;
     const float* ct = p.col_term + (uint64_t)b * p.zN;
+    bool marked = false;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         const float c = __ldg(ct + min(n + (uint32_t)i, p.zN - 1));
         const float a = __uint_as_float(r[i]);
         float v;
         if (EPI == 1) {
-            v = fmaxf(rt + c - 2.f * a, 0.f);
+            const float s = rt + c, d = s - 2.f * a;
+            marked |= d < p.sq_tau * s && n + (uint32_t)i < p.zN;
+            v = fmaxf(d, 0.f);
         } else if (a > 1e-30f) {
             v = rt + c + logf(a);
         } else {
@@ -397,6 +409,11 @@ __device__ __forceinline__ void apply_terms(const TcParams& p, uint32_t (&r)[32]
             if (p.mark_count) atomicAdd(p.mark_count, 1);
         }
         r[i] = __float_as_uint(v);
+    }
+    // the 32 columns n .. n + 31 lie in one 128-column tile (n is a multiple of 32)
+    if (EPI == 1 && marked && m < p.zM && p.fix_flags) {
+        p.fix_flags[((uint64_t)b * p.fix_tiles_m + m / 128u) * p.fix_tiles_n + n / 128u] = 1u;
+        p.fix_flags[p.fix_tag_index] = 1u;
     }
 }
 
@@ -501,8 +518,8 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorM
                 add_partial(ra, addp + j * add_stride, c, lane);
                 add_partial(rb, addp + j * add_stride, c + 1, lane);
             }
-            apply_terms<EPI>(p, ra, rt, b, n0 + c * 32u);
-            apply_terms<EPI>(p, rb, rt, b, n0 + c * 32u + 32u);
+            apply_terms<EPI>(p, ra, rt, b, m, n0 + c * 32u);
+            apply_terms<EPI>(p, rb, rt, b, m, n0 + c * 32u + 32u);
             if (!p.out_bf16) {
 #pragma unroll
                 for (int blk = 0; blk < 2; ++blk) {
@@ -545,8 +562,8 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorM
             add_partial(ra, addp + j * add_stride, c, lane);
             add_partial(rb, addp + j * add_stride, c + 1, lane);
         }
-        apply_terms<EPI>(p, ra, rt, b, n0 + c * 32u);
-        apply_terms<EPI>(p, rb, rt, b, n0 + c * 32u + 32u);
+        apply_terms<EPI>(p, ra, rt, b, m, n0 + c * 32u);
+        apply_terms<EPI>(p, rb, rt, b, m, n0 + c * 32u + 32u);
         store_block(p, stg, zr, __shfl_sync(0xffffffffu, zc_lane, c), lane, ra, n0 + c * 32u);
         store_block(p, stg, zr, __shfl_sync(0xffffffffu, zc_lane, c + 1), lane, rb, n0 + c * 32u + 32u);
     }
@@ -1309,6 +1326,7 @@ int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_
     tp.timeout_ns = 2000000000ull;  // 2 s per wait
     tp.zM = tp.M;
     tp.zN = tp.N;
+    tp.z_elems = (uint64_t)p.Z.total;
     if (ex) {
         if (ex->z_override) {
             if (t.z_tma) return fail(TRA_ERR_UNSUPPORTED, "output addressing override needs warp stores");
@@ -1322,11 +1340,17 @@ int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_
             tp.zn = ex->zn;
             tp.zM = ex->M;
             tp.zN = ex->N;
+            tp.z_elems = ex->z_elems;
         }
         tp.epi = (uint32_t)ex->epi;
         tp.row_term = ex->row_term;
         tp.col_term = ex->col_term;
         tp.mark_count = ex->mark_count;
+        tp.sq_tau = ex->sq_tau;
+        tp.fix_flags = ex->fix_flags;
+        tp.fix_tiles_m = ex->fix_tiles_m;
+        tp.fix_tiles_n = ex->fix_tiles_n;
+        tp.fix_tag_index = ex->fix_tag_index;
         tp.alpha = ex->alpha;
         if (tp.epi && (!tp.row_term || !tp.col_term)) return fail(TRA_ERR_ARG, "epilogue terms missing");
     }
@@ -1368,6 +1392,8 @@ int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_
     e = cudaGetLastError();
     return e == cudaSuccess ? TRA_OK : fail(TRA_ERR_CUDA, "tensor-core launch: %s", cudaGetErrorString(e));
 }
+
+TRA_CHECK_READER(read_and_clear_check_tc)
 
 cudaError_t read_and_clear_status(int* value, cudaStream_t s) {
     cudaError_t e = cudaMemcpyFromSymbolAsync(value, g_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s);

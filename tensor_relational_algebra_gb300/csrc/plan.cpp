@@ -20,6 +20,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 namespace tra {
@@ -41,6 +42,26 @@ void clear_error() { g_err.clear(); }
 const char* last_error() { return g_err.c_str(); }
 
 uint64_t align256(uint64_t v) { return (v + 255) & ~uint64_t(255); }
+
+// Guard of the squared-distance expansion |x|^2 + |y|^2 - 2 x.y (section 2.1's squared
+// distance, D = sum_k (x - y)^2 >= 0, zero for coincident points).  With S = |x|^2 + |y|^2 the
+// rounding error of the expansion in fp32 grows like c * sqrt(K) * u * S (u = 2^-24), whatever
+// D is, so its relative error is unbounded as D -> 0.  An output whose computed value falls
+// below tau * S, tau = c * sqrt(K) * u / 1e-5, is recomputed in the direct form; above it the
+// expansion's error stays under 1e-5 * D.  c: 3 for the fp32 expansion (largest error seen in
+// an fp32 simulation at K = 256 was 1.4 sqrt(K) u S, so a factor 2 of margin), 4.5 for
+// split=bf16x3, whose dropped lo.lo products add about three times that (margin 1: that path's
+// own bar is looser, see include/tra.h).  Capped at 2 (D <= 2 S: every output then qualifies).
+uint32_t next_gate_tag() {
+    static std::atomic<uint32_t> n{0x5eed0000u};
+    uint32_t t = n.fetch_add(1);
+    return t ? t : n.fetch_add(1);
+}
+
+float sqdist_guard_tau(uint64_t K, double c) {
+    const double t = c * std::sqrt((double)K) * 0x1p-24 / 1e-5;
+    return (float)(t < 2.0 ? t : 2.0);
+}
 
 // Elements whose owning block changes between two partitions of one tensor, blocks being
 // owned by their row-major linear key id L: |T| - sum_L |block_L(src) n block_L(dst)|.
@@ -287,7 +308,6 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
         }
     }
 
-    if (p->sqdiff_expand < 0) p->sqdiff_expand = p->in_bf16 ? 0 : 1;
 
     // roles
     bool inx[TRA_MAX_LABELS] = {}, iny[TRA_MAX_LABELS] = {}, inz[TRA_MAX_LABELS] = {};
@@ -356,6 +376,9 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
 
     // kernel choice and workspace
     p->ws_bytes = 0;
+    // squared distance: the expansion by default for fp32 inputs while its guard can pass
+    // typical outputs (threshold below 1), the direct form otherwise
+    if (p->sqdiff_expand < 0) p->sqdiff_expand = !p->in_bf16 && sqdist_guard_tau(p->ext[kK], kSqGuardFp32) < 1.f;
     for (int l = 0; l < p->n_labels; ++l)
         if (p->B[l] == 0) {
             // an empty EinSum: no output element, or only empty aggregations (agg's identity)
@@ -428,6 +451,8 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
         // operands, row / column terms, the fix-up's mark count (256 bytes), the statistics' partials
         p->ws_bytes = align256(nb * Mp * K3p * 2) + align256(nb * Np * K3p * 2) + align256(nb * M * 4) +
                       align256(nb * N * 4) + 256 + align256(parts * 4);
+        // squared distance: one word per 128 x 128 output tile marked by the expansion's guard
+        if (p->op == kSqdiff) p->ws_bytes += align256(sqdist_guard_bytes(nb, M, N));
     } else if (p->op == kAdd && p->agg == kLse) {
         p->kernel = TRA_KERNEL_LSE_FACTORED;
         const uint64_t nb = p->ext[kBatch];
@@ -444,11 +469,14 @@ int build_plan(const char* spec, const int64_t* bounds, int n_bounds, const int3
         if (p->op == kSqdiff && p->agg == kSum && p->sqdiff_expand) {
             if (p->in_bf16) return fail(TRA_ERR_UNSUPPORTED, "sqdiff=expand needs fp32 inputs");
             const uint64_t nb = p->ext[kBatch];
-            p->ws_bytes = align256(nb * p->ext[kM] * 4) + align256(nb * p->ext[kN] * 4);
+            // row norms, column norms, one guard word per 128 x 128 output tile
+            p->ws_bytes = align256(nb * p->ext[kM] * 4) + align256(nb * p->ext[kN] * 4) +
+                          align256(sqdist_guard_bytes(nb, p->ext[kM], p->ext[kN]));
         }
     }
+    // (split=bf16x3 squared distance: the guard's direct-form pass runs the CUDA-core kernel)
     if (!p->unary && p->kernel != TRA_KERNEL_TC_BF16 && p->kernel != TRA_KERNEL_TC_BF16_PAIR &&
-        p->kernel != TRA_KERNEL_ELEMENTWISE && p->kernel != TRA_KERNEL_TC_SPLIT3)
+        p->kernel != TRA_KERNEL_ELEMENTWISE && !(p->kernel == TRA_KERNEL_TC_SPLIT3 && p->op != kSqdiff))
         scan_vec_flags(role_map(*p, p->X, kBatch), role_map(*p, p->X, kM), role_map(*p, p->X, kK),
                        role_map(*p, p->Y, kBatch), role_map(*p, p->Y, kN), role_map(*p, p->Y, kK),
                        role_map(*p, p->Z, kBatch), role_map(*p, p->Z, kM), role_map(*p, p->Z, kN),

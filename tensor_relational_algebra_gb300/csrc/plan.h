@@ -96,6 +96,13 @@ struct TcExtra {
     RoleMap zb, zm, zn;
     uint32_t M = 0, N = 0;  // with z_override: the rows / columns stored (the product may be padded)
     int* mark_count = nullptr;  // epi 2: count of outputs marked for the underflow fix-up
+    // epi 1: guard of the expansion -- where r + c - 2 acc < sq_tau (r + c), the word of the
+    // output's 128 x 128 tile (b, m / 128, n / 128) in fix_flags (zeroed by the caller) is set
+    float sq_tau = 0.f;
+    uint32_t* fix_flags = nullptr;
+    uint32_t fix_tiles_m = 0, fix_tiles_n = 0;
+    uint64_t fix_tag_index = 0;  // fix_flags[fix_tag_index] is set to 1 when any tile is marked
+    uint64_t z_elems = 0;        // with z_override: elements of the output buffer
 };
 // ws: the plan's workspace (tc->ws_part + tc->ws_flags bytes) for the K split of the last
 // wave's tiles; without it, or with ex, every tile runs on one worker.
@@ -103,6 +110,8 @@ int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_
                void* ws = nullptr);
 
 uint64_t align256(uint64_t v);
+// constants c of the squared-distance guard (sqdist_guard_tau): fp32 expansion, split=bf16x3
+constexpr double kSqGuardFp32 = 3.0, kSqGuardSplit3 = 4.5;
 inline uint64_t split3_pad(uint64_t v, uint64_t q) { return (v + q - 1) / q * q; }
 uint64_t repartition_cost_elems(int rank, const int64_t* shape, const int32_t* src_d, const int32_t* dst_d);
 uint64_t repartition_messages(int rank, const int64_t* shape, const int32_t* src_d, const int32_t* dst_d);

@@ -78,6 +78,57 @@ inline int64_t affine_stride(const RoleMap& r) {
     return t.loc_stride;
 }
 
+// ---------------------------------------------------------------- check builds
+// Built with -DTRA_CHECK (libtra_check.so), the plain global loads and stores of the CUDA-core
+// semiring, reduction, element-wise, split and repartition kernels and the warp stores of the
+// tensor-core epilogue test their index against the extent of the buffer first (chk).  An
+// access outside is skipped -- a load reads the aggregation's padding or 0, a store is dropped --
+// and the translation unit's check word keeps the first site number that failed; ein_status()
+// then returns TRA_ERR_BOUNDS.  Nothing traps.  In the normal build chk is constant true and
+// the tests compile away.  Site numbers: 1xx semiring kernels, 2xx k_misc.cu, 3xx tensor-core
+// epilogue.
+#ifdef TRA_CHECK
+namespace {
+__device__ int g_check_site;  // one per translation unit (internal linkage)
+}
+__device__ __forceinline__ bool chk(int64_t off, uint64_t n, int site) {
+    if (off >= 0 && (uint64_t)off < n) return true;
+    atomicCAS(&g_check_site, 0, site);
+    return false;
+}
+#define TRA_CHECK_READER(fn)                                                                       \
+    cudaError_t fn(int* v, cudaStream_t s) {                                                       \
+        cudaError_t e = cudaMemcpyFromSymbolAsync(v, g_check_site, sizeof(int), 0,                 \
+                                                  cudaMemcpyDeviceToHost, s);                      \
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);                                        \
+        const int zero = 0;                                                                        \
+        if (e == cudaSuccess && *v)                                                                \
+            e = cudaMemcpyToSymbolAsync(g_check_site, &zero, sizeof(int), 0,                       \
+                                        cudaMemcpyHostToDevice, s);                                \
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);                                        \
+        return e;                                                                                  \
+    }
+#else
+#ifdef __CUDACC__
+__device__ __forceinline__ constexpr bool chk(int64_t, uint64_t, int) { return true; }
+#endif
+#define TRA_CHECK_READER(fn)                      \
+    cudaError_t fn(int* v, cudaStream_t) {        \
+        *v = 0;                                   \
+        return cudaSuccess;                       \
+    }
+#endif
+// check words of the kernels' translation units (always 0 outside check builds)
+cudaError_t read_and_clear_check_semiring(int* v, cudaStream_t s);
+cudaError_t read_and_clear_check_misc(int* v, cudaStream_t s);
+cudaError_t read_and_clear_check_tc(int* v, cudaStream_t s);
+constexpr bool kCheckBuild =
+#ifdef TRA_CHECK
+    true;
+#else
+    false;
+#endif
+
 // Join + aggregate on CUDA cores (register-tiled).  Operands may be fp32 or bf16.
 struct SemiringParams {
     const void* x;
@@ -108,12 +159,24 @@ struct SemiringParams {
     // squared distance by expansion: the epilogue forms xn + yn - 2*sum
     const float* xnorm;   // [nb * M] or null
     const float* ynorm;   // [nb * N] or null
+    // Guard of the expansion: where xn + yn - 2*sum < sq_tau * (xn + yn) the subtraction has
+    // cancelled too far for the fp32 bar, and the CTA records its tile in tile_mark (one word
+    // per 128 x 128 output tile, in launch order: 1 marked, 0 not; every CTA writes its own
+    // word), and a CTA that marked writes gate_tag to the word after the last tile's.  A launch
+    // with tile_gate set returns at once unless that word holds gate_tag, and otherwise
+    // computes only the tiles whose word is nonzero (the direct-form fix-up pass).
+    float sq_tau;
+    uint32_t* tile_mark;
+    const uint32_t* tile_gate;
+    uint32_t gate_tag;
     // the underflow fix-up returns at once when this count (written by the producer of the
     // marks) is zero; null: scan every output
     const int* mark_count;
     // 1 when z is device memory (the bulk-copy epilogue writes only there; pinned host memory
     // the device can address gets plain stores)
     int32_t z_device;
+    // elements of x (and x_raw), y (and y_raw) and z: the check build's bounds
+    uint64_t x_elems, y_elems, z_elems;
 };
 
 // Per-operand row-max / exp-shift preparation of the factored logsumexp.
@@ -130,6 +193,7 @@ struct LsePrepParams {
     int32_t k_simple;
     FastDiv k_sub;
     int64_t k_ks, k_ls;
+    uint64_t src_elems;   // elements of src (and dst): the check build's bound
 };
 
 // One fp32 operand of a sum-of-products split for three BF16 products (split=bf16x3):
@@ -150,6 +214,7 @@ struct Split3StatsParams {
     uint32_t nb, R, K, kc;
     int32_t mode;
     int32_t k_fast;       // set by the launcher
+    uint64_t src_elems;   // the check build's bound
 };
 uint32_t split3_stats_chunks(uint64_t rows, uint64_t K);  // kc for nb * R rows
 
@@ -164,6 +229,7 @@ struct Split3Params {
     int32_t k_fast;       // set by the launcher: the innermost contracted label is contiguous
     int32_t k_dense;      // set by the launcher: one unsplit contracted label (offset k * k_ls)
     int64_t k_ls;
+    uint64_t src_elems;   // the check build's bound on src (dst: nb * Rp * K3p)
 };
 
 // Unary aggregation over the contracted labels (row reduction).
@@ -177,6 +243,7 @@ struct RowReduceParams {
     float alpha;
     int32_t in_bf16, out_bf16;
     int32_t k_affine;     // the contracted composite is contiguous (stride 1) over all of [0, K)
+    uint64_t x_elems, z_elems;  // the check build's bounds
 };
 
 // Join with aggregation "none": every output element is op(x, y); operands may broadcast.
@@ -204,6 +271,7 @@ struct ElementwiseParams {
     int32_t flat;
     uint32_t y_div;
     uint64_t total;
+    uint64_t x_elems, y_elems;  // the check build's bounds (z: total)
 };
 
 // Repartition (permute copy) between two relation layouts of one tensor: walks the
@@ -239,6 +307,23 @@ cudaError_t launch_lse_prep(const LsePrepParams& p, cudaStream_t s);
 // Outputs of the factored logsumexp marked NaN (their exp-shifted sum underflowed) are
 // recomputed straight from p.x_raw / p.y_raw through p's role maps.
 cudaError_t launch_lse_fixup(const SemiringParams& p, cudaStream_t s);
+// Squared distance in the direct form sum_k (x - y)^2 (fp32 operands) over the 128 x 128 output
+// tiles whose word in p.tile_gate is nonzero, when the word after them holds p.gate_tag; the
+// other tiles are left as they are.
+cudaError_t launch_sqdist_fixup(const SemiringParams& p, cudaStream_t s);
+// Guard threshold of the squared-distance expansion for a contracted extent K (see plan.cpp).
+float sqdist_guard_tau(uint64_t K, double c);
+// 128 x 128 output tiles of the CUDA-core kernels (the fix-up pass's grid)
+inline uint64_t semiring_tiles(uint64_t nb, uint64_t M, uint64_t N) {
+    return nb * ((M + 127) / 128) * ((N + 127) / 128);
+}
+// Guard words of the squared-distance expansion: one per tile, then the launch's tag word.
+inline uint64_t sqdist_guard_bytes(uint64_t nb, uint64_t M, uint64_t N) {
+    return (semiring_tiles(nb, M, N) + 1) * 4;
+}
+// A fresh nonzero tag per launch of the expanded squared distance (the tag word then tells
+// the fix-up pass whether this launch marked anything).
+uint32_t next_gate_tag();
 cudaError_t launch_split3(const Split3Params& p, cudaStream_t s);
 cudaError_t launch_split3_stats(const Split3StatsParams& p, cudaStream_t s);
 cudaError_t launch_row_reduce(const RowReduceParams& p, cudaStream_t s);

@@ -123,6 +123,13 @@ def test_unary_plan(lib):
 
 def test_kernel_choice(lib):
     assert lib.Plan("ij,jk->ik:sqdiff:sum", [64, 64, 64], [1, 1, 1, 1]).kernel == "semiring_f32"
+    # squared distance: expansion (row norms, column norms, one guard word per 128 x 128 tile and
+    # the launch's tag word)
+    # while K <= 3127, where the guard threshold 3 sqrt(K) 2^-24 / 1e-5 stays below 1
+    a = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    assert lib.Plan("ij,jk->ik:sqdiff:sum", [300, 3127, 200], [1, 1, 1, 1]).workspace_bytes == a(1200) + a(800) + a(3 * 2 * 4 + 4)
+    assert lib.Plan("ij,jk->ik:sqdiff:sum", [300, 3128, 200], [1, 1, 1, 1]).workspace_bytes == 0  # direct
+    assert lib.Plan("ij,jk->ik:sqdiff:sum:sqdiff=expand", [300, 3128, 200], [1, 1, 1, 1]).workspace_bytes > 0
     assert lib.Plan("ij,jk->ik:add:lse", [64, 64, 64], [1, 1, 1, 1]).kernel == "lse_factored"
     assert lib.Plan("ij,jk->ik:add:max:mode=literal", [64, 64, 64], [1, 2, 2, 1]).kernel == "literal"
     assert lib.Plan("hst,hs->hst:expsub:none:out=bf16", [2, 4, 8], [1, 1, 1, 1, 1]).kernel == "elementwise"
@@ -143,12 +150,15 @@ def test_split3_plans(lib):
     p = lib.Plan("ij,jk->ik:sqdiff:sum:split=bf16x3", [8192, 256, 8192], [8, 1, 1, 8])
     assert p.kernel == "tc_split3"
     # + the statistics' partials: 256 row tiles of 32, 8 chunks of the 256 contracted indices at most -> 1
-    assert p.workspace_bytes == a(8192 * 768 * 2) + a(8192 * 768 * 2) + a(8192 * 4) + a(8192 * 4) + 256 + a(8192 * 4)
+    # + the guard words of the expansion, one per 128 x 128 output tile
+    assert p.workspace_bytes == (a(8192 * 768 * 2) + a(8192 * 768 * 2) + a(8192 * 4) + a(8192 * 4) + 256 + a(8192 * 4)
+                                 + a(64 * 64 * 4 + 4))
     assert lib.Plan("ij,jk->ik:add:lse:split=bf16x3", [256, 64, 384], [2, 2, 2, 3]).kernel == "tc_split3"
     p = lib.Plan("bij,bjk->bik:sqdiff:sum:split=bf16x3", [3, 130, 24, 96], [3, 2, 1, 3, 1, 3])
     assert p.kernel == "tc_split3"
     # padded to the GEMM's tiles: M 130 -> 256, N 96 -> 128, 3K = 72 -> 128
-    assert p.workspace_bytes == a(3 * 256 * 128 * 2) + a(3 * 128 * 128 * 2) + a(3 * 130 * 4) + a(3 * 96 * 4) + 256 + a(3 * 130 * 4)
+    assert p.workspace_bytes == (a(3 * 256 * 128 * 2) + a(3 * 128 * 128 * 2) + a(3 * 130 * 4) + a(3 * 96 * 4) + 256
+                                 + a(3 * 130 * 4) + a(3 * 2 * 1 * 4 + 4))
     # the cost terms are the plan's own (the split changes how, not what, is computed)
     q = lib.Plan("ij,jk->ik:sqdiff:sum", [8192, 256, 8192], [8, 1, 1, 8])
     p = lib.Plan("ij,jk->ik:sqdiff:sum:split=bf16x3", [8192, 256, 8192], [8, 1, 1, 8])
@@ -294,3 +304,24 @@ def test_back_to_back_detection():
     assert not AttentionGraph.back_to_back(buf[:10], buf[10:20].float(), buf[20:])  # dtypes differ
     strided = torch.zeros(60, dtype=torch.bfloat16)[::2]
     assert not AttentionGraph.back_to_back(strided[:10], strided[10:20], strided[20:])  # not contiguous
+
+
+def test_check_build_is_selected_by_the_environment(lib):
+    # TRA_CHECK=1 makes the binding load libtra_check.so, whose ein_build_flags reports the
+    # bounds-checked kernels; the default library reports none (no GPU needed to ask)
+    import subprocess
+    import sys
+
+    from tensor_relational_algebra_gb300 import _build
+
+    _build.build(check=True)
+    code = ("import tensor_relational_algebra_gb300 as t; l = t.load(); "
+            "print(l.ein_build_flags(), t._LIB_PATH.endswith('libtra_check.so'))")
+    out = {}
+    for flag in ("0", "1"):
+        r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                           env=dict(os.environ, TRA_CHECK=flag))
+        assert r.returncode == 0, r.stderr
+        out[flag] = r.stdout.split()
+    assert out["0"] == ["0", "False"]
+    assert out["1"] == ["1", "True"]
