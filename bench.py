@@ -804,7 +804,17 @@ def run_ours(args):
     value = job_throughput(ops, args.steps, world, total_ms)
 
     # end to end: pinned host inputs -> device, the step, results -> pinned host
-    pinned_in = [torch.from_numpy(h).reshape(-1).pin_memory() for h in host]
+    def pinned_host(h, like):
+        """Pinned host copy of one input with the device tensor's dtype: bf16 inputs are kept as
+        their bit patterns (uint16 viewed as bfloat16), so the copy is a plain byte transfer."""
+        t = torch.from_numpy(np.ascontiguousarray(h).reshape(-1))
+        if like.dtype == torch.bfloat16 and t.dtype == torch.uint16:
+            t = t.view(torch.bfloat16)
+        if t.dtype != like.dtype or t.numel() != like.numel():
+            raise ValueError(f"host input {t.dtype}[{t.numel()}] does not match device {like.dtype}[{like.numel()}]")
+        return t.pin_memory()
+
+    pinned_in = [pinned_host(h, d) for h, d in zip(host, wl.inputs_dev)]
     pinned_out = [torch.empty(o.numel(), dtype=o.dtype).pin_memory() for o in wl.outputs_dev]
 
     def h2d():
@@ -937,6 +947,63 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_probe_fp32(args):
+    """FP32 issue ceilings of the semiring kernels' inner step (ein_probe_fp32): one JSON record
+    with tuples per clock per SM, the SM clock the loop ran at (clock64 over the global timer)
+    and the absolute rate, for the sum of products (FFMA), max-plus (FADD + FADD + 3-input max)
+    and max-plus with the packed add."""
+    import torch
+
+    import tensor_relational_algebra_gb300 as tra
+
+    tra.load()
+    props = torch.cuda.get_device_properties(0)
+    sms = props.multi_processor_count
+    ctas = 2 * sms  # the semiring kernels' occupancy
+    sink = torch.empty(ctas * 256, dtype=torch.float32, device="cuda")
+    cyc = torch.empty(ctas, dtype=torch.int64, device="cuda")
+    nns = torch.empty(ctas, dtype=torch.int64, device="cuda")
+    peaks = measured_peaks()
+    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
+    kinds = [(0, "ffma: 2 FFMA per 2 tuples (sum of products)"),
+             (1, "max-plus: FADD + FADD + 3-input max.f32 per 2 tuples"),
+             (2, "max-plus: add.rn.f32x2 + 3-input max.f32 per 2 tuples")]
+    sampler = ClockSampler(0)
+    sampler.start()
+    w0 = time.time()
+    out = []
+    for kind, name in kinds:
+        for _ in range(2):  # warm-up launch
+            tra.ein_probe_fp32(kind, 64, ctas, sink, cyc, nns)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        per_cta = tra.ein_probe_fp32(kind, args.probe_iters, ctas, sink, cyc, nns)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        c = cyc.cpu().numpy().astype(np.float64)
+        n = nns.cpu().numpy().astype(np.float64)
+        cmed = float(np.median(c))
+        tpc = 2 * per_cta / cmed  # two CTAs per SM
+        mhz = float(np.median(c / n * 1e3))
+        rate = per_cta * ctas / (ms * 1e-3)
+        out.append({"kind": kind, "loop": name, "tuples_per_clk_per_sm": round(tpc, 2),
+                    "loop_cycles_min_median_max": [int(c.min()), int(cmed), int(c.max())],
+                    "loop_ms_min_median_max": [round(float(n.min()) * 1e-6, 3), round(float(np.median(n)) * 1e-6, 3),
+                                               round(float(n.max()) * 1e-6, 3)],
+                    "flop_per_clk_per_sm": round(2 * tpc, 2), "of_issue_peak_256_flop_per_clk": round(2 * tpc / 256, 4),
+                    "sm_mhz_in_loop": round(mhz, 1), "event_ms": round(ms, 3), "tuples_per_s": rate,
+                    "tflops_2_per_tuple": 2 * rate / 1e12,
+                    "of_fp32_peak_at_max_clock": 2 * rate / (sms * FP32_LANES_PER_SM * 2 * sm_max * 1e6)})
+    sampler.mark(w0, time.time())
+    rec = {"probe": "fp32", "sms": sms, "ctas": ctas, "threads_per_cta": 256, "iters": args.probe_iters,
+           "fp32_peak_tflops_at_max_clock": sms * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12,
+           "peak_derivation": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 flop x {sm_max:.0f} MHz",
+           "results": out, "clocks": sampler.stop(), "gpu": props.name}
+    print(json.dumps(rec))
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -982,10 +1049,15 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=None, help="oracle sample size of the CPU baseline")
     ap.add_argument("--ref-rows", type=int, default=None, help="oracle sample size per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--probe", choices=["fp32"], default=None,
+                    help="run a measurement probe instead of a workload (fp32: the semiring inner step's issue ceilings)")
+    ap.add_argument("--probe-iters", type=int, default=4000)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.probe == "fp32":
+        run_probe_fp32(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -313,6 +313,22 @@ int ein_execute_sqdist_noalloc(tra_plan_t plan, const void* in0, const void* in1
  * Errors: TRA_ERR_CUDA (launch failure). */
 int ein_selftest_wait_timeout(uint64_t timeout_ns, tra_stream_t stream);
 
+/* ein_probe_fp32 -- measurement aid (the EinDecomp page has no counterpart): the FP32 issue
+ * ceiling of the CUDA-core semiring kernels' inner step.  Launches ctas CTAs of 256 threads
+ * (two per SM, as the semiring kernels run); each thread keeps the kernels' 8 x 8 register
+ * tile and reads operands from shared memory in their staging layout, iters times 32 k, with
+ * no global memory traffic inside the timed loop.  kind 0: two FFMA per two tuples (sum of
+ * products); 1: FADD, FADD, one 3-input max.f32 (max-plus); 2: one add.rn.f32x2 and one
+ * 3-input max (max-plus, packed add).
+ * sink:   device, >= ctas * 256 floats (results that keep the loop alive)
+ * cycles: device, >= ctas uint64: SM clocks (clock64) of CTA i's loop
+ * nanos:  device, >= ctas uint64: the global timer's ns over the same loop
+ * tuples_per_cta (host): receives the tuples one CTA evaluates.
+ * Tuples per clock per SM = 2 * tuples_per_cta / cycles; the SM clock = cycles / nanos.
+ * Asynchronous on stream.  Errors: TRA_ERR_ARG, TRA_ERR_CUDA. */
+int ein_probe_fp32(int kind, int iters, int ctas, void* sink, void* cycles, void* nanos, uint64_t* tuples_per_cta,
+                   tra_stream_t stream);
+
 /* ein_build_flags -- how this library was built: TRA_BUILD_CHECK is set in the check build
  * (libtra_check.so, compiled with -DTRA_CHECK).  There every plain global load and store of
  * the CUDA-core semiring, reduction, element-wise, split and repartition kernels and the warp

@@ -119,6 +119,8 @@ def load():
     lib.ein_attention.argtypes = [i32, i32, i32, i32, ctypes.c_float, vp, vp, vp, vp, vp, vp]
     lib.ein_build_flags.argtypes = []
     lib.ein_build_flags.restype = ctypes.c_int
+    lib.ein_probe_fp32.argtypes = [i32, i32, i32, vp, vp, vp, u64p, vp]
+    lib.ein_probe_fp32.restype = ctypes.c_int
     for f in ("ein_plan", "ein_plan_info", "ein_plan_keys", "ein_execute", "ein_repartition",
               "ein_repartition_cost", "ein_repartition_messages", "ein_status", "ein_graph_decompose",
               "ein_attention"):
@@ -245,6 +247,14 @@ def ein_attention(s: int, t: int, h: int, d: int, scale: float, q, k, v, o, lse=
 def attention(q, k, v, o, s: int, t: int, h: int, d: int = 128, scale: float = None, lse=None, stream=None):
     """Fused Scores -> logsumexp -> exp -> A.V on device tensors (see ein_attention)."""
     ein_attention(s, t, h, d, (1.0 / d ** 0.5) if scale is None else scale, q, k, v, o, lse, stream)
+
+
+def ein_probe_fp32(kind: int, iters: int, ctas: int, sink, cycles, nanos, stream=None) -> int:
+    """Launch the FP32 issue-ceiling probe (see include/tra.h); returns tuples per CTA."""
+    n = ctypes.c_uint64()
+    _check(load().ein_probe_fp32(kind, iters, ctas, _ptr(sink), _ptr(cycles), _ptr(nanos), ctypes.byref(n),
+                                 _stream(stream)))
+    return n.value
 
 
 def ein_status(stream=None):
