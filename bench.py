@@ -713,18 +713,43 @@ def roofline_of(step, ms, peaks, props):
     return step.work / (ms * 1e-3) / 1e9, float(peaks.get("hbm_gbs", 6800.0)), "GB/s"
 
 
+def fp32_mix_ceilings():
+    """Fractions of the FP32 peak that the semiring inner step's instruction mix reaches by
+    itself (profiles/fp32_ceilings.json, written by --probe fp32): {kind: frac}."""
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "fp32_ceilings.json")))["record"]
+        return {r["kind"]: r["of_fp32_peak_at_max_clock"] for r in rec["results"]}
+    except (OSError, KeyError, ValueError):
+        return {}
+
+
+def mix_kind(step_name):
+    """Probe kind whose loop is the node's inner step: 1 for max/min-plus, 0 for FFMA loops."""
+    if "/max" in step_name or "/min" in step_name:
+        return 1
+    if "/sum" in step_name or "lse" in step_name or "logsumexp" in step_name:
+        return 0
+    return None
+
+
 def roofline_nodes(wl, means, peaks, props):
     nodes = []
+    mix = fp32_mix_ceilings()
     for step, ms in zip(wl.steps, means):
         a, pk, u = roofline_of(step, ms, peaks, props)
-        nodes.append({"name": step.name, "bound": step.bound, "ms": round(ms, 4), "achieved": round(a, 1),
-                      "unit": u, "frac": round(a / pk, 3)})
+        node = {"name": step.name, "bound": step.bound, "ms": round(ms, 4), "achieved": round(a, 1),
+                "unit": u, "frac": round(a / pk, 3)}
+        k = mix_kind(step.name) if step.bound == "alu" else None
+        if k in mix:
+            node["instruction_mix_ceiling_frac"] = round(mix[k], 3)
+        nodes.append(node)
     return nodes
 
 
 def peak_source(bound):
-    return ("derived: SMs x 128 FP32 lanes x 2 x max SM clock (MEASURED_PEAKS sm_max_mhz)" if bound == "alu"
-            else "MEASURED_PEAKS.json (of measured)")
+    return ("derived: SMs x 128 FP32 lanes x 2 x max SM clock (MEASURED_PEAKS sm_max_mhz); the inner step's "
+            "instruction-mix ceilings are measured in profiles/fp32_ceilings.json (bench.py --probe fp32)"
+            if bound == "alu" else "MEASURED_PEAKS.json (of measured)")
 
 
 def extra_workload(torch, tra, name, args, flush, local):
