@@ -164,9 +164,10 @@ int ein_plan_keys(tra_plan_t plan, int32_t* xyz_keys, int64_t capacity);
  * the plan's d (in1 = NULL for a unary EinSum); element types per the in=/out=
  * options (in0, in1 may be NULL for an empty plan, out too when the output has no
  * elements).  out may also be pinned host memory that the device can address (a
- * cudaHostAlloc'd buffer under unified addressing) for every kernel but the tensor-core
- * ones (TRA_KERNEL_TC_*, whose operands and outputs go through TMA tensor maps): the
- * kernels then store the result straight into host memory over the host link.  workspace: device scratch of at least info.workspace_bytes (may be NULL
+ * cudaHostAlloc'd buffer under unified addressing): the kernels then store the result
+ * straight into host memory over the host link (the tensor-core kernels switch to their
+ * warp-store epilogue for that call; their operands stay in device memory, read through
+ * TMA tensor maps).  workspace: device scratch of at least info.workspace_bytes (may be NULL
  * when that is 0); it is overwritten.  Asynchronous on stream.  Calls that may overlap
  * on the GPU need separate workspaces.  Tensor-core plans size their workspace at
  * ein_plan for the device current then (partial sums and flags of the K-split tiles,

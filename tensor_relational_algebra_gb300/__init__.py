@@ -371,11 +371,14 @@ class Plan:
         calls of one plan that may overlap on the GPU (other streams) must each pass their own
         workspace."""
         if workspace is None and self.info.workspace_bytes:
-            ws = getattr(self, "_workspace", None)
-            if ws is None or ws.device != z.device:
-                import torch
+            import torch
 
-                ws = torch.empty(self.info.workspace_bytes, dtype=torch.uint8, device=z.device)
+            # device scratch, on the inputs' device (z may be pinned host memory)
+            dev = x.device if x is not None and x.is_cuda else (z.device if z.is_cuda else
+                                                                 torch.device("cuda", torch.cuda.current_device()))
+            ws = getattr(self, "_workspace", None)
+            if ws is None or ws.device != dev:
+                ws = torch.empty(self.info.workspace_bytes, dtype=torch.uint8, device=dev)
                 self._workspace = ws
             workspace = ws
         ws_bytes = 0

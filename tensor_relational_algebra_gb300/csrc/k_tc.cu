@@ -1290,15 +1290,21 @@ int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_
     CUtensorMap ma, mb, mz;
     if (!encode(t.a, x, &ma) || !encode(t.b, y, &mb)) return fail(TRA_ERR_CUDA, "tensor map encoding failed");
     memset(&mz, 0, sizeof(mz));
-    if (t.z_tma && !encode(t.z, z, &mz, p.out_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                           p.out_bf16 ? 2 : 4))
+    // an output in pinned host memory (device-addressable under unified addressing) takes the
+    // warp-store epilogue: the tiles then cross the host link while later tiles compute
+    cudaPointerAttributes pa;
+    const bool z_device = cudaPointerGetAttributes(&pa, z) == cudaSuccess && pa.type == cudaMemoryTypeDevice;
+    (void)cudaGetLastError();
+    const bool z_tma = t.z_tma && z_device;
+    if (z_tma && !encode(t.z, z, &mz, p.out_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                         p.out_bf16 ? 2 : 4))
         return fail(TRA_ERR_CUDA, "output tensor map encoding failed");
     TcParams tp;
     memset(&tp, 0, sizeof(tp));
     tp.a = t.a.dev;
     tp.b = t.b.dev;
     tp.zt = t.z.dev;
-    tp.z_tma = t.z_tma ? 1u : 0u;
+    tp.z_tma = z_tma ? 1u : 0u;
     tp.nb = (uint32_t)p.ext[kBatch];
     tp.M = (uint32_t)p.ext[kM];
     tp.N = (uint32_t)p.ext[kN];
@@ -1329,7 +1335,7 @@ int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_
     tp.z_elems = (uint64_t)p.Z.total;
     if (ex) {
         if (ex->z_override) {
-            if (t.z_tma) return fail(TRA_ERR_UNSUPPORTED, "output addressing override needs warp stores");
+            if (z_tma) return fail(TRA_ERR_UNSUPPORTED, "output addressing override needs warp stores");
             if (ex->M > tp.M || ex->N > tp.N) return fail(TRA_ERR_ARG, "output bounds exceed the product");
             // the warp stores write runs of 32 columns: the map must keep each run contiguous
             if (ex->zn.n < 1 || ex->zn.t[0].div != 1 || ex->zn.t[0].loc_stride != 1 || ex->zn.t[0].sub % 32 ||

@@ -391,22 +391,29 @@ def test_empty_contraction(lib, cuda, eq, bounds, d, agg, out, alpha):
     (MM + ":sqdiff:sum", [300, 96, 264], [2, 2, 2, 2]),
     (MM + ":add:max", [300, 96, 264], [1, 1, 1, 1]),
     ("hst->hs::lse", [4, 96, 200], [2, 3, 1]),
+    # tensor cores: the TMA-store epilogue for device memory, warp stores for host memory
+    (MM + ":mul:sum:in=bf16", [512, 256, 384], [2, 1, 1, 3]),
+    (MM + ":mul:sum:in=bf16:tc=single:out=bf16", [384, 512, 192], [1, 1, 1, 1]),
+    (MM + ":mul:sum:in=bf16", [1024, 4096, 1024], [1, 1, 1, 1]),  # K-split tail
+    (MM + ":sqdiff:sum:split=bf16x3", [256, 64, 384], [1, 1, 1, 1]),
 ])
 def test_output_in_pinned_host_memory(lib, cuda, spec, bounds, d):
-    # the CUDA-core kernels may store their result straight into pinned host memory (unified
-    # addressing): bit-identical to the result written to device memory
+    # the kernels may store their result straight into pinned host memory (unified addressing):
+    # bit-identical to the result written to device memory
     import torch
 
     p = lib.Plan(spec, bounds, d)
     n_in = len(p.operands)
-    xs = [torch.from_numpy(gen(tuple(p.shape(w)), 15, i)).reshape(-1).cuda() for i, w in enumerate("xy"[:n_in])]
+    bf = "in=bf16" in spec
+    xs = [to_dev(gen(tuple(p.shape(w)), 15, i, bf16=bf)).reshape(-1) for i, w in enumerate("xy"[:n_in])]
     if n_in == 1:
         xs.append(None)
     nz = int(np.prod(p.shape("z")))
-    zd = torch.empty(nz, device="cuda")
-    zh = torch.full((nz,), 7.0).pin_memory()
+    odt = torch.bfloat16 if "out=bf16" in spec else torch.float32
+    zd = torch.empty(nz, device="cuda", dtype=odt)
+    zh = torch.full((nz,), 7.0, dtype=odt).pin_memory()
     p.execute(xs[0], xs[1], zd)
     p.execute(xs[0], xs[1], zh)
     torch.cuda.synchronize()
     lib.ein_status()
-    np.testing.assert_array_equal(zh.numpy(), zd.cpu().numpy())
+    assert torch.equal(zh, zd.cpu())
