@@ -104,11 +104,16 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     auto sk = [&](uint32_t st) { return base + (1 + st) * kTile; };
     auto sv = [&](uint32_t st) { return base + (1 + kKStages + st) * kTile; };
     const uint32_t bar = base + kTiles * kTile;
-    // barriers: q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], s_free[2], p_full,
-    // o_done[2], mma_done, xch[2][4]; then the TMEM slot, the abort flag and the exchange array
+    // barriers: q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], s_free[2], p_full
+    // of P buffer 0, o_done[2], mma_done, xch[2][4], (TMEM slot, abort flag), p_full of P buffer 1;
+    // then the exchange array
     const uint32_t q_full = bar, k_full = bar + 8, k_empty = bar + 32, v_full = bar + 56, v_empty = bar + 72,
-                   s_full = bar + 88, s_free = bar + 104, p_full = bar + 120, o_done = bar + 128,
-                   mma_done = bar + 144, xbar = bar + 152;
+                   s_full = bar + 88, s_free = bar + 104, o_done = bar + 128, mma_done = bar + 144,
+                   xbar = bar + 152;
+    // one "P_j published" barrier per P buffer: softmax can finish block j + 1 before the MMA warp
+    // waits for block j (P_{j+1} does not wait for P V_j), so a single barrier could run two
+    // phases ahead of its waiter; per buffer, block j + 2's phase needs P V_j, issued after the wait
+    auto p_full = [&](uint32_t b_) { return b_ ? bar + 224 : bar + 120; };
     uint8_t* gbase = smem_raw + (base - raw);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar + 216 - base));
     volatile int* abort = reinterpret_cast<volatile int*>(gbase + (bar + 220 - base));
@@ -131,7 +136,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             mbar_init(s_free + 8 * i, 8);   // one lane of each softmax warp: S_j is in registers
             mbar_init(o_done + 8 * i, 1);   // MMA commit after P_j V_j
         }
-        mbar_init(p_full, 8);               // one lane of each softmax warp: P_j stored, O rescaled
+        mbar_init(p_full(0), 8);            // one lane of each softmax warp: P_j stored, O rescaled
+        mbar_init(p_full(1), 8);
         mbar_init(mma_done, 1);
         for (int i = 0; i < 8; ++i) mbar_init(xbar + 8 * i, 64);  // both warps of a lane quarter
         *abort = 0;
@@ -147,8 +153,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
-    // columns: S buffers 0-127 and 128-255 (fp32), O 256-383 (fp32), P 384-447 (bf16 pairs:
-    // column c holds keys 2c and 2c + 1)
+    // columns: S buffers 0-127 and 128-255 (fp32), O 256-383 (fp32), P buffers 384-447 and
+    // 448-511 (bf16 pairs: column c holds keys 2c and 2c + 1); P_j goes to buffer j % 2
     const uint32_t t_s0 = tmem, t_o = tmem + 256, t_p = tmem + 384;
 
     // producer and MMA warps run their loops with the whole warp (waits taken by every lane, the
@@ -215,24 +221,28 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                 issue_s(j);
             }
         }
-        // Per block j every wait comes first (P_j published, V_j landed, and for S_{j+2} its S
-        // buffer read and K slot landed), then P V_j and S_{j+2} go out as one run of MMAs:
-        // a wait placed after a run of MMAs stalls until they have drained.
+        // Per block j: S_{j+2} goes out as soon as the softmax warps have read S_j into registers
+        // (its S buffer is then free) and K_{j+2} has landed -- early in softmax(j), so the tensor
+        // core computes it while softmax(j) runs -- and P V_j once P_j is published and V_j has
+        // landed.  (Issuing S_{j+2} only after P V_j left the tensor core idle between softmax
+        // blocks: softmax(j+1) waited for S_{j+1} behind the P_j hand-off.)
         for (uint32_t j = 0; ok && j < p.nb; ++j) {
             const uint32_t b = j & 1, ph = (j >> 1) & 1;
-            const bool more = j + 2 < p.nb;
-            if (!wait_u(p_full, j & 1) || !wait_u(v_full + 8 * b, ph)) break;
-            if (more && (!wait_u(s_free + 8 * b, ph) ||
-                         !wait_u(k_full + 8 * ((j + 2) % kKStages), ((j + 2) / kKStages) & 1)))
-                break;
+            if (j + 2 < p.nb) {
+                if (!wait_u(s_free + 8 * b, ph) ||
+                    !wait_u(k_full + 8 * ((j + 2) % kKStages), ((j + 2) / kKStages) & 1))
+                    break;
+                tc_fence_after();
+                issue_s(j + 2);  // into S buffer b, which the softmax warps have read
+            }
+            if (!wait_u(p_full(b), ph) || !wait_u(v_full + 8 * b, ph)) break;
             tc_fence_after();
             const uint64_t dvb = dv + ((b * kTile) >> 4);
 #pragma unroll
             for (uint32_t kk = 0; kk < kKeys / 16; ++kk)  // keys 16kk..16kk+15: P columns 8kk..8kk+7
-                tc_mma_ts_elect(t_o, t_p + kk * 8, dvb + ((kk * 2048) >> 4), id_o, (j | kk) != 0);
+                tc_mma_ts_elect(t_o, t_p + b * 64 + kk * 8, dvb + ((kk * 2048) >> 4), id_o, (j | kk) != 0);
             tc_commit_elect(o_done + 8 * b);
             tc_commit_elect(v_empty + 8 * b);
-            if (more) issue_s(j + 2);  // into S buffer b, which the softmax warps have read
         }
         // every MMA issued so far has completed once this commit arrives
         tc_commit_elect(mma_done);
@@ -246,10 +256,11 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         // halves' maxima through shared memory each block (so both use one reference maximum
         // m per row) and keep partial sums l_hf; O is shared.  m moves only when a block's
         // maximum exceeds it by more than 8 (log2 units): P stays below 2^8, and O is rescaled
-        // through tensor memory (each warp its 64 columns) only on such blocks.  P_j is stored
-        // to tensor memory once P V_{j-1} has completed (one P buffer), which is also when O
-        // may be rescaled.  The parity waits on o_done stay unambiguous: P V_j cannot complete
-        // before P_j is published.
+        // through tensor memory (each warp its 64 columns) only on such blocks, once P V_{j-1}
+        // has completed.  P_j goes to P buffer j % 2 once P V_{j-2}, the last reader of that
+        // buffer, has completed -- long before, so softmax(j) does not wait for P V_{j-1}.  The
+        // parity waits on o_done stay unambiguous: P V_j cannot complete before P_j is
+        // published.
         const uint32_t qr = warp & 3;                   // TMEM lane quarter
         const uint32_t hf = (uint32_t)(warp - 3) >> 2;  // key half
         const uint32_t row = qr * 32 + lane;            // query row inside the tile
@@ -307,17 +318,22 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                 }
                 sc[c] = s0 + s1;
             }
-            if (j >= 1 && !wait_a(o_done + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, abort, p.timeout_ns)) {
-                ok = false;
+            if (j >= 2 && !wait_a(o_done + 8 * b, ((j - 2) >> 1) & 1, abort, p.timeout_ns)) {
+                ok = false;  // P buffer b is free once P V_{j-2} has completed
                 break;
             }
             tc_fence_after();
-            tmem_st32(t_p + lanebase + hf * 32, pk);  // this half's 64 keys
+            tmem_st32(t_p + b * 64 + lanebase + hf * 32, pk);  // this half's 64 keys
             l = fmaf(l, corr, sc[0] + sc[1]);
             m_used = m_use;
             if (j > 0 && __any_sync(0xffffffffu, need)) {
-                // O *= corr, this warp's 64 columns (P V_{j-1} has completed; rows whose m_used
-                // stayed multiply by 1)
+                // O *= corr, this warp's 64 columns, once P V_{j-1} has completed (rows whose
+                // m_used stayed multiply by 1)
+                if (!wait_a(o_done + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, abort, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t orr[32];
@@ -331,7 +347,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(p_full(b));
         }
         // epilogue, once the last P V has completed (they complete in order): the two halves
         // add their partial sums (exchange slot nb % 2), then warp half hf writes output
