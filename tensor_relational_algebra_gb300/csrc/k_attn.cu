@@ -10,16 +10,16 @@
 // and O are rescaled by exp(m_old - m_new).  After the last block O / l is the chained
 // result and m + log l is L.
 //
-// One CTA per (head, 128 query rows); 11 warps:
+// One CTA per (head, 128 query rows); 7 warps:
 //   warp 0   TMA loads of Q (once) and of each K block (three slots, each freed once S_j is
 //            computed), one 32 KB copy per tile,
 //   warp 1   TMA loads of each V block (two slots, freed once P_j V_j is computed),
 //   warp 2   tensor memory and the MMAs: S_j = Q K_j^T into one of two TMEM buffers, then
-//            O += P_j V_j with P_j (bf16) read from tensor memory (one buffer),
-//   warps 3-10 (TMEM lane quarter warp % 4, one query row per thread, key half (warp - 3) / 4):
-//            the softmax update of that half (the halves share each block's row maximum), its
-//            P_j columns stored to tensor memory, the rescale of O, and the epilogue (O as bf16
-//            in [s][h][d]; L as fp32 in [h][s]).
+//            O += P_j V_j with P_j (bf16) read from tensor memory (two buffers),
+//   warps 3-6 (TMEM lane quarter warp % 4, one query row per thread, all 128 keys of a block in
+//            registers): the softmax update, P_j stored to tensor memory, the rescale of O, and
+//            the epilogue (O as bf16 in [s][h][d]; L as fp32 in [h][s]).  With whole rows per
+//            thread no warp waits on another for a row maximum or sum.
 // Every mbarrier wait is bounded; a wait that gives up records TRA_ERR_TIMEOUT in this unit's
 // status word (read by ein_status), raises the CTA's abort flag and the CTA leaves after its
 // copies and MMAs in flight have landed.
@@ -43,14 +43,13 @@ namespace {
 constexpr int kHead = 128;     // head dimension d
 constexpr int kRows = 128;     // query rows per CTA
 constexpr int kKeys = 128;     // keys per block
-constexpr int kThreadsA = 11 * 32;
+constexpr int kThreadsA = 7 * 32;
 constexpr uint32_t kTile = 128 * 128 * 2;   // one 128 x 128 bf16 operand tile (two 16 KB boxes)
 constexpr uint32_t kHalf = kTile / 2;       // one box: 64 columns x 128 rows
 constexpr uint32_t kKStages = 3;            // K tiles in flight; V has two
 constexpr uint32_t kTiles = 1 + kKStages + 2;
-// shared memory: Q | K0 K1 K2 | V0 V1 | barriers, TMEM slot, abort flag (256 B) | the softmax
-// warps' exchange array (2 KB); tiles 1024-aligned
-constexpr uint32_t kSmemA = kTiles * kTile + 1024 + 256 + 2048;
+// shared memory: Q | K0 K1 K2 | V0 V1 | barriers, TMEM slot, abort flag (256 B); tiles 1024-aligned
+constexpr uint32_t kSmemA = kTiles * kTile + 1024 + 256;
 
 struct AttnParams {
     uint32_t s, t, h, nb;   // query rows, keys, heads, key blocks
@@ -104,20 +103,17 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     auto sk = [&](uint32_t st) { return base + (1 + st) * kTile; };
     auto sv = [&](uint32_t st) { return base + (1 + kKStages + st) * kTile; };
     const uint32_t bar = base + kTiles * kTile;
-    // barriers: q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], s_free[2], p_full
-    // of P buffer 0, o_done[2], mma_done, xch[2][4], (TMEM slot, abort flag), p_full of P buffer 1;
-    // then the exchange array
+    // barriers: q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], s_free[2],
+    // p_full[2], o_done[2], mma_done; then the TMEM slot and the abort flag
     const uint32_t q_full = bar, k_full = bar + 8, k_empty = bar + 32, v_full = bar + 56, v_empty = bar + 72,
-                   s_full = bar + 88, s_free = bar + 104, o_done = bar + 128, mma_done = bar + 144,
-                   xbar = bar + 152;
+                   s_full = bar + 88, s_free = bar + 104, o_done = bar + 136, mma_done = bar + 152;
     // one "P_j published" barrier per P buffer: softmax can finish block j + 1 before the MMA warp
     // waits for block j (P_{j+1} does not wait for P V_j), so a single barrier could run two
     // phases ahead of its waiter; per buffer, block j + 2's phase needs P V_j, issued after the wait
-    auto p_full = [&](uint32_t b_) { return b_ ? bar + 224 : bar + 120; };
+    auto p_full = [&](uint32_t b_) { return bar + 120 + 8 * b_; };
     uint8_t* gbase = smem_raw + (base - raw);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar + 216 - base));
     volatile int* abort = reinterpret_cast<volatile int*>(gbase + (bar + 220 - base));
-    float* xval = reinterpret_cast<float*>(gbase + (bar + 256 - base));  // [2 slots][2 halves][128 rows]
 
     // warp index and tensor-memory base made provably warp-uniform (shuffled from lane 0), so the
     // tcgen05 operands derived from them live in uniform registers
@@ -133,13 +129,12 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             mbar_init(v_full + 8 * i, 1);
             mbar_init(v_empty + 8 * i, 1);  // MMA commit after P_j V_j
             mbar_init(s_full + 8 * i, 1);   // MMA commit after S_j
-            mbar_init(s_free + 8 * i, 8);   // one lane of each softmax warp: S_j is in registers
+            mbar_init(s_free + 8 * i, 4);   // one lane of each softmax warp: S_j is in registers
             mbar_init(o_done + 8 * i, 1);   // MMA commit after P_j V_j
         }
-        mbar_init(p_full(0), 8);            // one lane of each softmax warp: P_j stored, O rescaled
-        mbar_init(p_full(1), 8);
+        mbar_init(p_full(0), 4);            // one lane of each softmax warp: P_j stored, O rescaled
+        mbar_init(p_full(1), 4);
         mbar_init(mma_done, 1);
-        for (int i = 0; i < 8; ++i) mbar_init(xbar + 8 * i, 64);  // both warps of a lane quarter
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -251,19 +246,15 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------------ softmax, rescale, epilogue
-        // Warps 3-10: TMEM lane quarter warp % 4 (one query row per thread), key half
-        // hf = (warp - 3) / 4 of every block.  The two warps of a quarter exchange their
-        // halves' maxima through shared memory each block (so both use one reference maximum
-        // m per row) and keep partial sums l_hf; O is shared.  m moves only when a block's
-        // maximum exceeds it by more than 8 (log2 units): P stays below 2^8, and O is rescaled
-        // through tensor memory (each warp its 64 columns) only on such blocks, once P V_{j-1}
-        // has completed.  P_j goes to P buffer j % 2 once P V_{j-2}, the last reader of that
-        // buffer, has completed -- long before, so softmax(j) does not wait for P V_{j-1}.  The
-        // parity waits on o_done stay unambiguous: P V_j cannot complete before P_j is
-        // published.
-        const uint32_t qr = warp & 3;                   // TMEM lane quarter
-        const uint32_t hf = (uint32_t)(warp - 3) >> 2;  // key half
-        const uint32_t row = qr * 32 + lane;            // query row inside the tile
+        // Warps 3-6: TMEM lane quarter warp % 4, one query row per thread, all 128 keys of a
+        // block in registers (so the row maximum and sum need no exchange between warps).  m
+        // moves only when a block's maximum exceeds it by more than 8 (log2 units): P stays below
+        // 2^8, and O is rescaled through tensor memory only on such blocks, once P V_{j-1} has
+        // completed.  P_j goes to P buffer j % 2 once P V_{j-2}, the last reader of that buffer,
+        // has completed -- long before, so softmax(j) does not wait for P V_{j-1}.  The parity
+        // waits on o_done stay unambiguous: P V_j cannot complete before P_j is published.
+        const uint32_t qr = warp & 3;         // TMEM lane quarter
+        const uint32_t row = qr * 32 + lane;  // query row inside the tile
         const uint32_t lanebase = (qr * 32u) << 16;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
@@ -274,38 +265,31 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                 break;
             }
             tc_fence_after();
-            uint32_t sr[2][32];
+            uint32_t sr[4][32];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) tmem_ld32_nowait(t_s0 + lanebase + b * 128 + hf * 64 + c * 32, sr[c]);
+            for (int c = 0; c < 4; ++c) tmem_ld32_nowait(t_s0 + lanebase + b * 128 + c * 32, sr[c]);
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free + 8 * b);  // S buffer b may be overwritten
-            float mc[4];
+            float mc[8];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 8; ++c) {
                 const uint32_t* v = &sr[c >> 1][(c & 1) * 16];
                 float x = max3f(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
 #pragma unroll
                 for (int i = 3; i < 15; i += 2) x = max3f(x, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
                 mc[c] = fmaxf(x, __uint_as_float(v[15]));
             }
-            // the row maximum over both halves
-            xval[(b * 2 + hf) * 128 + row] = max3f(mc[0], mc[1], fmaxf(mc[2], mc[3]));
-            mbar_arrive(xbar + 8 * (b * 4 + qr));
-            if (!wait_a(xbar + 8 * (b * 4 + qr), ph, abort, p.timeout_ns)) {
-                ok = false;
-                break;
-            }
-            const float m_blk =
-                fmaxf(xval[(b * 2 + hf) * 128 + row], xval[(b * 2 + (hf ^ 1)) * 128 + row]) * p.scale_log2;
+            const float m_blk = max3f(max3f(mc[0], mc[1], mc[2]), max3f(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7])) *
+                                p.scale_log2;
             const bool need = m_blk > m_used + 8.f;
             const float m_use = need ? m_blk : m_used;
             const float corr = fast_exp2(m_used - m_use);  // 1 when m_used stays; 0 on the first block
-            uint32_t pk[32];
-            float sc[2];
+            uint32_t pk[2][32];
+            float sc[4];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 float s0 = 0.f, s1 = 0.f;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -314,7 +298,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                     s0 += p0;
                     s1 += p1;
                     const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-                    pk[c * 16 + i] = *reinterpret_cast<const uint32_t*>(&h2);
+                    pk[c >> 1][(c & 1) * 16 + i] = *reinterpret_cast<const uint32_t*>(&h2);
                 }
                 sc[c] = s0 + s1;
             }
@@ -323,25 +307,25 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                 break;
             }
             tc_fence_after();
-            tmem_st32(t_p + b * 64 + lanebase + hf * 32, pk);  // this half's 64 keys
-            l = fmaf(l, corr, sc[0] + sc[1]);
+            tmem_st32(t_p + b * 64 + lanebase, pk[0]);  // keys 0-63
+            tmem_st32(t_p + b * 64 + lanebase + 32, pk[1]);  // keys 64-127
+            l = fmaf(l, corr, (sc[0] + sc[1]) + (sc[2] + sc[3]));
             m_used = m_use;
             if (j > 0 && __any_sync(0xffffffffu, need)) {
-                // O *= corr, this warp's 64 columns, once P V_{j-1} has completed (rows whose
-                // m_used stayed multiply by 1)
+                // O *= corr, once P V_{j-1} has completed (rows whose m_used stayed multiply by 1)
                 if (!wait_a(o_done + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, abort, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     uint32_t orr[32];
-                    tmem_ld32_nowait(t_o + lanebase + hf * 64 + c * 32, orr);
+                    tmem_ld32_nowait(t_o + lanebase + c * 32, orr);
                     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
                     for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * corr);
-                    tmem_st32(t_o + lanebase + hf * 64 + c * 32, orr);
+                    tmem_st32(t_o + lanebase + c * 32, orr);
                 }
             }
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -349,25 +333,18 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full(b));
         }
-        // epilogue, once the last P V has completed (they complete in order): the two halves
-        // add their partial sums (exchange slot nb % 2), then warp half hf writes output
-        // columns 64hf..64hf+63 of O / l, and L = (m ln 2) + log(l).
-        const uint32_t jl = p.nb - 1, bx = p.nb & 1;
+        // epilogue, once the last P V has completed (they complete in order): O / l as bf16, and
+        // L = (m ln 2) + log(l)
+        const uint32_t jl = p.nb - 1;
         ok = ok && wait_a(o_done + 8 * (jl & 1), (jl >> 1) & 1, abort, p.timeout_ns);
         if (ok) {
-            xval[(bx * 2 + hf) * 128 + row] = l;
-            mbar_arrive(xbar + 8 * (bx * 4 + qr));
-            ok = wait_a(xbar + 8 * (bx * 4 + qr), (p.nb >> 1) & 1, abort, p.timeout_ns);
-        }
-        if (ok) {
-            const float lt = l + xval[(bx * 2 + (hf ^ 1)) * 128 + row];
-            const float inv = 1.f / lt;
+            const float inv = 1.f / l;
             tc_fence_after();
-            __nv_bfloat16* orow = p.o + ((uint64_t)(q0 + row) * p.h + hd) * kHead + hf * 64;
+            __nv_bfloat16* orow = p.o + ((uint64_t)(q0 + row) * p.h + hd) * kHead;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 uint32_t orr[32];
-                tmem_ld32_nowait(t_o + lanebase + hf * 64 + c * 32, orr);
+                tmem_ld32_nowait(t_o + lanebase + c * 32, orr);
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
@@ -381,7 +358,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                     *reinterpret_cast<uint4*>(orow + c * 32 + v * 8) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
-            if (p.lse && hf == 0) p.lse[(uint64_t)hd * p.s + q0 + row] = m_used * 0.6931471805599453f + logf(lt);
+            if (p.lse) p.lse[(uint64_t)hd * p.s + q0 + row] = m_used * 0.6931471805599453f + logf(l);
         }
     }
     tc_fence_before();
