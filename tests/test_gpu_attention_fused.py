@@ -58,6 +58,15 @@ def test_fused_attention_against_oracle(lib, cuda, s, t, h):
     assert np.all(np.abs(lse - L) <= 1e-4 * np.maximum(np.abs(L), 1.0))
 
 
+@pytest.mark.parametrize("s,t,h", [(10240, 256, 2), (8192, 128, 3)])
+def test_fused_attention_more_tiles_than_sms(lib, cuda, s, t, h):
+    # more (128-row query tile, head) CTAs than SMs (160 and 192 of them, t = 128: a single key
+    # block per tile), so CTAs of a later wave start while others run
+    o, lse, O, L = _run(lib, s, t, h, 90 + t + h)
+    check_bf16_bar(o, O)
+    assert np.all(np.abs(lse - L) <= 1e-4 * np.maximum(np.abs(L), 1.0))
+
+
 @pytest.mark.parametrize("factors", [[1, 2, 4, 8, 8, 16, 1, 16], [16, 8, 4, 2, 1, 1, 1, 1]])
 def test_fused_attention_growing_and_falling_block_maxima(lib, cuda, factors):
     """Key blocks scaled so the row maxima jump by more than 2^8 between blocks (the reference
