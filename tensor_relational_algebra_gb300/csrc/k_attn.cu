@@ -10,12 +10,12 @@
 // and O are rescaled by exp(m_old - m_new).  After the last block O / l is the chained
 // result and m + log l is L.
 //
-// One CTA per (head, 128 query rows); 7 warps:
+// One CTA per (head, 128 query rows); 8 warps:
 //   warp 0   TMA loads of Q (once) and of each K block (three slots, each freed once S_j is
 //            computed), one 32 KB copy per tile,
 //   warp 1   TMA loads of each V block (two slots, freed once P_j V_j is computed),
-//   warp 2   tensor memory and the MMAs: S_j = Q K_j^T into one of two TMEM buffers, then
-//            O += P_j V_j with P_j (bf16) read from tensor memory (two buffers),
+//   warp 2   tensor memory and the S MMAs: S_j = Q K_j^T into one of two TMEM buffers,
+//   warp 7   the P V MMAs: O += P_j V_j with P_j (bf16) read from tensor memory (two buffers),
 //   warps 3-6 (TMEM lane quarter warp % 4, one query row per thread, all 128 keys of a block in
 //            registers): the softmax update, P_j stored to tensor memory, the rescale of O, and
 //            the epilogue (O as bf16 in [s][h][d]; L as fp32 in [h][s]).  With whole rows per
@@ -43,7 +43,7 @@ namespace {
 constexpr int kHead = 128;     // head dimension d
 constexpr int kRows = 128;     // query rows per CTA
 constexpr int kKeys = 128;     // keys per block
-constexpr int kThreadsA = 7 * 32;
+constexpr int kThreadsA = 8 * 32;
 constexpr uint32_t kTile = 128 * 128 * 2;   // one 128 x 128 bf16 operand tile (two 16 KB boxes)
 constexpr uint32_t kHalf = kTile / 2;       // one box: 64 columns x 128 rows
 constexpr uint32_t kKStages = 3;            // K tiles in flight; V has two
@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     auto sv = [&](uint32_t st) { return base + (1 + kKStages + st) * kTile; };
     const uint32_t bar = base + kTiles * kTile;
     // barriers: q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], s_free[2],
-    // p_full[2], o_done[2], mma_done; then the TMEM slot and the abort flag
+    // p_full[2], o_done[2], mma_done[2]; then the TMEM slot and the abort flag
     const uint32_t q_full = bar, k_full = bar + 8, k_empty = bar + 32, v_full = bar + 56, v_empty = bar + 72,
                    s_full = bar + 88, s_free = bar + 104, o_done = bar + 136, mma_done = bar + 152;
     // one "P_j published" barrier per P buffer: softmax can finish block j + 1 before the MMA warp
@@ -134,7 +134,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         }
         mbar_init(p_full(0), 4);            // one lane of each softmax warp: P_j stored, O rescaled
         mbar_init(p_full(1), 4);
-        mbar_init(mma_done, 1);
+        mbar_init(mma_done, 1);      // the S issuer's last commit
+        mbar_init(mma_done + 8, 1);  // the P V issuer's last commit
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -186,63 +187,60 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             }
         }
         if (*abort) __nanosleep(20000);  // let copies already issued land before leaving
-    } else if (warp == 2) {
-        // ------------------------------------------------------------------ MMA issuer
-        // S = Q K^T: M = 128, N = 128 keys, Q and K K-major in shared memory.
+    } else if (warp == 2 || warp == 7) {
+        // ------------------------------------------------------------------ MMA issuers
+        // S = Q K^T: M = 128, N = 128 keys, Q and K K-major in shared memory (warp 2).
         // O += P V: M = 128, N = 128, P (A) in tensor memory, V M/N-major in shared memory
-        // (d innermost; its two 64-column boxes are 16 KB apart).  Descriptors are formed once;
-        // a tile or K-step offset is added to the start-address field (addresses stay below
-        // 2^18, so the field does not carry).
+        // (d innermost; its two 64-column boxes are 16 KB apart) (warp 7).
+        // Two issuing warps: a thread's mbarrier wait that follows its own tcgen05.commit stalls
+        // until the committed MMAs have drained, so one issuer would leave the tensor core idle
+        // between the S and P V streams (a clock64 trace showed ~500 cycles per block).  Apart,
+        // each stream's waits stall only on its own MMAs, and the tensor core interleaves the two.
+        // The streams touch separate tensor memory (S buffers / O and the P buffers they read),
+        // ordered through the softmax warps' barriers.  Descriptors are formed once; a tile or
+        // K-step offset is added to the start-address field (addresses stay below 2^18, so the
+        // field does not carry).
         const uint32_t id_s = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
         const uint32_t id_o = id_s | (1u << 16);
         const uint64_t dq = smem_desc(sq, 16, 1024), dk = smem_desc(sk(0), 16, 1024), dv = smem_desc(sv(0), kHalf, 1024);
-        bool ok = wait_u(q_full, 0);
-        // S_j = Q K_j^T into S buffer j % 2 (its K slot must have landed)
-        auto issue_s = [&](uint32_t j) {
-            const uint32_t st = j % kKStages, b = j & 1;
-            const uint64_t dks = dk + ((st * kTile) >> 4);
-#pragma unroll
-            for (uint32_t kk = 0; kk < kHead / 16; ++kk) {
-                const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-                tc_mma_elect(t_s0 + b * 128, dq + off, dks + off, id_s, kk != 0);
-            }
-            tc_commit_elect(s_full + 8 * b);
-            tc_commit_elect(k_empty + 8 * st);
-        };
-        for (uint32_t j = 0; ok && j < 2 && j < p.nb; ++j) {
-            ok = wait_u(k_full + 8 * (j % kKStages), (j / kKStages) & 1);
-            if (ok) {
+        bool ok = true;
+        if (warp == 2) {
+            // S_j = Q K_j^T into S buffer j % 2, as soon as the softmax warps have read S_{j-2}
+            // from that buffer and K_j has landed
+            ok = wait_u(q_full, 0);
+            for (uint32_t j = 0; ok && j < p.nb; ++j) {
+                const uint32_t st = j % kKStages, b = j & 1;
+                if (j >= 2 && !wait_u(s_free + 8 * b, ((j - 2) >> 1) & 1)) break;
+                if (!wait_u(k_full + 8 * st, (j / kKStages) & 1)) break;
                 tc_fence_after();
-                issue_s(j);
+                const uint64_t dks = dk + ((st * kTile) >> 4);
+#pragma unroll
+                for (uint32_t kk = 0; kk < kHead / 16; ++kk) {
+                    const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                    tc_mma_elect(t_s0 + b * 128, dq + off, dks + off, id_s, kk != 0);
+                }
+                tc_commit_elect(s_full + 8 * b);
+                tc_commit_elect(k_empty + 8 * st);
+            }
+        } else {
+            // P V_j once P_j is published and V_j has landed
+            for (uint32_t j = 0; ok && j < p.nb; ++j) {
+                const uint32_t b = j & 1, ph = (j >> 1) & 1;
+                if (!wait_u(p_full(b), ph) || !wait_u(v_full + 8 * b, ph)) break;
+                tc_fence_after();
+                const uint64_t dvb = dv + ((b * kTile) >> 4);
+#pragma unroll
+                for (uint32_t kk = 0; kk < kKeys / 16; ++kk)  // keys 16kk..16kk+15: P columns 8kk..8kk+7
+                    tc_mma_ts_elect(t_o, t_p + b * 64 + kk * 8, dvb + ((kk * 2048) >> 4), id_o, (j | kk) != 0);
+                tc_commit_elect(o_done + 8 * b);
+                tc_commit_elect(v_empty + 8 * b);
             }
         }
-        // Per block j: S_{j+2} goes out as soon as the softmax warps have read S_j into registers
-        // (its S buffer is then free) and K_{j+2} has landed -- early in softmax(j), so the tensor
-        // core computes it while softmax(j) runs -- and P V_j once P_j is published and V_j has
-        // landed.  (Issuing S_{j+2} only after P V_j left the tensor core idle between softmax
-        // blocks: softmax(j+1) waited for S_{j+1} behind the P_j hand-off.)
-        for (uint32_t j = 0; ok && j < p.nb; ++j) {
-            const uint32_t b = j & 1, ph = (j >> 1) & 1;
-            if (j + 2 < p.nb) {
-                if (!wait_u(s_free + 8 * b, ph) ||
-                    !wait_u(k_full + 8 * ((j + 2) % kKStages), ((j + 2) / kKStages) & 1))
-                    break;
-                tc_fence_after();
-                issue_s(j + 2);  // into S buffer b, which the softmax warps have read
-            }
-            if (!wait_u(p_full(b), ph) || !wait_u(v_full + 8 * b, ph)) break;
-            tc_fence_after();
-            const uint64_t dvb = dv + ((b * kTile) >> 4);
-#pragma unroll
-            for (uint32_t kk = 0; kk < kKeys / 16; ++kk)  // keys 16kk..16kk+15: P columns 8kk..8kk+7
-                tc_mma_ts_elect(t_o, t_p + b * 64 + kk * 8, dvb + ((kk * 2048) >> 4), id_o, (j | kk) != 0);
-            tc_commit_elect(o_done + 8 * b);
-            tc_commit_elect(v_empty + 8 * b);
-        }
-        // every MMA issued so far has completed once this commit arrives
-        tc_commit_elect(mma_done);
+        // every MMA this warp issued has completed once this commit arrives
+        const uint32_t done = warp == 2 ? mma_done : mma_done + 8;
+        tc_commit_elect(done);
         volatile int never = 0;
-        mbar_wait_status(mma_done, 0, &never, p.timeout_ns, &g_attn_status);
+        mbar_wait_status(done, 0, &never, p.timeout_ns, &g_attn_status);
         __syncwarp();
     } else {
         // ------------------------------------------------------------------ softmax, rescale, epilogue
