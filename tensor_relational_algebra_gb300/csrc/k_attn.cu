@@ -10,9 +10,13 @@
 // and O are rescaled by exp(m_old - m_new).  After the last block O / l is the chained
 // result and m + log l is L.
 //
-// One CTA per (head, 128 query rows); 8 warps:
-//   warp 0   TMA loads of Q (once) and of each K block (three slots, each freed once S_j is
-//            computed), one 32 KB copy per tile,
+// Persistent CTAs, one per SM, each taking work units (128 query rows of one head)
+// blockIdx.x, blockIdx.x + grid, ...; the key blocks of its units are counted in one sequence,
+// so the pipelines run on across unit boundaries (the next unit's Q loads into the other of two
+// Q buffers, its first S blocks compute while the current unit's last blocks finish, and its
+// first P V waits only until the softmax warps have read the previous unit's O).  8 warps:
+//   warp 0   TMA loads of Q (once per unit) and of each K block (three slots, each freed once
+//            S_j is computed), one 32 KB copy per tile,
 //   warp 1   TMA loads of each V block (two slots, freed once P_j V_j is computed),
 //   warp 2   tensor memory and the S MMAs: S_j = Q K_j^T into one of two TMEM buffers,
 //   warp 7   the P V MMAs: O += P_j V_j with P_j (bf16) read from tensor memory (two buffers),
@@ -47,12 +51,13 @@ constexpr int kThreadsA = 8 * 32;
 constexpr uint32_t kTile = 128 * 128 * 2;   // one 128 x 128 bf16 operand tile (two 16 KB boxes)
 constexpr uint32_t kHalf = kTile / 2;       // one box: 64 columns x 128 rows
 constexpr uint32_t kKStages = 3;            // K tiles in flight; V has two
-constexpr uint32_t kTiles = 1 + kKStages + 2;
-// shared memory: Q | K0 K1 K2 | V0 V1 | barriers, TMEM slot, abort flag (256 B); tiles 1024-aligned
+constexpr uint32_t kTiles = 2 + kKStages + 2;
+// shared memory: Q0 Q1 | K0 K1 K2 | V0 V1 | barriers, TMEM slot, abort flag (256 B); tiles 1024-aligned
 constexpr uint32_t kSmemA = kTiles * kTile + 1024 + 256;
 
 struct AttnParams {
     uint32_t s, t, h, nb;   // query rows, keys, heads, key blocks
+    uint32_t qtiles, units; // query tiles of 128 rows per head; units = qtiles * h
     float scale_log2;       // scale * log2(e)
     __nv_bfloat16* o;       // [s][h][d]
     float* lse;             // [h][s] or null
@@ -99,14 +104,18 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t sq = base;
-    auto sk = [&](uint32_t st) { return base + (1 + st) * kTile; };
-    auto sv = [&](uint32_t st) { return base + (1 + kKStages + st) * kTile; };
+    auto sq = [&](uint32_t qb) { return base + qb * kTile; };
+    auto sk = [&](uint32_t st) { return base + (2 + st) * kTile; };
+    auto sv = [&](uint32_t st) { return base + (2 + kKStages + st) * kTile; };
     const uint32_t bar = base + kTiles * kTile;
-    // barriers: q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], s_free[2],
-    // p_full[2], o_done[2], mma_done[2]; then the TMEM slot and the abort flag
+    // barriers: q_full (Q buffer 0), k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2],
+    // s_free[2], p_full[2], o_done[2], mma_done[2], q_full (Q buffer 1), q_empty[2] (a unit's last
+    // S has read its Q), o_free (the softmax warps have read a unit's O); then the TMEM slot and
+    // the abort flag
     const uint32_t q_full = bar, k_full = bar + 8, k_empty = bar + 32, v_full = bar + 56, v_empty = bar + 72,
-                   s_full = bar + 88, s_free = bar + 104, o_done = bar + 136, mma_done = bar + 152;
+                   s_full = bar + 88, s_free = bar + 104, o_done = bar + 136, mma_done = bar + 152,
+                   q_full2 = bar + 168, q_empty = bar + 176, o_free = bar + 192;
+    auto qf = [&](uint32_t qb) { return qb ? q_full2 : q_full; };
     // one "P_j published" barrier per P buffer: softmax can finish block j + 1 before the MMA warp
     // waits for block j (P_{j+1} does not wait for P V_j), so a single barrier could run two
     // phases ahead of its waiter; per buffer, block j + 2's phase needs P V_j, issued after the wait
@@ -118,9 +127,13 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     // warp index and tensor-memory base made provably warp-uniform (shuffled from lane 0), so the
     // tcgen05 operands derived from them live in uniform registers
     const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x / 32), 0), lane = threadIdx.x % 32;
-    const uint32_t hd = blockIdx.y, q0 = blockIdx.x * kRows;
+    const uint32_t nu = (p.units - blockIdx.x + gridDim.x - 1) / gridDim.x;
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        mbar_init(q_full2, 1);
+        mbar_init(q_empty, 1);
+        mbar_init(q_empty + 8, 1);
+        mbar_init(o_free, 4);
         for (int i = 0; i < kKStages; ++i) {
             mbar_init(k_full + 8 * i, 1);   // the K producer's arrive with its bytes
             mbar_init(k_empty + 8 * i, 1);  // MMA commit after S_j (K_j read)
@@ -161,27 +174,34 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     if (warp <= 1) {
         // ------------------------------------------------------------------ producers (K: warp 0, V: warp 1)
         // one 32 KB copy per tile (both 64-column halves)
-        if (warp == 0) {
-            if (elect_one()) {
-                mbar_expect_tx(q_full, kTile);
-                tma_load_tile(sq, &map_q, q_full, (int)(hd * p.s + q0));
-            }
-            for (uint32_t j = 0; j < p.nb; ++j) {
-                const uint32_t st = j % kKStages, ph = (j / kKStages) & 1;
-                if (!wait_u(k_empty + 8 * st, ph ^ 1)) break;
+        bool ok = true;
+        uint32_t g = 0;
+        for (uint32_t i = 0; ok && i < nu; ++i) {
+            const uint32_t u = blockIdx.x + i * gridDim.x, hd = u / p.qtiles, q0 = (u % p.qtiles) * kRows;
+            if (warp == 0) {
+                const uint32_t qb = i & 1;
+                if (i >= 2 && !wait_u(q_empty + 8 * qb, ((i - 2) >> 1) & 1)) break;
                 if (elect_one()) {
-                    mbar_expect_tx(k_full + 8 * st, kTile);
-                    tma_load_tile(sk(st), &map_k, k_full + 8 * st, (int)(hd * p.t + j * kKeys));
+                    mbar_expect_tx(qf(qb), kTile);
+                    tma_load_tile(sq(qb), &map_q, qf(qb), (int)(hd * p.s + q0));
                 }
                 __syncwarp();
             }
-        } else {
-            for (uint32_t j = 0; j < p.nb; ++j) {
-                const uint32_t st = j & 1, ph = (j >> 1) & 1;
-                if (!wait_u(v_empty + 8 * st, ph ^ 1)) break;
-                if (elect_one()) {
-                    mbar_expect_tx(v_full + 8 * st, kTile);
-                    tma_load_tile(sv(st), &map_v, v_full + 8 * st, (int)(hd * p.t + j * kKeys));
+            for (uint32_t j = 0; j < p.nb; ++j, ++g) {
+                if (warp == 0) {
+                    const uint32_t st = g % kKStages, ph = (g / kKStages) & 1;
+                    if (!wait_u(k_empty + 8 * st, ph ^ 1)) { ok = false; break; }
+                    if (elect_one()) {
+                        mbar_expect_tx(k_full + 8 * st, kTile);
+                        tma_load_tile(sk(st), &map_k, k_full + 8 * st, (int)(hd * p.t + j * kKeys));
+                    }
+                } else {
+                    const uint32_t st = g & 1, ph = (g >> 1) & 1;
+                    if (!wait_u(v_empty + 8 * st, ph ^ 1)) { ok = false; break; }
+                    if (elect_one()) {
+                        mbar_expect_tx(v_full + 8 * st, kTile);
+                        tma_load_tile(sv(st), &map_v, v_full + 8 * st, (int)(hd * p.t + j * kKeys));
+                    }
                 }
                 __syncwarp();
             }
@@ -202,38 +222,47 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         // field does not carry).
         const uint32_t id_s = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
         const uint32_t id_o = id_s | (1u << 16);
-        const uint64_t dq = smem_desc(sq, 16, 1024), dk = smem_desc(sk(0), 16, 1024), dv = smem_desc(sv(0), kHalf, 1024);
+        const uint64_t dq = smem_desc(sq(0), 16, 1024), dk = smem_desc(sk(0), 16, 1024), dv = smem_desc(sv(0), kHalf, 1024);
         bool ok = true;
         if (warp == 2) {
             // S_j = Q K_j^T into S buffer j % 2, as soon as the softmax warps have read S_{j-2}
             // from that buffer and K_j has landed
-            ok = wait_u(q_full, 0);
-            for (uint32_t j = 0; ok && j < p.nb; ++j) {
-                const uint32_t st = j % kKStages, b = j & 1;
-                if (j >= 2 && !wait_u(s_free + 8 * b, ((j - 2) >> 1) & 1)) break;
-                if (!wait_u(k_full + 8 * st, (j / kKStages) & 1)) break;
-                tc_fence_after();
-                const uint64_t dks = dk + ((st * kTile) >> 4);
+            uint32_t g = 0;
+            for (uint32_t i = 0; ok && i < nu; ++i) {
+                const uint32_t qb = i & 1;
+                ok = wait_u(qf(qb), (i >> 1) & 1);
+                for (uint32_t j = 0; ok && j < p.nb; ++j, ++g) {
+                    const uint32_t st = g % kKStages, b = g & 1;
+                    if (g >= 2 && !wait_u(s_free + 8 * b, ((g - 2) >> 1) & 1)) { ok = false; break; }
+                    if (!wait_u(k_full + 8 * st, (g / kKStages) & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t dqs = dq + ((qb * kTile) >> 4), dks = dk + ((st * kTile) >> 4);
 #pragma unroll
-                for (uint32_t kk = 0; kk < kHead / 16; ++kk) {
-                    const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-                    tc_mma_elect(t_s0 + b * 128, dq + off, dks + off, id_s, kk != 0);
+                    for (uint32_t kk = 0; kk < kHead / 16; ++kk) {
+                        const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                        tc_mma_elect(t_s0 + b * 128, dqs + off, dks + off, id_s, kk != 0);
+                    }
+                    tc_commit_elect(s_full + 8 * b);
+                    tc_commit_elect(k_empty + 8 * st);
                 }
-                tc_commit_elect(s_full + 8 * b);
-                tc_commit_elect(k_empty + 8 * st);
+                if (ok) tc_commit_elect(q_empty + 8 * qb);  // this unit's Q has been read
             }
         } else {
             // P V_j once P_j is published and V_j has landed
-            for (uint32_t j = 0; ok && j < p.nb; ++j) {
-                const uint32_t b = j & 1, ph = (j >> 1) & 1;
-                if (!wait_u(p_full(b), ph) || !wait_u(v_full + 8 * b, ph)) break;
-                tc_fence_after();
-                const uint64_t dvb = dv + ((b * kTile) >> 4);
+            uint32_t g = 0;
+            for (uint32_t i = 0; ok && i < nu; ++i) {
+                for (uint32_t j = 0; j < p.nb; ++j, ++g) {
+                    const uint32_t b = g & 1, ph = (g >> 1) & 1;
+                    if (!wait_u(p_full(b), ph) || !wait_u(v_full + 8 * b, ph)) { ok = false; break; }
+                    if (j == 0 && i >= 1 && !wait_u(o_free, (i - 1) & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t dvb = dv + ((b * kTile) >> 4);
 #pragma unroll
-                for (uint32_t kk = 0; kk < kKeys / 16; ++kk)  // keys 16kk..16kk+15: P columns 8kk..8kk+7
-                    tc_mma_ts_elect(t_o, t_p + b * 64 + kk * 8, dvb + ((kk * 2048) >> 4), id_o, (j | kk) != 0);
-                tc_commit_elect(o_done + 8 * b);
-                tc_commit_elect(v_empty + 8 * b);
+                    for (uint32_t kk = 0; kk < kKeys / 16; ++kk)  // keys 16kk..16kk+15: P columns 8kk..8kk+7
+                        tc_mma_ts_elect(t_o, t_p + b * 64 + kk * 8, dvb + ((kk * 2048) >> 4), id_o, (j | kk) != 0);
+                    tc_commit_elect(o_done + 8 * b);
+                    tc_commit_elect(v_empty + 8 * b);
+                }
             }
         }
         // every MMA this warp issued has completed once this commit arrives
@@ -254,10 +283,13 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         const uint32_t qr = warp & 3;         // TMEM lane quarter
         const uint32_t row = qr * 32 + lane;  // query row inside the tile
         const uint32_t lanebase = (qr * 32u) << 16;
-        float m_used = -INFINITY, l = 0.f;
         bool ok = true;
-        for (uint32_t j = 0; j < p.nb; ++j) {
-            const uint32_t b = j & 1, ph = (j >> 1) & 1;
+        uint32_t g = 0;
+        for (uint32_t i = 0; ok && i < nu; ++i) {
+        const uint32_t u = blockIdx.x + i * gridDim.x, hd = u / p.qtiles, q0 = (u % p.qtiles) * kRows;
+        float m_used = -INFINITY, l = 0.f;
+        for (uint32_t j = 0; j < p.nb; ++j, ++g) {
+            const uint32_t b = g & 1, ph = (g >> 1) & 1;
             if (!wait_a(s_full + 8 * b, ph, abort, p.timeout_ns)) {
                 ok = false;
                 break;
@@ -300,7 +332,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                 }
                 sc[c] = s0 + s1;
             }
-            if (j >= 2 && !wait_a(o_done + 8 * b, ((j - 2) >> 1) & 1, abort, p.timeout_ns)) {
+            if (g >= 2 && !wait_a(o_done + 8 * b, ((g - 2) >> 1) & 1, abort, p.timeout_ns)) {
                 ok = false;  // P buffer b is free once P V_{j-2} has completed
                 break;
             }
@@ -311,7 +343,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             m_used = m_use;
             if (j > 0 && __any_sync(0xffffffffu, need)) {
                 // O *= corr, once P V_{j-1} has completed (rows whose m_used stayed multiply by 1)
-                if (!wait_a(o_done + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, abort, p.timeout_ns)) {
+                if (!wait_a(o_done + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1, abort, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
@@ -333,8 +365,8 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         }
         // epilogue, once the last P V has completed (they complete in order): O / l as bf16, and
         // L = (m ln 2) + log(l)
-        const uint32_t jl = p.nb - 1;
-        ok = ok && wait_a(o_done + 8 * (jl & 1), (jl >> 1) & 1, abort, p.timeout_ns);
+        const uint32_t gl = g - 1;
+        ok = ok && wait_a(o_done + 8 * (gl & 1), (gl >> 1) & 1, abort, p.timeout_ns);
         if (ok) {
             const float inv = 1.f / l;
             tc_fence_after();
@@ -357,6 +389,10 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                 }
             }
             if (p.lse) p.lse[(uint64_t)hd * p.s + q0 + row] = m_used * 0.6931471805599453f + logf(l);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_free);
+        }
         }
     }
     tc_fence_before();
@@ -434,6 +470,8 @@ extern "C" int ein_attention(int s, int t, int h, int d, float scale, const void
     ap.t = (uint32_t)t;
     ap.h = (uint32_t)h;
     ap.nb = (uint32_t)(t / kKeys);
+    ap.qtiles = (uint32_t)(s / kRows);
+    ap.units = ap.qtiles * (uint32_t)h;
     ap.scale_log2 = scale * 1.4426950408889634f;
     ap.o = reinterpret_cast<__nv_bfloat16*>(o);
     ap.lse = reinterpret_cast<float*>(lse);
@@ -441,7 +479,13 @@ extern "C" int ein_attention(int s, int t, int h, int d, float scale, const void
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaFuncSetAttribute(attn_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemA);
     if (e != cudaSuccess) return fail(TRA_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(e));
-    attn_fwd<<<dim3((unsigned)(s / kRows), (unsigned)h), kThreadsA, kSmemA, st>>>(mq, mk, mv, ap);
+    // persistent: one CTA per SM (its shared and tensor memory allow no second one)
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess || sms < 1) return fail(TRA_ERR_CUDA, "SM count: %s", cudaGetErrorString(e));
+    const unsigned grid = ap.units < (uint32_t)sms ? ap.units : (unsigned)sms;
+    attn_fwd<<<grid, kThreadsA, kSmemA, st>>>(mq, mk, mv, ap);
     e = cudaGetLastError();
     return e == cudaSuccess ? TRA_OK : fail(TRA_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
 }
