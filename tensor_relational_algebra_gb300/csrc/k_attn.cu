@@ -87,6 +87,27 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+// Two lanes of fp32 work per instruction (sm_100 packed forms; each lane rounds as the scalar
+// instruction does): d = a * b + c and d = a + b.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b, float c) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %4};\n\t"
+        "mov.b64 rc, {%5, %5};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+__device__ __forceinline__ void fadd2(float& s0, float& s1, float a0, float a1) {
+    asm("{\n\t.reg .b64 rs, ra;\n\t"
+        "mov.b64 rs, {%0, %1};\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "add.rn.f32x2 rs, rs, ra;\n\t"
+        "mov.b64 {%0, %1}, rs;\n\t}"
+        : "+f"(s0), "+f"(s1)
+        : "f"(a0), "f"(a1));
+}
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -323,10 +344,11 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                 float s0 = 0.f, s1 = 0.f;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c][2 * i]), p.scale_log2, -m_use));
-                    const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c][2 * i + 1]), p.scale_log2, -m_use));
-                    s0 += p0;
-                    s1 += p1;
+                    float x0, x1;
+                    ffma2(x0, x1, __uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]), p.scale_log2, -m_use);
+                    const float p0 = fast_exp2(x0);
+                    const float p1 = fast_exp2(x1);
+                    fadd2(s0, s1, p0, p1);
                     const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
                     pk[c >> 1][(c & 1) * 16 + i] = *reinterpret_cast<const uint32_t*>(&h2);
                 }

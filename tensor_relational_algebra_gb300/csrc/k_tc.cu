@@ -232,16 +232,28 @@ __device__ __forceinline__ void tc_commit_pair_elect(uint32_t bar, uint16_t ctam
         : "memory");
 }
 
-// One producer thread's share of the K steps of every tile this CTA (or CTA pair) owns:
+// One producer warp's share of the K steps of every tile this CTA (or CTA pair) owns:
 // steps g = pw, pw + kProducers, ...  Stage g % stages, phase (g / stages) & 1.  A parity
-// wait cannot alias an older phase because stages >= kProducers: when this thread reaches
+// wait cannot alias an older phase because stages >= kProducers: when this warp reaches
 // step g it has seen step g - kProducers - stages released, and releases are in order.
+// Lane 0 waits for the stage and arms its full barrier; then lane L issues box L of the step
+// (the A boxes, then the B boxes).  The copies of one issuing thread complete one after
+// another (a fixed ~560 cycles per box, whatever its size), so one box per lane lets the
+// step's boxes travel together.
 // PAIR: the copy of this CTA's half counts on the even CTA's full barrier (cta_group::2).
 template <bool PAIR>
 __device__ __forceinline__ void producer_steps(const CUtensorMap* map_a, const CUtensorMap* map_b, const TcParams& p,
-                                               uint32_t pw, uint32_t first_tile, uint32_t tile_step, uint32_t rank,
-                                               uint32_t base, uint32_t full0, uint32_t empty0, volatile int* abort) {
+                                               uint32_t pw, int lane, uint32_t first_tile, uint32_t tile_step,
+                                               uint32_t rank, uint32_t base, uint32_t full0, uint32_t empty0,
+                                               volatile int* abort) {
     const uint32_t stage_bytes = p.a_bytes + p.b_bytes;
+    // this lane's box: operand, map, index within the operand and offset within the stage
+    const uint32_t na = (uint32_t)p.a.n_loads, nbox = na + (uint32_t)p.b.n_loads;
+    const bool mine = (uint32_t)lane < nbox, is_a = (uint32_t)lane < na;
+    const TcOpDev& op = is_a ? p.a : p.b;
+    const CUtensorMap* map = is_a ? map_a : map_b;
+    const uint32_t l = is_a ? (uint32_t)lane : (uint32_t)lane - na;
+    const uint32_t box_off = (is_a ? 0u : p.a_bytes) + 8192u * l;
     // this worker's units: n_whole whole tiles, then at most one split unit (K steps skb0 .. skb1)
     const uint32_t n_whole = first_tile < p.n_full ? (p.n_full - first_tile + tile_step - 1) / tile_step : 0u;
     const uint32_t split_u = p.n_full + first_tile;
@@ -250,7 +262,7 @@ __device__ __forceinline__ void producer_steps(const CUtensorMap* map_a, const C
     const uint32_t whole_steps = n_whole * p.num_kb;
     const uint32_t total = whole_steps + (skb1 - skb0);
     uint32_t cur = 0xffffffffu;
-    int fa[2][5], fbx[4][5];
+    int fc[5];
     uint32_t pend_stage[2] = {0, 0}, pend_phase[2] = {0, 0}, n_pend = 0;
     bool ok = true;
     for (uint32_t g = pw; g < total; g += kProducers) {
@@ -270,56 +282,39 @@ __device__ __forceinline__ void producer_steps(const CUtensorMap* map_a, const C
             tile_of(p, tile, b, mt, nt);
             const uint32_t m0 = PAIR ? mt * 2 * kBlockM + rank * kBlockM : mt * kBlockM;
             const uint32_t n0 = PAIR ? nt * p.block_n + rank * (p.block_n / 2) : nt * p.block_n;
-#pragma unroll
-            for (int l = 0; l < 2; ++l)
-                if (l < p.a.n_loads) fixed_coords(p.a, b, m0 + 64u * l, fa[l]);
-#pragma unroll
-            for (int l = 0; l < 4; ++l)
-                if (l < p.b.n_loads) fixed_coords(p.b, b, n0 + 64u * l, fbx[l]);
+            if (mine) fixed_coords(op, b, (is_a ? m0 : n0) + 64u * l, fc);
         }
         const uint32_t stage = g % p.stages, phase = (g / p.stages) & 1u;
-        const bool got = PAIR ? mbar_wait_cl(empty0 + 8 * stage, phase ^ 1, abort, p.timeout_ns)
-                              : mbar_wait(empty0 + 8 * stage, phase ^ 1, abort, p.timeout_ns);
-        if (!got) {
+        const uint32_t fb = full0 + 8 * stage;
+        int got = 1;
+        if (lane == 0) {
+            got = PAIR ? mbar_wait_cl(empty0 + 8 * stage, phase ^ 1, abort, p.timeout_ns)
+                       : mbar_wait(empty0 + 8 * stage, phase ^ 1, abort, p.timeout_ns);
+            if (got) {
+                if (!PAIR) mbar_expect_tx(fb, stage_bytes);
+                else if (rank == 0) mbar_expect_tx(fb, 2 * stage_bytes);  // both CTAs' bytes land on the even CTA's barrier
+            }
+        }
+        if (!__shfl_sync(0xffffffffu, got, 0)) {
             ok = false;
             break;
         }
-        const uint32_t fb = full0 + 8 * stage;
-        uint32_t fb_sig = fb;
-        if (PAIR) {
-            if (rank == 0) mbar_expect_tx(fb, 2 * stage_bytes);  // both CTAs' bytes land on the even CTA's barrier
-            fb_sig = mapa_shared(fb, 0);
-        } else {
-            mbar_expect_tx(fb, stage_bytes);
+        if (mine) {
+            int kc[5], c[5];
+            k_coords(op, kb * kBlockK, kc);
+#pragma unroll
+            for (int j = 0; j < 5; ++j) c[j] = fc[j] + kc[j];
+            const uint32_t dst = base + stage * stage_bytes + box_off;
+            if (PAIR) tma_load_5d_pair(dst, map, mapa_shared(fb, 0), c);
+            else tma_load_5d(dst, map, fb, c);
         }
-        const uint32_t sa = base + stage * stage_bytes, sb = sa + p.a_bytes;
-        const uint32_t k0 = kb * kBlockK;
-        int ka[5], kbc[5], c[5];
-        k_coords(p.a, k0, ka);
-        k_coords(p.b, k0, kbc);
-#pragma unroll
-        for (int l = 0; l < 2; ++l)
-            if (l < p.a.n_loads) {
-#pragma unroll
-                for (int j = 0; j < 5; ++j) c[j] = fa[l][j] + ka[j];
-                if (PAIR) tma_load_5d_pair(sa + 8192u * l, map_a, fb_sig, c);
-                else tma_load_5d(sa + 8192u * l, map_a, fb_sig, c);
-            }
-#pragma unroll
-        for (int l = 0; l < 4; ++l)
-            if (l < p.b.n_loads) {
-#pragma unroll
-                for (int j = 0; j < 5; ++j) c[j] = fbx[l][j] + kbc[j];
-                if (PAIR) tma_load_5d_pair(sb + 8192u * l, map_b, fb_sig, c);
-                else tma_load_5d(sb + 8192u * l, map_b, fb_sig, c);
-            }
         pend_stage[n_pend & 1] = stage;
         pend_phase[n_pend & 1] = phase;
         ++n_pend;
     }
-    if (!ok) {
-        // let the copies this thread issued land before the CTA leaves (at most
-        // ceil(stages / kProducers) <= 2 are outstanding)
+    if (!ok && lane == 0) {
+        // let the copies this warp issued land before the CTA leaves (at most
+        // ceil(stages / kProducers) <= 2 steps are outstanding)
         if (PAIR) {
             __nanosleep(20000);  // the pair's copies count on the even CTA's barriers
         } else {
@@ -327,6 +322,7 @@ __device__ __forceinline__ void producer_steps(const CUtensorMap* map_a, const C
             for (uint32_t j = 0; j < 2 && j < n_pend; ++j) mbar_wait(full0 + 8 * pend_stage[j], pend_phase[j], &never, p.timeout_ns);
         }
     }
+    __syncwarp();
 }
 
 // Output tensor-map coordinates of the box starting at (b, m, n).
@@ -647,8 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < kProducers) {
         // ---------------------------------------------------------------- TMA producers
-        if (lane == 0)
-            producer_steps<false>(&map_a, &map_b, p, (uint32_t)warp, blockIdx.x, gridDim.x, 0u, base, full0, empty0, abort);
+        producer_steps<false>(&map_a, &map_b, p, (uint32_t)warp, lane, blockIdx.x, gridDim.x, 0u, base, full0, empty0, abort);
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
         // The whole warp runs the loop (waits by every lane, results shuffled from lane 0 so
@@ -790,8 +785,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (warp < kProducers) {
         // ---------------------------------------------------------------- TMA producers (both CTAs)
-        if (lane == 0)
-            producer_steps<true>(&map_a, &map_b, p, (uint32_t)warp, pair, n_pairs, rank, base, full0, empty0, abort);
+        producer_steps<true>(&map_a, &map_b, p, (uint32_t)warp, lane, pair, n_pairs, rank, base, full0, empty0, abort);
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer (even CTA)
         // whole warp, uniform waits, elected issue, descriptors formed once (as in tc_gemm)
