@@ -140,10 +140,23 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- workloads
 class Step:
-    """One named launch group inside a step, with its algorithmic work per launch."""
+    """One named launch group inside a step, with its algorithmic work per launch.
 
-    def __init__(self, name, fn, work, unit, bound, launches):
+    A tensor-core node may also give the bytes it must move at least (operands read once,
+    output written once).  Its roofline is then the resource that bounds it: HBM when those
+    bytes at the measured copy peak take longer than its flops at the measured BF16 peak
+    (arithmetic intensity below the ridge point), the tensor cores otherwise.  A node that
+    turns out HBM-bound keeps its flops in tensor_work."""
+
+    def __init__(self, name, fn, work, unit, bound, launches, min_bytes=None):
         self.name, self.fn, self.work, self.unit, self.bound, self.launches = name, fn, work, unit, bound, launches
+        self.tensor_work = None
+        if bound == "tensor" and min_bytes:
+            pk = measured_peaks()
+            t_flop = work / (float(pk.get("bf16_tflops", 1900.0)) * 1e12)
+            t_byte = min_bytes / (float(pk.get("hbm_gbs", 6800.0)) * 1e9)
+            if t_byte > t_flop:
+                self.tensor_work, self.work, self.unit, self.bound = work, min_bytes, "bytes", "hbm"
 
 
 def kernel_launches(plan) -> int:
@@ -747,6 +760,11 @@ def roofline_nodes(wl, means, peaks, props):
         a, pk, u = roofline_of(step, ms, peaks, props)
         node = {"name": step.name, "bound": step.bound, "ms": round(ms, 4), "achieved": round(a, 1),
                 "unit": u, "frac": round(a / pk, 3)}
+        if step.tensor_work:  # HBM-bound tensor-core node: its flops against the BF16 peak too
+            tf = step.tensor_work / (ms * 1e-3) / 1e12
+            node["tensor_achieved"] = round(tf, 1)
+            node["tensor_frac"] = round(tf / float(peaks.get("bf16_tflops", 1900.0)), 3)
+            node["flop_per_byte"] = round(step.tensor_work / step.work, 1)
         k = mix_kind(step.name) if step.bound == "alu" else None
         if k in mix:
             node["instruction_mix_ceiling_frac"] = round(mix[k], 3)

@@ -70,34 +70,42 @@ class AttentionGraph:
             ts[i + 1].data_ptr() == ts[i].data_ptr() + ts[i].numel() * ts[i].element_size() for i in range(len(ts) - 1))
 
     def nodes(self, Q, K, V, WQ, WK, WV, WO):
-        """(name, callable, work, unit, bound, kernel launches) per node, in execution order."""
+        """(name, callable, work, unit, bound, kernel launches[, bytes]) per node, in execution
+        order.  Tensor-core nodes also give the bytes they must move at least (operands read
+        once, output written once), from which a roofline can tell whether the node is bound by
+        the tensor cores or by HBM."""
         s, a, h, d = self.s, self.a, self.h, self.d
         shd = [s, h, d]
         gemm = 2 * s * a * h * d
         att = 2 * h * s * s * d
+        act = s * h * d * 2  # one bf16 activation of s x h x d (Q, K, V, O or a projection)
+        proj_bytes = s * a * 2 + a * h * d * 2 + act
         if self.back_to_back(Q, K, V) and self.back_to_back(WQ, WK, WV):
             proj = [("proj Q, K, V (one EinSum, p = 3)", lambda: self.p_proj3.execute(Q, WQ, self.qkvp), 3 * gemm,
-                     "flop", "tensor", 1)]
+                     "flop", "tensor", 1, 3 * proj_bytes)]
         else:
             proj = [
-                ("proj Q", lambda: self.p_proj.execute(Q, WQ, self.qp), gemm, "flop", "tensor", 1),
-                ("proj K", lambda: self.p_proj.execute(K, WK, self.kp), gemm, "flop", "tensor", 1),
-                ("proj V", lambda: self.p_proj.execute(V, WV, self.vp), gemm, "flop", "tensor", 1),
+                ("proj Q", lambda: self.p_proj.execute(Q, WQ, self.qp), gemm, "flop", "tensor", 1, proj_bytes),
+                ("proj K", lambda: self.p_proj.execute(K, WK, self.kp), gemm, "flop", "tensor", 1, proj_bytes),
+                ("proj V", lambda: self.p_proj.execute(V, WV, self.vp), gemm, "flop", "tensor", 1, proj_bytes),
             ]
         return proj + ([
             ("attention (Scores -> L -> exp -> A.V fused)",
              lambda: attention(self.qp, self.kp, self.vp, self.O, s, s, h, d, lse=self.L),
-             2 * att, "flop", "tensor", 1),
+             2 * att, "flop", "tensor", 1, 4 * act + h * s * 4),
         ] if self.fused else [
-            ("scores", lambda: self.p_scores.execute(self.qp, self.kp, self.S), att, "flop", "tensor", 1),
+            ("scores", lambda: self.p_scores.execute(self.qp, self.kp, self.S), att, "flop", "tensor", 1,
+             2 * act + h * s * s * 4),
             ("logsumexp", lambda: self.p_lse.execute(self.S, None, self.L), h * s * s * 4 + h * s * 4, "bytes", "hbm", 1),
             ("exp(S-L)", lambda: self.p_exp.execute(self.S, self.L, self.A), h * s * s * (4 + 2) + h * s * 4, "bytes",
              "hbm", 1),
-            ("A.V", lambda: self.p_pv.execute(self.A, self.vp, self.Oh), att, "flop", "tensor", 1),
+            ("A.V", lambda: self.p_pv.execute(self.A, self.vp, self.Oh), att, "flop", "tensor", 1,
+             h * s * s * 2 + 2 * act),
             ("repartition O -> dense", lambda: repartition(self.Oh, self.O, shd, [1, h, 1], [1, 1, 1]),
              2 * s * h * d * 2, "bytes", "hbm", 1),
         ]) + [
-            ("out proj", lambda: self.p_out.execute(self.O, WO, self.out), gemm, "flop", "tensor", 1),
+            ("out proj", lambda: self.p_out.execute(self.O, WO, self.out), gemm, "flop", "tensor", 1,
+             act + a * h * d * 2 + s * a * 4),
         ]
 
     def projection_weight(self, W):
