@@ -14,16 +14,18 @@
 // blockIdx.x, blockIdx.x + grid, ...; the key blocks of its units are counted in one sequence,
 // so the pipelines run on across unit boundaries (the next unit's Q loads into the other of two
 // Q buffers, its first S blocks compute while the current unit's last blocks finish, and its
-// first P V waits only until the softmax warps have read the previous unit's O).  8 warps:
+// first P V waits only until the softmax warps have read the previous unit's O).  12 warps:
 //   warp 0   TMA loads of Q (once per unit) and of each K block (three slots, each freed once
 //            S_j is computed), one 32 KB copy per tile,
 //   warp 1   TMA loads of each V block (two slots, freed once P_j V_j is computed),
 //   warp 2   tensor memory and the S MMAs: S_j = Q K_j^T into one of two TMEM buffers,
 //   warp 7   the P V MMAs: O += P_j V_j with P_j (bf16) read from tensor memory (two buffers),
-//   warps 3-6 (TMEM lane quarter warp % 4, one query row per thread, all 128 keys of a block in
+//   warps 3-6 and 8-11, two sets of softmax warps taking alternate key blocks (TMEM lane
+//            quarter warp % 4, one query row per thread, all 128 keys of a block in
 //            registers): the softmax update, P_j stored to tensor memory, the rescale of O, and
 //            the epilogue (O as bf16 in [s][h][d]; L as fp32 in [h][s]).  With whole rows per
-//            thread no warp waits on another for a row maximum or sum.
+//            thread no warp waits on another for a row maximum or sum within a block; the
+//            reference maximum passes from one set to the other once per block.
 // Every mbarrier wait is bounded; a wait that gives up records TRA_ERR_TIMEOUT in this unit's
 // status word (read by ein_status), raises the CTA's abort flag and the CTA leaves after its
 // copies and MMAs in flight have landed.
@@ -47,13 +49,16 @@ namespace {
 constexpr int kHead = 128;     // head dimension d
 constexpr int kRows = 128;     // query rows per CTA
 constexpr int kKeys = 128;     // keys per block
-constexpr int kThreadsA = 8 * 32;
+constexpr int kThreadsA = 12 * 32;
 constexpr uint32_t kTile = 128 * 128 * 2;   // one 128 x 128 bf16 operand tile (two 16 KB boxes)
 constexpr uint32_t kHalf = kTile / 2;       // one box: 64 columns x 128 rows
 constexpr uint32_t kKStages = 3;            // K tiles in flight; V has two
 constexpr uint32_t kTiles = 2 + kKStages + 2;
 // shared memory: Q0 Q1 | K0 K1 K2 | V0 V1 | barriers, TMEM slot, abort flag (256 B); tiles 1024-aligned
-constexpr uint32_t kSmemA = kTiles * kTile + 1024 + 256;
+// after the barrier block: 4 hand-off barriers (one per TMEM lane quarter) and the hand-off
+// message (per query row: reference maximum, a row sum and that sum's reference)
+constexpr uint32_t kHandoff = 32 + 3 * 128 * 4;
+constexpr uint32_t kSmemA = kTiles * kTile + 1024 + 256 + kHandoff;
 
 struct AttnParams {
     uint32_t s, t, h, nb;   // query rows, keys, heads, key blocks
@@ -142,6 +147,10 @@ __global__ void __launch_bounds__(kThreadsA, 1)
     // phases ahead of its waiter; per buffer, block j + 2's phase needs P V_j, issued after the wait
     auto p_full = [&](uint32_t b_) { return bar + 120 + 8 * b_; };
     uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t hand0 = bar + 256;
+    float* msg_m = reinterpret_cast<float*>(gbase + (bar + 288 - base));
+    float* msg_l = msg_m + 128;
+    float* msg_r = msg_m + 256;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar + 216 - base));
     volatile int* abort = reinterpret_cast<volatile int*>(gbase + (bar + 220 - base));
 
@@ -154,7 +163,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         mbar_init(q_full2, 1);
         mbar_init(q_empty, 1);
         mbar_init(q_empty + 8, 1);
-        mbar_init(o_free, 4);
+        mbar_init(o_free, 4);  // one lane of each softmax warp of the set writing the unit's O
         for (int i = 0; i < kKStages; ++i) {
             mbar_init(k_full + 8 * i, 1);   // the K producer's arrive with its bytes
             mbar_init(k_empty + 8 * i, 1);  // MMA commit after S_j (K_j read)
@@ -163,11 +172,12 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             mbar_init(v_full + 8 * i, 1);
             mbar_init(v_empty + 8 * i, 1);  // MMA commit after P_j V_j
             mbar_init(s_full + 8 * i, 1);   // MMA commit after S_j
-            mbar_init(s_free + 8 * i, 4);   // one lane of each softmax warp: S_j is in registers
+            mbar_init(s_free + 8 * i, 4);   // one lane of each softmax warp of the block's set: S_j read
             mbar_init(o_done + 8 * i, 1);   // MMA commit after P_j V_j
         }
-        mbar_init(p_full(0), 4);            // one lane of each softmax warp: P_j stored, O rescaled
+        mbar_init(p_full(0), 4);            // one lane of each softmax warp of the set: P_j stored, O rescaled
         mbar_init(p_full(1), 4);
+        for (int i = 0; i < 4; ++i) mbar_init(hand0 + 8 * i, 1);  // one lane of the quarter's softmax warp
         mbar_init(mma_done, 1);      // the S issuer's last commit
         mbar_init(mma_done + 8, 1);  // the P V issuer's last commit
         *abort = 0;
@@ -301,16 +311,47 @@ __global__ void __launch_bounds__(kThreadsA, 1)
         // completed.  P_j goes to P buffer j % 2 once P V_{j-2}, the last reader of that buffer,
         // has completed -- long before, so softmax(j) does not wait for P V_{j-1}.  The parity
         // waits on o_done stay unambiguous: P V_j cannot complete before P_j is published.
+        // Two sets of four softmax warps (warps 3-6 and 8-11) take alternate key blocks: set k
+        // handles the blocks g with g % 2 = k, always in S and P buffer k, so two softmax warps
+        // share each scheduler and one block's exponentials overlap the next one's.  The
+        // reference maximum passes from block g to block g + 1 through a message per lane quarter
+        // (hand-off barrier, phase g), published right after block g's maximum: the maximum
+        // after block g, and the sender's row sum just before block g with that sum's reference.
+        // A set rescales its own sum whenever the maximum it receives has moved.  The set that
+        // handles a unit's last block writes O / l: the other set's sum reaches it in the next
+        // message (the first block of the next unit, or a closing message after the last unit).
+        const uint32_t set = warp >= 8 ? 1u : 0u;
         const uint32_t qr = warp & 3;         // TMEM lane quarter
         const uint32_t row = qr * 32 + lane;  // query row inside the tile
         const uint32_t lanebase = (qr * 32u) << 16;
+        const uint32_t hb = hand0 + 8 * qr;
         bool ok = true;
         uint32_t g = 0;
+        float m_used = -INFINITY, l = 0.f;  // this set's reference maximum and row sum (current unit)
+        uint32_t my_unit = 0xffffffffu;     // the unit m_used and l belong to
         for (uint32_t i = 0; ok && i < nu; ++i) {
         const uint32_t u = blockIdx.x + i * gridDim.x, hd = u / p.qtiles, q0 = (u % p.qtiles) * kRows;
-        float m_used = -INFINITY, l = 0.f;
         for (uint32_t j = 0; j < p.nb; ++j, ++g) {
+            if ((g & 1) != set) continue;
             const uint32_t b = g & 1, ph = (g >> 1) & 1;
+            float m_in = -INFINITY;
+            if (g >= 1) {
+                if (!wait_a(hb, (g - 1) & 1, abort, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                m_in = msg_m[row];
+            }
+            const float l_before = l, r_before = m_used;
+            if (my_unit != i) {  // this set's first block of the unit (j = 0 or 1)
+                my_unit = i;
+                m_used = -INFINITY;
+                l = 0.f;
+            }
+            if (j > 0 && m_in > m_used) {  // block g - 1 (the other set's) moved the reference
+                l *= fast_exp2(m_used - m_in);
+                m_used = m_in;
+            }
             if (!wait_a(s_full + 8 * b, ph, abort, p.timeout_ns)) {
                 ok = false;
                 break;
@@ -337,6 +378,12 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             const bool need = m_blk > m_used + 8.f;
             const float m_use = need ? m_blk : m_used;
             const float corr = fast_exp2(m_used - m_use);  // 1 when m_used stays; 0 on the first block
+            // message g: the maximum after this block, and this set's sum before it
+            msg_m[row] = m_use;
+            msg_l[row] = l_before;
+            msg_r[row] = r_before;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(hb);
             uint32_t pk[2][32];
             float sc[4];
 #pragma unroll
@@ -355,7 +402,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                 sc[c] = s0 + s1;
             }
             if (g >= 2 && !wait_a(o_done + 8 * b, ((g - 2) >> 1) & 1, abort, p.timeout_ns)) {
-                ok = false;  // P buffer b is free once P V_{j-2} has completed
+                ok = false;  // P buffer b is free once P V_{g-2} has completed
                 break;
             }
             tc_fence_after();
@@ -364,7 +411,7 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             l = fmaf(l, corr, (sc[0] + sc[1]) + (sc[2] + sc[3]));
             m_used = m_use;
             if (j > 0 && __any_sync(0xffffffffu, need)) {
-                // O *= corr, once P V_{j-1} has completed (rows whose m_used stayed multiply by 1)
+                // O *= corr, once P V_{g-1} has completed (rows whose m_used stayed multiply by 1)
                 if (!wait_a(o_done + 8 * ((g - 1) & 1), ((g - 1) >> 1) & 1, abort, p.timeout_ns)) {
                     ok = false;
                     break;
@@ -385,12 +432,20 @@ __global__ void __launch_bounds__(kThreadsA, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full(b));
         }
-        // epilogue, once the last P V has completed (they complete in order): O / l as bf16, and
-        // L = (m ln 2) + log(l)
+        if (!ok) break;
+        // epilogue by the set that handled the unit's last block, once the last P V has completed
+        // (they complete in order): O / l as bf16, and L = (m ln 2) + log(l)
         const uint32_t gl = g - 1;
-        ok = ok && wait_a(o_done + 8 * (gl & 1), (gl >> 1) & 1, abort, p.timeout_ns);
+        if ((gl & 1) != set) continue;
+        float l_tot = l;
+        if (p.nb >= 2) {  // the other set's sum over its blocks of this unit, from message g
+            ok = wait_a(hb, g & 1, abort, p.timeout_ns);
+            if (!ok) break;
+            l_tot += msg_l[row] * fast_exp2(msg_r[row] - m_used);
+        }
+        ok = wait_a(o_done + 8 * (gl & 1), (gl >> 1) & 1, abort, p.timeout_ns);
         if (ok) {
-            const float inv = 1.f / l;
+            const float inv = 1.f / l_tot;
             tc_fence_after();
             __nv_bfloat16* orow = p.o + ((uint64_t)(q0 + row) * p.h + hd) * kHead;
 #pragma unroll
@@ -410,11 +465,21 @@ __global__ void __launch_bounds__(kThreadsA, 1)
                     *reinterpret_cast<uint4*>(orow + c * 32 + v * 8) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
-            if (p.lse) p.lse[(uint64_t)hd * p.s + q0 + row] = m_used * 0.6931471805599453f + logf(l);
+            if (p.lse) p.lse[(uint64_t)hd * p.s + q0 + row] = m_used * 0.6931471805599453f + logf(l_tot);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(o_free);
         }
+        }
+        // closing message (index g = all blocks): the sum of this set's last unit, for the set
+        // that handled that unit's last block
+        if (ok && (g & 1) == set && g >= 1) {
+            if (wait_a(hb, (g - 1) & 1, abort, p.timeout_ns)) {
+                msg_l[row] = l;
+                msg_r[row] = m_used;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(hb);
+            }
         }
     }
     tc_fence_before();

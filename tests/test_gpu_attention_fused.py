@@ -4,8 +4,9 @@ the unfused EinGraph nodes ("EinDecomp ... tensor relational algebra", section 2
 O is compared at the BF16 bar (2e-2 of max|ref|) with the oracle's chain evaluated in double
 (S, L = logsumexp_t S, A = exp(S - L), O = A.V); L within 1e-4 of max(|L|, 1).  The cases
 cover one key block, an odd number of key blocks with s != t, several heads, key blocks
-whose maxima grow (the kernel's reference maximum moves) or fall, and the whole attention
-EinGraph with the fused node against the unfused one.
+whose maxima grow (the kernel's reference maximum moves) or fall, CTAs that take several query
+tiles with an odd number of key blocks each, and the whole attention EinGraph with the fused
+node against the unfused one.
 """
 import numpy as np
 import pytest
@@ -72,6 +73,17 @@ def test_fused_attention_growing_and_falling_block_maxima(lib, cuda, factors):
     """Key blocks scaled so the row maxima jump by more than 2^8 between blocks (the reference
     maximum moves and O is rescaled, for some rows of a warp but not others) or only fall."""
     o, lse, O, L = _run(lib, 256, 1024, 2, 77, key_scale=factors)
+    check_bf16_bar(o, O)
+    assert np.all(np.abs(lse - L) <= 1e-4 * np.maximum(np.abs(L), 1.0))
+
+
+@pytest.mark.parametrize("key_scale", [None, [1, 16, 1]])
+def test_fused_attention_odd_blocks_several_units_per_cta(lib, cuda, key_scale):
+    """Three key blocks per query tile and 160 tiles on at most 152 CTAs: the two sets of
+    softmax warps take alternate key blocks, so a CTA's second tile starts on the other set,
+    whose first block of that tile is its second.  With the middle block scaled by 16 the
+    reference maximum moves on that block, for either set."""
+    o, lse, O, L = _run(lib, 10240, 384, 2, 55, key_scale=key_scale)
     check_bf16_bar(o, O)
     assert np.all(np.abs(lse - L) <= 1e-4 * np.maximum(np.abs(L), 1.0))
 
