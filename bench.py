@@ -486,9 +486,17 @@ class C5Workload(_PointsWorkload):
     # its warp-store epilogue for a host output), so its 1 GiB crosses the host link while later
     # tiles compute, with no device staging buffer and no copy-engine pass
     e2e_host_outputs = True
+    # inputs 2 x 512 MiB (larger than L2): step k + 1's copy in can run while step k computes
+    e2e_pipeline = True
 
     def redirect_outputs(self, outs):
         self.Z = outs[0]
+
+    def use_inputs(self, bufs):
+        self.Xr, self.Yr = bufs
+
+    def use_outputs(self, bufs):
+        self.Z = bufs[0]
 
     def ops_per_step(self):
         return 2 * 16384 ** 3
@@ -618,6 +626,71 @@ WORKLOADS = {"pair": PairWorkload, "c1": C1Workload, "c1l": C1LiteralWorkload, "
 
 
 # ----------------------------------------------------------------------------- measurement
+def time_e2e_pipelined(torch, wl, pinned_in, pinned_out, steps, warmup, staged):
+    """End to end as a stream of steps: step k + 1's inputs are copied in from pinned host memory
+    on a copy stream while step k computes, into the other of two device input buffers (a buffer
+    is reloaded only once the step that used it has finished).  The results reach pinned host
+    memory either from the kernels themselves (staged=False: the workload's outputs already point
+    there) or through two device output buffers copied out on a second copy stream while the next
+    step computes (staged=True; a buffer is rewritten only once its copy has left).  Returns the
+    ms from the start of the first copy in to the end of the last step's results."""
+    comp = torch.cuda.current_stream()
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+    bin_ = [list(wl.inputs_dev), [torch.empty_like(t) for t in wl.inputs_dev]]
+    bout = [list(wl.outputs_dev), [torch.empty_like(t) for t in wl.outputs_dev]] if staged else None
+
+    def event(stream):
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        return ev
+
+    def run(n, record):
+        done, left = [None, None], [None, None]
+
+        def load(k):
+            if done[k & 1] is not None:
+                cin.wait_event(done[k & 1])
+            with torch.cuda.stream(cin):
+                for src, dst in zip(pinned_in, bin_[k & 1]):
+                    dst.copy_(src, non_blocking=True)
+            return event(cin)
+
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if record:
+            start.record(cin)
+        ready = load(0)
+        for k in range(n):
+            comp.wait_event(ready)
+            wl.use_inputs(bin_[k & 1])
+            if staged:
+                if left[k & 1] is not None:
+                    comp.wait_event(left[k & 1])
+                wl.use_outputs(bout[k & 1])
+            for st in wl.steps:
+                st.fn()
+            done[k & 1] = event(comp)
+            if staged:
+                cout.wait_event(done[k & 1])
+                with torch.cuda.stream(cout):
+                    for src, dst in zip(bout[k & 1], pinned_out):
+                        dst.copy_(src, non_blocking=True)
+                left[k & 1] = event(cout)
+            if k + 1 < n:
+                ready = load(k + 1)
+        if record:
+            end.record(cout if staged else comp)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) if record else None
+
+    run(warmup, False)
+    ms = run(steps, True)
+    wl.use_inputs(bin_[0])
+    if staged:
+        wl.use_outputs(bout[0])
+    return ms
+
+
 def time_steps(torch, wl, steps, warmup, flush, sampler=None, e2e_io=None):
     """Run warmup + timed steps; per-launch-group CUDA events on the launching stream."""
     stream = torch.cuda.current_stream()
@@ -889,6 +962,13 @@ def run_ours(args):
     def d2h():
         torch.cuda.current_stream().wait_stream(copy_stream)
 
+    n_e2e = max(3, args.steps // 4)
+    e2e_alt = None
+    if getattr(wl, "e2e_pipeline", False):
+        # results staged in device memory and copied out while the next step computes
+        barrier()
+        e2e_alt = max_over_ranks(time_e2e_pipelined(torch, wl, pinned_in, pinned_out, n_e2e, args.warmup, True),
+                                 world)
     if getattr(wl, "e2e_host_outputs", False):
         # the step's kernels write pinned host memory themselves: the same bytes cross to the
         # host, with no device-side staging buffer and no copy engine pass
@@ -901,11 +981,27 @@ def run_ours(args):
             return None
 
     barrier()
-    e2e_ms, _, _, _ = time_steps(torch, wl, max(3, args.steps // 4), args.warmup, flush, None,
-                                 {"h2d": h2d, "after": after, "d2h": d2h})
+    staged_method = ("pipelined: step k+1's inputs copied in on one copy stream and step k-1's results copied out "
+                     "on another while step k computes (two device buffers each); no L2 flush (inputs larger than "
+                     "L2); first copy in to last copy out")
+    if getattr(wl, "e2e_pipeline", False):
+        e2e_total, e2e_method = e2e_alt, staged_method
+        e2e_alt = None
+        if getattr(wl, "e2e_host_outputs", False):
+            direct = max_over_ranks(time_e2e_pipelined(torch, wl, pinned_in, pinned_out, n_e2e, args.warmup, False),
+                                    world)
+            direct_method = ("pipelined: step k+1's inputs copied in on a copy stream while step k computes (two "
+                             "device input buffers); results written into pinned host memory by the kernels; no "
+                             "L2 flush (inputs larger than L2); first copy in to last kernel")
+            e2e_alt = direct
+            if direct < e2e_total:
+                e2e_total, e2e_alt, e2e_method = direct, e2e_total, direct_method
+    else:
+        e2e_ms, _, _, _ = time_steps(torch, wl, n_e2e, args.warmup, flush, None,
+                                     {"h2d": h2d, "after": after, "d2h": d2h})
+        e2e_total = max_over_ranks(sum(e2e_ms), world)
+        e2e_method = "per step: inputs copied in, the step, results out; L2 flushed between steps"
     barrier()
-    n_e2e = max(3, args.steps // 4)
-    e2e_total = max_over_ranks(sum(e2e_ms), world)
     e2e_value = job_throughput(ops, n_e2e, world, e2e_total)
     h2d_bytes = sum(t.numel() * t.element_size() for t in pinned_in)
     d2h_bytes = sum(t.numel() * t.element_size() for t in pinned_out)
@@ -982,7 +1078,8 @@ def run_ours(args):
             if st.bound == "alu" and clocks and clocks.get("sm_mhz") else None),
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d_bytes,
-                "d2h_bytes_per_step": d2h_bytes},
+                "d2h_bytes_per_step": d2h_bytes, "steps": n_e2e, "method": e2e_method,
+                "other_method_value": (job_throughput(ops, n_e2e, world, e2e_alt) if e2e_alt else None)},
         "gpu_launches": gpu_launches,
         "plan_ms": plan_ms,
         "clocks": clocks,
