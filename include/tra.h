@@ -129,7 +129,10 @@ enum {
  *         ksplit=auto|off (tensor-core path: by default the tiles of a last, partly
  *         filled wave of the persistent grid have their K loop split into 2-4 runs on
  *         otherwise idle SMs, the partial sums kept in the workspace and added in a fixed
- *         order, so results stay deterministic; off keeps one worker per tile),
+ *         order, so results stay deterministic; a tile cut in two with an fp32 output
+ *         written through a tensor map instead has both halves added into the output,
+ *         zeroed at the start of the launch, by TMA reduce-add (the same bits in either
+ *         order); off keeps one worker per tile),
  *         split=bf16x3|none (fp32 "sqdiff:sum" and "add:lse" only: the squared-distance
  *         expansion |x|^2 + |y|^2 - 2 x.y, or the factored logsumexp
  *         mx + my + log sum e^(x-mx) e^(y-my), with the sum of products on BF16 tensor cores,

@@ -96,6 +96,10 @@ struct TcParams {
     // 0 .. split-2 each leave fp32 partial sums in a slot of `part` and release them through one
     // flag per (tile, part, epilogue warp); the last part adds them in part order.
     uint32_t n_full, split, n_units;
+    // split == 2 with an fp32 output tensor map: instead of passing partial sums, both parts add
+    // their sums into the output with TMA reduce-add, after the worker of part 0 has zeroed the
+    // tile at the start of the launch (flag per tile and epilogue warp, as for the partial sums)
+    uint32_t split_reduce;
     float* part;                 // [tile - n_full][part][lane quarter][column block][register][lane]
     unsigned long long* flags;   // [tile - n_full][part][epilogue warp]: tag | 1 once released
     unsigned long long tag;      // this launch's flag tag (the low 8 bits are zero)
@@ -413,6 +417,15 @@ __device__ __forceinline__ void apply_terms(const TcParams& p, uint32_t (&r)[32]
     }
 }
 
+// out[box] += smem box (fp32 add in L2), through the output tensor map
+__device__ __forceinline__ void tma_reduce_add_5d(const CUtensorMap* map, const int c[5], uint32_t src) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.5d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3, %4, %5}], [%6];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4]), "r"(src)
+        : "memory");
+}
+
 // Partial sums of a split tile, for one epilogue warp: column block c (32 columns) holds
 // register i of every lane at c * 1024 + i * 32 + lane, so each access of the warp is one
 // contiguous 128-byte line.  L2 only (the other parts run on other SMs).
@@ -455,6 +468,33 @@ __device__ __forceinline__ void set_flag(unsigned long long* f, unsigned long lo
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(f), "l"(v) : "memory");
 }
 
+// The worker of part 0 of a tile split in two (split_reduce): this epilogue warp zeroes its
+// share of the tile's output (the 32-column blocks it also stores: c = 2 half + 4 i, + 1) from
+// its zeroed staging tile by TMA stores, waits for them to complete and releases the flag.
+__device__ __forceinline__ void zero_split_share(const TcParams& p, const CUtensorMap* map_z, uint8_t* epi,
+                                                 uint32_t q, uint32_t half, int lane, uint32_t b, uint32_t m,
+                                                 uint32_t n0, unsigned long long* flag) {
+    float4* stg = reinterpret_cast<float4*>(epi + (q + 4 * half) * kEpiTile);
+#pragma unroll
+    for (int g = 0; g < 8; ++g) stg[lane * 8 + g] = make_float4(0.f, 0.f, 0.f, 0.f);
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        const uint32_t row0 = m - (uint32_t)lane;
+        for (uint32_t c = 2 * half; c < p.block_n / 32; c += 4)
+            for (uint32_t k = 0; k < 2; ++k) {
+                int cc[5];
+                z_coords(p.zt, b, row0, n0 + (c + k) * 32u, cc);
+                tma_store_5d(map_z, cc, smem_u32(stg));
+            }
+        bulk_commit();
+        bulk_wait_all();  // the zeros are written
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        set_flag(flag, p.tag | 1u);
+    }
+    __syncwarp();
+}
+
 // A part of a split tile other than the last: leave this warp's sums in the part's own slot of
 // the partial buffer and release them (no wait: every such part runs at once).
 __device__ __forceinline__ void split_partial(const TcParams& p, uint32_t tmem_acc, uint32_t q, uint32_t half,
@@ -478,7 +518,7 @@ template <int EPI>
 __device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorMap* map_z, uint8_t* epi,
                                               uint32_t tmem_acc, uint32_t q, uint32_t half, int lane, uint32_t b,
                                               uint32_t m, uint32_t n0, const float* addp = nullptr, uint32_t nadd = 0,
-                                              size_t add_stride = 0) {
+                                              size_t add_stride = 0, bool reduce = false) {
     float4* stg = reinterpret_cast<float4*>(epi + (q + 4 * half) * kEpiTile);
     const uint32_t nblk = p.block_n / 32;  // block_n is a multiple of 64
     const uint32_t taddr = tmem_acc + ((q * 32u) << 16);
@@ -501,7 +541,8 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorM
             if (lane == 0) {
                 int cc[5];
                 z_coords(p.zt, b, row0, n, cc);
-                tma_store_5d(map_z, cc, smem_u32(t));
+                if (reduce) tma_reduce_add_5d(map_z, cc, smem_u32(t));
+                else tma_store_5d(map_z, cc, smem_u32(t));
                 bulk_commit();
             }
         };
@@ -586,15 +627,25 @@ __device__ __forceinline__ bool epilogue_unit(const TcParams& p, const CUtensorM
     const size_t region = (size_t)p.block_n * 32u;
     float* slot0 = p.part + ((size_t)(tile - p.n_full) * others * regions + rank * 4u + q) * region;
     unsigned long long* flag0 = p.flags + (size_t)(tile - p.n_full) * others * (2u * regions) + rank * 8u + half * 4u + q;
-    if (part < others) {
+    if (p.split_reduce) {
+        // both parts add into the output zeroed by part 0's worker at the start of the launch
+        if (part == 1) {
+            if (!wait_flag(flag0, p.tag | 1u, abort, p.timeout_ns)) return false;
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+    } else if (part < others) {
         split_partial(p, tmem_acc, q, half, lane, slot0 + part * regions * region, flag0 + part * 2u * regions);
         return true;
+    } else {
+        for (uint32_t j = 0; j < others; ++j)
+            if (!wait_flag(flag0 + j * 2u * regions, p.tag | 1u, abort, p.timeout_ns)) return false;
     }
-    for (uint32_t j = 0; j < others; ++j)
-        if (!wait_flag(flag0 + j * 2u * regions, p.tag | 1u, abort, p.timeout_ns)) return false;
-    epilogue_tile<0>(p, map_z, epi, tmem_acc, q, half, lane, b, mrow, n0, slot0, others, regions * region);
-    if (lane == 0)  // ready for the next call
-        for (uint32_t j = 0; j < others; ++j) *reinterpret_cast<volatile unsigned long long*>(flag0 + j * 2u * regions) = 0ull;
+    const bool red = p.split_reduce != 0;
+    epilogue_tile<0>(p, map_z, epi, tmem_acc, q, half, lane, b, mrow, n0, red ? nullptr : slot0, red ? 0u : others,
+                     regions * region, red);
+    if (lane == 0 && (!red || part == 1))  // ready for the next call
+        for (uint32_t j = 0; j < (red ? 1u : others); ++j)
+            *reinterpret_cast<volatile unsigned long long*>(flag0 + j * 2u * regions) = 0ull;
     return true;
 }
 
@@ -701,6 +752,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t q = warp & 3;  // TMEM lane quarter this warp may access
         const uint32_t half = (uint32_t)(warp - kMmaWarp - 1) >> 2;
         uint32_t acc = 0, acc_phase = 0;
+        if (p.split_reduce && p.n_full + blockIdx.x < p.n_units) {  // this worker's split unit
+            uint32_t tile, kb0, kb1, part, b, mt, nt;
+            unit_of(p, p.n_full + blockIdx.x, tile, kb0, kb1, part);
+            if (part == 0) {
+                tile_of(p, tile, b, mt, nt);
+                zero_split_share(p, &map_z, epi, q, half, lane, b, mt * kBlockM + q * 32 + lane, nt * p.block_n,
+                                 p.flags + (size_t)(tile - p.n_full) * 8u + half * 4u + q);
+            }
+        }
         for (uint32_t u = blockIdx.x; u < p.n_units; u += gridDim.x) {
             uint32_t tile, kb0, kb1, part, b, mt, nt;
             unit_of(p, u, tile, kb0, kb1, part);
@@ -841,6 +901,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t q = warp & 3;
         const uint32_t half = (uint32_t)(warp - kMmaWarp - 1) >> 2;
         uint32_t acc = 0, acc_phase = 0;
+        if (p.split_reduce && p.n_full + pair < p.n_units) {  // this worker's split unit
+            uint32_t tile, kb0, kb1, part, b, mt, nt;
+            unit_of(p, p.n_full + pair, tile, kb0, kb1, part);
+            if (part == 0) {
+                tile_of(p, tile, b, mt, nt);
+                zero_split_share(p, &map_z, epi, q, half, lane, b, mt * 2 * kBlockM + rank * kBlockM + q * 32 + lane,
+                                 nt * p.block_n, p.flags + (size_t)(tile - p.n_full) * 16u + rank * 8u + half * 4u + q);
+            }
+        }
         for (uint32_t u = pair; u < p.n_units; u += n_pairs) {
             uint32_t tile, kb0, kb1, part, b, mt, nt;
             unit_of(p, u, tile, kb0, kb1, part);
@@ -1374,6 +1443,9 @@ int tc_execute(const Plan& p, const void* x, const void* y, void* z, cudaStream_
         tp.part = reinterpret_cast<float*>(ws);
         tp.flags = reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(ws) + t.ws_part);
         tp.tag = next_split_tag();
+        // two parts into an fp32 output through its tensor map: both add into the output (fp32
+        // addition of two values into zero gives the same bits in either order)
+        tp.split_reduce = split == 2 && z_tma && !p.out_bf16 ? 1u : 0u;
     }
     cudaError_t e;
     if (t.pair) {

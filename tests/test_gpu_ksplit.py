@@ -6,7 +6,10 @@ output tile may be cut into runs whose partial sums are added afterwards.  The
 persistent tensor-core kernels do that for the tiles of a last, partly filled wave:
 with T tiles on C workers, the T mod C tiles left over are each cut into 2-4 runs on
 otherwise idle workers, the partial sums go through the plan's workspace, and they are
-added in a fixed order.  Small problems (T < C) are all "last wave".
+added in a fixed order.  A tile cut in two with an fp32 output written through its tensor
+map skips the workspace: part 0's worker zeroes the tile at the start of the launch and both
+parts add into it with TMA reduce-add (two values added into zero give the same bits in
+either order).  Small problems (T < C) are all "last wave".
 
 Checked here: the result against the oracle (the same bars as the unsplit path), the
 result of ksplit=off within the fp32 summation bar, bit-identical repeats, and replay
@@ -33,7 +36,9 @@ def labels_of(eq):
     return ins, out, order
 
 
-# K of 1024, 1536 and 2048 gives 16, 24 and 32 K steps of 64: 2, 3 and 4 runs of at least 8
+# K of 1024, 1536 and 2048 gives 16, 24 and 32 K steps of 64: 2, 3 and 4 runs of at least 8.
+# Two runs into an fp32 output through the TMA-store epilogue add into the zeroed output (TMA
+# reduce-add); other splits gather the partial sums in part order.
 SPLIT_CASES = [
     ("ij,jk->ik", [256, 2048, 256], [1, 1, 1, 1], ""),                 # one pair tile, 4 runs
     ("ij,jk->ik", [512, 1536, 512], [2, 1, 1, 2], ""),                 # 4 tiles in 4 keys, 3 runs
@@ -111,12 +116,15 @@ def test_ksplit_contraction_4d_full_size(lib, cuda):
     assert np.abs(g - g_off).max() <= 1e-5 * np.abs(g_off).max()
 
 
-def test_ksplit_graph_replay(lib, cuda):
-    # a CUDA graph freezes the launch's arguments; the flags of the split tiles are cleared by
-    # the last part of each tile, so every replay starts from the same state
+@pytest.mark.parametrize("bounds", [[512, 1536, 512], [512, 1024, 512]])
+def test_ksplit_graph_replay(lib, cuda, bounds):
+    # a CUDA graph freezes the launch's arguments (the flag tag included); the flags of the split
+    # tiles are cleared by the last part of each tile, so every replay starts from the same state.
+    # K = 1536 splits each tile in three (partial sums gathered in order); K = 1024 in two, whose
+    # parts add into the output zeroed by part 0's worker (TMA reduce-add)
     import torch
 
-    eq, bounds, d = "ij,jk->ik", [512, 1536, 512], [2, 1, 1, 2]
+    eq, d = "ij,jk->ik", [2, 1, 1, 2]
     spec = eq + ":mul:sum:in=bf16"
     p = lib.Plan(spec, bounds, d)
     assert p.workspace_bytes > 0
