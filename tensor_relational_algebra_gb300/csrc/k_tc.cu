@@ -1021,10 +1021,8 @@ bool box_dims(const Plan& p, const Operand& t, const uint32_t (&tiles)[4], int e
         const int l = t.label[i];
         if (p.D[l] > 1) ph[n++] = {l, 1, (uint64_t)p.D[l], (uint64_t)t.key_stride[i]};
     }
-    if (n == 0 || n > 5) return false;
+    if (n == 0) return false;
     if (ph[0].stride != 1 || ph[0].key) return false;
-    for (int j = 1; j < n; ++j)
-        if ((ph[j].stride * (uint64_t)elem_bytes) % 16) return false;
     // composite stride of every label in its role
     uint64_t div[TRA_MAX_LABELS] = {};
     for (int r = 0; r < 4; ++r) {
@@ -1034,10 +1032,10 @@ bool box_dims(const Plan& p, const Operand& t, const uint32_t (&tiles)[4], int e
             d *= (uint64_t)p.B[l];
         }
     }
-    out.ndims = n;
+    TcDim dims[2 * TRA_MAX_RANK];
     for (int j = 0; j < n; ++j) {
         const int l = ph[j].label;
-        TcDim& dm = out.dims[j];
+        TcDim& dm = dims[j];
         dm.role = p.role[l];
         dm.extent = ph[j].extent;
         dm.stride = ph[j].stride;
@@ -1070,7 +1068,7 @@ bool box_dims(const Plan& p, const Operand& t, const uint32_t (&tiles)[4], int e
                     box = rem;
                 }
                 rem /= box;
-                out.dims[j].box = (uint32_t)box;
+                dims[j].box = (uint32_t)box;
                 if (box > 1) {
                     if (j <= last_dim) return false;  // box order must follow the composite order
                     last_dim = j;
@@ -1079,6 +1077,32 @@ bool box_dims(const Plan& p, const Operand& t, const uint32_t (&tiles)[4], int e
         }
         if (rem != 1) return false;
     }
+    // Merge neighbours that are one dimension in memory and in their role's composite index
+    // (the outer's stride and composite divisor continue the inner's): the box stays one
+    // contiguous range of the merged coordinate when the inner box is whole or the outer box is
+    // 1, and its bytes land in shared memory in the same order.  A relation with more than five
+    // physical dimensions (a blocked output, say) then fits a rank-5 tensor map.
+    int m = 0;
+    for (int j = 0; j < n; ++j) {
+        if (m > 0) {
+            TcDim& a = dims[m - 1];
+            const TcDim& b = dims[j];
+            const uint64_t box = b.box == 1 ? a.box : (uint64_t)a.box * b.box;
+            if (a.role == b.role && b.stride == a.stride * a.extent && (uint64_t)b.div == (uint64_t)a.div * a.mod &&
+                (a.box == a.extent || b.box == 1) && box <= 256 && a.extent * b.extent <= 0xffffffffull) {
+                a.box = (uint32_t)box;
+                a.extent *= b.extent;
+                a.mod = (uint32_t)a.extent;
+                continue;
+            }
+        }
+        dims[m++] = dims[j];
+    }
+    if (m > 5) return false;
+    for (int j = 1; j < m; ++j)
+        if ((dims[j].stride * (uint64_t)elem_bytes) % 16) return false;
+    out.ndims = m;
+    for (int j = 0; j < m; ++j) out.dims[j] = dims[j];
     return true;
 }
 
