@@ -846,9 +846,15 @@ def roofline_nodes(wl, means, peaks, props):
 
 
 def peak_source(bound):
-    return ("derived: SMs x 128 FP32 lanes x 2 x max SM clock (MEASURED_PEAKS sm_max_mhz); the inner step's "
-            "instruction-mix ceilings are measured in profiles/fp32_ceilings.json (bench.py --probe fp32)"
-            if bound == "alu" else "MEASURED_PEAKS.json (of measured)")
+    pk = measured_peaks()
+    if bound == "alu":
+        return ("derived: SMs x 128 FP32 lanes x 2 x max SM clock (" +
+                ("MEASURED_PEAKS sm_max_mhz" if "sm_max_mhz" in pk else "2070 MHz, of fallback") +
+                "); the inner step's instruction-mix ceilings are measured in profiles/fp32_ceilings.json "
+                "(bench.py --probe fp32)")
+    key = "hbm_gbs" if bound == "hbm" else "bf16_tflops"
+    return ("MEASURED_PEAKS.json (of measured)" if key in pk else
+            "fallback 6.8 TB/s copy, 1.9 PFLOP/s BF16 (one earlier GB300 measurement; of fallback)")
 
 
 def extra_workload(torch, tra, name, args, flush, local):
