@@ -325,3 +325,17 @@ def test_check_build_is_selected_by_the_environment(lib):
         out[flag] = r.stdout.split()
     assert out["0"] == ["0", "False"]
     assert out["1"] == ["1", "True"]
+
+
+def test_tensor_maps_merge_contiguous_dimensions(lib):
+    """The tensor-core planner describes a relation to TMA as at most five dimensions.  The 4-D
+    contraction's output C[a,b,c,d] under d = [4,1,4,1] has six physical dimensions, but the local
+    part of a runs on into b and the local part of c into d, both in memory and in their composite
+    index, so they merge and the output gets a tensor map (TMA-store epilogue).  With b or d split
+    the local parts are no longer contiguous with their neighbours and no map fits."""
+    spec = "abef,cfed->abcd:mul:sum:in=bf16"
+    assert lib.Plan(spec + ":tc_store=tma", [64] * 6, [4, 1, 1, 1, 4, 1, 1, 1]).kernel == "tc_bf16_pair"
+    for d in ([1, 2, 1, 1, 1, 1, 1, 2], [2, 2, 1, 1, 2, 1, 1, 2]):
+        with pytest.raises(lib.TraError) as e:
+            lib.Plan(spec + ":tc_store=tma", [64] * 6, d)
+        assert "TRA_ERR_UNSUPPORTED" in str(e.value)
